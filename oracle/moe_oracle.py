@@ -1,0 +1,420 @@
+"""Plain, slow CPU oracle for the forward pass of one sparse top-k MoE FFN layer.
+
+TEST INFRASTRUCTURE ONLY.  Nothing on the product path may import or call this
+module: only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline /
+reference legs of ``bench.py`` use it.  It shares no code, table or constant
+with the CUDA path under ``sparse_mixture_experts_65_b300/``; the two meet
+only through the seeded inputs that the tests hand to both.
+
+Everything here is the plain definition written out in float64 numpy with the
+loops the definition implies.  Inputs arrive as fp32 or bf16 values; the
+upcast of either to float64 is exact.  Library primitives used as single
+steps: ``numpy`` matrix-vector / matrix products (a plain inner product), and
+``numpy.lexsort`` (a sort).
+
+Sources (page title, then section):
+  [MoE-ch11]   "Mixture of Experts" (llm-tutorial, chapter 11):
+               § The mathematics; § Top-k routing: the gating function;
+               § Top-1 vs top-2; § The auxiliary loss; § Expert capacity and
+               dropped tokens; § Why MoE is hard (router precision); § Exercises.
+  [MoE-guide]  "Mixture of experts" (inside-the-model guide, chapter 14):
+               § The computation; § Auxiliary loss; § Fine-grained and shared
+               experts; § Auxiliary-loss-free balancing; § Check yourself.
+  [MoE-ch33]   "Chapter 33 — Mixture of Experts (MoE)": § The Router;
+               § Load Balancing; § Simple MoE Layer Implementation.
+  [MoE-visual] "Mixture-of-Experts" (neural networks visually, chapter 15):
+               routing figure; § Show the math.
+  [MoE-atlas]  "Mixture of experts (MoE)" (tech-atlas glossary entry).
+
+Readings taken where the pages are silent or garbled (each one also appears,
+with its reason, in the design notes of the repository):
+  * top-k order: descending selection score, ties to the lower expert index;
+  * capacity C = ceil(k*T*rho/E) evaluated in double, k*T first; rho <= 0
+    means no limit; the drop test is "earlier keys routed to e" < C with the
+    token-major key t*k + j (first come by token index);
+  * f_i counts routed (pre-drop) assignments over T*k; P_i averages the full
+    router distribution (softmax over all E, or sigmoid normalised over all E);
+  * GELU is the exact erf form; SwiGLU is silu(W1 x) * (W3 x) then W2;
+  * the shared expert is a SwiGLU expert added with weight 1, outside f/P and
+    outside capacity;
+  * a dropped slot contributes zero and the remaining gates are not
+    renormalised; y is the MoE branch only (the caller adds the residual).
+
+Parity pins: every function below is pinned by ``tests/test_oracle_pins.py``
+(brute force, closed forms, library special cases and page numbers under
+``tests/golden/``).  What no page value fixes -- the absolute output values
+for a given random seed -- is pinned only through those checks.
+"""
+
+from __future__ import annotations
+
+import math
+from dataclasses import dataclass, field
+from typing import Callable, Optional
+
+import numpy as np
+
+GATE_SOFTMAX_TOPK = "softmax_topk"
+GATE_SIGMOID_RENORM = "sigmoid_renorm"
+GATE_SOFTMAX_FULL = "softmax_full"
+GATE_MODES = (GATE_SOFTMAX_TOPK, GATE_SIGMOID_RENORM, GATE_SOFTMAX_FULL)
+
+ACT_GELU = "gelu"
+ACT_RELU = "relu"
+ACT_SWIGLU = "swiglu"
+ACTS = (ACT_GELU, ACT_RELU, ACT_SWIGLU)
+
+
+def _f64(a) -> np.ndarray:
+    return np.asarray(a, dtype=np.float64)
+
+
+# --------------------------------------------------------------------------
+# Stage 1: router scores.
+# [MoE-ch11] § The mathematics: the router W_r (N x d) gives one logit per
+# expert, l = W_r x.  [MoE-guide] § The computation: s = W_r x.
+# [MoE-ch33] § The Router: a bias-free linear map d_model -> n_experts.
+# The optional per-expert logit offset o_e is added to every token's logits
+# (a fixed skew of the router; it enters gates and P like any other logit).
+# --------------------------------------------------------------------------
+def router_logits(x, W_r, logit_offset=None) -> np.ndarray:
+    """s[t, e] = sum_c x[t, c] * W_r[e, c] (+ o_e), float64.  x: [T, d], W_r: [E, d]."""
+    x = _f64(x)
+    W_r = _f64(W_r)
+    s = x @ W_r.T
+    if logit_offset is not None:
+        s = s + _f64(logit_offset)[None, :]
+    return s
+
+
+def sigmoid(z) -> np.ndarray:
+    z = _f64(z)
+    return 1.0 / (1.0 + np.exp(-z))
+
+
+def softmax_rows(z) -> np.ndarray:
+    """Row softmax with the row maximum subtracted first ([MoE-ch11] demo code)."""
+    z = _f64(z)
+    m = z.max(axis=-1, keepdims=True)
+    ez = np.exp(z - m)
+    return ez / ez.sum(axis=-1, keepdims=True)
+
+
+# --------------------------------------------------------------------------
+# Stage 2: top-k selection and gates.
+# [MoE-ch11] § Top-k routing: the k largest logits are kept; softmax is taken
+# over only those k values, so the gates sum to 1 over the chosen experts.
+# [MoE-ch11] § Top-1 vs top-2: a top-1 gate is the softmax probability of the
+# chosen expert over all experts (or 1.0 in some variants).
+# [MoE-guide] § The computation: gates are a softmax over the chosen scores
+# or renormalised sigmoids.  [MoE-guide] § Auxiliary-loss-free balancing:
+# a per-expert bias b_i is added to the affinity only when choosing experts;
+# the gate values use the original affinity.
+# --------------------------------------------------------------------------
+def affinity(s, gate_mode: str) -> np.ndarray:
+    """Affinity per (token, expert): the logit itself, or its sigmoid."""
+    if gate_mode == GATE_SIGMOID_RENORM:
+        return sigmoid(s)
+    if gate_mode in (GATE_SOFTMAX_TOPK, GATE_SOFTMAX_FULL):
+        return _f64(s)
+    raise ValueError(gate_mode)
+
+
+def selection_scores(s, gate_mode: str, sel_bias=None) -> np.ndarray:
+    """sel = affinity + b (b only steers the choice, never the gate value)."""
+    a = affinity(s, gate_mode)
+    if sel_bias is not None:
+        a = a + _f64(sel_bias)[None, :]
+    return a
+
+
+def topk_indices(sel, k: int) -> np.ndarray:
+    """Indices of the k largest selection scores per row, in descending order;
+    equal scores go to the lower expert index.  [T, E] -> int64 [T, k]."""
+    sel = _f64(sel)
+    T, E = sel.shape
+    if not 1 <= k <= E:
+        raise ValueError("need 1 <= k <= E")
+    out = np.empty((T, k), dtype=np.int64)
+    order_key = np.arange(E)
+    for t in range(T):
+        # lexsort: last key is primary -> by -sel ascending, then by index.
+        perm = np.lexsort((order_key, -sel[t]))
+        out[t] = perm[:k]
+    return out
+
+
+def topk_gap(sel, k: int) -> np.ndarray:
+    """Per token: (k-th largest) - ((k+1)-th largest) selection score; +inf when k == E.
+    Tokens with a gap below the near-tie band may legitimately pick a different
+    set under a different (but valid) rounding of the scores."""
+    sel = _f64(sel)
+    T, E = sel.shape
+    if k >= E:
+        return np.full(T, np.inf)
+    srt = -np.sort(-sel, axis=1)
+    return srt[:, k - 1] - srt[:, k]
+
+
+def gate_values(s, idx, gate_mode: str) -> np.ndarray:
+    """Gate g[t, j] for chosen expert idx[t, j], from the unbiased logits s."""
+    s = _f64(s)
+    idx = np.asarray(idx)
+    T, k = idx.shape
+    g = np.empty((T, k), dtype=np.float64)
+    for t in range(T):
+        chosen = s[t, idx[t]]
+        if gate_mode == GATE_SOFTMAX_TOPK:
+            m = chosen.max()
+            e = np.exp(chosen - m)
+            g[t] = e / e.sum()
+        elif gate_mode == GATE_SIGMOID_RENORM:
+            a = sigmoid(chosen)
+            g[t] = a / a.sum()
+        elif gate_mode == GATE_SOFTMAX_FULL:
+            m = s[t].max()
+            e_all = np.exp(s[t] - m)
+            g[t] = np.exp(chosen - m) / e_all.sum()
+        else:
+            raise ValueError(gate_mode)
+    return g
+
+
+def router_probs(s, gate_mode: str) -> np.ndarray:
+    """Full per-token router distribution over all E experts (for P_i):
+    softmax of the logits, or sigmoid affinities normalised over all E."""
+    if gate_mode == GATE_SIGMOID_RENORM:
+        a = sigmoid(s)
+        return a / a.sum(axis=1, keepdims=True)
+    return softmax_rows(s)
+
+
+# --------------------------------------------------------------------------
+# Stage 3: expert capacity and drops.
+# [MoE-ch11] § Expert capacity and dropped tokens: capacity is the fair share
+# T/N scaled by rho; excess tokens skip the expert and pass on through the
+# residual.  [MoE-guide] § Auxiliary loss: capacity = (tokens per batch / N) x
+# capacity factor.  [MoE-ch11] § Exercises (exercise 4): drops per expert are
+# max(0, count - capacity).
+# --------------------------------------------------------------------------
+def expert_capacity(T: int, k: int, E: int, capacity_factor: float) -> Optional[int]:
+    """C = ceil(k*T*rho/E) in double precision (k*T formed first); None = no limit."""
+    if capacity_factor is None or capacity_factor <= 0:
+        return None
+    return int(math.ceil((k * T) * float(capacity_factor) / E))
+
+
+@dataclass
+class Assignment:
+    routed: np.ndarray          # [E] assignments per expert before drops
+    kept: np.ndarray            # [E] assignments per expert after drops
+    pos: np.ndarray             # [T, k] earlier keys routed to the same expert
+    slot_pos: np.ndarray        # [T, k] row in expert-contiguous order, -1 = dropped
+    offsets: np.ndarray         # [E+1] exclusive scan of kept
+    capacity: Optional[int]
+
+
+def assign_slots(idx, E: int, capacity: Optional[int]) -> Assignment:
+    """Walk the keys t*k + j in increasing order.  An assignment to expert e is
+    kept iff the number of earlier keys routed to e is below the capacity."""
+    idx = np.asarray(idx)
+    T, k = idx.shape
+    routed = np.zeros(E, dtype=np.int64)
+    kept = np.zeros(E, dtype=np.int64)
+    pos = np.empty((T, k), dtype=np.int64)
+    keep = np.empty((T, k), dtype=bool)
+    for t in range(T):
+        for j in range(k):
+            e = int(idx[t, j])
+            p = int(routed[e])
+            routed[e] += 1
+            pos[t, j] = p
+            if capacity is None or p < capacity:
+                keep[t, j] = True
+                kept[e] += 1
+            else:
+                keep[t, j] = False
+    offsets = np.zeros(E + 1, dtype=np.int64)
+    for e in range(E):
+        offsets[e + 1] = offsets[e] + kept[e]
+    slot_pos = np.full((T, k), -1, dtype=np.int64)
+    for t in range(T):
+        for j in range(k):
+            if keep[t, j]:
+                slot_pos[t, j] = offsets[int(idx[t, j])] + pos[t, j]
+    return Assignment(routed, kept, pos, slot_pos, offsets, capacity)
+
+
+def permutation_rows(asg: Assignment, idx) -> np.ndarray:
+    """Stage 4 as data: row_token[r] = token whose copy sits at expert-contiguous
+    row r (rows within one expert in increasing key order)."""
+    idx = np.asarray(idx)
+    T, k = idx.shape
+    n = int(asg.offsets[-1])
+    row_token = np.full(n, -1, dtype=np.int64)
+    for t in range(T):
+        for j in range(k):
+            r = asg.slot_pos[t, j]
+            if r >= 0:
+                row_token[r] = t
+    return row_token
+
+
+# --------------------------------------------------------------------------
+# Stage 5: expert MLPs.
+# [MoE-ch11] § The mathematics: an expert is a full FFN W2 sigma(W1 x), GeLU in
+# most production transformers, ReLU in the demo; no biases in the demo code.
+# [MoE-ch11] § Active vs total parameters and [MoE-ch33] § Simple MoE Layer
+# Implementation: SwiGLU experts with gate W1, up W3, down W2.
+# [MoE-guide] § Fine-grained and shared experts: shared experts run for every
+# token.
+# --------------------------------------------------------------------------
+class MultiplyCounter:
+    """Counts scalar multiplies performed by expert evaluations ([MoE-visual]
+    routing figure: 65,536 per token at top-2 versus 262,144 if all fire)."""
+
+    def __init__(self):
+        self.count = 0
+
+
+def gelu_erf(z) -> np.ndarray:
+    z = _f64(z)
+    erf = np.vectorize(math.erf, otypes=[np.float64])
+    return 0.5 * z * (1.0 + erf(z / math.sqrt(2.0)))
+
+
+def silu(z) -> np.ndarray:
+    z = _f64(z)
+    return z * sigmoid(z)
+
+
+def _matvec(W, v, counter: Optional[MultiplyCounter]) -> np.ndarray:
+    W = _f64(W)
+    if counter is not None:
+        counter.count += W.shape[0] * W.shape[1]
+    return W @ v
+
+
+def expert_ffn(xt, W1, W2, act: str, W3=None, counter: Optional[MultiplyCounter] = None) -> np.ndarray:
+    """One expert on one token.  W1, W3: [f, d]; W2: [d, f]; xt: [d]."""
+    xt = _f64(xt)
+    a = _matvec(W1, xt, counter)
+    if act == ACT_GELU:
+        h = gelu_erf(a)
+    elif act == ACT_RELU:
+        h = np.maximum(a, 0.0)
+    elif act == ACT_SWIGLU:
+        if W3 is None:
+            raise ValueError("SwiGLU needs W3")
+        b = _matvec(W3, xt, counter)
+        h = silu(a) * b
+    else:
+        raise ValueError(act)
+    return _matvec(W2, h, counter)
+
+
+# --------------------------------------------------------------------------
+# Stage 6: combine and balance statistics.
+# [MoE-ch11] § The mathematics / [MoE-guide] § The computation /
+# [MoE-visual] § Show the math: y = sum over chosen i of g_i * Expert_i(x);
+# unselected experts contribute exactly zero because they never run.
+# [MoE-guide] § Auxiliary loss: L = alpha * N * sum_i f_i * P_i with f_i the
+# fraction of tokens sent to i and P_i the average router probability of i.
+# --------------------------------------------------------------------------
+def balance_stats(routed, probs, T: int, k: int, alpha: float):
+    """f_i = routed_i / (T*k); P_i = mean over tokens of probs[:, i];
+    L = alpha * E * sum_i f_i * P_i.  Returns (f, P, L)."""
+    routed = _f64(routed)
+    probs = _f64(probs)
+    E = routed.shape[0]
+    if T == 0:
+        return np.zeros(E), np.zeros(E), 0.0
+    f = routed / float(T * k)
+    P = probs.sum(axis=0) / float(T)
+    L = float(alpha) * E * float(np.sum(f * P))
+    return f, P, L
+
+
+class _Indexable:
+    """Per-expert weight access; lets callers stream experts lazily."""
+
+    def __init__(self, arr):
+        self.arr = arr
+
+    def __getitem__(self, e):
+        return self.arr[e]
+
+
+@dataclass
+class OracleResult:
+    s: np.ndarray
+    sel: np.ndarray
+    topk_idx: np.ndarray
+    topk_w: np.ndarray
+    probs: np.ndarray
+    gap: np.ndarray
+    asg: Assignment
+    f: np.ndarray
+    P: np.ndarray
+    aux_loss: float
+    y: Optional[np.ndarray]            # [T, d], or rows for `tokens` only
+    tokens: Optional[np.ndarray] = None
+    multiplies: int = 0
+    extras: dict = field(default_factory=dict)
+
+
+def route(x, W_r, k: int, gate_mode: str, logit_offset=None, sel_bias=None,
+          capacity_factor=None, alpha: float = 0.01, forced_idx=None):
+    """Stages 1-3 and the balance statistics.  If forced_idx is given, the
+    selection is taken from it instead of being computed (used to condition
+    the later stages on another implementation's choice)."""
+    s = router_logits(x, W_r, logit_offset)
+    T, E = s.shape
+    sel = selection_scores(s, gate_mode, sel_bias)
+    idx = topk_indices(sel, k) if forced_idx is None else np.asarray(forced_idx, dtype=np.int64)
+    g = gate_values(s, idx, gate_mode)
+    probs = router_probs(s, gate_mode)
+    cap = expert_capacity(T, k, E, capacity_factor)
+    asg = assign_slots(idx, E, cap)
+    f, P, L = balance_stats(asg.routed, probs, T, k, alpha)
+    return s, sel, idx, g, probs, asg, f, P, L
+
+
+def moe_forward(x, W_r, W1, W2, k: int, act: str, gate_mode: str, W3=None,
+                logit_offset=None, sel_bias=None, capacity_factor=None,
+                alpha: float = 0.01, Ws1=None, Ws3=None, Ws2=None,
+                tokens=None, forced_idx=None, count_multiplies=False) -> OracleResult:
+    """The whole layer.  W1/W3/W2 may be arrays [E, ...] or any object whose
+    [e] returns expert e's matrix.  tokens: optional subset of token indices for
+    which y is evaluated (routing always runs on the whole batch, since capacity
+    is a property of the whole batch)."""
+    x = _f64(x)
+    T = x.shape[0]
+    s, sel, idx, g, probs, asg, f, P, L = route(
+        x, W_r, k, gate_mode, logit_offset, sel_bias, capacity_factor, alpha, forced_idx)
+    gap = topk_gap(sel, k)
+    counter = MultiplyCounter() if count_multiplies else None
+    tok = np.arange(T) if tokens is None else np.asarray(tokens, dtype=np.int64)
+    d = x.shape[1]
+    y = np.zeros((len(tok), d), dtype=np.float64)
+    W1i, W2i = _Indexable(W1), _Indexable(W2)
+    W3i = _Indexable(W3) if W3 is not None else None
+    # Group the kept (token, slot) pairs by expert so that lazily streamed
+    # weights are fetched once per expert.
+    work = {}
+    for r, t in enumerate(tok):
+        for j in range(k):
+            if asg.slot_pos[t, j] >= 0:
+                work.setdefault(int(idx[t, j]), []).append((r, int(t), j))
+    for e in sorted(work):
+        w1, w2 = W1i[e], W2i[e]
+        w3 = W3i[e] if W3i is not None else None
+        for r, t, j in work[e]:
+            y[r] += g[t, j] * expert_ffn(x[t], w1, w2, act, w3, counter)
+    if Ws1 is not None:
+        for r, t in enumerate(tok):
+            y[r] += expert_ffn(x[t], Ws1, Ws2, ACT_SWIGLU, Ws3, counter)
+    return OracleResult(s=s, sel=sel, topk_idx=idx, topk_w=g, probs=probs, gap=gap,
+                        asg=asg, f=f, P=P, aux_loss=L, y=y,
+                        tokens=None if tokens is None else tok,
+                        multiplies=counter.count if counter else 0)

@@ -1,0 +1,156 @@
+"""Seeded synthetic workloads for the MoE layer: shapes, modes and input draws.
+
+This module holds no arithmetic of the method.  It only names the layer
+shapes (taken from the models the MoE pages describe) and draws seeded random
+tensors with the stated distributions.  Both the CUDA path and the CPU oracle
+receive the very same tensors from here.
+
+Distribution convention: N(mu, v) names a normal with VARIANCE v, so weights
+drawn "N(0, 1/fan_in)" have standard deviation 1/sqrt(fan_in) and the Switch
+logit skew "N(0, 1.5)" has standard deviation sqrt(1.5).
+
+Seeds: tensor number i of workload number c uses a generator seeded with
+1000*c + i (+ the caller's extra seed), drawn in the fixed order below.
+"""
+
+from __future__ import annotations
+
+import math
+from dataclasses import dataclass, replace
+from typing import Optional
+
+import torch
+
+ACT_GELU, ACT_RELU, ACT_SWIGLU = "gelu", "relu", "swiglu"
+GATE_SOFTMAX_TOPK, GATE_SIGMOID_RENORM, GATE_SOFTMAX_FULL = (
+    "softmax_topk", "sigmoid_renorm", "softmax_full")
+
+
+@dataclass(frozen=True)
+class LayerShape:
+    name: str
+    cid: int                    # workload number (seed base)
+    T: int                      # tokens in the batch
+    d: int                      # model width
+    E: int                      # routed experts
+    k: int                      # experts per token
+    f: int                      # routed expert width
+    act: str
+    gate: str
+    dtype: str                  # "f32" or "bf16"
+    capacity_factor: float = 0.0        # <= 0: no capacity limit
+    alpha: float = 0.01
+    n_shared: int = 0
+    f_shared: int = 0
+    logit_offset_var: float = 0.0       # variance of a per-expert logit skew
+    sel_bias_halfwidth: float = 0.0     # sel bias ~ U(-h, h)
+
+    def with_T(self, T: int) -> "LayerShape":
+        return replace(self, T=T)
+
+
+# The layer shapes of the models the pages discuss.
+TOY = LayerShape("toy", 0, T=256, d=64, E=8, k=2, f=256, act=ACT_GELU,
+                 gate=GATE_SOFTMAX_TOPK, dtype="f32", alpha=0.01)
+SWITCH = LayerShape("switch", 1, T=4096, d=768, E=64, k=1, f=3072, act=ACT_RELU,
+                    gate=GATE_SOFTMAX_FULL, dtype="bf16", capacity_factor=1.25,
+                    alpha=0.01, logit_offset_var=1.5)
+MIXTRAL = LayerShape("mixtral", 2, T=8192, d=4096, E=8, k=2, f=14336, act=ACT_SWIGLU,
+                     gate=GATE_SOFTMAX_TOPK, dtype="bf16", alpha=0.01)
+DSV3 = LayerShape("dsv3", 3, T=4096, d=7168, E=256, k=8, f=2048, act=ACT_SWIGLU,
+                  gate=GATE_SIGMOID_RENORM, dtype="bf16", alpha=1e-4,
+                  n_shared=1, f_shared=2048, sel_bias_halfwidth=0.05)
+GPTOSS = LayerShape("gptoss", 4, T=256, d=2880, E=128, k=4, f=2880, act=ACT_SWIGLU,
+                    gate=GATE_SOFTMAX_TOPK, dtype="bf16", alpha=0.01)
+GPTOSS_SWEEP_T = (1, 16, 64, 256)
+
+WORKLOADS = {w.name: w for w in (TOY, SWITCH, MIXTRAL, DSV3, GPTOSS)}
+
+
+def get(name: str) -> LayerShape:
+    if name.startswith("gptoss") and name != "gptoss":
+        return GPTOSS.with_T(int(name[len("gptoss"):].lstrip("_T")))
+    return WORKLOADS[name]
+
+
+def torch_dtype(shape: LayerShape) -> torch.dtype:
+    return torch.float32 if shape.dtype == "f32" else torch.bfloat16
+
+
+def _gen(device, seed: int) -> torch.Generator:
+    g = torch.Generator(device=device)
+    g.manual_seed(seed)
+    return g
+
+
+def _normal(shape, std, g, device, dtype, chunk_dim0=False):
+    """std * N(0,1) drawn in fp32 and rounded once to `dtype`.  With
+    chunk_dim0 the leading dimension is drawn slice by slice (same stream)."""
+    if not chunk_dim0:
+        t = torch.randn(shape, generator=g, device=device, dtype=torch.float32)
+        return (t * std).to(dtype)
+    out = torch.empty(shape, device=device, dtype=dtype)
+    for i in range(shape[0]):
+        t = torch.randn(shape[1:], generator=g, device=device, dtype=torch.float32)
+        out[i] = (t * std).to(dtype)
+    return out
+
+
+@dataclass
+class LayerInputs:
+    shape: LayerShape
+    x: torch.Tensor                      # [T, d]
+    W_r: torch.Tensor                    # [E, d]
+    W1: torch.Tensor                     # [E, f, d]
+    W2: torch.Tensor                     # [E, d, f]
+    W3: Optional[torch.Tensor] = None    # [E, f, d] (SwiGLU only)
+    logit_offset: Optional[torch.Tensor] = None   # [E] fp32
+    sel_bias: Optional[torch.Tensor] = None       # [E] fp32
+    Ws1: Optional[torch.Tensor] = None   # [f_s, d]
+    Ws3: Optional[torch.Tensor] = None   # [f_s, d]
+    Ws2: Optional[torch.Tensor] = None   # [d, f_s]
+
+    def weight_bytes(self) -> int:
+        n = 0
+        for t in (self.W_r, self.W1, self.W2, self.W3, self.Ws1, self.Ws3, self.Ws2):
+            if t is not None:
+                n += t.numel() * t.element_size()
+        return n
+
+
+def make_x(shape: LayerShape, device="cpu", seed: int = 0) -> torch.Tensor:
+    """Activations only: x ~ N(0, 1), [T, d]."""
+    base = 1000 * shape.cid + seed * 100003
+    return _normal((shape.T, shape.d), 1.0, _gen(device, base + 0), device, torch_dtype(shape))
+
+
+def make_inputs(shape: LayerShape, device="cpu", seed: int = 0) -> LayerInputs:
+    """All tensors of one layer: x ~ N(0,1); W_r ~ N(0, 1/d); W1, W3 ~ N(0, 1/d);
+    W2 ~ N(0, 1/f); shared weights likewise; optional logit skew ~ N(0, v) and
+    selection bias ~ U(-h, h) in fp32."""
+    dt = torch_dtype(shape)
+    base = 1000 * shape.cid + seed * 100003
+    T, d, E, f = shape.T, shape.d, shape.E, shape.f
+    big = E * f * d > (1 << 26)
+    x = make_x(shape, device, seed)
+    W_r = _normal((E, d), 1.0 / math.sqrt(d), _gen(device, base + 1), device, dt)
+    W1 = _normal((E, f, d), 1.0 / math.sqrt(d), _gen(device, base + 2), device, dt, big)
+    W2 = _normal((E, d, f), 1.0 / math.sqrt(f), _gen(device, base + 3), device, dt, big)
+    W3 = None
+    if shape.act == ACT_SWIGLU:
+        W3 = _normal((E, f, d), 1.0 / math.sqrt(d), _gen(device, base + 4), device, dt, big)
+    logit_offset = None
+    if shape.logit_offset_var > 0:
+        logit_offset = torch.randn(E, generator=_gen(device, base + 5), device=device,
+                                   dtype=torch.float32) * math.sqrt(shape.logit_offset_var)
+    sel_bias = None
+    if shape.sel_bias_halfwidth > 0:
+        u = torch.rand(E, generator=_gen(device, base + 6), device=device, dtype=torch.float32)
+        sel_bias = (u * 2.0 - 1.0) * shape.sel_bias_halfwidth
+    Ws1 = Ws3 = Ws2 = None
+    if shape.n_shared:
+        fs = shape.f_shared
+        Ws1 = _normal((fs, d), 1.0 / math.sqrt(d), _gen(device, base + 7), device, dt)
+        Ws3 = _normal((fs, d), 1.0 / math.sqrt(d), _gen(device, base + 8), device, dt)
+        Ws2 = _normal((d, fs), 1.0 / math.sqrt(fs), _gen(device, base + 9), device, dt)
+    return LayerInputs(shape, x, W_r, W1, W2, W3, logit_offset, sel_bias, Ws1, Ws3, Ws2)

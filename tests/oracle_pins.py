@@ -1,0 +1,431 @@
+"""Checks that pin the CPU oracle to facts outside itself.
+
+Each check raises AssertionError on failure.  ``test_oracle_pins.py`` runs
+them against the oracle as written; ``test_oracle_mutations.py`` plants a
+plausible mistake in the oracle (on the CPU) and shows that a check fails.
+
+What each check leans on:
+  brute force      -- enumeration of all k-subsets; dense evaluation of all E
+                      experts with a gate vector that is zero off the chosen set
+  closed forms     -- hand-derived gate and loss values for tiny inputs
+  library cases    -- E = 1, k = 1 reduces the layer to one dense FFN, checked
+                      against torch.nn.functional in float64
+  page numbers     -- tests/golden/*.txt, each with its source
+"""
+
+import itertools
+import math
+
+import numpy as np
+import torch
+import torch.nn.functional as F
+
+import oracle.moe_oracle as O
+
+from conftest import read_golden
+
+
+def _rng(seed):
+    return np.random.default_rng(seed)
+
+
+# ---------------------------------------------------------------- stage 1
+def check_router_onehot():
+    """x_t = unit vector e_c picks out column c of W_r (catches a transposed
+    or mis-indexed router product) and the offset adds per expert."""
+    rng = _rng(1)
+    E, d = 3, 5
+    W_r = rng.normal(size=(E, d))
+    x = np.eye(d)
+    s = O.router_logits(x, W_r)
+    assert s.shape == (d, E)
+    for c in range(d):
+        np.testing.assert_array_equal(s[c], W_r[:, c])
+    off = np.array([0.5, -1.0, 2.0])
+    s2 = O.router_logits(x, W_r, off)
+    np.testing.assert_allclose(s2 - s, np.tile(off, (d, 1)), rtol=0, atol=1e-15)
+    # linearity in x with a general vector
+    xv = rng.normal(size=(1, d))
+    ref = sum(xv[0, c] * W_r[:, c] for c in range(d))
+    np.testing.assert_allclose(O.router_logits(xv, W_r)[0], ref, rtol=1e-14, atol=1e-14)
+
+
+# ---------------------------------------------------------------- stage 2
+def check_topk_bruteforce():
+    """For every E <= 7 and k <= E the chosen set maximises the summed selection
+    score over all C(E, k) subsets and is listed in descending order."""
+    rng = _rng(2)
+    for E in range(1, 8):
+        for k in range(1, E + 1):
+            sel = rng.normal(size=(6, E))
+            idx = O.topk_indices(sel, k)
+            for t in range(sel.shape[0]):
+                best = max(itertools.combinations(range(E), k),
+                           key=lambda c: sum(sel[t, list(c)]))
+                assert set(idx[t].tolist()) == set(best)
+                vals = sel[t, idx[t]]
+                assert np.all(np.diff(vals) <= 0)
+
+
+def check_topk_ties():
+    """Equal scores resolve to the lower expert index."""
+    sel = np.array([[1.0, 3.0, 3.0, 2.0], [0.0, 0.0, 0.0, 0.0]])
+    idx = O.topk_indices(sel, 2)
+    assert idx[0].tolist() == [1, 2]
+    assert idx[1].tolist() == [0, 1]
+    assert O.topk_indices(sel, 4)[1].tolist() == [0, 1, 2, 3]
+
+
+def check_gates_closed_form():
+    """Hand-derived gates for logits [2, 1, 0, -1] with k = 2."""
+    s = np.array([[2.0, 1.0, 0.0, -1.0]])
+    idx = np.array([[0, 1]])
+    e = math.e
+    g = O.gate_values(s, idx, O.GATE_SOFTMAX_TOPK)
+    np.testing.assert_allclose(g[0], [e / (e + 1), 1 / (e + 1)], rtol=1e-14)
+    g = O.gate_values(s, idx, O.GATE_SOFTMAX_FULL)
+    z = math.exp(2) + math.exp(1) + 1 + math.exp(-1)
+    np.testing.assert_allclose(g[0], [math.exp(2) / z, math.exp(1) / z], rtol=1e-14)
+    g = O.gate_values(s, idx, O.GATE_SIGMOID_RENORM)
+    s2, s1 = 1 / (1 + math.exp(-2)), 1 / (1 + math.exp(-1))
+    np.testing.assert_allclose(g[0], [s2 / (s1 + s2), s1 / (s1 + s2)], rtol=1e-14)
+
+
+def check_gates_invariants():
+    """Softmax over the chosen equals the full softmax renormalised over them;
+    top-k and sigmoid gates sum to 1; top-1 softmax-over-chosen is exactly 1."""
+    rng = _rng(3)
+    s = rng.normal(size=(20, 9)) * 2
+    for k in (1, 2, 3, 9):
+        idx = O.topk_indices(s, k)
+        g = O.gate_values(s, idx, O.GATE_SOFTMAX_TOPK)
+        full = O.softmax_rows(s)
+        ren = np.take_along_axis(full, idx, 1)
+        ren = ren / ren.sum(1, keepdims=True)
+        np.testing.assert_allclose(g, ren, rtol=1e-13, atol=1e-15)
+        np.testing.assert_allclose(g.sum(1), 1.0, rtol=1e-14)
+        gs = O.gate_values(s, idx, O.GATE_SIGMOID_RENORM)
+        np.testing.assert_allclose(gs.sum(1), 1.0, rtol=1e-14)
+        assert np.all(gs > 0)
+        if k == 1:
+            np.testing.assert_array_equal(g, 1.0)
+        gf = O.gate_values(s, idx, O.GATE_SOFTMAX_FULL)
+        np.testing.assert_allclose(gf, np.take_along_axis(full, idx, 1), rtol=1e-13)
+
+
+def check_router_probs():
+    """Full distributions: softmax rows and normalised sigmoids sum to 1 and
+    match hand values."""
+    s = np.array([[2.0, 1.0, 0.0, -1.0]])
+    p = O.router_probs(s, O.GATE_SOFTMAX_TOPK)
+    z = math.exp(2) + math.exp(1) + 1 + math.exp(-1)
+    np.testing.assert_allclose(p[0], [math.exp(v) / z for v in (2, 1, 0, -1)], rtol=1e-14)
+    q = O.router_probs(s, O.GATE_SIGMOID_RENORM)
+    sg = [1 / (1 + math.exp(-v)) for v in (2, 1, 0, -1)]
+    np.testing.assert_allclose(q[0], [v / sum(sg) for v in sg], rtol=1e-14)
+
+
+def check_selection_bias():
+    """The bias changes which experts are chosen, never the gate values; a
+    uniform shift of the bias changes nothing; a zero bias equals no bias."""
+    s = np.array([[0.0, 0.1, 0.2]])
+    b = np.array([0.5, 0.0, 0.0])
+    sel = O.selection_scores(s, O.GATE_SIGMOID_RENORM, b)
+    np.testing.assert_allclose(sel[0], [0.5 + 0.5, 1 / (1 + math.exp(-0.1)),
+                                        1 / (1 + math.exp(-0.2))], rtol=1e-14)
+    idx = O.topk_indices(sel, 2)
+    assert idx[0].tolist() == [0, 2]
+    g = O.gate_values(s, idx, O.GATE_SIGMOID_RENORM)
+    a0, a2 = 0.5, 1 / (1 + math.exp(-0.2))
+    np.testing.assert_allclose(g[0], [a0 / (a0 + a2), a2 / (a0 + a2)], rtol=1e-14)
+    rng = _rng(4)
+    s = rng.normal(size=(30, 8))
+    b = rng.uniform(-0.05, 0.05, size=8)
+    for mode in O.GATE_MODES:
+        r0 = O.route(s[:, :8] @ np.eye(8), np.eye(8), 3, mode, sel_bias=b)
+        r1 = O.route(s[:, :8] @ np.eye(8), np.eye(8), 3, mode, sel_bias=b + 0.37)
+        np.testing.assert_array_equal(r0[2], r1[2])
+        np.testing.assert_allclose(r0[3], r1[3], rtol=1e-14)
+        rz = O.route(s, np.eye(8), 3, mode, sel_bias=np.zeros(8))
+        rn = O.route(s, np.eye(8), 3, mode)
+        np.testing.assert_array_equal(rz[2], rn[2])
+        np.testing.assert_array_equal(rz[3], rn[3])
+        # gates depend on the unbiased logits only
+        np.testing.assert_allclose(r0[3], O.gate_values(s, r0[2], mode), rtol=1e-14)
+
+
+# ---------------------------------------------------------------- stage 3
+def check_capacity_formula():
+    """C = ceil(k*T*rho/E): the Switch layer gives 80; ragged cases round up;
+    no factor means no limit."""
+    assert O.expert_capacity(4096, 1, 64, 1.25) == 80
+    assert O.expert_capacity(10, 1, 3, 1.0) == 4
+    assert O.expert_capacity(10, 2, 3, 1.0) == 7
+    assert O.expert_capacity(7, 1, 8, 0.5) == 1
+    assert O.expert_capacity(100, 1, 4, 0.0) is None
+    assert O.expert_capacity(100, 1, 4, None) is None
+
+
+def check_capacity_drops():
+    """Top-1 drops equal sum_e max(0, routed_e - C) over a rho sweep 0.5..2.0
+    (chapter 11, exercise 4); kept + drops = T*k; no drops once rho >= E/k;
+    the kept assignments of each expert are its first C keys."""
+    rng = _rng(5)
+    T, E = 300, 6
+    for k in (1, 2, 3):
+        probs = rng.dirichlet([0.6] * E, size=T)
+        idx = np.stack([rng.choice(E, size=k, replace=False, p=probs[t]) for t in range(T)])
+        for rho in (0.5, 0.75, 1.0, 1.25, 1.5, 2.0, E / k):
+            C = O.expert_capacity(T, k, E, rho)
+            a = O.assign_slots(idx, E, C)
+            counts = np.bincount(idx.ravel(), minlength=E)
+            np.testing.assert_array_equal(a.routed, counts)
+            drops = int(sum(max(0, int(c) - C) for c in counts))
+            assert int(a.kept.sum()) == T * k - drops
+            np.testing.assert_array_equal(a.kept, np.minimum(counts, C))
+            if rho >= E / k:
+                assert drops == 0
+            # first come by token index: keys of expert e in key order
+            for e in range(E):
+                keys = [(t * k + j) for t in range(T) for j in range(k) if idx[t, j] == e]
+                kept_keys = [(t * k + j) for t in range(T) for j in range(k)
+                             if idx[t, j] == e and a.slot_pos[t, j] >= 0]
+                assert kept_keys == keys[:C]
+
+
+def check_offsets_and_permutation():
+    """offsets are the exclusive scan of kept counts; every kept slot has a
+    unique row inside its expert's segment; rows within a segment follow key
+    order; the permutation round-trips."""
+    rng = _rng(6)
+    T, E, k = 97, 5, 2
+    idx = np.stack([rng.choice(E, size=k, replace=False) for _ in range(T)])
+    for C in (None, 30, 7):
+        a = O.assign_slots(idx, E, C)
+        assert a.offsets[0] == 0
+        np.testing.assert_array_equal(np.diff(a.offsets), a.kept)
+        rows = O.permutation_rows(a, idx)
+        assert np.all(rows >= 0)
+        seen = set()
+        for t in range(T):
+            for j in range(k):
+                r = a.slot_pos[t, j]
+                if r < 0:
+                    continue
+                e = idx[t, j]
+                assert a.offsets[e] <= r < a.offsets[e + 1]
+                assert rows[r] == t
+                seen.add(int(r))
+        assert seen == set(range(int(a.offsets[-1])))
+        for e in range(E):
+            seg = rows[a.offsets[e]:a.offsets[e + 1]]
+            assert np.all(np.diff(seg) > 0)   # one key per (token, expert); key order
+
+
+# ---------------------------------------------------------------- stage 5/6
+def _rand_layer(seed, T, d, E, f, swiglu):
+    rng = _rng(seed)
+    x = rng.normal(size=(T, d))
+    W_r = rng.normal(size=(E, d)) / math.sqrt(d)
+    W1 = rng.normal(size=(E, f, d)) / math.sqrt(d)
+    W2 = rng.normal(size=(E, d, f)) / math.sqrt(f)
+    W3 = rng.normal(size=(E, f, d)) / math.sqrt(d) if swiglu else None
+    return x, W_r, W1, W2, W3
+
+
+def _dense_reference(x, W_r, W1, W2, W3, k, act, mode, sel_bias=None, Ws=None):
+    """Brute force: all E experts on every token, mixed by a dense gate vector
+    that is zero outside the chosen set, written without the oracle's sparse
+    loop; the expert itself is written out with torch.nn.functional."""
+    s = x @ W_r.T
+    sel = O.selection_scores(s, mode, sel_bias)
+    idx = O.topk_indices(sel, k)
+    g = O.gate_values(s, idx, mode)
+    T, E = s.shape
+    dense_g = np.zeros((T, E))
+    for t in range(T):
+        dense_g[t, idx[t]] = g[t]
+    xt = torch.from_numpy(x)
+    y = torch.zeros_like(xt)
+    for e in range(E):
+        a = F.linear(xt, torch.from_numpy(W1[e]))
+        if act == O.ACT_GELU:
+            h = F.gelu(a, approximate="none")
+        elif act == O.ACT_RELU:
+            h = F.relu(a)
+        else:
+            h = F.silu(a) * F.linear(xt, torch.from_numpy(W3[e]))
+        y += torch.from_numpy(dense_g[:, e:e + 1]) * F.linear(h, torch.from_numpy(W2[e]))
+    if Ws is not None:
+        Ws1, Ws3, Ws2 = (torch.from_numpy(w) for w in Ws)
+        y += F.linear(F.silu(F.linear(xt, Ws1)) * F.linear(xt, Ws3), Ws2)
+    return y.numpy()
+
+
+def check_sparse_equals_dense():
+    """The sparse evaluation (only chosen experts run) equals the dense mixture
+    with zero gates off the chosen set, for every activation and gate mode."""
+    for n, (act, mode, k) in enumerate([
+            (O.ACT_GELU, O.GATE_SOFTMAX_TOPK, 2),
+            (O.ACT_RELU, O.GATE_SOFTMAX_FULL, 1),
+            (O.ACT_SWIGLU, O.GATE_SIGMOID_RENORM, 3),
+            (O.ACT_SWIGLU, O.GATE_SOFTMAX_TOPK, 6)]):
+        T, d, E, f = 13, 8, 6, 12
+        x, W_r, W1, W2, W3 = _rand_layer(10 + n, T, d, E, f, act == O.ACT_SWIGLU)
+        b = _rng(20 + n).uniform(-0.05, 0.05, E) if mode == O.GATE_SIGMOID_RENORM else None
+        r = O.moe_forward(x, W_r, W1, W2, k, act, mode, W3=W3, sel_bias=b)
+        ref = _dense_reference(x, W_r, W1, W2, W3, k, act, mode, sel_bias=b)
+        np.testing.assert_allclose(r.y, ref, rtol=1e-12, atol=1e-12)
+    # with a shared SwiGLU expert added at weight 1
+    T, d, E, f = 9, 8, 4, 10
+    x, W_r, W1, W2, W3 = _rand_layer(40, T, d, E, f, True)
+    rng = _rng(41)
+    Ws = (rng.normal(size=(6, d)), rng.normal(size=(6, d)), rng.normal(size=(d, 6)))
+    r = O.moe_forward(x, W_r, W1, W2, 2, O.ACT_SWIGLU, O.GATE_SOFTMAX_TOPK, W3=W3,
+                      Ws1=Ws[0], Ws3=Ws[1], Ws2=Ws[2])
+    ref = _dense_reference(x, W_r, W1, W2, W3, 2, O.ACT_SWIGLU, O.GATE_SOFTMAX_TOPK, Ws=Ws)
+    np.testing.assert_allclose(r.y, ref, rtol=1e-12, atol=1e-12)
+
+
+def check_drop_is_identity_branch():
+    """A dropped slot contributes zero (the caller's residual carries the token);
+    the surviving slot keeps its gate (no renormalisation)."""
+    T, d, E, f, k = 8, 4, 2, 6, 2
+    x, W_r, W1, W2, W3 = _rand_layer(50, T, d, E, f, False)
+    full = O.moe_forward(x, W_r, W1, W2, k, O.ACT_RELU, O.GATE_SOFTMAX_TOPK)
+    capped = O.moe_forward(x, W_r, W1, W2, k, O.ACT_RELU, O.GATE_SOFTMAX_TOPK,
+                           capacity_factor=0.25)   # C = ceil(16*0.25/2) = 2
+    assert capped.asg.capacity == 2
+    for t in range(T):
+        ref = np.zeros(d)
+        for j in range(k):
+            if capped.asg.slot_pos[t, j] >= 0:
+                e = capped.topk_idx[t, j]
+                ref += full.topk_w[t, j] * O.expert_ffn(x[t], W1[e], W2[e], O.ACT_RELU)
+        np.testing.assert_allclose(capped.y[t], ref, rtol=1e-13, atol=1e-14)
+    # tokens 0 and 1 fill both experts (k = E = 2): every later token is dropped
+    assert np.all(capped.asg.slot_pos[2:] == -1)
+    np.testing.assert_array_equal(capped.y[2:], 0.0)
+
+
+def check_dense_ffn_special_case():
+    """E = 1, k = 1, no capacity: the layer is one dense FFN (gate 1), checked
+    against torch.nn.functional in float64 for GELU (erf), ReLU and SwiGLU."""
+    rng = _rng(7)
+    T, d, f = 11, 16, 24
+    x = rng.normal(size=(T, d))
+    W_r = rng.normal(size=(1, d))
+    W1 = rng.normal(size=(1, f, d)) / 4
+    W3 = rng.normal(size=(1, f, d)) / 4
+    W2 = rng.normal(size=(1, d, f)) / 5
+    xt = torch.from_numpy(x)
+    for act in O.ACTS:
+        r = O.moe_forward(x, W_r, W1, W2, 1, act, O.GATE_SOFTMAX_TOPK,
+                          W3=W3 if act == O.ACT_SWIGLU else None)
+        a = F.linear(xt, torch.from_numpy(W1[0]))
+        if act == O.ACT_GELU:
+            h = F.gelu(a, approximate="none")
+        elif act == O.ACT_RELU:
+            h = F.relu(a)
+        else:
+            h = F.silu(a) * F.linear(xt, torch.from_numpy(W3[0]))
+        ref = F.linear(h, torch.from_numpy(W2[0])).numpy()
+        np.testing.assert_allclose(r.y, ref, rtol=1e-12, atol=1e-13)
+
+
+def check_multiply_counts():
+    """Toy layer multiplies per token (page figure): 65,536 at top-2 and
+    262,144 when all 8 experts fire; SwiGLU experts cost 3*d*f; the active
+    fraction equals k/E (2/64 = 3.1%, 2/8 = 25%)."""
+    g = read_golden("toy_multiplies.txt")
+    acc = read_golden("expert_accounting.txt")
+    E, d, f = g["experts"], g["d_model"], g["d_ffn"]
+    assert 2 * d * f == g["weights_per_expert"]
+    T = 4
+    x, W_r, W1, W2, _ = _rand_layer(8, T, d, E, f, False)
+    r2 = O.moe_forward(x, W_r, W1, W2, 2, O.ACT_GELU, O.GATE_SOFTMAX_TOPK, count_multiplies=True)
+    assert r2.multiplies == T * g["multiplies_top2"]
+    r8 = O.moe_forward(x, W_r, W1, W2, E, O.ACT_GELU, O.GATE_SOFTMAX_TOPK, count_multiplies=True)
+    assert r8.multiplies == T * g["multiplies_all_fire"]
+    assert g["multiplies_all_fire"] // g["multiplies_top2"] == 4
+    # SwiGLU expert: 3*d*f multiplies per token; Mixtral shapes give ~5.6B per expert
+    c = O.MultiplyCounter()
+    dd, ff = 6, 10
+    rng = _rng(9)
+    O.expert_ffn(rng.normal(size=dd), rng.normal(size=(ff, dd)), rng.normal(size=(dd, ff)),
+                 O.ACT_SWIGLU, rng.normal(size=(ff, dd)), c)
+    assert c.count == 3 * dd * ff
+    per_expert = 3 * acc["d_model"] * acc["d_ffn"] * acc["layers"]
+    assert round(per_expert / 1e9, 1) == acc["per_expert_billions_rounded"]
+    # active fraction k/E from the counter, E = 64 and E = 8 at k = 2
+    for E_, pct in ((64, acc["active_fraction_percent_E64_k2"]), (8, acc["active_fraction_percent_E8_k2"])):
+        x, W_r, W1, W2, _ = _rand_layer(11, 3, 4, E_, 4, False)
+        rk = O.moe_forward(x, W_r, W1, W2, 2, O.ACT_RELU, O.GATE_SOFTMAX_TOPK, count_multiplies=True)
+        rall = O.moe_forward(x, W_r, W1, W2, E_, O.ACT_RELU, O.GATE_SOFTMAX_TOPK, count_multiplies=True)
+        assert round(100.0 * rk.multiplies / rall.multiplies, 1) == pct
+
+
+def check_balance_uniform():
+    """Uniform f and P give L = alpha exactly, for any N (the guide's 'Check
+    yourself': N makes the minimum 1 independent of N).  Built as a cyclic
+    layer: d = E, W_r = I, x_t = c * (e_{t mod E} + ... + e_{t+k-1 mod E})."""
+    for E, k in ((4, 1), (8, 2), (6, 3), (16, 1)):
+        T = 5 * E
+        x = np.zeros((T, E))
+        for t in range(T):
+            for j in range(k):
+                x[t, (t + j) % E] = 3.0
+        r = O.moe_forward(x, np.eye(E), np.zeros((E, 2, E)), np.zeros((E, E, 2)), k,
+                          O.ACT_RELU, O.GATE_SOFTMAX_TOPK, alpha=0.01)
+        np.testing.assert_allclose(r.f, 1.0 / E, rtol=1e-14)
+        np.testing.assert_allclose(r.P, 1.0 / E, rtol=1e-12)
+        assert abs(r.aux_loss - 0.01) < 1e-14
+        # sigmoid distribution, same symmetry
+        r = O.moe_forward(x, np.eye(E), np.zeros((E, 2, E)), np.zeros((E, E, 2)), k,
+                          O.ACT_RELU, O.GATE_SIGMOID_RENORM, alpha=1e-4)
+        assert abs(r.aux_loss - 1e-4) < 1e-16
+
+
+def check_balance_hand_and_collapse():
+    """Hand-computed f, P, L for 4 tokens; collapsed routing costs more than
+    balanced routing (chapter 11, exercise 3 and its demo)."""
+    probs = np.array([[0.7, 0.2, 0.1], [0.1, 0.8, 0.1], [0.6, 0.3, 0.1], [0.2, 0.2, 0.6]])
+    routed = np.array([2, 1, 1])
+    f, P, L = O.balance_stats(routed, probs, T=4, k=1, alpha=0.01)
+    np.testing.assert_allclose(f, [0.5, 0.25, 0.25], rtol=1e-15)
+    np.testing.assert_allclose(P, [0.4, 0.375, 0.225], rtol=1e-14)
+    assert abs(L - 0.01 * 3 * (0.5 * 0.4 + 0.25 * 0.375 + 0.25 * 0.225)) < 1e-16
+    # k = 2: f divides by T*k
+    f2, _, _ = O.balance_stats(np.array([3, 3, 2]), probs, T=4, k=2, alpha=0.01)
+    np.testing.assert_allclose(f2, [3 / 8, 3 / 8, 2 / 8], rtol=1e-15)
+    rng = _rng(0)
+    E, T = 4, 100
+    bal = rng.dirichlet([5.0] * E, size=T)
+    col = rng.dirichlet([10.0, 0.1, 0.1, 0.1], size=T)
+    Lb = O.balance_stats(np.bincount(bal.argmax(1), minlength=E), bal, T, 1, 0.01)[2]
+    Lc = O.balance_stats(np.bincount(col.argmax(1), minlength=E), col, T, 1, 0.01)[2]
+    assert Lc > Lb
+
+
+def check_pipeline_stats_pre_drop():
+    """In the full pipeline f counts assignments before drops (so sum f = 1
+    even when capacity drops some), while kept counts drop."""
+    T, d, E, f_, k = 40, 6, 4, 5, 2
+    x, W_r, W1, W2, _ = _rand_layer(60, T, d, E, f_, False)
+    off = np.array([2.0, 0.0, 0.0, -2.0])
+    r = O.moe_forward(x, W_r, W1, W2, k, O.ACT_RELU, O.GATE_SOFTMAX_TOPK,
+                      logit_offset=off, capacity_factor=1.0)
+    assert int(r.asg.kept.sum()) < T * k
+    np.testing.assert_allclose(r.f.sum(), 1.0, rtol=1e-15)
+    np.testing.assert_allclose(r.f, r.asg.routed / (T * k), rtol=1e-15)
+    np.testing.assert_allclose(r.P.sum(), 1.0, rtol=1e-14)
+
+
+ALL_CHECKS = [
+    check_router_onehot, check_topk_bruteforce, check_topk_ties, check_gates_closed_form,
+    check_gates_invariants, check_router_probs, check_selection_bias,
+    check_capacity_formula, check_capacity_drops, check_offsets_and_permutation,
+    check_sparse_equals_dense, check_drop_is_identity_branch, check_dense_ffn_special_case,
+    check_multiply_counts, check_balance_uniform, check_balance_hand_and_collapse,
+    check_pipeline_stats_pre_drop,
+]

@@ -1,0 +1,154 @@
+"""Plant plausible mistakes in the CPU oracle and show that a pin catches each.
+
+Every mutation below replaces one oracle function (on the CPU, for the
+duration of one test) with a wrong variant: a dropped term, a wrong sign or
+index, a transposed operand, a wrong rounding.  The named pin must then fail.
+"""
+import math
+
+import numpy as np
+import pytest
+
+import oracle as O
+import oracle.moe_oracle as M
+import oracle_pins as P
+
+_orig = {name: getattr(M, name) for name in (
+    "router_logits", "topk_indices", "gate_values", "affinity", "expert_capacity",
+    "assign_slots", "gelu_erf", "silu", "expert_ffn", "balance_stats", "router_probs",
+    "softmax_rows")}
+
+
+def _router_reversed(x, W_r, logit_offset=None):
+    return _orig["router_logits"](x, W_r, logit_offset)[:, ::-1]
+
+
+def _router_offset_sign(x, W_r, logit_offset=None):
+    s = _orig["router_logits"](x, W_r, None)
+    return s if logit_offset is None else s - np.asarray(logit_offset)[None, :]
+
+
+def _topk_ascending(sel, k):
+    return _orig["topk_indices"](-np.asarray(sel, dtype=float), k)
+
+
+def _topk_ties_high(sel, k):
+    sel = np.asarray(sel, dtype=float)
+    E = sel.shape[1]
+    return (E - 1) - _orig["topk_indices"](sel[:, ::-1], k)
+
+
+def _gates_full_softmax(s, idx, mode):
+    if mode == M.GATE_SOFTMAX_TOPK:
+        mode = M.GATE_SOFTMAX_FULL
+    return _orig["gate_values"](s, idx, mode)
+
+
+def _gates_sigmoid_unnormalised(s, idx, mode):
+    g = _orig["gate_values"](s, idx, mode)
+    if mode == M.GATE_SIGMOID_RENORM:
+        return M.sigmoid(np.take_along_axis(np.asarray(s, dtype=float), np.asarray(idx), 1))
+    return g
+
+
+def _affinity_no_sigmoid(s, mode):
+    return np.asarray(s, dtype=float)
+
+
+def _capacity_floor(T, k, E, rho):
+    if rho is None or rho <= 0:
+        return None
+    return int(math.floor(k * T * rho / E))
+
+
+def _capacity_no_k(T, k, E, rho):
+    return _orig["expert_capacity"](T, 1, E, rho)
+
+
+def _assign_last_come(idx, E, capacity):
+    idx = np.asarray(idx)
+    a = _orig["assign_slots"](idx[::-1, ::-1], E, capacity)
+    a.slot_pos = a.slot_pos[::-1, ::-1]
+    a.pos = a.pos[::-1, ::-1]
+    return a
+
+
+def _gelu_tanh(z):
+    z = np.asarray(z, dtype=float)
+    return 0.5 * z * (1 + np.tanh(math.sqrt(2 / math.pi) * (z + 0.044715 * z ** 3)))
+
+
+def _silu_plain_sigmoid(z):
+    return M.sigmoid(z)
+
+
+def _ffn_swiglu_no_up(xt, W1, W2, act, W3=None, counter=None):
+    if act == M.ACT_SWIGLU:
+        W3 = np.ones_like(np.asarray(W1, dtype=float)) * 0 + np.asarray(W1, dtype=float)
+    return _orig["expert_ffn"](xt, W1, W2, act, W3, counter)
+
+
+def _ffn_swapped_gate_up(xt, W1, W2, act, W3=None, counter=None):
+    if act == M.ACT_SWIGLU:
+        return _orig["expert_ffn"](xt, W3, W2, act, W1, counter)
+    return _orig["expert_ffn"](xt, W1, W2, act, W3, counter)
+
+
+def _ffn_transposed_down(xt, W1, W2, act, W3=None, counter=None):
+    W2 = np.asarray(W2, dtype=float)
+    if W2.shape[0] == W2.shape[1]:
+        W2 = W2.T
+    else:
+        W2 = W2[::-1]
+    return _orig["expert_ffn"](xt, W1, W2, act, W3, counter)
+
+
+def _balance_no_k(routed, probs, T, k, alpha):
+    return _orig["balance_stats"](routed, probs, T, 1, alpha)
+
+
+def _balance_no_E(routed, probs, T, k, alpha):
+    f, P, L = _orig["balance_stats"](routed, probs, T, k, alpha)
+    return f, P, L / len(np.asarray(routed))
+
+
+def _probs_unnormalised_sigmoid(s, mode):
+    if mode == M.GATE_SIGMOID_RENORM:
+        return M.sigmoid(s)
+    return _orig["router_probs"](s, mode)
+
+
+def _softmax_no_shift_bug(z):
+    z = np.asarray(z, dtype=float)
+    return np.exp(z) / np.exp(z).sum(axis=-1, keepdims=True) * 1.0000001
+
+
+MUTATIONS = [
+    ("router expert order reversed", "router_logits", _router_reversed, P.check_router_onehot),
+    ("router offset sign flipped", "router_logits", _router_offset_sign, P.check_router_onehot),
+    ("top-k takes the smallest", "topk_indices", _topk_ascending, P.check_topk_bruteforce),
+    ("ties go to the higher index", "topk_indices", _topk_ties_high, P.check_topk_ties),
+    ("top-k gates use the full softmax", "gate_values", _gates_full_softmax, P.check_gates_closed_form),
+    ("sigmoid gates not renormalised", "gate_values", _gates_sigmoid_unnormalised, P.check_gates_invariants),
+    ("sigmoid affinity dropped", "affinity", _affinity_no_sigmoid, P.check_selection_bias),
+    ("capacity rounded down", "expert_capacity", _capacity_floor, P.check_capacity_formula),
+    ("capacity ignores k", "expert_capacity", _capacity_no_k, P.check_capacity_formula),
+    ("last come kept instead of first", "assign_slots", _assign_last_come, P.check_capacity_drops),
+    ("GELU tanh approximation", "gelu_erf", _gelu_tanh, P.check_dense_ffn_special_case),
+    ("SiLU without the z factor", "silu", _silu_plain_sigmoid, P.check_dense_ffn_special_case),
+    ("SwiGLU up projection replaced", "expert_ffn", _ffn_swiglu_no_up, P.check_sparse_equals_dense),
+    ("SwiGLU gate and up swapped", "expert_ffn", _ffn_swapped_gate_up, P.check_dense_ffn_special_case),
+    ("down projection transposed", "expert_ffn", _ffn_transposed_down, P.check_sparse_equals_dense),
+    ("f divides by T, not T*k", "balance_stats", _balance_no_k, P.check_balance_uniform),
+    ("loss misses the factor N", "balance_stats", _balance_no_E, P.check_balance_uniform),
+    ("sigmoid P not normalised", "router_probs", _probs_unnormalised_sigmoid, P.check_router_probs),
+    ("softmax scaled wrongly", "softmax_rows", _softmax_no_shift_bug, P.check_gates_invariants),
+]
+
+
+@pytest.mark.parametrize("name,attr,bad,check", MUTATIONS, ids=[m[0] for m in MUTATIONS])
+def test_pin_catches_mutation(monkeypatch, name, attr, bad, check):
+    check()  # passes on the real oracle
+    monkeypatch.setattr(M, attr, bad)
+    with pytest.raises(AssertionError):
+        check()
