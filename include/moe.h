@@ -1,0 +1,241 @@
+/*
+ * moe.h -- C ABI of libmoe.so: the forward pass of one sparse top-k
+ * Mixture-of-Experts FFN layer on one NVIDIA B300 (sm_103a).
+ *
+ * What the layer computes (sources: page title, then section):
+ *   1. router scores  s = W_r x (+ o)        "Mixture of Experts" (llm-tutorial
+ *      ch. 11) § The mathematics; "Mixture of experts" (inside-the-model
+ *      guide) § The computation; "Chapter 33 — Mixture of Experts" § The Router.
+ *   2. top-k selection and gates: softmax over the k chosen logits
+ *      (ch. 11 § Top-k routing), the full-softmax probability of a top-1
+ *      choice (ch. 11 § Top-1 vs top-2), or sigmoid affinities renormalised
+ *      over the chosen (guide § The computation, § Auxiliary-loss-free
+ *      balancing); an optional per-expert bias steers only the choice.
+ *   3. expert capacity with overflow dropped to the residual, first come by
+ *      token index (ch. 11 § Expert capacity and dropped tokens; guide
+ *      § Auxiliary loss).
+ *   4. permutation of token copies into expert-contiguous order
+ *      ("Chapter 33" § Simple MoE Layer Implementation: per-expert gather).
+ *   5. expert MLPs: W2 act(W1 x) with GELU or ReLU, or SwiGLU
+ *      W2 (silu(W1 x) * (W3 x)); optional always-on shared SwiGLU expert
+ *      (guide § Fine-grained and shared experts).
+ *   6. combine y = sum_j g_j Expert_j(x) (+ shared), and the balance
+ *      statistics f_i, P_i, L = alpha * E * sum_i f_i P_i (guide § Auxiliary
+ *      loss; ch. 11 § The auxiliary loss).
+ *
+ * Conventions shared by every entry point:
+ *   - Every tensor pointer is DEVICE memory owned by the caller, unless the
+ *     entry point says "host".  The library allocates no memory, keeps no
+ *     state between calls and never synchronises the stream, except
+ *     moe_check_status, which does.
+ *   - All calls are asynchronous on `stream` (a cudaStream_t passed as
+ *     void*; NULL = the legacy default stream).  The return value covers
+ *     errors detected before or while enqueueing: argument checks and launch
+ *     failures.  Errors found on the device (a bounded wait that ran out) are
+ *     recorded in a status word inside the workspace.  moe_check_status
+ *     reports them.
+ *   - Row-major layouts, no padding:
+ *       x      [T, d]       dtype          y      [T, d]   dtype
+ *       W_r    [E, d]       dtype          W1, W3 [E, f, d] dtype
+ *       W2     [E, d, f]    dtype          Ws1,Ws3[f_s, d] dtype
+ *       Ws2    [d, f_s]     dtype
+ *       topk_idx [T, k] int32, topk_w [T, k] float32
+ *     dtype is float32 (MOE_F32) or bfloat16 (MOE_BF16) for all of x, W_r,
+ *     the expert weights and y.  logit_offset and sel_bias are float32 [E].
+ *     Router arithmetic, gates and statistics are float32 on both paths.
+ *   - Pointers to tensors must be 16-byte aligned.  On the bf16 path d, f
+ *     and f_s must be multiples of 8; on the float32 path, multiples of 4.
+ *   - The workspace is caller-owned device memory of at least
+ *     moe_workspace_size() bytes, 256-byte aligned.  Concurrent calls on
+ *     different streams need separate workspaces.
+ */
+#ifndef MOE_H_
+#define MOE_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---- status codes ------------------------------------------------------- */
+enum {
+  MOE_OK = 0,
+  MOE_ERR_ARG = 1,          /* NULL where a tensor is required, bad size or mode, misalignment */
+  MOE_ERR_UNSUPPORTED = 2,  /* valid layer this build does not run (E > 512, k > 32, ...) */
+  MOE_ERR_WORKSPACE = 3,    /* workspace NULL, too small or not 256-byte aligned */
+  MOE_ERR_CUDA = 4,         /* a CUDA runtime call or launch failed */
+  MOE_ERR_TIMEOUT = 5,      /* a bounded device wait ran out (reported by moe_check_status) */
+  MOE_ERR_DEVICE = 6        /* current device is not a compute-capability 10.3 GPU */
+};
+
+typedef enum { MOE_F32 = 0, MOE_BF16 = 1 } moe_dtype;
+typedef enum { MOE_ACT_GELU = 0, MOE_ACT_RELU = 1, MOE_ACT_SWIGLU = 2 } moe_act;
+typedef enum {
+  MOE_GATE_SOFTMAX_TOPK = 0,    /* g = softmax of the k chosen logits */
+  MOE_GATE_SIGMOID_RENORM = 1,  /* g = sigmoid(s_i) / sum over chosen of sigmoid(s_j) */
+  MOE_GATE_SOFTMAX_FULL = 2     /* g = softmax over all E logits, read at the chosen i */
+} moe_gate;
+
+/* Layer description.  All fields are read by value during the call. */
+typedef struct {
+  int32_t T;        /* tokens in the batch, >= 0 */
+  int32_t d;        /* model width, >= 1 */
+  int32_t E;        /* routed experts, 1..512 */
+  int32_t k;        /* experts per token, 1..min(E, 32) */
+  int32_t f;        /* routed expert width, >= 1 */
+  int32_t n_shared; /* 0 or 1 always-on shared SwiGLU expert */
+  int32_t f_shared; /* width of the shared expert (ignored when n_shared = 0) */
+  int32_t dtype;    /* moe_dtype */
+  int32_t act;      /* moe_act of the routed experts */
+  int32_t gate;     /* moe_gate */
+  double capacity_factor; /* rho; <= 0 means no capacity limit.  Otherwise the
+                             capacity is C = ceil((double)(k*T) * rho / E),
+                             the same C for every expert */
+  float alpha;      /* coefficient of the balance loss */
+  int32_t reserved; /* must be 0 */
+} moe_config;
+
+/* Number of bytes of workspace moe_forward needs for this layer. */
+int moe_workspace_size(const moe_config* cfg, size_t* bytes);
+
+/*
+ * moe_forward -- all six stages, enqueued on `stream`.
+ *
+ * Inputs (device, read only):
+ *   x, W_r, W1, W2            required
+ *   W3                        required iff act == MOE_ACT_SWIGLU, else NULL
+ *   Ws1, Ws3, Ws2             required iff n_shared == 1, else NULL
+ *   logit_offset [E] float32  optional: added to every token's logits; it
+ *                             enters the gates and P like the logits do
+ *   sel_bias [E] float32      optional: added to the affinity (the logit, or
+ *                             its sigmoid) for the choice only; gates and P
+ *                             ignore it ("Mixture of experts" guide
+ *                             § Auxiliary-loss-free balancing)
+ * Outputs (device, written):
+ *   y [T, d] (dtype)          MoE branch only; a token whose every slot was
+ *                             dropped gets 0 (the caller adds the residual)
+ *   topk_idx [T, k] int32     chosen experts, descending selection score,
+ *                             ties to the lower index
+ *   topk_w [T, k] float32     gates (also reported for dropped slots)
+ *   expert_counts [E] int32   assignments kept per expert (after capacity)
+ *   aux_loss [1] float32      alpha * E * sum_i f_i P_i
+ * Optional outputs (device, may be NULL):
+ *   routed_counts [E] int32   assignments per expert before capacity
+ *   offsets [E+1] int32       exclusive scan of expert_counts
+ *   slot_pos [T, k] int32     offsets[e] + position of the assignment among
+ *                             the kept ones of expert e, or -1 if dropped
+ *   f_out [E] float32         routed_counts / (T*k)
+ *   P_out [E] float32         mean over tokens of the full router
+ *                             distribution (softmax of s over all E, or
+ *                             sigmoid(s) normalised over all E)
+ * Errors: MOE_ERR_ARG / _UNSUPPORTED / _WORKSPACE before anything is
+ * enqueued; MOE_ERR_CUDA if a launch fails; MOE_ERR_DEVICE off sm_103.
+ * T = 0 is valid: counts, offsets, statistics and the loss are set to 0.
+ */
+int moe_forward(const moe_config* cfg,
+                const void* x, const void* W_r,
+                const float* logit_offset, const float* sel_bias,
+                const void* W1, const void* W3, const void* W2,
+                const void* Ws1, const void* Ws3, const void* Ws2,
+                void* y, int32_t* topk_idx, float* topk_w,
+                int32_t* expert_counts, float* aux_loss,
+                int32_t* routed_counts, int32_t* offsets, int32_t* slot_pos,
+                float* f_out, float* P_out,
+                void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * moe_route -- stages 1-3 and the balance statistics only (no expert
+ * MLPs): the routing half of moe_forward, with the same arguments, meaning
+ * and errors.  expert_counts and aux_loss are required; the other outputs
+ * are optional.  Needs moe_route_workspace_size() bytes.
+ */
+int moe_route_workspace_size(const moe_config* cfg, size_t* bytes);
+int moe_route(const moe_config* cfg,
+              const void* x, const void* W_r,
+              const float* logit_offset, const float* sel_bias,
+              int32_t* topk_idx, float* topk_w,
+              int32_t* expert_counts, float* aux_loss,
+              int32_t* routed_counts, int32_t* offsets, int32_t* slot_pos,
+              float* f_out, float* P_out,
+              void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * moe_forward_host_io -- moe_forward with the activations in HOST memory:
+ * x_host [T, d] is copied to the device, the layer runs, and y_host [T, d]
+ * and aux_loss_host [1] are copied back, all enqueued on `stream` (pinned
+ * host memory makes the copies asynchronous; the caller synchronises before
+ * reading y_host).  Weights, logit_offset and sel_bias are device pointers
+ * as in moe_forward.  topk_idx / topk_w / counts stay in the workspace.
+ * Needs moe_host_io_workspace_size() bytes.
+ */
+int moe_host_io_workspace_size(const moe_config* cfg, size_t* bytes);
+int moe_forward_host_io(const moe_config* cfg,
+                        const void* x_host, const void* W_r,
+                        const float* logit_offset, const float* sel_bias,
+                        const void* W1, const void* W3, const void* W2,
+                        const void* Ws1, const void* Ws3, const void* Ws2,
+                        void* y_host, float* aux_loss_host,
+                        void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * Synchronises `stream`, then reads and clears the device status word in
+ * `workspace`.  Returns MOE_OK, MOE_ERR_TIMEOUT when a bounded device wait
+ * gave up since the last check, or MOE_ERR_CUDA if the synchronisation
+ * itself failed.
+ */
+int moe_check_status(void* workspace, void* stream);
+
+/* Human-readable name of a status code (static storage, never NULL). */
+const char* moe_error_string(int code);
+
+/* ---- measurement support ------------------------------------------------ */
+
+/* Stages in the order moe_forward enqueues them. */
+enum {
+  MOE_STAGE_ROUTER = 0,   /* router scores + top-k + gates + block statistics */
+  MOE_STAGE_SCAN = 1,     /* counts, capacity, offsets, tile schedule, f, P, L */
+  MOE_STAGE_PERMUTE = 2,  /* slot positions and the copy into expert order */
+  MOE_STAGE_UP = 3,       /* expert up projection (+ activation / SwiGLU) */
+  MOE_STAGE_DOWN = 4,     /* expert down projection */
+  MOE_STAGE_COMBINE = 5,  /* gate-weighted combine (+ shared expert) */
+  MOE_NUM_STAGES = 6
+};
+
+/*
+ * Same as moe_forward, and also records events[i] (a cudaEvent_t passed as
+ * void*) on `stream` before stage i, and events[MOE_NUM_STAGES] after the
+ * last one: MOE_NUM_STAGES + 1 caller-created events.  Used to time each
+ * kernel on the stream it runs on.
+ */
+int moe_forward_timed(const moe_config* cfg,
+                      const void* x, const void* W_r,
+                      const float* logit_offset, const float* sel_bias,
+                      const void* W1, const void* W3, const void* W2,
+                      const void* Ws1, const void* Ws3, const void* Ws2,
+                      void* y, int32_t* topk_idx, float* topk_w,
+                      int32_t* expert_counts, float* aux_loss,
+                      int32_t* routed_counts, int32_t* offsets, int32_t* slot_pos,
+                      float* f_out, float* P_out,
+                      void* workspace, size_t workspace_bytes, void* stream,
+                      void* const* events);
+
+/* Number of kernels one moe_forward call launches for this layer. */
+int moe_launch_count(const moe_config* cfg, int32_t* launches);
+
+/*
+ * Self-test of the bounded device waits: launches one block that waits on
+ * a barrier nothing will complete, for at most `wait_ns` nanoseconds, then
+ * records a timeout in the workspace status word and returns.  A following
+ * moe_check_status returns MOE_ERR_TIMEOUT.
+ * The workspace needs at least 256 bytes.
+ */
+int moe_selftest_wait_timeout(void* workspace, size_t workspace_bytes,
+                              uint64_t wait_ns, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_H_ */

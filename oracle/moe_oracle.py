@@ -288,17 +288,19 @@ def silu(z) -> np.ndarray:
     return z * sigmoid(z)
 
 
-def _matvec(W, v, counter: Optional[MultiplyCounter]) -> np.ndarray:
+def _matmul_rows(X, W, counter: Optional[MultiplyCounter]) -> np.ndarray:
+    """Rows of X times W^T: each row is one token's matrix-vector product."""
     W = _f64(W)
     if counter is not None:
-        counter.count += W.shape[0] * W.shape[1]
-    return W @ v
+        counter.count += X.shape[0] * W.shape[0] * W.shape[1]
+    return X @ W.T
 
 
-def expert_ffn(xt, W1, W2, act: str, W3=None, counter: Optional[MultiplyCounter] = None) -> np.ndarray:
-    """One expert on one token.  W1, W3: [f, d]; W2: [d, f]; xt: [d]."""
-    xt = _f64(xt)
-    a = _matvec(W1, xt, counter)
+def expert_ffn_rows(X, W1, W2, act: str, W3=None, counter: Optional[MultiplyCounter] = None) -> np.ndarray:
+    """One expert applied to each row of X ([n, d]) independently.
+    W1, W3: [f, d]; W2: [d, f].  Returns [n, d]."""
+    X = _f64(X)
+    a = _matmul_rows(X, W1, counter)
     if act == ACT_GELU:
         h = gelu_erf(a)
     elif act == ACT_RELU:
@@ -306,11 +308,16 @@ def expert_ffn(xt, W1, W2, act: str, W3=None, counter: Optional[MultiplyCounter]
     elif act == ACT_SWIGLU:
         if W3 is None:
             raise ValueError("SwiGLU needs W3")
-        b = _matvec(W3, xt, counter)
+        b = _matmul_rows(X, W3, counter)
         h = silu(a) * b
     else:
         raise ValueError(act)
-    return _matvec(W2, h, counter)
+    return _matmul_rows(h, W2, counter)
+
+
+def expert_ffn(xt, W1, W2, act: str, W3=None, counter: Optional[MultiplyCounter] = None) -> np.ndarray:
+    """One expert on one token.  W1, W3: [f, d]; W2: [d, f]; xt: [d]."""
+    return expert_ffn_rows(_f64(xt)[None, :], W1, W2, act, W3, counter)[0]
 
 
 # --------------------------------------------------------------------------
@@ -409,11 +416,12 @@ def moe_forward(x, W_r, W1, W2, k: int, act: str, gate_mode: str, W3=None,
     for e in sorted(work):
         w1, w2 = W1i[e], W2i[e]
         w3 = W3i[e] if W3i is not None else None
-        for r, t, j in work[e]:
-            y[r] += g[t, j] * expert_ffn(x[t], w1, w2, act, w3, counter)
-    if Ws1 is not None:
-        for r, t in enumerate(tok):
-            y[r] += expert_ffn(x[t], Ws1, Ws2, ACT_SWIGLU, Ws3, counter)
+        items = work[e]
+        out = expert_ffn_rows(x[[t for _, t, _ in items]], w1, w2, act, w3, counter)
+        for i, (r, t, j) in enumerate(items):
+            y[r] += g[t, j] * out[i]
+    if Ws1 is not None and len(tok):
+        y += expert_ffn_rows(x[tok], Ws1, Ws2, ACT_SWIGLU, Ws3, counter)
     return OracleResult(s=s, sel=sel, topk_idx=idx, topk_w=g, probs=probs, gap=gap,
                         asg=asg, f=f, P=P, aux_loss=L, y=y,
                         tokens=None if tokens is None else tok,

@@ -1,0 +1,101 @@
+"""ctypes view of libmoe.so (the C ABI in include/moe.h).
+
+Loading fails loudly when the library has not been built: there is no
+fallback implementation of any stage.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libmoe.so")
+
+MOE_OK = 0
+MOE_ERR_ARG = 1
+MOE_ERR_UNSUPPORTED = 2
+MOE_ERR_WORKSPACE = 3
+MOE_ERR_CUDA = 4
+MOE_ERR_TIMEOUT = 5
+MOE_ERR_DEVICE = 6
+
+MOE_F32, MOE_BF16 = 0, 1
+MOE_ACT_GELU, MOE_ACT_RELU, MOE_ACT_SWIGLU = 0, 1, 2
+MOE_GATE_SOFTMAX_TOPK, MOE_GATE_SIGMOID_RENORM, MOE_GATE_SOFTMAX_FULL = 0, 1, 2
+MOE_NUM_STAGES = 6
+STAGE_NAMES = ("router", "scan", "permute", "up", "down", "combine")
+
+EXPORTS = (
+    "moe_workspace_size", "moe_forward", "moe_route_workspace_size", "moe_route",
+    "moe_host_io_workspace_size", "moe_forward_host_io", "moe_check_status",
+    "moe_error_string", "moe_forward_timed", "moe_launch_count", "moe_selftest_wait_timeout",
+)
+
+
+class MoeConfig(ctypes.Structure):
+    _fields_ = [
+        ("T", ctypes.c_int32), ("d", ctypes.c_int32), ("E", ctypes.c_int32),
+        ("k", ctypes.c_int32), ("f", ctypes.c_int32), ("n_shared", ctypes.c_int32),
+        ("f_shared", ctypes.c_int32), ("dtype", ctypes.c_int32), ("act", ctypes.c_int32),
+        ("gate", ctypes.c_int32), ("capacity_factor", ctypes.c_double),
+        ("alpha", ctypes.c_float), ("reserved", ctypes.c_int32),
+    ]
+
+
+class MoeError(RuntimeError):
+    def __init__(self, code: int, what: str):
+        self.code = code
+        super().__init__(f"{what}: {error_string(code)} (code {code})")
+
+
+_lib = None
+P = ctypes.c_void_p
+SZ = ctypes.c_size_t
+I32P = ctypes.POINTER(ctypes.c_int32)
+
+
+def lib() -> ctypes.CDLL:
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(
+                f"{LIB_PATH} is missing: build it with `python -m sparse_mixture_experts_65_b300.build`"
+                " (or __graft_entry__.build()); this package has no non-CUDA fallback")
+        L = ctypes.CDLL(LIB_PATH)
+        cfgp = ctypes.POINTER(MoeConfig)
+        for name in ("moe_workspace_size", "moe_route_workspace_size", "moe_host_io_workspace_size"):
+            f = getattr(L, name)
+            f.argtypes = [cfgp, ctypes.POINTER(SZ)]
+            f.restype = ctypes.c_int
+        fwd_args = [cfgp, P, P, P, P, P, P, P, P, P, P, P, P, P, P, P, P, P, P, P, P, P, SZ, P]
+        L.moe_forward.argtypes = fwd_args
+        L.moe_forward.restype = ctypes.c_int
+        L.moe_forward_timed.argtypes = fwd_args + [ctypes.POINTER(P)]
+        L.moe_forward_timed.restype = ctypes.c_int
+        L.moe_route.argtypes = [cfgp, P, P, P, P, P, P, P, P, P, P, P, P, P, P, SZ, P]
+        L.moe_route.restype = ctypes.c_int
+        L.moe_forward_host_io.argtypes = [cfgp, P, P, P, P, P, P, P, P, P, P, P, P, P, SZ, P]
+        L.moe_forward_host_io.restype = ctypes.c_int
+        L.moe_check_status.argtypes = [P, P]
+        L.moe_check_status.restype = ctypes.c_int
+        L.moe_error_string.argtypes = [ctypes.c_int]
+        L.moe_error_string.restype = ctypes.c_char_p
+        L.moe_launch_count.argtypes = [cfgp, I32P]
+        L.moe_launch_count.restype = ctypes.c_int
+        L.moe_selftest_wait_timeout.argtypes = [P, SZ, ctypes.c_uint64, P]
+        L.moe_selftest_wait_timeout.restype = ctypes.c_int
+        _lib = L
+    return _lib
+
+
+def error_string(code: int) -> str:
+    try:
+        return lib().moe_error_string(code).decode()
+    except Exception:  # pragma: no cover - only when the library itself is missing
+        return f"code {code}"
+
+
+def check(code: int, what: str) -> None:
+    if code != MOE_OK:
+        raise MoeError(code, what)

@@ -1,0 +1,82 @@
+// combine.cu -- stage 6: y[t] = shared(x_t) + sum_j g_tj * o[row(t, j)],
+// over the kept slots, accumulated in float32 in the fixed order j = 0..k-1
+// (no atomics), then rounded once to the output dtype.
+//
+// "Mixture of Experts" (llm-tutorial ch. 11) § The mathematics and
+// "Mixture-of-Experts" (neural networks visually) § Show the math: the layer
+// output is the gate-weighted sum over the chosen experts only; dropped
+// slots contribute nothing (ch. 11 § Expert capacity and dropped tokens).
+#include "common.cuh"
+#include "moe_internal.h"
+
+namespace moe {
+
+struct CombineArgs {
+  const float* o;        // [R_cap][d]
+  const float* os;       // [T_pad][d] or null
+  const int* key_row;    // [T*k]
+  const float* topk_w;   // [T*k]
+  void* y;               // [T][d]
+  int T, d, k;
+};
+
+__device__ __forceinline__ void store4(float* y, size_t i, float4 v) {
+  *reinterpret_cast<float4*>(y + i) = v;
+}
+__device__ __forceinline__ void store4(__nv_bfloat16* y, size_t i, float4 v) {
+  __nv_bfloat162 a = __floats2bfloat162_rn(v.x, v.y);
+  __nv_bfloat162 b = __floats2bfloat162_rn(v.z, v.w);
+  uint2 u;
+  u.x = *reinterpret_cast<uint32_t*>(&a);
+  u.y = *reinterpret_cast<uint32_t*>(&b);
+  *reinterpret_cast<uint2*>(y + i) = u;
+}
+
+template <typename TOut>
+__global__ void __launch_bounds__(kThreads) combine_kernel(const CombineArgs a) {
+  __shared__ int rows[kMaxK];
+  __shared__ float gates[kMaxK];
+  const int t = blockIdx.x;
+  if (threadIdx.x < a.k) {
+    rows[threadIdx.x] = a.key_row[(size_t)t * a.k + threadIdx.x];
+    gates[threadIdx.x] = a.topk_w[(size_t)t * a.k + threadIdx.x];
+  }
+  __syncthreads();
+  TOut* y = static_cast<TOut*>(a.y);
+  for (int c = threadIdx.x * 4; c < a.d; c += kThreads * 4) {
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (a.os) acc = *reinterpret_cast<const float4*>(a.os + (size_t)t * a.d + c);
+    for (int j = 0; j < a.k; ++j) {
+      const int r = rows[j];
+      if (r < 0) continue;
+      const float g = gates[j];
+      const float4 v = *reinterpret_cast<const float4*>(a.o + (size_t)r * a.d + c);
+      acc.x = fmaf(g, v.x, acc.x);
+      acc.y = fmaf(g, v.y, acc.y);
+      acc.z = fmaf(g, v.z, acc.z);
+      acc.w = fmaf(g, v.w, acc.w);
+    }
+    store4(y, (size_t)t * a.d + c, acc);
+  }
+}
+
+cudaError_t launch_combine(const Plan& p, const float* topk_w, void* y, void* ws,
+                           cudaStream_t st) {
+  CombineArgs a;
+  char* w = static_cast<char*>(ws);
+  a.o = reinterpret_cast<const float*>(w + p.ws.o);
+  a.os = p.cfg.n_shared ? reinterpret_cast<const float*>(w + p.ws.os) : nullptr;
+  a.key_row = reinterpret_cast<const int*>(w + p.ws.key_row);
+  a.topk_w = topk_w;
+  a.y = y;
+  a.T = p.cfg.T;
+  a.d = p.cfg.d;
+  a.k = p.cfg.k;
+  if (p.cfg.dtype == MOE_BF16)
+    combine_kernel<__nv_bfloat16><<<p.cfg.T, kThreads, 0, st>>>(a);
+  else
+    combine_kernel<float><<<p.cfg.T, kThreads, 0, st>>>(a);
+  return cudaGetLastError();
+}
+
+}  // namespace moe

@@ -1,0 +1,556 @@
+// gemm_tc.cu -- stage 5 on the bf16 path: the expert MLPs as grouped GEMMs
+// over ragged expert segments on the 5th-generation tensor cores.
+//
+// Expert forms: "Mixture of Experts" (llm-tutorial ch. 11) § The mathematics
+// (W2 act(W1 x): GELU in most production models, ReLU in the demo, no biases)
+// and § Active vs total parameters (SwiGLU: gate W1, up W3, down W2).  Only
+// chosen experts run: FLOPs per token scale with k (ch. 11 § The mathematics;
+// "Mixture-of-Experts" (neural networks visually) § Show the math).  The shared
+// expert of "Mixture of experts" (inside-the-model guide) § Fine-grained and
+// shared experts is one more segment of the same launch, reading x directly.
+//
+// Kernel shape (one CTA per SM, persistent over work items):
+//   warp 0    TMA producer: A tile (128 rows x 64 K) + B tile(s) (N rows x 64 K)
+//             per stage, 128-byte swizzle, completion on a transaction barrier;
+//   warp 1    allocates tensor memory; lane 0 issues tcgen05.mma (M=128,
+//             N=MMA_N, K=16) into one of two TMEM accumulators and commits
+//             stage releases and accumulator-ready signals;
+//   warps 2-5 epilogue: tcgen05.ld of the accumulator rows (one TMEM lane per
+//             thread), activation (SwiGLU: silu(gate) * up from the two halves
+//             of one N=2*BNH accumulator), bf16 or fp32 stores.
+// Work items are (segment, M tile, N tile) read from a device tile prefix
+// written by the scan kernel, N tiles outermost inside a segment so the CTAs
+// that run together share the weight tile through L2.  Expert segments start
+// on 128-row boundaries, so an M tile never mixes experts.
+//
+// Every wait is bounded: on a timeout the kernel records a status bit, tells
+// the other roles to stop, drains its own copies and MMAs, frees tensor
+// memory and returns.
+#include <cstdio>
+#include <mutex>
+
+#include "common.cuh"
+#include "moe_internal.h"
+#include "ptx.cuh"
+
+namespace moe {
+
+enum { EPI_SWIGLU = 0, EPI_GELU = 1, EPI_RELU = 2, EPI_F32 = 3 };
+
+struct TcArgs {
+  const int* tp;          // [E+2] tile prefix: routed segments, then the shared one
+  const int* seg_start;   // [E] first row of each routed segment
+  const int* mtiles;      // [E+1] M tiles per segment (index E: shared)
+  int E, has_shared;
+  int N, K;               // routed output columns / reduction length
+  int N_sh, K_sh;         // shared segment
+  void* out;              // routed output rows [R_cap][ld_out]
+  int ld_out;
+  void* out_sh;           // shared output rows [T_pad][ld_out_sh]
+  int ld_out_sh;
+  uint32_t* status;
+  uint64_t timeout_ns;
+};
+
+constexpr __host__ __device__ int pow2_at_least(int v) {
+  int p = 32;
+  while (p < v) p <<= 1;
+  return p;
+}
+
+template <int BNH, bool DUAL, int EPI>
+struct TcCfg {
+  static constexpr int BM = kTcBM;
+  static constexpr int BK = 64;
+  static constexpr int MMA_N = DUAL ? 2 * BNH : BNH;
+  static_assert(MMA_N % 16 == 0 && MMA_N >= 16 && MMA_N <= 256, "tcgen05 N for M=128");
+  static_assert(BNH % 32 == 0, "epilogue walks 32-column chunks");
+  static constexpr int A_BYTES = BM * BK * 2;
+  static constexpr int B_BYTES = MMA_N * BK * 2;
+  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+  static constexpr int STAGES_FIT = (200 * 1024) / STAGE_BYTES;
+  static constexpr int STAGES = STAGES_FIT > 8 ? 8 : STAGES_FIT;
+  static constexpr int TMEM_COLS = pow2_at_least(2 * MMA_N);
+  static_assert(TMEM_COLS <= 512, "two accumulators must fit in tensor memory");
+  static constexpr int BAR_BYTES = 8 * (2 * STAGES + 5) + 16;
+  static constexpr int SMEM = 1024 + STAGES * STAGE_BYTES + BAR_BYTES;
+  static constexpr uint32_t IDESC = idesc_bf16_f32(BM, MMA_N);
+};
+
+struct TileInfo {
+  int seg;
+  bool shared;
+  int a_row;    // first A row (and output row)
+  int n0;       // first output column
+  int K, N;
+};
+
+__device__ __forceinline__ TileInfo decode_tile(const TcArgs& a, int tile, int bnh) {
+  const int nseg = a.E + a.has_shared;
+  int lo = 0, hi = nseg - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (__ldg(a.tp + mid) <= tile) lo = mid; else hi = mid - 1;
+  }
+  TileInfo ti;
+  ti.seg = lo;
+  ti.shared = lo >= a.E;
+  const int local = tile - __ldg(a.tp + lo);
+  const int mt = __ldg(a.mtiles + lo);
+  const int n_t = local / mt, m_t = local - n_t * mt;
+  ti.a_row = (ti.shared ? 0 : __ldg(a.seg_start + lo)) + m_t * kTcBM;
+  ti.n0 = n_t * bnh;
+  ti.K = ti.shared ? a.K_sh : a.K;
+  ti.N = ti.shared ? a.N_sh : a.N;
+  return ti;
+}
+
+__device__ __forceinline__ float silu_mul(float g, float u) {
+  return g / (1.0f + __expf(-g)) * u;
+}
+
+template <int BNH, bool DUAL, int EPI>
+__global__ void __launch_bounds__(192, 1)
+tc_grouped_gemm(const __grid_constant__ CUtensorMap mA, const __grid_constant__ CUtensorMap mA_sh,
+                const __grid_constant__ CUtensorMap mB0, const __grid_constant__ CUtensorMap mB1,
+                const __grid_constant__ CUtensorMap mB0_sh,
+                const __grid_constant__ CUtensorMap mB1_sh, const TcArgs a) {
+  using C = TcCfg<BNH, DUAL, EPI>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::STAGES * C::STAGE_BYTES);
+  const uint32_t bar0 = smem_u32(bars);
+  auto full_bar = [&](int s) { return bar0 + 8u * s; };
+  auto empty_bar = [&](int s) { return bar0 + 8u * (C::STAGES + s); };
+  auto tfull_bar = [&](int b) { return bar0 + 8u * (2 * C::STAGES + b); };
+  auto tempty_bar = [&](int b) { return bar0 + 8u * (2 * C::STAGES + 2 + b); };
+  const uint32_t drain_bar = bar0 + 8u * (2 * C::STAGES + 4);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * C::STAGES + 5);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  const uint32_t smem_base = smem_u32(smem);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < C::STAGES; ++s) {
+      mbar_init(full_bar(s), 1);
+      mbar_init(empty_bar(s), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(tfull_bar(b), 1);
+      mbar_init(tempty_bar(b), 128);
+    }
+    mbar_init(drain_bar, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&mA);
+    tma_prefetch_desc(&mB0);
+    if (DUAL) tma_prefetch_desc(&mB1);
+    if (a.has_shared) {
+      tma_prefetch_desc(&mA_sh);
+      tma_prefetch_desc(&mB0_sh);
+      if (DUAL) tma_prefetch_desc(&mB1_sh);
+    }
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_slot), C::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  const int total = __ldg(a.tp + a.E + a.has_shared);
+
+  auto give_up = [&]() {
+    atomicOr(a.status, STATUS_TIMEOUT_GEMM);
+    *abort_flag = 1;
+  };
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ---------------- TMA producer ----------------
+      uint32_t g = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
+        const TileInfo ti = decode_tile(a, tile, BNH);
+        const CUtensorMap* pA = ti.shared ? &mA_sh : &mA;
+        const CUtensorMap* pB0 = ti.shared ? &mB0_sh : &mB0;
+        const CUtensorMap* pB1 = ti.shared ? &mB1_sh : &mB1;
+        const int e = ti.shared ? 0 : ti.seg;
+        const int nk = (ti.K + C::BK - 1) / C::BK;
+        for (int kb = 0; kb < nk; ++kb, ++g) {
+          const int s = g % C::STAGES;
+          const uint32_t ph = (g / C::STAGES) & 1u;
+          if (!mbar_wait_bounded(empty_bar(s), ph ^ 1u, a.timeout_ns, abort_flag)) {
+            give_up();
+            ok = false;
+            break;
+          }
+          const uint32_t sa = smem_base + s * C::STAGE_BYTES;
+          const uint32_t sb = sa + C::A_BYTES;
+          mbar_arrive_expect_tx(full_bar(s), C::STAGE_BYTES);
+          tma_load_2d(sa, pA, full_bar(s), kb * C::BK, ti.a_row);
+          tma_load_3d(sb, pB0, full_bar(s), kb * C::BK, ti.n0, e);
+          if (DUAL) tma_load_3d(sb + BNH * 128, pB1, full_bar(s), kb * C::BK, ti.n0, e);
+        }
+      }
+      // Tail: on the normal path wait until the MMA warp has released every
+      // stage (its last commits have landed); after a give-up, wait until
+      // every copy already issued has landed.  Either way nothing asynchronous
+      // still targets this block's shared memory when it exits.
+      for (int s = 0; s < C::STAGES; ++s) {
+        if (g > static_cast<uint32_t>(s)) {
+          const uint32_t issues = (g - 1 - s) / C::STAGES + 1;
+          if (ok)
+            mbar_wait_bounded(empty_bar(s), (issues - 1) & 1u, a.timeout_ns, abort_flag);
+          else
+            mbar_wait_bounded(full_bar(s), (issues - 1) & 1u, a.timeout_ns, nullptr);
+        }
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ---------------- MMA issuer ----------------
+      uint32_t g = 0;
+      int it = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x, ++it) {
+        const TileInfo ti = decode_tile(a, tile, BNH);
+        const int ab = it & 1;
+        const uint32_t aph = (it >> 1) & 1;
+        if (!mbar_wait_bounded(tempty_bar(ab), aph ^ 1u, a.timeout_ns, abort_flag)) {
+          give_up();
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + ab * C::MMA_N;
+        const int nk = (ti.K + C::BK - 1) / C::BK;
+        for (int kb = 0; kb < nk; ++kb, ++g) {
+          const int s = g % C::STAGES;
+          const uint32_t ph = (g / C::STAGES) & 1u;
+          if (!mbar_wait_bounded(full_bar(s), ph, a.timeout_ns, abort_flag)) {
+            give_up();
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t sa = smem_base + s * C::STAGE_BYTES;
+          const uint32_t sb = sa + C::A_BYTES;
+#pragma unroll
+          for (int kk = 0; kk < C::BK / 16; ++kk) {
+            const uint64_t ad = smem_desc_k128(sa + kk * 32);
+            const uint64_t bd = smem_desc_k128(sb + kk * 32);
+            tc_mma_bf16(d_tmem, ad, bd, C::IDESC, (kb | kk) != 0 ? 1u : 0u);
+          }
+          tc_commit(empty_bar(s));
+        }
+        if (!ok) break;
+        tc_commit(tfull_bar(ab));
+      }
+      if (!ok) {
+        tc_commit(drain_bar);
+        mbar_wait_bounded(drain_bar, 0, a.timeout_ns, nullptr);
+      }
+    }
+  } else {
+    // ---------------- epilogue (warps 2..5) ----------------
+    const int q = warp & 3;                  // TMEM lane quarter this warp may read
+    const int row_in_tile = q * 32 + lane;
+    int it = 0;
+    for (int tile = blockIdx.x; tile < total; tile += gridDim.x, ++it) {
+      const TileInfo ti = decode_tile(a, tile, BNH);
+      const int ab = it & 1;
+      const uint32_t aph = (it >> 1) & 1;
+      if (!mbar_wait_bounded(tfull_bar(ab), aph, a.timeout_ns, abort_flag)) {
+        give_up();
+        break;
+      }
+      tc_fence_after();
+      const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + ab * C::MMA_N;
+      const size_t orow = static_cast<size_t>(ti.a_row + row_in_tile);
+#pragma unroll 1
+      for (int c = 0; c < BNH; c += 32) {
+        uint32_t r0[32];
+        tmem_ld32(t_row + c, r0);
+        uint32_t r1[32];
+        if (DUAL) tmem_ld32(t_row + BNH + c, r1);
+        tmem_ld_wait();
+        const int col = ti.n0 + c;
+        if (EPI == EPI_F32) {
+          float* out = static_cast<float*>(ti.shared ? a.out_sh : a.out);
+          const int ld = ti.shared ? a.ld_out_sh : a.ld_out;
+          float* dst = out + orow * ld + col;
+          if (col + 32 <= ti.N) {
+#pragma unroll
+            for (int v = 0; v < 8; ++v) {
+              float4 f4 = make_float4(__uint_as_float(r0[4 * v]), __uint_as_float(r0[4 * v + 1]),
+                                      __uint_as_float(r0[4 * v + 2]),
+                                      __uint_as_float(r0[4 * v + 3]));
+              reinterpret_cast<float4*>(dst)[v] = f4;
+            }
+          } else {
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+              if (col + i < ti.N) dst[i] = __uint_as_float(r0[i]);
+          }
+        } else {
+          __nv_bfloat16* out = static_cast<__nv_bfloat16*>(ti.shared ? a.out_sh : a.out);
+          const int ld = ti.shared ? a.ld_out_sh : a.ld_out;
+          __nv_bfloat16* dst = out + orow * ld + col;
+          uint32_t pk[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            float v0 = __uint_as_float(r0[2 * i]), v1 = __uint_as_float(r0[2 * i + 1]);
+            if (EPI == EPI_SWIGLU) {
+              v0 = silu_mul(v0, __uint_as_float(r1[2 * i]));
+              v1 = silu_mul(v1, __uint_as_float(r1[2 * i + 1]));
+            } else if (EPI == EPI_RELU) {
+              v0 = fmaxf(v0, 0.f);
+              v1 = fmaxf(v1, 0.f);
+            } else if (EPI == EPI_GELU) {
+              v0 = 0.5f * v0 * (1.0f + erff(v0 * 0.70710678118654752f));
+              v1 = 0.5f * v1 * (1.0f + erff(v1 * 0.70710678118654752f));
+            }
+            __nv_bfloat162 b2 = __floats2bfloat162_rn(v0, v1);
+            pk[i] = *reinterpret_cast<uint32_t*>(&b2);
+          }
+          if (col + 32 <= ti.N) {
+#pragma unroll
+            for (int v = 0; v < 4; ++v)
+              reinterpret_cast<uint4*>(dst)[v] =
+                  make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
+          } else {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+              if (col + i < ti.N) {
+                const uint32_t w = pk[i >> 1];
+                reinterpret_cast<uint16_t*>(dst)[i] =
+                    (i & 1) ? static_cast<uint16_t>(w >> 16) : static_cast<uint16_t>(w);
+              }
+            }
+          }
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(tempty_bar(ab));
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, C::TMEM_COLS);
+  }
+}
+
+// ---------------------------------------------------------------- host side
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+static EncodeTiledFn get_encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, []() {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+// 2-D map over a row-major [rows][cols] bf16 matrix, box 64 cols x box_rows.
+static bool encode_2d(CUtensorMap* m, const void* ptr, uint64_t rows, uint64_t cols,
+                      uint32_t box_rows) {
+  EncodeTiledFn fn = get_encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {cols * 2};
+  cuuint32_t box[2] = {64, box_rows};
+  cuuint32_t es[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box,
+            es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// 3-D map over [n_mat][rows][cols] bf16, box 64 cols x box_rows x 1.
+static bool encode_3d(CUtensorMap* m, const void* ptr, uint64_t n_mat, uint64_t rows,
+                      uint64_t cols, uint32_t box_rows) {
+  EncodeTiledFn fn = get_encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[3] = {cols, rows, n_mat};
+  cuuint64_t strides[2] = {cols * 2, rows * cols * 2};
+  cuuint32_t box[3] = {64, box_rows, 1};
+  cuuint32_t es[3] = {1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides, box,
+            es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+struct TcMaps {
+  CUtensorMap A, A_sh, B0, B1, B0_sh, B1_sh;
+};
+
+template <int BNH, bool DUAL, int EPI>
+static cudaError_t run_tc(const TcMaps& m, const TcArgs& a, int grid, cudaStream_t st) {
+  using C = TcCfg<BNH, DUAL, EPI>;
+  auto kern = tc_grouped_gemm<BNH, DUAL, EPI>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+  if (e != cudaSuccess) return e;
+  kern<<<grid, 192, C::SMEM, st>>>(m.A, m.A_sh, m.B0, m.B1, m.B0_sh, m.B1_sh, a);
+  return cudaGetLastError();
+}
+
+static cudaError_t dispatch_up(int bn, int act, const TcMaps& m, const TcArgs& a, int grid,
+                               cudaStream_t st) {
+  if (act == MOE_ACT_SWIGLU) {
+    switch (bn) {
+      case 128: return run_tc<128, true, EPI_SWIGLU>(m, a, grid, st);
+      case 96: return run_tc<96, true, EPI_SWIGLU>(m, a, grid, st);
+      case 64: return run_tc<64, true, EPI_SWIGLU>(m, a, grid, st);
+      case 32: return run_tc<32, true, EPI_SWIGLU>(m, a, grid, st);
+    }
+  } else if (act == MOE_ACT_RELU) {
+    switch (bn) {
+      case 256: return run_tc<256, false, EPI_RELU>(m, a, grid, st);
+      case 128: return run_tc<128, false, EPI_RELU>(m, a, grid, st);
+      case 96: return run_tc<96, false, EPI_RELU>(m, a, grid, st);
+      case 64: return run_tc<64, false, EPI_RELU>(m, a, grid, st);
+    }
+  } else {
+    switch (bn) {
+      case 256: return run_tc<256, false, EPI_GELU>(m, a, grid, st);
+      case 128: return run_tc<128, false, EPI_GELU>(m, a, grid, st);
+      case 96: return run_tc<96, false, EPI_GELU>(m, a, grid, st);
+      case 64: return run_tc<64, false, EPI_GELU>(m, a, grid, st);
+    }
+  }
+  return cudaErrorInvalidValue;
+}
+
+static cudaError_t dispatch_down(int bn, const TcMaps& m, const TcArgs& a, int grid,
+                                 cudaStream_t st) {
+  switch (bn) {
+    case 256: return run_tc<256, false, EPI_F32>(m, a, grid, st);
+    case 192: return run_tc<192, false, EPI_F32>(m, a, grid, st);
+    case 128: return run_tc<128, false, EPI_F32>(m, a, grid, st);
+    case 96: return run_tc<96, false, EPI_F32>(m, a, grid, st);
+    case 64: return run_tc<64, false, EPI_F32>(m, a, grid, st);
+  }
+  return cudaErrorInvalidValue;
+}
+
+constexpr uint64_t kGemmTimeoutNs = 2000000000ull;   // 2 s
+
+cudaError_t launch_experts_tc(const Plan& p, const void* x, const void* W1, const void* W3,
+                              const void* W2, const void* Ws1, const void* Ws3, const void* Ws2,
+                              void* ws, cudaStream_t st, cudaEvent_t mid_event) {
+  const moe_config& c = p.cfg;
+  char* w = static_cast<char*>(ws);
+  const Meta meta = meta_ptrs(p, ws);
+  const bool sh = c.n_shared != 0;
+  const bool dual = c.act == MOE_ACT_SWIGLU;
+  uint32_t* status = reinterpret_cast<uint32_t*>(w + p.ws.status);
+  const void* xp = w + p.ws.xp;
+  const void* h = w + p.ws.h;
+  const void* hs = sh ? static_cast<const void*>(w + p.ws.hs) : h;
+
+  // ---- up projection: h = act(xp W1^T) or silu(xp W1^T) * (xp W3^T) ----
+  TcMaps mu;
+  bool ok = encode_2d(&mu.A, xp, p.R_cap, c.d, kTcBM);
+  ok = ok && encode_3d(&mu.B0, W1, c.E, c.f, c.d, p.up_bn);
+  ok = ok && encode_3d(&mu.B1, dual ? W3 : W1, c.E, c.f, c.d, p.up_bn);
+  if (sh) {
+    ok = ok && encode_2d(&mu.A_sh, x, c.T, c.d, kTcBM);
+    ok = ok && encode_3d(&mu.B0_sh, Ws1, 1, c.f_shared, c.d, p.up_bn);
+    ok = ok && encode_3d(&mu.B1_sh, Ws3, 1, c.f_shared, c.d, p.up_bn);
+  } else {
+    mu.A_sh = mu.A;
+    mu.B0_sh = mu.B0;
+    mu.B1_sh = mu.B1;
+  }
+  if (!ok) return cudaErrorInvalidValue;
+  TcArgs au;
+  au.tp = meta.tp_up;
+  au.seg_start = meta.seg_start;
+  au.mtiles = meta.mtiles;
+  au.E = c.E;
+  au.has_shared = sh ? 1 : 0;
+  au.N = c.f;
+  au.K = c.d;
+  au.N_sh = sh ? c.f_shared : 0;
+  au.K_sh = c.d;
+  au.out = w + p.ws.h;
+  au.ld_out = c.f;
+  au.out_sh = sh ? static_cast<void*>(w + p.ws.hs) : nullptr;
+  au.ld_out_sh = sh ? c.f_shared : 0;
+  au.status = status;
+  au.timeout_ns = kGemmTimeoutNs;
+  const int grid_up = p.max_tiles_up < p.num_sms ? p.max_tiles_up : p.num_sms;
+  cudaError_t e = dispatch_up(p.up_bn, c.act, mu, au, grid_up, st);
+  if (e != cudaSuccess) return e;
+  if (mid_event) {
+    e = cudaEventRecord(mid_event, st);
+    if (e != cudaSuccess) return e;
+  }
+
+  // ---- down projection: o = h W2^T (fp32) ----
+  TcMaps md;
+  ok = encode_2d(&md.A, h, p.R_cap, c.f, kTcBM);
+  ok = ok && encode_3d(&md.B0, W2, c.E, c.d, c.f, p.dn_bn);
+  md.B1 = md.B0;
+  if (sh) {
+    ok = ok && encode_2d(&md.A_sh, hs, p.T_pad, c.f_shared, kTcBM);
+    ok = ok && encode_3d(&md.B0_sh, Ws2, 1, c.d, c.f_shared, p.dn_bn);
+  } else {
+    md.A_sh = md.A;
+    md.B0_sh = md.B0;
+  }
+  md.B1_sh = md.B0_sh;
+  if (!ok) return cudaErrorInvalidValue;
+  TcArgs ad = au;
+  ad.tp = meta.tp_dn;
+  ad.N = c.d;
+  ad.K = c.f;
+  ad.N_sh = sh ? c.d : 0;
+  ad.K_sh = sh ? c.f_shared : 0;
+  ad.out = w + p.ws.o;
+  ad.ld_out = c.d;
+  ad.out_sh = sh ? static_cast<void*>(w + p.ws.os) : nullptr;
+  ad.ld_out_sh = sh ? c.d : 0;
+  const int grid_dn = p.max_tiles_dn < p.num_sms ? p.max_tiles_dn : p.num_sms;
+  return dispatch_down(p.dn_bn, md, ad, grid_dn, st);
+}
+
+// ---------------------------------------------------------------- self-test
+// One block waits on a barrier that nothing completes; the bounded wait gives
+// up after wait_ns, records the timeout bit and the block returns normally.
+__global__ void selftest_wait_kernel(uint32_t* status, uint64_t wait_ns) {
+  __shared__ __align__(8) uint64_t bar;
+  if (threadIdx.x == 0) {
+    mbar_init(smem_u32(&bar), 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    if (!mbar_wait_bounded(smem_u32(&bar), 0, wait_ns, nullptr))
+      atomicOr(status, STATUS_TIMEOUT_SELFTEST);
+  }
+}
+
+cudaError_t launch_selftest_wait(uint32_t* status, uint64_t wait_ns, cudaStream_t st) {
+  selftest_wait_kernel<<<1, 32, 0, st>>>(status, wait_ns);
+  return cudaGetLastError();
+}
+
+}  // namespace moe

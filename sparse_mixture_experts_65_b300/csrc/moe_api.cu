@@ -1,0 +1,415 @@
+// moe_api.cu -- the C ABI declared in include/moe.h: argument checks, the
+// per-call plan (workspace layout, routing blocks, GEMM tiling) and the
+// enqueueing of the stage kernels on the caller's stream.
+#include <climits>
+#include <cmath>
+#include <cstdlib>
+#include <cstring>
+
+#include "moe_internal.h"
+
+namespace moe {
+
+static size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+static int ceil_div(long long a, long long b) { return static_cast<int>((a + b - 1) / b); }
+
+// Output columns per tile: minimise (waves of tiles over the SMs) x (tile
+// width + a fixed per-tile cost); ties go to the wider tile.
+static int choose_bn(const int* cands, int ncand, int N, long long est_mtiles, long long extra_m,
+                     int N_extra, int num_sms) {
+  int best = cands[0];
+  long long best_cost = LLONG_MAX;
+  for (int i = 0; i < ncand; ++i) {
+    const int bn = cands[i];
+    const long long tiles = est_mtiles * ceil_div(N, bn) + extra_m * ceil_div(N_extra, bn);
+    const long long waves = (tiles + num_sms - 1) / num_sms;
+    const long long cost = waves * (bn + 16);
+    if (cost < best_cost) {
+      best_cost = cost;
+      best = bn;
+    }
+  }
+  return best;
+}
+
+int make_plan(const moe_config* cfg, WsKind kind, Plan* p, int num_sms);
+
+static int env_int(const char* name) {
+  const char* v = std::getenv(name);
+  return v ? std::atoi(v) : 0;
+}
+
+int make_plan(const moe_config* cfg, WsKind kind, Plan* p) { return make_plan(cfg, kind, p, 0); }
+
+int make_plan(const moe_config* cfg, WsKind kind, Plan* p, int num_sms) {
+  if (!cfg || !p) return MOE_ERR_ARG;
+  const moe_config& c = *cfg;
+  if (c.reserved != 0 || c.T < 0 || c.d < 1 || c.E < 1 || c.k < 1 || c.k > c.E || c.f < 1)
+    return MOE_ERR_ARG;
+  if (c.n_shared != 0 && c.n_shared != 1) return MOE_ERR_ARG;
+  if (c.n_shared == 1 && c.f_shared < 1) return MOE_ERR_ARG;
+  if (c.dtype != MOE_F32 && c.dtype != MOE_BF16) return MOE_ERR_ARG;
+  if (c.act < MOE_ACT_GELU || c.act > MOE_ACT_SWIGLU) return MOE_ERR_ARG;
+  if (c.gate < MOE_GATE_SOFTMAX_TOPK || c.gate > MOE_GATE_SOFTMAX_FULL) return MOE_ERR_ARG;
+  if (!std::isfinite(c.capacity_factor) || !std::isfinite(c.alpha)) return MOE_ERR_ARG;
+  if (c.E > kMaxE || c.k > kMaxK) return MOE_ERR_UNSUPPORTED;
+  const int vec = c.dtype == MOE_BF16 ? 8 : 4;
+  if (c.d % vec || c.f % vec || (c.n_shared && c.f_shared % vec)) return MOE_ERR_UNSUPPORTED;
+  // every row index and element count of one matrix must fit in int32 / the TMA limits
+  const long long Tk = (long long)c.T * c.k;
+  if (Tk > (1LL << 30) || (long long)c.T * c.d > (1LL << 40)) return MOE_ERR_UNSUPPORTED;
+
+  Plan& P = *p;
+  std::memset(&P, 0, sizeof(P));
+  P.cfg = c;
+  P.elem = c.dtype == MOE_BF16 ? 2 : 4;
+  if (c.capacity_factor > 0) {
+    const double cap = std::ceil(static_cast<double>(Tk) * c.capacity_factor / c.E);
+    P.capacity = cap >= (double)INT_MAX ? INT_MAX : static_cast<int>(cap);
+  } else {
+    P.capacity = INT_MAX;
+  }
+  P.E_pad = c.E <= 32 ? 32 : c.E <= 64 ? 64 : c.E <= 128 ? 128 : c.E <= 256 ? 256 : 512;
+  const int EC = P.E_pad < 256 ? P.E_pad : 256;
+  P.BT = (kThreads / EC) * kRouterRT;
+  P.KC = P.E_pad > 256 ? 16 : 32;
+  P.nblk = ceil_div(c.T, P.BT);
+  P.tc = c.dtype == MOE_BF16;
+  P.bm = P.tc ? kTcBM : kSimtBM;
+  const long long nonempty = Tk < c.E ? Tk : c.E;
+  P.R_cap = static_cast<int>(align_up((size_t)(Tk + nonempty * (P.bm - 1)), (size_t)P.bm));
+  P.T_pad = static_cast<int>(align_up((size_t)c.T, (size_t)kSegAlign));
+  P.mt_sh = c.n_shared ? ceil_div(c.T, P.bm) : 0;
+  P.num_sms = num_sms > 0 ? num_sms : 148;
+
+  if (P.tc) {
+    long long est = nonempty + Tk / P.bm;
+    if (P.capacity != INT_MAX) {
+      const long long capb = (long long)c.E * ceil_div(P.capacity, P.bm);
+      if (capb < est) est = capb;
+    }
+    static const int dual_c[] = {128, 96, 64, 32};
+    static const int single_c[] = {256, 128, 96, 64};
+    static const int down_c[] = {256, 192, 128, 96, 64};
+    if (c.act == MOE_ACT_SWIGLU)
+      P.up_bn = choose_bn(dual_c, 4, c.f, est, P.mt_sh, c.f_shared, P.num_sms);
+    else
+      P.up_bn = choose_bn(single_c, 4, c.f, est, P.mt_sh, c.f_shared, P.num_sms);
+    P.dn_bn = choose_bn(down_c, 5, c.d, est, P.mt_sh, c.d, P.num_sms);
+    // Tuning override (tile sweeps and tests): MOE_TILE_N_UP / MOE_TILE_N_DOWN
+    // select one of the compiled tile widths; other values are ignored.
+    const int up_env = env_int("MOE_TILE_N_UP"), dn_env = env_int("MOE_TILE_N_DOWN");
+    const int* up_list = c.act == MOE_ACT_SWIGLU ? dual_c : single_c;
+    for (int i = 0; i < 4; ++i)
+      if (up_env == up_list[i]) P.up_bn = up_env;
+    for (int i = 0; i < 5; ++i)
+      if (dn_env == down_c[i]) P.dn_bn = dn_env;
+  } else {
+    P.up_bn = kSimtBN;
+    P.dn_bn = kSimtBN;
+  }
+  P.nt_up = ceil_div(c.f, P.up_bn);
+  P.nt_dn = ceil_div(c.d, P.dn_bn);
+  P.nt_up_sh = c.n_shared ? ceil_div(c.f_shared, P.up_bn) : 0;
+  P.nt_dn_sh = c.n_shared ? ceil_div(c.d, P.dn_bn) : 0;
+  P.max_tiles_up = (P.R_cap / P.bm) * P.nt_up + P.mt_sh * P.nt_up_sh;
+  P.max_tiles_dn = (P.R_cap / P.bm) * P.nt_dn + P.mt_sh * P.nt_dn_sh;
+
+  // ---- workspace layout ----
+  WsLayout& L = P.ws;
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    const size_t at = off;
+    off = align_up(off + bytes, 256);
+    return at;
+  };
+  const size_t E = c.E;
+  L.status = take(256);
+  L.blk_cnt = take(sizeof(int) * (size_t)P.nblk * E);
+  L.blk_prob = take(sizeof(float) * (size_t)P.nblk * E);
+  L.meta = take(sizeof(int) * (E + (E + 1) * 3 + (E + 2) * 2));
+  L.key_row = take(sizeof(int) * (size_t)Tk);
+  if (kind != WsKind::Route) {
+    const size_t act_elem = P.elem;   // h is bf16 on the tensor-core path, fp32 otherwise
+    L.xp = take((size_t)P.R_cap * c.d * P.elem);
+    L.h = take((size_t)P.R_cap * c.f * act_elem);
+    L.o = take((size_t)P.R_cap * c.d * sizeof(float));
+    if (c.n_shared) {
+      L.hs = take((size_t)P.T_pad * c.f_shared * act_elem);
+      L.os = take((size_t)P.T_pad * c.d * sizeof(float));
+    }
+  }
+  if (kind == WsKind::HostIO) {
+    L.x_dev = take((size_t)c.T * c.d * P.elem);
+    L.y_dev = take((size_t)c.T * c.d * P.elem);
+    L.topk_idx = take(sizeof(int) * (size_t)Tk);
+    L.topk_w = take(sizeof(float) * (size_t)Tk);
+    L.counts = take(sizeof(int) * E);
+    L.aux = take(sizeof(float));
+  }
+  L.total = off;
+  return MOE_OK;
+}
+
+static int device_sms(int* sms) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return MOE_ERR_CUDA;
+  int major = 0, minor = 0;
+  if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  if (major != 10 || minor != 3) return MOE_ERR_DEVICE;
+  return MOE_OK;
+}
+
+static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+static bool aligned4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
+
+struct Tensors {
+  const void *x, *W_r;
+  const float *logit_offset, *sel_bias;
+  const void *W1, *W3, *W2, *Ws1, *Ws3, *Ws2;
+  void* y;
+  int32_t* topk_idx;
+  float* topk_w;
+  int32_t* expert_counts;
+  float* aux_loss;
+  int32_t *routed_counts, *offsets, *slot_pos;
+  float *f_out, *P_out;
+};
+
+static int check_tensors(const moe_config& c, const Tensors& t, bool route_only) {
+  // With T = 0 the per-token tensors are empty and may be NULL.
+  const bool empty = c.T == 0;
+  if (!t.W_r || !t.expert_counts || !t.aux_loss) return MOE_ERR_ARG;
+  if (!empty && (!t.x || !t.topk_idx || !t.topk_w)) return MOE_ERR_ARG;
+  if (!aligned16(t.x) || !aligned4(t.W_r) || !aligned4(t.topk_idx) || !aligned4(t.topk_w))
+    return MOE_ERR_ARG;
+  if (route_only) return MOE_OK;
+  if (!t.W1 || !t.W2 || (!empty && !t.y)) return MOE_ERR_ARG;
+  if (!aligned16(t.W1) || !aligned16(t.W2) || !aligned16(t.y)) return MOE_ERR_ARG;
+  if (c.act == MOE_ACT_SWIGLU ? (!t.W3 || !aligned16(t.W3)) : t.W3 != nullptr) return MOE_ERR_ARG;
+  if (c.n_shared) {
+    if (!t.Ws1 || !t.Ws3 || !t.Ws2) return MOE_ERR_ARG;
+    if (!aligned16(t.Ws1) || !aligned16(t.Ws3) || !aligned16(t.Ws2)) return MOE_ERR_ARG;
+  } else if (t.Ws1 || t.Ws3 || t.Ws2) {
+    return MOE_ERR_ARG;
+  }
+  return MOE_OK;
+}
+
+static int check_workspace(const Plan& p, const void* ws, size_t bytes) {
+  if (!ws || (reinterpret_cast<uintptr_t>(ws) & 255u) != 0 || bytes < p.ws.total)
+    return MOE_ERR_WORKSPACE;
+  return MOE_OK;
+}
+
+#define MOE_TRY_CUDA(expr)                       \
+  do {                                           \
+    if ((expr) != cudaSuccess) return MOE_ERR_CUDA; \
+  } while (0)
+
+static int zero_outputs(const moe_config& c, const Tensors& t, cudaStream_t st) {
+  const size_t E = c.E;
+  MOE_TRY_CUDA(cudaMemsetAsync(t.expert_counts, 0, E * sizeof(int32_t), st));
+  MOE_TRY_CUDA(cudaMemsetAsync(t.aux_loss, 0, sizeof(float), st));
+  if (t.routed_counts) MOE_TRY_CUDA(cudaMemsetAsync(t.routed_counts, 0, E * sizeof(int32_t), st));
+  if (t.offsets) MOE_TRY_CUDA(cudaMemsetAsync(t.offsets, 0, (E + 1) * sizeof(int32_t), st));
+  if (t.f_out) MOE_TRY_CUDA(cudaMemsetAsync(t.f_out, 0, E * sizeof(float), st));
+  if (t.P_out) MOE_TRY_CUDA(cudaMemsetAsync(t.P_out, 0, E * sizeof(float), st));
+  return MOE_OK;
+}
+
+static int record(void* const* events, int i, cudaStream_t st) {
+  if (events && events[i])
+    MOE_TRY_CUDA(cudaEventRecord(static_cast<cudaEvent_t>(events[i]), st));
+  return MOE_OK;
+}
+
+static int forward_impl(const moe_config* cfg, const Tensors& t, void* ws, size_t ws_bytes,
+                        cudaStream_t st, void* const* events, bool route_only, WsKind kind) {
+  if (!cfg) return MOE_ERR_ARG;
+  Plan p;
+  int rc = make_plan(cfg, kind, &p, 0);
+  if (rc != MOE_OK) return rc;
+  rc = check_tensors(*cfg, t, route_only);
+  if (rc != MOE_OK) return rc;
+  rc = check_workspace(p, ws, ws_bytes);
+  if (rc != MOE_OK) return rc;
+  int sms = 0;
+  rc = device_sms(&sms);
+  if (rc != MOE_OK) return rc;
+  rc = make_plan(cfg, kind, &p, sms);
+  if (rc != MOE_OK) return rc;
+  const moe_config& c = *cfg;
+  if (c.T == 0) return zero_outputs(c, t, st);
+
+  if ((rc = record(events, MOE_STAGE_ROUTER, st)) != MOE_OK) return rc;
+  MOE_TRY_CUDA(launch_router(p, t.x, t.W_r, t.logit_offset, t.sel_bias, t.topk_idx, t.topk_w, ws,
+                             st));
+  if ((rc = record(events, MOE_STAGE_SCAN, st)) != MOE_OK) return rc;
+  MOE_TRY_CUDA(launch_scan(p, ws, t.expert_counts, t.aux_loss, t.routed_counts, t.offsets,
+                           t.f_out, t.P_out, st));
+  if ((rc = record(events, MOE_STAGE_PERMUTE, st)) != MOE_OK) return rc;
+  MOE_TRY_CUDA(launch_permute(p, t.x, t.topk_idx, t.slot_pos, !route_only, ws, st));
+  if (route_only) return MOE_OK;
+  if ((rc = record(events, MOE_STAGE_UP, st)) != MOE_OK) return rc;
+  cudaEvent_t mid = events ? static_cast<cudaEvent_t>(events[MOE_STAGE_DOWN]) : nullptr;
+  if (p.tc)
+    MOE_TRY_CUDA(launch_experts_tc(p, t.x, t.W1, t.W3, t.W2, t.Ws1, t.Ws3, t.Ws2, ws, st, mid));
+  else
+    MOE_TRY_CUDA(launch_experts_simt(p, t.x, t.W1, t.W3, t.W2, t.Ws1, t.Ws3, t.Ws2, ws, st, mid));
+  if ((rc = record(events, MOE_STAGE_COMBINE, st)) != MOE_OK) return rc;
+  MOE_TRY_CUDA(launch_combine(p, t.topk_w, t.y, ws, st));
+  if ((rc = record(events, MOE_NUM_STAGES, st)) != MOE_OK) return rc;
+  return MOE_OK;
+}
+
+}  // namespace moe
+
+using namespace moe;
+
+extern "C" {
+
+int moe_workspace_size(const moe_config* cfg, size_t* bytes) {
+  if (!bytes) return MOE_ERR_ARG;
+  Plan p;
+  const int rc = make_plan(cfg, WsKind::Forward, &p);
+  if (rc == MOE_OK) *bytes = p.ws.total;
+  return rc;
+}
+
+int moe_route_workspace_size(const moe_config* cfg, size_t* bytes) {
+  if (!bytes) return MOE_ERR_ARG;
+  Plan p;
+  const int rc = make_plan(cfg, WsKind::Route, &p);
+  if (rc == MOE_OK) *bytes = p.ws.total;
+  return rc;
+}
+
+int moe_host_io_workspace_size(const moe_config* cfg, size_t* bytes) {
+  if (!bytes) return MOE_ERR_ARG;
+  Plan p;
+  const int rc = make_plan(cfg, WsKind::HostIO, &p);
+  if (rc == MOE_OK) *bytes = p.ws.total;
+  return rc;
+}
+
+int moe_forward_timed(const moe_config* cfg, const void* x, const void* W_r,
+                      const float* logit_offset, const float* sel_bias, const void* W1,
+                      const void* W3, const void* W2, const void* Ws1, const void* Ws3,
+                      const void* Ws2, void* y, int32_t* topk_idx, float* topk_w,
+                      int32_t* expert_counts, float* aux_loss, int32_t* routed_counts,
+                      int32_t* offsets, int32_t* slot_pos, float* f_out, float* P_out,
+                      void* workspace, size_t workspace_bytes, void* stream,
+                      void* const* events) {
+  Tensors t{x,  W_r, logit_offset, sel_bias, W1,       W3,      W2,      Ws1,      Ws3,  Ws2,
+            y,  topk_idx, topk_w, expert_counts, aux_loss, routed_counts, offsets, slot_pos,
+            f_out, P_out};
+  return forward_impl(cfg, t, workspace, workspace_bytes, static_cast<cudaStream_t>(stream),
+                      events, false, WsKind::Forward);
+}
+
+int moe_forward(const moe_config* cfg, const void* x, const void* W_r, const float* logit_offset,
+                const float* sel_bias, const void* W1, const void* W3, const void* W2,
+                const void* Ws1, const void* Ws3, const void* Ws2, void* y, int32_t* topk_idx,
+                float* topk_w, int32_t* expert_counts, float* aux_loss, int32_t* routed_counts,
+                int32_t* offsets, int32_t* slot_pos, float* f_out, float* P_out,
+                void* workspace, size_t workspace_bytes, void* stream) {
+  return moe_forward_timed(cfg, x, W_r, logit_offset, sel_bias, W1, W3, W2, Ws1, Ws3, Ws2, y,
+                           topk_idx, topk_w, expert_counts, aux_loss, routed_counts, offsets,
+                           slot_pos, f_out, P_out, workspace, workspace_bytes, stream, nullptr);
+}
+
+int moe_route(const moe_config* cfg, const void* x, const void* W_r, const float* logit_offset,
+              const float* sel_bias, int32_t* topk_idx, float* topk_w, int32_t* expert_counts,
+              float* aux_loss, int32_t* routed_counts, int32_t* offsets, int32_t* slot_pos,
+              float* f_out, float* P_out, void* workspace, size_t workspace_bytes,
+              void* stream) {
+  Tensors t{x,       W_r,     logit_offset, sel_bias, nullptr, nullptr,       nullptr,
+            nullptr, nullptr, nullptr,      nullptr,  topk_idx, topk_w,       expert_counts,
+            aux_loss, routed_counts, offsets, slot_pos, f_out,  P_out};
+  return forward_impl(cfg, t, workspace, workspace_bytes, static_cast<cudaStream_t>(stream),
+                      nullptr, true, WsKind::Route);
+}
+
+int moe_forward_host_io(const moe_config* cfg, const void* x_host, const void* W_r,
+                        const float* logit_offset, const float* sel_bias, const void* W1,
+                        const void* W3, const void* W2, const void* Ws1, const void* Ws3,
+                        const void* Ws2, void* y_host, float* aux_loss_host, void* workspace,
+                        size_t workspace_bytes, void* stream) {
+  if (!cfg || !x_host || !y_host || !aux_loss_host) return MOE_ERR_ARG;
+  Plan p;
+  int rc = make_plan(cfg, WsKind::HostIO, &p);
+  if (rc != MOE_OK) return rc;
+  rc = check_workspace(p, workspace, workspace_bytes);
+  if (rc != MOE_OK) return rc;
+  char* w = static_cast<char*>(workspace);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const size_t io_bytes = (size_t)cfg->T * cfg->d * p.elem;
+  void* x_dev = w + p.ws.x_dev;
+  void* y_dev = w + p.ws.y_dev;
+  float* aux_dev = reinterpret_cast<float*>(w + p.ws.aux);
+  Tensors t{x_dev, W_r, logit_offset, sel_bias, W1, W3, W2, Ws1, Ws3, Ws2, y_dev,
+            reinterpret_cast<int32_t*>(w + p.ws.topk_idx), reinterpret_cast<float*>(w + p.ws.topk_w),
+            reinterpret_cast<int32_t*>(w + p.ws.counts), aux_dev, nullptr, nullptr, nullptr,
+            nullptr, nullptr};
+  rc = check_tensors(*cfg, t, false);
+  if (rc != MOE_OK) return rc;
+  if (io_bytes) MOE_TRY_CUDA(cudaMemcpyAsync(x_dev, x_host, io_bytes, cudaMemcpyHostToDevice, st));
+  rc = forward_impl(cfg, t, workspace, workspace_bytes, st, nullptr, false, WsKind::HostIO);
+  if (rc != MOE_OK) return rc;
+  if (io_bytes) MOE_TRY_CUDA(cudaMemcpyAsync(y_host, y_dev, io_bytes, cudaMemcpyDeviceToHost, st));
+  MOE_TRY_CUDA(cudaMemcpyAsync(aux_loss_host, aux_dev, sizeof(float), cudaMemcpyDeviceToHost, st));
+  return MOE_OK;
+}
+
+int moe_check_status(void* workspace, void* stream) {
+  if (!workspace) return MOE_ERR_WORKSPACE;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  uint32_t status = 0;
+  if (cudaMemcpyAsync(&status, workspace, sizeof(status), cudaMemcpyDeviceToHost, st) !=
+          cudaSuccess ||
+      cudaMemsetAsync(workspace, 0, sizeof(status), st) != cudaSuccess ||
+      cudaStreamSynchronize(st) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  return status ? MOE_ERR_TIMEOUT : MOE_OK;
+}
+
+const char* moe_error_string(int code) {
+  switch (code) {
+    case MOE_OK: return "MOE_OK";
+    case MOE_ERR_ARG: return "MOE_ERR_ARG: invalid argument";
+    case MOE_ERR_UNSUPPORTED: return "MOE_ERR_UNSUPPORTED: layer shape not supported";
+    case MOE_ERR_WORKSPACE: return "MOE_ERR_WORKSPACE: workspace missing, small or misaligned";
+    case MOE_ERR_CUDA: return "MOE_ERR_CUDA: CUDA runtime error";
+    case MOE_ERR_TIMEOUT: return "MOE_ERR_TIMEOUT: a bounded device wait ran out";
+    case MOE_ERR_DEVICE: return "MOE_ERR_DEVICE: needs a compute capability 10.3 GPU";
+  }
+  return "MOE_ERR_UNKNOWN";
+}
+
+int moe_launch_count(const moe_config* cfg, int32_t* launches) {
+  if (!launches) return MOE_ERR_ARG;
+  Plan p;
+  const int rc = make_plan(cfg, WsKind::Forward, &p);
+  if (rc != MOE_OK) return rc;
+  *launches = cfg->T == 0 ? 0 : MOE_NUM_STAGES;
+  return MOE_OK;
+}
+
+int moe_selftest_wait_timeout(void* workspace, size_t workspace_bytes, uint64_t wait_ns,
+                              void* stream) {
+  if (!workspace || workspace_bytes < 256 || (reinterpret_cast<uintptr_t>(workspace) & 255u))
+    return MOE_ERR_WORKSPACE;
+  int sms = 0;
+  const int rc = device_sms(&sms);
+  if (rc != MOE_OK) return rc;
+  MOE_TRY_CUDA(launch_selftest_wait(static_cast<uint32_t*>(workspace), wait_ns,
+                                    static_cast<cudaStream_t>(stream)));
+  return MOE_OK;
+}
+
+}  // extern "C"

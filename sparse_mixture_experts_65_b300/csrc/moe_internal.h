@@ -1,0 +1,98 @@
+// moe_internal.h -- host-side plan of one layer call and the launchers of
+// the individual kernels.  Not part of the public ABI.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "../../include/moe.h"
+
+namespace moe {
+
+constexpr int kThreads = 256;        // block size of the SIMT kernels
+constexpr int kRouterRT = 8;         // tokens per thread in the router GEMM
+constexpr int kMaxE = 512;
+constexpr int kMaxK = 32;
+constexpr int kSegAlign = 128;       // expert segments start on multiples of this row
+constexpr int kTcBM = 128;           // rows per tensor-core tile
+constexpr int kSimtBM = 64;          // rows per SIMT tile (fp32 path)
+constexpr int kSimtBN = 64;
+
+// Workspace regions, all 256-byte aligned.  Offsets in bytes.
+struct WsLayout {
+  size_t status;      // uint32 status word (+ padding)
+  size_t blk_cnt;     // int32  [nblk][E]  per-block expert histogram, then its exclusive scan
+  size_t blk_prob;    // float  [nblk][E]  per-block sums of the router distribution
+  size_t meta;        // int32  kept[E] | offsets[E+1] | seg_start[E+1] | mtiles[E+1]
+                      //        | tp_up[E+2] | tp_dn[E+2]
+  size_t key_row;     // int32  [T*k]      padded row of each assignment, -1 if dropped
+  size_t xp;          // dtype  [R_cap][d] token copies in expert order
+  size_t h;           // dtype  [R_cap][f] expert hidden activations
+  size_t o;           // float  [R_cap][d] expert outputs
+  size_t hs;          // dtype  [T_pad][f_s] shared-expert hidden
+  size_t os;          // float  [T_pad][d]   shared-expert output
+  // host-io staging
+  size_t x_dev, y_dev, topk_idx, topk_w, counts, aux;
+  size_t total;
+};
+
+struct Plan {
+  moe_config cfg;
+  int elem;           // bytes per element of x / weights / y
+  int capacity;       // INT32_MAX when unlimited
+  int E_pad;          // E rounded up to 32
+  int BT;             // tokens per routing block
+  int KC;             // router K chunk
+  int nblk;           // routing blocks
+  int bm;             // rows per GEMM tile (128 tensor core, 64 SIMT)
+  int R_cap;          // rows reserved for the expert-ordered buffers
+  int T_pad;          // T rounded up to kSegAlign
+  bool tc;            // tensor-core path (bf16)
+  // GEMM tiling
+  int up_bn;          // output columns per up-projection tile
+  int dn_bn;          // output columns per down-projection tile
+  int nt_up, nt_dn;           // N tiles of a routed segment
+  int nt_up_sh, nt_dn_sh;     // N tiles of the shared segment
+  int mt_sh;                  // M tiles of the shared segment
+  int max_tiles_up, max_tiles_dn;  // host upper bounds (grid sizing)
+  int num_sms;
+  WsLayout ws;
+};
+
+enum class WsKind { Forward, Route, HostIO };
+
+int make_plan(const moe_config* cfg, WsKind kind, Plan* p);
+
+// Device pointers of the meta region.
+struct Meta {
+  int* kept;
+  int* offsets;
+  int* seg_start;
+  int* mtiles;
+  int* tp_up;
+  int* tp_dn;
+};
+Meta meta_ptrs(const Plan& p, void* ws);
+
+// ---- launchers (return a cudaError_t of the launch) ----------------------
+cudaError_t launch_router(const Plan& p, const void* x, const void* W_r, const float* logit_offset,
+                          const float* sel_bias, int32_t* topk_idx, float* topk_w, void* ws,
+                          cudaStream_t st);
+cudaError_t launch_scan(const Plan& p, void* ws, int32_t* expert_counts, float* aux_loss,
+                        int32_t* routed_counts, int32_t* offsets, float* f_out, float* P_out,
+                        cudaStream_t st);
+cudaError_t launch_permute(const Plan& p, const void* x, const int32_t* topk_idx,
+                           int32_t* slot_pos, bool copy_rows, void* ws, cudaStream_t st);
+cudaError_t launch_experts_tc(const Plan& p, const void* x, const void* W1, const void* W3,
+                              const void* W2, const void* Ws1, const void* Ws3, const void* Ws2,
+                              void* ws, cudaStream_t st, cudaEvent_t mid_event);
+cudaError_t launch_experts_simt(const Plan& p, const void* x, const void* W1, const void* W3,
+                                const void* W2, const void* Ws1, const void* Ws3,
+                                const void* Ws2, void* ws, cudaStream_t st,
+                                cudaEvent_t mid_event);
+cudaError_t launch_combine(const Plan& p, const float* topk_w, void* y, void* ws,
+                           cudaStream_t st);
+cudaError_t launch_selftest_wait(uint32_t* status, uint64_t wait_ns, cudaStream_t st);
+
+}  // namespace moe

@@ -1,0 +1,170 @@
+"""Python entry points over libmoe.so: argument marshalling only.
+
+Every stage of the layer runs in the library's CUDA kernels; torch provides
+device memory, streams and events.  Names follow the C ABI (include/moe.h).
+"""
+
+from __future__ import annotations
+
+import ctypes
+from dataclasses import dataclass
+from typing import Optional
+
+import torch
+
+from . import _native as N
+from .workloads import (ACT_GELU, ACT_RELU, ACT_SWIGLU, GATE_SIGMOID_RENORM,
+                        GATE_SOFTMAX_FULL, GATE_SOFTMAX_TOPK, LayerShape)
+
+_ACT = {ACT_GELU: N.MOE_ACT_GELU, ACT_RELU: N.MOE_ACT_RELU, ACT_SWIGLU: N.MOE_ACT_SWIGLU}
+_GATE = {GATE_SOFTMAX_TOPK: N.MOE_GATE_SOFTMAX_TOPK, GATE_SIGMOID_RENORM: N.MOE_GATE_SIGMOID_RENORM,
+         GATE_SOFTMAX_FULL: N.MOE_GATE_SOFTMAX_FULL}
+
+
+def make_config(T, d, E, k, f, act=ACT_SWIGLU, gate=GATE_SOFTMAX_TOPK, dtype="bf16",
+                capacity_factor=0.0, alpha=0.01, n_shared=0, f_shared=0) -> N.MoeConfig:
+    return N.MoeConfig(T=T, d=d, E=E, k=k, f=f, n_shared=n_shared,
+                       f_shared=f_shared if n_shared else 0,
+                       dtype=N.MOE_BF16 if dtype == "bf16" else N.MOE_F32,
+                       act=_ACT[act] if isinstance(act, str) else act,
+                       gate=_GATE[gate] if isinstance(gate, str) else gate,
+                       capacity_factor=float(capacity_factor), alpha=float(alpha), reserved=0)
+
+
+def config_for(shape: LayerShape, T: Optional[int] = None) -> N.MoeConfig:
+    return make_config(shape.T if T is None else T, shape.d, shape.E, shape.k, shape.f,
+                       shape.act, shape.gate, shape.dtype, shape.capacity_factor, shape.alpha,
+                       shape.n_shared, shape.f_shared)
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    if t is None:
+        return None
+    if not t.is_contiguous():
+        raise ValueError("tensors passed to libmoe must be contiguous")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream_handle(stream: Optional[torch.cuda.Stream]):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def workspace_size(cfg: N.MoeConfig, kind: str = "forward") -> int:
+    n = ctypes.c_size_t(0)
+    fn = {"forward": N.lib().moe_workspace_size, "route": N.lib().moe_route_workspace_size,
+          "host_io": N.lib().moe_host_io_workspace_size}[kind]
+    N.check(fn(ctypes.byref(cfg), ctypes.byref(n)), "moe_workspace_size")
+    return n.value
+
+
+def alloc_workspace(cfg: N.MoeConfig, device="cuda", kind: str = "forward") -> torch.Tensor:
+    """Device workspace; its first 256 bytes (the status word) start at zero."""
+    n = workspace_size(cfg, kind)
+    ws = torch.empty(max(n, 256), dtype=torch.uint8, device=device)
+    ws[:256].zero_()
+    return ws
+
+
+def launch_count(cfg: N.MoeConfig) -> int:
+    n = ctypes.c_int32(0)
+    N.check(N.lib().moe_launch_count(ctypes.byref(cfg), ctypes.byref(n)), "moe_launch_count")
+    return n.value
+
+
+@dataclass
+class MoeOutputs:
+    y: torch.Tensor
+    topk_idx: torch.Tensor
+    topk_w: torch.Tensor
+    expert_counts: torch.Tensor
+    aux_loss: torch.Tensor
+    routed_counts: Optional[torch.Tensor] = None
+    offsets: Optional[torch.Tensor] = None
+    slot_pos: Optional[torch.Tensor] = None
+    f: Optional[torch.Tensor] = None
+    P: Optional[torch.Tensor] = None
+
+
+def alloc_outputs(cfg: N.MoeConfig, device="cuda", dtype=torch.bfloat16, full=True,
+                  with_y=True) -> MoeOutputs:
+    T, d, E, k = cfg.T, cfg.d, cfg.E, cfg.k
+    i32, f32 = torch.int32, torch.float32
+    return MoeOutputs(
+        y=torch.empty((T, d), dtype=dtype, device=device) if with_y else None,
+        topk_idx=torch.empty((T, k), dtype=i32, device=device),
+        topk_w=torch.empty((T, k), dtype=f32, device=device),
+        expert_counts=torch.empty(E, dtype=i32, device=device),
+        aux_loss=torch.empty(1, dtype=f32, device=device),
+        routed_counts=torch.empty(E, dtype=i32, device=device) if full else None,
+        offsets=torch.empty(E + 1, dtype=i32, device=device) if full else None,
+        slot_pos=torch.empty((T, k), dtype=i32, device=device) if full else None,
+        f=torch.empty(E, dtype=f32, device=device) if full else None,
+        P=torch.empty(E, dtype=f32, device=device) if full else None)
+
+
+def forward(cfg: N.MoeConfig, x, W_r, W1, W2, W3=None, logit_offset=None, sel_bias=None,
+            Ws1=None, Ws3=None, Ws2=None, out: Optional[MoeOutputs] = None,
+            workspace: Optional[torch.Tensor] = None, stream=None, events=None) -> MoeOutputs:
+    """One call of moe_forward (or moe_forward_timed when `events` is a list of
+    MOE_NUM_STAGES + 1 torch.cuda.Event objects)."""
+    if out is None:
+        out = alloc_outputs(cfg, x.device, x.dtype)
+    if workspace is None:
+        workspace = alloc_workspace(cfg, x.device)
+    args = [ctypes.byref(cfg), _ptr(x), _ptr(W_r), _ptr(logit_offset), _ptr(sel_bias),
+            _ptr(W1), _ptr(W3), _ptr(W2), _ptr(Ws1), _ptr(Ws3), _ptr(Ws2),
+            _ptr(out.y), _ptr(out.topk_idx), _ptr(out.topk_w), _ptr(out.expert_counts),
+            _ptr(out.aux_loss), _ptr(out.routed_counts), _ptr(out.offsets), _ptr(out.slot_pos),
+            _ptr(out.f), _ptr(out.P), _ptr(workspace), ctypes.c_size_t(workspace.numel()),
+            _stream_handle(stream)]
+    if events is None:
+        rc = N.lib().moe_forward(*args)
+    else:
+        arr = (ctypes.c_void_p * len(events))(*[ctypes.c_void_p(e.cuda_event) for e in events])
+        rc = N.lib().moe_forward_timed(*args, arr)
+    N.check(rc, "moe_forward")
+    return out
+
+
+def route(cfg: N.MoeConfig, x, W_r, logit_offset=None, sel_bias=None,
+          out: Optional[MoeOutputs] = None, workspace: Optional[torch.Tensor] = None,
+          stream=None) -> MoeOutputs:
+    """Stages 1-3 and the balance statistics (moe_route)."""
+    if out is None:
+        out = alloc_outputs(cfg, x.device, x.dtype, with_y=False)
+    if workspace is None:
+        workspace = alloc_workspace(cfg, x.device, "route")
+    rc = N.lib().moe_route(
+        ctypes.byref(cfg), _ptr(x), _ptr(W_r), _ptr(logit_offset), _ptr(sel_bias),
+        _ptr(out.topk_idx), _ptr(out.topk_w), _ptr(out.expert_counts), _ptr(out.aux_loss),
+        _ptr(out.routed_counts), _ptr(out.offsets), _ptr(out.slot_pos), _ptr(out.f),
+        _ptr(out.P), _ptr(workspace), ctypes.c_size_t(workspace.numel()), _stream_handle(stream))
+    N.check(rc, "moe_route")
+    return out
+
+
+def forward_host_io(cfg: N.MoeConfig, x_host: torch.Tensor, y_host: torch.Tensor,
+                    aux_host: torch.Tensor, W_r, W1, W2, W3=None, logit_offset=None,
+                    sel_bias=None, Ws1=None, Ws3=None, Ws2=None, workspace=None, stream=None):
+    """moe_forward_host_io: x_host / y_host / aux_host are (pinned) host tensors."""
+    if workspace is None:
+        workspace = alloc_workspace(cfg, W_r.device, "host_io")
+    rc = N.lib().moe_forward_host_io(
+        ctypes.byref(cfg), _ptr(x_host), _ptr(W_r), _ptr(logit_offset), _ptr(sel_bias),
+        _ptr(W1), _ptr(W3), _ptr(W2), _ptr(Ws1), _ptr(Ws3), _ptr(Ws2), _ptr(y_host),
+        _ptr(aux_host), _ptr(workspace), ctypes.c_size_t(workspace.numel()),
+        _stream_handle(stream))
+    N.check(rc, "moe_forward_host_io")
+    return y_host, aux_host
+
+
+def check_status(workspace: torch.Tensor, stream=None) -> int:
+    """Synchronise and return (and clear) the device status of a workspace."""
+    return N.lib().moe_check_status(_ptr(workspace), _stream_handle(stream))
+
+
+def selftest_wait_timeout(workspace: torch.Tensor, wait_ns: int, stream=None) -> None:
+    N.check(N.lib().moe_selftest_wait_timeout(_ptr(workspace), ctypes.c_size_t(workspace.numel()),
+                                              ctypes.c_uint64(wait_ns), _stream_handle(stream)),
+            "moe_selftest_wait_timeout")

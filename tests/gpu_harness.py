@@ -1,0 +1,136 @@
+"""Runs the CUDA layer and the CPU oracle on the same seeded inputs and
+compares them under the parity rules:
+
+* routing (top-k indices) is bit-exact, except tokens whose oracle
+  selection scores have an adjacent gap below NEAR_TIE among their k+1 best
+  (the k-th / (k+1)-th gap for a changed set, a gap inside the chosen set for
+  a changed order); such tokens are counted and reported, never hidden;
+* the oracle is then re-run with the GPU's choice forced, and every integer
+  output (routed / kept counts, offsets, slot positions) must match exactly;
+* floats: gates and P within float32 rounding of the float64 values, the
+  balance loss within 1e-5 relative, y within rel-L2 1e-5 / max-abs 1e-4
+  (float32 path) or rel-L2 1e-2 / max-abs 3e-2 (bf16 path).
+"""
+
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+import oracle.moe_oracle as O
+from sparse_mixture_experts_65_b300 import layer as L
+
+NEAR_TIE = 1e-5
+TOL = {"f32": (1e-5, 1e-4), "bf16": (1e-2, 3e-2)}
+GATE_RTOL, GATE_ATOL = 1e-5, 2e-6
+P_RTOL, P_ATOL = 1e-5, 1e-8
+AUX_RTOL = 1e-5
+
+
+def host64(t):
+    return None if t is None else t.detach().float().cpu().numpy().astype(np.float64)
+
+
+class LazyExperts:
+    """Expert weights streamed to the host one expert at a time (float64)."""
+
+    def __init__(self, t):
+        self.t = t
+        self._e = None
+        self._v = None
+
+    def __getitem__(self, e):
+        if self._e != e:
+            self._v = self.t[e].float().cpu().numpy().astype(np.float64)
+            self._e = e
+        return self._v
+
+
+def run_gpu(inp, cfg=None, workspace=None):
+    cfg = cfg if cfg is not None else L.config_for(inp.shape)
+    out = L.forward(cfg, inp.x, inp.W_r, inp.W1, inp.W2, inp.W3, inp.logit_offset, inp.sel_bias,
+                    inp.Ws1, inp.Ws3, inp.Ws2, workspace=workspace)
+    torch.cuda.synchronize()
+    return cfg, out
+
+
+def near_tie_mask(sel, k):
+    T, E = sel.shape
+    if k >= E:
+        srt = -np.sort(-sel, axis=1)
+        gaps = srt[:, :-1] - srt[:, 1:] if E > 1 else np.full((T, 1), np.inf)
+    else:
+        srt = -np.sort(-sel, axis=1)[:, :k + 1]
+        gaps = srt[:, :-1] - srt[:, 1:]
+    return gaps.min(axis=1) < NEAR_TIE
+
+
+def rel_l2(a, b):
+    den = np.linalg.norm(b)
+    return float(np.linalg.norm(a - b) / den) if den > 0 else float(np.linalg.norm(a - b))
+
+
+def check_layer(inp, out, sample=None, check_y=True):
+    """Compare one GPU call with the oracle.  `sample`: token indices whose y
+    rows are checked (None = all).  Returns a report dict; raises on failure."""
+    s = inp.shape
+    x64 = host64(inp.x)
+    Wr = host64(inp.W_r)
+    off = host64(inp.logit_offset)
+    bias = host64(inp.sel_bias)
+    rep = {"T": s.T, "tokens_checked": None}
+
+    # unconditioned selection
+    logits = O.router_logits(x64, Wr, off)
+    sel = O.selection_scores(logits, s.gate, bias)
+    idx_ref = O.topk_indices(sel, s.k) if s.T else np.zeros((0, s.k), np.int64)
+    idx_gpu = out.topk_idx.cpu().numpy().astype(np.int64)
+    assert idx_gpu.shape == idx_ref.shape
+    assert np.all((idx_gpu >= 0) & (idx_gpu < s.E)), "expert index out of range"
+    for t in range(s.T):
+        assert len(set(idx_gpu[t].tolist())) == s.k, "repeated expert within a token"
+    diff = np.any(idx_gpu != idx_ref, axis=1)
+    near = near_tie_mask(sel, s.k) if s.T else np.zeros(0, bool)
+    rep["near_tie_tokens"] = int(near.sum())
+    rep["flipped_tokens"] = int(diff.sum())
+    bad = np.nonzero(diff & ~near)[0]
+    assert bad.size == 0, f"{bad.size} tokens chose different experts outside the near-tie band: {bad[:10]}"
+
+    # oracle conditioned on the GPU's choice
+    W3 = LazyExperts(inp.W3) if inp.W3 is not None else None
+    tokens = None if sample is None else np.asarray(sample)
+    r = O.moe_forward(x64, Wr, LazyExperts(inp.W1), LazyExperts(inp.W2), s.k, s.act, s.gate,
+                      W3=W3, logit_offset=off, sel_bias=bias, capacity_factor=s.capacity_factor,
+                      alpha=s.alpha, Ws1=host64(inp.Ws1), Ws3=host64(inp.Ws3), Ws2=host64(inp.Ws2),
+                      tokens=tokens if check_y else np.zeros(0, np.int64), forced_idx=idx_gpu)
+    a = r.asg
+    np.testing.assert_array_equal(out.expert_counts.cpu().numpy(), a.kept)
+    if out.routed_counts is not None:
+        np.testing.assert_array_equal(out.routed_counts.cpu().numpy(), a.routed)
+    if out.offsets is not None:
+        np.testing.assert_array_equal(out.offsets.cpu().numpy(), a.offsets)
+    if out.slot_pos is not None:
+        np.testing.assert_array_equal(out.slot_pos.cpu().numpy(), a.slot_pos)
+    rep["kept"] = int(a.kept.sum())
+    rep["dropped"] = int(s.T * s.k - a.kept.sum())
+    np.testing.assert_allclose(out.topk_w.cpu().numpy(), r.topk_w, rtol=GATE_RTOL, atol=GATE_ATOL)
+    if out.f is not None:
+        np.testing.assert_allclose(out.f.cpu().numpy(), r.f, rtol=1e-6, atol=0)
+    if out.P is not None:
+        np.testing.assert_allclose(out.P.cpu().numpy(), r.P, rtol=P_RTOL, atol=P_ATOL)
+    aux = float(out.aux_loss.cpu()[0])
+    assert abs(aux - r.aux_loss) <= AUX_RTOL * abs(r.aux_loss) + 1e-12, (aux, r.aux_loss)
+    rep["aux_loss"] = aux
+
+    if check_y and s.T:
+        y_gpu = out.y.float().cpu().numpy().astype(np.float64)
+        if tokens is not None:
+            y_gpu = y_gpu[tokens]
+        rtol_l2, atol_max = TOL[s.dtype]
+        rl2 = rel_l2(y_gpu, r.y)
+        mx = float(np.max(np.abs(y_gpu - r.y))) if y_gpu.size else 0.0
+        rep.update(rel_l2=rl2, max_abs=mx, tokens_checked=len(r.y))
+        assert np.all(np.isfinite(y_gpu)), "non-finite output"
+        assert rl2 <= rtol_l2, f"rel-L2 {rl2:.3e} > {rtol_l2}"
+        assert mx <= atol_max, f"max-abs {mx:.3e} > {atol_max}"
+    return rep

@@ -1,0 +1,274 @@
+"""CUDA layer versus the CPU oracle on seeded inputs, through the C ABI.
+
+Small cases span several tiles with ragged tails (rows, N columns and the K
+reduction); the named layers run at full size with routing checked over the
+whole batch and y on every token or on a seeded sample the oracle can afford.
+"""
+import gc
+
+import numpy as np
+import pytest
+import torch
+
+from sparse_mixture_experts_65_b300 import layer as L
+from sparse_mixture_experts_65_b300 import workloads as W
+from sparse_mixture_experts_65_b300.workloads import LayerShape
+
+from gpu_harness import check_layer, host64, run_gpu
+
+pytestmark = pytest.mark.gpu
+
+SW, RE, GE = W.ACT_SWIGLU, W.ACT_RELU, W.ACT_GELU
+TOPK, SIG, FULL = W.GATE_SOFTMAX_TOPK, W.GATE_SIGMOID_RENORM, W.GATE_SOFTMAX_FULL
+
+SMALL = [
+    LayerShape("bf16_swiglu_ragged", 10, T=300, d=256, E=8, k=2, f=384, act=SW, gate=TOPK,
+               dtype="bf16"),
+    LayerShape("bf16_relu_capacity_skew", 11, T=517, d=192, E=16, k=1, f=256, act=RE, gate=FULL,
+               dtype="bf16", capacity_factor=1.0, logit_offset_var=1.5),
+    LayerShape("bf16_sigmoid_bias_shared", 12, T=130, d=136, E=32, k=4, f=160, act=SW, gate=SIG,
+               dtype="bf16", alpha=1e-4, n_shared=1, f_shared=96, sel_bias_halfwidth=0.05),
+    LayerShape("bf16_gelu_ntail", 13, T=77, d=64, E=4, k=2, f=200, act=GE, gate=TOPK, dtype="bf16"),
+    LayerShape("bf16_many_experts", 16, T=64, d=128, E=300, k=6, f=64, act=SW, gate=SIG,
+               dtype="bf16", sel_bias_halfwidth=0.05),
+    LayerShape("f32_swiglu_shared_cap", 14, T=150, d=48, E=6, k=3, f=80, act=SW, gate=SIG,
+               dtype="f32", capacity_factor=1.1, n_shared=1, f_shared=40),
+    LayerShape("f32_relu_full", 15, T=99, d=36, E=5, k=1, f=52, act=RE, gate=FULL, dtype="f32",
+               capacity_factor=0.9, logit_offset_var=1.5),
+]
+
+
+def _free():
+    gc.collect()
+    torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("shape", SMALL, ids=lambda s: s.name)
+def test_small_layers(shape):
+    inp = W.make_inputs(shape, "cuda", seed=1)
+    _, out = run_gpu(inp)
+    rep = check_layer(inp, out)
+    print(shape.name, rep)
+
+
+@pytest.mark.parametrize("up_bn,dn_bn", [(32, 64), (64, 96), (96, 128), (128, 192), (128, 256)])
+def test_every_swiglu_tile_width(monkeypatch, up_bn, dn_bn):
+    """Force each tile width of the tensor-core kernels on a ragged layer."""
+    monkeypatch.setenv("MOE_TILE_N_UP", str(up_bn))
+    monkeypatch.setenv("MOE_TILE_N_DOWN", str(dn_bn))
+    shape = LayerShape("tiles", 20, T=211, d=200, E=6, k=2, f=416, act=SW, gate=TOPK,
+                       dtype="bf16", n_shared=1, f_shared=136)
+    inp = W.make_inputs(shape, "cuda", seed=2)
+    _, out = run_gpu(inp)
+    check_layer(inp, out)
+
+
+@pytest.mark.parametrize("act", [RE, GE])
+@pytest.mark.parametrize("up_bn", [64, 96, 128, 256])
+def test_every_plain_tile_width(monkeypatch, act, up_bn):
+    monkeypatch.setenv("MOE_TILE_N_UP", str(up_bn))
+    shape = LayerShape("plain", 21, T=190, d=96, E=5, k=2, f=328, act=act, gate=TOPK, dtype="bf16")
+    inp = W.make_inputs(shape, "cuda", seed=3)
+    _, out = run_gpu(inp)
+    check_layer(inp, out)
+
+
+def test_toy_layer_full():
+    inp = W.make_inputs(W.TOY, "cuda")
+    _, out = run_gpu(inp)
+    rep = check_layer(inp, out)
+    assert rep["flipped_tokens"] == 0
+    print("toy", rep)
+
+
+def test_switch_layer_full():
+    inp = W.make_inputs(W.SWITCH, "cuda")
+    _, out = run_gpu(inp)
+    rep = check_layer(inp, out)
+    assert rep["dropped"] > 0       # the logit skew overflows some experts at rho = 1.25
+    print("switch", rep)
+    del inp, out
+    _free()
+
+
+def test_mixtral_layer_sampled():
+    inp = W.make_inputs(W.MIXTRAL, "cuda")
+    _, out = run_gpu(inp)
+    sample = np.sort(np.random.default_rng(7).choice(W.MIXTRAL.T, 192, replace=False))
+    rep = check_layer(inp, out, sample=sample)
+    print("mixtral", rep)
+    del inp, out
+    _free()
+
+
+def test_dsv3_layer_sampled():
+    inp = W.make_inputs(W.DSV3, "cuda")
+    _, out = run_gpu(inp)
+    sample = np.sort(np.random.default_rng(8).choice(W.DSV3.T, 48, replace=False))
+    rep = check_layer(inp, out, sample=sample)
+    print("dsv3", rep)
+    del inp, out
+    _free()
+
+
+@pytest.mark.parametrize("T", W.GPTOSS_SWEEP_T)
+def test_gptoss_decode_sweep(T):
+    shape = W.GPTOSS.with_T(T)
+    inp = W.make_inputs(shape, "cuda")
+    _, out = run_gpu(inp)
+    sample = None if T <= 64 else np.sort(np.random.default_rng(9).choice(T, 48, replace=False))
+    rep = check_layer(inp, out, sample=sample)
+    print("gptoss", T, rep)
+    del inp, out
+    _free()
+
+
+# ---------------------------------------------------------------- edge cases
+def test_empty_batch():
+    shape = LayerShape("empty", 30, T=0, d=64, E=4, k=2, f=64, act=SW, gate=TOPK, dtype="bf16")
+    inp = W.make_inputs(shape, "cuda")
+    cfg, out = run_gpu(inp)
+    assert out.expert_counts.sum().item() == 0
+    assert out.offsets.cpu().tolist() == [0] * 5
+    assert float(out.aux_loss.cpu()[0]) == 0.0
+    assert L.launch_count(cfg) == 0
+
+
+@pytest.mark.parametrize("T", [1, 2, 129])
+def test_tiny_batches(T):
+    shape = LayerShape("tiny", 31, T=T, d=128, E=8, k=2, f=128, act=SW, gate=TOPK, dtype="bf16",
+                       n_shared=1, f_shared=64)
+    inp = W.make_inputs(shape, "cuda")
+    _, out = run_gpu(inp)
+    check_layer(inp, out)
+
+
+def test_single_expert_is_dense_ffn():
+    shape = LayerShape("dense", 32, T=200, d=64, E=1, k=1, f=192, act=GE, gate=TOPK, dtype="bf16")
+    inp = W.make_inputs(shape, "cuda")
+    _, out = run_gpu(inp)
+    np.testing.assert_array_equal(out.topk_w.cpu().numpy(), 1.0)
+    check_layer(inp, out)
+
+
+def test_k_equals_E():
+    shape = LayerShape("allk", 33, T=70, d=64, E=4, k=4, f=64, act=SW, gate=TOPK, dtype="bf16")
+    inp = W.make_inputs(shape, "cuda")
+    _, out = run_gpu(inp)
+    check_layer(inp, out)
+
+
+def test_all_tokens_to_one_expert_with_drops():
+    shape = LayerShape("onehot", 34, T=400, d=64, E=8, k=1, f=128, act=RE, gate=FULL,
+                       dtype="bf16", capacity_factor=1.25)
+    inp = W.make_inputs(shape, "cuda")
+    inp.logit_offset = torch.zeros(8, device="cuda")
+    inp.logit_offset[5] = 100.0
+    _, out = run_gpu(inp)
+    counts = out.routed_counts.cpu().numpy()
+    assert counts[5] == 400
+    C = int(np.ceil(400 * 1.25 / 8))
+    assert out.expert_counts.cpu().numpy()[5] == C
+    slot = out.slot_pos.cpu().numpy()[:, 0]
+    assert np.all(slot[:C] == np.arange(C)) and np.all(slot[C:] == -1)   # first come by token
+    assert torch.all(out.y[C:] == 0)                                     # dropped tokens: y = 0
+    check_layer(inp, out)
+
+
+def test_tiny_capacity():
+    shape = LayerShape("tinycap", 35, T=333, d=64, E=8, k=2, f=64, act=SW, gate=TOPK,
+                       dtype="bf16", capacity_factor=0.05)
+    inp = W.make_inputs(shape, "cuda")
+    _, out = run_gpu(inp)
+    C = int(np.ceil(333 * 2 * 0.05 / 8))
+    assert out.expert_counts.cpu().numpy().max() <= C
+    check_layer(inp, out)
+
+
+def test_selection_bias_moves_choice_not_gates():
+    shape = LayerShape("bias", 36, T=256, d=64, E=16, k=2, f=64, act=SW, gate=SIG, dtype="bf16")
+    inp = W.make_inputs(shape, "cuda")
+    _, out0 = run_gpu(inp)
+    inp.sel_bias = torch.zeros(16, device="cuda")
+    inp.sel_bias[3] = 2.0                 # sigmoid <= 1, so expert 3 always wins
+    _, out1 = run_gpu(inp)
+    assert torch.all(out1.topk_idx[:, 0] == 3)
+    check_layer(inp, out1)
+    # the same bias on every expert changes nothing
+    inp.sel_bias = torch.full((16,), 0.3, device="cuda")
+    _, out2 = run_gpu(inp)
+    assert torch.equal(out2.topk_idx, out0.topk_idx)
+    assert torch.equal(out2.y, out0.y)
+
+
+# ---------------------------------------------------------------- properties
+def test_repeat_calls_bitwise_identical():
+    inp = W.make_inputs(SMALL[2], "cuda", seed=4)
+    cfg = L.config_for(inp.shape)
+    ws = L.alloc_workspace(cfg)
+    _, a = run_gpu(inp, cfg, ws)
+    _, b = run_gpu(inp, cfg, ws)
+    for name in ("y", "topk_idx", "topk_w", "expert_counts", "aux_loss", "slot_pos", "P"):
+        assert torch.equal(getattr(a, name), getattr(b, name)), name
+
+
+def test_route_entry_point_matches_forward():
+    shape = SMALL[1]
+    inp = W.make_inputs(shape, "cuda", seed=5)
+    cfg, fw = run_gpu(inp)
+    rt = L.route(cfg, inp.x, inp.W_r, inp.logit_offset, inp.sel_bias)
+    torch.cuda.synchronize()
+    for name in ("topk_idx", "topk_w", "expert_counts", "aux_loss", "routed_counts", "offsets",
+                 "slot_pos", "f", "P"):
+        assert torch.equal(getattr(rt, name), getattr(fw, name)), name
+
+
+def test_host_io_entry_point_matches_forward():
+    shape = SMALL[0]
+    inp = W.make_inputs(shape, "cuda", seed=6)
+    cfg, fw = run_gpu(inp)
+    x_h = inp.x.cpu().pin_memory()
+    y_h = torch.empty_like(x_h).pin_memory()
+    aux_h = torch.empty(1, dtype=torch.float32).pin_memory()
+    L.forward_host_io(cfg, x_h, y_h, aux_h, inp.W_r, inp.W1, inp.W2, inp.W3)
+    torch.cuda.synchronize()
+    assert torch.equal(y_h, fw.y.cpu())
+    assert torch.equal(aux_h, fw.aux_loss.cpu())
+
+
+def test_bounded_wait_reports_timeout():
+    """A wait on a barrier nothing completes gives up after ~1 ms and the host
+    reads MOE_ERR_TIMEOUT; the context stays usable afterwards."""
+    ws = torch.zeros(256, dtype=torch.uint8, device="cuda")
+    assert L.check_status(ws) == L.N.MOE_OK
+    L.selftest_wait_timeout(ws, 1_000_000)
+    assert L.check_status(ws) == L.N.MOE_ERR_TIMEOUT
+    assert L.check_status(ws) == L.N.MOE_OK          # cleared by the first check
+    inp = W.make_inputs(SMALL[3], "cuda")
+    _, out = run_gpu(inp)
+    check_layer(inp, out)
+
+
+def test_status_clean_after_full_layer():
+    inp = W.make_inputs(SMALL[0], "cuda", seed=9)
+    cfg = L.config_for(inp.shape)
+    ws = L.alloc_workspace(cfg)
+    run_gpu(inp, cfg, ws)
+    assert L.check_status(ws) == L.N.MOE_OK
+
+
+def test_bad_arguments_rejected_on_device():
+    inp = W.make_inputs(SMALL[0], "cuda", seed=10)
+    cfg = L.config_for(inp.shape)
+    ws = L.alloc_workspace(cfg)
+    with pytest.raises(L.N.MoeError) as e:
+        L.forward(cfg, inp.x, inp.W_r, inp.W1, inp.W2, None, workspace=ws)   # SwiGLU needs W3
+    assert e.value.code == L.N.MOE_ERR_ARG
+    with pytest.raises(L.N.MoeError) as e:
+        L.forward(cfg, inp.x, inp.W_r, inp.W1, inp.W2, inp.W3, workspace=ws[:1024])
+    assert e.value.code == L.N.MOE_ERR_WORKSPACE
+    xbig = torch.empty(inp.x.numel() + 8, dtype=inp.x.dtype, device="cuda")
+    xmis = xbig[1:1 + inp.x.numel()].view_as(inp.x)     # 2-byte offset: not 16-byte aligned
+    with pytest.raises(L.N.MoeError) as e:
+        L.forward(cfg, xmis, inp.W_r, inp.W1, inp.W2, inp.W3, workspace=ws)
+    assert e.value.code == L.N.MOE_ERR_ARG

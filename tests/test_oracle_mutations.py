@@ -15,7 +15,7 @@ import oracle_pins as P
 
 _orig = {name: getattr(M, name) for name in (
     "router_logits", "topk_indices", "gate_values", "affinity", "expert_capacity",
-    "assign_slots", "gelu_erf", "silu", "expert_ffn", "balance_stats", "router_probs",
+    "assign_slots", "gelu_erf", "silu", "expert_ffn_rows", "balance_stats", "router_probs",
     "softmax_rows")}
 
 
@@ -82,25 +82,25 @@ def _silu_plain_sigmoid(z):
     return M.sigmoid(z)
 
 
-def _ffn_swiglu_no_up(xt, W1, W2, act, W3=None, counter=None):
+def _ffn_swiglu_no_up(X, W1, W2, act, W3=None, counter=None):
     if act == M.ACT_SWIGLU:
-        W3 = np.ones_like(np.asarray(W1, dtype=float)) * 0 + np.asarray(W1, dtype=float)
-    return _orig["expert_ffn"](xt, W1, W2, act, W3, counter)
+        W3 = np.asarray(W1, dtype=float)
+    return _orig["expert_ffn_rows"](X, W1, W2, act, W3, counter)
 
 
-def _ffn_swapped_gate_up(xt, W1, W2, act, W3=None, counter=None):
+def _ffn_swapped_gate_up(X, W1, W2, act, W3=None, counter=None):
     if act == M.ACT_SWIGLU:
-        return _orig["expert_ffn"](xt, W3, W2, act, W1, counter)
-    return _orig["expert_ffn"](xt, W1, W2, act, W3, counter)
+        return _orig["expert_ffn_rows"](X, W3, W2, act, W1, counter)
+    return _orig["expert_ffn_rows"](X, W1, W2, act, W3, counter)
 
 
-def _ffn_transposed_down(xt, W1, W2, act, W3=None, counter=None):
+def _ffn_transposed_down(X, W1, W2, act, W3=None, counter=None):
     W2 = np.asarray(W2, dtype=float)
     if W2.shape[0] == W2.shape[1]:
         W2 = W2.T
     else:
         W2 = W2[::-1]
-    return _orig["expert_ffn"](xt, W1, W2, act, W3, counter)
+    return _orig["expert_ffn_rows"](X, W1, W2, act, W3, counter)
 
 
 def _balance_no_k(routed, probs, T, k, alpha):
@@ -136,9 +136,9 @@ MUTATIONS = [
     ("last come kept instead of first", "assign_slots", _assign_last_come, P.check_capacity_drops),
     ("GELU tanh approximation", "gelu_erf", _gelu_tanh, P.check_dense_ffn_special_case),
     ("SiLU without the z factor", "silu", _silu_plain_sigmoid, P.check_dense_ffn_special_case),
-    ("SwiGLU up projection replaced", "expert_ffn", _ffn_swiglu_no_up, P.check_sparse_equals_dense),
-    ("SwiGLU gate and up swapped", "expert_ffn", _ffn_swapped_gate_up, P.check_dense_ffn_special_case),
-    ("down projection transposed", "expert_ffn", _ffn_transposed_down, P.check_sparse_equals_dense),
+    ("SwiGLU up projection replaced", "expert_ffn_rows", _ffn_swiglu_no_up, P.check_sparse_equals_dense),
+    ("SwiGLU gate and up swapped", "expert_ffn_rows", _ffn_swapped_gate_up, P.check_dense_ffn_special_case),
+    ("down projection transposed", "expert_ffn_rows", _ffn_transposed_down, P.check_sparse_equals_dense),
     ("f divides by T, not T*k", "balance_stats", _balance_no_k, P.check_balance_uniform),
     ("loss misses the factor N", "balance_stats", _balance_no_E, P.check_balance_uniform),
     ("sigmoid P not normalised", "router_probs", _probs_unnormalised_sigmoid, P.check_router_probs),
