@@ -1,0 +1,530 @@
+#!/usr/bin/env python
+"""Throughput of the B300 MoE layer forward pass (tokens/s), one JSON line.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl b300|reference]
+                    [--workload switch|mixtral|dsv3|gptoss<T>|toy]
+
+A step is one call of the whole layer (router, top-k, capacity, permute,
+expert MLPs, combine and balance statistics) on one batch of seeded
+synthetic input already resident in HBM.  K steps run back to back between
+a barrier and a device synchronisation on each side, timed with CUDA
+events on the launching stream; the job time is the maximum over ranks.
+Each rank of a torchrun launch runs an independent replica on its own GPU
+(weak scaling; the layer has no exchange step between replicas).
+
+Also reported:
+  roofline     the dominant kernel's algorithmic bytes (or FLOPs) per launch
+               over its average duration, from per-stage CUDA events recorded
+               inside the timed region, against the measured peak;
+  e2e          the same metric through moe_forward_host_io: x copied from
+               pinned host memory and y copied back inside every step;
+  cpu_baseline the fp64 CPU oracle on the host cores (rank 0, N = 1 only);
+  clocks       SM clocks and throttle reasons sampled during the timed region.
+
+--impl reference times the CPU oracle itself on the same workload (bounded
+per-step samples), the way the pages' own numpy / PyTorch loops would run.
+"""
+
+from __future__ import annotations
+
+import argparse
+import glob
+import hashlib
+import json
+import math
+import os
+import statistics
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "MoE-layer tokens/sec on 1 B300 (bf16); % of tensor-core or HBM roofline"
+L2_BYTES = 126 * 1024 * 1024
+FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
+STAGES = ("router", "topk", "permute", "up", "down", "combine")
+DEFAULT_STEPS = {"switch": 5000, "toy": 5000, "mixtral": 300, "dsv3": 300, "gptoss": 3000}
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=None)
+    ap.add_argument("--warmup", type=int, default=None)
+    ap.add_argument("--impl", default="b300", choices=["b300", "reference"])
+    ap.add_argument("--workload", default="switch")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0,
+                    help="target CPU time of the oracle baseline sample")
+    a = ap.parse_args()
+    base = a.workload.rstrip("0123456789_T") or a.workload
+    if a.steps is None:
+        a.steps = DEFAULT_STEPS.get(base, 200)
+    if a.warmup is None:
+        a.warmup = max(3, min(20, a.steps // 10))
+    a.warmup = max(3, a.warmup)
+    return a
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def max_over_ranks(value, dist=None, device="cpu"):
+    """Largest value over all ranks of the job (the job time is the slowest
+    rank's).  `dist` is torch.distributed when the job has several ranks."""
+    if dist is None or not dist.is_initialized() or dist.get_world_size() == 1:
+        return float(value)
+    import torch
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as fh:
+            d = json.load(fh)
+        return {k: float(d[k]) for k in FALLBACK_PEAKS}, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def source_sha():
+    h = hashlib.sha256()
+    for f in sorted(glob.glob(os.path.join(ROOT, "sparse_mixture_experts_65_b300", "csrc", "*"))):
+        with open(f, "rb") as fh:
+            h.update(os.path.basename(f).encode() + fh.read())
+    return h.hexdigest()[:16]
+
+
+# ----------------------------------------------------------------- accounting
+def accounting(shape, kept):
+    """Algorithmic bytes and FLOPs per launch of each kernel and of the layer,
+    from the kept assignments per expert.  Weights count once per active
+    expert; activations at their stored widths (bf16 x/h/y, fp32 o)."""
+    T, d, E, k, f = shape.T, shape.d, shape.E, shape.k, shape.f
+    el = 2 if shape.dtype == "bf16" else 4
+    rows = int(sum(kept))
+    active = int(sum(1 for c in kept if c > 0))
+    sw = shape.act == "swiglu"
+    m_up = 2 if sw else 1
+    S, fs = shape.n_shared, shape.f_shared
+    w_up = active * m_up * f * d * el + S * 2 * fs * d * el
+    w_dn = active * d * f * el + S * d * fs * el
+    acc = {
+        "router": {"bytes": T * d * el + E * d * el + T * k * 8, "flops": 2 * T * d * E},
+        "topk": {"bytes": (2 * T * E + 8 * T * k) * 4, "flops": 0},
+        "permute": {"bytes": 2 * rows * d * el, "flops": 0},
+        "up": {"bytes": w_up + (rows + S * T) * d * el + (rows * f + S * T * fs) * el,
+               "flops": 2 * rows * d * f * m_up + S * 2 * T * d * fs * 2},
+        "down": {"bytes": w_dn + (rows * f + S * T * fs) * el + (rows + S * T) * d * 4,
+                 "flops": 2 * rows * f * d + S * 2 * T * fs * d},
+        "combine": {"bytes": (rows + S * T) * d * 4 + T * d * el, "flops": 2 * rows * d},
+    }
+    layer_bytes = (active * (m_up + 1) * f * d + S * 3 * fs * d + E * d + 2 * T * d) * el
+    layer_flops = 2 * rows * (m_up + 1) * d * f + S * 2 * T * 3 * d * fs + 2 * T * d * E
+    return acc, {"bytes": layer_bytes, "flops": layer_flops, "active_experts": active,
+                 "kept_rows": rows, "active_weight_bytes": w_up + w_dn}
+
+
+def roofline_for(stage, acc, ms, peaks, peak_kind):
+    a = acc[stage]
+    sec = ms / 1e3
+    ridge = peaks["bf16_tflops"] * 1e12 / (peaks["hbm_gbs"] * 1e9)
+    ai = a["flops"] / a["bytes"] if a["bytes"] else float("inf")
+    if a["flops"] and ai > ridge:
+        peak = peaks["bf16_tflops_sustained"]
+        ach = a["flops"] / sec / 1e12
+        return {"bound": "tensor", "achieved": round(ach, 2), "peak": peak, "unit": "TFLOP/s",
+                "frac": round(ach / peak, 4), "kernel": stage,
+                "peak_source": f"{peak_kind} bf16 sustained (kernel runs inside a seconds-long loop)",
+                "flops_per_launch": a["flops"], "ms_per_launch": round(ms, 5)}
+    ach = a["bytes"] / sec / 1e9
+    peak = peaks["hbm_gbs"]
+    return {"bound": "hbm", "achieved": round(ach, 1), "peak": peak, "unit": "GB/s",
+            "frac": round(ach / peak, 4), "kernel": stage, "peak_source": f"{peak_kind} HBM copy",
+            "bytes_per_launch": a["bytes"], "ms_per_launch": round(ms, 5)}
+
+
+def ncu_traffic(stage, workload):
+    """dram bytes per launch of a kernel from the committed ncu summary, or
+    None when no capture exists for the current sources."""
+    p = os.path.join(ROOT, "profiles", "ncu_traffic.txt")
+    if not os.path.exists(p):
+        return None
+    with open(p) as fh:
+        d = json.load(fh)
+    ent = d.get(f"{workload}:{stage}")
+    if not ent or ent.get("source_sha") != source_sha():
+        return None
+    return ent.get("dram_bytes_per_launch")
+
+
+# ----------------------------------------------------------------- clocks
+class ClockSampler:
+    """SM clock and throttle reasons during the timed region: NVML when the
+    Python bindings are installed, else `nvidia-smi -lms` in the background."""
+    REASONS = {"hw_slowdown": 0x8, "hw_thermal_slowdown": 0x40, "sw_thermal_slowdown": 0x20,
+               "sw_power_cap": 0x4, "hw_power_brake_slowdown": 0x80}
+    SMI_FIELDS = ("timestamp,clocks.sm,clocks.max.sm,clocks_event_reasons.hw_slowdown,"
+                  "clocks_event_reasons.hw_thermal_slowdown,"
+                  "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index, period_s=0.005):
+        self.samples, self.reasons, self.max_mhz = [], set(), None
+        self._raw = []
+        self.period = period_s
+        self._stop = threading.Event()
+        self._h = None
+        self._smi = None
+        self.error = None
+        self._uuid = None
+        try:
+            import torch
+            u = str(torch.cuda.get_device_properties(device_index).uuid)
+            self._uuid = u if u.startswith("GPU-") else "GPU-" + u
+        except Exception:
+            pass
+        try:
+            import pynvml
+            pynvml.nvmlInit()
+            self._nv = pynvml
+            try:   # CUDA and NVML number devices differently: match by UUID
+                self._h = pynvml.nvmlDeviceGetHandleByUUID(self._uuid)
+            except Exception:
+                self._h = pynvml.nvmlDeviceGetHandleByIndex(device_index)
+            self.max_mhz = pynvml.nvmlDeviceGetMaxClockInfo(self._h, pynvml.NVML_CLOCK_SM)
+        except Exception as e:  # pragma: no cover - reported in the JSON line
+            self.error = repr(e)
+
+    window = (0.0, float("inf"))
+
+    def mark(self, t0, t1):
+        """Wall-clock bounds of the timed region (used to filter samples)."""
+        self.window = (t0, t1)
+
+    def _sample(self):
+        nv = self._nv
+        mhz = nv.nvmlDeviceGetClockInfo(self._h, nv.NVML_CLOCK_SM)
+        r = nv.nvmlDeviceGetCurrentClocksEventReasons(self._h)
+        self._raw.append((time.time(), mhz, r))
+
+    def _run(self):
+        while not self._stop.is_set():
+            self._sample()
+            time.sleep(self.period)
+
+    def start(self):
+        if self._h is None:
+            import subprocess
+            try:
+                cmd = ["nvidia-smi", f"--query-gpu={self.SMI_FIELDS}", "--format=csv,noheader,nounits",
+                       "-lms", "20"]
+                if self._uuid:
+                    cmd += ["-i", self._uuid]
+                self._smi = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL,
+                                             text=True)
+                time.sleep(0.1)
+            except Exception as e:
+                self.error = repr(e)
+            return
+        self._sample()
+        self._t = threading.Thread(target=self._run, daemon=True)
+        self._t.start()
+
+    def stop(self):
+        if self._h is None:
+            if self._smi is not None:
+                time.sleep(0.05)
+                self._smi.terminate()
+                out, _ = self._smi.communicate(timeout=10)
+                names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+                import datetime
+                rows = []
+                for line in out.strip().splitlines():
+                    f = [v.strip() for v in line.split(",")]
+                    if len(f) < 7 or not f[1].isdigit():
+                        continue
+                    try:
+                        ts = datetime.datetime.strptime(f[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                    except ValueError:
+                        ts = None
+                    rows.append((ts, f))
+                lo, hi = self.window
+                inside = [f for ts, f in rows if ts is None or lo - 0.05 <= ts <= hi + 0.05]
+                if not inside and rows:       # timed region shorter than one sample period
+                    inside = [min(rows, key=lambda r: abs((r[0] or lo) - (lo + hi) / 2))[1]]
+                for f in inside:
+                    self.samples.append(int(f[1]))
+                    self.max_mhz = int(f[2]) if f[2].isdigit() else self.max_mhz
+                    for n, v in zip(names, f[3:7]):
+                        if v.lower() == "active":
+                            self.reasons.add(n)
+            return
+        self._sample()
+        self._stop.set()
+        self._t.join()
+        lo, hi = self.window
+        inside = [r for r in self._raw if lo <= r[0] <= hi] or self._raw[-1:]
+        for _, mhz, r in inside:
+            self.samples.append(mhz)
+            for name, bit in self.REASONS.items():
+                if r & bit:
+                    self.reasons.add(name)
+
+    def summary(self):
+        if not self.samples:
+            return {"sm_mhz": None, "sm_max_mhz": self.max_mhz, "reasons": sorted(self.reasons),
+                    "samples": 0, "error": self.error}
+        return {"sm_mhz": statistics.median(self.samples), "sm_max_mhz": self.max_mhz,
+                "reasons": sorted(self.reasons), "samples": len(self.samples),
+                "source": "nvml" if self._h is not None else "nvidia-smi"}
+
+
+# ----------------------------------------------------------------- CPU oracle
+class _LazyExpert:
+    def __init__(self, t):
+        self.t, self._e, self._v = t, None, None
+
+    def __getitem__(self, e):
+        if self._e != e:
+            import numpy as np
+            self._v = self.t[e].float().cpu().numpy().astype(np.float64)
+            self._e = e
+        return self._v
+
+
+def oracle_call(inp, T_s):
+    """One oracle layer call on the first T_s tokens of the batch."""
+    import numpy as np
+    import oracle.moe_oracle as O
+
+    def h(t):
+        return None if t is None else t.float().cpu().numpy().astype(np.float64)
+
+    s = inp.shape
+    x = h(inp.x[:T_s])
+    W3 = _LazyExpert(inp.W3) if inp.W3 is not None else None
+    return O.moe_forward(x, h(inp.W_r), _LazyExpert(inp.W1), _LazyExpert(inp.W2), s.k, s.act,
+                         s.gate, W3=W3, logit_offset=h(inp.logit_offset), sel_bias=h(inp.sel_bias),
+                         capacity_factor=s.capacity_factor, alpha=s.alpha, Ws1=h(inp.Ws1),
+                         Ws3=h(inp.Ws3), Ws2=h(inp.Ws2))
+
+
+def blas_threads():
+    try:
+        from threadpoolctl import threadpool_info
+        n = [i.get("num_threads", 1) for i in threadpool_info() if i.get("user_api") == "blas"]
+        return max(n) if n else 1
+    except Exception:
+        return os.cpu_count() or 1
+
+
+def size_oracle_sample(inp, seconds):
+    """Tokens per oracle call so that one call takes about `seconds`."""
+    T = inp.shape.T
+    t_s = min(T, 16)
+    t0 = time.perf_counter()
+    oracle_call(inp, t_s)
+    dt = max(time.perf_counter() - t0, 1e-3)
+    return max(1, min(T, int(t_s * seconds / dt)))
+
+
+def cpu_baseline(inp, seconds):
+    T_s = size_oracle_sample(inp, seconds)
+    n, tot = 0, 0.0
+    while tot < seconds or n == 0:
+        t0 = time.perf_counter()
+        oracle_call(inp, T_s)
+        tot += time.perf_counter() - t0
+        n += 1
+    return {"value": round(n * T_s / tot, 2), "unit": "tokens/s", "cores": blas_threads(),
+            "kind": "oracle",
+            "sample": f"{n} oracle call(s) on the first {T_s} of {inp.shape.T} tokens "
+                      f"({tot:.1f} s of CPU time, float64 numpy)"}
+
+
+# ----------------------------------------------------------------- arms
+def workload_config(shape, extra=None):
+    c = {"workload": f"{shape.name} MoE layer", "T": shape.T, "d": shape.d, "E": shape.E,
+         "k": shape.k, "f": shape.f, "act": shape.act, "gate": shape.gate,
+         "capacity_factor": shape.capacity_factor or None, "n_shared": shape.n_shared,
+         "f_shared": shape.f_shared or None, "alpha": shape.alpha}
+    if extra:
+        c.update(extra)
+    return c
+
+
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    import torch
+    from sparse_mixture_experts_65_b300 import workloads as W
+
+    shape = W.get(args.workload)
+    inp = W.make_inputs(shape, "cpu")
+    steps, warm = args.steps, args.warmup
+    budget = 150.0                                # whole run, seconds
+    T_s = size_oracle_sample(inp, budget / (steps + warm))
+    for _ in range(warm):
+        oracle_call(inp, T_s)
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        oracle_call(inp, T_s)
+    dt = time.perf_counter() - t0
+    value = steps * T_s / dt
+    sample = f"each step: one oracle call on the first {T_s} of {shape.T} tokens"
+    line = {"impl": "reference", "metric": METRIC, "value": round(value, 3), "unit": "tokens/s",
+            "n_gpus": world, "steps": steps, "warmup": warm,
+            "ms_per_step": round(dt / steps * 1e3, 3), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": workload_config(shape, {"oracle_tokens_per_step": T_s}),
+            "cpu_baseline": {"value": round(value, 3), "unit": "tokens/s", "kind": "oracle",
+                             "cores": blas_threads(), "sample": sample},
+            "e2e": {"value": round(value, 3), "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def run_b300(args):
+    import torch
+    from sparse_mixture_experts_65_b300 import layer as L
+    from sparse_mixture_experts_65_b300 import workloads as W
+
+    rank, world, local = dist_env()
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA device")
+    torch.cuda.set_device(local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+
+    def barrier():
+        if dist is not None:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    shape = W.get(args.workload)
+    inp = W.make_inputs(shape, "cuda")
+    cfg = L.config_for(shape)
+    stream = torch.cuda.current_stream()
+    fwd = L.BoundForward(cfg, inp.x, inp.W_r, inp.W1, inp.W2, inp.W3, inp.logit_offset,
+                         inp.sel_bias, inp.Ws1, inp.Ws3, inp.Ws2, stream=stream)
+    K, Wm = args.steps, args.warmup
+    for _ in range(Wm):
+        fwd()
+    torch.cuda.synchronize()
+    assert L.check_status(fwd.workspace) == 0, "device status after warm-up"
+    kept = fwd.out.expert_counts.cpu().tolist()
+    acc, layer = accounting(shape, kept)
+
+    # per-stage events: MOE_NUM_STAGES + 1 per step
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(len(STAGES) + 1)]
+           for _ in range(K)]
+    arrs = [L.BoundForward.event_array(e, stream) for e in evs]
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(torch.cuda.current_device())
+    clocks.start()
+    for _ in range(Wm):
+        fwd()
+    barrier()
+    w0 = time.time()
+    start.record(stream)
+    for i in range(K):
+        fwd(arrs[i])
+    end.record(stream)
+    torch.cuda.synchronize()
+    w1 = time.time()
+    clocks.mark(w0, w1)
+    clocks.stop()
+    barrier()
+    ms_total = max_over_ranks(start.elapsed_time(end), dist, "cuda")
+    assert L.check_status(fwd.workspace) == 0, "device status after the timed region"
+    stage_ms = {s: statistics.fmean(evs[i][j].elapsed_time(evs[i][j + 1]) for i in range(K))
+                for j, s in enumerate(STAGES)}
+    ms_step = ms_total / K
+    value = world * shape.T * K / (ms_total / 1e3)
+
+    peaks, peak_kind = load_peaks()
+    dominant = max(STAGES, key=lambda s: stage_ms[s])
+    roof = roofline_for(dominant, acc, stage_ms[dominant], peaks, peak_kind)
+    roof["traffic"] = ncu_traffic(dominant, shape.name)
+    roof["share_of_step"] = round(stage_ms[dominant] / sum(stage_ms.values()), 4)
+    layer_sec = ms_step / 1e3
+    layer_roof = {
+        "hbm_frac": round(layer["bytes"] / layer_sec / 1e9 / peaks["hbm_gbs"], 4),
+        "tensor_frac_sustained": round(layer["flops"] / layer_sec / 1e12 /
+                                       peaks["bf16_tflops_sustained"], 4),
+        "bytes_per_step": layer["bytes"], "flops_per_step": layer["flops"],
+        "active_experts": layer["active_experts"], "kept_rows": layer["kept_rows"]}
+
+    e2e = None
+    if not args.no_e2e:
+        x_h = inp.x.cpu().pin_memory()
+        y_h = torch.empty_like(x_h).pin_memory()
+        aux_h = torch.empty(1, dtype=torch.float32).pin_memory()
+        hio = L.BoundHostIO(cfg, x_h, y_h, aux_h, inp.W_r, inp.W1, inp.W2, inp.W3,
+                            inp.logit_offset, inp.sel_bias, inp.Ws1, inp.Ws3, inp.Ws2,
+                            stream=stream)
+        for _ in range(Wm):
+            hio()
+        barrier()
+        s2, e2 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s2.record(stream)
+        for _ in range(K):
+            hio()
+        e2.record(stream)
+        torch.cuda.synchronize()
+        barrier()
+        ms_e2e = max_over_ranks(s2.elapsed_time(e2), dist, "cuda")
+        io = shape.T * shape.d * x_h.element_size()
+        e2e = {"value": round(world * shape.T * K / (ms_e2e / 1e3), 1), "unit": "tokens/s",
+               "h2d_bytes_per_step": io, "d2h_bytes_per_step": io + 4,
+               "ms_per_step": round(ms_e2e / K, 5), "api": "moe_forward_host_io"}
+        del hio, x_h, y_h
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(inp, args.cpu_seconds)
+
+    active_w = layer["active_weight_bytes"]
+    l2_note = (f"inputs larger than L2: {active_w / 1e6:.0f} MB of active expert weights "
+               f"stream every step (L2 {L2_BYTES / 1e6:.0f} MB)") if active_w > L2_BYTES else \
+        f"working set {active_w / 1e6:.0f} MB fits L2: numbers include L2 reuse across steps"
+    line = {"impl": "b300", "metric": METRIC, "value": round(value, 1), "unit": "tokens/s",
+            "n_gpus": world, "steps": K, "warmup": Wm, "ms_per_step": round(ms_step, 5),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16"
+            if shape.dtype == "bf16" else "f32",
+            "data": "synthetic (seeded; the layer shape and input distributions of the workload)",
+            "config": workload_config(shape, {"l2": l2_note,
+                                              "parallelism": f"replicas x{world}"}),
+            "roofline": roof, "layer_roofline": layer_roof,
+            "stages_ms": {s: round(v, 5) for s, v in stage_ms.items()},
+            "cpu_baseline": cpu, "e2e": e2e,
+            "gpu_launches": K * L.launch_count(cfg), "clocks": clocks.summary(),
+            "source_sha": source_sha()}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_b300(args)
+
+
+if __name__ == "__main__":
+    main()

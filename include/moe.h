@@ -46,8 +46,14 @@
  *   - Pointers to tensors must be 16-byte aligned.  On the bf16 path d, f
  *     and f_s must be multiples of 8; on the float32 path, multiples of 4.
  *   - The workspace is caller-owned device memory of at least
- *     moe_workspace_size() bytes, 256-byte aligned.  Concurrent calls on
- *     different streams need separate workspaces.
+ *     moe_workspace_size() bytes, 256-byte aligned.  Its first 4096 bytes
+ *     hold the device status word and the counters the kernels use to find
+ *     the last block of a reduction: zero them once when the workspace is
+ *     created; every call leaves them valid for the next.  Concurrent calls
+ *     on different streams need separate workspaces.
+ *   - Kernels are launched with programmatic dependent launch: each may begin
+ *     its prologue while the previous kernel in the stream finishes, and waits
+ *     for that kernel's results before reading them.  Stream order is kept.
  */
 #ifndef MOE_H_
 #define MOE_H_
@@ -162,6 +168,16 @@ int moe_route(const moe_config* cfg,
               void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * moe_router_scores -- stage 1 alone: scores [T, E] float32 (device) gets the
+ * router logits s = x W_r^T (+ logit_offset), computed exactly as
+ * moe_forward computes them (same kernels, same summation order).  Needs
+ * moe_route_workspace_size() bytes.  x and W_r must be 16-byte aligned.
+ */
+int moe_router_scores(const moe_config* cfg, const void* x, const void* W_r,
+                      const float* logit_offset, float* scores,
+                      void* workspace, size_t workspace_bytes, void* stream);
+
+/*
  * moe_forward_host_io -- moe_forward with the activations in HOST memory:
  * x_host [T, d] is copied to the device, the layer runs, and y_host [T, d]
  * and aux_loss_host [1] are copied back, all enqueued on `stream` (pinned
@@ -194,13 +210,14 @@ const char* moe_error_string(int code);
 
 /* Stages in the order moe_forward enqueues them. */
 enum {
-  MOE_STAGE_ROUTER = 0,   /* router scores + top-k + gates + block statistics */
-  MOE_STAGE_SCAN = 1,     /* counts, capacity, offsets, tile schedule, f, P, L */
+  MOE_STAGE_ROUTER = 0,   /* router logits (float32 GEMM) */
+  MOE_STAGE_TOPK = 1,     /* top-k, gates, router distribution, expert counts, and the
+                             capacity scan: offsets, tile schedule, f, P, L */
   MOE_STAGE_PERMUTE = 2,  /* slot positions and the copy into expert order */
   MOE_STAGE_UP = 3,       /* expert up projection (+ activation / SwiGLU) */
   MOE_STAGE_DOWN = 4,     /* expert down projection */
   MOE_STAGE_COMBINE = 5,  /* gate-weighted combine (+ shared expert) */
-  MOE_NUM_STAGES = 6
+  MOE_NUM_STAGES = 6      /* one kernel per stage */
 };
 
 /*

@@ -24,12 +24,13 @@ MOE_F32, MOE_BF16 = 0, 1
 MOE_ACT_GELU, MOE_ACT_RELU, MOE_ACT_SWIGLU = 0, 1, 2
 MOE_GATE_SOFTMAX_TOPK, MOE_GATE_SIGMOID_RENORM, MOE_GATE_SOFTMAX_FULL = 0, 1, 2
 MOE_NUM_STAGES = 6
-STAGE_NAMES = ("router", "scan", "permute", "up", "down", "combine")
+STAGE_NAMES = ("router", "topk", "permute", "up", "down", "combine")
 
 EXPORTS = (
     "moe_workspace_size", "moe_forward", "moe_route_workspace_size", "moe_route",
     "moe_host_io_workspace_size", "moe_forward_host_io", "moe_check_status",
     "moe_error_string", "moe_forward_timed", "moe_launch_count", "moe_selftest_wait_timeout",
+    "moe_router_scores",
 )
 
 
@@ -77,6 +78,8 @@ def lib() -> ctypes.CDLL:
         L.moe_route.restype = ctypes.c_int
         L.moe_forward_host_io.argtypes = [cfgp, P, P, P, P, P, P, P, P, P, P, P, P, P, SZ, P]
         L.moe_forward_host_io.restype = ctypes.c_int
+        L.moe_router_scores.argtypes = [cfgp, P, P, P, P, P, SZ, P]
+        L.moe_router_scores.restype = ctypes.c_int
         L.moe_check_status.argtypes = [P, P]
         L.moe_check_status.restype = ctypes.c_int
         L.moe_error_string.argtypes = [ctypes.c_int]

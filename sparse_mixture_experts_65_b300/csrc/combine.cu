@@ -7,6 +7,7 @@
 // output is the gate-weighted sum over the chosen experts only; dropped
 // slots contribute nothing (ch. 11 § Expert capacity and dropped tokens).
 #include "common.cuh"
+#include "launch.cuh"
 #include "moe_internal.h"
 
 namespace moe {
@@ -37,6 +38,8 @@ __global__ void __launch_bounds__(kThreads) combine_kernel(const CombineArgs a) 
   __shared__ int rows[kMaxK];
   __shared__ float gates[kMaxK];
   const int t = blockIdx.x;
+  pdl_wait();
+  pdl_trigger();
   if (threadIdx.x < a.k) {
     rows[threadIdx.x] = a.key_row[(size_t)t * a.k + threadIdx.x];
     gates[threadIdx.x] = a.topk_w[(size_t)t * a.k + threadIdx.x];
@@ -73,10 +76,8 @@ cudaError_t launch_combine(const Plan& p, const float* topk_w, void* y, void* ws
   a.d = p.cfg.d;
   a.k = p.cfg.k;
   if (p.cfg.dtype == MOE_BF16)
-    combine_kernel<__nv_bfloat16><<<p.cfg.T, kThreads, 0, st>>>(a);
-  else
-    combine_kernel<float><<<p.cfg.T, kThreads, 0, st>>>(a);
-  return cudaGetLastError();
+    return launch_pdl(combine_kernel<__nv_bfloat16>, dim3(p.cfg.T), dim3(kThreads), 0, st, a);
+  return launch_pdl(combine_kernel<float>, dim3(p.cfg.T), dim3(kThreads), 0, st, a);
 }
 
 }  // namespace moe

@@ -16,6 +16,7 @@
 #include <cmath>
 
 #include "common.cuh"
+#include "launch.cuh"
 #include "moe_internal.h"
 
 namespace moe {
@@ -53,6 +54,8 @@ __global__ void __launch_bounds__(kThreads) simt_grouped_gemm(const SimtArgs a) 
   __shared__ __align__(16) float As[SB_K][SB_M + 4];
   __shared__ __align__(16) float Bs[SB_K][SB_N + 4];
   __shared__ __align__(16) float Cs[SB_K][SB_N + 4];   // second B operand (SwiGLU up)
+  pdl_wait();
+  pdl_trigger();
   const int nseg = a.E + a.has_shared;
   const int total = a.tp[nseg];
   const int tx = threadIdx.x % 16, ty = threadIdx.x / 16;
@@ -172,8 +175,7 @@ cudaError_t launch_experts_simt(const Plan& p, const void* x, const void* W1, co
   u.K_sh = p.cfg.d;
   u.act = simt_act(p.cfg.act);
   u.act_sh = SIMT_SWIGLU;
-  simt_grouped_gemm<<<grid_up, kThreads, 0, st>>>(u);
-  cudaError_t e = cudaGetLastError();
+  cudaError_t e = launch_pdl(simt_grouped_gemm, dim3(grid_up), dim3(kThreads), 0, st, u);
   if (e != cudaSuccess) return e;
   if (mid_event) {
     e = cudaEventRecord(mid_event, st);
@@ -200,8 +202,7 @@ cudaError_t launch_experts_simt(const Plan& p, const void* x, const void* W1, co
   dn.K_sh = p.cfg.f_shared;
   dn.act = SIMT_NONE;
   dn.act_sh = SIMT_NONE;
-  simt_grouped_gemm<<<grid_dn, kThreads, 0, st>>>(dn);
-  return cudaGetLastError();
+  return launch_pdl(simt_grouped_gemm, dim3(grid_dn), dim3(kThreads), 0, st, dn);
 }
 
 }  // namespace moe

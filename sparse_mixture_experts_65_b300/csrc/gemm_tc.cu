@@ -26,10 +26,13 @@
 // Every wait is bounded: on a timeout the kernel records a status bit, tells
 // the other roles to stop, drains its own copies and MMAs, frees tensor
 // memory and returns.
+#include <atomic>
 #include <cstdio>
+#include <cstring>
 #include <mutex>
 
 #include "common.cuh"
+#include "launch.cuh"
 #include "moe_internal.h"
 #include "ptx.cuh"
 
@@ -41,6 +44,10 @@ struct TcArgs {
   const int* tp;          // [E+2] tile prefix: routed segments, then the shared one
   const int* seg_start;   // [E] first row of each routed segment
   const int* mtiles;      // [E+1] M tiles per segment (index E: shared)
+  const int* kept;        // [E] rows of each routed segment (padding rows follow)
+  int rows_sh;            // rows of the shared segment (T)
+  int static_mt;          // > 0: one dense segment of static_mt M tiles (no device schedule)
+  int static_total;       // its tile count
   int E, has_shared;
   int N, K;               // routed output columns / reduction length
   int N_sh, K_sh;         // shared segment
@@ -81,11 +88,24 @@ struct TileInfo {
   int seg;
   bool shared;
   int a_row;    // first A row (and output row)
+  int row_end;  // rows at or past this index are segment padding: not stored
   int n0;       // first output column
   int K, N;
 };
 
 __device__ __forceinline__ TileInfo decode_tile(const TcArgs& a, int tile, int bnh) {
+  if (a.static_mt > 0) {   // dense GEMM: rows [0, rows_sh), tiles N-major
+    TileInfo ti;
+    ti.seg = 0;
+    ti.shared = false;
+    const int n_t = tile / a.static_mt, m_t = tile - n_t * a.static_mt;
+    ti.a_row = m_t * kTcBM;
+    ti.row_end = a.rows_sh;
+    ti.n0 = n_t * bnh;
+    ti.K = a.K;
+    ti.N = a.N;
+    return ti;
+  }
   const int nseg = a.E + a.has_shared;
   int lo = 0, hi = nseg - 1;
   while (lo < hi) {
@@ -98,7 +118,9 @@ __device__ __forceinline__ TileInfo decode_tile(const TcArgs& a, int tile, int b
   const int local = tile - __ldg(a.tp + lo);
   const int mt = __ldg(a.mtiles + lo);
   const int n_t = local / mt, m_t = local - n_t * mt;
-  ti.a_row = (ti.shared ? 0 : __ldg(a.seg_start + lo)) + m_t * kTcBM;
+  const int seg0 = ti.shared ? 0 : __ldg(a.seg_start + lo);
+  ti.a_row = seg0 + m_t * kTcBM;
+  ti.row_end = ti.shared ? a.rows_sh : seg0 + __ldg(a.kept + lo);
   ti.n0 = n_t * bnh;
   ti.K = ti.shared ? a.K_sh : a.K;
   ti.N = ti.shared ? a.N_sh : a.N;
@@ -163,7 +185,9 @@ tc_grouped_gemm(const __grid_constant__ CUtensorMap mA, const __grid_constant__ 
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
-  const int total = __ldg(a.tp + a.E + a.has_shared);
+  pdl_wait();      // everything above ran while the previous kernel finished
+  pdl_trigger();
+  const int total = a.static_mt > 0 ? a.static_total : __ldg(a.tp + a.E + a.has_shared);
 
   auto give_up = [&]() {
     atomicOr(a.status, STATUS_TIMEOUT_GEMM);
@@ -273,6 +297,7 @@ tc_grouped_gemm(const __grid_constant__ CUtensorMap mA, const __grid_constant__ 
       tc_fence_after();
       const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + ab * C::MMA_N;
       const size_t orow = static_cast<size_t>(ti.a_row + row_in_tile);
+      const bool row_ok = ti.a_row + row_in_tile < ti.row_end;
 #pragma unroll 1
       for (int c = 0; c < BNH; c += 32) {
         uint32_t r0[32];
@@ -285,7 +310,8 @@ tc_grouped_gemm(const __grid_constant__ CUtensorMap mA, const __grid_constant__ 
           float* out = static_cast<float*>(ti.shared ? a.out_sh : a.out);
           const int ld = ti.shared ? a.ld_out_sh : a.ld_out;
           float* dst = out + orow * ld + col;
-          if (col + 32 <= ti.N) {
+          if (!row_ok) {
+          } else if (col + 32 <= ti.N) {
 #pragma unroll
             for (int v = 0; v < 8; ++v) {
               float4 f4 = make_float4(__uint_as_float(r0[4 * v]), __uint_as_float(r0[4 * v + 1]),
@@ -319,7 +345,8 @@ tc_grouped_gemm(const __grid_constant__ CUtensorMap mA, const __grid_constant__ 
             __nv_bfloat162 b2 = __floats2bfloat162_rn(v0, v1);
             pk[i] = *reinterpret_cast<uint32_t*>(&b2);
           }
-          if (col + 32 <= ti.N) {
+          if (!row_ok) {
+          } else if (col + 32 <= ti.N) {
 #pragma unroll
             for (int v = 0; v < 4; ++v)
               reinterpret_cast<uint4*>(dst)[v] =
@@ -401,14 +428,28 @@ struct TcMaps {
   CUtensorMap A, A_sh, B0, B1, B0_sh, B1_sh;
 };
 
+// Raise the dynamic shared-memory limit of a kernel once per device.
+template <typename K>
+static cudaError_t smem_attr_once(K kern, int bytes, std::atomic<uint64_t>& done) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const uint64_t bit = 1ull << (dev & 63);
+  if (done.load(std::memory_order_acquire) & bit) return cudaSuccess;
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess) done.fetch_or(bit, std::memory_order_release);
+  return e;
+}
+
 template <int BNH, bool DUAL, int EPI>
 static cudaError_t run_tc(const TcMaps& m, const TcArgs& a, int grid, cudaStream_t st) {
   using C = TcCfg<BNH, DUAL, EPI>;
+  static std::atomic<uint64_t> attr_done{0};
   auto kern = tc_grouped_gemm<BNH, DUAL, EPI>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+  cudaError_t e = smem_attr_once(kern, C::SMEM, attr_done);
   if (e != cudaSuccess) return e;
-  kern<<<grid, 192, C::SMEM, st>>>(m.A, m.A_sh, m.B0, m.B1, m.B0_sh, m.B1_sh, a);
-  return cudaGetLastError();
+  return launch_pdl(kern, dim3(grid), dim3(192), C::SMEM, st, m.A, m.A_sh, m.B0, m.B1, m.B0_sh,
+                    m.B1_sh, a);
 }
 
 static cudaError_t dispatch_up(int bn, int act, const TcMaps& m, const TcArgs& a, int grid,
@@ -484,6 +525,10 @@ cudaError_t launch_experts_tc(const Plan& p, const void* x, const void* W1, cons
   au.tp = meta.tp_up;
   au.seg_start = meta.seg_start;
   au.mtiles = meta.mtiles;
+  au.kept = meta.kept;
+  au.rows_sh = c.T;
+  au.static_mt = 0;
+  au.static_total = 0;
   au.E = c.E;
   au.has_shared = sh ? 1 : 0;
   au.N = c.f;
@@ -530,6 +575,36 @@ cudaError_t launch_experts_tc(const Plan& p, const void* x, const void* W1, cons
   ad.ld_out_sh = sh ? c.d : 0;
   const int grid_dn = p.max_tiles_dn < p.num_sms ? p.max_tiles_dn : p.num_sms;
   return dispatch_down(p.dn_bn, md, ad, grid_dn, st);
+}
+
+// ---------------------------------------------------------------- router
+// Router logits s = x W_r^T on the tensor cores: bf16 operands (their products
+// are exact), float32 accumulation in tensor memory, float32 output [T][E].
+constexpr int kRouterTcBN = 64;
+
+cudaError_t launch_router_tc(const Plan& p, const void* x, const void* W_r, float* scores,
+                             uint32_t* status, cudaStream_t st) {
+  const moe_config& c = p.cfg;
+  TcMaps m;
+  bool ok = encode_2d(&m.A, x, c.T, c.d, kTcBM);
+  ok = ok && encode_3d(&m.B0, W_r, 1, c.E, c.d, kRouterTcBN);
+  if (!ok) return cudaErrorInvalidValue;
+  m.A_sh = m.A;
+  m.B1 = m.B0_sh = m.B1_sh = m.B0;
+  TcArgs a;
+  std::memset(&a, 0, sizeof(a));
+  a.E = 1;
+  a.N = c.E;
+  a.K = c.d;
+  a.out = scores;
+  a.ld_out = c.E;
+  a.rows_sh = c.T;
+  a.static_mt = (c.T + kTcBM - 1) / kTcBM;
+  a.static_total = a.static_mt * ((c.E + kRouterTcBN - 1) / kRouterTcBN);
+  a.status = status;
+  a.timeout_ns = kGemmTimeoutNs;
+  const int grid = a.static_total < p.num_sms ? a.static_total : p.num_sms;
+  return run_tc<kRouterTcBN, false, EPI_F32>(m, a, grid, st);
 }
 
 // ---------------------------------------------------------------- self-test

@@ -1,6 +1,7 @@
 // moe_api.cu -- the C ABI declared in include/moe.h: argument checks, the
 // per-call plan (workspace layout, routing blocks, GEMM tiling) and the
 // enqueueing of the stage kernels on the caller's stream.
+#include <atomic>
 #include <climits>
 #include <cmath>
 #include <cstdlib>
@@ -70,18 +71,61 @@ int make_plan(const moe_config* cfg, WsKind kind, Plan* p, int num_sms) {
   } else {
     P.capacity = INT_MAX;
   }
-  P.E_pad = c.E <= 32 ? 32 : c.E <= 64 ? 64 : c.E <= 128 ? 128 : c.E <= 256 ? 256 : 512;
-  const int EC = P.E_pad < 256 ? P.E_pad : 256;
-  P.BT = (kThreads / EC) * kRouterRT;
-  P.KC = P.E_pad > 256 ? 16 : 32;
+  {
+    // routing blocks: 16 tokens per pass (one per warp), enough passes that
+    // the batch needs about kRouteMaxBlocks blocks, at most kRouteMaxBT tokens
+    const int passes = ceil_div(c.T, kRouteTokensPerPass * kRouteMaxBlocks);
+    const int bt = kRouteTokensPerPass * (passes < 1 ? 1 : passes);
+    P.BT = bt > kRouteMaxBT ? kRouteMaxBT : bt;
+  }
   P.nblk = ceil_div(c.T, P.BT);
+  P.num_sms = num_sms > 0 ? num_sms : 148;
+  // router GEMM: 128-token x (16*TN)-expert tiles, K split until >= 2 blocks per SM
+  P.sc_tn = c.E > 32 ? 4 : 2;
+  P.sc_mblocks = ceil_div(c.T, 128);
+  P.sc_nblocks = ceil_div(c.E, 16 * P.sc_tn);
+  {
+    // choose the split with the best wave efficiency over 2 blocks per SM
+    // (ties: fewer splits), each split at least 128 wide
+    const int tiles = P.sc_mblocks * P.sc_nblocks;
+    const int max_split = c.d / 128 > 1 ? c.d / 128 : 1;
+    const int slots = 2 * 148;    // fixed, so that the workspace layout never depends on the GPU
+    int S = 1;
+    double best = -1.0;
+    for (int s = 1; s <= max_split && tiles > 0; ++s) {
+      const int blocks = tiles * s;
+      const int waves = ceil_div(blocks, slots);
+      double eff = (double)blocks / ((double)waves * slots);
+      if (blocks < slots) eff *= 0.999;   // a partial single wave: prefer more work per block
+      if (eff > best + 1e-9) {
+        best = eff;
+        S = s;
+      }
+      if (waves > 4) break;
+    }
+    if (tiles > kMaxTileCounters) S = 1;   // plenty of tiles already; no counters needed
+    P.sc_ksplit = ceil_div(ceil_div(c.d, S), 32) * 32;
+    P.sc_splits = ceil_div(c.d, P.sc_ksplit);
+  }
+  // The router runs on float32 FMA: its logits stay within 1e-6 of the exact
+  // values, well inside the 1e-5 band in which near-tied experts may swap.
+  // MOE_ROUTER=tc (bf16 layers only) moves it to the tensor cores, which are
+  // ~30x faster but whose float32 accumulation errs by up to ~4e-5 on a
+  // 7168-wide router; it is an experiment switch, never the default.
+  {
+    const char* r = std::getenv("MOE_ROUTER");
+    P.router_tc = c.dtype == MOE_BF16 && r && std::strcmp(r, "tc") == 0;
+    if (P.router_tc) {
+      P.sc_splits = 1;
+      P.sc_ksplit = c.d;
+    }
+  }
   P.tc = c.dtype == MOE_BF16;
   P.bm = P.tc ? kTcBM : kSimtBM;
   const long long nonempty = Tk < c.E ? Tk : c.E;
   P.R_cap = static_cast<int>(align_up((size_t)(Tk + nonempty * (P.bm - 1)), (size_t)P.bm));
   P.T_pad = static_cast<int>(align_up((size_t)c.T, (size_t)kSegAlign));
   P.mt_sh = c.n_shared ? ceil_div(c.T, P.bm) : 0;
-  P.num_sms = num_sms > 0 ? num_sms : 148;
 
   if (P.tc) {
     long long est = nonempty + Tk / P.bm;
@@ -125,7 +169,9 @@ int make_plan(const moe_config* cfg, WsKind kind, Plan* p, int num_sms) {
     return at;
   };
   const size_t E = c.E;
-  L.status = take(256);
+  L.status = take(kWsHeaderBytes);
+  L.scores = take(sizeof(float) * (size_t)c.T * E);
+  L.score_parts = take(P.sc_splits > 1 ? sizeof(float) * (size_t)P.sc_splits * c.T * E : 0);
   L.blk_cnt = take(sizeof(int) * (size_t)P.nblk * E);
   L.blk_prob = take(sizeof(float) * (size_t)P.nblk * E);
   L.meta = take(sizeof(int) * (E + (E + 1) * 3 + (E + 2) * 2));
@@ -152,16 +198,29 @@ int make_plan(const moe_config* cfg, WsKind kind, Plan* p, int num_sms) {
   return MOE_OK;
 }
 
+// Per-device facts, read once per device (the values never change while the
+// process runs).  0 = not read yet, else the SM count or -1 for "not sm_103".
+static std::atomic<int> g_dev_sms[64];
+
 static int device_sms(int* sms) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return MOE_ERR_CUDA;
+  if (dev >= 0 && dev < 64) {
+    const int v = g_dev_sms[dev].load(std::memory_order_relaxed);
+    if (v > 0) {
+      *sms = v;
+      return MOE_OK;
+    }
+    if (v < 0) return MOE_ERR_DEVICE;
+  }
   int major = 0, minor = 0;
   if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
       cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
       cudaDeviceGetAttribute(sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
     return MOE_ERR_CUDA;
-  if (major != 10 || minor != 3) return MOE_ERR_DEVICE;
-  return MOE_OK;
+  const bool ok = major == 10 && minor == 3;
+  if (dev >= 0 && dev < 64) g_dev_sms[dev].store(ok ? *sms : -1, std::memory_order_relaxed);
+  return ok ? MOE_OK : MOE_ERR_DEVICE;
 }
 
 static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -185,7 +244,7 @@ static int check_tensors(const moe_config& c, const Tensors& t, bool route_only)
   const bool empty = c.T == 0;
   if (!t.W_r || !t.expert_counts || !t.aux_loss) return MOE_ERR_ARG;
   if (!empty && (!t.x || !t.topk_idx || !t.topk_w)) return MOE_ERR_ARG;
-  if (!aligned16(t.x) || !aligned4(t.W_r) || !aligned4(t.topk_idx) || !aligned4(t.topk_w))
+  if (!aligned16(t.x) || !aligned16(t.W_r) || !aligned4(t.topk_idx) || !aligned4(t.topk_w))
     return MOE_ERR_ARG;
   if (route_only) return MOE_OK;
   if (!t.W1 || !t.W2 || (!empty && !t.y)) return MOE_ERR_ARG;
@@ -241,17 +300,18 @@ static int forward_impl(const moe_config* cfg, const Tensors& t, void* ws, size_
   int sms = 0;
   rc = device_sms(&sms);
   if (rc != MOE_OK) return rc;
-  rc = make_plan(cfg, kind, &p, sms);
-  if (rc != MOE_OK) return rc;
+  if (sms != p.num_sms) {        // tiling depends on the SM count; the layout does not
+    rc = make_plan(cfg, kind, &p, sms);
+    if (rc != MOE_OK) return rc;
+  }
   const moe_config& c = *cfg;
   if (c.T == 0) return zero_outputs(c, t, st);
 
   if ((rc = record(events, MOE_STAGE_ROUTER, st)) != MOE_OK) return rc;
+  const ScanOutputs so{t.expert_counts, t.aux_loss, t.routed_counts, t.offsets, t.f_out, t.P_out};
+  cudaEvent_t topk_ev = events ? static_cast<cudaEvent_t>(events[MOE_STAGE_TOPK]) : nullptr;
   MOE_TRY_CUDA(launch_router(p, t.x, t.W_r, t.logit_offset, t.sel_bias, t.topk_idx, t.topk_w, ws,
-                             st));
-  if ((rc = record(events, MOE_STAGE_SCAN, st)) != MOE_OK) return rc;
-  MOE_TRY_CUDA(launch_scan(p, ws, t.expert_counts, t.aux_loss, t.routed_counts, t.offsets,
-                           t.f_out, t.P_out, st));
+                             so, st, topk_ev));
   if ((rc = record(events, MOE_STAGE_PERMUTE, st)) != MOE_OK) return rc;
   MOE_TRY_CUDA(launch_permute(p, t.x, t.topk_idx, t.slot_pos, !route_only, ws, st));
   if (route_only) return MOE_OK;
@@ -335,6 +395,27 @@ int moe_route(const moe_config* cfg, const void* x, const void* W_r, const float
                       nullptr, true, WsKind::Route);
 }
 
+int moe_router_scores(const moe_config* cfg, const void* x, const void* W_r,
+                      const float* logit_offset, float* scores, void* workspace,
+                      size_t workspace_bytes, void* stream) {
+  if (!cfg) return MOE_ERR_ARG;
+  Plan p;
+  int rc = make_plan(cfg, WsKind::Route, &p);
+  if (rc != MOE_OK) return rc;
+  if (cfg->T > 0 && (!x || !W_r || !scores || !aligned16(x) || !aligned16(W_r)))
+    return MOE_ERR_ARG;
+  rc = check_workspace(p, workspace, workspace_bytes);
+  if (rc != MOE_OK) return rc;
+  int sms = 0;
+  rc = device_sms(&sms);
+  if (rc != MOE_OK) return rc;
+  if (sms != p.num_sms && (rc = make_plan(cfg, WsKind::Route, &p, sms)) != MOE_OK) return rc;
+  if (cfg->T == 0) return MOE_OK;
+  MOE_TRY_CUDA(launch_router_scores(p, x, W_r, logit_offset, scores, workspace,
+                                    static_cast<cudaStream_t>(stream)));
+  return MOE_OK;
+}
+
 int moe_forward_host_io(const moe_config* cfg, const void* x_host, const void* W_r,
                         const float* logit_offset, const float* sel_bias, const void* W1,
                         const void* W3, const void* W2, const void* Ws1, const void* Ws3,
@@ -396,7 +477,7 @@ int moe_launch_count(const moe_config* cfg, int32_t* launches) {
   Plan p;
   const int rc = make_plan(cfg, WsKind::Forward, &p);
   if (rc != MOE_OK) return rc;
-  *launches = cfg->T == 0 ? 0 : MOE_NUM_STAGES;
+  *launches = cfg->T == 0 ? 0 : MOE_NUM_STAGES;   // one kernel per stage
   return MOE_OK;
 }
 

@@ -11,17 +11,27 @@
 namespace moe {
 
 constexpr int kThreads = 256;        // block size of the SIMT kernels
-constexpr int kRouterRT = 8;         // tokens per thread in the router GEMM
+constexpr int kRouteTokensPerPass = 16;   // tokens a top-k block handles at once (one per warp)
+constexpr int kRouteMaxBlocks = 128;      // routing blocks are sized to stay near this count
+constexpr int kRouteMaxBT = 256;
 constexpr int kMaxE = 512;
 constexpr int kMaxK = 32;
 constexpr int kSegAlign = 128;       // expert segments start on multiples of this row
 constexpr int kTcBM = 128;           // rows per tensor-core tile
 constexpr int kSimtBM = 64;          // rows per SIMT tile (fp32 path)
 constexpr int kSimtBN = 64;
+// Workspace header (zeroed once by the caller): status word at 0, routing
+// block-completion counter at 16, router split-reduction tile counters from
+// kTileCounterOffset on.
+constexpr int kWsHeaderBytes = 4096;
+constexpr int kTileCounterOffset = 256;
+constexpr int kMaxTileCounters = (kWsHeaderBytes - kTileCounterOffset) / 4;
 
 // Workspace regions, all 256-byte aligned.  Offsets in bytes.
 struct WsLayout {
   size_t status;      // uint32 status word (+ padding)
+  size_t scores;      // float  [T][E]     router logits
+  size_t score_parts; // float  [S][T][E]  split partial router logits (S > 1)
   size_t blk_cnt;     // int32  [nblk][E]  per-block expert histogram, then its exclusive scan
   size_t blk_prob;    // float  [nblk][E]  per-block sums of the router distribution
   size_t meta;        // int32  kept[E] | offsets[E+1] | seg_start[E+1] | mtiles[E+1]
@@ -41,10 +51,11 @@ struct Plan {
   moe_config cfg;
   int elem;           // bytes per element of x / weights / y
   int capacity;       // INT32_MAX when unlimited
-  int E_pad;          // E rounded up to 32
   int BT;             // tokens per routing block
-  int KC;             // router K chunk
   int nblk;           // routing blocks
+  bool router_tc;     // router logits on the tensor cores (bf16 path, large T)
+  int sc_tn;          // router GEMM: experts per thread (2 or 4)
+  int sc_mblocks, sc_nblocks, sc_splits, sc_ksplit;   // router GEMM grid and K split
   int bm;             // rows per GEMM tile (128 tensor core, 64 SIMT)
   int R_cap;          // rows reserved for the expert-ordered buffers
   int T_pad;          // T rounded up to kSegAlign
@@ -76,12 +87,24 @@ struct Meta {
 Meta meta_ptrs(const Plan& p, void* ws);
 
 // ---- launchers (return a cudaError_t of the launch) ----------------------
+// Caller-visible outputs of the capacity scan.
+struct ScanOutputs {
+  int32_t* expert_counts;
+  float* aux_loss;
+  int32_t* routed_counts;
+  int32_t* offsets;
+  float* f_out;
+  float* P_out;
+};
+
 cudaError_t launch_router(const Plan& p, const void* x, const void* W_r, const float* logit_offset,
                           const float* sel_bias, int32_t* topk_idx, float* topk_w, void* ws,
-                          cudaStream_t st);
-cudaError_t launch_scan(const Plan& p, void* ws, int32_t* expert_counts, float* aux_loss,
-                        int32_t* routed_counts, int32_t* offsets, float* f_out, float* P_out,
-                        cudaStream_t st);
+                          const ScanOutputs& so, cudaStream_t st, cudaEvent_t mid_event);
+cudaError_t launch_router_tc(const Plan& p, const void* x, const void* W_r, float* scores,
+                             uint32_t* status, cudaStream_t st);
+cudaError_t launch_router_scores(const Plan& p, const void* x, const void* W_r,
+                                 const float* logit_offset, float* out, void* ws,
+                                 cudaStream_t st);
 cudaError_t launch_permute(const Plan& p, const void* x, const int32_t* topk_idx,
                            int32_t* slot_pos, bool copy_rows, void* ws, cudaStream_t st);
 cudaError_t launch_experts_tc(const Plan& p, const void* x, const void* W1, const void* W3,

@@ -1,5 +1,6 @@
-// route.cu -- stage 3 (capacity and drops), stage 4 (permutation into
-// expert-contiguous order) and the balance statistics of stage 6.
+// route.cu -- stage 4: positions of the kept assignments and the permutation
+// of token rows into expert-contiguous order (the capacity scan that feeds it
+// runs at the end of the top-k kernel, see route_scan.cuh).
 //
 // "Mixture of Experts" (llm-tutorial ch. 11) § Expert capacity and dropped
 // tokens, and "Mixture of experts" (inside-the-model guide) § Auxiliary loss:
@@ -17,95 +18,10 @@
 #include <climits>
 
 #include "common.cuh"
+#include "launch.cuh"
 #include "moe_internal.h"
 
 namespace moe {
-
-struct ScanArgs {
-  int* blk_cnt;          // [nblk][E] in: histogram; out: exclusive scan over blocks
-  const float* blk_prob; // [nblk][E]
-  Meta m;
-  int nblk, E, T, k, capacity, bm;
-  int nt_up, nt_dn, nt_up_sh, nt_dn_sh, mt_sh, has_shared;
-  float alpha;
-  int32_t* expert_counts;
-  float* aux_loss;
-  int32_t* routed_counts;
-  int32_t* offsets_out;
-  float* f_out;
-  float* P_out;
-};
-
-// One block of 512 threads; thread e owns expert e.
-__global__ void __launch_bounds__(512) scan_kernel(const ScanArgs a) {
-  __shared__ int scratch[33];
-  __shared__ double red[512];
-  const int e = threadIdx.x;
-  int routed = 0, kept = 0, mt = 0;
-  float P = 0.f, fr = 0.f;
-  if (e < a.E) {
-    int* col = a.blk_cnt + e;
-    int b = 0;
-    for (; b + 4 <= a.nblk; b += 4) {
-      const int c0 = col[(size_t)(b + 0) * a.E], c1 = col[(size_t)(b + 1) * a.E];
-      const int c2 = col[(size_t)(b + 2) * a.E], c3 = col[(size_t)(b + 3) * a.E];
-      col[(size_t)(b + 0) * a.E] = routed;
-      col[(size_t)(b + 1) * a.E] = routed + c0;
-      col[(size_t)(b + 2) * a.E] = routed + c0 + c1;
-      col[(size_t)(b + 3) * a.E] = routed + c0 + c1 + c2;
-      routed += c0 + c1 + c2 + c3;
-    }
-    for (; b < a.nblk; ++b) {
-      const int c = col[(size_t)b * a.E];
-      col[(size_t)b * a.E] = routed;
-      routed += c;
-    }
-    float ps = 0.f;
-    for (int bb = 0; bb < a.nblk; ++bb) ps += a.blk_prob[(size_t)bb * a.E + e];
-    kept = routed < a.capacity ? routed : a.capacity;
-    mt = (kept + a.bm - 1) / a.bm;
-    P = a.T > 0 ? ps / (float)a.T : 0.f;
-    fr = a.T > 0 ? (float)routed / (float)(a.T * a.k) : 0.f;
-  }
-  int tot_kept, tot_mt, tot_up, tot_dn;
-  const int ex_kept = block_exclusive_scan(kept, scratch, &tot_kept);
-  const int ex_mt = block_exclusive_scan(mt, scratch, &tot_mt);
-  const int ex_up = block_exclusive_scan(mt * a.nt_up, scratch, &tot_up);
-  const int ex_dn = block_exclusive_scan(mt * a.nt_dn, scratch, &tot_dn);
-  if (e < a.E) {
-    a.m.kept[e] = kept;
-    a.m.offsets[e] = ex_kept;
-    a.m.seg_start[e] = ex_mt * a.bm;
-    a.m.mtiles[e] = mt;
-    a.m.tp_up[e] = ex_up;
-    a.m.tp_dn[e] = ex_dn;
-    a.expert_counts[e] = kept;
-    if (a.routed_counts) a.routed_counts[e] = routed;
-    if (a.offsets_out) a.offsets_out[e] = ex_kept;
-    if (a.f_out) a.f_out[e] = fr;
-    if (a.P_out) a.P_out[e] = P;
-  }
-  if (e == 0) {
-    const int sh_up = a.has_shared ? a.mt_sh * a.nt_up_sh : 0;
-    const int sh_dn = a.has_shared ? a.mt_sh * a.nt_dn_sh : 0;
-    a.m.offsets[a.E] = tot_kept;
-    a.m.seg_start[a.E] = tot_mt * a.bm;
-    a.m.mtiles[a.E] = a.has_shared ? a.mt_sh : 0;
-    a.m.tp_up[a.E] = tot_up;
-    a.m.tp_up[a.E + 1] = tot_up + sh_up;
-    a.m.tp_dn[a.E] = tot_dn;
-    a.m.tp_dn[a.E + 1] = tot_dn + sh_dn;
-    if (a.offsets_out) a.offsets_out[a.E] = tot_kept;
-  }
-  // L = alpha * E * sum_i f_i P_i, summed as a fixed binary tree in double.
-  red[e] = (e < a.E) ? (double)fr * (double)P : 0.0;
-  __syncthreads();
-  for (int s = 256; s > 0; s >>= 1) {
-    if (e < s) red[e] += red[e + s];
-    __syncthreads();
-  }
-  if (e == 0) a.aux_loss[0] = (float)((double)a.alpha * (double)a.E * red[0]);
-}
 
 struct PermuteArgs {
   const void* x;
@@ -115,46 +31,81 @@ struct PermuteArgs {
   const int* blk_base;   // [nblk][E] exclusive scan over blocks
   Meta m;
   void* xp;
-  int T, d, E, k, BT, capacity, row_bytes;
+  int T, E, k, BT, capacity, nvec;   // nvec: 16-byte vectors per token row
   int copy;
 };
 
-// One block per routing block: rank every key among the earlier keys of the
-// block that chose the same expert, add the block's base, apply the capacity
-// test and write the row; then copy the kept token rows into expert order.
-__global__ void __launch_bounds__(kThreads) permute_kernel(const PermuteArgs a) {
+// One block per routing block.  Warp 0 ranks every key among the earlier keys
+// of the block that chose the same expert: keys go through in order, 32 at a
+// time; __match_any_sync groups equal experts inside a chunk and a per-expert
+// counter in shared memory carries the count across chunks.  Rank plus the
+// block's base is the key's position; the capacity test and the row follow.
+// Then all warps copy the kept token rows into expert order, one row per warp.
+constexpr int kPermuteThreads = 512;
+
+__global__ void __launch_bounds__(kPermuteThreads) permute_kernel(const PermuteArgs a) {
   extern __shared__ int smi[];
+  int* cnt = smi;                 // [E]
+  int* row_s = smi + a.E;         // [BT*k]
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int b = blockIdx.x;
   const int t0 = b * a.BT;
-  const int ntok = min(a.BT, a.T - t0);
-  const int nk = ntok * a.k;
-  int* e_s = smi;            // [BT*k]
-  int* row_s = smi + a.BT * a.k;
+  const int nk = min(a.BT, a.T - t0) * a.k;
   const size_t key0 = (size_t)t0 * a.k;
-  for (int q = threadIdx.x; q < nk; q += kThreads) e_s[q] = a.topk_idx[key0 + q];
+  for (int e = tid; e < a.E; e += kPermuteThreads) cnt[e] = 0;
+  pdl_wait();
+  pdl_trigger();
   __syncthreads();
-  for (int q = threadIdx.x; q < nk; q += kThreads) {
-    const int e = e_s[q];
-    int rank = 0;
-    for (int q2 = 0; q2 < q; ++q2) rank += (e_s[q2] == e);
-    const int pos = a.blk_base[(size_t)b * a.E + e] + rank;
-    const bool keep = pos < a.capacity;
-    const int row = keep ? a.m.seg_start[e] + pos : -1;
-    a.key_row[key0 + q] = row;
-    if (a.slot_pos) a.slot_pos[key0 + q] = keep ? a.m.offsets[e] + pos : -1;
-    row_s[q] = row;
+  if (warp == 0) {
+    const int* base = a.blk_base + (size_t)b * a.E;
+    for (int c = 0; c < nk; c += 32) {
+      const int q = c + lane;
+      const bool valid = q < nk;
+      const int e = valid ? a.topk_idx[key0 + q] : -1 - lane;   // invalid lanes never match
+      const unsigned peers = __match_any_sync(0xffffffffu, e);
+      const int before = __popc(peers & ((1u << lane) - 1u));
+      const int prior = valid ? cnt[e] : 0;
+      __syncwarp();
+      if (valid) {
+        const int pos = base[e] + prior + before;
+        const bool keep = pos < a.capacity;
+        const int row = keep ? a.m.seg_start[e] + pos : -1;
+        a.key_row[key0 + q] = row;
+        if (a.slot_pos) a.slot_pos[key0 + q] = keep ? a.m.offsets[e] + pos : -1;
+        row_s[q] = row;
+        if (before == 0) cnt[e] = prior + __popc(peers);
+      }
+      __syncwarp();
+    }
   }
   __syncthreads();
   if (!a.copy) return;
-  const int nvec = a.row_bytes / 16;
+  // Row copies: (key, 16-byte vector) pairs spread over the block, four
+  // independent loads in flight per thread before their stores.
   const uint4* xs = static_cast<const uint4*>(a.x);
   uint4* xp = static_cast<uint4*>(a.xp);
-  for (int i = threadIdx.x; i < nk * nvec; i += kThreads) {
-    const int q = i / nvec, v = i - q * nvec;
-    const int row = row_s[q];
-    if (row >= 0) {
-      const int t = t0 + q / a.k;
-      xp[(size_t)row * nvec + v] = xs[(size_t)t * nvec + v];
+  const int total = nk * a.nvec;
+  constexpr int U = 4;
+  for (int i0 = tid; i0 < total; i0 += kPermuteThreads * U) {
+    uint4 v[U];
+    int dst_i[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int i = i0 + u * kPermuteThreads;
+      dst_i[u] = -1;
+      if (i < total) {
+        const int q = i / a.nvec, c = i - q * a.nvec;
+        const int row = row_s[q];
+        if (row >= 0) {
+          v[u] = xs[(size_t)(t0 + q / a.k) * a.nvec + c];
+          dst_i[u] = row;
+        }
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int i = i0 + u * kPermuteThreads;
+      if (dst_i[u] >= 0) xp[(size_t)dst_i[u] * a.nvec + (i - (i / a.nvec) * a.nvec)] = v[u];
     }
   }
 }
@@ -172,36 +123,6 @@ Meta meta_ptrs(const Plan& p, void* ws) {
   return m;
 }
 
-cudaError_t launch_scan(const Plan& p, void* ws, int32_t* expert_counts, float* aux_loss,
-                        int32_t* routed_counts, int32_t* offsets, float* f_out, float* P_out,
-                        cudaStream_t st) {
-  ScanArgs a;
-  a.blk_cnt = reinterpret_cast<int*>(static_cast<char*>(ws) + p.ws.blk_cnt);
-  a.blk_prob = reinterpret_cast<const float*>(static_cast<char*>(ws) + p.ws.blk_prob);
-  a.m = meta_ptrs(p, ws);
-  a.nblk = p.nblk;
-  a.E = p.cfg.E;
-  a.T = p.cfg.T;
-  a.k = p.cfg.k;
-  a.capacity = p.capacity;
-  a.bm = p.bm;
-  a.nt_up = p.nt_up;
-  a.nt_dn = p.nt_dn;
-  a.nt_up_sh = p.nt_up_sh;
-  a.nt_dn_sh = p.nt_dn_sh;
-  a.mt_sh = p.mt_sh;
-  a.has_shared = p.cfg.n_shared;
-  a.alpha = p.cfg.alpha;
-  a.expert_counts = expert_counts;
-  a.aux_loss = aux_loss;
-  a.routed_counts = routed_counts;
-  a.offsets_out = offsets;
-  a.f_out = f_out;
-  a.P_out = P_out;
-  scan_kernel<<<1, 512, 0, st>>>(a);
-  return cudaGetLastError();
-}
-
 cudaError_t launch_permute(const Plan& p, const void* x, const int32_t* topk_idx,
                            int32_t* slot_pos, bool copy_rows, void* ws, cudaStream_t st) {
   PermuteArgs a;
@@ -213,16 +134,14 @@ cudaError_t launch_permute(const Plan& p, const void* x, const int32_t* topk_idx
   a.m = meta_ptrs(p, ws);
   a.xp = static_cast<char*>(ws) + p.ws.xp;
   a.T = p.cfg.T;
-  a.d = p.cfg.d;
   a.E = p.cfg.E;
   a.k = p.cfg.k;
   a.BT = p.BT;
   a.capacity = p.capacity;
-  a.row_bytes = p.cfg.d * p.elem;
+  a.nvec = p.cfg.d * p.elem / 16;
   a.copy = copy_rows ? 1 : 0;
-  const size_t smem = 2 * sizeof(int) * (size_t)p.BT * p.cfg.k;
-  permute_kernel<<<p.nblk, kThreads, smem, st>>>(a);
-  return cudaGetLastError();
+  const size_t smem = sizeof(int) * ((size_t)p.cfg.E + (size_t)p.BT * p.cfg.k);
+  return launch_pdl(permute_kernel, dim3(p.nblk), dim3(kPermuteThreads), smem, st, a);
 }
 
 }  // namespace moe

@@ -1,7 +1,6 @@
-// router.cu -- stage 1 and 2 of the layer in one kernel: router scores
-// s = W_r x (+ o) with float32 accumulation, warp-level top-k with the
-// selection bias, gate normalisation, the full router distribution for P_i,
-// and per-block expert histograms.
+// router.cu -- stages 1 and 2 of the layer: router scores s = W_r x (+ o) in
+// float32, then top-k selection with the selection bias, gate normalisation,
+// the full router distribution for P_i and per-block expert histograms.
 //
 // "Mixture of Experts" (llm-tutorial ch. 11) § Top-k routing: softmax over the
 // k chosen logits; § Top-1 vs top-2: the full-softmax probability of a top-1
@@ -10,148 +9,352 @@
 // and § Auxiliary-loss-free balancing: renormalised sigmoid gates and a bias
 // that steers only the choice.
 //
-// One block owns BT tokens and all experts.  Phase 1 is a float32 FMA GEMM
-// (bf16 x bf16 products are exact in float32) with the reduction split into
-// KC-wide chunks summed separately, which keeps the rounding error of a
-// d = 7168 dot product near 1e-7 relative.  Phase 2 gives each warp whole
-// tokens: lanes hold E/32 scores, k rounds of warp arg-max pick the experts
-// (larger score first, equal scores to the lower index).
+// Kernel 1 (scores) is a float32 FMA GEMM over [T x d] x [d x E]: 128-token x
+// BN-expert tiles, 8 x TN outputs per thread, register-prefetched double
+// buffering, and a split of the reduction over blockIdx.z so that small
+// batches still fill the GPU.  bf16 x bf16 products are exact in float32;
+// each thread adds its products in 128-wide chunks before folding them into
+// the running sum, which keeps the rounding error of a 7168-long dot product
+// near 1e-7 relative.  Partial sums go to [S][T][E].
+//
+// Kernel 2 (top-k) gives each warp whole tokens: lanes hold E/32 scores (the
+// split partials summed in a fixed order), k rounds of warp arg-max pick the
+// experts (larger score first, equal scores to the lower index), then gates,
+// the router distribution and the block's expert histogram.
+#include <atomic>
 #include <cfloat>
 #include <climits>
 
 #include "common.cuh"
+#include "launch.cuh"
 #include "moe_internal.h"
+#include "route_scan.cuh"
 
 namespace moe {
 
-struct RouterArgs {
-  const void* x;
-  const void* W_r;
+// ---------------------------------------------------------------- scores
+struct ScoresArgs {
+  const void* x;       // [T][d]
+  const void* W_r;     // [E][d]
+  const float* logit_offset;   // [E] or null
+  float* part;         // [S][T][E] split partials (S > 1)
+  float* scores;       // [T][E] final logits
+  unsigned int* tile_counter;  // [mblocks * nblocks] split blocks done per tile
+  int T, d, E, k_split, S;
+};
+
+constexpr int kScBM = 128, kScBK = 32, kScTM = 8, kScStages = 4;
+
+__device__ __forceinline__ void cp_async16(void* smem_dst, const void* src, bool ok) {
+  const uint32_t d = static_cast<uint32_t>(__cvta_generic_to_shared(smem_dst));
+  const int n = ok ? 16 : 0;     // 0 source bytes: the 16 destination bytes are zero-filled
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(d), "l"(src), "r"(n)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+__device__ __forceinline__ void to_float8(const uint4& u, const __nv_bfloat16*, float (&v)[8]) {
+  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    v[2 * i] = __uint_as_float(w[i] << 16);
+    v[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+  }
+}
+__device__ __forceinline__ void to_float8(const uint4& u, const float*, float (&v)[8]) {
+  v[0] = __uint_as_float(u.x);
+  v[1] = __uint_as_float(u.y);
+  v[2] = __uint_as_float(u.z);
+  v[3] = __uint_as_float(u.w);
+}
+
+// Raw input tiles stream through a kScStages-deep cp.async pipeline in their
+// stored precision.  Each stage is converted once to float32 and transposed
+// into a k-major tile; the inner loop then reads 8 token values and TN expert
+// values with vector loads and forms products in increasing k order.
+// Thread (ty, tx) of 16 x 16 owns tokens ty*8 .. ty*8+7 and experts
+// tx*TN .. tx*TN+TN-1.
+template <typename TIn, int TN>
+__global__ void __launch_bounds__(kThreads) router_scores_kernel(const ScoresArgs a) {
+  constexpr int BM = kScBM, BK = kScBK, TM = kScTM, BN = 16 * TN;
+  constexpr int EPC = 16 / sizeof(TIn);          // elements per 16-byte chunk
+  constexpr int LD = BK + EPC;                   // raw smem row stride (elements)
+  constexpr int A_EL = BM * LD, B_EL = BN * LD;
+  constexpr int CPR = BK / EPC;                  // 16-byte chunks per tile row
+  extern __shared__ __align__(16) uint8_t sc_smem[];
+  float* Af = reinterpret_cast<float*>(sc_smem);             // [BK][BM + 4]
+  float* Bf = Af + BK * (BM + 4);                            // [BK][BN + 4]
+  TIn* As = reinterpret_cast<TIn*>(Bf + BK * (BN + 4));      // [stages][BM][LD]
+  TIn* Bs = As + kScStages * A_EL;                           // [stages][BN][LD]
+  __shared__ int am_last;
+  const int tid = threadIdx.x;
+  const int tx = tid & 15, ty = tid >> 4;
+  const int m0 = blockIdx.x * BM, n0 = blockIdx.y * BN;
+  const int k_beg = blockIdx.z * a.k_split;
+  const int k_end = min(a.d, k_beg + a.k_split);
+  const TIn* X = static_cast<const TIn*>(a.x);
+  const TIn* Wr = static_cast<const TIn*>(a.W_r);
+  pdl_wait();
+  pdl_trigger();
+
+  auto issue = [&](int stage, int k0) {
+    TIn* as = As + stage * A_EL;
+    TIn* bs = Bs + stage * B_EL;
+    for (int c = tid; c < BM * CPR; c += kThreads) {
+      const int r = c % BM, kc = (c / BM) * EPC;
+      const int gm = m0 + r, gk = k0 + kc;
+      const bool ok = gm < a.T && gk < k_end;
+      cp_async16(as + r * LD + kc, X + (ok ? (size_t)gm * a.d + gk : 0), ok);
+    }
+    for (int c = tid; c < BN * CPR; c += kThreads) {
+      const int r = c % BN, kc = (c / BN) * EPC;
+      const int gn = n0 + r, gk = k0 + kc;
+      const bool ok = gn < a.E && gk < k_end;
+      cp_async16(bs + r * LD + kc, Wr + (ok ? (size_t)gn * a.d + gk : 0), ok);
+    }
+  };
+  // raw stage -> float32, transposed to [k][row]; consecutive threads take
+  // consecutive rows, so both the 16-byte reads and the scalar writes are
+  // free of bank conflicts
+  auto convert = [&](int stage) {
+    const TIn* as = As + stage * A_EL;
+    const TIn* bs = Bs + stage * B_EL;
+    for (int c = tid; c < BM * CPR; c += kThreads) {
+      const int r = c % BM, kc = (c / BM) * EPC;
+      float v[8];
+      to_float8(*reinterpret_cast<const uint4*>(as + r * LD + kc), as, v);
+#pragma unroll
+      for (int i = 0; i < EPC; ++i) Af[(kc + i) * (BM + 4) + r] = v[i];
+    }
+    for (int c = tid; c < BN * CPR; c += kThreads) {
+      const int r = c % BN, kc = (c / BN) * EPC;
+      float v[8];
+      to_float8(*reinterpret_cast<const uint4*>(bs + r * LD + kc), bs, v);
+#pragma unroll
+      for (int i = 0; i < EPC; ++i) Bf[(kc + i) * (BN + 4) + r] = v[i];
+    }
+  };
+
+  float acc[TM][TN], part[TM][TN];
+#pragma unroll
+  for (int i = 0; i < TM; ++i)
+#pragma unroll
+    for (int j = 0; j < TN; ++j) acc[i][j] = part[i][j] = 0.f;
+
+  const int nk = (k_end - k_beg + BK - 1) / BK;
+#pragma unroll
+  for (int s = 0; s < kScStages - 1; ++s) {
+    if (s < nk) issue(s, k_beg + s * BK);
+    cp_async_commit();
+  }
+  for (int it = 0; it < nk; ++it) {
+    cp_async_wait<kScStages - 2>();
+    __syncthreads();                      // stage `it` landed; the float tile is free
+    convert(it % kScStages);
+    {
+      const int nxt = it + kScStages - 1;
+      if (nxt < nk) issue(nxt % kScStages, k_beg + nxt * BK);
+      cp_async_commit();
+    }
+    __syncthreads();
+#pragma unroll
+    for (int kk = 0; kk < BK; ++kk) {
+      const float4 a0 = *reinterpret_cast<const float4*>(Af + kk * (BM + 4) + ty * TM);
+      const float4 a1 = *reinterpret_cast<const float4*>(Af + kk * (BM + 4) + ty * TM + 4);
+      const float av[TM] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+      float bv[TN];
+      if (TN == 4) {
+        const float4 b4 = *reinterpret_cast<const float4*>(Bf + kk * (BN + 4) + tx * TN);
+        bv[0] = b4.x; bv[1] = b4.y; bv[2] = b4.z; bv[3] = b4.w;
+      } else {
+        const float2 b2 = *reinterpret_cast<const float2*>(Bf + kk * (BN + 4) + tx * TN);
+        bv[0] = b2.x; bv[1] = b2.y;
+      }
+#pragma unroll
+      for (int i = 0; i < TM; ++i)
+#pragma unroll
+        for (int j = 0; j < TN; ++j) part[i][j] = fmaf(av[i], bv[j], part[i][j]);
+    }
+    if ((it & 3) == 3 || it + 1 == nk) {   // fold every 128 k into the running sum
+#pragma unroll
+      for (int i = 0; i < TM; ++i)
+#pragma unroll
+        for (int j = 0; j < TN; ++j) {
+          acc[i][j] += part[i][j];
+          part[i][j] = 0.f;
+        }
+    }
+  }
+  cp_async_wait<0>();
+
+  if (a.S == 1) {
+#pragma unroll
+    for (int i = 0; i < TM; ++i) {
+      const int m = m0 + ty * TM + i;
+      if (m >= a.T) continue;
+#pragma unroll
+      for (int j = 0; j < TN; ++j) {
+        const int n = n0 + tx * TN + j;
+        if (n < a.E)
+          a.scores[(size_t)m * a.E + n] = acc[i][j] + (a.logit_offset ? a.logit_offset[n] : 0.f);
+      }
+    }
+    return;
+  }
+  // Split reduction: every split block publishes its partial; the last one
+  // to finish for this tile adds the S partials in split order.
+  float* out = a.part + (size_t)blockIdx.z * a.T * a.E;
+#pragma unroll
+  for (int i = 0; i < TM; ++i) {
+    const int m = m0 + ty * TM + i;
+    if (m >= a.T) continue;
+#pragma unroll
+    for (int j = 0; j < TN; ++j) {
+      const int n = n0 + tx * TN + j;
+      if (n < a.E) out[(size_t)m * a.E + n] = acc[i][j];
+    }
+  }
+  __threadfence();
+  __syncthreads();
+  unsigned int* ctr = a.tile_counter + blockIdx.x * gridDim.y + blockIdx.y;
+  if (tid == 0) am_last = atomicAdd(ctr, 1u) == (unsigned)(a.S - 1);
+  __syncthreads();
+  if (!am_last) return;
+  __threadfence();
+  // all TM x TN partials of one split are loaded before any of them is added
+  const size_t TE = (size_t)a.T * a.E;
+  float sum[TM][TN];
+  for (int z = 0; z < a.S; ++z) {
+    float v[TM][TN];
+#pragma unroll
+    for (int i = 0; i < TM; ++i) {
+      const int m = m0 + ty * TM + i;
+#pragma unroll
+      for (int j = 0; j < TN; ++j) {
+        const int n = n0 + tx * TN + j;
+        v[i][j] = (m < a.T && n < a.E) ? __ldcg(a.part + z * TE + (size_t)m * a.E + n) : 0.f;
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < TM; ++i)
+#pragma unroll
+      for (int j = 0; j < TN; ++j) sum[i][j] = z == 0 ? v[i][j] : sum[i][j] + v[i][j];
+  }
+#pragma unroll
+  for (int i = 0; i < TM; ++i) {
+    const int m = m0 + ty * TM + i;
+    if (m >= a.T) continue;
+#pragma unroll
+    for (int j = 0; j < TN; ++j) {
+      const int n = n0 + tx * TN + j;
+      if (n < a.E)
+        a.scores[(size_t)m * a.E + n] = sum[i][j] + (a.logit_offset ? a.logit_offset[n] : 0.f);
+    }
+  }
+  if (tid == 0) *ctr = 0;
+}
+
+// ---------------------------------------------------------------- top-k
+struct TopkArgs {
+  const float* part;         // [S][T][E]
+  int S;
   const float* logit_offset;
   const float* sel_bias;
   int32_t* topk_idx;
   float* topk_w;
-  int* blk_cnt;
-  float* blk_prob;
-  int T, d, E, E_pad, k, BT, KC, gate;
+  int T, E, k, BT, gate;
+  ScanArgs scan;             // blk_cnt / blk_prob / counter and the scan outputs
 };
 
-template <typename TIn>
-__global__ void __launch_bounds__(kThreads) router_topk_kernel(const RouterArgs a) {
-  extern __shared__ __align__(16) float sm[];
-  constexpr int RT = kRouterRT;
-  const int E_pad = a.E_pad, BT = a.BT, KC = a.KC;
-  const int EC = E_pad < 256 ? E_pad : 256;   // experts per pass of the block
-  const int EPT = (E_pad + 255) / 256;        // expert passes per thread (1 or 2)
-  const int XS = BT + 4;                      // row stride of the x tile
-  const int WS = E_pad + 1;                   // row stride of the W tile / scores
-  float* xs = sm;                             // [KC][XS]
-  float* wt = xs + KC * XS;                   // [KC][WS]
-  float* S = wt + KC * WS;                    // [BT][WS]
-  float* Pw = S + BT * WS;                    // [8][E_pad]
-  int* cnt = reinterpret_cast<int*>(Pw + 8 * E_pad);  // [E_pad]
+constexpr int kTopkThreads = 512;
+constexpr int kTopkWarps = kTopkThreads / 32;
 
+union TopkSmem {
+  struct {
+    float Pw[kTopkWarps][kMaxE];
+    int cnt[kMaxE];
+  } t;
+  ScanSmem<kTopkThreads> scan;
+};
+
+// One routing block of BT tokens; warp w takes tokens w, w + 16, ...  After
+// the block has published its histogram and probability sums, the last block
+// to finish runs the capacity scan for the whole batch.
+__global__ void __launch_bounds__(kTopkThreads) router_topk_kernel(const TopkArgs a) {
+  __shared__ TopkSmem sm;
+  __shared__ int am_last;
   const int tid = threadIdx.x;
-  const int el = tid % EC, grp = tid / EC;
-  const int t0 = blockIdx.x * BT;
-  const TIn* x = static_cast<const TIn*>(a.x);
-  const TIn* W = static_cast<const TIn*>(a.W_r);
-
-  for (int e = tid; e < E_pad; e += kThreads) cnt[e] = 0;
-
-  // ---- phase 1: scores ---------------------------------------------------
-  float acc[2][RT];
-#pragma unroll
-  for (int c = 0; c < 2; ++c)
-#pragma unroll
-    for (int r = 0; r < RT; ++r) acc[c][r] = 0.f;
-
-  for (int c0 = 0; c0 < a.d; c0 += KC) {
-    for (int i = tid; i < BT * KC; i += kThreads) {
-      const int tok = i / KC, kc = i - tok * KC;
-      const int t = t0 + tok, c = c0 + kc;
-      xs[kc * XS + tok] = (t < a.T && c < a.d) ? to_float(x[(size_t)t * a.d + c]) : 0.f;
-    }
-    for (int i = tid; i < E_pad * KC; i += kThreads) {
-      const int e = i / KC, kc = i - e * KC;
-      const int c = c0 + kc;
-      wt[kc * WS + e] = (e < a.E && c < a.d) ? to_float(W[(size_t)e * a.d + c]) : 0.f;
-    }
-    __syncthreads();
-    float part[2][RT];
-#pragma unroll
-    for (int c = 0; c < 2; ++c)
-#pragma unroll
-      for (int r = 0; r < RT; ++r) part[c][r] = 0.f;
-    const int kcn = min(KC, a.d - c0);
-    for (int kc = 0; kc < kcn; ++kc) {
-      const float4* xr = reinterpret_cast<const float4*>(xs + kc * XS + grp * RT);
-      const float4 xa = xr[0], xb = xr[1];
-      const float xv[RT] = {xa.x, xa.y, xa.z, xa.w, xb.x, xb.y, xb.z, xb.w};
-#pragma unroll
-      for (int c = 0; c < 2; ++c) {
-        if (c < EPT) {
-          const float w = wt[kc * WS + el + c * 256];
-#pragma unroll
-          for (int r = 0; r < RT; ++r) part[c][r] = fmaf(w, xv[r], part[c][r]);
-        }
-      }
-    }
-#pragma unroll
-    for (int c = 0; c < 2; ++c)
-#pragma unroll
-      for (int r = 0; r < RT; ++r) acc[c][r] += part[c][r];
-    __syncthreads();
-  }
-#pragma unroll
-  for (int c = 0; c < 2; ++c) {
-    const int e = el + c * 256;
-    if (c < EPT && e < a.E) {
-      const float off = a.logit_offset ? a.logit_offset[e] : 0.f;
-#pragma unroll
-      for (int r = 0; r < RT; ++r) S[(grp * RT + r) * WS + e] = acc[c][r] + off;
-    }
-  }
-  __syncthreads();
-
-  // ---- phase 2: top-k, gates, router distribution --------------------------
   const int warp = tid >> 5, lane = tid & 31;
-  const int NPL = E_pad >> 5;   // scores per lane, <= 16
+  const int E = a.E;
+  const int NPL = (E + 31) >> 5;     // scores per lane, <= 16
+  for (int e = tid; e < E; e += kTopkThreads) sm.t.cnt[e] = 0;
+  pdl_wait();
+  pdl_trigger();
+  __syncthreads();
   float psum[16];
 #pragma unroll
   for (int i = 0; i < 16; ++i) psum[i] = 0.f;
   const bool sigm = a.gate == MOE_GATE_SIGMOID_RENORM;
+  const size_t TE = (size_t)a.T * E;
+  const int t0 = blockIdx.x * a.BT;
 
-  for (int tl = warp; tl < BT; tl += kThreads / 32) {
+  for (int tl = warp; tl < a.BT; tl += kTopkWarps) {
     const int t = t0 + tl;
     if (t >= a.T) break;
-    const float* St = S + tl * WS;
     float sv[16], sel[16];
 #pragma unroll
     for (int i = 0; i < 16; ++i) {
       sv[i] = -INFINITY;
       sel[i] = -INFINITY;
+    }
+    // the split partials: all loads first, then the sums in split order
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
       const int e = lane + 32 * i;
-      if (i < NPL && e < a.E) {
-        const float s = St[e];
+      if (i < NPL && e < E) sv[i] = a.part[(size_t)t * E + e];
+    }
+    for (int z = 1; z < a.S; ++z) {
+      float pz[16];
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        const int e = lane + 32 * i;
+        pz[i] = (i < NPL && e < E) ? a.part[z * TE + (size_t)t * E + e] : 0.f;
+      }
+#pragma unroll
+      for (int i = 0; i < 16; ++i) sv[i] += pz[i];
+    }
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      const int e = lane + 32 * i;
+      if (i < NPL && e < E) {
+        float s = sv[i];
+        if (a.logit_offset) s += a.logit_offset[e];
         sv[i] = s;
         float v = sigm ? sigmoidf_(s) : s;
         if (a.sel_bias) v += a.sel_bias[e];
         sel[i] = (v != v) ? -INFINITY : v;   // NaN never outranks a number
+      } else {
+        sv[i] = -INFINITY;
       }
     }
     uint32_t taken = 0;
     int my_idx = 0;
+    float my_s = -INFINITY;
     for (int r = 0; r < a.k; ++r) {
-      float bv = -INFINITY;
+      float bv = -INFINITY, bs = -INFINITY;
       int bi = INT_MAX;
 #pragma unroll
       for (int i = 0; i < 16; ++i) {
         const int e = lane + 32 * i;
-        if (i < NPL && e < a.E && !((taken >> i) & 1u)) {
+        if (i < NPL && e < E && !((taken >> i) & 1u)) {
           if (sel[i] > bv || (sel[i] == bv && e < bi)) {
             bv = sel[i];
             bi = e;
+            bs = sv[i];
           }
         }
       }
@@ -159,27 +362,30 @@ __global__ void __launch_bounds__(kThreads) router_topk_kernel(const RouterArgs 
       for (int o = 16; o > 0; o >>= 1) {
         const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
         const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+        const float os = __shfl_xor_sync(0xffffffffu, bs, o);
         if (ov > bv || (ov == bv && oi < bi)) {
           bv = ov;
           bi = oi;
+          bs = os;
         }
       }
-      if (bi < a.E && (bi & 31) == lane) taken |= 1u << (bi >> 5);
-      if (lane == r) my_idx = bi < a.E ? bi : 0;
+      if (bi < E && (bi & 31) == lane) taken |= 1u << (bi >> 5);
+      if (lane == r) {
+        my_idx = bi < E ? bi : 0;
+        my_s = bs;
+      }
     }
     const bool mine = lane < a.k;
-    const float s_me = mine ? St[my_idx] : -INFINITY;
+    const float s_me = mine ? my_s : -INFINITY;
 
-    // full distribution over all experts
     float m_all = -INFINITY;
 #pragma unroll
     for (int i = 0; i < 16; ++i) m_all = fmaxf(m_all, sv[i]);
     m_all = warp_max(m_all);
     float z_all = 0.f;
 #pragma unroll
-    for (int i = 0; i < 16; ++i) {
-      if (i < NPL && lane + 32 * i < a.E) z_all += sigm ? sigmoidf_(sv[i]) : expf(sv[i] - m_all);
-    }
+    for (int i = 0; i < 16; ++i)
+      if (i < NPL && lane + 32 * i < E) z_all += sigm ? sigmoidf_(sv[i]) : expf(sv[i] - m_all);
     z_all = warp_sum(z_all);
 
     float g;
@@ -196,68 +402,151 @@ __global__ void __launch_bounds__(kThreads) router_topk_kernel(const RouterArgs 
     if (mine) {
       a.topk_idx[(size_t)t * a.k + lane] = my_idx;
       a.topk_w[(size_t)t * a.k + lane] = g;
-      atomicAdd(&cnt[my_idx], 1);
+      atomicAdd(&sm.t.cnt[my_idx], 1);
     }
 #pragma unroll
-    for (int i = 0; i < 16; ++i) {
-      if (i < NPL && lane + 32 * i < a.E)
+    for (int i = 0; i < 16; ++i)
+      if (i < NPL && lane + 32 * i < E)
         psum[i] += sigm ? sigmoidf_(sv[i]) / z_all : expf(sv[i] - m_all) / z_all;
-    }
   }
 
-  // ---- block statistics, fixed summation order ----------------------------
+  // block statistics, fixed summation order over the warps
 #pragma unroll
   for (int i = 0; i < 16; ++i)
-    if (i < NPL) Pw[warp * E_pad + lane + 32 * i] = psum[i];
+    if (i < NPL && lane + 32 * i < E) sm.t.Pw[warp][lane + 32 * i] = psum[i];
   __syncthreads();
-  for (int e = tid; e < a.E; e += kThreads) {
+  for (int e = tid; e < E; e += kTopkThreads) {
     float s = 0.f;
 #pragma unroll
-    for (int w = 0; w < kThreads / 32; ++w) s += Pw[w * E_pad + e];
-    a.blk_prob[(size_t)blockIdx.x * a.E + e] = s;
-    a.blk_cnt[(size_t)blockIdx.x * a.E + e] = cnt[e];
+    for (int w = 0; w < kTopkWarps; ++w) s += sm.t.Pw[w][e];
+    a.scan.blk_prob[(size_t)blockIdx.x * E + e] = s;
+    a.scan.blk_cnt[(size_t)blockIdx.x * E + e] = sm.t.cnt[e];
   }
+  // publish, then let the last block to finish run the scan
+  __threadfence();
+  __syncthreads();
+  if (tid == 0) am_last = atomicAdd(a.scan.done_counter, 1u) == gridDim.x - 1;
+  __syncthreads();
+  if (!am_last) return;
+  __threadfence();
+  scan_block<kTopkThreads>(a.scan, sm.scan);
+  if (tid == 0) *a.scan.done_counter = 0;
 }
 
-size_t router_smem_bytes(const Plan& p) {
-  const size_t f = (size_t)p.KC * (p.BT + 4) + (size_t)p.KC * (p.E_pad + 1) +
-                   (size_t)p.BT * (p.E_pad + 1) + 8 * (size_t)p.E_pad;
-  return f * sizeof(float) + (size_t)p.E_pad * sizeof(int);
+template <typename TIn, int TN>
+static cudaError_t launch_scores_t(const Plan& p, const ScoresArgs& a, cudaStream_t st) {
+  constexpr int EPC = 16 / sizeof(TIn), LD = kScBK + EPC;
+  const int smem = kScBK * (kScBM + 4 + 16 * TN + 4) * (int)sizeof(float) +
+                   kScStages * (kScBM + 16 * TN) * LD * (int)sizeof(TIn);
+  static std::atomic<uint64_t> attr_done{0};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (!(attr_done.load(std::memory_order_acquire) & (1ull << (dev & 63)))) {
+    e = cudaFuncSetAttribute(router_scores_kernel<TIn, TN>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    attr_done.fetch_or(1ull << (dev & 63), std::memory_order_release);
+  }
+  const dim3 grid(p.sc_mblocks, p.sc_nblocks, p.sc_splits);
+  return launch_pdl(router_scores_kernel<TIn, TN>, grid, dim3(kThreads), (size_t)smem, st, a);
 }
+
+// Router logits into `scores` ([T][E], float32, offset included).
+static cudaError_t launch_logits(const Plan& p, const void* x, const void* W_r,
+                                 const float* logit_offset, float* scores, void* ws,
+                                 cudaStream_t st);
 
 cudaError_t launch_router(const Plan& p, const void* x, const void* W_r, const float* logit_offset,
                           const float* sel_bias, int32_t* topk_idx, float* topk_w, void* ws,
-                          cudaStream_t st) {
-  RouterArgs a;
+                          const ScanOutputs& so, cudaStream_t st, cudaEvent_t mid_event) {
+  char* w = static_cast<char*>(ws);
+  float* scores = reinterpret_cast<float*>(w + p.ws.scores);
+  cudaError_t e = launch_logits(p, x, W_r, logit_offset, scores, ws, st);
+  if (e != cudaSuccess) return e;
+  if (mid_event && (e = cudaEventRecord(mid_event, st)) != cudaSuccess) return e;
+  TopkArgs t;
+  t.part = scores;
+  t.S = 1;
+  t.logit_offset = nullptr;     // already in the logits
+  t.sel_bias = sel_bias;
+  t.topk_idx = topk_idx;
+  t.topk_w = topk_w;
+  t.T = p.cfg.T;
+  t.E = p.cfg.E;
+  t.k = p.cfg.k;
+  t.BT = p.BT;
+  t.gate = p.cfg.gate;
+  ScanArgs& c = t.scan;
+  c.blk_cnt = reinterpret_cast<int*>(w + p.ws.blk_cnt);
+  c.blk_prob = reinterpret_cast<float*>(w + p.ws.blk_prob);
+  c.m = meta_ptrs(p, ws);
+  c.nblk = p.nblk;
+  c.E = p.cfg.E;
+  c.T = p.cfg.T;
+  c.k = p.cfg.k;
+  c.capacity = p.capacity;
+  c.bm = p.bm;
+  c.nt_up = p.nt_up;
+  c.nt_dn = p.nt_dn;
+  c.nt_up_sh = p.nt_up_sh;
+  c.nt_dn_sh = p.nt_dn_sh;
+  c.mt_sh = p.mt_sh;
+  c.has_shared = p.cfg.n_shared;
+  c.alpha = p.cfg.alpha;
+  c.expert_counts = so.expert_counts;
+  c.aux_loss = so.aux_loss;
+  c.routed_counts = so.routed_counts;
+  c.offsets_out = so.offsets;
+  c.f_out = so.f_out;
+  c.P_out = so.P_out;
+  c.done_counter = reinterpret_cast<unsigned int*>(w + p.ws.status + 16);
+  return launch_pdl(router_topk_kernel, dim3(p.nblk), dim3(kTopkThreads), 0, st, t);
+}
+
+// Adds the per-expert offset to logits computed without it.
+__global__ void __launch_bounds__(kThreads) add_offset_kernel(float* s, size_t TE, int E,
+                                                              const float* off) {
+  pdl_wait();
+  pdl_trigger();
+  const size_t i = (size_t)blockIdx.x * kThreads + threadIdx.x;
+  if (i < TE) s[i] += off[i % E];
+}
+
+static cudaError_t launch_logits(const Plan& p, const void* x, const void* W_r,
+                                 const float* logit_offset, float* scores, void* ws,
+                                 cudaStream_t st) {
+  char* w = static_cast<char*>(ws);
+  if (p.router_tc) {
+    cudaError_t e =
+        launch_router_tc(p, x, W_r, scores, reinterpret_cast<uint32_t*>(w + p.ws.status), st);
+    if (e != cudaSuccess || !logit_offset) return e;
+    const size_t TE = (size_t)p.cfg.T * p.cfg.E;
+    return launch_pdl(add_offset_kernel, dim3((unsigned)((TE + kThreads - 1) / kThreads)),
+                      dim3(kThreads), 0, st, scores, TE, p.cfg.E, logit_offset);
+  }
+  ScoresArgs a;
   a.x = x;
   a.W_r = W_r;
   a.logit_offset = logit_offset;
-  a.sel_bias = sel_bias;
-  a.topk_idx = topk_idx;
-  a.topk_w = topk_w;
-  a.blk_cnt = reinterpret_cast<int*>(static_cast<char*>(ws) + p.ws.blk_cnt);
-  a.blk_prob = reinterpret_cast<float*>(static_cast<char*>(ws) + p.ws.blk_prob);
+  a.part = reinterpret_cast<float*>(w + p.ws.score_parts);
+  a.scores = scores;
+  a.tile_counter = reinterpret_cast<unsigned int*>(w + p.ws.status + kTileCounterOffset);
   a.T = p.cfg.T;
   a.d = p.cfg.d;
   a.E = p.cfg.E;
-  a.E_pad = p.E_pad;
-  a.k = p.cfg.k;
-  a.BT = p.BT;
-  a.KC = p.KC;
-  a.gate = p.cfg.gate;
-  const size_t smem = router_smem_bytes(p);
-  if (p.cfg.dtype == MOE_BF16) {
-    cudaError_t e = cudaFuncSetAttribute(router_topk_kernel<__nv_bfloat16>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-    router_topk_kernel<__nv_bfloat16><<<p.nblk, kThreads, smem, st>>>(a);
-  } else {
-    cudaError_t e = cudaFuncSetAttribute(router_topk_kernel<float>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-    router_topk_kernel<float><<<p.nblk, kThreads, smem, st>>>(a);
-  }
-  return cudaGetLastError();
+  a.k_split = p.sc_ksplit;
+  a.S = p.sc_splits;
+  if (p.cfg.dtype == MOE_BF16)
+    return p.sc_tn == 4 ? launch_scores_t<__nv_bfloat16, 4>(p, a, st)
+                        : launch_scores_t<__nv_bfloat16, 2>(p, a, st);
+  return p.sc_tn == 4 ? launch_scores_t<float, 4>(p, a, st) : launch_scores_t<float, 2>(p, a, st);
+}
+
+cudaError_t launch_router_scores(const Plan& p, const void* x, const void* W_r,
+                                 const float* logit_offset, float* out, void* ws,
+                                 cudaStream_t st) {
+  return launch_logits(p, x, W_r, logit_offset, out, ws, st);
 }
 
 }  // namespace moe

@@ -58,11 +58,15 @@ def workspace_size(cfg: N.MoeConfig, kind: str = "forward") -> int:
     return n.value
 
 
+WS_HEADER_BYTES = 4096
+
+
 def alloc_workspace(cfg: N.MoeConfig, device="cuda", kind: str = "forward") -> torch.Tensor:
-    """Device workspace; its first 256 bytes (the status word) start at zero."""
+    """Device workspace; its first 4096 bytes (status word and reduction
+    counters) start at zero, as the C ABI requires."""
     n = workspace_size(cfg, kind)
-    ws = torch.empty(max(n, 256), dtype=torch.uint8, device=device)
-    ws[:256].zero_()
+    ws = torch.empty(max(n, WS_HEADER_BYTES), dtype=torch.uint8, device=device)
+    ws[:WS_HEADER_BYTES].zero_()
     return ws
 
 
@@ -121,8 +125,7 @@ def forward(cfg: N.MoeConfig, x, W_r, W1, W2, W3=None, logit_offset=None, sel_bi
     if events is None:
         rc = N.lib().moe_forward(*args)
     else:
-        arr = (ctypes.c_void_p * len(events))(*[ctypes.c_void_p(e.cuda_event) for e in events])
-        rc = N.lib().moe_forward_timed(*args, arr)
+        rc = N.lib().moe_forward_timed(*args, BoundForward.event_array(events, stream))
     N.check(rc, "moe_forward")
     return out
 
@@ -141,6 +144,20 @@ def route(cfg: N.MoeConfig, x, W_r, logit_offset=None, sel_bias=None,
         _ptr(out.routed_counts), _ptr(out.offsets), _ptr(out.slot_pos), _ptr(out.f),
         _ptr(out.P), _ptr(workspace), ctypes.c_size_t(workspace.numel()), _stream_handle(stream))
     N.check(rc, "moe_route")
+    return out
+
+
+def router_scores(cfg: N.MoeConfig, x, W_r, logit_offset=None, out=None, workspace=None,
+                  stream=None) -> torch.Tensor:
+    """Stage 1 alone (moe_router_scores): float32 logits [T, E]."""
+    if out is None:
+        out = torch.empty((cfg.T, cfg.E), dtype=torch.float32, device=x.device)
+    if workspace is None:
+        workspace = alloc_workspace(cfg, x.device, "route")
+    N.check(N.lib().moe_router_scores(ctypes.byref(cfg), _ptr(x), _ptr(W_r), _ptr(logit_offset),
+                                      _ptr(out), _ptr(workspace),
+                                      ctypes.c_size_t(workspace.numel()), _stream_handle(stream)),
+            "moe_router_scores")
     return out
 
 
@@ -168,3 +185,64 @@ def selftest_wait_timeout(workspace: torch.Tensor, wait_ns: int, stream=None) ->
     N.check(N.lib().moe_selftest_wait_timeout(_ptr(workspace), ctypes.c_size_t(workspace.numel()),
                                               ctypes.c_uint64(wait_ns), _stream_handle(stream)),
             "moe_selftest_wait_timeout")
+
+
+class BoundForward:
+    """moe_forward with every argument marshalled once: calling it enqueues
+    one layer call (used by timing loops, where per-call Python work would
+    otherwise sit between kernel launches)."""
+
+    def __init__(self, cfg: N.MoeConfig, x, W_r, W1, W2, W3=None, logit_offset=None,
+                 sel_bias=None, Ws1=None, Ws3=None, Ws2=None, out: Optional[MoeOutputs] = None,
+                 workspace: Optional[torch.Tensor] = None, stream=None):
+        self.cfg = cfg
+        self.out = out if out is not None else alloc_outputs(cfg, x.device, x.dtype)
+        self.workspace = workspace if workspace is not None else alloc_workspace(cfg, x.device)
+        self._keep = (x, W_r, W1, W2, W3, logit_offset, sel_bias, Ws1, Ws3, Ws2)
+        o = self.out
+        self.args = (ctypes.byref(cfg), _ptr(x), _ptr(W_r), _ptr(logit_offset), _ptr(sel_bias),
+                     _ptr(W1), _ptr(W3), _ptr(W2), _ptr(Ws1), _ptr(Ws3), _ptr(Ws2),
+                     _ptr(o.y), _ptr(o.topk_idx), _ptr(o.topk_w), _ptr(o.expert_counts),
+                     _ptr(o.aux_loss), _ptr(o.routed_counts), _ptr(o.offsets), _ptr(o.slot_pos),
+                     _ptr(o.f), _ptr(o.P), _ptr(self.workspace),
+                     ctypes.c_size_t(self.workspace.numel()), _stream_handle(stream))
+        self._fwd = N.lib().moe_forward
+        self._timed = N.lib().moe_forward_timed
+
+    def __call__(self, events=None) -> None:
+        """events: None, or a ctypes array of MOE_NUM_STAGES + 1 cudaEvent_t."""
+        rc = self._fwd(*self.args) if events is None else self._timed(*self.args, events)
+        if rc != N.MOE_OK:
+            raise N.MoeError(rc, "moe_forward")
+
+    @staticmethod
+    def event_array(events, stream=None):
+        """cudaEvent_t handles of torch events.  torch creates an event on its
+        first record, so each one is recorded once here; the library then
+        re-records it between the stage kernels."""
+        s = stream if stream is not None else torch.cuda.current_stream()
+        for e in events:
+            e.record(s)
+        return (ctypes.c_void_p * len(events))(*[ctypes.c_void_p(e.cuda_event) for e in events])
+
+
+class BoundHostIO:
+    """moe_forward_host_io with every argument marshalled once."""
+
+    def __init__(self, cfg: N.MoeConfig, x_host, y_host, aux_host, W_r, W1, W2, W3=None,
+                 logit_offset=None, sel_bias=None, Ws1=None, Ws3=None, Ws2=None,
+                 workspace: Optional[torch.Tensor] = None, stream=None):
+        self.workspace = (workspace if workspace is not None
+                          else alloc_workspace(cfg, W_r.device, "host_io"))
+        self._keep = (x_host, y_host, aux_host, W_r, W1, W2, W3, logit_offset, sel_bias, Ws1,
+                      Ws3, Ws2)
+        self.args = (ctypes.byref(cfg), _ptr(x_host), _ptr(W_r), _ptr(logit_offset),
+                     _ptr(sel_bias), _ptr(W1), _ptr(W3), _ptr(W2), _ptr(Ws1), _ptr(Ws3),
+                     _ptr(Ws2), _ptr(y_host), _ptr(aux_host), _ptr(self.workspace),
+                     ctypes.c_size_t(self.workspace.numel()), _stream_handle(stream))
+        self._fn = N.lib().moe_forward_host_io
+
+    def __call__(self) -> None:
+        rc = self._fn(*self.args)
+        if rc != N.MOE_OK:
+            raise N.MoeError(rc, "moe_forward_host_io")

@@ -1,0 +1,86 @@
+"""Host-side logic of bench.py, no GPU: the max-over-ranks job time on a
+world-size-2 gloo group, the reference arm's rank behaviour, the algorithmic
+byte / FLOP accounting behind the roofline numbers."""
+import os
+import socket
+
+import pytest
+import torch
+import torch.distributed as dist
+import torch.multiprocessing as mp
+
+import bench
+from sparse_mixture_experts_65_b300 import workloads as W
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _rank_main(rank, world, port, out):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        mine = [3.5, 7.25][rank]
+        out[rank] = bench.max_over_ranks(mine, dist)
+        dist.barrier()
+    finally:
+        dist.destroy_process_group()
+
+
+def test_job_time_is_max_over_ranks_gloo():
+    world = 2
+    mgr = mp.get_context("spawn").Manager()
+    out = mgr.dict()
+    mp.start_processes(_rank_main, args=(world, _free_port(), out), nprocs=world,
+                       start_method="spawn", join=True)
+    assert dict(out) == {0: 7.25, 1: 7.25}
+
+
+def test_single_rank_max_is_identity():
+    assert bench.max_over_ranks(1.5) == 1.5
+
+
+def test_reference_arm_other_ranks_do_no_work(monkeypatch, capsys):
+    monkeypatch.setenv("RANK", "1")
+    monkeypatch.setenv("WORLD_SIZE", "2")
+
+    class A:
+        workload = "toy"
+        steps = 3
+        warmup = 3
+    assert bench.run_reference(A()) is None
+    assert capsys.readouterr().out == ""
+
+
+def test_accounting_switch_shape():
+    s = W.SWITCH
+    kept = [0] * 64
+    kept[3], kept[7] = 80, 50
+    acc, layer = bench.accounting(s, kept)
+    el = 2
+    w1 = 2 * s.f * s.d * el          # two active experts, plain (ReLU) up projection
+    assert acc["up"]["bytes"] == w1 + 130 * s.d * el + 130 * s.f * el
+    assert acc["up"]["flops"] == 2 * 130 * s.d * s.f
+    assert acc["down"]["flops"] == 2 * 130 * s.f * s.d
+    assert layer["active_experts"] == 2 and layer["kept_rows"] == 130
+    assert layer["bytes"] == (2 * 2 * s.f * s.d + s.E * s.d + 2 * s.T * s.d) * el
+
+
+def test_roofline_bound_selection():
+    peaks = dict(bench.FALLBACK_PEAKS)
+    acc = {"k": {"bytes": 1e9, "flops": 1e9}}
+    r = bench.roofline_for("k", acc, 1.0, peaks, "fallback")
+    assert r["bound"] == "hbm" and abs(r["achieved"] - 1000.0) < 1e-6
+    acc = {"k": {"bytes": 1e6, "flops": 1e12}}
+    r = bench.roofline_for("k", acc, 1.0, peaks, "fallback")
+    assert r["bound"] == "tensor" and abs(r["achieved"] - 1000.0) < 1e-6
+
+
+def test_default_arguments_finish_within_minutes(monkeypatch):
+    monkeypatch.setattr("sys.argv", ["bench.py"])
+    a = bench.parse()
+    assert a.gpus == 1 and a.impl == "b300" and a.workload == "switch"
+    assert a.warmup >= 3 and a.steps >= 1
