@@ -178,6 +178,27 @@ int moe_router_scores(const moe_config* cfg, const void* x, const void* W_r,
                       void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * moe_router_scores_noalloc -- moe_router_scores without a workspace, for
+ * callers that cannot allocate device memory per call: a host framework that
+ * owns all device memory and hands none out, or a latency-critical path that
+ * must not enter the CUDA allocator.  The pages have no counterpart of this
+ * entry point; it repackages stage 1 for such callers.
+ * Inputs, output ([T, E] float32 logits, offset included) and arithmetic are
+ * those of moe_router_scores, bit for bit.  The router GEMM's scratch (split
+ * partial logits and the counters of their reduction) lives in one 8 MiB array
+ * inside the library, which every GPU that loads libmoe.so holds until the
+ * process exits.  A layer whose partials do not fit (4 KiB of counters plus
+ * S*T*E*4 bytes, S the reduction split) returns MOE_ERR_UNSUPPORTED.  The
+ * call allocates nothing.  The first call on a device looks up the array's
+ * device address; make that first call before any stream capture.  All calls
+ * share the one array and it keeps the last call's contents: calls that
+ * overlap on the GPU (other streams, other threads) race, so the caller must
+ * serialise them.
+ */
+int moe_router_scores_noalloc(const moe_config* cfg, const void* x, const void* W_r,
+                              const float* logit_offset, float* scores, void* stream);
+
+/*
  * moe_forward_host_io -- moe_forward with the activations in HOST memory:
  * x_host [T, d] is copied to the device, the layer runs, and y_host [T, d]
  * and aux_loss_host [1] are copied back, all enqueued on `stream` (pinned

@@ -24,6 +24,7 @@
 #include <atomic>
 #include <cfloat>
 #include <climits>
+#include <mutex>
 
 #include "common.cuh"
 #include "launch.cuh"
@@ -550,3 +551,100 @@ cudaError_t launch_router_scores(const Plan& p, const void* x, const void* W_r,
 }
 
 }  // namespace moe
+
+// ---------------------------------------------------------------------------
+// Router logits without a caller workspace.
+//
+// For callers that cannot hand the library a workspace: a host framework that
+// owns all device memory and gives none out per call, or code that must not
+// enter the CUDA allocator on its latency path.  The router GEMM's scratch
+// (split-K partial logits and the tile counters of its reduction) lives in the
+// file-scope array below instead.  The array costs every GPU that loads this
+// library kNoAllocScratchBytes of device memory until the process exits.
+//
+// Host code must not pass `g_noalloc_scratch` itself to a kernel: in host code
+// that name is a host-side stand-in, not a device address.  The device address
+// is looked up once per device with cudaGetSymbolAddress (on the first call
+// made with that device current) and cached.
+namespace {
+
+constexpr size_t kNoAllocScratchBytes = 8u << 20;       // 8 MiB
+constexpr size_t kNoAllocCounterBytes = moe::kWsHeaderBytes;   // tile counters, zeroed per call
+
+__device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+std::mutex g_noalloc_mu;
+void* g_noalloc_addr[64] = {};
+int g_noalloc_sms[64] = {};
+
+// Device address of the scratch array (and the SM count) for the current
+// device; resolved once per device.
+int noalloc_setup(void** addr, int* sms) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return MOE_ERR_CUDA;
+  if (dev < 0 || dev >= 64) return MOE_ERR_DEVICE;
+  std::lock_guard<std::mutex> lock(g_noalloc_mu);
+  if (g_noalloc_addr[dev] == nullptr) {
+    int major = 0, minor = 0, n = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return MOE_ERR_CUDA;
+    if (major != 10 || minor != 3) return MOE_ERR_DEVICE;
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr)
+      return MOE_ERR_CUDA;
+    g_noalloc_sms[dev] = n;
+    g_noalloc_addr[dev] = p;
+  }
+  *addr = g_noalloc_addr[dev];
+  *sms = g_noalloc_sms[dev];
+  return MOE_OK;
+}
+
+}  // namespace
+
+extern "C" int moe_router_scores_noalloc(const moe_config* cfg, const void* x, const void* W_r,
+                                         const float* logit_offset, float* scores,
+                                         void* stream) {
+  using namespace moe;
+  if (!cfg) return MOE_ERR_ARG;
+  Plan p;
+  int rc = make_plan(cfg, WsKind::Route, &p);
+  if (rc != MOE_OK) return rc;
+  if (cfg->T == 0) return MOE_OK;
+  if (!x || !W_r || !scores) return MOE_ERR_ARG;
+  if ((reinterpret_cast<uintptr_t>(x) & 15u) || (reinterpret_cast<uintptr_t>(W_r) & 15u) ||
+      (reinterpret_cast<uintptr_t>(scores) & 3u))
+    return MOE_ERR_ARG;
+  // the same split of the reduction as moe_router_scores, which needs
+  // S*T*E floats of partials next to the counters
+  const size_t parts = p.sc_splits > 1 ? sizeof(float) * (size_t)p.sc_splits * cfg->T * cfg->E : 0;
+  if (kNoAllocCounterBytes + parts > kNoAllocScratchBytes) return MOE_ERR_UNSUPPORTED;
+  void* base = nullptr;
+  int sms = 0;
+  rc = noalloc_setup(&base, &sms);
+  if (rc != MOE_OK) return rc;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  // the array keeps the previous call's contents: start the counters at zero
+  if (cudaMemsetAsync(base, 0, kNoAllocCounterBytes, st) != cudaSuccess) return MOE_ERR_CUDA;
+  ScoresArgs a;
+  a.x = x;
+  a.W_r = W_r;
+  a.logit_offset = logit_offset;
+  a.part = reinterpret_cast<float*>(static_cast<unsigned char*>(base) + kNoAllocCounterBytes);
+  a.scores = scores;
+  a.tile_counter = static_cast<unsigned int*>(base);
+  a.T = cfg->T;
+  a.d = cfg->d;
+  a.E = cfg->E;
+  a.k_split = p.sc_ksplit;
+  a.S = p.sc_splits;
+  cudaError_t e;
+  if (cfg->dtype == MOE_BF16)
+    e = p.sc_tn == 4 ? launch_scores_t<__nv_bfloat16, 4>(p, a, st)
+                     : launch_scores_t<__nv_bfloat16, 2>(p, a, st);
+  else
+    e = p.sc_tn == 4 ? launch_scores_t<float, 4>(p, a, st) : launch_scores_t<float, 2>(p, a, st);
+  return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
