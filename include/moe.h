@@ -169,9 +169,11 @@ int moe_route(const moe_config* cfg,
 
 /*
  * moe_router_scores -- stage 1 alone: scores [T, E] float32 (device) gets the
- * router logits s = x W_r^T (+ logit_offset), computed exactly as
- * moe_forward computes them (same kernels, same summation order).  Needs
- * moe_route_workspace_size() bytes.  x and W_r must be 16-byte aligned.
+ * router logits s = x W_r^T (+ logit_offset), from the router kernel
+ * moe_forward uses for the same layer (bf16 layers with T >= 256: tensor-core
+ * products with the reduction added in 128-wide float32 chunks; otherwise
+ * float32 FMA).  Needs moe_route_workspace_size() bytes.  x and W_r must be
+ * 16-byte aligned.
  */
 int moe_router_scores(const moe_config* cfg, const void* x, const void* W_r,
                       const float* logit_offset, float* scores,
@@ -183,9 +185,12 @@ int moe_router_scores(const moe_config* cfg, const void* x, const void* W_r,
  * owns all device memory and hands none out, or a latency-critical path that
  * must not enter the CUDA allocator.  The pages have no counterpart of this
  * entry point; it repackages stage 1 for such callers.
- * Inputs, output ([T, E] float32 logits, offset included) and arithmetic are
- * those of moe_router_scores, bit for bit.  The router GEMM's scratch (split
- * partial logits and the counters of their reduction) lives in one 8 MiB array
+ * Inputs and output ([T, E] float32 logits, offset included) are those of
+ * moe_router_scores; the logits come from the float32 FMA router (bit for bit
+ * what moe_router_scores gives when MOE_ROUTER=simt selects that kernel, and
+ * within 5e-6 of its default tensor-core router for large bf16 batches).  The
+ * router GEMM's scratch (split partial logits and the counters of their
+ * reduction) lives in one 8 MiB array
  * inside the library, which every GPU that loads libmoe.so holds until the
  * process exits.  A layer whose partials do not fit (4 KiB of counters plus
  * S*T*E*4 bytes, S the reduction split) returns MOE_ERR_UNSUPPORTED.  The

@@ -38,7 +38,14 @@
 
 namespace moe {
 
-enum { EPI_SWIGLU = 0, EPI_GELU = 1, EPI_RELU = 2, EPI_F32 = 3 };
+enum { EPI_SWIGLU = 0, EPI_GELU = 1, EPI_RELU = 2, EPI_F32 = 3, EPI_F32_CHUNKED = 4 };
+
+// EPI_F32_CHUNKED: the reduction runs in chunks of kChunkKB k-blocks (128 k),
+// each accumulated by the tensor cores from zero; the epilogue adds the chunk
+// results in float32, round to nearest, in chunk order.  The tensor cores'
+// own float32 accumulation then spans at most 8 MMA steps, which keeps a
+// 7168-wide dot product within ~2e-6 of exact (measured) instead of ~4e-5.
+constexpr int kChunkKB = 2;
 
 struct TcArgs {
   const int* tp;          // [E+2] tile prefix: routed segments, then the shared one
@@ -55,6 +62,7 @@ struct TcArgs {
   int ld_out;
   void* out_sh;           // shared output rows [T_pad][ld_out_sh]
   int ld_out_sh;
+  const float* col_bias;  // EPI_F32_CHUNKED: added per output column (may be null)
   uint32_t* status;
   uint64_t timeout_ns;
 };
@@ -129,6 +137,78 @@ __device__ __forceinline__ TileInfo decode_tile(const TcArgs& a, int tile, int b
 
 __device__ __forceinline__ float silu_mul(float g, float u) {
   return g / (1.0f + __expf(-g)) * u;
+}
+
+// Epilogue of one accumulator: activation (or none), bf16 / fp32 stores of
+// this thread's row, masked at the segment's last row and the last column.
+template <int BNH, bool DUAL, int EPI>
+__device__ __forceinline__ void epilogue_tile(const TcArgs& a, const TileInfo& ti, uint32_t t_row,
+                                              size_t orow, bool row_ok) {
+#pragma unroll 1
+  for (int c = 0; c < BNH; c += 32) {
+    uint32_t r0[32];
+    tmem_ld32(t_row + c, r0);
+    uint32_t r1[32];
+    if (DUAL) tmem_ld32(t_row + BNH + c, r1);
+    tmem_ld_wait();
+    const int col = ti.n0 + c;
+    if (EPI == EPI_F32) {
+      float* out = static_cast<float*>(ti.shared ? a.out_sh : a.out);
+      const int ld = ti.shared ? a.ld_out_sh : a.ld_out;
+      float* dst = out + orow * ld + col;
+      if (!row_ok) {
+      } else if (col + 32 <= ti.N) {
+#pragma unroll
+        for (int v = 0; v < 8; ++v) {
+          float4 f4 = make_float4(__uint_as_float(r0[4 * v]), __uint_as_float(r0[4 * v + 1]),
+                                  __uint_as_float(r0[4 * v + 2]),
+                                  __uint_as_float(r0[4 * v + 3]));
+          reinterpret_cast<float4*>(dst)[v] = f4;
+        }
+      } else {
+#pragma unroll
+        for (int i = 0; i < 32; ++i)
+          if (col + i < ti.N) dst[i] = __uint_as_float(r0[i]);
+      }
+    } else {
+      __nv_bfloat16* out = static_cast<__nv_bfloat16*>(ti.shared ? a.out_sh : a.out);
+      const int ld = ti.shared ? a.ld_out_sh : a.ld_out;
+      __nv_bfloat16* dst = out + orow * ld + col;
+      uint32_t pk[16];
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        float v0 = __uint_as_float(r0[2 * i]), v1 = __uint_as_float(r0[2 * i + 1]);
+        if (EPI == EPI_SWIGLU) {
+          v0 = silu_mul(v0, __uint_as_float(r1[2 * i]));
+          v1 = silu_mul(v1, __uint_as_float(r1[2 * i + 1]));
+        } else if (EPI == EPI_RELU) {
+          v0 = fmaxf(v0, 0.f);
+          v1 = fmaxf(v1, 0.f);
+        } else if (EPI == EPI_GELU) {
+          v0 = 0.5f * v0 * (1.0f + erff(v0 * 0.70710678118654752f));
+          v1 = 0.5f * v1 * (1.0f + erff(v1 * 0.70710678118654752f));
+        }
+        __nv_bfloat162 b2 = __floats2bfloat162_rn(v0, v1);
+        pk[i] = *reinterpret_cast<uint32_t*>(&b2);
+      }
+      if (!row_ok) {
+      } else if (col + 32 <= ti.N) {
+#pragma unroll
+        for (int v = 0; v < 4; ++v)
+          reinterpret_cast<uint4*>(dst)[v] =
+              make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
+      } else {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          if (col + i < ti.N) {
+            const uint32_t w = pk[i >> 1];
+            reinterpret_cast<uint16_t*>(dst)[i] =
+                (i & 1) ? static_cast<uint16_t>(w >> 16) : static_cast<uint16_t>(w);
+          }
+        }
+      }
+    }
+  }
 }
 
 template <int BNH, bool DUAL, int EPI>
@@ -242,39 +322,43 @@ tc_grouped_gemm(const __grid_constant__ CUtensorMap mA, const __grid_constant__ 
       uint32_t g = 0;
       int it = 0;
       bool ok = true;
-      for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x, ++it) {
+      for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
         const TileInfo ti = decode_tile(a, tile, BNH);
-        const int ab = it & 1;
-        const uint32_t aph = (it >> 1) & 1;
-        if (!mbar_wait_bounded(tempty_bar(ab), aph ^ 1u, a.timeout_ns, abort_flag)) {
-          give_up();
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        const uint32_t d_tmem = tmem_base + ab * C::MMA_N;
         const int nk = (ti.K + C::BK - 1) / C::BK;
-        for (int kb = 0; kb < nk; ++kb, ++g) {
-          const int s = g % C::STAGES;
-          const uint32_t ph = (g / C::STAGES) & 1u;
-          if (!mbar_wait_bounded(full_bar(s), ph, a.timeout_ns, abort_flag)) {
+        const int ck = EPI == EPI_F32_CHUNKED ? kChunkKB : nk;   // k-blocks per accumulator
+        for (int kb0 = 0; kb0 < nk && ok; kb0 += ck, ++it) {
+          const int ab = it & 1;
+          const uint32_t aph = (it >> 1) & 1;
+          if (!mbar_wait_bounded(tempty_bar(ab), aph ^ 1u, a.timeout_ns, abort_flag)) {
             give_up();
             ok = false;
             break;
           }
           tc_fence_after();
-          const uint32_t sa = smem_base + s * C::STAGE_BYTES;
-          const uint32_t sb = sa + C::A_BYTES;
+          const uint32_t d_tmem = tmem_base + ab * C::MMA_N;
+          const int kb1 = kb0 + ck < nk ? kb0 + ck : nk;
+          for (int kb = kb0; kb < kb1; ++kb, ++g) {
+            const int s = g % C::STAGES;
+            const uint32_t ph = (g / C::STAGES) & 1u;
+            if (!mbar_wait_bounded(full_bar(s), ph, a.timeout_ns, abort_flag)) {
+              give_up();
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const uint32_t sa = smem_base + s * C::STAGE_BYTES;
+            const uint32_t sb = sa + C::A_BYTES;
 #pragma unroll
-          for (int kk = 0; kk < C::BK / 16; ++kk) {
-            const uint64_t ad = smem_desc_k128(sa + kk * 32);
-            const uint64_t bd = smem_desc_k128(sb + kk * 32);
-            tc_mma_bf16(d_tmem, ad, bd, C::IDESC, (kb | kk) != 0 ? 1u : 0u);
+            for (int kk = 0; kk < C::BK / 16; ++kk) {
+              const uint64_t ad = smem_desc_k128(sa + kk * 32);
+              const uint64_t bd = smem_desc_k128(sb + kk * 32);
+              tc_mma_bf16(d_tmem, ad, bd, C::IDESC, (kb != kb0 || kk != 0) ? 1u : 0u);
+            }
+            tc_commit(empty_bar(s));
           }
-          tc_commit(empty_bar(s));
+          if (!ok) break;
+          tc_commit(tfull_bar(ab));
         }
-        if (!ok) break;
-        tc_commit(tfull_bar(ab));
       }
       if (!ok) {
         tc_commit(drain_bar);
@@ -286,85 +370,53 @@ tc_grouped_gemm(const __grid_constant__ CUtensorMap mA, const __grid_constant__ 
     const int q = warp & 3;                  // TMEM lane quarter this warp may read
     const int row_in_tile = q * 32 + lane;
     int it = 0;
-    for (int tile = blockIdx.x; tile < total; tile += gridDim.x, ++it) {
+    bool ok = true;
+    for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
       const TileInfo ti = decode_tile(a, tile, BNH);
-      const int ab = it & 1;
-      const uint32_t aph = (it >> 1) & 1;
-      if (!mbar_wait_bounded(tfull_bar(ab), aph, a.timeout_ns, abort_flag)) {
-        give_up();
-        break;
-      }
-      tc_fence_after();
-      const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + ab * C::MMA_N;
       const size_t orow = static_cast<size_t>(ti.a_row + row_in_tile);
       const bool row_ok = ti.a_row + row_in_tile < ti.row_end;
-#pragma unroll 1
-      for (int c = 0; c < BNH; c += 32) {
-        uint32_t r0[32];
-        tmem_ld32(t_row + c, r0);
-        uint32_t r1[32];
-        if (DUAL) tmem_ld32(t_row + BNH + c, r1);
-        tmem_ld_wait();
-        const int col = ti.n0 + c;
-        if (EPI == EPI_F32) {
-          float* out = static_cast<float*>(ti.shared ? a.out_sh : a.out);
-          const int ld = ti.shared ? a.ld_out_sh : a.ld_out;
-          float* dst = out + orow * ld + col;
-          if (!row_ok) {
-          } else if (col + 32 <= ti.N) {
+      const int nk = (ti.K + C::BK - 1) / C::BK;
+      const int ck = EPI == EPI_F32_CHUNKED ? kChunkKB : nk;
+      float csum[EPI == EPI_F32_CHUNKED ? BNH : 1];
+      if constexpr (EPI == EPI_F32_CHUNKED) {
 #pragma unroll
-            for (int v = 0; v < 8; ++v) {
-              float4 f4 = make_float4(__uint_as_float(r0[4 * v]), __uint_as_float(r0[4 * v + 1]),
-                                      __uint_as_float(r0[4 * v + 2]),
-                                      __uint_as_float(r0[4 * v + 3]));
-              reinterpret_cast<float4*>(dst)[v] = f4;
-            }
-          } else {
+        for (int i = 0; i < BNH; ++i) csum[i] = 0.f;
+      }
+      for (int kb0 = 0; kb0 < nk; kb0 += ck, ++it) {
+        const int ab = it & 1;
+        const uint32_t aph = (it >> 1) & 1;
+        if (!mbar_wait_bounded(tfull_bar(ab), aph, a.timeout_ns, abort_flag)) {
+          give_up();
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + ab * C::MMA_N;
+        if constexpr (EPI == EPI_F32_CHUNKED) {
 #pragma unroll
-            for (int i = 0; i < 32; ++i)
-              if (col + i < ti.N) dst[i] = __uint_as_float(r0[i]);
+          for (int c = 0; c < BNH; c += 32) {
+            uint32_t r0[32];
+            tmem_ld32(t_row + c, r0);
+            tmem_ld_wait();
+#pragma unroll
+            for (int i = 0; i < 32; ++i) csum[c + i] += __uint_as_float(r0[i]);
           }
         } else {
-          __nv_bfloat16* out = static_cast<__nv_bfloat16*>(ti.shared ? a.out_sh : a.out);
-          const int ld = ti.shared ? a.ld_out_sh : a.ld_out;
-          __nv_bfloat16* dst = out + orow * ld + col;
-          uint32_t pk[16];
+          epilogue_tile<BNH, DUAL, EPI>(a, ti, t_row, orow, row_ok);
+        }
+        tc_fence_before();
+        mbar_arrive(tempty_bar(ab));
+      }
+      if constexpr (EPI == EPI_F32_CHUNKED) {
+        if (ok && row_ok) {
+          float* dst = static_cast<float*>(a.out) + orow * a.ld_out + ti.n0;
 #pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            float v0 = __uint_as_float(r0[2 * i]), v1 = __uint_as_float(r0[2 * i + 1]);
-            if (EPI == EPI_SWIGLU) {
-              v0 = silu_mul(v0, __uint_as_float(r1[2 * i]));
-              v1 = silu_mul(v1, __uint_as_float(r1[2 * i + 1]));
-            } else if (EPI == EPI_RELU) {
-              v0 = fmaxf(v0, 0.f);
-              v1 = fmaxf(v1, 0.f);
-            } else if (EPI == EPI_GELU) {
-              v0 = 0.5f * v0 * (1.0f + erff(v0 * 0.70710678118654752f));
-              v1 = 0.5f * v1 * (1.0f + erff(v1 * 0.70710678118654752f));
-            }
-            __nv_bfloat162 b2 = __floats2bfloat162_rn(v0, v1);
-            pk[i] = *reinterpret_cast<uint32_t*>(&b2);
-          }
-          if (!row_ok) {
-          } else if (col + 32 <= ti.N) {
-#pragma unroll
-            for (int v = 0; v < 4; ++v)
-              reinterpret_cast<uint4*>(dst)[v] =
-                  make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
-          } else {
-#pragma unroll
-            for (int i = 0; i < 32; ++i) {
-              if (col + i < ti.N) {
-                const uint32_t w = pk[i >> 1];
-                reinterpret_cast<uint16_t*>(dst)[i] =
-                    (i & 1) ? static_cast<uint16_t>(w >> 16) : static_cast<uint16_t>(w);
-              }
-            }
+          for (int i = 0; i < BNH; ++i) {
+            const int col = ti.n0 + i;
+            if (col < ti.N) dst[i] = csum[i] + (a.col_bias ? a.col_bias[col] : 0.f);
           }
         }
       }
-      tc_fence_before();
-      mbar_arrive(tempty_bar(ab));
     }
   }
 
@@ -529,6 +581,7 @@ cudaError_t launch_experts_tc(const Plan& p, const void* x, const void* W1, cons
   au.rows_sh = c.T;
   au.static_mt = 0;
   au.static_total = 0;
+  au.col_bias = nullptr;
   au.E = c.E;
   au.has_shared = sh ? 1 : 0;
   au.N = c.f;
@@ -578,12 +631,15 @@ cudaError_t launch_experts_tc(const Plan& p, const void* x, const void* W1, cons
 }
 
 // ---------------------------------------------------------------- router
-// Router logits s = x W_r^T on the tensor cores: bf16 operands (their products
-// are exact), float32 accumulation in tensor memory, float32 output [T][E].
+// Router logits s = x W_r^T (+ offset) on the tensor cores: bf16 operands
+// (their products are exact), each 128-wide chunk of the reduction
+// accumulated in tensor memory, the chunks added in float32 by the epilogue,
+// float32 output [T][E].
 constexpr int kRouterTcBN = 64;
 
-cudaError_t launch_router_tc(const Plan& p, const void* x, const void* W_r, float* scores,
-                             uint32_t* status, cudaStream_t st) {
+cudaError_t launch_router_tc(const Plan& p, const void* x, const void* W_r,
+                             const float* logit_offset, float* scores, uint32_t* status,
+                             cudaStream_t st) {
   const moe_config& c = p.cfg;
   TcMaps m;
   bool ok = encode_2d(&m.A, x, c.T, c.d, kTcBM);
@@ -601,10 +657,11 @@ cudaError_t launch_router_tc(const Plan& p, const void* x, const void* W_r, floa
   a.rows_sh = c.T;
   a.static_mt = (c.T + kTcBM - 1) / kTcBM;
   a.static_total = a.static_mt * ((c.E + kRouterTcBN - 1) / kRouterTcBN);
+  a.col_bias = logit_offset;
   a.status = status;
   a.timeout_ns = kGemmTimeoutNs;
   const int grid = a.static_total < p.num_sms ? a.static_total : p.num_sms;
-  return run_tc<kRouterTcBN, false, EPI_F32>(m, a, grid, st);
+  return run_tc<kRouterTcBN, false, EPI_F32_CHUNKED>(m, a, grid, st);
 }
 
 // ---------------------------------------------------------------- self-test

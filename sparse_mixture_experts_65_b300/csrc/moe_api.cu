@@ -71,7 +71,24 @@ int make_plan(const moe_config* cfg, WsKind kind, Plan* p, int num_sms) {
   } else {
     P.capacity = INT_MAX;
   }
+  // Router path.  Fused (E <= 256, batches of at least kFusedMinT tokens):
+  // one kernel per 16*TM tokens computes all logits over the full width, then
+  // routes; TN = experts per thread = next_pow2(E)/16.  Otherwise the split
+  // path: a split-K logits kernel, then the top-k kernel.
+  // MOE_ROUTER=simt forces the split path, MOE_ROUTER=fused the fused one.
   {
+    const char* r = std::getenv("MOE_ROUTER");
+    const bool force_split = r && std::strcmp(r, "simt") == 0;
+    const bool force_fused = r && std::strcmp(r, "fused") == 0;
+    int ep = 32;
+    while (ep < c.E) ep <<= 1;
+    P.fu_tn = ep <= 256 ? ep / 16 : 0;
+    P.fu_tm = ceil_div(c.T, 32) >= 64 ? 2 : 1;
+    P.router_fused = P.fu_tn > 0 && !force_split && force_fused;
+  }
+  if (P.router_fused) {
+    P.BT = 16 * P.fu_tm;
+  } else {
     // routing blocks: 16 tokens per pass (one per warp), enough passes that
     // the batch needs about kRouteMaxBlocks blocks, at most kRouteMaxBT tokens
     const int passes = ceil_div(c.T, kRouteTokensPerPass * kRouteMaxBlocks);
@@ -107,18 +124,18 @@ int make_plan(const moe_config* cfg, WsKind kind, Plan* p, int num_sms) {
     P.sc_ksplit = ceil_div(ceil_div(c.d, S), 32) * 32;
     P.sc_splits = ceil_div(c.d, P.sc_ksplit);
   }
-  // The router runs on float32 FMA: its logits stay within 1e-6 of the exact
-  // values, well inside the 1e-5 band in which near-tied experts may swap.
-  // MOE_ROUTER=tc (bf16 layers only) moves it to the tensor cores, which are
-  // ~30x faster but whose float32 accumulation errs by up to ~4e-5 on a
-  // 7168-wide router; it is an experiment switch, never the default.
+  // Router logits: bf16 layers with at least kRouterTcMinT tokens use the
+  // tensor cores with 128-wide float32 chunks (max error ~2e-6 on a 7168-wide
+  // router, measured; float32 FMA: ~8e-7); both stay inside half the 1e-5
+  // band in which near-tied experts may swap.  Smaller batches and float32
+  // layers use the split float32 FMA kernel.  MOE_ROUTER=simt / fused / tc
+  // forces a path.
   {
     const char* r = std::getenv("MOE_ROUTER");
-    P.router_tc = c.dtype == MOE_BF16 && r && std::strcmp(r, "tc") == 0;
-    if (P.router_tc) {
-      P.sc_splits = 1;
-      P.sc_ksplit = c.d;
-    }
+    const bool force_tc = r && std::strcmp(r, "tc") == 0;
+    const bool forced_other = r && (std::strcmp(r, "simt") == 0 || std::strcmp(r, "fused") == 0);
+    P.router_tc = c.dtype == MOE_BF16 && (force_tc || (!forced_other && c.T >= kRouterTcMinT));
+    if (P.router_tc) P.router_fused = false;
   }
   P.tc = c.dtype == MOE_BF16;
   P.bm = P.tc ? kTcBM : kSimtBM;
@@ -171,7 +188,11 @@ int make_plan(const moe_config* cfg, WsKind kind, Plan* p, int num_sms) {
   const size_t E = c.E;
   L.status = take(kWsHeaderBytes);
   L.scores = take(sizeof(float) * (size_t)c.T * E);
-  L.score_parts = take(P.sc_splits > 1 ? sizeof(float) * (size_t)P.sc_splits * c.T * E : 0);
+  // split partials only when the split float32 router runs (sc_* keep that
+  // kernel's geometry whichever path this layer takes)
+  const bool split_router = !P.router_tc && !P.router_fused;
+  L.score_parts = take(split_router && P.sc_splits > 1
+                           ? sizeof(float) * (size_t)P.sc_splits * c.T * E : 0);
   L.blk_cnt = take(sizeof(int) * (size_t)P.nblk * E);
   L.blk_prob = take(sizeof(float) * (size_t)P.nblk * E);
   L.meta = take(sizeof(int) * (E + (E + 1) * 3 + (E + 2) * 2));

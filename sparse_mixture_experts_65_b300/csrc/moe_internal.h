@@ -14,6 +14,8 @@ constexpr int kThreads = 256;        // block size of the SIMT kernels
 constexpr int kRouteTokensPerPass = 16;   // tokens a top-k block handles at once (one per warp)
 constexpr int kRouteMaxBlocks = 128;      // routing blocks are sized to stay near this count
 constexpr int kRouteMaxBT = 256;
+constexpr int kFusedMinT = 1024;          // smaller batches route through the split path
+constexpr int kRouterTcMinT = 256;        // bf16 batches from this size use the tensor-core router
 constexpr int kMaxE = 512;
 constexpr int kMaxK = 32;
 constexpr int kSegAlign = 128;       // expert segments start on multiples of this row
@@ -53,7 +55,9 @@ struct Plan {
   int capacity;       // INT32_MAX when unlimited
   int BT;             // tokens per routing block
   int nblk;           // routing blocks
-  bool router_tc;     // router logits on the tensor cores (bf16 path, large T)
+  bool router_tc;     // router logits on the tensor cores (experiment switch)
+  bool router_fused;  // one kernel: logits, top-k, histogram, scan (E <= 256)
+  int fu_tm, fu_tn;   // fused router: tokens per thread (1, 2), experts per thread
   int sc_tn;          // router GEMM: experts per thread (2 or 4)
   int sc_mblocks, sc_nblocks, sc_splits, sc_ksplit;   // router GEMM grid and K split
   int bm;             // rows per GEMM tile (128 tensor core, 64 SIMT)
@@ -100,8 +104,9 @@ struct ScanOutputs {
 cudaError_t launch_router(const Plan& p, const void* x, const void* W_r, const float* logit_offset,
                           const float* sel_bias, int32_t* topk_idx, float* topk_w, void* ws,
                           const ScanOutputs& so, cudaStream_t st, cudaEvent_t mid_event);
-cudaError_t launch_router_tc(const Plan& p, const void* x, const void* W_r, float* scores,
-                             uint32_t* status, cudaStream_t st);
+cudaError_t launch_router_tc(const Plan& p, const void* x, const void* W_r,
+                             const float* logit_offset, float* scores, uint32_t* status,
+                             cudaStream_t st);
 cudaError_t launch_router_scores(const Plan& p, const void* x, const void* W_r,
                                  const float* logit_offset, float* out, void* ws,
                                  cudaStream_t st);

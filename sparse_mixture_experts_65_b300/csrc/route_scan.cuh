@@ -78,14 +78,15 @@ __device__ __forceinline__ int block_exscan(int v, int* scratch, int* total) {
   return out;
 }
 
-// One block of NT threads.  G = NT / next_pow2(E) threads share expert e:
+// One block of NT threads, E <= NT (the split path runs it with 512 threads for
+// E <= 512, the fused router with 256 threads for E <= 256).
+// G = NT / next_pow2(E) threads share expert e:
 // each sums a contiguous run of routing blocks, one thread per expert scans
 // the G partial counts, and every thread then writes the exclusive per-block
 // bases of its run.  Threads e < E then finish the per-expert values (kept
 // count, segment start, tile counts, f_i, P_i) and the block-wide scans.
 template <int NT>
 __device__ void scan_block(const ScanArgs& a, ScanSmem<NT>& sm) {
-  static_assert(NT >= kMaxE, "one thread per expert in the final pass");
   const int tid = threadIdx.x;
   int Epow = 1;
   while (Epow < a.E) Epow <<= 1;

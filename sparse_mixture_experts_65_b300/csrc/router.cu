@@ -24,6 +24,8 @@
 #include <atomic>
 #include <cfloat>
 #include <climits>
+#include <cstdlib>
+#include <cstring>
 #include <mutex>
 
 #include "common.cuh"
@@ -260,10 +262,129 @@ __global__ void __launch_bounds__(kThreads) router_scores_kernel(const ScoresArg
 }
 
 // ---------------------------------------------------------------- top-k
+// One warp routes one token.  sv[i] holds the logit of expert lane + 32 i
+// (logit offset included, -inf past E).  Selection: k rounds of warp arg-max
+// over sel = affinity + bias (larger first, equal to the lower index; NaN never
+// outranks a number).  Gates from the unbiased logits; the full router
+// distribution (softmax, or sigmoid normalised over all E) is added to psum;
+// the chosen experts are counted into the block histogram `cnt`.
+template <int NPL_MAX>
+__device__ __forceinline__ void route_one_token(const float (&sv)[NPL_MAX], int E, int k, int gate,
+                                                const float* sel_bias, int32_t* idx_out,
+                                                float* w_out, int* cnt,
+                                                float (&psum)[NPL_MAX]) {
+  const int lane = threadIdx.x & 31;
+  const bool sigm = gate == MOE_GATE_SIGMOID_RENORM;
+  float sel[NPL_MAX];
+#pragma unroll
+  for (int i = 0; i < NPL_MAX; ++i) {
+    const int e = lane + 32 * i;
+    sel[i] = -INFINITY;
+    if (e < E) {
+      float v = sigm ? sigmoidf_(sv[i]) : sv[i];
+      if (sel_bias) v += sel_bias[e];
+      sel[i] = (v != v) ? -INFINITY : v;
+    }
+  }
+  uint32_t taken = 0;
+  int my_idx = 0;
+  float my_s = -INFINITY;
+  for (int r = 0; r < k; ++r) {
+    float bv = -INFINITY, bs = -INFINITY;
+    int bi = INT_MAX;
+#pragma unroll
+    for (int i = 0; i < NPL_MAX; ++i) {
+      const int e = lane + 32 * i;
+      if (e < E && !((taken >> i) & 1u)) {
+        if (sel[i] > bv || (sel[i] == bv && e < bi)) {
+          bv = sel[i];
+          bi = e;
+          bs = sv[i];
+        }
+      }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+      const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+      const float os = __shfl_xor_sync(0xffffffffu, bs, o);
+      if (ov > bv || (ov == bv && oi < bi)) {
+        bv = ov;
+        bi = oi;
+        bs = os;
+      }
+    }
+    if (bi < E && (bi & 31) == lane) taken |= 1u << (bi >> 5);
+    if (lane == r) {
+      my_idx = bi < E ? bi : 0;
+      my_s = bs;
+    }
+  }
+  const bool mine = lane < k;
+  const float s_me = mine ? my_s : -INFINITY;
+  float m_all = -INFINITY;
+#pragma unroll
+  for (int i = 0; i < NPL_MAX; ++i) m_all = fmaxf(m_all, sv[i]);
+  m_all = warp_max(m_all);
+  float z_all = 0.f;
+#pragma unroll
+  for (int i = 0; i < NPL_MAX; ++i)
+    if (lane + 32 * i < E) z_all += sigm ? sigmoidf_(sv[i]) : expf(sv[i] - m_all);
+  z_all = warp_sum(z_all);
+  float g;
+  if (gate == MOE_GATE_SOFTMAX_TOPK) {
+    const float m_k = warp_max(s_me);
+    const float ek = mine ? expf(s_me - m_k) : 0.f;
+    g = ek / warp_sum(ek);
+  } else if (sigm) {
+    const float ak = mine ? sigmoidf_(s_me) : 0.f;
+    g = ak / warp_sum(ak);
+  } else {
+    g = expf(s_me - m_all) / z_all;
+  }
+  if (mine) {
+    idx_out[lane] = my_idx;
+    w_out[lane] = g;
+    atomicAdd(&cnt[my_idx], 1);
+  }
+#pragma unroll
+  for (int i = 0; i < NPL_MAX; ++i)
+    if (lane + 32 * i < E)
+      psum[i] += sigm ? sigmoidf_(sv[i]) / z_all : expf(sv[i] - m_all) / z_all;
+}
+
+// Block epilogue of a routing block: the per-warp probability sums (fixed
+// warp order) and the histogram go to the block's row; the last block to
+// finish runs the capacity scan for the whole batch.
+template <int NT, int NPL_MAX>
+__device__ __forceinline__ void publish_and_scan(const ScanArgs& a, const float (&psum)[NPL_MAX],
+                                                 float (*Pw)[kMaxE], const int* cnt,
+                                                 ScanSmem<NT>& scan_sm, int* am_last) {
+  constexpr int NW = NT / 32;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+#pragma unroll
+  for (int i = 0; i < NPL_MAX; ++i)
+    if (lane + 32 * i < a.E) Pw[warp][lane + 32 * i] = psum[i];
+  __syncthreads();
+  for (int e = tid; e < a.E; e += NT) {
+    float s = 0.f;
+#pragma unroll
+    for (int w = 0; w < NW; ++w) s += Pw[w][e];
+    a.blk_prob[(size_t)blockIdx.x * a.E + e] = s;
+    a.blk_cnt[(size_t)blockIdx.x * a.E + e] = cnt[e];
+  }
+  __threadfence();
+  __syncthreads();
+  if (tid == 0) *am_last = atomicAdd(a.done_counter, 1u) == gridDim.x - 1;
+  __syncthreads();
+  if (!*am_last) return;
+  __threadfence();
+  scan_block<NT>(a, scan_sm);
+  if (tid == 0) *a.done_counter = 0;
+}
+
 struct TopkArgs {
-  const float* part;         // [S][T][E]
-  int S;
-  const float* logit_offset;
+  const float* scores;       // [T][E] logits, offset included
   const float* sel_bias;
   int32_t* topk_idx;
   float* topk_w;
@@ -282,16 +403,13 @@ union TopkSmem {
   ScanSmem<kTopkThreads> scan;
 };
 
-// One routing block of BT tokens; warp w takes tokens w, w + 16, ...  After
-// the block has published its histogram and probability sums, the last block
-// to finish runs the capacity scan for the whole batch.
+// Split path: one routing block of BT tokens, warp w takes tokens w, w + 16, ...
 __global__ void __launch_bounds__(kTopkThreads) router_topk_kernel(const TopkArgs a) {
   __shared__ TopkSmem sm;
   __shared__ int am_last;
   const int tid = threadIdx.x;
   const int warp = tid >> 5, lane = tid & 31;
   const int E = a.E;
-  const int NPL = (E + 31) >> 5;     // scores per lane, <= 16
   for (int e = tid; e < E; e += kTopkThreads) sm.t.cnt[e] = 0;
   pdl_wait();
   pdl_trigger();
@@ -299,139 +417,217 @@ __global__ void __launch_bounds__(kTopkThreads) router_topk_kernel(const TopkArg
   float psum[16];
 #pragma unroll
   for (int i = 0; i < 16; ++i) psum[i] = 0.f;
-  const bool sigm = a.gate == MOE_GATE_SIGMOID_RENORM;
-  const size_t TE = (size_t)a.T * E;
   const int t0 = blockIdx.x * a.BT;
-
   for (int tl = warp; tl < a.BT; tl += kTopkWarps) {
     const int t = t0 + tl;
     if (t >= a.T) break;
-    float sv[16], sel[16];
-#pragma unroll
-    for (int i = 0; i < 16; ++i) {
-      sv[i] = -INFINITY;
-      sel[i] = -INFINITY;
-    }
-    // the split partials: all loads first, then the sums in split order
+    float sv[16];
 #pragma unroll
     for (int i = 0; i < 16; ++i) {
       const int e = lane + 32 * i;
-      if (i < NPL && e < E) sv[i] = a.part[(size_t)t * E + e];
+      sv[i] = e < E ? a.scores[(size_t)t * E + e] : -INFINITY;
     }
-    for (int z = 1; z < a.S; ++z) {
-      float pz[16];
-#pragma unroll
-      for (int i = 0; i < 16; ++i) {
-        const int e = lane + 32 * i;
-        pz[i] = (i < NPL && e < E) ? a.part[z * TE + (size_t)t * E + e] : 0.f;
-      }
-#pragma unroll
-      for (int i = 0; i < 16; ++i) sv[i] += pz[i];
+    route_one_token<16>(sv, E, a.k, a.gate, a.sel_bias, a.topk_idx + (size_t)t * a.k,
+                        a.topk_w + (size_t)t * a.k, sm.t.cnt, psum);
+  }
+  publish_and_scan<kTopkThreads, 16>(a.scan, psum, sm.t.Pw, sm.t.cnt, sm.scan, &am_last);
+}
+
+// ---------------------------------------------------------------- fused router
+// Fused path (E <= 256): one block computes the float32 logits of BM = 16 TM
+// tokens for all experts over the full model width, keeps them in shared
+// memory, routes its tokens (one warp per token) and publishes its histogram;
+// the last block runs the capacity scan.  Thread (ty, tx) of 16 x 16 owns
+// tokens ty*TM .. +TM-1 and experts tx*TN .. +TN-1 (E padded to 16 TN).
+struct FusedArgs {
+  const void* x;
+  const void* W_r;
+  const float* logit_offset;
+  const float* sel_bias;
+  int32_t* topk_idx;
+  float* topk_w;
+  float* scores_out;         // logits-only mode: write [T][E] and stop
+  int T, d, E, k, gate;
+  ScanArgs scan;
+};
+
+constexpr int kFuBK = 32, kFuStages = 3;
+
+template <typename TIn, int TM, int TN>
+struct FusedCfg {
+  static constexpr int BM = 16 * TM, EP = 16 * TN;
+  static constexpr int EPC = 16 / sizeof(TIn), LD = kFuBK + EPC, CPR = kFuBK / EPC;
+  static constexpr size_t A_RAW = (size_t)BM * LD * sizeof(TIn);
+  static constexpr size_t B_RAW = (size_t)EP * LD * sizeof(TIn);
+  static constexpr size_t AF = (size_t)kFuBK * (BM + 4) * sizeof(float);
+  static constexpr size_t BF = (size_t)kFuBK * (EP + 4) * sizeof(float);
+  static constexpr size_t PIPE = AF + BF + kFuStages * (A_RAW + B_RAW);
+  static constexpr size_t ROUTE = (size_t)BM * (EP + 1) * sizeof(float) +
+                                  sizeof(float) * 8 * kMaxE + sizeof(int) * kMaxE;
+  static constexpr size_t SCAN = sizeof(ScanSmem<kThreads>);
+  static constexpr size_t SMEM = PIPE > ROUTE ? (PIPE > SCAN ? PIPE : SCAN)
+                                              : (ROUTE > SCAN ? ROUTE : SCAN);
+};
+
+template <typename TIn, int TM, int TN>
+__global__ void __launch_bounds__(kThreads) router_fused_kernel(const FusedArgs a) {
+  using C = FusedCfg<TIn, TM, TN>;
+  constexpr int BM = C::BM, EP = C::EP, LD = C::LD, CPR = C::CPR, EPC = C::EPC;
+  constexpr int BK = kFuBK;
+  extern __shared__ __align__(16) uint8_t fu_smem[];
+  float* Af = reinterpret_cast<float*>(fu_smem);                    // [BK][BM+4]
+  float* Bf = Af + BK * (BM + 4);                                   // [BK][EP+4]
+  TIn* As = reinterpret_cast<TIn*>(Bf + BK * (EP + 4));             // [stages][BM][LD]
+  TIn* Bs = As + kFuStages * BM * LD;                               // [stages][EP][LD]
+  __shared__ int am_last;
+  const int tid = threadIdx.x;
+  const int tx = tid & 15, ty = tid >> 4;
+  const int m0 = blockIdx.x * BM;
+  const TIn* X = static_cast<const TIn*>(a.x);
+  const TIn* Wr = static_cast<const TIn*>(a.W_r);
+  pdl_wait();
+  pdl_trigger();
+
+  auto issue = [&](int stage, int k0) {
+    TIn* as = As + stage * BM * LD;
+    TIn* bs = Bs + stage * EP * LD;
+    for (int c = tid; c < BM * CPR; c += kThreads) {
+      const int r = c % BM, kc = (c / BM) * EPC;
+      const int gm = m0 + r, gk = k0 + kc;
+      const bool ok = gm < a.T && gk < a.d;
+      cp_async16(as + r * LD + kc, X + (ok ? (size_t)gm * a.d + gk : 0), ok);
     }
+    for (int c = tid; c < EP * CPR; c += kThreads) {
+      const int r = c % EP, kc = (c / EP) * EPC;
+      const int gk = k0 + kc;
+      const bool ok = r < a.E && gk < a.d;
+      cp_async16(bs + r * LD + kc, Wr + (ok ? (size_t)r * a.d + gk : 0), ok);
+    }
+  };
+  auto convert = [&](int stage) {
+    const TIn* as = As + stage * BM * LD;
+    const TIn* bs = Bs + stage * EP * LD;
+    for (int c = tid; c < BM * CPR; c += kThreads) {
+      const int r = c % BM, kc = (c / BM) * EPC;
+      float v[8];
+      to_float8(*reinterpret_cast<const uint4*>(as + r * LD + kc), as, v);
 #pragma unroll
-    for (int i = 0; i < 16; ++i) {
-      const int e = lane + 32 * i;
-      if (i < NPL && e < E) {
-        float s = sv[i];
-        if (a.logit_offset) s += a.logit_offset[e];
-        sv[i] = s;
-        float v = sigm ? sigmoidf_(s) : s;
-        if (a.sel_bias) v += a.sel_bias[e];
-        sel[i] = (v != v) ? -INFINITY : v;   // NaN never outranks a number
+      for (int i = 0; i < EPC; ++i) Af[(kc + i) * (BM + 4) + r] = v[i];
+    }
+    for (int c = tid; c < EP * CPR; c += kThreads) {
+      const int r = c % EP, kc = (c / EP) * EPC;
+      float v[8];
+      to_float8(*reinterpret_cast<const uint4*>(bs + r * LD + kc), bs, v);
+#pragma unroll
+      for (int i = 0; i < EPC; ++i) Bf[(kc + i) * (EP + 4) + r] = v[i];
+    }
+  };
+
+  float acc[TM][TN], part[TM][TN];
+#pragma unroll
+  for (int i = 0; i < TM; ++i)
+#pragma unroll
+    for (int j = 0; j < TN; ++j) acc[i][j] = part[i][j] = 0.f;
+  const int nk = (a.d + BK - 1) / BK;
+#pragma unroll
+  for (int s = 0; s < kFuStages - 1; ++s) {
+    if (s < nk) issue(s, s * BK);
+    cp_async_commit();
+  }
+  for (int it = 0; it < nk; ++it) {
+    cp_async_wait<kFuStages - 2>();
+    __syncthreads();
+    convert(it % kFuStages);
+    {
+      const int nxt = it + kFuStages - 1;
+      if (nxt < nk) issue(nxt % kFuStages, nxt * BK);
+      cp_async_commit();
+    }
+    __syncthreads();
+#pragma unroll 8
+    for (int kk = 0; kk < BK; ++kk) {
+      float av[TM], bv[TN];
+      if (TM == 2) {
+        const float2 a2 = *reinterpret_cast<const float2*>(Af + kk * (BM + 4) + ty * TM);
+        av[0] = a2.x;
+        av[TM - 1] = a2.y;
       } else {
-        sv[i] = -INFINITY;
+        av[0] = Af[kk * (BM + 4) + ty];
       }
-    }
-    uint32_t taken = 0;
-    int my_idx = 0;
-    float my_s = -INFINITY;
-    for (int r = 0; r < a.k; ++r) {
-      float bv = -INFINITY, bs = -INFINITY;
-      int bi = INT_MAX;
+      if (TN >= 4) {
 #pragma unroll
-      for (int i = 0; i < 16; ++i) {
-        const int e = lane + 32 * i;
-        if (i < NPL && e < E && !((taken >> i) & 1u)) {
-          if (sel[i] > bv || (sel[i] == bv && e < bi)) {
-            bv = sel[i];
-            bi = e;
-            bs = sv[i];
-          }
+        for (int j = 0; j < TN; j += 4) {
+          const float4 b4 = *reinterpret_cast<const float4*>(Bf + kk * (EP + 4) + tx * TN + j);
+          bv[j] = b4.x;
+          bv[j + 1] = b4.y;
+          bv[j + 2] = b4.z;
+          bv[j + 3] = b4.w;
         }
+      } else {
+        const float2 b2 = *reinterpret_cast<const float2*>(Bf + kk * (EP + 4) + tx * TN);
+        bv[0] = b2.x;
+        bv[TN - 1] = b2.y;
       }
 #pragma unroll
-      for (int o = 16; o > 0; o >>= 1) {
-        const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-        const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
-        const float os = __shfl_xor_sync(0xffffffffu, bs, o);
-        if (ov > bv || (ov == bv && oi < bi)) {
-          bv = ov;
-          bi = oi;
-          bs = os;
+      for (int i = 0; i < TM; ++i)
+#pragma unroll
+        for (int j = 0; j < TN; ++j) part[i][j] = fmaf(av[i], bv[j], part[i][j]);
+    }
+    if ((it & 3) == 3 || it + 1 == nk) {   // fold every 128 k into the running sum
+#pragma unroll
+      for (int i = 0; i < TM; ++i)
+#pragma unroll
+        for (int j = 0; j < TN; ++j) {
+          acc[i][j] += part[i][j];
+          part[i][j] = 0.f;
         }
-      }
-      if (bi < E && (bi & 31) == lane) taken |= 1u << (bi >> 5);
-      if (lane == r) {
-        my_idx = bi < E ? bi : 0;
-        my_s = bs;
-      }
     }
-    const bool mine = lane < a.k;
-    const float s_me = mine ? my_s : -INFINITY;
-
-    float m_all = -INFINITY;
-#pragma unroll
-    for (int i = 0; i < 16; ++i) m_all = fmaxf(m_all, sv[i]);
-    m_all = warp_max(m_all);
-    float z_all = 0.f;
-#pragma unroll
-    for (int i = 0; i < 16; ++i)
-      if (i < NPL && lane + 32 * i < E) z_all += sigm ? sigmoidf_(sv[i]) : expf(sv[i] - m_all);
-    z_all = warp_sum(z_all);
-
-    float g;
-    if (a.gate == MOE_GATE_SOFTMAX_TOPK) {
-      const float m_k = warp_max(s_me);
-      const float ek = mine ? expf(s_me - m_k) : 0.f;
-      g = ek / warp_sum(ek);
-    } else if (sigm) {
-      const float ak = mine ? sigmoidf_(s_me) : 0.f;
-      g = ak / warp_sum(ak);
-    } else {
-      g = expf(s_me - m_all) / z_all;
-    }
-    if (mine) {
-      a.topk_idx[(size_t)t * a.k + lane] = my_idx;
-      a.topk_w[(size_t)t * a.k + lane] = g;
-      atomicAdd(&sm.t.cnt[my_idx], 1);
-    }
-#pragma unroll
-    for (int i = 0; i < 16; ++i)
-      if (i < NPL && lane + 32 * i < E)
-        psum[i] += sigm ? sigmoidf_(sv[i]) / z_all : expf(sv[i] - m_all) / z_all;
   }
+  cp_async_wait<0>();
+  __syncthreads();                        // pipeline buffers become the routing area
 
-  // block statistics, fixed summation order over the warps
+  float* S = reinterpret_cast<float*>(fu_smem);                      // [BM][EP+1]
+  float (*Pw)[kMaxE] = reinterpret_cast<float (*)[kMaxE]>(S + BM * (EP + 1));
+  int* cnt = reinterpret_cast<int*>(Pw + 8);
 #pragma unroll
-  for (int i = 0; i < 16; ++i)
-    if (i < NPL && lane + 32 * i < E) sm.t.Pw[warp][lane + 32 * i] = psum[i];
-  __syncthreads();
-  for (int e = tid; e < E; e += kTopkThreads) {
-    float s = 0.f;
+  for (int i = 0; i < TM; ++i) {
+    const int m = ty * TM + i;
 #pragma unroll
-    for (int w = 0; w < kTopkWarps; ++w) s += sm.t.Pw[w][e];
-    a.scan.blk_prob[(size_t)blockIdx.x * E + e] = s;
-    a.scan.blk_cnt[(size_t)blockIdx.x * E + e] = sm.t.cnt[e];
+    for (int j = 0; j < TN; ++j) {
+      const int e = tx * TN + j;
+      if (e < a.E) {
+        const float s = acc[i][j] + (a.logit_offset ? a.logit_offset[e] : 0.f);
+        S[m * (EP + 1) + e] = s;
+        if (a.scores_out && m0 + m < a.T) a.scores_out[(size_t)(m0 + m) * a.E + e] = s;
+      }
+    }
   }
-  // publish, then let the last block to finish run the scan
-  __threadfence();
+  if (a.scores_out) return;
+  for (int e = tid; e < a.E; e += kThreads) cnt[e] = 0;
   __syncthreads();
-  if (tid == 0) am_last = atomicAdd(a.scan.done_counter, 1u) == gridDim.x - 1;
+
+  constexpr int NPL = EP / 32 > 0 ? EP / 32 : 1;
+  const int warp = tid >> 5, lane = tid & 31;
+  float psum[NPL];
+#pragma unroll
+  for (int i = 0; i < NPL; ++i) psum[i] = 0.f;
+  for (int tl = warp; tl < BM; tl += kThreads / 32) {
+    const int t = m0 + tl;
+    if (t >= a.T) break;
+    float sv[NPL];
+#pragma unroll
+    for (int i = 0; i < NPL; ++i) {
+      const int e = lane + 32 * i;
+      sv[i] = e < a.E ? S[tl * (EP + 1) + e] : -INFINITY;
+    }
+    route_one_token<NPL>(sv, a.E, a.k, a.gate, a.sel_bias, a.topk_idx + (size_t)t * a.k,
+                         a.topk_w + (size_t)t * a.k, cnt, psum);
+  }
   __syncthreads();
-  if (!am_last) return;
-  __threadfence();
-  scan_block<kTopkThreads>(a.scan, sm.scan);
-  if (tid == 0) *a.scan.done_counter = 0;
+  // Pw/cnt live in the routing area; the scan area overlaps it only after
+  // publish_and_scan has read them (it synchronises before the scan).
+  publish_and_scan<kThreads, NPL>(a.scan, psum, Pw, cnt,
+                                  *reinterpret_cast<ScanSmem<kThreads>*>(fu_smem), &am_last);
 }
 
 template <typename TIn, int TN>
@@ -458,27 +654,9 @@ static cudaError_t launch_logits(const Plan& p, const void* x, const void* W_r,
                                  const float* logit_offset, float* scores, void* ws,
                                  cudaStream_t st);
 
-cudaError_t launch_router(const Plan& p, const void* x, const void* W_r, const float* logit_offset,
-                          const float* sel_bias, int32_t* topk_idx, float* topk_w, void* ws,
-                          const ScanOutputs& so, cudaStream_t st, cudaEvent_t mid_event) {
+static ScanArgs scan_args(const Plan& p, void* ws, const ScanOutputs& so) {
   char* w = static_cast<char*>(ws);
-  float* scores = reinterpret_cast<float*>(w + p.ws.scores);
-  cudaError_t e = launch_logits(p, x, W_r, logit_offset, scores, ws, st);
-  if (e != cudaSuccess) return e;
-  if (mid_event && (e = cudaEventRecord(mid_event, st)) != cudaSuccess) return e;
-  TopkArgs t;
-  t.part = scores;
-  t.S = 1;
-  t.logit_offset = nullptr;     // already in the logits
-  t.sel_bias = sel_bias;
-  t.topk_idx = topk_idx;
-  t.topk_w = topk_w;
-  t.T = p.cfg.T;
-  t.E = p.cfg.E;
-  t.k = p.cfg.k;
-  t.BT = p.BT;
-  t.gate = p.cfg.gate;
-  ScanArgs& c = t.scan;
+  ScanArgs c;
   c.blk_cnt = reinterpret_cast<int*>(w + p.ws.blk_cnt);
   c.blk_prob = reinterpret_cast<float*>(w + p.ws.blk_prob);
   c.m = meta_ptrs(p, ws);
@@ -502,30 +680,95 @@ cudaError_t launch_router(const Plan& p, const void* x, const void* W_r, const f
   c.f_out = so.f_out;
   c.P_out = so.P_out;
   c.done_counter = reinterpret_cast<unsigned int*>(w + p.ws.status + 16);
-  return launch_pdl(router_topk_kernel, dim3(p.nblk), dim3(kTopkThreads), 0, st, t);
+  return c;
 }
 
-// Adds the per-expert offset to logits computed without it.
-__global__ void __launch_bounds__(kThreads) add_offset_kernel(float* s, size_t TE, int E,
-                                                              const float* off) {
-  pdl_wait();
-  pdl_trigger();
-  const size_t i = (size_t)blockIdx.x * kThreads + threadIdx.x;
-  if (i < TE) s[i] += off[i % E];
+template <typename TIn, int TM, int TN>
+static cudaError_t launch_fused_t(const Plan& p, const FusedArgs& a, cudaStream_t st) {
+  using C = FusedCfg<TIn, TM, TN>;
+  static std::atomic<uint64_t> attr_done{0};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (!(attr_done.load(std::memory_order_acquire) & (1ull << (dev & 63)))) {
+    e = cudaFuncSetAttribute(router_fused_kernel<TIn, TM, TN>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::SMEM);
+    if (e != cudaSuccess) return e;
+    attr_done.fetch_or(1ull << (dev & 63), std::memory_order_release);
+  }
+  const int blocks = (p.cfg.T + C::BM - 1) / C::BM;
+  return launch_pdl(router_fused_kernel<TIn, TM, TN>, dim3(blocks), dim3(kThreads), C::SMEM, st,
+                    a);
+}
+
+template <typename TIn, int TM>
+static cudaError_t launch_fused_tm(const Plan& p, const FusedArgs& a, cudaStream_t st) {
+  switch (p.fu_tn) {
+    case 2: return launch_fused_t<TIn, TM, 2>(p, a, st);
+    case 4: return launch_fused_t<TIn, TM, 4>(p, a, st);
+    case 8: return launch_fused_t<TIn, TM, 8>(p, a, st);
+    case 16: return launch_fused_t<TIn, TM, 16>(p, a, st);
+  }
+  return cudaErrorInvalidValue;
+}
+
+static cudaError_t launch_fused(const Plan& p, const FusedArgs& a, cudaStream_t st) {
+  if (p.cfg.dtype == MOE_BF16)
+    return p.fu_tm == 2 ? launch_fused_tm<__nv_bfloat16, 2>(p, a, st)
+                        : launch_fused_tm<__nv_bfloat16, 1>(p, a, st);
+  return p.fu_tm == 2 ? launch_fused_tm<float, 2>(p, a, st) : launch_fused_tm<float, 1>(p, a, st);
+}
+
+cudaError_t launch_router(const Plan& p, const void* x, const void* W_r, const float* logit_offset,
+                          const float* sel_bias, int32_t* topk_idx, float* topk_w, void* ws,
+                          const ScanOutputs& so, cudaStream_t st, cudaEvent_t mid_event) {
+  char* w = static_cast<char*>(ws);
+  cudaError_t e;
+  if (p.router_fused) {
+    FusedArgs f;
+    f.x = x;
+    f.W_r = W_r;
+    f.logit_offset = logit_offset;
+    f.sel_bias = sel_bias;
+    f.topk_idx = topk_idx;
+    f.topk_w = topk_w;
+    f.scores_out = nullptr;
+    f.T = p.cfg.T;
+    f.d = p.cfg.d;
+    f.E = p.cfg.E;
+    f.k = p.cfg.k;
+    f.gate = p.cfg.gate;
+    f.scan = scan_args(p, ws, so);
+    e = launch_fused(p, f, st);
+    if (e != cudaSuccess) return e;
+    if (mid_event && (e = cudaEventRecord(mid_event, st)) != cudaSuccess) return e;
+    return cudaSuccess;
+  }
+  float* scores = reinterpret_cast<float*>(w + p.ws.scores);
+  e = launch_logits(p, x, W_r, logit_offset, scores, ws, st);
+  if (e != cudaSuccess) return e;
+  if (mid_event && (e = cudaEventRecord(mid_event, st)) != cudaSuccess) return e;
+  TopkArgs t;
+  t.scores = scores;
+  t.sel_bias = sel_bias;
+  t.topk_idx = topk_idx;
+  t.topk_w = topk_w;
+  t.T = p.cfg.T;
+  t.E = p.cfg.E;
+  t.k = p.cfg.k;
+  t.BT = p.BT;
+  t.gate = p.cfg.gate;
+  t.scan = scan_args(p, ws, so);
+  return launch_pdl(router_topk_kernel, dim3(p.nblk), dim3(kTopkThreads), 0, st, t);
 }
 
 static cudaError_t launch_logits(const Plan& p, const void* x, const void* W_r,
                                  const float* logit_offset, float* scores, void* ws,
                                  cudaStream_t st) {
   char* w = static_cast<char*>(ws);
-  if (p.router_tc) {
-    cudaError_t e =
-        launch_router_tc(p, x, W_r, scores, reinterpret_cast<uint32_t*>(w + p.ws.status), st);
-    if (e != cudaSuccess || !logit_offset) return e;
-    const size_t TE = (size_t)p.cfg.T * p.cfg.E;
-    return launch_pdl(add_offset_kernel, dim3((unsigned)((TE + kThreads - 1) / kThreads)),
-                      dim3(kThreads), 0, st, scores, TE, p.cfg.E, logit_offset);
-  }
+  if (p.router_tc)
+    return launch_router_tc(p, x, W_r, logit_offset, scores,
+                            reinterpret_cast<uint32_t*>(w + p.ws.status), st);
   ScoresArgs a;
   a.x = x;
   a.W_r = W_r;
@@ -547,6 +790,22 @@ static cudaError_t launch_logits(const Plan& p, const void* x, const void* W_r,
 cudaError_t launch_router_scores(const Plan& p, const void* x, const void* W_r,
                                  const float* logit_offset, float* out, void* ws,
                                  cudaStream_t st) {
+  const char* r = std::getenv("MOE_ROUTER");
+  if (r && std::strcmp(r, "fused") == 0 && p.fu_tn > 0) {
+    // the fused kernel's own logits, written out before its routing step
+    FusedArgs f;
+    std::memset(&f, 0, sizeof(f));
+    f.x = x;
+    f.W_r = W_r;
+    f.logit_offset = logit_offset;
+    f.scores_out = out;
+    f.T = p.cfg.T;
+    f.d = p.cfg.d;
+    f.E = p.cfg.E;
+    f.k = p.cfg.k;
+    f.gate = p.cfg.gate;
+    return launch_fused(p, f, st);
+  }
   return launch_logits(p, x, W_r, logit_offset, out, ws, st);
 }
 

@@ -43,7 +43,7 @@ def _noalloc(cfg, x, W_r, off, out):
 
 
 @pytest.mark.parametrize("order", [("switch", "gptoss256"), ("gptoss256", "switch")])
-def test_noalloc_matches_workspace_entry_point_on_two_calls_in_a_row(order):
+def test_noalloc_matches_workspace_entry_point_on_two_calls_in_a_row(order, monkeypatch):
     for name in order:                     # the second call finds the first one's leftovers
         shape = W.get(name)
         x, W_r, off = _router_inputs(shape, seed=3)
@@ -54,7 +54,12 @@ def test_noalloc_matches_workspace_entry_point_on_two_calls_in_a_row(order):
         torch.cuda.synchronize()
         diff = (out - ref).abs().max().item()
         assert np.isfinite(diff) and diff <= ROUTER_ATOL, (name, diff)
-        assert torch.equal(out, ref), (name, diff)   # same kernel, same split: identical bits
+        # with moe_router_scores on the same float32 kernel the bits agree too
+        monkeypatch.setenv("MOE_ROUTER", "simt")
+        ref_same = L.router_scores(cfg, x, W_r, off)
+        monkeypatch.delenv("MOE_ROUTER")
+        torch.cuda.synchronize()
+        assert torch.equal(out, ref_same), name
 
 
 def test_noalloc_rejects_layers_beyond_its_scratch():
