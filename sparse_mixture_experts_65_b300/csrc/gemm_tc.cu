@@ -38,7 +38,14 @@
 
 namespace moe {
 
-enum { EPI_SWIGLU = 0, EPI_GELU = 1, EPI_RELU = 2, EPI_F32 = 3, EPI_F32_CHUNKED = 4 };
+enum { EPI_SWIGLU = 0, EPI_GELU = 1, EPI_RELU = 2, EPI_F32 = 3, EPI_F32_CHUNKED = 4,
+       EPI_COMBINE1 = 5 };
+
+// EPI_COMBINE1 (down projection of a top-1 layer without a shared expert):
+// the combine is folded into the epilogue.  Row r of expert e holds the single
+// kept slot of token t = row_token[r], so y[t] = bf16(g_t * acc) is written
+// directly -- the same float32 product and the same single rounding as the
+// separate combine kernel.
 
 // EPI_F32_CHUNKED: the reduction runs in chunks of kChunkKB k-blocks (128 k),
 // each accumulated by the tensor cores from zero; the epilogue adds the chunk
@@ -63,6 +70,11 @@ struct TcArgs {
   void* out_sh;           // shared output rows [T_pad][ld_out_sh]
   int ld_out_sh;
   const float* col_bias;  // EPI_F32_CHUNKED: added per output column (may be null)
+  int partial_rows;       // A tiles with at most this many real rows load 32-row boxes
+  const int* row_token;   // EPI_COMBINE1: token of each expert-ordered row
+  const float* gate;      // EPI_COMBINE1: topk_w, one gate per token
+  void* y;                // EPI_COMBINE1: [T][ld_y] bf16 layer output
+  int ld_y;
   uint32_t* status;
   uint64_t timeout_ns;
 };
@@ -88,7 +100,10 @@ struct TcCfg {
   static constexpr int TMEM_COLS = pow2_at_least(2 * MMA_N);
   static_assert(TMEM_COLS <= 512, "two accumulators must fit in tensor memory");
   static constexpr int BAR_BYTES = 8 * (2 * STAGES + 5) + 16;
-  static constexpr int SMEM = 1024 + STAGES * STAGE_BYTES + BAR_BYTES;
+  // the device tile schedule, copied to shared memory once per CTA:
+  // tp[E+2] | seg_start[E] | mtiles[E+1] | kept[E]
+  static constexpr int SCHED_INTS = 4 * (kMaxE + 2);
+  static constexpr int SMEM = 1024 + STAGES * STAGE_BYTES + BAR_BYTES + 4 * SCHED_INTS;
   static constexpr uint32_t IDESC = idesc_bf16_f32(BM, MMA_N);
 };
 
@@ -101,7 +116,17 @@ struct TileInfo {
   int K, N;
 };
 
-__device__ __forceinline__ TileInfo decode_tile(const TcArgs& a, int tile, int bnh) {
+// Tile schedule as seen by the kernel (shared-memory copies of the device
+// arrays, or the global arrays in the static mode).
+struct Sched {
+  const int* tp;
+  const int* seg_start;
+  const int* mtiles;
+  const int* kept;
+};
+
+__device__ __forceinline__ TileInfo decode_tile(const TcArgs& a, const Sched& sc, int tile,
+                                                int bnh) {
   if (a.static_mt > 0) {   // dense GEMM: rows [0, rows_sh), tiles N-major
     TileInfo ti;
     ti.seg = 0;
@@ -118,17 +143,17 @@ __device__ __forceinline__ TileInfo decode_tile(const TcArgs& a, int tile, int b
   int lo = 0, hi = nseg - 1;
   while (lo < hi) {
     const int mid = (lo + hi + 1) >> 1;
-    if (__ldg(a.tp + mid) <= tile) lo = mid; else hi = mid - 1;
+    if (sc.tp[mid] <= tile) lo = mid; else hi = mid - 1;
   }
   TileInfo ti;
   ti.seg = lo;
   ti.shared = lo >= a.E;
-  const int local = tile - __ldg(a.tp + lo);
-  const int mt = __ldg(a.mtiles + lo);
+  const int local = tile - sc.tp[lo];
+  const int mt = sc.mtiles[lo];
   const int n_t = local / mt, m_t = local - n_t * mt;
-  const int seg0 = ti.shared ? 0 : __ldg(a.seg_start + lo);
+  const int seg0 = ti.shared ? 0 : sc.seg_start[lo];
   ti.a_row = seg0 + m_t * kTcBM;
-  ti.row_end = ti.shared ? a.rows_sh : seg0 + __ldg(a.kept + lo);
+  ti.row_end = ti.shared ? a.rows_sh : seg0 + sc.kept[lo];
   ti.n0 = n_t * bnh;
   ti.K = ti.shared ? a.K_sh : a.K;
   ti.N = ti.shared ? a.N_sh : a.N;
@@ -143,7 +168,7 @@ __device__ __forceinline__ float silu_mul(float g, float u) {
 // this thread's row, masked at the segment's last row and the last column.
 template <int BNH, bool DUAL, int EPI>
 __device__ __forceinline__ void epilogue_tile(const TcArgs& a, const TileInfo& ti, uint32_t t_row,
-                                              size_t orow, bool row_ok) {
+                                              size_t orow, bool row_ok, float scale) {
 #pragma unroll 1
   for (int c = 0; c < BNH; c += 32) {
     uint32_t r0[32];
@@ -171,8 +196,9 @@ __device__ __forceinline__ void epilogue_tile(const TcArgs& a, const TileInfo& t
           if (col + i < ti.N) dst[i] = __uint_as_float(r0[i]);
       }
     } else {
-      __nv_bfloat16* out = static_cast<__nv_bfloat16*>(ti.shared ? a.out_sh : a.out);
-      const int ld = ti.shared ? a.ld_out_sh : a.ld_out;
+      __nv_bfloat16* out = static_cast<__nv_bfloat16*>(
+          EPI == EPI_COMBINE1 ? a.y : (ti.shared ? a.out_sh : a.out));
+      const int ld = EPI == EPI_COMBINE1 ? a.ld_y : (ti.shared ? a.ld_out_sh : a.ld_out);
       __nv_bfloat16* dst = out + orow * ld + col;
       uint32_t pk[16];
 #pragma unroll
@@ -187,6 +213,9 @@ __device__ __forceinline__ void epilogue_tile(const TcArgs& a, const TileInfo& t
         } else if (EPI == EPI_GELU) {
           v0 = 0.5f * v0 * (1.0f + erff(v0 * 0.70710678118654752f));
           v1 = 0.5f * v1 * (1.0f + erff(v1 * 0.70710678118654752f));
+        } else if (EPI == EPI_COMBINE1) {
+          v0 = fmaf(scale, v0, 0.f);
+          v1 = fmaf(scale, v1, 0.f);
         }
         __nv_bfloat162 b2 = __floats2bfloat162_rn(v0, v1);
         pk[i] = *reinterpret_cast<uint32_t*>(&b2);
@@ -211,9 +240,17 @@ __device__ __forceinline__ void epilogue_tile(const TcArgs& a, const TileInfo& t
   }
 }
 
+// A tiles with at most kPartialRows real rows (small expert segments, decode
+// batches) are loaded as ceil(rows / 32) boxes of 32 rows instead of one
+// 128-row box: the rows left unloaded only feed accumulator rows that the
+// epilogue never stores.
+constexpr int kPartialRows = 96;
+constexpr int kABox = 32;
+
 template <int BNH, bool DUAL, int EPI>
 __global__ void __launch_bounds__(192, 1)
 tc_grouped_gemm(const __grid_constant__ CUtensorMap mA, const __grid_constant__ CUtensorMap mA_sh,
+                const __grid_constant__ CUtensorMap mA32, const __grid_constant__ CUtensorMap mA32_sh,
                 const __grid_constant__ CUtensorMap mB0, const __grid_constant__ CUtensorMap mB1,
                 const __grid_constant__ CUtensorMap mB0_sh,
                 const __grid_constant__ CUtensorMap mB1_sh, const TcArgs a) {
@@ -249,10 +286,12 @@ tc_grouped_gemm(const __grid_constant__ CUtensorMap mA, const __grid_constant__ 
   }
   if (warp == 0 && lane == 0) {
     tma_prefetch_desc(&mA);
+    tma_prefetch_desc(&mA32);
     tma_prefetch_desc(&mB0);
     if (DUAL) tma_prefetch_desc(&mB1);
     if (a.has_shared) {
       tma_prefetch_desc(&mA_sh);
+      tma_prefetch_desc(&mA32_sh);
       tma_prefetch_desc(&mB0_sh);
       if (DUAL) tma_prefetch_desc(&mB1_sh);
     }
@@ -267,7 +306,28 @@ tc_grouped_gemm(const __grid_constant__ CUtensorMap mA, const __grid_constant__ 
   const uint32_t tmem_base = *tmem_slot;
   pdl_wait();      // everything above ran while the previous kernel finished
   pdl_trigger();
-  const int total = a.static_mt > 0 ? a.static_total : __ldg(a.tp + a.E + a.has_shared);
+  Sched sc;
+  {
+    int* s_tp = reinterpret_cast<int*>(smem + C::STAGES * C::STAGE_BYTES + C::BAR_BYTES);
+    int* s_seg = s_tp + (kMaxE + 2);
+    int* s_mt = s_seg + (kMaxE + 2);
+    int* s_kept = s_mt + (kMaxE + 2);
+    if (a.static_mt == 0) {
+      const int nseg = a.E + a.has_shared;
+      for (int i = threadIdx.x; i <= nseg; i += blockDim.x) s_tp[i] = __ldg(a.tp + i);
+      for (int i = threadIdx.x; i < nseg; i += blockDim.x) s_mt[i] = __ldg(a.mtiles + i);
+      for (int i = threadIdx.x; i < a.E; i += blockDim.x) {
+        s_seg[i] = __ldg(a.seg_start + i);
+        s_kept[i] = __ldg(a.kept + i);
+      }
+    }
+    __syncthreads();
+    sc.tp = s_tp;
+    sc.seg_start = s_seg;
+    sc.mtiles = s_mt;
+    sc.kept = s_kept;
+  }
+  const int total = a.static_mt > 0 ? a.static_total : sc.tp[a.E + a.has_shared];
 
   auto give_up = [&]() {
     atomicOr(a.status, STATUS_TIMEOUT_GEMM);
@@ -280,12 +340,16 @@ tc_grouped_gemm(const __grid_constant__ CUtensorMap mA, const __grid_constant__ 
       uint32_t g = 0;
       bool ok = true;
       for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
-        const TileInfo ti = decode_tile(a, tile, BNH);
+        const TileInfo ti = decode_tile(a, sc, tile, BNH);
         const CUtensorMap* pA = ti.shared ? &mA_sh : &mA;
+        const CUtensorMap* pA32 = ti.shared ? &mA32_sh : &mA32;
         const CUtensorMap* pB0 = ti.shared ? &mB0_sh : &mB0;
         const CUtensorMap* pB1 = ti.shared ? &mB1_sh : &mB1;
         const int e = ti.shared ? 0 : ti.seg;
         const int nk = (ti.K + C::BK - 1) / C::BK;
+        const int rows = ti.row_end - ti.a_row < kTcBM ? ti.row_end - ti.a_row : kTcBM;
+        const int a_boxes = rows > a.partial_rows ? 0 : (rows + kABox - 1) / kABox;
+        const uint32_t a_bytes = a_boxes ? a_boxes * kABox * 128u : (uint32_t)C::A_BYTES;
         for (int kb = 0; kb < nk; ++kb, ++g) {
           const int s = g % C::STAGES;
           const uint32_t ph = (g / C::STAGES) & 1u;
@@ -296,8 +360,13 @@ tc_grouped_gemm(const __grid_constant__ CUtensorMap mA, const __grid_constant__ 
           }
           const uint32_t sa = smem_base + s * C::STAGE_BYTES;
           const uint32_t sb = sa + C::A_BYTES;
-          mbar_arrive_expect_tx(full_bar(s), C::STAGE_BYTES);
-          tma_load_2d(sa, pA, full_bar(s), kb * C::BK, ti.a_row);
+          mbar_arrive_expect_tx(full_bar(s), a_bytes + C::B_BYTES);
+          if (a_boxes == 0) {
+            tma_load_2d(sa, pA, full_bar(s), kb * C::BK, ti.a_row);
+          } else {
+            for (int b = 0; b < a_boxes; ++b)
+              tma_load_2d(sa + b * kABox * 128, pA32, full_bar(s), kb * C::BK, ti.a_row + b * kABox);
+          }
           tma_load_3d(sb, pB0, full_bar(s), kb * C::BK, ti.n0, e);
           if (DUAL) tma_load_3d(sb + BNH * 128, pB1, full_bar(s), kb * C::BK, ti.n0, e);
         }
@@ -323,7 +392,7 @@ tc_grouped_gemm(const __grid_constant__ CUtensorMap mA, const __grid_constant__ 
       int it = 0;
       bool ok = true;
       for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
-        const TileInfo ti = decode_tile(a, tile, BNH);
+        const TileInfo ti = decode_tile(a, sc, tile, BNH);
         const int nk = (ti.K + C::BK - 1) / C::BK;
         const int ck = EPI == EPI_F32_CHUNKED ? kChunkKB : nk;   // k-blocks per accumulator
         for (int kb0 = 0; kb0 < nk && ok; kb0 += ck, ++it) {
@@ -372,7 +441,7 @@ tc_grouped_gemm(const __grid_constant__ CUtensorMap mA, const __grid_constant__ 
     int it = 0;
     bool ok = true;
     for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
-      const TileInfo ti = decode_tile(a, tile, BNH);
+      const TileInfo ti = decode_tile(a, sc, tile, BNH);
       const size_t orow = static_cast<size_t>(ti.a_row + row_in_tile);
       const bool row_ok = ti.a_row + row_in_tile < ti.row_end;
       const int nk = (ti.K + C::BK - 1) / C::BK;
@@ -401,8 +470,13 @@ tc_grouped_gemm(const __grid_constant__ CUtensorMap mA, const __grid_constant__ 
 #pragma unroll
             for (int i = 0; i < 32; ++i) csum[c + i] += __uint_as_float(r0[i]);
           }
+        } else if constexpr (EPI == EPI_COMBINE1) {
+          // y row of the token this expert row belongs to, scaled by its gate
+          const int tok = row_ok ? __ldg(a.row_token + orow) : 0;
+          const float g = row_ok ? __ldg(a.gate + tok) : 0.f;
+          epilogue_tile<BNH, DUAL, EPI>(a, ti, t_row, (size_t)tok, row_ok, g);
         } else {
-          epilogue_tile<BNH, DUAL, EPI>(a, ti, t_row, orow, row_ok);
+          epilogue_tile<BNH, DUAL, EPI>(a, ti, t_row, orow, row_ok, 1.f);
         }
         tc_fence_before();
         mbar_arrive(tempty_bar(ab));
@@ -477,7 +551,7 @@ static bool encode_3d(CUtensorMap* m, const void* ptr, uint64_t n_mat, uint64_t 
 }
 
 struct TcMaps {
-  CUtensorMap A, A_sh, B0, B1, B0_sh, B1_sh;
+  CUtensorMap A, A_sh, A32, A32_sh, B0, B1, B0_sh, B1_sh;
 };
 
 // Raise the dynamic shared-memory limit of a kernel once per device.
@@ -500,8 +574,8 @@ static cudaError_t run_tc(const TcMaps& m, const TcArgs& a, int grid, cudaStream
   auto kern = tc_grouped_gemm<BNH, DUAL, EPI>;
   cudaError_t e = smem_attr_once(kern, C::SMEM, attr_done);
   if (e != cudaSuccess) return e;
-  return launch_pdl(kern, dim3(grid), dim3(192), C::SMEM, st, m.A, m.A_sh, m.B0, m.B1, m.B0_sh,
-                    m.B1_sh, a);
+  return launch_pdl(kern, dim3(grid), dim3(192), C::SMEM, st, m.A, m.A_sh, m.A32, m.A32_sh, m.B0,
+                    m.B1, m.B0_sh, m.B1_sh, a);
 }
 
 static cudaError_t dispatch_up(int bn, int act, const TcMaps& m, const TcArgs& a, int grid,
@@ -531,8 +605,18 @@ static cudaError_t dispatch_up(int bn, int act, const TcMaps& m, const TcArgs& a
   return cudaErrorInvalidValue;
 }
 
-static cudaError_t dispatch_down(int bn, const TcMaps& m, const TcArgs& a, int grid,
-                                 cudaStream_t st) {
+static cudaError_t dispatch_down(int bn, bool combine1, const TcMaps& m, const TcArgs& a,
+                                 int grid, cudaStream_t st) {
+  if (combine1) {
+    switch (bn) {
+      case 256: return run_tc<256, false, EPI_COMBINE1>(m, a, grid, st);
+      case 192: return run_tc<192, false, EPI_COMBINE1>(m, a, grid, st);
+      case 128: return run_tc<128, false, EPI_COMBINE1>(m, a, grid, st);
+      case 96: return run_tc<96, false, EPI_COMBINE1>(m, a, grid, st);
+      case 64: return run_tc<64, false, EPI_COMBINE1>(m, a, grid, st);
+    }
+    return cudaErrorInvalidValue;
+  }
   switch (bn) {
     case 256: return run_tc<256, false, EPI_F32>(m, a, grid, st);
     case 192: return run_tc<192, false, EPI_F32>(m, a, grid, st);
@@ -547,7 +631,8 @@ constexpr uint64_t kGemmTimeoutNs = 2000000000ull;   // 2 s
 
 cudaError_t launch_experts_tc(const Plan& p, const void* x, const void* W1, const void* W3,
                               const void* W2, const void* Ws1, const void* Ws3, const void* Ws2,
-                              void* ws, cudaStream_t st, cudaEvent_t mid_event) {
+                              void* ws, cudaStream_t st, cudaEvent_t mid_event, void* y,
+                              const float* topk_w) {
   const moe_config& c = p.cfg;
   char* w = static_cast<char*>(ws);
   const Meta meta = meta_ptrs(p, ws);
@@ -561,14 +646,17 @@ cudaError_t launch_experts_tc(const Plan& p, const void* x, const void* W1, cons
   // ---- up projection: h = act(xp W1^T) or silu(xp W1^T) * (xp W3^T) ----
   TcMaps mu;
   bool ok = encode_2d(&mu.A, xp, p.R_cap, c.d, kTcBM);
+  ok = ok && encode_2d(&mu.A32, xp, p.R_cap, c.d, kABox);
   ok = ok && encode_3d(&mu.B0, W1, c.E, c.f, c.d, p.up_bn);
   ok = ok && encode_3d(&mu.B1, dual ? W3 : W1, c.E, c.f, c.d, p.up_bn);
   if (sh) {
     ok = ok && encode_2d(&mu.A_sh, x, c.T, c.d, kTcBM);
+    ok = ok && encode_2d(&mu.A32_sh, x, c.T, c.d, kABox);
     ok = ok && encode_3d(&mu.B0_sh, Ws1, 1, c.f_shared, c.d, p.up_bn);
     ok = ok && encode_3d(&mu.B1_sh, Ws3, 1, c.f_shared, c.d, p.up_bn);
   } else {
     mu.A_sh = mu.A;
+    mu.A32_sh = mu.A32;
     mu.B0_sh = mu.B0;
     mu.B1_sh = mu.B1;
   }
@@ -582,6 +670,11 @@ cudaError_t launch_experts_tc(const Plan& p, const void* x, const void* W1, cons
   au.static_mt = 0;
   au.static_total = 0;
   au.col_bias = nullptr;
+  au.partial_rows = p.partial_rows_up;
+  au.row_token = nullptr;
+  au.gate = nullptr;
+  au.y = nullptr;
+  au.ld_y = 0;
   au.E = c.E;
   au.has_shared = sh ? 1 : 0;
   au.N = c.f;
@@ -605,18 +698,28 @@ cudaError_t launch_experts_tc(const Plan& p, const void* x, const void* W1, cons
   // ---- down projection: o = h W2^T (fp32) ----
   TcMaps md;
   ok = encode_2d(&md.A, h, p.R_cap, c.f, kTcBM);
+  ok = ok && encode_2d(&md.A32, h, p.R_cap, c.f, kABox);
   ok = ok && encode_3d(&md.B0, W2, c.E, c.d, c.f, p.dn_bn);
   md.B1 = md.B0;
   if (sh) {
     ok = ok && encode_2d(&md.A_sh, hs, p.T_pad, c.f_shared, kTcBM);
+    ok = ok && encode_2d(&md.A32_sh, hs, p.T_pad, c.f_shared, kABox);
     ok = ok && encode_3d(&md.B0_sh, Ws2, 1, c.d, c.f_shared, p.dn_bn);
   } else {
     md.A_sh = md.A;
+    md.A32_sh = md.A32;
     md.B0_sh = md.B0;
   }
   md.B1_sh = md.B0_sh;
   if (!ok) return cudaErrorInvalidValue;
   TcArgs ad = au;
+  ad.partial_rows = p.partial_rows;
+  if (p.combine_in_down) {
+    ad.row_token = reinterpret_cast<const int*>(w + p.ws.row_token);
+    ad.gate = topk_w;
+    ad.y = y;
+    ad.ld_y = c.d;
+  }
   ad.tp = meta.tp_dn;
   ad.N = c.d;
   ad.K = c.f;
@@ -627,7 +730,7 @@ cudaError_t launch_experts_tc(const Plan& p, const void* x, const void* W1, cons
   ad.out_sh = sh ? static_cast<void*>(w + p.ws.os) : nullptr;
   ad.ld_out_sh = sh ? c.d : 0;
   const int grid_dn = p.max_tiles_dn < p.num_sms ? p.max_tiles_dn : p.num_sms;
-  return dispatch_down(p.dn_bn, md, ad, grid_dn, st);
+  return dispatch_down(p.dn_bn, p.combine_in_down, md, ad, grid_dn, st);
 }
 
 // ---------------------------------------------------------------- router
@@ -635,17 +738,20 @@ cudaError_t launch_experts_tc(const Plan& p, const void* x, const void* W1, cons
 // (their products are exact), each 128-wide chunk of the reduction
 // accumulated in tensor memory, the chunks added in float32 by the epilogue,
 // float32 output [T][E].
-constexpr int kRouterTcBN = 64;
 
 cudaError_t launch_router_tc(const Plan& p, const void* x, const void* W_r,
                              const float* logit_offset, float* scores, uint32_t* status,
                              cudaStream_t st) {
   const moe_config& c = p.cfg;
+  // experts per tile: 32 for small E (twice the tiles), else 64
+  const int bn = c.E <= 64 ? 32 : 64;
   TcMaps m;
   bool ok = encode_2d(&m.A, x, c.T, c.d, kTcBM);
-  ok = ok && encode_3d(&m.B0, W_r, 1, c.E, c.d, kRouterTcBN);
+  ok = ok && encode_2d(&m.A32, x, c.T, c.d, kABox);
+  ok = ok && encode_3d(&m.B0, W_r, 1, c.E, c.d, bn);
   if (!ok) return cudaErrorInvalidValue;
   m.A_sh = m.A;
+  m.A32_sh = m.A32;
   m.B1 = m.B0_sh = m.B1_sh = m.B0;
   TcArgs a;
   std::memset(&a, 0, sizeof(a));
@@ -656,12 +762,18 @@ cudaError_t launch_router_tc(const Plan& p, const void* x, const void* W_r,
   a.ld_out = c.E;
   a.rows_sh = c.T;
   a.static_mt = (c.T + kTcBM - 1) / kTcBM;
-  a.static_total = a.static_mt * ((c.E + kRouterTcBN - 1) / kRouterTcBN);
+  a.static_total = a.static_mt * ((c.E + bn - 1) / bn);
   a.col_bias = logit_offset;
+  a.partial_rows = p.partial_rows;
+  a.row_token = nullptr;
+  a.gate = nullptr;
+  a.y = nullptr;
+  a.ld_y = 0;
   a.status = status;
   a.timeout_ns = kGemmTimeoutNs;
   const int grid = a.static_total < p.num_sms ? a.static_total : p.num_sms;
-  return run_tc<kRouterTcBN, false, EPI_F32_CHUNKED>(m, a, grid, st);
+  return bn == 32 ? run_tc<32, false, EPI_F32_CHUNKED>(m, a, grid, st)
+                  : run_tc<64, false, EPI_F32_CHUNKED>(m, a, grid, st);
 }
 
 // ---------------------------------------------------------------- self-test

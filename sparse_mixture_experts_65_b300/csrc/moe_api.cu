@@ -15,17 +15,19 @@ static size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
 static int ceil_div(long long a, long long b) { return static_cast<int>((a + b - 1) / b); }
 
-// Output columns per tile: minimise (waves of tiles over the SMs) x (tile
-// width + a fixed per-tile cost); ties go to the wider tile.
+// Output columns per tile: minimise (waves of tiles over the SMs) x (bytes a
+// tile moves per k: B rows = mma_mult * bn weight rows plus the 128-row A
+// tile re-read for every N tile); ties go to the wider tile.  Matches tile
+// sweeps on B300 (Switch, gpt-oss decode, DeepSeek-V3 shapes).
 static int choose_bn(const int* cands, int ncand, int N, long long est_mtiles, long long extra_m,
-                     int N_extra, int num_sms) {
+                     int N_extra, int num_sms, int mma_mult) {
   int best = cands[0];
   long long best_cost = LLONG_MAX;
   for (int i = 0; i < ncand; ++i) {
     const int bn = cands[i];
     const long long tiles = est_mtiles * ceil_div(N, bn) + extra_m * ceil_div(N_extra, bn);
     const long long waves = (tiles + num_sms - 1) / num_sms;
-    const long long cost = waves * (bn + 16);
+    const long long cost = waves * (mma_mult * bn + kTcBM);
     if (cost < best_cost) {
       best_cost = cost;
       best = bn;
@@ -154,10 +156,10 @@ int make_plan(const moe_config* cfg, WsKind kind, Plan* p, int num_sms) {
     static const int single_c[] = {256, 128, 96, 64};
     static const int down_c[] = {256, 192, 128, 96, 64};
     if (c.act == MOE_ACT_SWIGLU)
-      P.up_bn = choose_bn(dual_c, 4, c.f, est, P.mt_sh, c.f_shared, P.num_sms);
+      P.up_bn = choose_bn(dual_c, 4, c.f, est, P.mt_sh, c.f_shared, P.num_sms, 2);
     else
-      P.up_bn = choose_bn(single_c, 4, c.f, est, P.mt_sh, c.f_shared, P.num_sms);
-    P.dn_bn = choose_bn(down_c, 5, c.d, est, P.mt_sh, c.d, P.num_sms);
+      P.up_bn = choose_bn(single_c, 4, c.f, est, P.mt_sh, c.f_shared, P.num_sms, 1);
+    P.dn_bn = choose_bn(down_c, 5, c.d, est, P.mt_sh, c.d, P.num_sms, 1);
     // Tuning override (tile sweeps and tests): MOE_TILE_N_UP / MOE_TILE_N_DOWN
     // select one of the compiled tile widths; other values are ignored.
     const int up_env = env_int("MOE_TILE_N_UP"), dn_env = env_int("MOE_TILE_N_DOWN");
@@ -170,6 +172,15 @@ int make_plan(const moe_config* cfg, WsKind kind, Plan* p, int num_sms) {
     P.up_bn = kSimtBN;
     P.dn_bn = kSimtBN;
   }
+  {
+    // Partial A tiles (<= 64 real rows loaded as 32-row boxes) measured
+    // faster for the single-operand GEMMs (down projections, plain up
+    // projections) and slower for the dual-operand SwiGLU up projection.
+    const char* v = std::getenv("MOE_PARTIAL_A_ROWS");   // tuning override
+    P.partial_rows = v ? std::atoi(v) : 64;
+    P.partial_rows_up = v ? P.partial_rows : (c.act == MOE_ACT_SWIGLU ? 0 : 64);
+  }
+  P.combine_in_down = P.tc && c.k == 1 && c.n_shared == 0;
   P.nt_up = ceil_div(c.f, P.up_bn);
   P.nt_dn = ceil_div(c.d, P.dn_bn);
   P.nt_up_sh = c.n_shared ? ceil_div(c.f_shared, P.up_bn) : 0;
@@ -197,6 +208,7 @@ int make_plan(const moe_config* cfg, WsKind kind, Plan* p, int num_sms) {
   L.blk_prob = take(sizeof(float) * (size_t)P.nblk * E);
   L.meta = take(sizeof(int) * (E + (E + 1) * 3 + (E + 2) * 2));
   L.key_row = take(sizeof(int) * (size_t)Tk);
+  L.row_token = take(sizeof(int) * (size_t)P.R_cap);
   if (kind != WsKind::Route) {
     const size_t act_elem = P.elem;   // h is bf16 on the tensor-core path, fp32 otherwise
     L.xp = take((size_t)P.R_cap * c.d * P.elem);
@@ -334,16 +346,17 @@ static int forward_impl(const moe_config* cfg, const Tensors& t, void* ws, size_
   MOE_TRY_CUDA(launch_router(p, t.x, t.W_r, t.logit_offset, t.sel_bias, t.topk_idx, t.topk_w, ws,
                              so, st, topk_ev));
   if ((rc = record(events, MOE_STAGE_PERMUTE, st)) != MOE_OK) return rc;
-  MOE_TRY_CUDA(launch_permute(p, t.x, t.topk_idx, t.slot_pos, !route_only, ws, st));
+  MOE_TRY_CUDA(launch_permute(p, t.x, t.topk_idx, t.slot_pos, !route_only, ws, st, t.y));
   if (route_only) return MOE_OK;
   if ((rc = record(events, MOE_STAGE_UP, st)) != MOE_OK) return rc;
   cudaEvent_t mid = events ? static_cast<cudaEvent_t>(events[MOE_STAGE_DOWN]) : nullptr;
   if (p.tc)
-    MOE_TRY_CUDA(launch_experts_tc(p, t.x, t.W1, t.W3, t.W2, t.Ws1, t.Ws3, t.Ws2, ws, st, mid));
+    MOE_TRY_CUDA(launch_experts_tc(p, t.x, t.W1, t.W3, t.W2, t.Ws1, t.Ws3, t.Ws2, ws, st, mid,
+                                   t.y, t.topk_w));
   else
     MOE_TRY_CUDA(launch_experts_simt(p, t.x, t.W1, t.W3, t.W2, t.Ws1, t.Ws3, t.Ws2, ws, st, mid));
   if ((rc = record(events, MOE_STAGE_COMBINE, st)) != MOE_OK) return rc;
-  MOE_TRY_CUDA(launch_combine(p, t.topk_w, t.y, ws, st));
+  if (!p.combine_in_down) MOE_TRY_CUDA(launch_combine(p, t.topk_w, t.y, ws, st));
   if ((rc = record(events, MOE_NUM_STAGES, st)) != MOE_OK) return rc;
   return MOE_OK;
 }
@@ -498,7 +511,9 @@ int moe_launch_count(const moe_config* cfg, int32_t* launches) {
   Plan p;
   const int rc = make_plan(cfg, WsKind::Forward, &p);
   if (rc != MOE_OK) return rc;
-  *launches = cfg->T == 0 ? 0 : MOE_NUM_STAGES;   // one kernel per stage
+  // one kernel per stage; top-1 bf16 layers without a shared expert fold the
+  // combine into the down projection
+  *launches = cfg->T == 0 ? 0 : (p.combine_in_down ? MOE_NUM_STAGES - 1 : MOE_NUM_STAGES);
   return MOE_OK;
 }
 

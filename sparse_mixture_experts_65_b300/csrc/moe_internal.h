@@ -39,6 +39,7 @@ struct WsLayout {
   size_t meta;        // int32  kept[E] | offsets[E+1] | seg_start[E+1] | mtiles[E+1]
                       //        | tp_up[E+2] | tp_dn[E+2]
   size_t key_row;     // int32  [T*k]      padded row of each assignment, -1 if dropped
+  size_t row_token;   // int32  [R_cap]    token of each expert-ordered row
   size_t xp;          // dtype  [R_cap][d] token copies in expert order
   size_t h;           // dtype  [R_cap][f] expert hidden activations
   size_t o;           // float  [R_cap][d] expert outputs
@@ -71,6 +72,9 @@ struct Plan {
   int nt_up_sh, nt_dn_sh;     // N tiles of the shared segment
   int mt_sh;                  // M tiles of the shared segment
   int max_tiles_up, max_tiles_dn;  // host upper bounds (grid sizing)
+  int partial_rows;           // A tiles with at most this many rows load only those rows
+  int partial_rows_up;        // the same for the up projection
+  bool combine_in_down;       // top-1, no shared expert, bf16: y written by the down epilogue
   int num_sms;
   WsLayout ws;
 };
@@ -111,10 +115,12 @@ cudaError_t launch_router_scores(const Plan& p, const void* x, const void* W_r,
                                  const float* logit_offset, float* out, void* ws,
                                  cudaStream_t st);
 cudaError_t launch_permute(const Plan& p, const void* x, const int32_t* topk_idx,
-                           int32_t* slot_pos, bool copy_rows, void* ws, cudaStream_t st);
+                           int32_t* slot_pos, bool copy_rows, void* ws, cudaStream_t st,
+                           void* y);
 cudaError_t launch_experts_tc(const Plan& p, const void* x, const void* W1, const void* W3,
                               const void* W2, const void* Ws1, const void* Ws3, const void* Ws2,
-                              void* ws, cudaStream_t st, cudaEvent_t mid_event);
+                              void* ws, cudaStream_t st, cudaEvent_t mid_event, void* y,
+                              const float* topk_w);
 cudaError_t launch_experts_simt(const Plan& p, const void* x, const void* W1, const void* W3,
                                 const void* W2, const void* Ws1, const void* Ws3,
                                 const void* Ws2, void* ws, cudaStream_t st,

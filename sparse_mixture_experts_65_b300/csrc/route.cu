@@ -31,6 +31,9 @@ struct PermuteArgs {
   const int* blk_base;   // [nblk][E] exclusive scan over blocks
   Meta m;
   void* xp;
+  int* row_token;        // [R_cap]: token of each kept row
+  void* y_zero;          // top-1 layers whose combine runs in the down projection:
+                         // the y rows of dropped tokens are zeroed here
   int T, E, k, BT, capacity, nvec;   // nvec: 16-byte vectors per token row
   int copy;
 };
@@ -72,6 +75,7 @@ __global__ void __launch_bounds__(kPermuteThreads) permute_kernel(const PermuteA
         const int row = keep ? a.m.seg_start[e] + pos : -1;
         a.key_row[key0 + q] = row;
         if (a.slot_pos) a.slot_pos[key0 + q] = keep ? a.m.offsets[e] + pos : -1;
+        if (keep) a.row_token[row] = t0 + q / a.k;
         row_s[q] = row;
         if (before == 0) cnt[e] = prior + __popc(peers);
       }
@@ -79,6 +83,13 @@ __global__ void __launch_bounds__(kPermuteThreads) permute_kernel(const PermuteA
     }
   }
   __syncthreads();
+  if (a.y_zero) {                 // top-1: a dropped slot leaves its token's y at zero
+    uint4* y = static_cast<uint4*>(a.y_zero);
+    for (int i = tid; i < nk * a.nvec; i += kPermuteThreads) {
+      const int q = i / a.nvec;
+      if (row_s[q] < 0) y[(size_t)(t0 + q) * a.nvec + (i - q * a.nvec)] = make_uint4(0, 0, 0, 0);
+    }
+  }
   if (!a.copy) return;
   // Row copies: (key, 16-byte vector) pairs spread over the block, four
   // independent loads in flight per thread before their stores.
@@ -124,7 +135,8 @@ Meta meta_ptrs(const Plan& p, void* ws) {
 }
 
 cudaError_t launch_permute(const Plan& p, const void* x, const int32_t* topk_idx,
-                           int32_t* slot_pos, bool copy_rows, void* ws, cudaStream_t st) {
+                           int32_t* slot_pos, bool copy_rows, void* ws, cudaStream_t st,
+                           void* y) {
   PermuteArgs a;
   a.x = x;
   a.topk_idx = topk_idx;
@@ -133,6 +145,8 @@ cudaError_t launch_permute(const Plan& p, const void* x, const int32_t* topk_idx
   a.blk_base = reinterpret_cast<const int*>(static_cast<char*>(ws) + p.ws.blk_cnt);
   a.m = meta_ptrs(p, ws);
   a.xp = static_cast<char*>(ws) + p.ws.xp;
+  a.row_token = reinterpret_cast<int*>(static_cast<char*>(ws) + p.ws.row_token);
+  a.y_zero = (copy_rows && p.combine_in_down) ? y : nullptr;
   a.T = p.cfg.T;
   a.E = p.cfg.E;
   a.k = p.cfg.k;

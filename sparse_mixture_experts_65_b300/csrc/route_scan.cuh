@@ -38,43 +38,59 @@ struct ScanArgs {
 
 template <int NT>
 struct ScanSmem {
-  int scratch[33];
+  int scratch[4 * 33];
   int pc[NT];
   float pp[NT];
   int routed_s[kMaxE];
   float psum_s[kMaxE];
-  double red[NT];
+  double red[NT / 32];
 };
 
-// Exclusive prefix sum over NT threads (NT a multiple of 32, <= 1024).
+// Exclusive prefix sums of four integers per thread over NT threads (NT a
+// multiple of 32, <= 1024), in one pass.  `scratch` holds 4*33 ints.
 template <int NT>
-__device__ __forceinline__ int block_exscan(int v, int* scratch, int* total) {
+__device__ __forceinline__ int4 block_exscan4(int4 v, int* scratch, int4* total) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   constexpr int NW = NT / 32;
-  int inc = v;
+  int4 inc = v;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
-    const int n = __shfl_up_sync(0xffffffffu, inc, o);
-    if (lane >= o) inc += n;
+    const int nx = __shfl_up_sync(0xffffffffu, inc.x, o);
+    const int ny = __shfl_up_sync(0xffffffffu, inc.y, o);
+    const int nz = __shfl_up_sync(0xffffffffu, inc.z, o);
+    const int nw = __shfl_up_sync(0xffffffffu, inc.w, o);
+    if (lane >= o) {
+      inc.x += nx;
+      inc.y += ny;
+      inc.z += nz;
+      inc.w += nw;
+    }
   }
-  __syncthreads();
-  if (lane == 31) scratch[warp] = inc;
+  if (lane == 31) {
+    scratch[warp] = inc.x;
+    scratch[33 + warp] = inc.y;
+    scratch[66 + warp] = inc.z;
+    scratch[99 + warp] = inc.w;
+  }
   __syncthreads();
   if (warp == 0) {
-    const int w = lane < NW ? scratch[lane] : 0;
-    int winc = w;
 #pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int n = __shfl_up_sync(0xffffffffu, winc, o);
-      if (lane >= o) winc += n;
+    for (int c = 0; c < 4; ++c) {
+      const int w = lane < NW ? scratch[33 * c + lane] : 0;
+      int winc = w;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int n = __shfl_up_sync(0xffffffffu, winc, o);
+        if (lane >= o) winc += n;
+      }
+      if (lane < NW) scratch[33 * c + lane] = winc - w;
+      if (lane == 31) scratch[33 * c + 32] = winc;
     }
-    if (lane < NW) scratch[lane] = winc - w;
-    if (lane == 31) scratch[32] = winc;
   }
   __syncthreads();
-  const int out = scratch[warp] + inc - v;
-  *total = scratch[32];
-  __syncthreads();
+  const int4 out = make_int4(scratch[warp] + inc.x - v.x, scratch[33 + warp] + inc.y - v.y,
+                             scratch[66 + warp] + inc.z - v.z, scratch[99 + warp] + inc.w - v.w);
+  *total = make_int4(scratch[32], scratch[65], scratch[98], scratch[131]);
   return out;
 }
 
@@ -158,11 +174,11 @@ __device__ void scan_block(const ScanArgs& a, ScanSmem<NT>& sm) {
       P = a.T > 0 ? sm.psum_s[e] / (float)a.T : 0.f;
       fr = a.T > 0 ? (float)routed / (float)(a.T * a.k) : 0.f;
     }
-    int tot_kept, tot_mt, tot_up, tot_dn;
-    const int ex_kept = block_exscan<NT>(kept, sm.scratch, &tot_kept);
-    const int ex_mt = block_exscan<NT>(mt, sm.scratch, &tot_mt);
-    const int ex_up = block_exscan<NT>(mt * a.nt_up, sm.scratch, &tot_up);
-    const int ex_dn = block_exscan<NT>(mt * a.nt_dn, sm.scratch, &tot_dn);
+    int4 tot;
+    const int4 ex = block_exscan4<NT>(make_int4(kept, mt, mt * a.nt_up, mt * a.nt_dn),
+                                      sm.scratch, &tot);
+    const int ex_kept = ex.x, ex_mt = ex.y, ex_up = ex.z, ex_dn = ex.w;
+    const int tot_kept = tot.x, tot_mt = tot.y, tot_up = tot.z, tot_dn = tot.w;
     if (e < a.E) {
       a.m.kept[e] = kept;
       a.m.offsets[e] = ex_kept;
@@ -188,14 +204,18 @@ __device__ void scan_block(const ScanArgs& a, ScanSmem<NT>& sm) {
       a.m.tp_dn[a.E + 1] = tot_dn + sh_dn;
       if (a.offsets_out) a.offsets_out[a.E] = tot_kept;
     }
-    // L = alpha * E * sum_i f_i P_i, summed as a fixed binary tree in double.
-    sm.red[tid] = (e < a.E) ? (double)fr * (double)P : 0.0;
+    // L = alpha * E * sum_i f_i P_i in double: a fixed butterfly inside each
+    // warp, then the warp sums in warp order.
+    double l = (e < a.E) ? (double)fr * (double)P : 0.0;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) l += __shfl_xor_sync(0xffffffffu, l, o);
+    if ((tid & 31) == 0) sm.red[tid >> 5] = l;
     __syncthreads();
-    for (int s = NT / 2; s > 0; s >>= 1) {
-      if (tid < s) sm.red[tid] += sm.red[tid + s];
-      __syncthreads();
+    if (tid == 0) {
+      double t = 0.0;
+      for (int w = 0; w < NT / 32; ++w) t += sm.red[w];
+      a.aux_loss[0] = (float)((double)a.alpha * (double)a.E * t);
     }
-    if (tid == 0) a.aux_loss[0] = (float)((double)a.alpha * (double)a.E * sm.red[0]);
   }
 }
 

@@ -404,6 +404,8 @@ union TopkSmem {
 };
 
 // Split path: one routing block of BT tokens, warp w takes tokens w, w + 16, ...
+// NPL = logits per lane (E <= 32 NPL).
+template <int NPL>
 __global__ void __launch_bounds__(kTopkThreads) router_topk_kernel(const TopkArgs a) {
   __shared__ TopkSmem sm;
   __shared__ int am_last;
@@ -414,23 +416,23 @@ __global__ void __launch_bounds__(kTopkThreads) router_topk_kernel(const TopkArg
   pdl_wait();
   pdl_trigger();
   __syncthreads();
-  float psum[16];
+  float psum[NPL];
 #pragma unroll
-  for (int i = 0; i < 16; ++i) psum[i] = 0.f;
+  for (int i = 0; i < NPL; ++i) psum[i] = 0.f;
   const int t0 = blockIdx.x * a.BT;
   for (int tl = warp; tl < a.BT; tl += kTopkWarps) {
     const int t = t0 + tl;
     if (t >= a.T) break;
-    float sv[16];
+    float sv[NPL];
 #pragma unroll
-    for (int i = 0; i < 16; ++i) {
+    for (int i = 0; i < NPL; ++i) {
       const int e = lane + 32 * i;
       sv[i] = e < E ? a.scores[(size_t)t * E + e] : -INFINITY;
     }
-    route_one_token<16>(sv, E, a.k, a.gate, a.sel_bias, a.topk_idx + (size_t)t * a.k,
-                        a.topk_w + (size_t)t * a.k, sm.t.cnt, psum);
+    route_one_token<NPL>(sv, E, a.k, a.gate, a.sel_bias, a.topk_idx + (size_t)t * a.k,
+                         a.topk_w + (size_t)t * a.k, sm.t.cnt, psum);
   }
-  publish_and_scan<kTopkThreads, 16>(a.scan, psum, sm.t.Pw, sm.t.cnt, sm.scan, &am_last);
+  publish_and_scan<kTopkThreads, NPL>(a.scan, psum, sm.t.Pw, sm.t.cnt, sm.scan, &am_last);
 }
 
 // ---------------------------------------------------------------- fused router
@@ -759,7 +761,13 @@ cudaError_t launch_router(const Plan& p, const void* x, const void* W_r, const f
   t.BT = p.BT;
   t.gate = p.cfg.gate;
   t.scan = scan_args(p, ws, so);
-  return launch_pdl(router_topk_kernel, dim3(p.nblk), dim3(kTopkThreads), 0, st, t);
+  const dim3 g(p.nblk), b(kTopkThreads);
+  const int npl = (p.cfg.E + 31) / 32;
+  if (npl <= 1) return launch_pdl(router_topk_kernel<1>, g, b, 0, st, t);
+  if (npl <= 2) return launch_pdl(router_topk_kernel<2>, g, b, 0, st, t);
+  if (npl <= 4) return launch_pdl(router_topk_kernel<4>, g, b, 0, st, t);
+  if (npl <= 8) return launch_pdl(router_topk_kernel<8>, g, b, 0, st, t);
+  return launch_pdl(router_topk_kernel<16>, g, b, 0, st, t);
 }
 
 static cudaError_t launch_logits(const Plan& p, const void* x, const void* W_r,

@@ -55,7 +55,7 @@ def test_workspace_sizes(name):
     elem = 4 if s.dtype == "f32" else 2
     # the expert-ordered copies alone: at least T*k rows of x, h and o
     assert fw >= s.T * s.k * (s.d * elem + s.f * elem + s.d * 4)
-    assert L.launch_count(cfg) == 6
+    assert L.launch_count(cfg) == (5 if (s.k == 1 and s.dtype == "bf16" and not s.n_shared) else 6)
 
 
 def _rc_size(cfg):
