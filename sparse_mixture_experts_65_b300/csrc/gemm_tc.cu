@@ -35,6 +35,7 @@
 #include "launch.cuh"
 #include "moe_internal.h"
 #include "ptx.cuh"
+#include "tma_host.cuh"
 
 namespace moe {
 
@@ -45,7 +46,8 @@ enum { EPI_SWIGLU = 0, EPI_GELU = 1, EPI_RELU = 2, EPI_F32 = 3, EPI_F32_CHUNKED 
 // the combine is folded into the epilogue.  Row r of expert e holds the single
 // kept slot of token t = row_token[r], so y[t] = bf16(g_t * acc) is written
 // directly -- the same float32 product and the same single rounding as the
-// separate combine kernel.
+// separate combine kernel.  The epilogue warps also write y = 0 for the
+// dropped tokens (key_row < 0).
 
 // EPI_F32_CHUNKED: the reduction runs in chunks of kChunkKB k-blocks (128 k),
 // each accumulated by the tensor cores from zero; the epilogue adds the chunk
@@ -71,10 +73,14 @@ struct TcArgs {
   int ld_out_sh;
   const float* col_bias;  // EPI_F32_CHUNKED: added per output column (may be null)
   int partial_rows;       // A tiles with at most this many real rows load 32-row boxes
-  const int* row_token;   // EPI_COMBINE1: token of each expert-ordered row
+  const int* row_token;   // token of each expert-ordered row (gather, EPI_COMBINE1)
   const float* gate;      // EPI_COMBINE1: topk_w, one gate per token
   void* y;                // EPI_COMBINE1: [T][ld_y] bf16 layer output
   int ld_y;
+  const int* key_row;     // EPI_COMBINE1: [T] row of each token's slot, -1 if dropped
+  int T_tokens;
+  const char* gx;         // gathering up projection: x, rows of gx_row_bytes
+  int gx_row_bytes;
   uint32_t* status;
   uint64_t timeout_ns;
 };
@@ -103,7 +109,9 @@ struct TcCfg {
   // the device tile schedule, copied to shared memory once per CTA:
   // tp[E+2] | seg_start[E] | mtiles[E+1] | kept[E]
   static constexpr int SCHED_INTS = 4 * (kMaxE + 2);
-  static constexpr int SMEM = 1024 + STAGES * STAGE_BYTES + BAR_BYTES + 4 * SCHED_INTS;
+  // row -> token tables of the four gathering producer warps (128 each)
+  static constexpr int TOK_BYTES = 4 * 128 * 4;
+  static constexpr int SMEM = 1024 + STAGES * STAGE_BYTES + BAR_BYTES + 4 * SCHED_INTS + TOK_BYTES;
   static constexpr uint32_t IDESC = idesc_bf16_f32(BM, MMA_N);
 };
 
@@ -240,15 +248,24 @@ __device__ __forceinline__ void epilogue_tile(const TcArgs& a, const TileInfo& t
   }
 }
 
-// A tiles with at most kPartialRows real rows (small expert segments, decode
-// batches) are loaded as ceil(rows / 32) boxes of 32 rows instead of one
-// 128-row box: the rows left unloaded only feed accumulator rows that the
+// A tiles with at most TcArgs::partial_rows real rows (small expert segments,
+// decode batches) are loaded as ceil(rows / 32) boxes of 32 rows instead of
+// one 128-row box: the rows left unloaded only feed accumulator rows that the
 // epilogue never stores.
-constexpr int kPartialRows = 96;
 constexpr int kABox = 32;
 
-template <int BNH, bool DUAL, int EPI>
-__global__ void __launch_bounds__(192, 1)
+// Warp roles: producer warps (one TMA warp, or four gathering warps), one MMA
+// warp, four epilogue warps.
+template <bool GATHER>
+struct TcWarps {
+  static constexpr int PROD = GATHER ? 4 : 1;
+  static constexpr int MMA = PROD;
+  static constexpr int EPI0 = PROD + 1;
+  static constexpr int THREADS = (PROD + 5) * 32;
+};
+
+template <int BNH, bool DUAL, int EPI, bool GATHER>
+__global__ void __launch_bounds__(TcWarps<GATHER>::THREADS, 1)
 tc_grouped_gemm(const __grid_constant__ CUtensorMap mA, const __grid_constant__ CUtensorMap mA_sh,
                 const __grid_constant__ CUtensorMap mA32, const __grid_constant__ CUtensorMap mA32_sh,
                 const __grid_constant__ CUtensorMap mB0, const __grid_constant__ CUtensorMap mB1,
@@ -273,7 +290,9 @@ tc_grouped_gemm(const __grid_constant__ CUtensorMap mA, const __grid_constant__ 
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::STAGES; ++s) {
-      mbar_init(full_bar(s), 1);
+      // gathering: the transaction arrive of the stage's warp, then its
+      // second arrive once the warp's row copies have landed
+      mbar_init(full_bar(s), GATHER ? 2 : 1);
       mbar_init(empty_bar(s), 1);
     }
     for (int b = 0; b < 2; ++b) {
@@ -296,7 +315,8 @@ tc_grouped_gemm(const __grid_constant__ CUtensorMap mA, const __grid_constant__ 
       if (DUAL) tma_prefetch_desc(&mB1_sh);
     }
   }
-  if (warp == 1) {
+  using Wr = TcWarps<GATHER>;
+  if (warp == Wr::MMA) {
     tmem_alloc(smem_u32(tmem_slot), C::TMEM_COLS);
     tmem_relinquish();
   }
@@ -334,8 +354,114 @@ tc_grouped_gemm(const __grid_constant__ CUtensorMap mA, const __grid_constant__ 
     *abort_flag = 1;
   };
 
-  if (warp == 0) {
-    if (lane == 0) {
+  if (warp < Wr::PROD) {
+    if constexpr (GATHER) {
+      // ---------------- gathering producers (four warps) ----------------
+      // Warp w fills the stages of uses g = w, w + 4, ...  Routed tiles: the
+      // 128 A rows come straight from the token rows of x (row_token), by
+      // cp.async into the 128-byte-swizzled layout the MMA descriptors
+      // expect (16-byte chunk c of row i at i*128 + (c ^ (i & 7))*16); one
+      // warp instruction moves 4 whole 128-byte row segments (lanes 8r..8r+7
+      // take the 8 chunks of row 4t + r).  The warp waits for its copies,
+      // fences them for the tensor cores (generic -> async proxy) and
+      // arrives; meanwhile the other three warps fill their stages.
+      // Shared-expert tiles read x through the tensor map; B always by TMA.
+      uint32_t g = 0;
+      bool ok = true;
+      const int sub = lane >> 3, chunk = lane & 7;
+      for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
+        const TileInfo ti = decode_tile(a, sc, tile, BNH);
+        const int nk = (ti.K + C::BK - 1) / C::BK;
+        // does this warp fill any stage of the tile?
+        if (nk < Wr::PROD && (int)((uint32_t)(warp - (int)(g & 3u)) & 3u) >= nk) {
+          g += nk;
+          continue;
+        }
+        const bool gat = !ti.shared;
+        const CUtensorMap* pB0 = ti.shared ? &mB0_sh : &mB0;
+        const CUtensorMap* pB1 = ti.shared ? &mB1_sh : &mB1;
+        const int e = ti.shared ? 0 : ti.seg;
+        const int rows = ti.row_end - ti.a_row < kTcBM ? ti.row_end - ti.a_row : kTcBM;
+        const int a_boxes = gat || rows > a.partial_rows ? 0 : (rows + kABox - 1) / kABox;
+        const uint32_t a_bytes =
+            gat ? 0u : (a_boxes ? a_boxes * kABox * 128u : (uint32_t)C::A_BYTES);
+        // token of every row of the tile (-1 for padding rows), per warp
+        int* tok_s = reinterpret_cast<int*>(smem + C::STAGES * C::STAGE_BYTES + C::BAR_BYTES +
+                                            4 * C::SCHED_INTS) + warp * 128;
+        __syncwarp();
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const int r = ti.a_row + lane + 32 * j;
+          tok_s[lane + 32 * j] = (gat && r < ti.row_end) ? __ldg(a.row_token + r) : -1;
+        }
+        __syncwarp();
+        for (int kb = 0; kb < nk; ++kb, ++g) {
+          if ((int)(g & 3u) != warp) continue;
+          const int s = g % C::STAGES;
+          const uint32_t ph = (g / C::STAGES) & 1u;
+          int okw = 1;
+          if (lane == 0)
+            okw = mbar_wait_bounded(empty_bar(s), ph ^ 1u, a.timeout_ns, abort_flag) ? 1 : 0;
+          okw = __shfl_sync(0xffffffffu, okw, 0);
+          __syncwarp();
+          if (!okw) {
+            if (lane == 0) give_up();
+            ok = false;
+            break;
+          }
+          const uint32_t sa = smem_base + s * C::STAGE_BYTES;
+          const uint32_t sb = sa + C::A_BYTES;
+          if (lane == 0) {
+            mbar_arrive_expect_tx(full_bar(s), a_bytes + C::B_BYTES);
+            if (!gat) {
+              if (a_boxes == 0) {
+                tma_load_2d(sa, &mA_sh, full_bar(s), kb * C::BK, ti.a_row);
+              } else {
+                for (int b = 0; b < a_boxes; ++b)
+                  tma_load_2d(sa + b * kABox * 128, &mA32_sh, full_bar(s), kb * C::BK,
+                              ti.a_row + b * kABox);
+              }
+            }
+            tma_load_3d(sb, pB0, full_bar(s), kb * C::BK, ti.n0, e);
+            if (DUAL) tma_load_3d(sb + BNH * 128, pB1, full_bar(s), kb * C::BK, ti.n0, e);
+          }
+          if (gat) {
+            const int col = kb * C::BK + chunk * 8;
+            const bool in = col < ti.K;   // K is a multiple of 8
+#pragma unroll 8
+            for (int t = 0; t < 32; ++t) {
+              const int i = 4 * t + sub;
+              const int tok = tok_s[i];
+              if (tok >= 0)
+                cp_async16_s(sa + i * 128 + ((chunk ^ (i & 7)) << 4),
+                             in ? (const void*)(a.gx + (size_t)tok * a.gx_row_bytes +
+                                                (size_t)col * 2)
+                                : (const void*)a.gx,
+                             in ? 16u : 0u);
+            }
+            cp_async_commit_group();
+            cp_async_wait_group<0>();
+            fence_proxy_async_smem();
+          }
+          __syncwarp();
+          if (lane == 0) mbar_arrive(full_bar(s));
+        }
+      }
+      // nothing asynchronous may still target shared memory at exit: warp 0
+      // waits for the release (or, after a give-up, the landing) of the last
+      // use of every stage
+      if (warp == 0 && lane == 0) {
+        for (int s = 0; s < C::STAGES; ++s) {
+          if (g > static_cast<uint32_t>(s)) {
+            const uint32_t issues = (g - 1 - s) / C::STAGES + 1;
+            if (ok)
+              mbar_wait_bounded(empty_bar(s), (issues - 1) & 1u, a.timeout_ns, abort_flag);
+            else
+              mbar_wait_bounded(full_bar(s), (issues - 1) & 1u, a.timeout_ns, nullptr);
+          }
+        }
+      }
+    } else if (lane == 0) {
       // ---------------- TMA producer ----------------
       uint32_t g = 0;
       bool ok = true;
@@ -385,7 +511,7 @@ tc_grouped_gemm(const __grid_constant__ CUtensorMap mA, const __grid_constant__ 
         }
       }
     }
-  } else if (warp == 1) {
+  } else if (warp == Wr::MMA) {
     if (lane == 0) {
       // ---------------- MMA issuer ----------------
       uint32_t g = 0;
@@ -435,9 +561,21 @@ tc_grouped_gemm(const __grid_constant__ CUtensorMap mA, const __grid_constant__ 
       }
     }
   } else {
-    // ---------------- epilogue (warps 2..5) ----------------
+    // ---------------- epilogue (the last four warps) ----------------
     const int q = warp & 3;                  // TMEM lane quarter this warp may read
     const int row_in_tile = q * 32 + lane;
+    if constexpr (EPI == EPI_COMBINE1) {
+      // a dropped token (key_row < 0, top-1) gets y = 0: its rows are spread
+      // over all epilogue warps of the grid, written while the first
+      // accumulator is still being computed
+      uint4* y = static_cast<uint4*>(a.y);
+      const int nvec = a.ld_y * 2 / 16;
+      const int gw = blockIdx.x * 4 + (warp - Wr::EPI0), nw = gridDim.x * 4;
+      for (int t = gw; t < a.T_tokens; t += nw) {
+        if (__ldg(a.key_row + t) < 0)
+          for (int c = lane; c < nvec; c += 32) y[(size_t)t * nvec + c] = make_uint4(0, 0, 0, 0);
+      }
+    }
     int it = 0;
     bool ok = true;
     for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
@@ -496,113 +634,61 @@ tc_grouped_gemm(const __grid_constant__ CUtensorMap mA, const __grid_constant__ 
 
   tc_fence_before();
   __syncthreads();
-  if (warp == 1) {
+  if (warp == Wr::MMA) {
     tc_fence_after();
     tmem_dealloc(tmem_base, C::TMEM_COLS);
   }
 }
 
 // ---------------------------------------------------------------- host side
-typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
-                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
-                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
-                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-static EncodeTiledFn get_encode_fn() {
-  static EncodeTiledFn fn = nullptr;
-  static std::once_flag once;
-  std::call_once(once, []() {
-    void* p = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
-                                         &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<EncodeTiledFn>(p);
-  });
-  return fn;
-}
-
-// 2-D map over a row-major [rows][cols] bf16 matrix, box 64 cols x box_rows.
-static bool encode_2d(CUtensorMap* m, const void* ptr, uint64_t rows, uint64_t cols,
-                      uint32_t box_rows) {
-  EncodeTiledFn fn = get_encode_fn();
-  if (!fn) return false;
-  cuuint64_t dims[2] = {cols, rows};
-  cuuint64_t strides[1] = {cols * 2};
-  cuuint32_t box[2] = {64, box_rows};
-  cuuint32_t es[2] = {1, 1};
-  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box,
-            es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
-// 3-D map over [n_mat][rows][cols] bf16, box 64 cols x box_rows x 1.
-static bool encode_3d(CUtensorMap* m, const void* ptr, uint64_t n_mat, uint64_t rows,
-                      uint64_t cols, uint32_t box_rows) {
-  EncodeTiledFn fn = get_encode_fn();
-  if (!fn) return false;
-  cuuint64_t dims[3] = {cols, rows, n_mat};
-  cuuint64_t strides[2] = {cols * 2, rows * cols * 2};
-  cuuint32_t box[3] = {64, box_rows, 1};
-  cuuint32_t es[3] = {1, 1, 1};
-  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides, box,
-            es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 struct TcMaps {
   CUtensorMap A, A_sh, A32, A32_sh, B0, B1, B0_sh, B1_sh;
 };
 
-// Raise the dynamic shared-memory limit of a kernel once per device.
-template <typename K>
-static cudaError_t smem_attr_once(K kern, int bytes, std::atomic<uint64_t>& done) {
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return e;
-  const uint64_t bit = 1ull << (dev & 63);
-  if (done.load(std::memory_order_acquire) & bit) return cudaSuccess;
-  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
-  if (e == cudaSuccess) done.fetch_or(bit, std::memory_order_release);
-  return e;
-}
-
-template <int BNH, bool DUAL, int EPI>
+template <int BNH, bool DUAL, int EPI, bool GATHER = false>
 static cudaError_t run_tc(const TcMaps& m, const TcArgs& a, int grid, cudaStream_t st) {
   using C = TcCfg<BNH, DUAL, EPI>;
   static std::atomic<uint64_t> attr_done{0};
-  auto kern = tc_grouped_gemm<BNH, DUAL, EPI>;
+  auto kern = tc_grouped_gemm<BNH, DUAL, EPI, GATHER>;
   cudaError_t e = smem_attr_once(kern, C::SMEM, attr_done);
   if (e != cudaSuccess) return e;
-  return launch_pdl(kern, dim3(grid), dim3(192), C::SMEM, st, m.A, m.A_sh, m.A32, m.A32_sh, m.B0,
+  return launch_pdl(kern, dim3(grid), dim3(TcWarps<GATHER>::THREADS), C::SMEM, st, m.A, m.A_sh,
+                    m.A32, m.A32_sh, m.B0,
                     m.B1, m.B0_sh, m.B1_sh, a);
 }
 
-static cudaError_t dispatch_up(int bn, int act, const TcMaps& m, const TcArgs& a, int grid,
-                               cudaStream_t st) {
+template <bool GATHER>
+static cudaError_t dispatch_up_t(int bn, int act, const TcMaps& m, const TcArgs& a, int grid,
+                                 cudaStream_t st) {
   if (act == MOE_ACT_SWIGLU) {
     switch (bn) {
-      case 128: return run_tc<128, true, EPI_SWIGLU>(m, a, grid, st);
-      case 96: return run_tc<96, true, EPI_SWIGLU>(m, a, grid, st);
-      case 64: return run_tc<64, true, EPI_SWIGLU>(m, a, grid, st);
-      case 32: return run_tc<32, true, EPI_SWIGLU>(m, a, grid, st);
+      case 128: return run_tc<128, true, EPI_SWIGLU, GATHER>(m, a, grid, st);
+      case 96: return run_tc<96, true, EPI_SWIGLU, GATHER>(m, a, grid, st);
+      case 64: return run_tc<64, true, EPI_SWIGLU, GATHER>(m, a, grid, st);
+      case 32: return run_tc<32, true, EPI_SWIGLU, GATHER>(m, a, grid, st);
     }
   } else if (act == MOE_ACT_RELU) {
     switch (bn) {
-      case 256: return run_tc<256, false, EPI_RELU>(m, a, grid, st);
-      case 128: return run_tc<128, false, EPI_RELU>(m, a, grid, st);
-      case 96: return run_tc<96, false, EPI_RELU>(m, a, grid, st);
-      case 64: return run_tc<64, false, EPI_RELU>(m, a, grid, st);
+      case 256: return run_tc<256, false, EPI_RELU, GATHER>(m, a, grid, st);
+      case 128: return run_tc<128, false, EPI_RELU, GATHER>(m, a, grid, st);
+      case 96: return run_tc<96, false, EPI_RELU, GATHER>(m, a, grid, st);
+      case 64: return run_tc<64, false, EPI_RELU, GATHER>(m, a, grid, st);
     }
   } else {
     switch (bn) {
-      case 256: return run_tc<256, false, EPI_GELU>(m, a, grid, st);
-      case 128: return run_tc<128, false, EPI_GELU>(m, a, grid, st);
-      case 96: return run_tc<96, false, EPI_GELU>(m, a, grid, st);
-      case 64: return run_tc<64, false, EPI_GELU>(m, a, grid, st);
+      case 256: return run_tc<256, false, EPI_GELU, GATHER>(m, a, grid, st);
+      case 128: return run_tc<128, false, EPI_GELU, GATHER>(m, a, grid, st);
+      case 96: return run_tc<96, false, EPI_GELU, GATHER>(m, a, grid, st);
+      case 64: return run_tc<64, false, EPI_GELU, GATHER>(m, a, grid, st);
     }
   }
   return cudaErrorInvalidValue;
+}
+
+static cudaError_t dispatch_up(bool gather, int bn, int act, const TcMaps& m, const TcArgs& a,
+                               int grid, cudaStream_t st) {
+  return gather ? dispatch_up_t<true>(bn, act, m, a, grid, st)
+                : dispatch_up_t<false>(bn, act, m, a, grid, st);
 }
 
 static cudaError_t dispatch_down(int bn, bool combine1, const TcMaps& m, const TcArgs& a,
@@ -639,14 +725,18 @@ cudaError_t launch_experts_tc(const Plan& p, const void* x, const void* W1, cons
   const bool sh = c.n_shared != 0;
   const bool dual = c.act == MOE_ACT_SWIGLU;
   uint32_t* status = reinterpret_cast<uint32_t*>(w + p.ws.status);
-  const void* xp = w + p.ws.xp;
   const void* h = w + p.ws.h;
   const void* hs = sh ? static_cast<const void*>(w + p.ws.hs) : h;
 
-  // ---- up projection: h = act(xp W1^T) or silu(xp W1^T) * (xp W3^T) ----
+  // ---- up projection: h = act(xp W1^T) or silu(xp W1^T) * (xp W3^T), where
+  // xp holds the routed rows of x in expert order: either gathered through
+  // row_token inside the kernel, or copied beforehand and read by TMA; the
+  // shared expert reads x itself ----
+  const void* a_src = p.gather ? x : static_cast<const void*>(w + p.ws.xp);
+  const uint64_t a_rows = p.gather ? (uint64_t)c.T : (uint64_t)p.R_cap;
   TcMaps mu;
-  bool ok = encode_2d(&mu.A, xp, p.R_cap, c.d, kTcBM);
-  ok = ok && encode_2d(&mu.A32, xp, p.R_cap, c.d, kABox);
+  bool ok = encode_2d(&mu.A, a_src, a_rows, c.d, kTcBM);
+  ok = ok && encode_2d(&mu.A32, a_src, a_rows, c.d, kABox);
   ok = ok && encode_3d(&mu.B0, W1, c.E, c.f, c.d, p.up_bn);
   ok = ok && encode_3d(&mu.B1, dual ? W3 : W1, c.E, c.f, c.d, p.up_bn);
   if (sh) {
@@ -671,10 +761,14 @@ cudaError_t launch_experts_tc(const Plan& p, const void* x, const void* W1, cons
   au.static_total = 0;
   au.col_bias = nullptr;
   au.partial_rows = p.partial_rows_up;
-  au.row_token = nullptr;
+  au.row_token = reinterpret_cast<const int*>(w + p.ws.row_token);
+  au.gx = static_cast<const char*>(x);
+  au.gx_row_bytes = c.d * 2;
   au.gate = nullptr;
   au.y = nullptr;
   au.ld_y = 0;
+  au.key_row = nullptr;
+  au.T_tokens = 0;
   au.E = c.E;
   au.has_shared = sh ? 1 : 0;
   au.N = c.f;
@@ -688,7 +782,7 @@ cudaError_t launch_experts_tc(const Plan& p, const void* x, const void* W1, cons
   au.status = status;
   au.timeout_ns = kGemmTimeoutNs;
   const int grid_up = p.max_tiles_up < p.num_sms ? p.max_tiles_up : p.num_sms;
-  cudaError_t e = dispatch_up(p.up_bn, c.act, mu, au, grid_up, st);
+  cudaError_t e = dispatch_up(p.gather, p.up_bn, c.act, mu, au, grid_up, st);
   if (e != cudaSuccess) return e;
   if (mid_event) {
     e = cudaEventRecord(mid_event, st);
@@ -719,6 +813,8 @@ cudaError_t launch_experts_tc(const Plan& p, const void* x, const void* W1, cons
     ad.gate = topk_w;
     ad.y = y;
     ad.ld_y = c.d;
+    ad.key_row = reinterpret_cast<const int*>(w + p.ws.key_row);
+    ad.T_tokens = c.T;
   }
   ad.tp = meta.tp_dn;
   ad.N = c.d;
@@ -769,6 +865,10 @@ cudaError_t launch_router_tc(const Plan& p, const void* x, const void* W_r,
   a.gate = nullptr;
   a.y = nullptr;
   a.ld_y = 0;
+  a.key_row = nullptr;
+  a.T_tokens = 0;
+  a.gx = nullptr;
+  a.gx_row_bytes = 0;
   a.status = status;
   a.timeout_ns = kGemmTimeoutNs;
   const int grid = a.static_total < p.num_sms ? a.static_total : p.num_sms;

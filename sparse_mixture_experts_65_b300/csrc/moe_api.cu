@@ -88,7 +88,18 @@ int make_plan(const moe_config* cfg, WsKind kind, Plan* p, int num_sms) {
     P.fu_tm = ceil_div(c.T, 32) >= 64 ? 2 : 1;
     P.router_fused = P.fu_tn > 0 && !force_split && force_fused;
   }
-  if (P.router_fused) {
+  // One-launch tensor-core routing (bf16, E <= 64, k <= 8) unless MOE_ROUTER
+  // forces another path; its routing blocks are its 128-token tiles.
+  {
+    const char* r = std::getenv("MOE_ROUTER");
+    const bool forced = r && (std::strcmp(r, "simt") == 0 || std::strcmp(r, "fused") == 0 ||
+                              std::strcmp(r, "tc") == 0);
+    P.route_tc = route_tc_eligible(c) && !forced;
+    if (P.route_tc) P.router_fused = false;
+  }
+  if (P.route_tc) {
+    P.BT = kTcBM;
+  } else if (P.router_fused) {
     P.BT = 16 * P.fu_tm;
   } else {
     // routing blocks: 16 tokens per pass (one per warp), enough passes that
@@ -181,6 +192,18 @@ int make_plan(const moe_config* cfg, WsKind kind, Plan* p, int num_sms) {
     P.partial_rows_up = v ? P.partial_rows : (c.act == MOE_ACT_SWIGLU ? 0 : 64);
   }
   P.combine_in_down = P.tc && c.k == 1 && c.n_shared == 0;
+  // The up projection gathers the token rows itself (cp.async) for
+  // tensor-core layers routed in one launch whose experts average at most
+  // one 128-row tile: there the weights dominate and the gather costs
+  // nothing (measured: Switch layer).  Wider experts (Mixtral-like) and the
+  // split router read an expert-ordered copy through TMA, which keeps the
+  // compute-bound up projection fed.  MOE_GATHER=0/1 overrides.
+  {
+    const long long per_expert = Tk / (c.E > 0 ? c.E : 1);
+    P.gather = P.tc && P.route_tc && per_expert <= kTcBM;
+    const char* gv = std::getenv("MOE_GATHER");
+    if (gv && P.tc && P.route_tc) P.gather = std::atoi(gv) != 0;
+  }
   P.nt_up = ceil_div(c.f, P.up_bn);
   P.nt_dn = ceil_div(c.d, P.dn_bn);
   P.nt_up_sh = c.n_shared ? ceil_div(c.f_shared, P.up_bn) : 0;
@@ -211,7 +234,7 @@ int make_plan(const moe_config* cfg, WsKind kind, Plan* p, int num_sms) {
   L.row_token = take(sizeof(int) * (size_t)P.R_cap);
   if (kind != WsKind::Route) {
     const size_t act_elem = P.elem;   // h is bf16 on the tensor-core path, fp32 otherwise
-    L.xp = take((size_t)P.R_cap * c.d * P.elem);
+    L.xp = take(P.gather ? 0 : (size_t)P.R_cap * c.d * P.elem);
     L.h = take((size_t)P.R_cap * c.f * act_elem);
     L.o = take((size_t)P.R_cap * c.d * sizeof(float));
     if (c.n_shared) {
@@ -342,11 +365,22 @@ static int forward_impl(const moe_config* cfg, const Tensors& t, void* ws, size_
 
   if ((rc = record(events, MOE_STAGE_ROUTER, st)) != MOE_OK) return rc;
   const ScanOutputs so{t.expert_counts, t.aux_loss, t.routed_counts, t.offsets, t.f_out, t.P_out};
-  cudaEvent_t topk_ev = events ? static_cast<cudaEvent_t>(events[MOE_STAGE_TOPK]) : nullptr;
-  MOE_TRY_CUDA(launch_router(p, t.x, t.W_r, t.logit_offset, t.sel_bias, t.topk_idx, t.topk_w, ws,
-                             so, st, topk_ev));
-  if ((rc = record(events, MOE_STAGE_PERMUTE, st)) != MOE_OK) return rc;
-  MOE_TRY_CUDA(launch_permute(p, t.x, t.topk_idx, t.slot_pos, !route_only, ws, st, t.y));
+  if (p.route_tc) {
+    // stages 1-4 in one launch; the top-k and permute stages are empty
+    MOE_TRY_CUDA(launch_route_tc(p, t.x, t.W_r, t.logit_offset, t.sel_bias, t.topk_idx, t.topk_w,
+                                 t.slot_pos, ws, so, st));
+    if ((rc = record(events, MOE_STAGE_TOPK, st)) != MOE_OK) return rc;
+    if ((rc = record(events, MOE_STAGE_PERMUTE, st)) != MOE_OK) return rc;
+    if (!route_only && !p.gather) MOE_TRY_CUDA(launch_gather_rows(p, t.x, ws, st));
+  } else {
+    cudaEvent_t topk_ev = events ? static_cast<cudaEvent_t>(events[MOE_STAGE_TOPK]) : nullptr;
+    MOE_TRY_CUDA(launch_router(p, t.x, t.W_r, t.logit_offset, t.sel_bias, t.topk_idx, t.topk_w,
+                               ws, so, st, topk_ev));
+    if ((rc = record(events, MOE_STAGE_PERMUTE, st)) != MOE_OK) return rc;
+    // the expert-ordered copies (unless the up projection gathers rows)
+    MOE_TRY_CUDA(
+        launch_permute(p, t.x, t.topk_idx, t.slot_pos, !route_only && !p.gather, ws, st, t.y));
+  }
   if (route_only) return MOE_OK;
   if ((rc = record(events, MOE_STAGE_UP, st)) != MOE_OK) return rc;
   cudaEvent_t mid = events ? static_cast<cudaEvent_t>(events[MOE_STAGE_DOWN]) : nullptr;
@@ -511,9 +545,13 @@ int moe_launch_count(const moe_config* cfg, int32_t* launches) {
   Plan p;
   const int rc = make_plan(cfg, WsKind::Forward, &p);
   if (rc != MOE_OK) return rc;
-  // one kernel per stage; top-1 bf16 layers without a shared expert fold the
-  // combine into the down projection
-  *launches = cfg->T == 0 ? 0 : (p.combine_in_down ? MOE_NUM_STAGES - 1 : MOE_NUM_STAGES);
+  // routing: one launch (tensor-core routing; a second one copies the rows
+  // unless the up projection gathers them), two (fused float32 router +
+  // permute) or three (logits, top-k, permute); then the two projections and
+  // the combine, which top-1 bf16 layers without a shared expert fold into
+  // the down projection
+  const int routing = p.route_tc ? (p.gather ? 1 : 2) : (p.router_fused ? 2 : 3);
+  *launches = cfg->T == 0 ? 0 : routing + 2 + (p.combine_in_down ? 0 : 1);
   return MOE_OK;
 }
 

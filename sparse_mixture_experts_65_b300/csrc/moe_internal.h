@@ -23,9 +23,15 @@ constexpr int kTcBM = 128;           // rows per tensor-core tile
 constexpr int kSimtBM = 64;          // rows per SIMT tile (fp32 path)
 constexpr int kSimtBN = 64;
 // Workspace header (zeroed once by the caller): status word at 0, routing
-// block-completion counter at 16, router split-reduction tile counters from
-// kTileCounterOffset on.
+// block-completion counter at 16, the one-launch router's grid-wait
+// counters (arrivals, passes) at 32 and 48, router split-reduction tile
+// counters from kTileCounterOffset on.  Every counter is back at zero when a
+// call has finished without a timeout.
 constexpr int kWsHeaderBytes = 4096;
+constexpr int kRouteDoneOffset = 16;
+constexpr int kRouteArriveOffset = 32;
+constexpr int kRoutePassedOffset = 48;
+constexpr int kRouteTcMaxOwn = 16;        // 128-token tiles per CTA of the one-launch router
 constexpr int kTileCounterOffset = 256;
 constexpr int kMaxTileCounters = (kWsHeaderBytes - kTileCounterOffset) / 4;
 
@@ -40,7 +46,8 @@ struct WsLayout {
                       //        | tp_up[E+2] | tp_dn[E+2]
   size_t key_row;     // int32  [T*k]      padded row of each assignment, -1 if dropped
   size_t row_token;   // int32  [R_cap]    token of each expert-ordered row
-  size_t xp;          // dtype  [R_cap][d] token copies in expert order
+  size_t xp;          // dtype  [R_cap][d] token copies in expert order (absent when the
+                      //        tensor-core up projection gathers the rows of x itself)
   size_t h;           // dtype  [R_cap][f] expert hidden activations
   size_t o;           // float  [R_cap][d] expert outputs
   size_t hs;          // dtype  [T_pad][f_s] shared-expert hidden
@@ -56,7 +63,8 @@ struct Plan {
   int capacity;       // INT32_MAX when unlimited
   int BT;             // tokens per routing block
   int nblk;           // routing blocks
-  bool router_tc;     // router logits on the tensor cores (experiment switch)
+  bool router_tc;     // router logits on the tensor cores
+  bool route_tc;      // stages 1-4 in one tensor-core launch (bf16, E <= 64, k <= 8)
   bool router_fused;  // one kernel: logits, top-k, histogram, scan (E <= 256)
   int fu_tm, fu_tn;   // fused router: tokens per thread (1, 2), experts per thread
   int sc_tn;          // router GEMM: experts per thread (2 or 4)
@@ -75,6 +83,7 @@ struct Plan {
   int partial_rows;           // A tiles with at most this many rows load only those rows
   int partial_rows_up;        // the same for the up projection
   bool combine_in_down;       // top-1, no shared expert, bf16: y written by the down epilogue
+  bool gather;                // the up projection gathers token rows (no expert-ordered copy)
   int num_sms;
   WsLayout ws;
 };
@@ -108,6 +117,12 @@ struct ScanOutputs {
 cudaError_t launch_router(const Plan& p, const void* x, const void* W_r, const float* logit_offset,
                           const float* sel_bias, int32_t* topk_idx, float* topk_w, void* ws,
                           const ScanOutputs& so, cudaStream_t st, cudaEvent_t mid_event);
+bool route_tc_eligible(const moe_config& c);
+cudaError_t launch_route_tc(const Plan& p, const void* x, const void* W_r,
+                            const float* logit_offset, const float* sel_bias, int32_t* topk_idx,
+                            float* topk_w, int32_t* slot_pos, void* ws, const ScanOutputs& so,
+                            cudaStream_t st);
+cudaError_t launch_gather_rows(const Plan& p, const void* x, void* ws, cudaStream_t st);
 cudaError_t launch_router_tc(const Plan& p, const void* x, const void* W_r,
                              const float* logit_offset, float* scores, uint32_t* status,
                              cudaStream_t st);

@@ -32,8 +32,6 @@ struct PermuteArgs {
   Meta m;
   void* xp;
   int* row_token;        // [R_cap]: token of each kept row
-  void* y_zero;          // top-1 layers whose combine runs in the down projection:
-                         // the y rows of dropped tokens are zeroed here
   int T, E, k, BT, capacity, nvec;   // nvec: 16-byte vectors per token row
   int copy;
 };
@@ -83,13 +81,6 @@ __global__ void __launch_bounds__(kPermuteThreads) permute_kernel(const PermuteA
     }
   }
   __syncthreads();
-  if (a.y_zero) {                 // top-1: a dropped slot leaves its token's y at zero
-    uint4* y = static_cast<uint4*>(a.y_zero);
-    for (int i = tid; i < nk * a.nvec; i += kPermuteThreads) {
-      const int q = i / a.nvec;
-      if (row_s[q] < 0) y[(size_t)(t0 + q) * a.nvec + (i - q * a.nvec)] = make_uint4(0, 0, 0, 0);
-    }
-  }
   if (!a.copy) return;
   // Row copies: (key, 16-byte vector) pairs spread over the block, four
   // independent loads in flight per thread before their stores.
@@ -121,6 +112,56 @@ __global__ void __launch_bounds__(kPermuteThreads) permute_kernel(const PermuteA
   }
 }
 
+// Copy of the kept token rows into expert order after the one-launch router
+// (key_row is final): grid-stride over (key, 16-byte vector), eight loads in
+// flight per thread.
+constexpr int kGatherThreads = 256;
+
+__global__ void __launch_bounds__(kGatherThreads) gather_rows_kernel(
+    const uint4* x, uint4* xp, const int* key_row, int nkeys, int k, int nvec) {
+  pdl_wait();
+  pdl_trigger();
+  const long long total = (long long)nkeys * nvec;
+  const long long stride = (long long)gridDim.x * kGatherThreads;
+  constexpr int U = 8;
+  for (long long i0 = (long long)blockIdx.x * kGatherThreads + threadIdx.x; i0 < total;
+       i0 += stride * U) {
+    uint4 v[U];
+    long long dst[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const long long i = i0 + u * stride;
+      dst[u] = -1;
+      if (i < total) {
+        const int q = (int)(i / nvec);
+        const int c = (int)(i - (long long)q * nvec);
+        const int row = key_row[q];
+        if (row >= 0) {
+          v[u] = x[(size_t)(q / k) * nvec + c];
+          dst[u] = (long long)row * nvec + c;
+        }
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u)
+      if (dst[u] >= 0) xp[dst[u]] = v[u];
+  }
+}
+
+cudaError_t launch_gather_rows(const Plan& p, const void* x, void* ws, cudaStream_t st) {
+  char* w = static_cast<char*>(ws);
+  const int nkeys = p.cfg.T * p.cfg.k;
+  const int nvec = p.cfg.d * p.elem / 16;
+  const long long total = (long long)nkeys * nvec;
+  long long blocks = (total + kGatherThreads * 8 - 1) / (kGatherThreads * 8);
+  const long long cap = 8LL * p.num_sms;
+  if (blocks > cap) blocks = cap;
+  if (blocks < 1) blocks = 1;
+  return launch_pdl(gather_rows_kernel, dim3((unsigned)blocks), dim3(kGatherThreads), 0, st,
+                    static_cast<const uint4*>(x), reinterpret_cast<uint4*>(w + p.ws.xp),
+                    reinterpret_cast<const int*>(w + p.ws.key_row), nkeys, p.cfg.k, nvec);
+}
+
 Meta meta_ptrs(const Plan& p, void* ws) {
   int* base = reinterpret_cast<int*>(static_cast<char*>(ws) + p.ws.meta);
   const int E = p.cfg.E;
@@ -146,7 +187,7 @@ cudaError_t launch_permute(const Plan& p, const void* x, const int32_t* topk_idx
   a.m = meta_ptrs(p, ws);
   a.xp = static_cast<char*>(ws) + p.ws.xp;
   a.row_token = reinterpret_cast<int*>(static_cast<char*>(ws) + p.ws.row_token);
-  a.y_zero = (copy_rows && p.combine_in_down) ? y : nullptr;
+  (void)y;
   a.T = p.cfg.T;
   a.E = p.cfg.E;
   a.k = p.cfg.k;

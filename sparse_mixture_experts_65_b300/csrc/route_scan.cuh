@@ -36,6 +36,36 @@ struct ScanArgs {
   unsigned int* done_counter;   // routing blocks finished (reset by the last one)
 };
 
+// Scan arguments of a layer call: workspace regions and caller outputs.
+inline ScanArgs scan_args(const Plan& p, void* ws, const ScanOutputs& so) {
+  char* w = static_cast<char*>(ws);
+  ScanArgs c;
+  c.blk_cnt = reinterpret_cast<int*>(w + p.ws.blk_cnt);
+  c.blk_prob = reinterpret_cast<float*>(w + p.ws.blk_prob);
+  c.m = meta_ptrs(p, ws);
+  c.nblk = p.nblk;
+  c.E = p.cfg.E;
+  c.T = p.cfg.T;
+  c.k = p.cfg.k;
+  c.capacity = p.capacity;
+  c.bm = p.bm;
+  c.nt_up = p.nt_up;
+  c.nt_dn = p.nt_dn;
+  c.nt_up_sh = p.nt_up_sh;
+  c.nt_dn_sh = p.nt_dn_sh;
+  c.mt_sh = p.mt_sh;
+  c.has_shared = p.cfg.n_shared;
+  c.alpha = p.cfg.alpha;
+  c.expert_counts = so.expert_counts;
+  c.aux_loss = so.aux_loss;
+  c.routed_counts = so.routed_counts;
+  c.offsets_out = so.offsets;
+  c.f_out = so.f_out;
+  c.P_out = so.P_out;
+  c.done_counter = reinterpret_cast<unsigned int*>(w + p.ws.status + kRouteDoneOffset);
+  return c;
+}
+
 template <int NT>
 struct ScanSmem {
   int scratch[4 * 33];

@@ -297,10 +297,49 @@ def test_router_logits_within_half_the_near_tie_band(monkeypatch, path, name):
     assert err.max() < 5e-6
 
 
+ONE_LAUNCH = [
+    # 150 tiles of 128 tokens on 148 SMs: two routing CTAs own two tiles each
+    LayerShape("route_multi_tile", 40, T=19200, d=64, E=64, k=1, f=64, act=RE, gate=FULL,
+               dtype="bf16", capacity_factor=1.25, logit_offset_var=1.5),
+    # the largest k of the one-launch router, with sigmoid gates and a bias
+    LayerShape("route_k8_sigmoid", 41, T=300, d=128, E=64, k=8, f=64, act=SW, gate=SIG,
+               dtype="bf16", sel_bias_halfwidth=0.05, capacity_factor=1.5),
+    # a wider model: 16 k-blocks per row gathered by the up projection
+    LayerShape("route_wide_rows", 42, T=1024, d=1024, E=8, k=2, f=64, act=SW, gate=TOPK,
+               dtype="bf16"),
+    # E = 33: the 64-wide expert tile with a ragged tail, k = 3
+    LayerShape("route_e33", 43, T=700, d=96, E=33, k=3, f=64, act=GE, gate=FULL, dtype="bf16",
+               capacity_factor=1.0, logit_offset_var=1.5),
+]
+
+
+@pytest.mark.parametrize("shape", ONE_LAUNCH, ids=lambda s: s.name)
+def test_one_launch_router_layers(shape):
+    """Layers routed by the one-launch tensor-core router (bf16, E <= 64,
+    k <= 8): several tiles per CTA, k = 8, wide rows, a ragged E."""
+    inp = W.make_inputs(shape, "cuda", seed=2)
+    _, out = run_gpu(inp)
+    rep = check_layer(inp, out)
+    print(shape.name, rep)
+
+
+@pytest.mark.parametrize("gather", ["0", "1"])
+def test_up_projection_row_source(monkeypatch, gather):
+    """Both row sources of the tensor-core up projection on one-launch-routed
+    layers: rows gathered from x inside the GEMM (cp.async), and an
+    expert-ordered copy read through TMA."""
+    monkeypatch.setenv("MOE_GATHER", gather)
+    for shape in (SMALL[0], SMALL[1], SMALL[2], SMALL[3], ONE_LAUNCH[1], ONE_LAUNCH[3]):
+        inp = W.make_inputs(shape, "cuda", seed=12)
+        _, out = run_gpu(inp)
+        check_layer(inp, out)
+
+
 @pytest.mark.parametrize("path", ["simt", "fused", "tc"])
 def test_forced_router_path_parity(monkeypatch, path):
-    """Both float32 router paths (split-K logits + top-k kernel; fused logits,
-    top-k and scan) on small ragged layers, each routing as the oracle does."""
+    """The split router paths (split-K float32 logits, the fused float32
+    router, tensor-core logits; each followed by the top-k and permute
+    kernels) on small ragged layers, each routing as the oracle does."""
     monkeypatch.setenv("MOE_ROUTER", path)
     shapes = (SMALL[0], SMALL[1], SMALL[2], SMALL[3], SMALL[4], SMALL[5], SMALL[6])
     for shape in shapes:
