@@ -427,10 +427,10 @@ def run_b300(args):
     kept = fwd.out.expert_counts.cpu().tolist()
     acc, layer = accounting(shape, kept)
 
-    # per-stage events: MOE_NUM_STAGES + 1 per step
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(len(STAGES) + 1)]
-           for _ in range(K)]
-    arrs = [L.BoundForward.event_array(e, stream) for e in evs]
+    # The timed region runs the plain forward call, exactly as a user issues
+    # it (no per-stage events: an event between two kernels would stop the
+    # next one from starting its prologue early).  The per-stage times come
+    # from a separate, shorter pass with CUDA events between the stages.
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     clocks = ClockSampler(torch.cuda.current_device())
     clocks.start()
@@ -440,7 +440,7 @@ def run_b300(args):
     w0 = time.time()
     start.record(stream)
     for i in range(K):
-        fwd(arrs[i])
+        fwd()
     end.record(stream)
     torch.cuda.synchronize()
     w1 = time.time()
@@ -449,7 +449,14 @@ def run_b300(args):
     barrier()
     ms_total = max_over_ranks(start.elapsed_time(end), dist, "cuda")
     assert L.check_status(fwd.workspace) == 0, "device status after the timed region"
-    stage_ms = {s: statistics.fmean(evs[i][j].elapsed_time(evs[i][j + 1]) for i in range(K))
+    K_st = min(K, 200)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(len(STAGES) + 1)]
+           for _ in range(K_st)]
+    arrs = [L.BoundForward.event_array(e, stream) for e in evs]
+    for i in range(K_st):
+        fwd(arrs[i])
+    torch.cuda.synchronize()
+    stage_ms = {s: statistics.fmean(evs[i][j].elapsed_time(evs[i][j + 1]) for i in range(K_st))
                 for j, s in enumerate(STAGES)}
     ms_step = ms_total / K
     value = world * shape.T * K / (ms_total / 1e3)

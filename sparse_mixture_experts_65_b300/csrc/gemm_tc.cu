@@ -81,6 +81,7 @@ struct TcArgs {
   int T_tokens;
   const char* gx;         // gathering up projection: x, rows of gx_row_bytes
   int gx_row_bytes;
+  int early_b;            // the schedule predates the previous kernel: stream B before the wait
   uint32_t* status;
   uint64_t timeout_ns;
 };
@@ -324,11 +325,14 @@ tc_grouped_gemm(const __grid_constant__ CUtensorMap mA, const __grid_constant__ 
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
-  pdl_wait();      // everything above ran while the previous kernel finished
-  pdl_trigger();
+  // The tile schedule is copied to shared memory.  With early_b it was
+  // written two launches back (the routing kernel, which completed before the
+  // previous grid could start us), so it is read before the wait and the
+  // producer can stream the first stages' B tiles (weights) while the
+  // previous kernel finishes; everything that kernel writes (A) waits.
   Sched sc;
-  {
-    int* s_tp = reinterpret_cast<int*>(smem + C::STAGES * C::STAGE_BYTES + C::BAR_BYTES);
+  int* s_tp = reinterpret_cast<int*>(smem + C::STAGES * C::STAGE_BYTES + C::BAR_BYTES);
+  auto copy_sched = [&]() {
     int* s_seg = s_tp + (kMaxE + 2);
     int* s_mt = s_seg + (kMaxE + 2);
     int* s_kept = s_mt + (kMaxE + 2);
@@ -346,8 +350,34 @@ tc_grouped_gemm(const __grid_constant__ CUtensorMap mA, const __grid_constant__ 
     sc.seg_start = s_seg;
     sc.mtiles = s_mt;
     sc.kept = s_kept;
+  };
+  if (a.early_b) copy_sched();
+  const int total = a.static_mt > 0 ? a.static_total : (a.early_b ? s_tp[a.E + a.has_shared] : 0);
+  uint32_t npre = 0;   // uses whose B tiles were issued before the wait
+  if (!GATHER && a.early_b && warp == 0 && lane == 0) {
+    for (int tile = blockIdx.x; tile < total && npre < (uint32_t)C::STAGES; tile += gridDim.x) {
+      const TileInfo ti = decode_tile(a, sc, tile, BNH);
+      const int e = ti.shared ? 0 : ti.seg;
+      const int nk = (ti.K + C::BK - 1) / C::BK;
+      const int rows = ti.row_end - ti.a_row < kTcBM ? ti.row_end - ti.a_row : kTcBM;
+      const int a_boxes = rows > a.partial_rows ? 0 : (rows + kABox - 1) / kABox;
+      const uint32_t a_bytes = a_boxes ? a_boxes * kABox * 128u : (uint32_t)C::A_BYTES;
+      for (int kb = 0; kb < nk && npre < (uint32_t)C::STAGES; ++kb, ++npre) {
+        const uint32_t sb = smem_base + npre * C::STAGE_BYTES + C::A_BYTES;
+        mbar_arrive_expect_tx(full_bar(npre), a_bytes + C::B_BYTES);
+        tma_load_3d(sb, ti.shared ? &mB0_sh : &mB0, full_bar(npre), kb * C::BK, ti.n0, e);
+        if (DUAL)
+          tma_load_3d(sb + BNH * 128, ti.shared ? &mB1_sh : &mB1, full_bar(npre), kb * C::BK,
+                      ti.n0, e);
+      }
+    }
   }
-  const int total = a.static_mt > 0 ? a.static_total : sc.tp[a.E + a.has_shared];
+  pdl_wait();      // everything above ran while the previous kernel finished
+  pdl_trigger();
+  if (!a.early_b) copy_sched();
+  const int total_all =
+      a.static_mt > 0 ? a.static_total : sc.tp[a.E + a.has_shared];
+  (void)total;
 
   auto give_up = [&]() {
     atomicOr(a.status, STATUS_TIMEOUT_GEMM);
@@ -369,7 +399,7 @@ tc_grouped_gemm(const __grid_constant__ CUtensorMap mA, const __grid_constant__ 
       uint32_t g = 0;
       bool ok = true;
       const int sub = lane >> 3, chunk = lane & 7;
-      for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
+      for (int tile = blockIdx.x; tile < total_all && ok; tile += gridDim.x) {
         const TileInfo ti = decode_tile(a, sc, tile, BNH);
         const int nk = (ti.K + C::BK - 1) / C::BK;
         // does this warp fill any stage of the tile?
@@ -385,16 +415,11 @@ tc_grouped_gemm(const __grid_constant__ CUtensorMap mA, const __grid_constant__ 
         const int a_boxes = gat || rows > a.partial_rows ? 0 : (rows + kABox - 1) / kABox;
         const uint32_t a_bytes =
             gat ? 0u : (a_boxes ? a_boxes * kABox * 128u : (uint32_t)C::A_BYTES);
-        // token of every row of the tile (-1 for padding rows), per warp
+        // token of every row of the tile (-1 for padding rows), per warp;
+        // loaded after the warp's first B tile of the tile is in flight
         int* tok_s = reinterpret_cast<int*>(smem + C::STAGES * C::STAGE_BYTES + C::BAR_BYTES +
                                             4 * C::SCHED_INTS) + warp * 128;
-        __syncwarp();
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const int r = ti.a_row + lane + 32 * j;
-          tok_s[lane + 32 * j] = (gat && r < ti.row_end) ? __ldg(a.row_token + r) : -1;
-        }
-        __syncwarp();
+        bool tok_ready = !gat;
         for (int kb = 0; kb < nk; ++kb, ++g) {
           if ((int)(g & 3u) != warp) continue;
           const int s = g % C::STAGES;
@@ -424,6 +449,16 @@ tc_grouped_gemm(const __grid_constant__ CUtensorMap mA, const __grid_constant__ 
             }
             tma_load_3d(sb, pB0, full_bar(s), kb * C::BK, ti.n0, e);
             if (DUAL) tma_load_3d(sb + BNH * 128, pB1, full_bar(s), kb * C::BK, ti.n0, e);
+          }
+          if (!tok_ready) {
+            __syncwarp();
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              const int r = ti.a_row + lane + 32 * j;
+              tok_s[lane + 32 * j] = r < ti.row_end ? __ldg(a.row_token + r) : -1;
+            }
+            __syncwarp();
+            tok_ready = true;
           }
           if (gat) {
             const int col = kb * C::BK + chunk * 8;
@@ -465,7 +500,7 @@ tc_grouped_gemm(const __grid_constant__ CUtensorMap mA, const __grid_constant__ 
       // ---------------- TMA producer ----------------
       uint32_t g = 0;
       bool ok = true;
-      for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
+      for (int tile = blockIdx.x; tile < total_all && ok; tile += gridDim.x) {
         const TileInfo ti = decode_tile(a, sc, tile, BNH);
         const CUtensorMap* pA = ti.shared ? &mA_sh : &mA;
         const CUtensorMap* pA32 = ti.shared ? &mA32_sh : &mA32;
@@ -479,22 +514,25 @@ tc_grouped_gemm(const __grid_constant__ CUtensorMap mA, const __grid_constant__ 
         for (int kb = 0; kb < nk; ++kb, ++g) {
           const int s = g % C::STAGES;
           const uint32_t ph = (g / C::STAGES) & 1u;
-          if (!mbar_wait_bounded(empty_bar(s), ph ^ 1u, a.timeout_ns, abort_flag)) {
+          const bool pre = g < npre;   // B already in flight, transaction count set
+          if (!pre && !mbar_wait_bounded(empty_bar(s), ph ^ 1u, a.timeout_ns, abort_flag)) {
             give_up();
             ok = false;
             break;
           }
           const uint32_t sa = smem_base + s * C::STAGE_BYTES;
           const uint32_t sb = sa + C::A_BYTES;
-          mbar_arrive_expect_tx(full_bar(s), a_bytes + C::B_BYTES);
+          if (!pre) mbar_arrive_expect_tx(full_bar(s), a_bytes + C::B_BYTES);
           if (a_boxes == 0) {
             tma_load_2d(sa, pA, full_bar(s), kb * C::BK, ti.a_row);
           } else {
             for (int b = 0; b < a_boxes; ++b)
               tma_load_2d(sa + b * kABox * 128, pA32, full_bar(s), kb * C::BK, ti.a_row + b * kABox);
           }
-          tma_load_3d(sb, pB0, full_bar(s), kb * C::BK, ti.n0, e);
-          if (DUAL) tma_load_3d(sb + BNH * 128, pB1, full_bar(s), kb * C::BK, ti.n0, e);
+          if (!pre) {
+            tma_load_3d(sb, pB0, full_bar(s), kb * C::BK, ti.n0, e);
+            if (DUAL) tma_load_3d(sb + BNH * 128, pB1, full_bar(s), kb * C::BK, ti.n0, e);
+          }
         }
       }
       // Tail: on the normal path wait until the MMA warp has released every
@@ -517,7 +555,7 @@ tc_grouped_gemm(const __grid_constant__ CUtensorMap mA, const __grid_constant__ 
       uint32_t g = 0;
       int it = 0;
       bool ok = true;
-      for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
+      for (int tile = blockIdx.x; tile < total_all && ok; tile += gridDim.x) {
         const TileInfo ti = decode_tile(a, sc, tile, BNH);
         const int nk = (ti.K + C::BK - 1) / C::BK;
         const int ck = EPI == EPI_F32_CHUNKED ? kChunkKB : nk;   // k-blocks per accumulator
@@ -578,7 +616,7 @@ tc_grouped_gemm(const __grid_constant__ CUtensorMap mA, const __grid_constant__ 
     }
     int it = 0;
     bool ok = true;
-    for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
+    for (int tile = blockIdx.x; tile < total_all && ok; tile += gridDim.x) {
       const TileInfo ti = decode_tile(a, sc, tile, BNH);
       const size_t orow = static_cast<size_t>(ti.a_row + row_in_tile);
       const bool row_ok = ti.a_row + row_in_tile < ti.row_end;
@@ -764,6 +802,7 @@ cudaError_t launch_experts_tc(const Plan& p, const void* x, const void* W1, cons
   au.row_token = reinterpret_cast<const int*>(w + p.ws.row_token);
   au.gx = static_cast<const char*>(x);
   au.gx_row_bytes = c.d * 2;
+  au.early_b = 0;
   au.gate = nullptr;
   au.y = nullptr;
   au.ld_y = 0;
@@ -808,6 +847,7 @@ cudaError_t launch_experts_tc(const Plan& p, const void* x, const void* W1, cons
   if (!ok) return cudaErrorInvalidValue;
   TcArgs ad = au;
   ad.partial_rows = p.partial_rows;
+  ad.early_b = 1;   // the schedule comes from the routing kernel, two launches back
   if (p.combine_in_down) {
     ad.row_token = reinterpret_cast<const int*>(w + p.ws.row_token);
     ad.gate = topk_w;
@@ -869,6 +909,7 @@ cudaError_t launch_router_tc(const Plan& p, const void* x, const void* W_r,
   a.T_tokens = 0;
   a.gx = nullptr;
   a.gx_row_bytes = 0;
+  a.early_b = 0;
   a.status = status;
   a.timeout_ns = kGemmTimeoutNs;
   const int grid = a.static_total < p.num_sms ? a.static_total : p.num_sms;
