@@ -91,7 +91,8 @@ typedef struct {
   int32_t E;        /* routed experts, 1..512 */
   int32_t k;        /* experts per token, 1..min(E, 32) */
   int32_t f;        /* routed expert width, >= 1 */
-  int32_t n_shared; /* 0 or 1 always-on shared SwiGLU expert */
+  int32_t n_shared; /* 0 or 1 always-on shared SwiGLU expert (bf16: SwiGLU layers only,
+                       else MOE_ERR_UNSUPPORTED) */
   int32_t f_shared; /* width of the shared expert (ignored when n_shared = 0) */
   int32_t dtype;    /* moe_dtype */
   int32_t act;      /* moe_act of the routed experts */

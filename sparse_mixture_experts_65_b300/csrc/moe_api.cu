@@ -59,6 +59,9 @@ int make_plan(const moe_config* cfg, WsKind kind, Plan* p, int num_sms) {
   if (c.E > kMaxE || c.k > kMaxK) return MOE_ERR_UNSUPPORTED;
   const int vec = c.dtype == MOE_BF16 ? 8 : 4;
   if (c.d % vec || c.f % vec || (c.n_shared && c.f_shared % vec)) return MOE_ERR_UNSUPPORTED;
+  // the tensor-core kernels run the (SwiGLU) shared expert as one more
+  // segment of the routed experts' launches, so they need SwiGLU experts too
+  if (c.dtype == MOE_BF16 && c.n_shared && c.act != MOE_ACT_SWIGLU) return MOE_ERR_UNSUPPORTED;
   // every row index and element count of one matrix must fit in int32 / the TMA limits
   const long long Tk = (long long)c.T * c.k;
   if (Tk > (1LL << 30) || (long long)c.T * c.d > (1LL << 40)) return MOE_ERR_UNSUPPORTED;

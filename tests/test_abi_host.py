@@ -85,6 +85,20 @@ def test_bad_configs(field, value, code):
     assert _rc_size(cfg) == code
 
 
+def test_bf16_shared_expert_needs_swiglu_layers():
+    """The tensor-core path runs the SwiGLU shared expert inside the routed
+    experts' launches: a plain (ReLU / GELU) bf16 layer with a shared expert
+    is reported unsupported; float32 layers and SwiGLU layers take it."""
+    cfg = L.make_config(T=16, d=64, E=8, k=2, f=64, act=N.MOE_ACT_RELU, dtype="bf16")
+    cfg.n_shared, cfg.f_shared = 1, 64
+    assert _rc_size(cfg) == N.MOE_ERR_UNSUPPORTED
+    cfg.dtype = N.MOE_F32
+    assert _rc_size(cfg) == N.MOE_OK
+    cfg = L.make_config(T=16, d=64, E=8, k=2, f=64, dtype="bf16")
+    cfg.n_shared, cfg.f_shared = 1, 64
+    assert _rc_size(cfg) == N.MOE_OK
+
+
 def test_forward_rejects_null_and_small_workspace_without_gpu():
     cfg = L.make_config(T=16, d=64, E=8, k=2, f=64)
     lib = N.lib()
