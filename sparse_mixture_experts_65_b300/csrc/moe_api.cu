@@ -97,10 +97,15 @@ int make_plan(const moe_config* cfg, WsKind kind, Plan* p, int num_sms) {
     const char* r = std::getenv("MOE_ROUTER");
     const bool forced = r && (std::strcmp(r, "simt") == 0 || std::strcmp(r, "fused") == 0 ||
                               std::strcmp(r, "tc") == 0);
-    P.route_tc = route_tc_eligible(c) && !forced;
-    if (P.route_tc) P.router_fused = false;
+    // decode batches (T <= kSmallT): split-K logits, top-k, scan and
+    // positions in one small launch
+    P.route_small = !forced && c.T >= 1 && c.T <= kSmallT && c.E <= kSmallMaxE;
+    P.route_tc = route_tc_eligible(c) && !forced && !P.route_small;
+    if (P.route_tc || P.route_small) P.router_fused = false;
   }
-  if (P.route_tc) {
+  if (P.route_small) {
+    P.BT = c.T;
+  } else if (P.route_tc) {
     P.BT = kTcBM;
   } else if (P.router_fused) {
     P.BT = 16 * P.fu_tm;
@@ -228,8 +233,12 @@ int make_plan(const moe_config* cfg, WsKind kind, Plan* p, int num_sms) {
   // split partials only when the split float32 router runs (sc_* keep that
   // kernel's geometry whichever path this layer takes)
   const bool split_router = !P.router_tc && !P.router_fused;
-  L.score_parts = take(split_router && P.sc_splits > 1
-                           ? sizeof(float) * (size_t)P.sc_splits * c.T * E : 0);
+  size_t parts = split_router && P.sc_splits > 1 ? sizeof(float) * (size_t)P.sc_splits * c.T * E : 0;
+  if (P.route_small) {
+    const size_t small = sizeof(float) * (size_t)route_small_splits(c.d) * c.T * E;
+    if (small > parts) parts = small;
+  }
+  L.score_parts = take(parts);
   L.blk_cnt = take(sizeof(int) * (size_t)P.nblk * E);
   L.blk_prob = take(sizeof(float) * (size_t)P.nblk * E);
   L.meta = take(sizeof(int) * (E + (E + 1) * 3 + (E + 2) * 2));
@@ -368,7 +377,13 @@ static int forward_impl(const moe_config* cfg, const Tensors& t, void* ws, size_
 
   if ((rc = record(events, MOE_STAGE_ROUTER, st)) != MOE_OK) return rc;
   const ScanOutputs so{t.expert_counts, t.aux_loss, t.routed_counts, t.offsets, t.f_out, t.P_out};
-  if (p.route_tc) {
+  if (p.route_small) {
+    // stages 1-4 in one launch for a decode batch; top-k and permute are empty
+    MOE_TRY_CUDA(launch_route_small(p, t.x, t.W_r, t.logit_offset, t.sel_bias, t.topk_idx,
+                                    t.topk_w, t.slot_pos, !route_only && !p.gather, ws, so, st));
+    if ((rc = record(events, MOE_STAGE_TOPK, st)) != MOE_OK) return rc;
+    if ((rc = record(events, MOE_STAGE_PERMUTE, st)) != MOE_OK) return rc;
+  } else if (p.route_tc) {
     // stages 1-4 in one launch; the top-k and permute stages are empty
     MOE_TRY_CUDA(launch_route_tc(p, t.x, t.W_r, t.logit_offset, t.sel_bias, t.topk_idx, t.topk_w,
                                  t.slot_pos, ws, so, st));
@@ -548,12 +563,14 @@ int moe_launch_count(const moe_config* cfg, int32_t* launches) {
   Plan p;
   const int rc = make_plan(cfg, WsKind::Forward, &p);
   if (rc != MOE_OK) return rc;
-  // routing: one launch (tensor-core routing; a second one copies the rows
-  // unless the up projection gathers them), two (fused float32 router +
+  // routing: one launch (decode batches; tensor-core routing, plus a row
+  // copy unless the up projection gathers rows), two (fused float32 router +
   // permute) or three (logits, top-k, permute); then the two projections and
   // the combine, which top-1 bf16 layers without a shared expert fold into
   // the down projection
-  const int routing = p.route_tc ? (p.gather ? 1 : 2) : (p.router_fused ? 2 : 3);
+  const int routing = p.route_small ? 1
+                      : p.route_tc  ? (p.gather ? 1 : 2)
+                                    : (p.router_fused ? 2 : 3);
   *launches = cfg->T == 0 ? 0 : routing + 2 + (p.combine_in_down ? 0 : 1);
   return MOE_OK;
 }

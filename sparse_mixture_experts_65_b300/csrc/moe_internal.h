@@ -32,6 +32,8 @@ constexpr int kRouteDoneOffset = 16;
 constexpr int kRouteArriveOffset = 32;
 constexpr int kRoutePassedOffset = 48;
 constexpr int kRouteTcMaxOwn = 16;        // 128-token tiles per CTA of the one-launch router
+constexpr int kSmallT = 16;               // batches up to this size route in one small launch
+constexpr int kSmallMaxE = 256;
 constexpr int kTileCounterOffset = 256;
 constexpr int kMaxTileCounters = (kWsHeaderBytes - kTileCounterOffset) / 4;
 
@@ -65,6 +67,7 @@ struct Plan {
   int nblk;           // routing blocks
   bool router_tc;     // router logits on the tensor cores
   bool route_tc;      // stages 1-4 in one tensor-core launch (bf16, E <= 64, k <= 8)
+  bool route_small;   // stages 1-4 in one launch for decode batches (T <= kSmallT)
   bool router_fused;  // one kernel: logits, top-k, histogram, scan (E <= 256)
   int fu_tm, fu_tn;   // fused router: tokens per thread (1, 2), experts per thread
   int sc_tn;          // router GEMM: experts per thread (2 or 4)
@@ -123,6 +126,12 @@ cudaError_t launch_route_tc(const Plan& p, const void* x, const void* W_r,
                             float* topk_w, int32_t* slot_pos, void* ws, const ScanOutputs& so,
                             cudaStream_t st);
 cudaError_t launch_gather_rows(const Plan& p, const void* x, void* ws, cudaStream_t st);
+size_t route_small_smem(int E);
+int route_small_splits(int d);
+cudaError_t launch_route_small(const Plan& p, const void* x, const void* W_r,
+                               const float* logit_offset, const float* sel_bias,
+                               int32_t* topk_idx, float* topk_w, int32_t* slot_pos, bool copy_rows,
+                               void* ws, const ScanOutputs& so, cudaStream_t st);
 cudaError_t launch_router_tc(const Plan& p, const void* x, const void* W_r,
                              const float* logit_offset, float* scores, uint32_t* status,
                              cudaStream_t st);

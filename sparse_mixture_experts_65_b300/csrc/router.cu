@@ -435,6 +435,228 @@ __global__ void __launch_bounds__(kTopkThreads) router_topk_kernel(const TopkArg
   publish_and_scan<kTopkThreads, NPL>(a.scan, psum, sm.t.Pw, sm.t.cnt, sm.scan, &am_last);
 }
 
+// ---------------------------------------------------------------- small batches
+// Decode-sized batches (T <= kSmallT): stages 1-4 in one launch.  Block s takes
+// the 128-wide slice s of the model width and writes float32 partial logits
+// for every token and expert (x and W_r staged in shared memory as float32,
+// 128 sequential FMAs per output); the last block to finish adds the partials
+// in slice order (plus the offset), routes one token per warp, runs the
+// capacity scan of the single routing block, ranks the keys in key order and
+// writes positions, rows, the row -> token map and the expert-ordered copies.
+constexpr int kSmallThreads = 512;
+constexpr int kSmallKs = 128;
+
+struct SmallArgs {
+  const void* x;
+  const void* W_r;
+  const float* logit_offset;
+  const float* sel_bias;
+  int32_t* topk_idx;
+  float* topk_w;
+  int32_t* slot_pos;
+  float* part;      // [S][T][E]
+  int* key_row;     // [T*k]
+  int* row_token;   // [R_cap]
+  void* xp;         // [R_cap][d] or null (no copy)
+  int T, d, E, k, gate, capacity, S, nvec, elem;
+  ScanArgs scan;
+};
+
+template <typename TIn>
+__device__ __forceinline__ void load_row_f32(const TIn* src, int n, float* dst) {
+  for (int i = 0; i < n; ++i) dst[i] = to_float(src[i]);
+}
+
+template <typename TIn, int NPL>
+__global__ void __launch_bounds__(kSmallThreads) route_small_kernel(const SmallArgs a) {
+  extern __shared__ __align__(16) uint8_t sm_raw[];
+  __shared__ int am_last;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int E = a.E, T = a.T;
+  const int Ep = E + 1;   // padded row of the transposed weight slice
+  pdl_wait();
+  pdl_trigger();
+  {
+    // ---- partial logits of slice s ----
+    float* xs = reinterpret_cast<float*>(sm_raw);        // [T][Ks]
+    float* ws = xs + kSmallT * kSmallKs;                 // [Ks][Ep]
+    const int s = blockIdx.x;
+    const int k0 = s * kSmallKs, kn = min(kSmallKs, a.d - k0);
+    const TIn* X = static_cast<const TIn*>(a.x);
+    const TIn* Wr = static_cast<const TIn*>(a.W_r);
+    for (int i = tid; i < T * kSmallKs; i += kSmallThreads) {
+      const int t = i / kSmallKs, kk = i - t * kSmallKs;
+      xs[i] = kk < kn ? to_float(X[(size_t)t * a.d + k0 + kk]) : 0.f;
+    }
+    for (int i = tid; i < E * kSmallKs; i += kSmallThreads) {
+      const int e = i / kSmallKs, kk = i - e * kSmallKs;
+      ws[kk * Ep + e] = kk < kn ? to_float(Wr[(size_t)e * a.d + k0 + kk]) : 0.f;
+    }
+    __syncthreads();
+    for (int i = tid; i < T * E; i += kSmallThreads) {
+      const int t = i / E, e = i - t * E;
+      const float* xr = xs + t * kSmallKs;
+      float acc = 0.f;
+#pragma unroll 8
+      for (int kk = 0; kk < kSmallKs; ++kk) acc = fmaf(xr[kk], ws[kk * Ep + e], acc);
+      a.part[((size_t)s * T + t) * E + e] = acc;
+    }
+  }
+  __threadfence();
+  __syncthreads();
+  if (tid == 0) am_last = atomicAdd(a.scan.done_counter, 1u) == (unsigned)a.S - 1u;
+  __syncthreads();
+  if (!am_last) return;
+  __threadfence();
+  // ---- the last block: logits, routing, scan, positions, copies ----
+  float* lg = reinterpret_cast<float*>(sm_raw);                       // [T][E]
+  float* Pw = lg + kSmallT * kMaxE;                                   // [16 warps][E]
+  int* cnt = reinterpret_cast<int*>(Pw + (kSmallThreads / 32) * kMaxE);   // [E]
+  int* row_s = cnt + kMaxE;                                           // [T*k]
+  ScanSmem<kSmallThreads>& scan_sm =
+      *reinterpret_cast<ScanSmem<kSmallThreads>*>(row_s + kSmallT * kMaxK);
+  for (int i = tid; i < T * E; i += kSmallThreads) {
+    const int t = i / E, e = i - t * E;
+    float l = 0.f;
+    for (int s = 0; s < a.S; ++s) l += __ldcg(a.part + ((size_t)s * T + t) * E + e);
+    lg[t * E + e] = l + (a.logit_offset ? a.logit_offset[e] : 0.f);
+  }
+  for (int e = tid; e < E; e += kSmallThreads) cnt[e] = 0;
+  __syncthreads();
+  float psum[NPL];
+#pragma unroll
+  for (int i = 0; i < NPL; ++i) psum[i] = 0.f;
+  for (int t = warp; t < T; t += kSmallThreads / 32) {
+    float sv[NPL];
+#pragma unroll
+    for (int i = 0; i < NPL; ++i) {
+      const int e = lane + 32 * i;
+      sv[i] = e < E ? lg[t * E + e] : -INFINITY;
+    }
+    route_one_token<NPL>(sv, E, a.k, a.gate, a.sel_bias, a.topk_idx + (size_t)t * a.k,
+                         a.topk_w + (size_t)t * a.k, cnt, psum);
+  }
+#pragma unroll
+  for (int i = 0; i < NPL; ++i)
+    if (lane + 32 * i < E) Pw[warp * E + lane + 32 * i] = psum[i];
+  __syncthreads();
+  for (int e = tid; e < E; e += kSmallThreads) {
+    float p = 0.f;
+    for (int w = 0; w < kSmallThreads / 32; ++w) p += Pw[w * E + e];
+    a.scan.blk_prob[e] = p;
+    a.scan.blk_cnt[e] = cnt[e];
+    cnt[e] = 0;
+  }
+  __threadfence();
+  __syncthreads();
+  scan_block<kSmallThreads>(a.scan, scan_sm);
+  __threadfence();
+  __syncthreads();
+  if (warp == 0) {
+    // ranks in key order (one routing block: no base), then rows
+    const int nk = T * a.k;
+    for (int c = 0; c < nk; c += 32) {
+      const int q = c + lane;
+      const bool valid = q < nk;
+      const int e = valid ? a.topk_idx[q] : -1 - lane;
+      const unsigned peers = __match_any_sync(0xffffffffu, e);
+      const int before = __popc(peers & ((1u << lane) - 1u));
+      const int prior = valid ? cnt[e] : 0;
+      __syncwarp();
+      if (valid) {
+        const int pos = prior + before;
+        const bool keep = pos < a.capacity;
+        const int row = keep ? __ldcg(a.scan.m.seg_start + e) + pos : -1;
+        a.key_row[q] = row;
+        if (a.slot_pos) a.slot_pos[q] = keep ? __ldcg(a.scan.m.offsets + e) + pos : -1;
+        if (keep) a.row_token[row] = q / a.k;
+        row_s[q] = row;
+        if (before == 0) cnt[e] = prior + __popc(peers);
+      }
+      __syncwarp();
+    }
+  }
+  __syncthreads();
+  if (a.xp) {
+    const uint4* xs = static_cast<const uint4*>(a.x);
+    uint4* xp = static_cast<uint4*>(a.xp);
+    const int total = T * a.k * a.nvec;
+    for (int i = tid; i < total; i += kSmallThreads) {
+      const int q = i / a.nvec, c = i - q * a.nvec;
+      const int row = row_s[q];
+      if (row >= 0) xp[(size_t)row * a.nvec + c] = xs[(size_t)(q / a.k) * a.nvec + c];
+    }
+  }
+  if (tid == 0) *a.scan.done_counter = 0;
+}
+
+size_t route_small_smem(int E) {
+  const size_t p1 = sizeof(float) * ((size_t)kSmallT * kSmallKs + (size_t)kSmallKs * (E + 1));
+  const size_t p2 = sizeof(float) * ((size_t)kSmallT * kMaxE + (kSmallThreads / 32) * kMaxE) +
+                    sizeof(int) * ((size_t)kMaxE + kSmallT * kMaxK) +
+                    sizeof(ScanSmem<kSmallThreads>);
+  return p1 > p2 ? p1 : p2;
+}
+
+int route_small_splits(int d) { return (d + kSmallKs - 1) / kSmallKs; }
+
+template <typename TIn, int NPL>
+static cudaError_t launch_small_t(const SmallArgs& a, size_t smem, cudaStream_t st) {
+  static std::atomic<uint64_t> attr_done{0};
+  auto kern = route_small_kernel<TIn, NPL>;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const uint64_t bit = 1ull << (dev & 63);
+  if (!(attr_done.load(std::memory_order_acquire) & bit)) {
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
+    if (e != cudaSuccess) return e;
+    attr_done.fetch_or(bit, std::memory_order_release);
+  }
+  return launch_pdl(kern, dim3(a.S), dim3(kSmallThreads), smem, st, a);
+}
+
+template <typename TIn>
+static cudaError_t launch_small_npl(const SmallArgs& a, size_t smem, cudaStream_t st) {
+  const int npl = (a.E + 31) / 32;
+  if (npl <= 1) return launch_small_t<TIn, 1>(a, smem, st);
+  if (npl <= 2) return launch_small_t<TIn, 2>(a, smem, st);
+  if (npl <= 4) return launch_small_t<TIn, 4>(a, smem, st);
+  return launch_small_t<TIn, 8>(a, smem, st);
+}
+
+cudaError_t launch_route_small(const Plan& p, const void* x, const void* W_r,
+                               const float* logit_offset, const float* sel_bias,
+                               int32_t* topk_idx, float* topk_w, int32_t* slot_pos, bool copy_rows,
+                               void* ws, const ScanOutputs& so, cudaStream_t st) {
+  char* w = static_cast<char*>(ws);
+  SmallArgs a;
+  a.x = x;
+  a.W_r = W_r;
+  a.logit_offset = logit_offset;
+  a.sel_bias = sel_bias;
+  a.topk_idx = topk_idx;
+  a.topk_w = topk_w;
+  a.slot_pos = slot_pos;
+  a.part = reinterpret_cast<float*>(w + p.ws.score_parts);
+  a.key_row = reinterpret_cast<int*>(w + p.ws.key_row);
+  a.row_token = reinterpret_cast<int*>(w + p.ws.row_token);
+  a.xp = copy_rows ? static_cast<void*>(w + p.ws.xp) : nullptr;
+  a.T = p.cfg.T;
+  a.d = p.cfg.d;
+  a.E = p.cfg.E;
+  a.k = p.cfg.k;
+  a.gate = p.cfg.gate;
+  a.capacity = p.capacity;
+  a.S = route_small_splits(p.cfg.d);
+  a.elem = p.elem;
+  a.nvec = p.cfg.d * p.elem / 16;
+  a.scan = scan_args(p, ws, so);
+  const size_t smem = route_small_smem(p.cfg.E);
+  if (p.cfg.dtype == MOE_BF16) return launch_small_npl<__nv_bfloat16>(a, smem, st);
+  return launch_small_npl<float>(a, smem, st);
+}
+
 // ---------------------------------------------------------------- fused router
 // Fused path (E <= 256): one block computes the float32 logits of BM = 16 TM
 // tokens for all experts over the full model width, keeps them in shared

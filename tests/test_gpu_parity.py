@@ -323,6 +323,28 @@ def test_one_launch_router_layers(shape):
     print(shape.name, rep)
 
 
+DECODE = [
+    LayerShape("small_f32_sigmoid_cap", 50, T=5, d=72, E=6, k=3, f=40, act=SW, gate=SIG,
+               dtype="f32", capacity_factor=0.8, sel_bias_halfwidth=0.05),
+    LayerShape("small_bf16_dsv3_like", 51, T=16, d=256, E=256, k=8, f=64, act=SW, gate=SIG,
+               dtype="bf16", n_shared=1, f_shared=64, sel_bias_halfwidth=0.05),
+    LayerShape("small_bf16_e200_full", 52, T=11, d=200, E=200, k=2, f=96, act=GE, gate=FULL,
+               dtype="bf16", capacity_factor=1.0, logit_offset_var=1.5),
+    LayerShape("small_bf16_top1", 53, T=1, d=640, E=16, k=1, f=128, act=RE, gate=FULL,
+               dtype="bf16"),
+]
+
+
+@pytest.mark.parametrize("shape", DECODE, ids=lambda s: s.name)
+def test_decode_batch_router(shape):
+    """Decode batches (T <= 16) route in one launch: split-K partial logits,
+    the last block's top-k, capacity scan and positions."""
+    inp = W.make_inputs(shape, "cuda", seed=3)
+    _, out = run_gpu(inp)
+    rep = check_layer(inp, out)
+    print(shape.name, rep)
+
+
 @pytest.mark.parametrize("gather", ["0", "1"])
 def test_up_projection_row_source(monkeypatch, gather):
     """Both row sources of the tensor-core up projection on one-launch-routed
