@@ -14,9 +14,11 @@
 // Determinism: the histogram is an integer count, the scans run in a fixed
 // order and every float sum has a fixed association, so repeated calls give
 // bitwise-identical results.
+#include <atomic>
 #include <cfloat>
 #include <climits>
 
+#include "bulk_rows.cuh"
 #include "common.cuh"
 #include "launch.cuh"
 #include "moe_internal.h"
@@ -32,6 +34,7 @@ struct PermuteArgs {
   Meta m;
   void* xp;
   int* row_token;        // [R_cap]: token of each kept row
+  uint32_t* status;
   int T, E, k, BT, capacity, nvec;   // nvec: 16-byte vectors per token row
   int copy;
 };
@@ -43,6 +46,19 @@ struct PermuteArgs {
 // block's base is the key's position; the capacity test and the row follow.
 // Then all warps copy the kept token rows into expert order, one row per warp.
 constexpr int kPermuteThreads = 512;
+constexpr uint32_t kPermuteStage = 128u << 10;   // bulk-copy staging per block
+constexpr uint64_t kPermuteTimeoutNs = 2000000000ull;
+
+// Rows of at least 1 KB (and at most a quarter of the stage) move by bulk
+// copies; shorter rows by 16-byte loads and stores.
+__host__ __device__ inline bool permute_bulk(uint32_t row_bytes) {
+  return row_bytes >= 1024u && row_bytes * kBulkIssuers <= kPermuteStage;
+}
+
+// Shared memory: cnt[E] | row_s[BT*k] | (128-aligned) stage | 4 mbarriers.
+__host__ __device__ inline size_t permute_stage_offset(int E, int keys) {
+  return ((sizeof(int) * ((size_t)E + keys)) + 127) / 128 * 128;
+}
 
 __global__ void __launch_bounds__(kPermuteThreads) permute_kernel(const PermuteArgs a) {
   extern __shared__ int smi[];
@@ -82,6 +98,23 @@ __global__ void __launch_bounds__(kPermuteThreads) permute_kernel(const PermuteA
   }
   __syncthreads();
   if (!a.copy) return;
+  const uint32_t row_bytes = (uint32_t)a.nvec * 16u;
+  if (permute_bulk(row_bytes)) {
+    // bulk row copies through shared memory: many kilobytes in flight per SM
+    uint8_t* stage = reinterpret_cast<uint8_t*>(smi) + permute_stage_offset(a.E, a.BT * a.k);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(stage + kPermuteStage);
+    const char* xs = static_cast<const char*>(a.x);
+    char* xp = static_cast<char*>(a.xp);
+    bulk_copy_rows(
+        nk, row_bytes,
+        [&](int q) { return static_cast<const void*>(xs + (size_t)(t0 + q / a.k) * row_bytes); },
+        [&](int q) {
+          const int row = row_s[q];
+          return row >= 0 ? static_cast<void*>(xp + (size_t)row * row_bytes) : nullptr;
+        },
+        stage, kPermuteStage, bars, a.status, STATUS_TIMEOUT_ROUTE, kPermuteTimeoutNs);
+    return;
+  }
   // Row copies: (key, 16-byte vector) pairs spread over the block, four
   // independent loads in flight per thread before their stores.
   const uint4* xs = static_cast<const uint4*>(a.x);
@@ -113,53 +146,54 @@ __global__ void __launch_bounds__(kPermuteThreads) permute_kernel(const PermuteA
 }
 
 // Copy of the kept token rows into expert order after the one-launch router
-// (key_row is final): grid-stride over (key, 16-byte vector), eight loads in
-// flight per thread.
-constexpr int kGatherThreads = 256;
+// (key_row is final): every block takes a contiguous range of keys and moves
+// the kept rows with bulk copies through shared memory.
+constexpr int kGatherThreads = 32 * kBulkIssuers;
+constexpr uint32_t kGatherStage = 160u << 10;
 
 __global__ void __launch_bounds__(kGatherThreads) gather_rows_kernel(
-    const uint4* x, uint4* xp, const int* key_row, int nkeys, int k, int nvec) {
+    const char* x, char* xp, const int* key_row, int nkeys, int k, uint32_t row_bytes,
+    uint32_t* status) {
+  extern __shared__ __align__(128) uint8_t gsm[];
   pdl_wait();
   pdl_trigger();
-  const long long total = (long long)nkeys * nvec;
-  const long long stride = (long long)gridDim.x * kGatherThreads;
-  constexpr int U = 8;
-  for (long long i0 = (long long)blockIdx.x * kGatherThreads + threadIdx.x; i0 < total;
-       i0 += stride * U) {
-    uint4 v[U];
-    long long dst[U];
-#pragma unroll
-    for (int u = 0; u < U; ++u) {
-      const long long i = i0 + u * stride;
-      dst[u] = -1;
-      if (i < total) {
-        const int q = (int)(i / nvec);
-        const int c = (int)(i - (long long)q * nvec);
-        const int row = key_row[q];
-        if (row >= 0) {
-          v[u] = x[(size_t)(q / k) * nvec + c];
-          dst[u] = (long long)row * nvec + c;
-        }
-      }
-    }
-#pragma unroll
-    for (int u = 0; u < U; ++u)
-      if (dst[u] >= 0) xp[dst[u]] = v[u];
-  }
+  const int per = (nkeys + gridDim.x - 1) / gridDim.x;
+  const int q0 = blockIdx.x * per;
+  const int n = min(per, nkeys - q0);
+  if (n <= 0) return;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(gsm + kGatherStage);
+  bulk_copy_rows(
+      n, row_bytes,
+      [&](int i) { return static_cast<const void*>(x + (size_t)((q0 + i) / k) * row_bytes); },
+      [&](int i) {
+        const int row = __ldg(key_row + q0 + i);
+        return row >= 0 ? static_cast<void*>(xp + (size_t)row * row_bytes) : nullptr;
+      },
+      gsm, kGatherStage, bars, status, STATUS_TIMEOUT_ROUTE, 2000000000ull);
 }
 
 cudaError_t launch_gather_rows(const Plan& p, const void* x, void* ws, cudaStream_t st) {
   char* w = static_cast<char*>(ws);
   const int nkeys = p.cfg.T * p.cfg.k;
-  const int nvec = p.cfg.d * p.elem / 16;
-  const long long total = (long long)nkeys * nvec;
-  long long blocks = (total + kGatherThreads * 8 - 1) / (kGatherThreads * 8);
-  const long long cap = 8LL * p.num_sms;
-  if (blocks > cap) blocks = cap;
-  if (blocks < 1) blocks = 1;
-  return launch_pdl(gather_rows_kernel, dim3((unsigned)blocks), dim3(kGatherThreads), 0, st,
-                    static_cast<const uint4*>(x), reinterpret_cast<uint4*>(w + p.ws.xp),
-                    reinterpret_cast<const int*>(w + p.ws.key_row), nkeys, p.cfg.k, nvec);
+  const uint32_t row_bytes = (uint32_t)p.cfg.d * p.elem;
+  static std::atomic<uint64_t> attr_done{0};
+  const size_t smem = kGatherStage + 8 * kBulkIssuers;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const uint64_t bit = 1ull << (dev & 63);
+  if (!(attr_done.load(std::memory_order_acquire) & bit)) {
+    e = cudaFuncSetAttribute(gather_rows_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)smem);
+    if (e != cudaSuccess) return e;
+    attr_done.fetch_or(bit, std::memory_order_release);
+  }
+  int blocks = p.num_sms;
+  if (blocks > nkeys) blocks = nkeys > 0 ? nkeys : 1;
+  return launch_pdl(gather_rows_kernel, dim3(blocks), dim3(kGatherThreads), smem, st,
+                    static_cast<const char*>(x), w + p.ws.xp,
+                    reinterpret_cast<const int*>(w + p.ws.key_row), nkeys, p.cfg.k, row_bytes,
+                    reinterpret_cast<uint32_t*>(w + p.ws.status));
 }
 
 Meta meta_ptrs(const Plan& p, void* ws) {
@@ -195,7 +229,25 @@ cudaError_t launch_permute(const Plan& p, const void* x, const int32_t* topk_idx
   a.capacity = p.capacity;
   a.nvec = p.cfg.d * p.elem / 16;
   a.copy = copy_rows ? 1 : 0;
-  const size_t smem = sizeof(int) * ((size_t)p.cfg.E + (size_t)p.BT * p.cfg.k);
+  a.status = reinterpret_cast<uint32_t*>(static_cast<char*>(ws) + p.ws.status);
+  const bool bulk = copy_rows && permute_bulk((uint32_t)a.nvec * 16u);
+  const size_t ints = sizeof(int) * ((size_t)p.cfg.E + (size_t)p.BT * p.cfg.k);
+  const size_t smem =
+      bulk ? permute_stage_offset(p.cfg.E, p.BT * p.cfg.k) + kPermuteStage + 8 * kBulkIssuers
+           : ints;
+  if (bulk) {
+    static std::atomic<uint64_t> attr_done{0};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    const uint64_t bit = 1ull << (dev & 63);
+    if (!(attr_done.load(std::memory_order_acquire) & bit)) {
+      e = cudaFuncSetAttribute(permute_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               200 * 1024);
+      if (e != cudaSuccess) return e;
+      attr_done.fetch_or(bit, std::memory_order_release);
+    }
+  }
   return launch_pdl(permute_kernel, dim3(p.nblk), dim3(kPermuteThreads), smem, st, a);
 }
 
