@@ -28,6 +28,7 @@
 #include <cstring>
 #include <mutex>
 
+#include "bulk_rows.cuh"
 #include "common.cuh"
 #include "launch.cuh"
 #include "moe_internal.h"
@@ -445,6 +446,7 @@ __global__ void __launch_bounds__(kTopkThreads) router_topk_kernel(const TopkArg
 // writes positions, rows, the row -> token map and the expert-ordered copies.
 constexpr int kSmallThreads = 512;
 constexpr int kSmallKs = 128;
+constexpr uint32_t kSmallStage = 96u << 10;   // bulk-copy staging of the last block
 
 struct SmallArgs {
   const void* x;
@@ -459,6 +461,7 @@ struct SmallArgs {
   int* row_token;   // [R_cap]
   void* xp;         // [R_cap][d] or null (no copy)
   int T, d, E, k, gate, capacity, S, nvec, elem;
+  uint32_t* status;
   ScanArgs scan;
 };
 
@@ -484,22 +487,58 @@ __global__ void __launch_bounds__(kSmallThreads) route_small_kernel(const SmallA
     const int k0 = s * kSmallKs, kn = min(kSmallKs, a.d - k0);
     const TIn* X = static_cast<const TIn*>(a.x);
     const TIn* Wr = static_cast<const TIn*>(a.W_r);
-    for (int i = tid; i < T * kSmallKs; i += kSmallThreads) {
-      const int t = i / kSmallKs, kk = i - t * kSmallKs;
-      xs[i] = kk < kn ? to_float(X[(size_t)t * a.d + k0 + kk]) : 0.f;
+    // 16-byte loads (the slice width and d are multiples of the vector)
+    constexpr int V = 16 / (int)sizeof(TIn);
+    constexpr int NV = kSmallKs / V;
+    for (int i = tid; i < T * NV; i += kSmallThreads) {
+      const int t = i / NV, kk = (i - t * NV) * V;
+      float v[8];
+      if (kk < kn) {
+        to_float8(*reinterpret_cast<const uint4*>(X + (size_t)t * a.d + k0 + kk), X, v);
+      } else {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) v[j] = 0.f;
+      }
+#pragma unroll
+      for (int j = 0; j < V; ++j) xs[t * kSmallKs + kk + j] = v[j];
     }
-    for (int i = tid; i < E * kSmallKs; i += kSmallThreads) {
-      const int e = i / kSmallKs, kk = i - e * kSmallKs;
-      ws[kk * Ep + e] = kk < kn ? to_float(Wr[(size_t)e * a.d + k0 + kk]) : 0.f;
+    for (int i = tid; i < E * NV; i += kSmallThreads) {
+      const int e = i / NV, kk = (i - e * NV) * V;
+      float v[8];
+      if (kk < kn) {
+        to_float8(*reinterpret_cast<const uint4*>(Wr + (size_t)e * a.d + k0 + kk), Wr, v);
+      } else {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) v[j] = 0.f;
+      }
+#pragma unroll
+      for (int j = 0; j < V; ++j) ws[(kk + j) * Ep + e] = v[j];
     }
     __syncthreads();
-    for (int i = tid; i < T * E; i += kSmallThreads) {
-      const int t = i / E, e = i - t * E;
-      const float* xr = xs + t * kSmallKs;
-      float acc = 0.f;
-#pragma unroll 8
-      for (int kk = 0; kk < kSmallKs; ++kk) acc = fmaf(xr[kk], ws[kk * Ep + e], acc);
-      a.part[((size_t)s * T + t) * E + e] = acc;
+    // thread (expert e, group of 4 tokens): a weight value is loaded once for
+    // the 4 tokens, the x values 4 k at a time (16-byte loads); every output
+    // still sums its 128 products in k order
+    const int ngrp = (T + 3) / 4;
+    for (int i = tid; i < E * ngrp; i += kSmallThreads) {
+      const int e = i % E, t0 = (i / E) * 4;
+      float acc[4] = {0.f, 0.f, 0.f, 0.f};
+      for (int kk = 0; kk < kSmallKs; kk += 4) {
+        const float w0 = ws[kk * Ep + e], w1 = ws[(kk + 1) * Ep + e];
+        const float w2 = ws[(kk + 2) * Ep + e], w3 = ws[(kk + 3) * Ep + e];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          if (t0 + j < T) {
+            const float4 x4 = *reinterpret_cast<const float4*>(xs + (t0 + j) * kSmallKs + kk);
+            acc[j] = fmaf(x4.x, w0, acc[j]);
+            acc[j] = fmaf(x4.y, w1, acc[j]);
+            acc[j] = fmaf(x4.z, w2, acc[j]);
+            acc[j] = fmaf(x4.w, w3, acc[j]);
+          }
+        }
+      }
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        if (t0 + j < T) a.part[((size_t)s * T + t0 + j) * E + e] = acc[j];
     }
   }
   __threadfence();
@@ -515,10 +554,36 @@ __global__ void __launch_bounds__(kSmallThreads) route_small_kernel(const SmallA
   int* row_s = cnt + kMaxE;                                           // [T*k]
   ScanSmem<kSmallThreads>& scan_sm =
       *reinterpret_cast<ScanSmem<kSmallThreads>*>(row_s + kSmallT * kMaxK);
+  uint8_t* stage = reinterpret_cast<uint8_t*>(&scan_sm + 1);
+  stage = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(stage) + 127) & ~uintptr_t(127));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(stage + kSmallStage);
+  const uint32_t row_bytes = (uint32_t)a.nvec * 16u;
+  // When all T token rows fit the stage, they are loaded now, while the
+  // logits, routing and scan run, and later stored straight to their rows.
+  const bool stage_x = a.xp != nullptr && (size_t)T * row_bytes <= kSmallStage;
+  uint64_t* xbar = bars + kBulkIssuers;
+  if (stage_x && tid == 0) {
+    mbar_init(smem_u32(xbar), 1);
+    fence_mbar_init();
+    mbar_arrive_expect_tx(smem_u32(xbar), (uint32_t)T * row_bytes);
+    for (int t = 0; t < T; ++t)
+      bulk_load(smem_u32(stage) + t * row_bytes, static_cast<const char*>(a.x) + (size_t)t * row_bytes,
+                row_bytes, smem_u32(xbar));
+  }
   for (int i = tid; i < T * E; i += kSmallThreads) {
     const int t = i / E, e = i - t * E;
+    const float* pp = a.part + (size_t)t * E + e;
+    const size_t ss = (size_t)T * E;   // slice stride
     float l = 0.f;
-    for (int s = 0; s < a.S; ++s) l += __ldcg(a.part + ((size_t)s * T + t) * E + e);
+    // up to 32 loads in flight, added in slice order
+    for (int s0 = 0; s0 < a.S; s0 += 32) {
+      float v[32];
+#pragma unroll
+      for (int u = 0; u < 32; ++u) v[u] = s0 + u < a.S ? __ldcg(pp + (size_t)(s0 + u) * ss) : 0.f;
+#pragma unroll
+      for (int u = 0; u < 32; ++u)
+        if (s0 + u < a.S) l += v[u];
+    }
     lg[t * E + e] = l + (a.logit_offset ? a.logit_offset[e] : 0.f);
   }
   for (int e = tid; e < E; e += kSmallThreads) cnt[e] = 0;
@@ -540,17 +605,67 @@ __global__ void __launch_bounds__(kSmallThreads) route_small_kernel(const SmallA
   for (int i = 0; i < NPL; ++i)
     if (lane + 32 * i < E) Pw[warp * E + lane + 32 * i] = psum[i];
   __syncthreads();
-  for (int e = tid; e < E; e += kSmallThreads) {
-    float p = 0.f;
-    for (int w = 0; w < kSmallThreads / 32; ++w) p += Pw[w * E + e];
-    a.scan.blk_prob[e] = p;
-    a.scan.blk_cnt[e] = cnt[e];
-    cnt[e] = 0;
+  // capacity scan of the single routing block: its histogram is the total
+  {
+    const ScanArgs& sa = a.scan;
+    int* seg_s = scan_sm.routed_s;      // first row of each expert's segment
+    int* off_s = reinterpret_cast<int*>(scan_sm.psum_s);   // first slot of each expert
+    const int e = tid;
+    int routed = 0, kept = 0, mt = 0;
+    float P = 0.f, fr = 0.f;
+    if (e < E) {
+      float pe = 0.f;
+      for (int w = 0; w < kSmallThreads / 32; ++w) pe += Pw[w * E + e];
+      routed = cnt[e];
+      kept = routed < a.capacity ? routed : a.capacity;
+      mt = (kept + sa.bm - 1) / sa.bm;
+      P = pe / (float)T;
+      fr = (float)routed / (float)(T * a.k);
+    }
+    int4 tot;
+    const int4 ex = block_exscan4<kSmallThreads>(
+        make_int4(kept, mt, mt * sa.nt_up, mt * sa.nt_dn), scan_sm.scratch, &tot);
+    if (e < E) {
+      seg_s[e] = ex.y * sa.bm;
+      off_s[e] = ex.x;
+      cnt[e] = 0;
+      sa.m.kept[e] = kept;
+      sa.m.offsets[e] = ex.x;
+      sa.m.seg_start[e] = ex.y * sa.bm;
+      sa.m.mtiles[e] = mt;
+      sa.m.tp_up[e] = ex.z;
+      sa.m.tp_dn[e] = ex.w;
+      sa.expert_counts[e] = kept;
+      if (sa.routed_counts) sa.routed_counts[e] = routed;
+      if (sa.offsets_out) sa.offsets_out[e] = ex.x;
+      if (sa.f_out) sa.f_out[e] = fr;
+      if (sa.P_out) sa.P_out[e] = P;
+    }
+    if (tid == 0) {
+      const int sh_up = sa.has_shared ? sa.mt_sh * sa.nt_up_sh : 0;
+      const int sh_dn = sa.has_shared ? sa.mt_sh * sa.nt_dn_sh : 0;
+      sa.m.offsets[E] = tot.x;
+      sa.m.seg_start[E] = tot.y * sa.bm;
+      sa.m.mtiles[E] = sa.has_shared ? sa.mt_sh : 0;
+      sa.m.tp_up[E] = tot.z;
+      sa.m.tp_up[E + 1] = tot.z + sh_up;
+      sa.m.tp_dn[E] = tot.w;
+      sa.m.tp_dn[E + 1] = tot.w + sh_dn;
+      if (sa.offsets_out) sa.offsets_out[E] = tot.x;
+    }
+    // L = alpha * E * sum_i f_i P_i in double: a fixed butterfly inside each
+    // warp, then the warp sums in warp order
+    double l = e < E ? (double)fr * (double)P : 0.0;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) l += __shfl_xor_sync(0xffffffffu, l, o);
+    if (lane == 0) scan_sm.red[warp] = l;
+    __syncthreads();
+    if (tid == 0) {
+      double t = 0.0;
+      for (int w = 0; w < kSmallThreads / 32; ++w) t += scan_sm.red[w];
+      sa.aux_loss[0] = (float)((double)sa.alpha * (double)E * t);
+    }
   }
-  __threadfence();
-  __syncthreads();
-  scan_block<kSmallThreads>(a.scan, scan_sm);
-  __threadfence();
   __syncthreads();
   if (warp == 0) {
     // ranks in key order (one routing block: no base), then rows
@@ -566,9 +681,10 @@ __global__ void __launch_bounds__(kSmallThreads) route_small_kernel(const SmallA
       if (valid) {
         const int pos = prior + before;
         const bool keep = pos < a.capacity;
-        const int row = keep ? __ldcg(a.scan.m.seg_start + e) + pos : -1;
+        const int row = keep ? scan_sm.routed_s[e] + pos : -1;
         a.key_row[q] = row;
-        if (a.slot_pos) a.slot_pos[q] = keep ? __ldcg(a.scan.m.offsets + e) + pos : -1;
+        if (a.slot_pos)
+          a.slot_pos[q] = keep ? reinterpret_cast<const int*>(scan_sm.psum_s)[e] + pos : -1;
         if (keep) a.row_token[row] = q / a.k;
         row_s[q] = row;
         if (before == 0) cnt[e] = prior + __popc(peers);
@@ -577,24 +693,44 @@ __global__ void __launch_bounds__(kSmallThreads) route_small_kernel(const SmallA
     }
   }
   __syncthreads();
-  if (a.xp) {
-    const uint4* xs = static_cast<const uint4*>(a.x);
-    uint4* xp = static_cast<uint4*>(a.xp);
-    const int total = T * a.k * a.nvec;
-    for (int i = tid; i < total; i += kSmallThreads) {
-      const int q = i / a.nvec, c = i - q * a.nvec;
-      const int row = row_s[q];
-      if (row >= 0) xp[(size_t)row * a.nvec + c] = xs[(size_t)(q / a.k) * a.nvec + c];
-    }
-  }
   if (tid == 0) *a.scan.done_counter = 0;
+  if (stage_x) {
+    // every kept key's token row from the staged copy of x, four issuers
+    if (warp < kBulkIssuers && lane == 0) {
+      if (!mbar_wait_bounded(smem_u32(xbar), 0, 2000000000ull, nullptr)) {
+        atomicOr(a.status, STATUS_TIMEOUT_ROUTE);
+      } else {
+        char* xp = static_cast<char*>(a.xp);
+        for (int q = warp; q < T * a.k; q += kBulkIssuers) {
+          const int row = row_s[q];
+          if (row >= 0)
+            bulk_store(xp + (size_t)row * row_bytes, smem_u32(stage) + (q / a.k) * row_bytes,
+                       row_bytes);
+        }
+        bulk_commit();
+        bulk_wait_all();
+      }
+    }
+  } else if (a.xp) {
+    // the kept rows into expert order: bulk copies through shared memory
+    const char* xs = static_cast<const char*>(a.x);
+    char* xp = static_cast<char*>(a.xp);
+    bulk_copy_rows(
+        T * a.k, row_bytes,
+        [&](int q) { return static_cast<const void*>(xs + (size_t)(q / a.k) * row_bytes); },
+        [&](int q) {
+          const int row = row_s[q];
+          return row >= 0 ? static_cast<void*>(xp + (size_t)row * row_bytes) : nullptr;
+        },
+        stage, kSmallStage, bars, a.status, STATUS_TIMEOUT_ROUTE, 2000000000ull);
+  }
 }
 
 size_t route_small_smem(int E) {
   const size_t p1 = sizeof(float) * ((size_t)kSmallT * kSmallKs + (size_t)kSmallKs * (E + 1));
   const size_t p2 = sizeof(float) * ((size_t)kSmallT * kMaxE + (kSmallThreads / 32) * kMaxE) +
                     sizeof(int) * ((size_t)kMaxE + kSmallT * kMaxK) +
-                    sizeof(ScanSmem<kSmallThreads>);
+                    sizeof(ScanSmem<kSmallThreads>) + 128 + kSmallStage + 8 * (kBulkIssuers + 1);
   return p1 > p2 ? p1 : p2;
 }
 
@@ -651,6 +787,7 @@ cudaError_t launch_route_small(const Plan& p, const void* x, const void* W_r,
   a.S = route_small_splits(p.cfg.d);
   a.elem = p.elem;
   a.nvec = p.cfg.d * p.elem / 16;
+  a.status = reinterpret_cast<uint32_t*>(w + p.ws.status);
   a.scan = scan_args(p, ws, so);
   const size_t smem = route_small_smem(p.cfg.E);
   if (p.cfg.dtype == MOE_BF16) return launch_small_npl<__nv_bfloat16>(a, smem, st);
