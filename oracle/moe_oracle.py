@@ -16,7 +16,8 @@ Sources (page title, then section):
   [MoE-ch11]   "Mixture of Experts" (llm-tutorial, chapter 11):
                § The mathematics; § Top-k routing: the gating function;
                § Top-1 vs top-2; § The auxiliary loss; § Expert capacity and
-               dropped tokens; § Why MoE is hard (router precision); § Exercises.
+               dropped tokens; § Why MoE is hard (router precision, router
+               z-loss); § Exercises.
   [MoE-guide]  "Mixture of experts" (inside-the-model guide, chapter 14):
                § The computation; § Auxiliary loss; § Fine-grained and shared
                experts; § Auxiliary-loss-free balancing; § Check yourself.
@@ -38,7 +39,12 @@ with its reason, in the design notes of the repository):
   * the shared expert is a SwiGLU expert added with weight 1, outside f/P and
     outside capacity;
   * a dropped slot contributes zero and the remaining gates are not
-    renormalised; y is the MoE branch only (the caller adds the residual).
+    renormalised; y is the MoE branch only (the caller adds the residual);
+  * router z-loss: the ST-MoE form, mean over tokens of logsumexp(s_t)^2
+    (the pages give no formula, so this function is pinned only to that
+    reading: closed forms and a library logsumexp);
+  * bias balancing step: load = routed count, overloaded iff
+    routed_i * E > T * k, underloaded iff below, float32 state.
 
 Parity pins: every function below is pinned by ``tests/test_oracle_pins.py``
 (brute force, closed forms, library special cases and page numbers under
@@ -340,6 +346,51 @@ def balance_stats(routed, probs, T: int, k: int, alpha: float):
     P = probs.sum(axis=0) / float(T)
     L = float(alpha) * E * float(np.sum(f * P))
     return f, P, L
+
+
+# [MoE-ch11] § Why MoE is hard: the router z-loss (from ST-MoE) penalises
+# large router logits so that the softmax stays well conditioned.  The pages
+# name it and its purpose but print no formula; the reading taken is the
+# ST-MoE form, the batch mean of the squared log-partition function of each
+# token's logits, without its coefficient:  z = (1/T) sum_t (log sum_e
+# exp s_te)^2.  The logits are those the layer routes with (offset included).
+# --------------------------------------------------------------------------
+def router_z_loss(s) -> float:
+    """z = mean over tokens of logsumexp(s_t)^2, in float64 with the row
+    maximum taken out before the exponentials.  T = 0 gives 0."""
+    s = _f64(s)
+    T = s.shape[0]
+    if T == 0:
+        return 0.0
+    z = 0.0
+    for t in range(T):
+        m = float(np.max(s[t]))
+        lse = m + math.log(float(np.sum(np.exp(s[t] - m))))
+        z += lse * lse
+    return z / T
+
+
+# [MoE-guide] § Auxiliary-loss-free balancing: every expert keeps a bias that
+# only steers the choice; after each step it goes down by a small gamma for an
+# overloaded expert and up by gamma for an underloaded one.  Readings (the
+# pages fix neither): the load of expert i is its routed (pre-drop) count,
+# "overloaded" means above the mean load T*k/E and "underloaded" below it,
+# compared exactly as routed_i * E against T * k; an expert at the mean keeps
+# its bias.  The bias is float32 state and each step is one float32 add.
+# --------------------------------------------------------------------------
+def bias_update(sel_bias, routed, T: int, k: int, gamma: float) -> np.ndarray:
+    """The biases after one balancing step (float32 [E])."""
+    b = np.array(sel_bias, dtype=np.float32, copy=True).reshape(-1)
+    E = b.shape[0]
+    g = np.float32(gamma)
+    mean_scaled = int(T) * int(k)
+    for i in range(E):
+        load_scaled = int(routed[i]) * E
+        if load_scaled > mean_scaled:
+            b[i] = np.float32(b[i] - g)
+        elif load_scaled < mean_scaled:
+            b[i] = np.float32(b[i] + g)
+    return b
 
 
 class _Indexable:

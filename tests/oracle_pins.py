@@ -421,11 +421,67 @@ def check_pipeline_stats_pre_drop():
     np.testing.assert_allclose(r.P.sum(), 1.0, rtol=1e-14)
 
 
+# ---------------------------------------------------------------- next rows
+def check_z_loss_closed_forms():
+    """Router z-loss, pinned to its reading (mean over tokens of the squared
+    log-partition function): constant logits c give (c + ln E)^2; E = 1 gives
+    the mean square of the logits; two experts give logaddexp; random rows
+    agree with scipy's logsumexp; a per-token shift moves each term."""
+    from scipy.special import logsumexp
+    for E, c in ((1, 0.7), (4, 0.0), (64, -2.5), (256, 3.0)):
+        s = np.full((5, E), c)
+        assert abs(O.router_z_loss(s) - (c + math.log(E)) ** 2) < 1e-12 * max(1.0, (c + math.log(E)) ** 2)
+    v = _rng(70).normal(size=(9, 1))
+    assert abs(O.router_z_loss(v) - float(np.mean(v[:, 0] ** 2))) < 1e-14
+    ab = _rng(71).normal(size=(7, 2)) * 4
+    lse2 = np.logaddexp(ab[:, 0], ab[:, 1])
+    assert abs(O.router_z_loss(ab) - float(np.mean(lse2 ** 2))) < 1e-13
+    s = _rng(72).normal(size=(33, 17)) * 3
+    ref = float(np.mean(logsumexp(s, axis=1) ** 2))
+    assert abs(O.router_z_loss(s) - ref) < 1e-12 * ref
+    shift = _rng(73).normal(size=(33, 1)) * 10
+    ref_shift = float(np.mean((logsumexp(s, axis=1) + shift[:, 0]) ** 2))
+    assert abs(O.router_z_loss(s + shift) - ref_shift) < 1e-12 * ref_shift
+    # huge logits stay finite (the maximum is taken out first)
+    big = np.array([[1000.0, 999.0, -1000.0]])
+    assert abs(O.router_z_loss(big) - (1000.0 + math.log1p(math.exp(-1.0))) ** 2) < 1e-9
+    assert O.router_z_loss(np.zeros((0, 8))) == 0.0
+
+
+def check_bias_update_rule():
+    """One balancing step of the per-expert selection bias (the guide's
+    auxiliary-loss-free balancing): down by gamma above the mean load, up by
+    gamma below it, unchanged at the mean; float32 state."""
+    g = 0.25
+    # T = 8, k = 1, E = 4: mean load 2
+    np.testing.assert_array_equal(O.bias_update([0, 0, 0, 0], [5, 2, 1, 0], 8, 1, g),
+                                  np.array([-0.25, 0.0, 0.25, 0.25], dtype=np.float32))
+    # non-integer mean 4/3 (T = 4, k = 1, E = 3): nobody sits at the mean
+    np.testing.assert_array_equal(O.bias_update([1, 1, 1], [2, 1, 1], 4, 1, g),
+                                  np.array([0.75, 1.25, 1.25], dtype=np.float32))
+    # k = 2 doubles the mean (T = 6, E = 4: mean 3)
+    np.testing.assert_array_equal(O.bias_update([0, 0, 0, 0], [3, 4, 2, 3], 6, 2, g),
+                                  np.array([0.0, -0.25, 0.25, 0.0], dtype=np.float32))
+    # balanced loads keep every bias
+    b0 = _rng(74).uniform(-0.05, 0.05, size=16).astype(np.float32)
+    np.testing.assert_array_equal(O.bias_update(b0, [10] * 16, 40, 4, 1e-3), b0)
+    # a collapsed router: n steps move the favourite down by n*gamma and the
+    # rest up by n*gamma (exact in binary for gamma = 2^-6)
+    b = np.zeros(8, dtype=np.float32)
+    for _ in range(5):
+        b = O.bias_update(b, [64, 0, 0, 0, 0, 0, 0, 0], 64, 1, 2.0 ** -6)
+    np.testing.assert_array_equal(b, np.array([-5 / 64] + [5 / 64] * 7, dtype=np.float32))
+    # float32 state: a step below half an ulp of 1.0 leaves 1.0
+    assert O.bias_update([1.0, 1.0], [2, 0], 2, 1, 1e-8)[0] == np.float32(1.0)
+    out = O.bias_update([0.1], [1], 2, 1, 0.3)   # E = 1, load 1 < mean 2
+    assert out.dtype == np.float32 and out[0] == np.float32(np.float32(0.1) + np.float32(0.3))
+
+
 ALL_CHECKS = [
     check_router_onehot, check_topk_bruteforce, check_topk_ties, check_gates_closed_form,
     check_gates_invariants, check_router_probs, check_selection_bias,
     check_capacity_formula, check_capacity_drops, check_offsets_and_permutation,
     check_sparse_equals_dense, check_drop_is_identity_branch, check_dense_ffn_special_case,
     check_multiply_counts, check_balance_uniform, check_balance_hand_and_collapse,
-    check_pipeline_stats_pre_drop,
+    check_pipeline_stats_pre_drop, check_z_loss_closed_forms, check_bias_update_rule,
 ]

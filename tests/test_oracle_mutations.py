@@ -16,7 +16,7 @@ import oracle_pins as P
 _orig = {name: getattr(M, name) for name in (
     "router_logits", "topk_indices", "gate_values", "affinity", "expert_capacity",
     "assign_slots", "gelu_erf", "silu", "expert_ffn_rows", "balance_stats", "router_probs",
-    "softmax_rows")}
+    "softmax_rows", "router_z_loss", "bias_update")}
 
 
 def _router_reversed(x, W_r, logit_offset=None):
@@ -123,6 +123,41 @@ def _softmax_no_shift_bug(z):
     return np.exp(z) / np.exp(z).sum(axis=-1, keepdims=True) * 1.0000001
 
 
+def _z_no_square(s):
+    s = np.asarray(s, dtype=float)
+    if s.shape[0] == 0:
+        return 0.0
+    m = s.max(axis=1)
+    return float(np.mean(m + np.log(np.exp(s - m[:, None]).sum(axis=1))))
+
+
+def _z_no_max_term(s):
+    s = np.asarray(s, dtype=float)
+    if s.shape[0] == 0:
+        return 0.0
+    m = s.max(axis=1)
+    return float(np.mean(np.log(np.exp(s - m[:, None]).sum(axis=1)) ** 2))
+
+
+def _bias_sign_flipped(sel_bias, routed, T, k, gamma):
+    return _orig["bias_update"](sel_bias, routed, T, k, -gamma)
+
+
+def _bias_mean_ignores_k(sel_bias, routed, T, k, gamma):
+    return _orig["bias_update"](sel_bias, routed, T, 1, gamma)
+
+
+def _bias_float64_state(sel_bias, routed, T, k, gamma):
+    b = np.array(sel_bias, dtype=np.float64)
+    E = b.shape[0]
+    for i in range(E):
+        if routed[i] * E > T * k:
+            b[i] -= gamma
+        elif routed[i] * E < T * k:
+            b[i] += gamma
+    return b
+
+
 MUTATIONS = [
     ("router expert order reversed", "router_logits", _router_reversed, P.check_router_onehot),
     ("router offset sign flipped", "router_logits", _router_offset_sign, P.check_router_onehot),
@@ -143,6 +178,11 @@ MUTATIONS = [
     ("loss misses the factor N", "balance_stats", _balance_no_E, P.check_balance_uniform),
     ("sigmoid P not normalised", "router_probs", _probs_unnormalised_sigmoid, P.check_router_probs),
     ("softmax scaled wrongly", "softmax_rows", _softmax_no_shift_bug, P.check_gates_invariants),
+    ("z-loss without the square", "router_z_loss", _z_no_square, P.check_z_loss_closed_forms),
+    ("z-loss drops the row maximum", "router_z_loss", _z_no_max_term, P.check_z_loss_closed_forms),
+    ("bias step has the wrong sign", "bias_update", _bias_sign_flipped, P.check_bias_update_rule),
+    ("bias mean load ignores k", "bias_update", _bias_mean_ignores_k, P.check_bias_update_rule),
+    ("bias state kept in float64", "bias_update", _bias_float64_state, P.check_bias_update_rule),
 ]
 
 
