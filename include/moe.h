@@ -205,6 +205,40 @@ int moe_router_scores_noalloc(const moe_config* cfg, const void* x, const void* 
                               const float* logit_offset, float* scores, void* stream);
 
 /*
+ * moe_router_z_loss -- the router z-loss of a batch of router logits:
+ *     z_loss[0] = (1/T) * sum_t ( log sum_e exp(scores[t, e]) )^2
+ * "Mixture of Experts" (llm-tutorial ch. 11) § Why MoE is hard names the
+ * ST-MoE router z-loss, which penalises large router logits; the pages give
+ * no formula, and this is the ST-MoE form without its coefficient (the caller
+ * scales it).  scores: [T, E] float32 row-major device memory, finite values,
+ * e.g. from moe_router_scores (offset included).  z_loss: one float32 on the
+ * device.  T = 0 writes 0.  The log-partition function of each token is taken
+ * in float32 with the running row maximum subtracted; the squares are summed
+ * in double in a fixed order, so repeated calls give identical bits.  One
+ * launch of a single 8-CTA thread-block cluster; no workspace.
+ * Errors: MOE_ERR_ARG for T < 0, E outside 1..512, NULL or unaligned (4-byte)
+ * pointers; MOE_ERR_DEVICE, MOE_ERR_CUDA as elsewhere.
+ */
+int moe_router_z_loss(const float* scores, int32_t T, int32_t E, float* z_loss, void* stream);
+
+/*
+ * moe_bias_update -- one step of auxiliary-loss-free balancing ("Mixture of
+ * experts" (inside-the-model guide) § Auxiliary-loss-free balancing): the
+ * selection bias of every expert (sel_bias [E] float32, device, updated in
+ * place; the same array moe_forward takes) moves
+ *     down by gamma  when routed_counts[i] * E > T * k   (above the mean load),
+ *     up by gamma    when routed_counts[i] * E < T * k   (below it),
+ * and stays when the expert carries exactly the mean load.  routed_counts
+ * [E] int32 (device) is the pre-drop count per expert that moe_forward or
+ * moe_route wrote for the T-token batch with top-k; each change is one
+ * float32 add, rounded to nearest.  The comparison is exact integer
+ * arithmetic.  Errors: MOE_ERR_ARG for E outside 1..512, T < 0, k outside
+ * 1..E, NULL or unaligned pointers, gamma negative or not finite.
+ */
+int moe_bias_update(const int32_t* routed_counts, int32_t E, int32_t T, int32_t k, float gamma,
+                    float* sel_bias, void* stream);
+
+/*
  * moe_forward_host_io -- moe_forward with the activations in HOST memory:
  * x_host [T, d] is copied to the device, the layer runs, and y_host [T, d]
  * and aux_loss_host [1] are copied back, all enqueued on `stream` (pinned

@@ -30,7 +30,7 @@ EXPORTS = (
     "moe_workspace_size", "moe_forward", "moe_route_workspace_size", "moe_route",
     "moe_host_io_workspace_size", "moe_forward_host_io", "moe_check_status",
     "moe_error_string", "moe_forward_timed", "moe_launch_count", "moe_selftest_wait_timeout",
-    "moe_router_scores",
+    "moe_router_scores", "moe_router_scores_noalloc", "moe_router_z_loss", "moe_bias_update",
 )
 
 
@@ -80,6 +80,11 @@ def lib() -> ctypes.CDLL:
         L.moe_forward_host_io.restype = ctypes.c_int
         L.moe_router_scores.argtypes = [cfgp, P, P, P, P, P, SZ, P]
         L.moe_router_scores.restype = ctypes.c_int
+        L.moe_router_z_loss.argtypes = [P, ctypes.c_int32, ctypes.c_int32, P, P]
+        L.moe_router_z_loss.restype = ctypes.c_int
+        L.moe_bias_update.argtypes = [P, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
+                                      ctypes.c_float, P, P]
+        L.moe_bias_update.restype = ctypes.c_int
         L.moe_check_status.argtypes = [P, P]
         L.moe_check_status.restype = ctypes.c_int
         L.moe_error_string.argtypes = [ctypes.c_int]

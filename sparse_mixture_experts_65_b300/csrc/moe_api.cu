@@ -587,4 +587,28 @@ int moe_selftest_wait_timeout(void* workspace, size_t workspace_bytes, uint64_t 
   return MOE_OK;
 }
 
+int moe_router_z_loss(const float* scores, int32_t T, int32_t E, float* z_loss, void* stream) {
+  if (T < 0 || E < 1 || E > kMaxE || !z_loss || !aligned4(z_loss)) return MOE_ERR_ARG;
+  if (T > 0 && (!scores || !aligned4(scores))) return MOE_ERR_ARG;
+  int sms = 0;
+  const int rc = device_sms(&sms);
+  if (rc != MOE_OK) return rc;
+  MOE_TRY_CUDA(launch_router_z_loss(scores, T, E, z_loss, static_cast<cudaStream_t>(stream)));
+  return MOE_OK;
+}
+
+int moe_bias_update(const int32_t* routed_counts, int32_t E, int32_t T, int32_t k, float gamma,
+                    float* sel_bias, void* stream) {
+  if (E < 1 || E > kMaxE || T < 0 || k < 1 || k > E) return MOE_ERR_ARG;
+  if (!routed_counts || !sel_bias || !aligned4(routed_counts) || !aligned4(sel_bias))
+    return MOE_ERR_ARG;
+  if (!(gamma >= 0.f) || !std::isfinite(gamma)) return MOE_ERR_ARG;
+  int sms = 0;
+  const int rc = device_sms(&sms);
+  if (rc != MOE_OK) return rc;
+  MOE_TRY_CUDA(launch_bias_update(routed_counts, E, T, k, gamma, sel_bias,
+                                  static_cast<cudaStream_t>(stream)));
+  return MOE_OK;
+}
+
 }  // extern "C"

@@ -151,6 +151,10 @@ cudaError_t launch_experts_simt(const Plan& p, const void* x, const void* W1, co
                                 cudaEvent_t mid_event);
 cudaError_t launch_combine(const Plan& p, const float* topk_w, void* y, void* ws,
                            cudaStream_t st);
+cudaError_t launch_router_z_loss(const float* scores, int T, int E, float* z_loss,
+                                 cudaStream_t st);
+cudaError_t launch_bias_update(const int32_t* routed_counts, int E, int T, int k, float gamma,
+                               float* sel_bias, cudaStream_t st);
 cudaError_t launch_selftest_wait(uint32_t* status, uint64_t wait_ns, cudaStream_t st);
 
 }  // namespace moe

@@ -161,6 +161,34 @@ def router_scores(cfg: N.MoeConfig, x, W_r, logit_offset=None, out=None, workspa
     return out
 
 
+def router_z_loss(scores: torch.Tensor, out=None, stream=None) -> torch.Tensor:
+    """Router z-loss of [T, E] float32 logits (moe_router_z_loss): a one-element
+    float32 device tensor."""
+    if scores.dtype != torch.float32 or scores.dim() != 2 or not scores.is_contiguous():
+        raise ValueError("scores must be a contiguous [T, E] float32 tensor")
+    if out is None:
+        out = torch.empty(1, dtype=torch.float32, device=scores.device)
+    T, E = scores.shape
+    N.check(N.lib().moe_router_z_loss(_ptr(scores), T, E, _ptr(out), _stream_handle(stream)),
+            "moe_router_z_loss")
+    return out
+
+
+def bias_update(sel_bias: torch.Tensor, routed_counts: torch.Tensor, T: int, k: int,
+                gamma: float, stream=None) -> torch.Tensor:
+    """One auxiliary-loss-free balancing step on sel_bias, in place
+    (moe_bias_update); returns sel_bias."""
+    if sel_bias.dtype != torch.float32 or routed_counts.dtype != torch.int32:
+        raise ValueError("sel_bias must be float32 and routed_counts int32")
+    if sel_bias.numel() != routed_counts.numel():
+        raise ValueError("sel_bias and routed_counts need one entry per expert")
+    N.check(N.lib().moe_bias_update(_ptr(routed_counts), sel_bias.numel(), int(T), int(k),
+                                    ctypes.c_float(gamma), _ptr(sel_bias),
+                                    _stream_handle(stream)),
+            "moe_bias_update")
+    return sel_bias
+
+
 def forward_host_io(cfg: N.MoeConfig, x_host: torch.Tensor, y_host: torch.Tensor,
                     aux_host: torch.Tensor, W_r, W1, W2, W3=None, logit_offset=None,
                     sel_bias=None, Ws1=None, Ws3=None, Ws2=None, workspace=None, stream=None):

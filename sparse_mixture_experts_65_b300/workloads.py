@@ -154,3 +154,33 @@ def make_inputs(shape: LayerShape, device="cpu", seed: int = 0) -> LayerInputs:
         Ws3 = _normal((fs, d), 1.0 / math.sqrt(d), _gen(device, base + 8), device, dt)
         Ws2 = _normal((d, fs), 1.0 / math.sqrt(fs), _gen(device, base + 9), device, dt)
     return LayerInputs(shape, x, W_r, W1, W2, W3, logit_offset, sel_bias, Ws1, Ws3, Ws2)
+
+
+def make_logits(T: int, E: int, seed: int, scale: float = 1.0, shift: float = 0.0,
+                device="cpu") -> torch.Tensor:
+    """Router-logit-shaped float32 [T, E]: scale * N(0, 1) + shift."""
+    g = _gen(device, 7_000_003 + seed)
+    return torch.randn((T, E), generator=g, device=device, dtype=torch.float32) * scale + shift
+
+
+def make_routed_counts(E: int, T: int, k: int, seed: int, skew: float = 1.0,
+                       device="cpu") -> torch.Tensor:
+    """Per-expert routed counts int32 [E] summing to T*k: the T*k assignments
+    are dealt by a seeded multinomial over E experts with weights exp(skew * N(0,1)).
+    When E divides T*k, every third expert is then set to the exact mean load
+    where the last expert can absorb the difference (so the 'at the mean' case
+    occurs); the total stays T*k."""
+    g = _gen("cpu", 8_000_009 + seed)
+    w = torch.exp(skew * torch.randn(E, generator=g, dtype=torch.float64))
+    counts = torch.zeros(E, dtype=torch.int64)
+    if T * k > 0:
+        draws = torch.multinomial(w, T * k, replacement=True, generator=g)
+        counts = torch.bincount(draws, minlength=E)
+    if E > 1 and (T * k) % E == 0:
+        mean = (T * k) // E
+        for i in range(0, E - 1, 3):
+            delta = int(counts[i]) - mean
+            if int(counts[E - 1]) + delta >= 0:   # the last expert absorbs the difference
+                counts[i] = mean
+                counts[E - 1] += delta
+    return counts.to(torch.int32).to(device)

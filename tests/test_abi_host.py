@@ -122,3 +122,25 @@ def test_capacity_formula_matches_documented_rounding():
     # check that huge factors do not overflow the size computation
     cfg = L.make_config(T=4096, d=768, E=64, k=1, f=3072, act=W.ACT_RELU, capacity_factor=1e12)
     assert _rc_size(cfg) == N.MOE_OK
+
+
+def test_balance_controls_check_arguments_without_gpu():
+    """moe_router_z_loss and moe_bias_update reject bad sizes, NULL and
+    unaligned pointers before any device work."""
+    lib = N.lib()
+    fake = ctypes.c_void_p(1 << 20)
+    odd = ctypes.c_void_p((1 << 20) + 2)
+    assert lib.moe_router_z_loss(fake, -1, 8, fake, None) == N.MOE_ERR_ARG
+    assert lib.moe_router_z_loss(fake, 4, 0, fake, None) == N.MOE_ERR_ARG
+    assert lib.moe_router_z_loss(fake, 4, 513, fake, None) == N.MOE_ERR_ARG
+    assert lib.moe_router_z_loss(None, 4, 8, fake, None) == N.MOE_ERR_ARG
+    assert lib.moe_router_z_loss(odd, 4, 8, fake, None) == N.MOE_ERR_ARG
+    assert lib.moe_router_z_loss(fake, 4, 8, None, None) == N.MOE_ERR_ARG
+    f = ctypes.c_float
+    assert lib.moe_bias_update(fake, 0, 4, 1, f(1e-3), fake, None) == N.MOE_ERR_ARG
+    assert lib.moe_bias_update(fake, 8, 4, 9, f(1e-3), fake, None) == N.MOE_ERR_ARG
+    assert lib.moe_bias_update(fake, 8, -1, 1, f(1e-3), fake, None) == N.MOE_ERR_ARG
+    assert lib.moe_bias_update(fake, 8, 4, 1, f(-1.0), fake, None) == N.MOE_ERR_ARG
+    assert lib.moe_bias_update(fake, 8, 4, 1, f(float("nan")), fake, None) == N.MOE_ERR_ARG
+    assert lib.moe_bias_update(None, 8, 4, 1, f(1e-3), fake, None) == N.MOE_ERR_ARG
+    assert lib.moe_bias_update(fake, 8, 4, 1, f(1e-3), odd, None) == N.MOE_ERR_ARG
