@@ -257,6 +257,30 @@ constexpr int kABox = 32;
 
 // Warp roles: producer warps (one TMA warp, or four gathering warps), one MMA
 // warp, four epilogue warps.
+// The A rows of one stage gathered from the token rows of x: 32 warp
+// instructions of 4 whole 128-byte row pieces each (lanes 8r..8r+7 take the
+// 8 16-byte chunks of row 4t + r), written in the 128-byte swizzle the MMA
+// descriptors read (chunk c of row i at i*128 + (c ^ (i & 7))*16).  Rows whose
+// token is -1 are skipped; with `in` false every copy reads nothing and writes
+// zeros.  Kept out of line so that one dry call before the grid wait (all rows
+// absent) loads these instructions into the SM's instruction cache: fetched
+// for the first time after the wait they queue behind the weight traffic.
+__device__ __noinline__ void gather_stage(uint32_t sa, const int* tok_s, const char* gx,
+                                          size_t row_bytes, int col, bool in, int sub,
+                                          int chunk) {
+#pragma unroll 8
+  for (int t = 0; t < 32; ++t) {
+    const int i = 4 * t + sub;
+    const int tok = tok_s[i];
+    if (tok >= 0)
+      cp_async16_s(sa + i * 128 + ((chunk ^ (i & 7)) << 4),
+                   in ? (const void*)(gx + (size_t)tok * row_bytes + (size_t)col * 2)
+                      : (const void*)gx,
+                   in ? 16u : 0u);
+  }
+  cp_async_commit_group();
+}
+
 template <bool GATHER>
 struct TcWarps {
   static constexpr int PROD = GATHER ? 4 : 1;
@@ -372,6 +396,20 @@ tc_grouped_gemm(const __grid_constant__ CUtensorMap mA, const __grid_constant__ 
       }
     }
   }
+  if constexpr (GATHER) {
+    // dry run of the row gather with every row marked absent: no copy is
+    // issued, but the instructions are fetched into the instruction cache
+    if (warp < Wr::PROD) {
+      int* tok_w = reinterpret_cast<int*>(smem + C::STAGES * C::STAGE_BYTES + C::BAR_BYTES +
+                                          4 * C::SCHED_INTS) + warp * 128;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) tok_w[lane + 32 * j] = -1;
+      __syncwarp();
+      gather_stage(smem_base + warp * C::STAGE_BYTES, tok_w, a.gx, a.gx_row_bytes, 0, false,
+                   lane >> 3, lane & 7);
+      __syncwarp();
+    }
+  }
   pdl_wait();      // everything above ran while the previous kernel finished
   pdl_trigger();
   if (!a.early_b) copy_sched();
@@ -462,19 +500,7 @@ tc_grouped_gemm(const __grid_constant__ CUtensorMap mA, const __grid_constant__ 
           }
           if (gat) {
             const int col = kb * C::BK + chunk * 8;
-            const bool in = col < ti.K;   // K is a multiple of 8
-#pragma unroll 8
-            for (int t = 0; t < 32; ++t) {
-              const int i = 4 * t + sub;
-              const int tok = tok_s[i];
-              if (tok >= 0)
-                cp_async16_s(sa + i * 128 + ((chunk ^ (i & 7)) << 4),
-                             in ? (const void*)(a.gx + (size_t)tok * a.gx_row_bytes +
-                                                (size_t)col * 2)
-                                : (const void*)a.gx,
-                             in ? 16u : 0u);
-            }
-            cp_async_commit_group();
+            gather_stage(sa, tok_s, a.gx, a.gx_row_bytes, col, col < ti.K, sub, chunk);
             cp_async_wait_group<0>();
             fence_proxy_async_smem();
           }
