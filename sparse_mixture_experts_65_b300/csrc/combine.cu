@@ -1,6 +1,8 @@
 // combine.cu -- stage 6: y[t] = shared(x_t) + sum_j g_tj * o[row(t, j)],
 // over the kept slots, accumulated in float32 in the fixed order j = 0..k-1
-// (no atomics), then rounded once to the output dtype.
+// (no atomics), then rounded once to the output dtype.  The expert outputs o
+// (and the shared expert's) arrive in the layer dtype: bf16 on the
+// tensor-core path, float32 on the float32 path.
 //
 // "Mixture of Experts" (llm-tutorial ch. 11) § The mathematics and
 // "Mixture-of-Experts" (neural networks visually) § Show the math: the layer
@@ -13,8 +15,8 @@
 namespace moe {
 
 struct CombineArgs {
-  const float* o;        // [R_cap][d]
-  const float* os;       // [T_pad][d] or null
+  const void* o;         // [R_cap][d] TOut
+  const void* os;        // [T_pad][d] TOut, or null
   const int* key_row;    // [T*k]
   const float* topk_w;   // [T*k]
   void* y;               // [T][d]
@@ -33,6 +35,16 @@ __device__ __forceinline__ void store4(__nv_bfloat16* y, size_t i, float4 v) {
   *reinterpret_cast<uint2*>(y + i) = u;
 }
 
+__device__ __forceinline__ float4 load4(const float* p, size_t i) {
+  return *reinterpret_cast<const float4*>(p + i);
+}
+__device__ __forceinline__ float4 load4(const __nv_bfloat16* p, size_t i) {
+  const uint2 u = *reinterpret_cast<const uint2*>(p + i);
+  const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.x));
+  const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.y));
+  return make_float4(a.x, a.y, b.x, b.y);
+}
+
 template <typename TOut>
 __global__ void __launch_bounds__(kThreads) combine_kernel(const CombineArgs a) {
   __shared__ int rows[kMaxK];
@@ -45,15 +57,17 @@ __global__ void __launch_bounds__(kThreads) combine_kernel(const CombineArgs a) 
     gates[threadIdx.x] = a.topk_w[(size_t)t * a.k + threadIdx.x];
   }
   __syncthreads();
+  const TOut* o = static_cast<const TOut*>(a.o);
+  const TOut* os = static_cast<const TOut*>(a.os);
   TOut* y = static_cast<TOut*>(a.y);
   for (int c = threadIdx.x * 4; c < a.d; c += kThreads * 4) {
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (a.os) acc = *reinterpret_cast<const float4*>(a.os + (size_t)t * a.d + c);
+    if (os) acc = load4(os, (size_t)t * a.d + c);
     for (int j = 0; j < a.k; ++j) {
       const int r = rows[j];
       if (r < 0) continue;
       const float g = gates[j];
-      const float4 v = *reinterpret_cast<const float4*>(a.o + (size_t)r * a.d + c);
+      const float4 v = load4(o, (size_t)r * a.d + c);
       acc.x = fmaf(g, v.x, acc.x);
       acc.y = fmaf(g, v.y, acc.y);
       acc.z = fmaf(g, v.z, acc.z);
@@ -67,8 +81,8 @@ cudaError_t launch_combine(const Plan& p, const float* topk_w, void* y, void* ws
                            cudaStream_t st) {
   CombineArgs a;
   char* w = static_cast<char*>(ws);
-  a.o = reinterpret_cast<const float*>(w + p.ws.o);
-  a.os = p.cfg.n_shared ? reinterpret_cast<const float*>(w + p.ws.os) : nullptr;
+  a.o = w + p.ws.o;
+  a.os = p.cfg.n_shared ? static_cast<const void*>(w + p.ws.os) : nullptr;
   a.key_row = reinterpret_cast<const int*>(w + p.ws.key_row);
   a.topk_w = topk_w;
   a.y = y;

@@ -39,8 +39,12 @@
 
 namespace moe {
 
-enum { EPI_SWIGLU = 0, EPI_GELU = 1, EPI_RELU = 2, EPI_F32 = 3, EPI_F32_CHUNKED = 4,
+enum { EPI_SWIGLU = 0, EPI_GELU = 1, EPI_RELU = 2, EPI_OUT16 = 3, EPI_F32_CHUNKED = 4,
        EPI_COMBINE1 = 5 };
+
+// EPI_OUT16 (down projection when the combine is a separate kernel): the
+// expert output rows o are stored as bf16, rounded once from the float32
+// accumulator; the combine sums g * o in float32 and rounds y once more.
 
 // EPI_COMBINE1 (down projection of a top-1 layer without a shared expert):
 // the combine is folded into the epilogue.  Row r of expert e holds the single
@@ -173,8 +177,9 @@ __device__ __forceinline__ float silu_mul(float g, float u) {
   return g / (1.0f + __expf(-g)) * u;
 }
 
-// Epilogue of one accumulator: activation (or none), bf16 / fp32 stores of
-// this thread's row, masked at the segment's last row and the last column.
+// Epilogue of one accumulator: activation (or none, or the gate of a top-1
+// combine), bf16 stores of this thread's row, masked at the segment's last
+// row and the last column.
 template <int BNH, bool DUAL, int EPI>
 __device__ __forceinline__ void epilogue_tile(const TcArgs& a, const TileInfo& ti, uint32_t t_row,
                                               size_t orow, bool row_ok, float scale) {
@@ -186,63 +191,43 @@ __device__ __forceinline__ void epilogue_tile(const TcArgs& a, const TileInfo& t
     if (DUAL) tmem_ld32(t_row + BNH + c, r1);
     tmem_ld_wait();
     const int col = ti.n0 + c;
-    if (EPI == EPI_F32) {
-      float* out = static_cast<float*>(ti.shared ? a.out_sh : a.out);
-      const int ld = ti.shared ? a.ld_out_sh : a.ld_out;
-      float* dst = out + orow * ld + col;
-      if (!row_ok) {
-      } else if (col + 32 <= ti.N) {
+    __nv_bfloat16* out = static_cast<__nv_bfloat16*>(
+        EPI == EPI_COMBINE1 ? a.y : (ti.shared ? a.out_sh : a.out));
+    const int ld = EPI == EPI_COMBINE1 ? a.ld_y : (ti.shared ? a.ld_out_sh : a.ld_out);
+    __nv_bfloat16* dst = out + orow * ld + col;
+    uint32_t pk[16];
 #pragma unroll
-        for (int v = 0; v < 8; ++v) {
-          float4 f4 = make_float4(__uint_as_float(r0[4 * v]), __uint_as_float(r0[4 * v + 1]),
-                                  __uint_as_float(r0[4 * v + 2]),
-                                  __uint_as_float(r0[4 * v + 3]));
-          reinterpret_cast<float4*>(dst)[v] = f4;
-        }
-      } else {
-#pragma unroll
-        for (int i = 0; i < 32; ++i)
-          if (col + i < ti.N) dst[i] = __uint_as_float(r0[i]);
+    for (int i = 0; i < 16; ++i) {
+      float v0 = __uint_as_float(r0[2 * i]), v1 = __uint_as_float(r0[2 * i + 1]);
+      if (EPI == EPI_SWIGLU) {
+        v0 = silu_mul(v0, __uint_as_float(r1[2 * i]));
+        v1 = silu_mul(v1, __uint_as_float(r1[2 * i + 1]));
+      } else if (EPI == EPI_RELU) {
+        v0 = fmaxf(v0, 0.f);
+        v1 = fmaxf(v1, 0.f);
+      } else if (EPI == EPI_GELU) {
+        v0 = 0.5f * v0 * (1.0f + erff(v0 * 0.70710678118654752f));
+        v1 = 0.5f * v1 * (1.0f + erff(v1 * 0.70710678118654752f));
+      } else if (EPI == EPI_COMBINE1) {
+        v0 = fmaf(scale, v0, 0.f);
+        v1 = fmaf(scale, v1, 0.f);
       }
+      __nv_bfloat162 b2 = __floats2bfloat162_rn(v0, v1);
+      pk[i] = *reinterpret_cast<uint32_t*>(&b2);
+    }
+    if (!row_ok) {
+    } else if (col + 32 <= ti.N) {
+#pragma unroll
+      for (int v = 0; v < 4; ++v)
+        reinterpret_cast<uint4*>(dst)[v] =
+            make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
     } else {
-      __nv_bfloat16* out = static_cast<__nv_bfloat16*>(
-          EPI == EPI_COMBINE1 ? a.y : (ti.shared ? a.out_sh : a.out));
-      const int ld = EPI == EPI_COMBINE1 ? a.ld_y : (ti.shared ? a.ld_out_sh : a.ld_out);
-      __nv_bfloat16* dst = out + orow * ld + col;
-      uint32_t pk[16];
 #pragma unroll
-      for (int i = 0; i < 16; ++i) {
-        float v0 = __uint_as_float(r0[2 * i]), v1 = __uint_as_float(r0[2 * i + 1]);
-        if (EPI == EPI_SWIGLU) {
-          v0 = silu_mul(v0, __uint_as_float(r1[2 * i]));
-          v1 = silu_mul(v1, __uint_as_float(r1[2 * i + 1]));
-        } else if (EPI == EPI_RELU) {
-          v0 = fmaxf(v0, 0.f);
-          v1 = fmaxf(v1, 0.f);
-        } else if (EPI == EPI_GELU) {
-          v0 = 0.5f * v0 * (1.0f + erff(v0 * 0.70710678118654752f));
-          v1 = 0.5f * v1 * (1.0f + erff(v1 * 0.70710678118654752f));
-        } else if (EPI == EPI_COMBINE1) {
-          v0 = fmaf(scale, v0, 0.f);
-          v1 = fmaf(scale, v1, 0.f);
-        }
-        __nv_bfloat162 b2 = __floats2bfloat162_rn(v0, v1);
-        pk[i] = *reinterpret_cast<uint32_t*>(&b2);
-      }
-      if (!row_ok) {
-      } else if (col + 32 <= ti.N) {
-#pragma unroll
-        for (int v = 0; v < 4; ++v)
-          reinterpret_cast<uint4*>(dst)[v] =
-              make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
-      } else {
-#pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          if (col + i < ti.N) {
-            const uint32_t w = pk[i >> 1];
-            reinterpret_cast<uint16_t*>(dst)[i] =
-                (i & 1) ? static_cast<uint16_t>(w >> 16) : static_cast<uint16_t>(w);
-          }
+      for (int i = 0; i < 32; ++i) {
+        if (col + i < ti.N) {
+          const uint32_t w = pk[i >> 1];
+          reinterpret_cast<uint16_t*>(dst)[i] =
+              (i & 1) ? static_cast<uint16_t>(w >> 16) : static_cast<uint16_t>(w);
         }
       }
     }
@@ -255,8 +240,6 @@ __device__ __forceinline__ void epilogue_tile(const TcArgs& a, const TileInfo& t
 // epilogue never stores.
 constexpr int kABox = 32;
 
-// Warp roles: producer warps (one TMA warp, or four gathering warps), one MMA
-// warp, four epilogue warps.
 // The A rows of one stage gathered from the token rows of x: 32 warp
 // instructions of 4 whole 128-byte row pieces each (lanes 8r..8r+7 take the
 // 8 16-byte chunks of row 4t + r), written in the 128-byte swizzle the MMA
@@ -281,6 +264,8 @@ __device__ __noinline__ void gather_stage(uint32_t sa, const int* tok_s, const c
   cp_async_commit_group();
 }
 
+// Warp roles: producer warps (one TMA warp, or four gathering warps), one MMA
+// warp, four epilogue warps.
 template <bool GATHER>
 struct TcWarps {
   static constexpr int PROD = GATHER ? 4 : 1;
@@ -768,11 +753,11 @@ static cudaError_t dispatch_down(int bn, bool combine1, const TcMaps& m, const T
     return cudaErrorInvalidValue;
   }
   switch (bn) {
-    case 256: return run_tc<256, false, EPI_F32>(m, a, grid, st);
-    case 192: return run_tc<192, false, EPI_F32>(m, a, grid, st);
-    case 128: return run_tc<128, false, EPI_F32>(m, a, grid, st);
-    case 96: return run_tc<96, false, EPI_F32>(m, a, grid, st);
-    case 64: return run_tc<64, false, EPI_F32>(m, a, grid, st);
+    case 256: return run_tc<256, false, EPI_OUT16>(m, a, grid, st);
+    case 192: return run_tc<192, false, EPI_OUT16>(m, a, grid, st);
+    case 128: return run_tc<128, false, EPI_OUT16>(m, a, grid, st);
+    case 96: return run_tc<96, false, EPI_OUT16>(m, a, grid, st);
+    case 64: return run_tc<64, false, EPI_OUT16>(m, a, grid, st);
   }
   return cudaErrorInvalidValue;
 }

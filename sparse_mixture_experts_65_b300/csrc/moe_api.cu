@@ -210,7 +210,7 @@ int make_plan(const moe_config* cfg, WsKind kind, Plan* p, int num_sms) {
     const long long per_expert = Tk / (c.E > 0 ? c.E : 1);
     P.gather = P.tc && P.route_tc && per_expert <= kTcBM;
     const char* gv = std::getenv("MOE_GATHER");
-    if (gv && P.tc && P.route_tc) P.gather = std::atoi(gv) != 0;
+    if (gv && P.tc) P.gather = std::atoi(gv) != 0;
   }
   P.nt_up = ceil_div(c.f, P.up_bn);
   P.nt_dn = ceil_div(c.d, P.dn_bn);
@@ -248,10 +248,12 @@ int make_plan(const moe_config* cfg, WsKind kind, Plan* p, int num_sms) {
     const size_t act_elem = P.elem;   // h is bf16 on the tensor-core path, fp32 otherwise
     L.xp = take(P.gather ? 0 : (size_t)P.R_cap * c.d * P.elem);
     L.h = take((size_t)P.R_cap * c.f * act_elem);
-    L.o = take((size_t)P.R_cap * c.d * sizeof(float));
+    // expert outputs in the layer dtype: bf16 rounded once from the float32
+    // accumulator on the tensor-core path, float32 otherwise
+    L.o = take((size_t)P.R_cap * c.d * P.elem);
     if (c.n_shared) {
       L.hs = take((size_t)P.T_pad * c.f_shared * act_elem);
-      L.os = take((size_t)P.T_pad * c.d * sizeof(float));
+      L.os = take((size_t)P.T_pad * c.d * P.elem);
     }
   }
   if (kind == WsKind::HostIO) {

@@ -51,9 +51,9 @@ struct WsLayout {
   size_t xp;          // dtype  [R_cap][d] token copies in expert order (absent when the
                       //        tensor-core up projection gathers the rows of x itself)
   size_t h;           // dtype  [R_cap][f] expert hidden activations
-  size_t o;           // float  [R_cap][d] expert outputs
+  size_t o;           // dtype  [R_cap][d] expert outputs
   size_t hs;          // dtype  [T_pad][f_s] shared-expert hidden
-  size_t os;          // float  [T_pad][d]   shared-expert output
+  size_t os;          // dtype  [T_pad][d]   shared-expert output
   // host-io staging
   size_t x_dev, y_dev, topk_idx, topk_w, counts, aux;
   size_t total;

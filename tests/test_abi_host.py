@@ -53,10 +53,11 @@ def test_workspace_sizes(name):
     assert 0 < rt < fw < io
     assert fw % 256 == 0
     elem = 4 if s.dtype == "f32" else 2
-    # the expert-ordered buffers alone: at least T*k rows of h and o (and of
-    # x unless the up projection gathers rows: the Switch layer)
+    # the expert-ordered buffers alone: at least T*k rows of h and o, both in
+    # the layer dtype (and of x unless the up projection gathers rows: the
+    # Switch layer)
     x_rows = 0 if name == "switch" else s.d * elem
-    assert fw >= s.T * s.k * (x_rows + s.f * elem + s.d * 4)
+    assert fw >= s.T * s.k * (x_rows + s.f * elem + s.d * elem)
     # routing: one tensor-core launch for bf16 layers with E <= 64 and k <= 8
     # (plus a row copy unless the up projection gathers rows: Mixtral copies),
     # else three (logits, top-k, permute); two projections; the combine unless

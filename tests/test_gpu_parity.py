@@ -347,11 +347,13 @@ def test_decode_batch_router(shape):
 
 @pytest.mark.parametrize("gather", ["0", "1"])
 def test_up_projection_row_source(monkeypatch, gather):
-    """Both row sources of the tensor-core up projection on one-launch-routed
-    layers: rows gathered from x inside the GEMM (cp.async), and an
-    expert-ordered copy read through TMA."""
+    """Both row sources of the tensor-core up projection, on layers of every
+    routing path (one-launch tensor-core router, split router with E > 64,
+    decode-batch router): rows gathered from x inside the GEMM (cp.async),
+    and an expert-ordered copy read through TMA."""
     monkeypatch.setenv("MOE_GATHER", gather)
-    for shape in (SMALL[0], SMALL[1], SMALL[2], SMALL[3], ONE_LAUNCH[1], ONE_LAUNCH[3]):
+    for shape in (SMALL[0], SMALL[1], SMALL[2], SMALL[3], SMALL[4], ONE_LAUNCH[1], ONE_LAUNCH[3],
+                  DECODE[1], DECODE[3]):
         inp = W.make_inputs(shape, "cuda", seed=12)
         _, out = run_gpu(inp)
         check_layer(inp, out)
