@@ -245,10 +245,8 @@ constexpr int kABox = 32;
 // 8 16-byte chunks of row 4t + r), written in the 128-byte swizzle the MMA
 // descriptors read (chunk c of row i at i*128 + (c ^ (i & 7))*16).  Rows whose
 // token is -1 are skipped; with `in` false every copy reads nothing and writes
-// zeros.  Kept out of line so that one dry call before the grid wait (all rows
-// absent) loads these instructions into the SM's instruction cache: fetched
-// for the first time after the wait they queue behind the weight traffic.
-__device__ __noinline__ void gather_stage(uint32_t sa, const int* tok_s, const char* gx,
+// zeros.
+__device__ __forceinline__ void gather_stage(uint32_t sa, const int* tok_s, const char* gx,
                                           size_t row_bytes, int col, bool in, int sub,
                                           int chunk) {
 #pragma unroll 8
@@ -379,20 +377,6 @@ tc_grouped_gemm(const __grid_constant__ CUtensorMap mA, const __grid_constant__ 
           tma_load_3d(sb + BNH * 128, ti.shared ? &mB1_sh : &mB1, full_bar(npre), kb * C::BK,
                       ti.n0, e);
       }
-    }
-  }
-  if constexpr (GATHER) {
-    // dry run of the row gather with every row marked absent: no copy is
-    // issued, but the instructions are fetched into the instruction cache
-    if (warp < Wr::PROD) {
-      int* tok_w = reinterpret_cast<int*>(smem + C::STAGES * C::STAGE_BYTES + C::BAR_BYTES +
-                                          4 * C::SCHED_INTS) + warp * 128;
-#pragma unroll
-      for (int j = 0; j < 4; ++j) tok_w[lane + 32 * j] = -1;
-      __syncwarp();
-      gather_stage(smem_base + warp * C::STAGE_BYTES, tok_w, a.gx, a.gx_row_bytes, 0, false,
-                   lane >> 3, lane & 7);
-      __syncwarp();
     }
   }
   pdl_wait();      // everything above ran while the previous kernel finished
