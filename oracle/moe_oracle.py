@@ -44,7 +44,10 @@ with its reason, in the design notes of the repository):
     (the pages give no formula, so this function is pinned only to that
     reading: closed forms and a library logsumexp);
   * bias balancing step: load = routed count, overloaded iff
-    routed_i * E > T * k, underloaded iff below, float32 state.
+    routed_i * E > T * k, underloaded iff below, float32 state;
+  * fp8 variant (not on the pages): e4m3 gate/up weights with per-channel
+    scales, token rows quantised with a power-of-two scale (the smallest
+    with max|x| / s <= 448), values rounded to nearest e4m3, ties to even.
 
 Parity pins: every function below is pinned by ``tests/test_oracle_pins.py``
 (brute force, closed forms, library special cases and page numbers under
@@ -393,6 +396,86 @@ def bias_update(sel_bias, routed, T: int, k: int, gamma: float) -> np.ndarray:
     return b
 
 
+# Variant with fp8 (e4m3) gate and up expert weights.  The pages use no 8-bit
+# formats: this is the plain definition of that variant of the same layer.
+# The weights arrive as e4m3 codes with one float32 scale per output channel
+# (W[e][n][c] = scale[e][n] * e4m3(code[e][n][c])); every token row entering the
+# up projection is quantised with a power-of-two scale s_t = 2^q, q the
+# smallest integer (not below -126) with max|x_t| / 2^q <= 448 (s_t = 1 for an
+# all-zero row), its values rounded to the nearest e4m3 value (ties to even);
+# the products are then exact and summed in float64.  The down projection
+# reads the same h as the bf16 layer.
+# --------------------------------------------------------------------------
+E4M3_MAX = 448.0
+
+
+def e4m3_decode(codes) -> np.ndarray:
+    """Values of e4m3 codes (sign bit, 4 exponent bits with bias 7, 3 mantissa
+    bits; exponent 0 is subnormal, m * 2^-9; code S.1111.111 is NaN)."""
+    c = np.asarray(codes, dtype=np.int64) & 0xFF
+    sign = np.where(c & 0x80, -1.0, 1.0)
+    ex = (c >> 3) & 0xF
+    man = (c & 0x7).astype(np.float64)
+    val = np.where(ex == 0, man * 2.0 ** -9, (1.0 + man / 8.0) * np.exp2(ex - 7.0))
+    val = np.where((ex == 15) & ((c & 0x7) == 7), np.nan, val)
+    return sign * val
+
+
+def e4m3_round(v) -> np.ndarray:
+    """Nearest e4m3 value (ties to even), magnitudes above 448 saturated."""
+    v = _f64(v)
+    a = np.abs(v)
+    _, q = np.frexp(a)                       # a = f * 2^q, f in [0.5, 1)
+    # spacing of e4m3 values around a: 2^(exponent - 3) for normals
+    # (|a| >= 2^-6), 2^-9 in the subnormal range
+    quantum = np.where(a >= 2.0 ** -6, np.exp2(q - 1.0 - 3.0), 2.0 ** -9)
+    r = np.rint(a / quantum) * quantum       # rint: half to even
+    r = np.minimum(r, E4M3_MAX)
+    return np.sign(v) * r
+
+
+def row_scale_exponent(amax: float) -> int:
+    """The q of s = 2^q: smallest integer >= -126 with amax / 2^q <= 448."""
+    if not amax > 0.0:
+        return 0
+    f, q = math.frexp(float(amax))          # amax = f * 2^q, f in [0.5, 1)
+    e = q - 9 + (1 if f > 0.875 else 0)     # 448 = 1.75 * 2^8
+    return max(e, -126)
+
+
+def quantize_rows_e4m3(X):
+    """(values, scales): each row of X as e4m3 values times its power-of-two
+    scale; values * scale[:, None] is the row the fp8 up projection reads."""
+    X = _f64(X)
+    scales = np.empty(X.shape[0])
+    vals = np.empty_like(X)
+    for t in range(X.shape[0]):
+        s = 2.0 ** row_scale_exponent(float(np.max(np.abs(X[t]))) if X.shape[1] else 0.0)
+        scales[t] = s
+        vals[t] = e4m3_round(X[t] / s)
+    return vals, scales
+
+
+def dequantize_weights(codes, scales) -> np.ndarray:
+    """[E, n, c] e4m3 codes and [E, n] float32 scales -> float64 weights."""
+    return e4m3_decode(codes) * _f64(scales)[..., None]
+
+
+def moe_forward_fp8(x, W_r, W1q, W1s, W3q, W3s, W2, k: int, gate_mode: str,
+                    logit_offset=None, sel_bias=None, capacity_factor=None,
+                    alpha: float = 0.01, tokens=None, forced_idx=None) -> OracleResult:
+    """The SwiGLU layer with e4m3 gate/up weights (codes + per-channel scales):
+    routing on x, the up projection on the quantised rows of x."""
+    vals, scales = quantize_rows_e4m3(x)
+    xq = vals * scales[:, None]
+    W1 = dequantize_weights(W1q, W1s)
+    W3 = dequantize_weights(W3q, W3s)
+    return moe_forward(x, W_r, W1, W2, k, ACT_SWIGLU, gate_mode, W3=W3,
+                       logit_offset=logit_offset, sel_bias=sel_bias,
+                       capacity_factor=capacity_factor, alpha=alpha, tokens=tokens,
+                       forced_idx=forced_idx, x_experts=xq)
+
+
 class _Indexable:
     """Per-expert weight access; lets callers stream experts lazily."""
 
@@ -441,12 +524,16 @@ def route(x, W_r, k: int, gate_mode: str, logit_offset=None, sel_bias=None,
 def moe_forward(x, W_r, W1, W2, k: int, act: str, gate_mode: str, W3=None,
                 logit_offset=None, sel_bias=None, capacity_factor=None,
                 alpha: float = 0.01, Ws1=None, Ws3=None, Ws2=None,
-                tokens=None, forced_idx=None, count_multiplies=False) -> OracleResult:
+                tokens=None, forced_idx=None, count_multiplies=False,
+                x_experts=None) -> OracleResult:
     """The whole layer.  W1/W3/W2 may be arrays [E, ...] or any object whose
     [e] returns expert e's matrix.  tokens: optional subset of token indices for
     which y is evaluated (routing always runs on the whole batch, since capacity
-    is a property of the whole batch)."""
+    is a property of the whole batch).  x_experts: optional [T, d] rows that
+    the routed experts read instead of x (the fp8 variant's quantised rows);
+    routing always reads x."""
     x = _f64(x)
+    xe = x if x_experts is None else _f64(x_experts)
     T = x.shape[0]
     s, sel, idx, g, probs, asg, f, P, L = route(
         x, W_r, k, gate_mode, logit_offset, sel_bias, capacity_factor, alpha, forced_idx)
@@ -468,7 +555,7 @@ def moe_forward(x, W_r, W1, W2, k: int, act: str, gate_mode: str, W3=None,
         w1, w2 = W1i[e], W2i[e]
         w3 = W3i[e] if W3i is not None else None
         items = work[e]
-        out = expert_ffn_rows(x[[t for _, t, _ in items]], w1, w2, act, w3, counter)
+        out = expert_ffn_rows(xe[[t for _, t, _ in items]], w1, w2, act, w3, counter)
         for i, (r, t, j) in enumerate(items):
             y[r] += g[t, j] * out[i]
     if Ws1 is not None and len(tok):

@@ -477,6 +477,71 @@ def check_bias_update_rule():
     assert out.dtype == np.float32 and out[0] == np.float32(np.float32(0.1) + np.float32(0.3))
 
 
+# ---------------------------------------------------------------- fp8 variant
+def check_e4m3_format():
+    """e4m3 decoding and rounding against torch's float8_e4m3fn (a library
+    routine) on all 256 codes and on sampled values, plus hand-checked ties."""
+    codes = np.arange(256)
+    ref = torch.tensor(codes, dtype=torch.uint8).view(torch.float8_e4m3fn).float().numpy()
+    got = O.e4m3_decode(codes)
+    finite = ~np.isnan(ref)
+    assert np.array_equal(np.isnan(got), np.isnan(ref))
+    assert np.array_equal(got[finite], ref[finite])
+    rng = _rng(80)
+    v = np.concatenate([rng.normal(size=20000) * rng.choice([1e-3, 0.05, 1.0, 30.0], 20000),
+                        rng.uniform(-448, 448, 5000)]).astype(np.float32)
+    r = O.e4m3_round(v)
+    t = torch.tensor(v).to(torch.float8_e4m3fn).float().numpy()
+    assert np.array_equal(r, t)
+    # ties go to the even mantissa; subnormal spacing 2^-9; saturation at 448
+    hand = {1.0625: 1.0, 1.1875: 1.25, 2.0 ** -10: 0.0, 3 * 2.0 ** -10: 2.0 ** -8,
+            448.0: 448.0, 464.0: 448.0, 1000.0: 448.0, -0.6875: -0.6875, -0.71875: -0.75}
+    for a, b in hand.items():
+        assert O.e4m3_round(np.array([a]))[0] == b, (a, b)
+
+
+def check_row_scale_rule():
+    """The power-of-two row scale is the smallest with max|x| / s <= 448."""
+    cases = {448.0: 0, 449.0: 1, 1.0: -8, 1.75: -8, 1.8: -7, 0.0: 0, 1e-40: -126,
+             3.0e38: 120}
+    for amax, e in cases.items():
+        assert O.row_scale_exponent(amax) == e, (amax, e)
+    for amax in _rng(81).lognormal(0.0, 6.0, size=2000):
+        e = O.row_scale_exponent(amax)
+        assert amax / 2.0 ** e <= 448.0 < amax / 2.0 ** (e - 1)
+    vals, scales = O.quantize_rows_e4m3(np.array([[1.1, 0.5], [0.0, 0.0], [-448.0, 3.0]]))
+    np.testing.assert_array_equal(scales, [2.0 ** -8, 1.0, 1.0])
+    np.testing.assert_array_equal(vals, [[288.0, 128.0], [0.0, 0.0], [-448.0, 3.0]])
+
+
+def check_fp8_layer():
+    """The fp8 layer: a hand-computed one-expert case (the row 1.1, 0.5 is
+    read as 1.125, 0.5), and rows that are already e4m3 values with max 448
+    (scale 1: quantisation is the identity) reduce to the bf16 layer on the
+    dequantised weights."""
+    one = np.array([[[0x38, 0x00]]])          # e4m3 1.0 and 0.0
+    r = O.moe_forward_fp8(np.array([[1.1, 0.5]]), np.ones((1, 2)), one, np.ones((1, 1)),
+                          one, np.ones((1, 1)), np.ones((1, 2, 1)), 1, O.GATE_SOFTMAX_TOPK)
+    g = 1.125
+    assert abs(r.y[0, 0] - g * g / (1 + math.exp(-g))) < 1e-15
+    assert abs(r.y[0, 1] - g * g / (1 + math.exp(-g))) < 1e-15
+    rng = _rng(82)
+    T, d, E, f, k = 12, 16, 4, 8, 2
+    x = O.e4m3_decode(rng.integers(0, 0x7E, size=(T, d)))
+    x[:, 0] = 448.0
+    # codes of magnitudes 2^-5 .. 1 with either sign, small channel scales
+    W1q = rng.integers(0x10, 0x38, size=(E, f, d)) | (rng.integers(0, 2, size=(E, f, d)) << 7)
+    W3q = rng.integers(0x10, 0x38, size=(E, f, d))
+    W1s = rng.uniform(1e-3, 2e-3, size=(E, f)).astype(np.float32)
+    W3s = rng.uniform(1e-3, 2e-3, size=(E, f)).astype(np.float32)
+    W2 = rng.normal(size=(E, d, f))
+    W_r = rng.normal(size=(E, d))
+    a = O.moe_forward_fp8(x, W_r, W1q, W1s, W3q, W3s, W2, k, O.GATE_SOFTMAX_TOPK)
+    b = O.moe_forward(x, W_r, O.dequantize_weights(W1q, W1s), W2, k, O.ACT_SWIGLU,
+                      O.GATE_SOFTMAX_TOPK, W3=O.dequantize_weights(W3q, W3s))
+    np.testing.assert_array_equal(a.y, b.y)
+
+
 ALL_CHECKS = [
     check_router_onehot, check_topk_bruteforce, check_topk_ties, check_gates_closed_form,
     check_gates_invariants, check_router_probs, check_selection_bias,
@@ -484,4 +549,5 @@ ALL_CHECKS = [
     check_sparse_equals_dense, check_drop_is_identity_branch, check_dense_ffn_special_case,
     check_multiply_counts, check_balance_uniform, check_balance_hand_and_collapse,
     check_pipeline_stats_pre_drop, check_z_loss_closed_forms, check_bias_update_rule,
+    check_e4m3_format, check_row_scale_rule, check_fp8_layer,
 ]

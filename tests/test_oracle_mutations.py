@@ -16,7 +16,8 @@ import oracle_pins as P
 _orig = {name: getattr(M, name) for name in (
     "router_logits", "topk_indices", "gate_values", "affinity", "expert_capacity",
     "assign_slots", "gelu_erf", "silu", "expert_ffn_rows", "balance_stats", "router_probs",
-    "softmax_rows", "router_z_loss", "bias_update")}
+    "softmax_rows", "router_z_loss", "bias_update", "e4m3_round", "row_scale_exponent",
+    "quantize_rows_e4m3", "moe_forward_fp8")}
 
 
 def _router_reversed(x, W_r, logit_offset=None):
@@ -158,6 +159,39 @@ def _bias_float64_state(sel_bias, routed, T, k, gamma):
     return b
 
 
+def _e4m3_truncate(v):
+    v = np.asarray(v, dtype=float)
+    a = np.abs(v)
+    _, q = np.frexp(a)
+    quantum = np.where(a >= 2.0 ** -6, np.exp2(q - 4.0), 2.0 ** -9)
+    return np.sign(v) * np.minimum(np.floor(a / quantum) * quantum, 448.0)
+
+
+def _e4m3_ties_away(v):
+    v = np.asarray(v, dtype=float)
+    a = np.abs(v)
+    _, q = np.frexp(a)
+    quantum = np.where(a >= 2.0 ** -6, np.exp2(q - 4.0), 2.0 ** -9)
+    return np.sign(v) * np.minimum(np.floor(a / quantum + 0.5) * quantum, 448.0)
+
+
+def _scale_no_mantissa_check(amax):
+    if not amax > 0.0:
+        return 0
+    _, q = math.frexp(float(amax))
+    return max(q - 9, -126)
+
+
+def _quantize_rows_unit_scale(X):
+    X = np.asarray(X, dtype=float)
+    return _orig["e4m3_round"](X), np.ones(X.shape[0])
+
+
+def _fp8_layer_unquantised_rows(x, W_r, W1q, W1s, W3q, W3s, W2, k, gate_mode, **kw):
+    return M.moe_forward(x, W_r, M.dequantize_weights(W1q, W1s), W2, k, M.ACT_SWIGLU, gate_mode,
+                         W3=M.dequantize_weights(W3q, W3s), **kw)
+
+
 MUTATIONS = [
     ("router expert order reversed", "router_logits", _router_reversed, P.check_router_onehot),
     ("router offset sign flipped", "router_logits", _router_offset_sign, P.check_router_onehot),
@@ -183,6 +217,14 @@ MUTATIONS = [
     ("bias step has the wrong sign", "bias_update", _bias_sign_flipped, P.check_bias_update_rule),
     ("bias mean load ignores k", "bias_update", _bias_mean_ignores_k, P.check_bias_update_rule),
     ("bias state kept in float64", "bias_update", _bias_float64_state, P.check_bias_update_rule),
+    ("e4m3 truncates", "e4m3_round", _e4m3_truncate, P.check_e4m3_format),
+    ("e4m3 ties away from zero", "e4m3_round", _e4m3_ties_away, P.check_e4m3_format),
+    ("row scale ignores the mantissa", "row_scale_exponent", _scale_no_mantissa_check,
+     P.check_row_scale_rule),
+    ("rows quantised without a scale", "quantize_rows_e4m3", _quantize_rows_unit_scale,
+     P.check_row_scale_rule),
+    ("fp8 layer skips the row quantisation", "moe_forward_fp8", _fp8_layer_unquantised_rows,
+     P.check_fp8_layer),
 ]
 
 
