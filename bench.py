@@ -108,7 +108,9 @@ def source_sha():
 def accounting(shape, kept):
     """Algorithmic bytes and FLOPs per launch of each kernel and of the layer,
     from the kept assignments per expert.  Weights count once per active
-    expert; activations at their stored widths (bf16 x/h/y, fp32 o)."""
+    expert (e4m3 gate/up weights at one byte plus a float32 scale per
+    channel); activations at their stored widths (x, h, o, y in the layer
+    dtype; the fp8 variant's quantised rows at one byte)."""
     T, d, E, k, f = shape.T, shape.d, shape.E, shape.k, shape.f
     el = 2 if shape.dtype == "bf16" else 4
     rows = int(sum(kept))
@@ -116,19 +118,23 @@ def accounting(shape, kept):
     sw = shape.act == "swiglu"
     m_up = 2 if sw else 1
     S, fs = shape.n_shared, shape.f_shared
-    w_up = active * m_up * f * d * el + S * 2 * fs * d * el
+    fp8 = getattr(shape, "w_fp8", False)
+    w_el = 1 if fp8 else el                      # bytes per gate/up weight
+    w_up = active * m_up * f * (d * w_el + (4 if fp8 else 0)) + S * 2 * fs * d * el
     w_dn = active * d * f * el + S * d * fs * el
+    a_el = 1 if fp8 else el                      # bytes per up-projection input element
     acc = {
         "router": {"bytes": T * d * el + E * d * el + T * k * 8, "flops": 2 * T * d * E},
         "topk": {"bytes": (2 * T * E + 8 * T * k) * 4, "flops": 0},
-        "permute": {"bytes": 2 * rows * d * el, "flops": 0},
-        "up": {"bytes": w_up + (rows + S * T) * d * el + (rows * f + S * T * fs) * el,
+        # the expert-ordered copy of the rows, or (fp8) their quantisation
+        "permute": {"bytes": rows * d * el + rows * (d * a_el + (4 if fp8 else 0)), "flops": 0},
+        "up": {"bytes": w_up + (rows + S * T) * d * a_el + (rows * f + S * T * fs) * el,
                "flops": 2 * rows * d * f * m_up + S * 2 * T * d * fs * 2},
-        "down": {"bytes": w_dn + (rows * f + S * T * fs) * el + (rows + S * T) * d * 4,
+        "down": {"bytes": w_dn + (rows * f + S * T * fs) * el + (rows + S * T) * d * el,
                  "flops": 2 * rows * f * d + S * 2 * T * fs * d},
-        "combine": {"bytes": (rows + S * T) * d * 4 + T * d * el, "flops": 2 * rows * d},
+        "combine": {"bytes": (rows + S * T) * d * el + T * d * el, "flops": 2 * rows * d},
     }
-    layer_bytes = (active * (m_up + 1) * f * d + S * 3 * fs * d + E * d + 2 * T * d) * el
+    layer_bytes = (w_up + w_dn + E * d * el + 2 * T * d * el)
     layer_flops = 2 * rows * (m_up + 1) * d * f + S * 2 * T * 3 * d * fs + 2 * T * d * E
     return acc, {"bytes": layer_bytes, "flops": layer_flops, "active_experts": active,
                  "kept_rows": rows, "active_weight_bytes": w_up + w_dn}
@@ -311,6 +317,12 @@ def oracle_call(inp, T_s):
 
     s = inp.shape
     x = h(inp.x[:T_s])
+    if inp.W1q is not None:      # e4m3 gate/up weights: the oracle's fp8 variant
+        return O.moe_forward_fp8(x, h(inp.W_r), inp.W1q.cpu().numpy(), inp.W1s.cpu().numpy(),
+                                 inp.W3q.cpu().numpy(), inp.W3s.cpu().numpy(),
+                                 _LazyExpert(inp.W2), s.k, s.gate,
+                                 logit_offset=h(inp.logit_offset), sel_bias=h(inp.sel_bias),
+                                 capacity_factor=s.capacity_factor, alpha=s.alpha)
     W3 = _LazyExpert(inp.W3) if inp.W3 is not None else None
     return O.moe_forward(x, h(inp.W_r), _LazyExpert(inp.W1), _LazyExpert(inp.W2), s.k, s.act,
                          s.gate, W3=W3, logit_offset=h(inp.logit_offset), sel_bias=h(inp.sel_bias),
@@ -357,6 +369,8 @@ def workload_config(shape, extra=None):
          "k": shape.k, "f": shape.f, "act": shape.act, "gate": shape.gate,
          "capacity_factor": shape.capacity_factor or None, "n_shared": shape.n_shared,
          "f_shared": shape.f_shared or None, "alpha": shape.alpha}
+    if getattr(shape, "w_fp8", False):
+        c["expert_weights"] = "gate/up e4m3 + float32 channel scales, down bf16"
     if extra:
         c.update(extra)
     return c
@@ -417,8 +431,8 @@ def run_b300(args):
     inp = W.make_inputs(shape, "cuda")
     cfg = L.config_for(shape)
     stream = torch.cuda.current_stream()
-    fwd = L.BoundForward(cfg, inp.x, inp.W_r, inp.W1, inp.W2, inp.W3, inp.logit_offset,
-                         inp.sel_bias, inp.Ws1, inp.Ws3, inp.Ws2, stream=stream)
+    fwd = L.bound_forward(cfg, inp, stream=stream)
+    fp8 = inp.W1q is not None
     K, Wm = args.steps, args.warmup
     for _ in range(Wm):
         fwd()
@@ -475,7 +489,10 @@ def run_b300(args):
         "active_experts": layer["active_experts"], "kept_rows": layer["kept_rows"]}
 
     e2e = None
-    if not args.no_e2e:
+    if fp8 and not args.no_e2e:
+        e2e = {"value": None, "unavailable": "the host-memory entry point serves the bf16 "
+               "weights only; moe_forward_fp8 takes device tensors"}
+    elif not args.no_e2e:
         x_h = inp.x.cpu().pin_memory()
         y_h = torch.empty_like(x_h).pin_memory()
         aux_h = torch.empty(1, dtype=torch.float32).pin_memory()
@@ -509,15 +526,15 @@ def run_b300(args):
         f"working set {active_w / 1e6:.0f} MB fits L2: numbers include L2 reuse across steps"
     line = {"impl": "b300", "metric": METRIC, "value": round(value, 1), "unit": "tokens/s",
             "n_gpus": world, "steps": K, "warmup": Wm, "ms_per_step": round(ms_step, 5),
-            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16"
-            if shape.dtype == "bf16" else "f32",
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": ("bf16+e4m3" if fp8 else "bf16") if shape.dtype == "bf16" else "f32",
             "data": "synthetic (seeded; the layer shape and input distributions of the workload)",
             "config": workload_config(shape, {"l2": l2_note,
                                               "parallelism": f"replicas x{world}"}),
             "roofline": roof, "layer_roofline": layer_roof,
             "stages_ms": {s: round(v, 5) for s, v in stage_ms.items()},
             "cpu_baseline": cpu, "e2e": e2e,
-            "gpu_launches": K * L.launch_count(cfg), "clocks": clocks.summary(),
+            "gpu_launches": K * L.launch_count(cfg, fp8), "clocks": clocks.summary(),
             "source_sha": source_sha()}
     if rank == 0:
         print(json.dumps(line), flush=True)

@@ -205,6 +205,49 @@ int moe_router_scores_noalloc(const moe_config* cfg, const void* x, const void* 
                               const float* logit_offset, float* scores, void* stream);
 
 /*
+ * moe_forward_fp8 -- moe_forward for a bf16 SwiGLU layer whose gate and up
+ * expert weights are stored as fp8 (e4m3).  The pages use no 8-bit formats;
+ * this variant halves the bytes of the weights that dominate a decode step.
+ *   W1q, W3q  [E, f, d] uint8: e4m3 codes (sign, 4 exponent bits with bias 7,
+ *             3 mantissa bits; the FN encoding, no infinities);
+ *   W1s, W3s  [E, f] float32: one scale per output channel, so that
+ *             W1[e][n][c] = W1s[e][n] * e4m3(W1q[e][n][c]) (likewise W3);
+ *   W2        [E, d, f] bf16, as in moe_forward.
+ * Routing reads x as in moe_forward.  Every routed row of x is quantised to
+ * e4m3 before the up projection: s_t = 2^q with q the smallest integer (not
+ * below -126) such that max_c |x[t][c]| / 2^q <= 448 (s_t = 1 for a zero
+ * row), values x[t][c] / s_t rounded to the nearest e4m3 value, ties to even.
+ * The up projection multiplies e4m3 operands on the tensor cores
+ * (kind::f8f6f4) with float32 accumulation and scales each accumulator by
+ * s_t * W1s[e][n] (resp. W3s) before SwiGLU; h, the down projection and the
+ * combine are those of moe_forward.  Every other argument, output and
+ * convention is moe_forward's.  Requirements: cfg->dtype MOE_BF16, act
+ * MOE_ACT_SWIGLU, n_shared 0, d a multiple of 16, f a multiple of 8, else
+ * MOE_ERR_UNSUPPORTED; W1q, W3q, W1s, W3s 16-byte aligned, else MOE_ERR_ARG.
+ * Needs moe_workspace_size_fp8() bytes of workspace (zeroed header as for
+ * moe_forward).  moe_forward_fp8_timed takes the stage events of
+ * moe_forward_timed (the row quantisation is timed with the permute stage).
+ * moe_launch_count_fp8 gives the kernels one call launches.
+ */
+int moe_workspace_size_fp8(const moe_config* cfg, size_t* bytes);
+int moe_forward_fp8(const moe_config* cfg, const void* x, const void* W_r,
+                    const float* logit_offset, const float* sel_bias,
+                    const uint8_t* W1q, const float* W1s, const uint8_t* W3q, const float* W3s,
+                    const void* W2, void* y, int32_t* topk_idx, float* topk_w,
+                    int32_t* expert_counts, float* aux_loss, int32_t* routed_counts,
+                    int32_t* offsets, int32_t* slot_pos, float* f_out, float* P_out,
+                    void* workspace, size_t workspace_bytes, void* stream);
+int moe_forward_fp8_timed(const moe_config* cfg, const void* x, const void* W_r,
+                          const float* logit_offset, const float* sel_bias,
+                          const uint8_t* W1q, const float* W1s, const uint8_t* W3q,
+                          const float* W3s, const void* W2, void* y, int32_t* topk_idx,
+                          float* topk_w, int32_t* expert_counts, float* aux_loss,
+                          int32_t* routed_counts, int32_t* offsets, int32_t* slot_pos,
+                          float* f_out, float* P_out, void* workspace, size_t workspace_bytes,
+                          void* stream, void* const* events);
+int moe_launch_count_fp8(const moe_config* cfg, int32_t* launches);
+
+/*
  * moe_router_z_loss -- the router z-loss of a batch of router logits:
  *     z_loss[0] = (1/T) * sum_t ( log sum_e exp(scores[t, e]) )^2
  * "Mixture of Experts" (llm-tutorial ch. 11) § Why MoE is hard names the

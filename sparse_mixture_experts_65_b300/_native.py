@@ -31,6 +31,7 @@ EXPORTS = (
     "moe_host_io_workspace_size", "moe_forward_host_io", "moe_check_status",
     "moe_error_string", "moe_forward_timed", "moe_launch_count", "moe_selftest_wait_timeout",
     "moe_router_scores", "moe_router_scores_noalloc", "moe_router_z_loss", "moe_bias_update",
+    "moe_workspace_size_fp8", "moe_forward_fp8", "moe_forward_fp8_timed", "moe_launch_count_fp8",
 )
 
 
@@ -65,7 +66,8 @@ def lib() -> ctypes.CDLL:
                 " (or __graft_entry__.build()); this package has no non-CUDA fallback")
         L = ctypes.CDLL(LIB_PATH)
         cfgp = ctypes.POINTER(MoeConfig)
-        for name in ("moe_workspace_size", "moe_route_workspace_size", "moe_host_io_workspace_size"):
+        for name in ("moe_workspace_size", "moe_route_workspace_size", "moe_host_io_workspace_size",
+                     "moe_workspace_size_fp8"):
             f = getattr(L, name)
             f.argtypes = [cfgp, ctypes.POINTER(SZ)]
             f.restype = ctypes.c_int
@@ -80,6 +82,13 @@ def lib() -> ctypes.CDLL:
         L.moe_forward_host_io.restype = ctypes.c_int
         L.moe_router_scores.argtypes = [cfgp, P, P, P, P, P, SZ, P]
         L.moe_router_scores.restype = ctypes.c_int
+        fp8_args = [cfgp] + [P] * 20 + [SZ, P]
+        L.moe_forward_fp8.argtypes = fp8_args
+        L.moe_forward_fp8.restype = ctypes.c_int
+        L.moe_forward_fp8_timed.argtypes = fp8_args + [ctypes.POINTER(P)]
+        L.moe_forward_fp8_timed.restype = ctypes.c_int
+        L.moe_launch_count_fp8.argtypes = [cfgp, I32P]
+        L.moe_launch_count_fp8.restype = ctypes.c_int
         L.moe_router_z_loss.argtypes = [P, ctypes.c_int32, ctypes.c_int32, P, P]
         L.moe_router_z_loss.restype = ctypes.c_int
         L.moe_bias_update.argtypes = [P, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,

@@ -86,6 +86,9 @@ struct TcArgs {
   const char* gx;         // gathering up projection: x, rows of gx_row_bytes
   int gx_row_bytes;
   int early_b;            // the schedule predates the previous kernel: stream B before the wait
+  const float* a_scale = nullptr;   // fp8 operands: scale of each A row (routed rows) ...
+  const float* b0_scale = nullptr;  // ... and of each output column of B0 / B1, [E][N]
+  const float* b1_scale = nullptr;
   uint32_t* status;
   uint64_t timeout_ns;
 };
@@ -96,15 +99,18 @@ constexpr __host__ __device__ int pow2_at_least(int v) {
   return p;
 }
 
-template <int BNH, bool DUAL, int EPI>
+template <int BNH, bool DUAL, int EPI, bool F8 = false>
 struct TcCfg {
   static constexpr int BM = kTcBM;
-  static constexpr int BK = 64;
+  static constexpr int ELEM = F8 ? 1 : 2;          // bytes per operand element
+  static constexpr int BK = 128 / ELEM;            // k per stage: one 128-byte row
+  static constexpr int BKX = 64;                   // the same in 16-bit tensor-map units
+  static constexpr int KSTEPS = 4;                 // MMAs per stage, 32 bytes of k each
   static constexpr int MMA_N = DUAL ? 2 * BNH : BNH;
   static_assert(MMA_N % 16 == 0 && MMA_N >= 16 && MMA_N <= 256, "tcgen05 N for M=128");
   static_assert(BNH % 32 == 0, "epilogue walks 32-column chunks");
-  static constexpr int A_BYTES = BM * BK * 2;
-  static constexpr int B_BYTES = MMA_N * BK * 2;
+  static constexpr int A_BYTES = BM * 128;
+  static constexpr int B_BYTES = MMA_N * 128;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
   static constexpr int STAGES_FIT = (200 * 1024) / STAGE_BYTES;
   static constexpr int STAGES = STAGES_FIT > 8 ? 8 : STAGES_FIT;
@@ -116,8 +122,11 @@ struct TcCfg {
   static constexpr int SCHED_INTS = 4 * (kMaxE + 2);
   // row -> token tables of the four gathering producer warps (128 each)
   static constexpr int TOK_BYTES = 4 * 128 * 4;
-  static constexpr int SMEM = 1024 + STAGES * STAGE_BYTES + BAR_BYTES + 4 * SCHED_INTS + TOK_BYTES;
-  static constexpr uint32_t IDESC = idesc_bf16_f32(BM, MMA_N);
+  // fp8 operands: the output-column scales of the tile's two B halves
+  static constexpr int CSCALE_BYTES = F8 ? 2 * 128 * 4 : 0;
+  static constexpr int SMEM =
+      1024 + STAGES * STAGE_BYTES + BAR_BYTES + 4 * SCHED_INTS + TOK_BYTES + CSCALE_BYTES;
+  static constexpr uint32_t IDESC = F8 ? idesc_e4m3_f32(BM, MMA_N) : idesc_bf16_f32(BM, MMA_N);
 };
 
 struct TileInfo {
@@ -180,7 +189,7 @@ __device__ __forceinline__ float silu_mul(float g, float u) {
 // Epilogue of one accumulator: activation (or none, or the gate of a top-1
 // combine), bf16 stores of this thread's row, masked at the segment's last
 // row and the last column.
-template <int BNH, bool DUAL, int EPI>
+template <int BNH, bool DUAL, int EPI, bool F8 = false>
 __device__ __forceinline__ void epilogue_tile(const TcArgs& a, const TileInfo& ti, uint32_t t_row,
                                               size_t orow, bool row_ok, float scale) {
 #pragma unroll 1
@@ -199,7 +208,20 @@ __device__ __forceinline__ void epilogue_tile(const TcArgs& a, const TileInfo& t
 #pragma unroll
     for (int i = 0; i < 16; ++i) {
       float v0 = __uint_as_float(r0[2 * i]), v1 = __uint_as_float(r0[2 * i + 1]);
-      if (EPI == EPI_SWIGLU) {
+      if (EPI == EPI_SWIGLU && F8) {
+        // fp8 operands: gate and up accumulators times the row scale and the
+        // column scales of W1 / W3 (N is a multiple of 4: a pair is in range
+        // or out of it as a whole)
+        const int cc = col + 2 * i;
+        float2 sg = make_float2(0.f, 0.f), su = make_float2(0.f, 0.f);
+        if (cc < ti.N) {
+          const size_t si = (size_t)ti.seg * a.N + cc;
+          sg = __ldg(reinterpret_cast<const float2*>(a.b0_scale + si));
+          su = __ldg(reinterpret_cast<const float2*>(a.b1_scale + si));
+        }
+        v0 = silu_mul(v0 * (scale * sg.x), __uint_as_float(r1[2 * i]) * (scale * su.x));
+        v1 = silu_mul(v1 * (scale * sg.y), __uint_as_float(r1[2 * i + 1]) * (scale * su.y));
+      } else if (EPI == EPI_SWIGLU) {
         v0 = silu_mul(v0, __uint_as_float(r1[2 * i]));
         v1 = silu_mul(v1, __uint_as_float(r1[2 * i + 1]));
       } else if (EPI == EPI_RELU) {
@@ -272,14 +294,15 @@ struct TcWarps {
   static constexpr int THREADS = (PROD + 5) * 32;
 };
 
-template <int BNH, bool DUAL, int EPI, bool GATHER>
+template <int BNH, bool DUAL, int EPI, bool GATHER, bool F8 = false>
 __global__ void __launch_bounds__(TcWarps<GATHER>::THREADS, 1)
 tc_grouped_gemm(const __grid_constant__ CUtensorMap mA, const __grid_constant__ CUtensorMap mA_sh,
                 const __grid_constant__ CUtensorMap mA32, const __grid_constant__ CUtensorMap mA32_sh,
                 const __grid_constant__ CUtensorMap mB0, const __grid_constant__ CUtensorMap mB1,
                 const __grid_constant__ CUtensorMap mB0_sh,
                 const __grid_constant__ CUtensorMap mB1_sh, const TcArgs a) {
-  using C = TcCfg<BNH, DUAL, EPI>;
+  using C = TcCfg<BNH, DUAL, EPI, F8>;
+  static_assert(!F8 || (EPI == EPI_SWIGLU && !GATHER), "fp8 operands: SwiGLU up projection");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -372,9 +395,9 @@ tc_grouped_gemm(const __grid_constant__ CUtensorMap mA, const __grid_constant__ 
       for (int kb = 0; kb < nk && npre < (uint32_t)C::STAGES; ++kb, ++npre) {
         const uint32_t sb = smem_base + npre * C::STAGE_BYTES + C::A_BYTES;
         mbar_arrive_expect_tx(full_bar(npre), a_bytes + C::B_BYTES);
-        tma_load_3d(sb, ti.shared ? &mB0_sh : &mB0, full_bar(npre), kb * C::BK, ti.n0, e);
+        tma_load_3d(sb, ti.shared ? &mB0_sh : &mB0, full_bar(npre), kb * C::BKX, ti.n0, e);
         if (DUAL)
-          tma_load_3d(sb + BNH * 128, ti.shared ? &mB1_sh : &mB1, full_bar(npre), kb * C::BK,
+          tma_load_3d(sb + BNH * 128, ti.shared ? &mB1_sh : &mB1, full_bar(npre), kb * C::BKX,
                       ti.n0, e);
       }
     }
@@ -447,15 +470,15 @@ tc_grouped_gemm(const __grid_constant__ CUtensorMap mA, const __grid_constant__ 
             mbar_arrive_expect_tx(full_bar(s), a_bytes + C::B_BYTES);
             if (!gat) {
               if (a_boxes == 0) {
-                tma_load_2d(sa, &mA_sh, full_bar(s), kb * C::BK, ti.a_row);
+                tma_load_2d(sa, &mA_sh, full_bar(s), kb * C::BKX, ti.a_row);
               } else {
                 for (int b = 0; b < a_boxes; ++b)
-                  tma_load_2d(sa + b * kABox * 128, &mA32_sh, full_bar(s), kb * C::BK,
+                  tma_load_2d(sa + b * kABox * 128, &mA32_sh, full_bar(s), kb * C::BKX,
                               ti.a_row + b * kABox);
               }
             }
-            tma_load_3d(sb, pB0, full_bar(s), kb * C::BK, ti.n0, e);
-            if (DUAL) tma_load_3d(sb + BNH * 128, pB1, full_bar(s), kb * C::BK, ti.n0, e);
+            tma_load_3d(sb, pB0, full_bar(s), kb * C::BKX, ti.n0, e);
+            if (DUAL) tma_load_3d(sb + BNH * 128, pB1, full_bar(s), kb * C::BKX, ti.n0, e);
           }
           if (!tok_ready) {
             __syncwarp();
@@ -519,14 +542,14 @@ tc_grouped_gemm(const __grid_constant__ CUtensorMap mA, const __grid_constant__ 
           const uint32_t sb = sa + C::A_BYTES;
           if (!pre) mbar_arrive_expect_tx(full_bar(s), a_bytes + C::B_BYTES);
           if (a_boxes == 0) {
-            tma_load_2d(sa, pA, full_bar(s), kb * C::BK, ti.a_row);
+            tma_load_2d(sa, pA, full_bar(s), kb * C::BKX, ti.a_row);
           } else {
             for (int b = 0; b < a_boxes; ++b)
-              tma_load_2d(sa + b * kABox * 128, pA32, full_bar(s), kb * C::BK, ti.a_row + b * kABox);
+              tma_load_2d(sa + b * kABox * 128, pA32, full_bar(s), kb * C::BKX, ti.a_row + b * kABox);
           }
           if (!pre) {
-            tma_load_3d(sb, pB0, full_bar(s), kb * C::BK, ti.n0, e);
-            if (DUAL) tma_load_3d(sb + BNH * 128, pB1, full_bar(s), kb * C::BK, ti.n0, e);
+            tma_load_3d(sb, pB0, full_bar(s), kb * C::BKX, ti.n0, e);
+            if (DUAL) tma_load_3d(sb + BNH * 128, pB1, full_bar(s), kb * C::BKX, ti.n0, e);
           }
         }
       }
@@ -577,10 +600,13 @@ tc_grouped_gemm(const __grid_constant__ CUtensorMap mA, const __grid_constant__ 
             const uint32_t sa = smem_base + s * C::STAGE_BYTES;
             const uint32_t sb = sa + C::A_BYTES;
 #pragma unroll
-            for (int kk = 0; kk < C::BK / 16; ++kk) {
+            for (int kk = 0; kk < C::KSTEPS; ++kk) {
               const uint64_t ad = smem_desc_k128(sa + kk * 32);
               const uint64_t bd = smem_desc_k128(sb + kk * 32);
-              tc_mma_bf16(d_tmem, ad, bd, C::IDESC, (kb != kb0 || kk != 0) ? 1u : 0u);
+              if constexpr (F8)
+                tc_mma_f8(d_tmem, ad, bd, C::IDESC, (kb != kb0 || kk != 0) ? 1u : 0u);
+              else
+                tc_mma_bf16(d_tmem, ad, bd, C::IDESC, (kb != kb0 || kk != 0) ? 1u : 0u);
             }
             tc_commit(empty_bar(s));
           }
@@ -646,6 +672,9 @@ tc_grouped_gemm(const __grid_constant__ CUtensorMap mA, const __grid_constant__ 
           const int tok = row_ok ? __ldg(a.row_token + orow) : 0;
           const float g = row_ok ? __ldg(a.gate + tok) : 0.f;
           epilogue_tile<BNH, DUAL, EPI>(a, ti, t_row, (size_t)tok, row_ok, g);
+        } else if constexpr (F8) {
+          const float rs = row_ok ? __ldg(a.a_scale + orow) : 0.f;
+          epilogue_tile<BNH, DUAL, EPI, true>(a, ti, t_row, orow, row_ok, rs);
         } else {
           epilogue_tile<BNH, DUAL, EPI>(a, ti, t_row, orow, row_ok, 1.f);
         }
@@ -678,11 +707,11 @@ struct TcMaps {
   CUtensorMap A, A_sh, A32, A32_sh, B0, B1, B0_sh, B1_sh;
 };
 
-template <int BNH, bool DUAL, int EPI, bool GATHER = false>
+template <int BNH, bool DUAL, int EPI, bool GATHER = false, bool F8 = false>
 static cudaError_t run_tc(const TcMaps& m, const TcArgs& a, int grid, cudaStream_t st) {
-  using C = TcCfg<BNH, DUAL, EPI>;
+  using C = TcCfg<BNH, DUAL, EPI, F8>;
   static std::atomic<uint64_t> attr_done{0};
-  auto kern = tc_grouped_gemm<BNH, DUAL, EPI, GATHER>;
+  auto kern = tc_grouped_gemm<BNH, DUAL, EPI, GATHER, F8>;
   cudaError_t e = smem_attr_once(kern, C::SMEM, attr_done);
   if (e != cudaSuccess) return e;
   return launch_pdl(kern, dim3(grid), dim3(TcWarps<GATHER>::THREADS), C::SMEM, st, m.A, m.A_sh,
@@ -714,6 +743,18 @@ static cudaError_t dispatch_up_t(int bn, int act, const TcMaps& m, const TcArgs&
       case 96: return run_tc<96, false, EPI_GELU, GATHER>(m, a, grid, st);
       case 64: return run_tc<64, false, EPI_GELU, GATHER>(m, a, grid, st);
     }
+  }
+  return cudaErrorInvalidValue;
+}
+
+// fp8 (e4m3) A and B: the SwiGLU up projection of a layer with fp8 gate/up weights
+static cudaError_t dispatch_up_f8(int bn, const TcMaps& m, const TcArgs& a, int grid,
+                                  cudaStream_t st) {
+  switch (bn) {
+    case 128: return run_tc<128, true, EPI_SWIGLU, false, true>(m, a, grid, st);
+    case 96: return run_tc<96, true, EPI_SWIGLU, false, true>(m, a, grid, st);
+    case 64: return run_tc<64, true, EPI_SWIGLU, false, true>(m, a, grid, st);
+    case 32: return run_tc<32, true, EPI_SWIGLU, false, true>(m, a, grid, st);
   }
   return cudaErrorInvalidValue;
 }
@@ -751,7 +792,7 @@ constexpr uint64_t kGemmTimeoutNs = 2000000000ull;   // 2 s
 cudaError_t launch_experts_tc(const Plan& p, const void* x, const void* W1, const void* W3,
                               const void* W2, const void* Ws1, const void* Ws3, const void* Ws2,
                               void* ws, cudaStream_t st, cudaEvent_t mid_event, void* y,
-                              const float* topk_w) {
+                              const float* topk_w, const float* W1s, const float* W3s) {
   const moe_config& c = p.cfg;
   char* w = static_cast<char*>(ws);
   const Meta meta = meta_ptrs(p, ws);
@@ -765,13 +806,17 @@ cudaError_t launch_experts_tc(const Plan& p, const void* x, const void* W1, cons
   // xp holds the routed rows of x in expert order: either gathered through
   // row_token inside the kernel, or copied beforehand and read by TMA; the
   // shared expert reads x itself ----
-  const void* a_src = p.gather ? x : static_cast<const void*>(w + p.ws.xp);
+  // (fp8 gate/up weights: A is the e4m3 copy xq of the routed rows, one
+  // scale per row in xs; B holds e4m3 codes with one scale per column)
+  const int el = p.fp8 ? 1 : 2;
+  const void* a_src = p.fp8 ? static_cast<const void*>(w + p.ws.xq)
+                      : p.gather ? x : static_cast<const void*>(w + p.ws.xp);
   const uint64_t a_rows = p.gather ? (uint64_t)c.T : (uint64_t)p.R_cap;
   TcMaps mu;
-  bool ok = encode_2d(&mu.A, a_src, a_rows, c.d, kTcBM);
-  ok = ok && encode_2d(&mu.A32, a_src, a_rows, c.d, kABox);
-  ok = ok && encode_3d(&mu.B0, W1, c.E, c.f, c.d, p.up_bn);
-  ok = ok && encode_3d(&mu.B1, dual ? W3 : W1, c.E, c.f, c.d, p.up_bn);
+  bool ok = encode_2d(&mu.A, a_src, a_rows, c.d, kTcBM, el);
+  ok = ok && encode_2d(&mu.A32, a_src, a_rows, c.d, kABox, el);
+  ok = ok && encode_3d(&mu.B0, W1, c.E, c.f, c.d, p.up_bn, el);
+  ok = ok && encode_3d(&mu.B1, dual ? W3 : W1, c.E, c.f, c.d, p.up_bn, el);
   if (sh) {
     ok = ok && encode_2d(&mu.A_sh, x, c.T, c.d, kTcBM);
     ok = ok && encode_2d(&mu.A32_sh, x, c.T, c.d, kABox);
@@ -798,6 +843,9 @@ cudaError_t launch_experts_tc(const Plan& p, const void* x, const void* W1, cons
   au.gx = static_cast<const char*>(x);
   au.gx_row_bytes = c.d * 2;
   au.early_b = 0;
+  au.a_scale = p.fp8 ? reinterpret_cast<const float*>(w + p.ws.xs) : nullptr;
+  au.b0_scale = W1s;
+  au.b1_scale = W3s;
   au.gate = nullptr;
   au.y = nullptr;
   au.ld_y = 0;
@@ -816,7 +864,8 @@ cudaError_t launch_experts_tc(const Plan& p, const void* x, const void* W1, cons
   au.status = status;
   au.timeout_ns = kGemmTimeoutNs;
   const int grid_up = p.max_tiles_up < p.num_sms ? p.max_tiles_up : p.num_sms;
-  cudaError_t e = dispatch_up(p.gather, p.up_bn, c.act, mu, au, grid_up, st);
+  cudaError_t e = p.fp8 ? dispatch_up_f8(p.up_bn, mu, au, grid_up, st)
+                        : dispatch_up(p.gather, p.up_bn, c.act, mu, au, grid_up, st);
   if (e != cudaSuccess) return e;
   if (mid_event) {
     e = cudaEventRecord(mid_event, st);

@@ -62,6 +62,13 @@ int make_plan(const moe_config* cfg, WsKind kind, Plan* p, int num_sms) {
   // the tensor-core kernels run the (SwiGLU) shared expert as one more
   // segment of the routed experts' launches, so they need SwiGLU experts too
   if (c.dtype == MOE_BF16 && c.n_shared && c.act != MOE_ACT_SWIGLU) return MOE_ERR_UNSUPPORTED;
+  // fp8 gate/up weights: a bf16 SwiGLU layer without a shared expert; rows of
+  // d e4m3 bytes must be 16-byte multiples (TMA) and the column scales are
+  // read in pairs
+  if (kind == WsKind::ForwardFp8 &&
+      (c.dtype != MOE_BF16 || c.act != MOE_ACT_SWIGLU || c.n_shared != 0 || c.d % 16 ||
+       c.f % 4))
+    return MOE_ERR_UNSUPPORTED;
   // every row index and element count of one matrix must fit in int32 / the TMA limits
   const long long Tk = (long long)c.T * c.k;
   if (Tk > (1LL << 30) || (long long)c.T * c.d > (1LL << 40)) return MOE_ERR_UNSUPPORTED;
@@ -69,6 +76,7 @@ int make_plan(const moe_config* cfg, WsKind kind, Plan* p, int num_sms) {
   Plan& P = *p;
   std::memset(&P, 0, sizeof(P));
   P.cfg = c;
+  P.fp8 = kind == WsKind::ForwardFp8;
   P.elem = c.dtype == MOE_BF16 ? 2 : 4;
   if (c.capacity_factor > 0) {
     const double cap = std::ceil(static_cast<double>(Tk) * c.capacity_factor / c.E);
@@ -211,6 +219,7 @@ int make_plan(const moe_config* cfg, WsKind kind, Plan* p, int num_sms) {
     P.gather = P.tc && P.route_tc && per_expert <= kTcBM;
     const char* gv = std::getenv("MOE_GATHER");
     if (gv && P.tc) P.gather = std::atoi(gv) != 0;
+    if (P.fp8) P.gather = false;   // the fp8 up projection reads the quantised rows by TMA
   }
   P.nt_up = ceil_div(c.f, P.up_bn);
   P.nt_dn = ceil_div(c.d, P.dn_bn);
@@ -246,7 +255,9 @@ int make_plan(const moe_config* cfg, WsKind kind, Plan* p, int num_sms) {
   L.row_token = take(sizeof(int) * (size_t)P.R_cap);
   if (kind != WsKind::Route) {
     const size_t act_elem = P.elem;   // h is bf16 on the tensor-core path, fp32 otherwise
-    L.xp = take(P.gather ? 0 : (size_t)P.R_cap * c.d * P.elem);
+    L.xp = take(P.gather || P.fp8 ? 0 : (size_t)P.R_cap * c.d * P.elem);
+    L.xq = take(P.fp8 ? (size_t)P.R_cap * c.d : 0);
+    L.xs = take(P.fp8 ? (size_t)P.R_cap * sizeof(float) : 0);
     L.h = take((size_t)P.R_cap * c.f * act_elem);
     // expert outputs in the layer dtype: bf16 rounded once from the float32
     // accumulator on the tensor-core path, float32 otherwise
@@ -307,6 +318,7 @@ struct Tensors {
   float* aux_loss;
   int32_t *routed_counts, *offsets, *slot_pos;
   float *f_out, *P_out;
+  const float *W1s = nullptr, *W3s = nullptr;   // fp8 gate/up weights: column scales
 };
 
 static int check_tensors(const moe_config& c, const Tensors& t, bool route_only) {
@@ -320,6 +332,8 @@ static int check_tensors(const moe_config& c, const Tensors& t, bool route_only)
   if (!t.W1 || !t.W2 || (!empty && !t.y)) return MOE_ERR_ARG;
   if (!aligned16(t.W1) || !aligned16(t.W2) || !aligned16(t.y)) return MOE_ERR_ARG;
   if (c.act == MOE_ACT_SWIGLU ? (!t.W3 || !aligned16(t.W3)) : t.W3 != nullptr) return MOE_ERR_ARG;
+  if ((t.W1s != nullptr) != (t.W3s != nullptr)) return MOE_ERR_ARG;
+  if (t.W1s && (!aligned16(t.W1s) || !aligned16(t.W3s))) return MOE_ERR_ARG;
   if (c.n_shared) {
     if (!t.Ws1 || !t.Ws3 || !t.Ws2) return MOE_ERR_ARG;
     if (!aligned16(t.Ws1) || !aligned16(t.Ws3) || !aligned16(t.Ws2)) return MOE_ERR_ARG;
@@ -365,6 +379,7 @@ static int forward_impl(const moe_config* cfg, const Tensors& t, void* ws, size_
   if (rc != MOE_OK) return rc;
   rc = check_tensors(*cfg, t, route_only);
   if (rc != MOE_OK) return rc;
+  if (p.fp8 != (t.W1s != nullptr)) return MOE_ERR_ARG;   // fp8 weights come with their scales
   rc = check_workspace(p, ws, ws_bytes);
   if (rc != MOE_OK) return rc;
   int sms = 0;
@@ -379,10 +394,13 @@ static int forward_impl(const moe_config* cfg, const Tensors& t, void* ws, size_
 
   if ((rc = record(events, MOE_STAGE_ROUTER, st)) != MOE_OK) return rc;
   const ScanOutputs so{t.expert_counts, t.aux_loss, t.routed_counts, t.offsets, t.f_out, t.P_out};
+  // expert-ordered bf16 copies of the rows, unless the up projection gathers
+  // them or reads their e4m3 form
+  const bool copy = !route_only && !p.gather && !p.fp8;
   if (p.route_small) {
     // stages 1-4 in one launch for a decode batch; top-k and permute are empty
     MOE_TRY_CUDA(launch_route_small(p, t.x, t.W_r, t.logit_offset, t.sel_bias, t.topk_idx,
-                                    t.topk_w, t.slot_pos, !route_only && !p.gather, ws, so, st));
+                                    t.topk_w, t.slot_pos, copy, ws, so, st));
     if ((rc = record(events, MOE_STAGE_TOPK, st)) != MOE_OK) return rc;
     if ((rc = record(events, MOE_STAGE_PERMUTE, st)) != MOE_OK) return rc;
   } else if (p.route_tc) {
@@ -391,22 +409,22 @@ static int forward_impl(const moe_config* cfg, const Tensors& t, void* ws, size_
                                  t.slot_pos, ws, so, st));
     if ((rc = record(events, MOE_STAGE_TOPK, st)) != MOE_OK) return rc;
     if ((rc = record(events, MOE_STAGE_PERMUTE, st)) != MOE_OK) return rc;
-    if (!route_only && !p.gather) MOE_TRY_CUDA(launch_gather_rows(p, t.x, ws, st));
+    if (copy) MOE_TRY_CUDA(launch_gather_rows(p, t.x, ws, st));
   } else {
     cudaEvent_t topk_ev = events ? static_cast<cudaEvent_t>(events[MOE_STAGE_TOPK]) : nullptr;
     MOE_TRY_CUDA(launch_router(p, t.x, t.W_r, t.logit_offset, t.sel_bias, t.topk_idx, t.topk_w,
                                ws, so, st, topk_ev));
     if ((rc = record(events, MOE_STAGE_PERMUTE, st)) != MOE_OK) return rc;
     // the expert-ordered copies (unless the up projection gathers rows)
-    MOE_TRY_CUDA(
-        launch_permute(p, t.x, t.topk_idx, t.slot_pos, !route_only && !p.gather, ws, st, t.y));
+    MOE_TRY_CUDA(launch_permute(p, t.x, t.topk_idx, t.slot_pos, copy, ws, st, t.y));
   }
   if (route_only) return MOE_OK;
+  if (p.fp8) MOE_TRY_CUDA(launch_quant_rows(p, t.x, ws, st));
   if ((rc = record(events, MOE_STAGE_UP, st)) != MOE_OK) return rc;
   cudaEvent_t mid = events ? static_cast<cudaEvent_t>(events[MOE_STAGE_DOWN]) : nullptr;
   if (p.tc)
     MOE_TRY_CUDA(launch_experts_tc(p, t.x, t.W1, t.W3, t.W2, t.Ws1, t.Ws3, t.Ws2, ws, st, mid,
-                                   t.y, t.topk_w));
+                                   t.y, t.topk_w, t.W1s, t.W3s));
   else
     MOE_TRY_CUDA(launch_experts_simt(p, t.x, t.W1, t.W3, t.W2, t.Ws1, t.Ws3, t.Ws2, ws, st, mid));
   if ((rc = record(events, MOE_STAGE_COMBINE, st)) != MOE_OK) return rc;
@@ -469,6 +487,42 @@ int moe_forward(const moe_config* cfg, const void* x, const void* W_r, const flo
   return moe_forward_timed(cfg, x, W_r, logit_offset, sel_bias, W1, W3, W2, Ws1, Ws3, Ws2, y,
                            topk_idx, topk_w, expert_counts, aux_loss, routed_counts, offsets,
                            slot_pos, f_out, P_out, workspace, workspace_bytes, stream, nullptr);
+}
+
+int moe_workspace_size_fp8(const moe_config* cfg, size_t* bytes) {
+  if (!bytes) return MOE_ERR_ARG;
+  Plan p;
+  const int rc = make_plan(cfg, WsKind::ForwardFp8, &p);
+  if (rc == MOE_OK) *bytes = p.ws.total;
+  return rc;
+}
+
+int moe_forward_fp8_timed(const moe_config* cfg, const void* x, const void* W_r,
+                          const float* logit_offset, const float* sel_bias, const uint8_t* W1q,
+                          const float* W1s, const uint8_t* W3q, const float* W3s, const void* W2,
+                          void* y, int32_t* topk_idx, float* topk_w, int32_t* expert_counts,
+                          float* aux_loss, int32_t* routed_counts, int32_t* offsets,
+                          int32_t* slot_pos, float* f_out, float* P_out, void* workspace,
+                          size_t workspace_bytes, void* stream, void* const* events) {
+  if (!W1s || !W3s) return MOE_ERR_ARG;
+  Tensors t{x,  W_r, logit_offset, sel_bias, W1q,     W3q,     W2,      nullptr,  nullptr, nullptr,
+            y,  topk_idx, topk_w, expert_counts, aux_loss, routed_counts, offsets, slot_pos,
+            f_out, P_out, W1s, W3s};
+  return forward_impl(cfg, t, workspace, workspace_bytes, static_cast<cudaStream_t>(stream),
+                      events, false, WsKind::ForwardFp8);
+}
+
+int moe_forward_fp8(const moe_config* cfg, const void* x, const void* W_r,
+                    const float* logit_offset, const float* sel_bias, const uint8_t* W1q,
+                    const float* W1s, const uint8_t* W3q, const float* W3s, const void* W2,
+                    void* y, int32_t* topk_idx, float* topk_w, int32_t* expert_counts,
+                    float* aux_loss, int32_t* routed_counts, int32_t* offsets, int32_t* slot_pos,
+                    float* f_out, float* P_out, void* workspace, size_t workspace_bytes,
+                    void* stream) {
+  return moe_forward_fp8_timed(cfg, x, W_r, logit_offset, sel_bias, W1q, W1s, W3q, W3s, W2, y,
+                               topk_idx, topk_w, expert_counts, aux_loss, routed_counts, offsets,
+                               slot_pos, f_out, P_out, workspace, workspace_bytes, stream,
+                               nullptr);
 }
 
 int moe_route(const moe_config* cfg, const void* x, const void* W_r, const float* logit_offset,
@@ -574,6 +628,18 @@ int moe_launch_count(const moe_config* cfg, int32_t* launches) {
                       : p.route_tc  ? (p.gather ? 1 : 2)
                                     : (p.router_fused ? 2 : 3);
   *launches = cfg->T == 0 ? 0 : routing + 2 + (p.combine_in_down ? 0 : 1);
+  return MOE_OK;
+}
+
+int moe_launch_count_fp8(const moe_config* cfg, int32_t* launches) {
+  if (!launches) return MOE_ERR_ARG;
+  Plan p;
+  const int rc = make_plan(cfg, WsKind::ForwardFp8, &p);
+  if (rc != MOE_OK) return rc;
+  // routing without a row copy, the row quantisation, the two projections
+  // and the combine (folded into the down projection for top-1 layers)
+  const int routing = p.route_small || p.route_tc ? 1 : (p.router_fused ? 2 : 3);
+  *launches = cfg->T == 0 ? 0 : routing + 1 + 2 + (p.combine_in_down ? 0 : 1);
   return MOE_OK;
 }
 

@@ -50,6 +50,8 @@ struct WsLayout {
   size_t row_token;   // int32  [R_cap]    token of each expert-ordered row
   size_t xp;          // dtype  [R_cap][d] token copies in expert order (absent when the
                       //        tensor-core up projection gathers the rows of x itself)
+  size_t xq;          // uint8  [R_cap][d] e4m3 token rows in expert order (fp8 weights only)
+  size_t xs;          // float  [R_cap]    their power-of-two scales
   size_t h;           // dtype  [R_cap][f] expert hidden activations
   size_t o;           // dtype  [R_cap][d] expert outputs
   size_t hs;          // dtype  [T_pad][f_s] shared-expert hidden
@@ -87,11 +89,12 @@ struct Plan {
   int partial_rows_up;        // the same for the up projection
   bool combine_in_down;       // top-1, no shared expert, bf16: y written by the down epilogue
   bool gather;                // the up projection gathers token rows (no expert-ordered copy)
+  bool fp8;                   // gate/up weights in e4m3: quantised rows, fp8 up projection
   int num_sms;
   WsLayout ws;
 };
 
-enum class WsKind { Forward, Route, HostIO };
+enum class WsKind { Forward, Route, HostIO, ForwardFp8 };
 
 int make_plan(const moe_config* cfg, WsKind kind, Plan* p);
 
@@ -144,7 +147,9 @@ cudaError_t launch_permute(const Plan& p, const void* x, const int32_t* topk_idx
 cudaError_t launch_experts_tc(const Plan& p, const void* x, const void* W1, const void* W3,
                               const void* W2, const void* Ws1, const void* Ws3, const void* Ws2,
                               void* ws, cudaStream_t st, cudaEvent_t mid_event, void* y,
-                              const float* topk_w);
+                              const float* topk_w, const float* W1s = nullptr,
+                              const float* W3s = nullptr);
+cudaError_t launch_quant_rows(const Plan& p, const void* x, void* ws, cudaStream_t st);
 cudaError_t launch_experts_simt(const Plan& p, const void* x, const void* W1, const void* W3,
                                 const void* W2, const void* Ws1, const void* Ws3,
                                 const void* Ws2, void* ws, cudaStream_t st,

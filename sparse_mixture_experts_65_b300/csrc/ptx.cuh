@@ -177,6 +177,18 @@ __device__ __forceinline__ void tc_mma_bf16(uint32_t d_tmem, uint64_t a_desc, ui
       : "memory");
 }
 
+// D[tmem] (+)= A[smem] * B[smem]^T, both operands fp8 (e4m3), fp32
+// accumulation; one instruction covers K = 32 (32 bytes of each row).
+__device__ __forceinline__ void tc_mma_f8(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                          uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}"
+      ::"r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
 // Arrive once on `bar` when every tcgen05.mma issued so far by this thread
 // has completed.
 __device__ __forceinline__ void tc_commit(uint32_t bar) {
@@ -215,6 +227,14 @@ __device__ __forceinline__ uint64_t smem_desc_k128(uint32_t saddr) {
   desc |= static_cast<uint64_t>(1u) << 46;                       // descriptor version
   desc |= static_cast<uint64_t>(2u) << 61;                       // 128-byte swizzle
   return desc;
+}
+
+// Instruction descriptor of kind::f8f6f4: e4m3 x e4m3 -> fp32 (A and B format
+// fields 0 = E4M3), both operands K-major.
+__host__ __device__ constexpr uint32_t idesc_e4m3_f32(int M, int N) {
+  return (1u << 4)                                   // D format: f32
+         | (static_cast<uint32_t>(N >> 3) << 17)     // N / 8
+         | (static_cast<uint32_t>(M >> 4) << 24);    // M / 16
 }
 
 // Instruction descriptor: bf16 x bf16 -> fp32, both operands K-major.

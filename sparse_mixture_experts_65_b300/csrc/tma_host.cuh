@@ -29,31 +29,39 @@ inline EncodeTiledFn get_encode_fn() {
   return fn;
 }
 
-// 2-D map over a row-major [rows][cols] bf16 matrix, box 64 cols x box_rows.
+// Every map moves 16-bit units: bf16 values, or pairs of fp8 bytes (a map
+// of `elem` = 1 covers cols / 2 units per row; cols must be even).  The box
+// is 64 units = 128 bytes of a row wide; x coordinates count 16-bit units.
+inline CUtensorMapDataType map_type(int elem) {
+  return elem == 1 ? CU_TENSOR_MAP_DATA_TYPE_UINT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+}
+
+// 2-D map over a row-major [rows][cols] matrix of `elem`-byte elements, box
+// 128 bytes of columns x box_rows, 128-byte swizzle.
 inline bool encode_2d(CUtensorMap* m, const void* ptr, uint64_t rows, uint64_t cols,
-                      uint32_t box_rows) {
+                      uint32_t box_rows, int elem = 2) {
   EncodeTiledFn fn = get_encode_fn();
   if (!fn) return false;
-  cuuint64_t dims[2] = {cols, rows};
-  cuuint64_t strides[1] = {cols * 2};
-  cuuint32_t box[2] = {64, box_rows};
+  cuuint64_t dims[2] = {cols * (uint64_t)elem / 2, rows};
+  cuuint64_t strides[1] = {cols * (uint64_t)elem};
+  cuuint32_t box[2] = {64u, box_rows};
   cuuint32_t es[2] = {1, 1};
-  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box,
-            es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+  return fn(m, map_type(elem), 2, const_cast<void*>(ptr), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// 3-D map over [n_mat][rows][cols] bf16, box 64 cols x box_rows x 1.
+// 3-D map over [n_mat][rows][cols], box 128 bytes of columns x box_rows x 1.
 inline bool encode_3d(CUtensorMap* m, const void* ptr, uint64_t n_mat, uint64_t rows,
-                      uint64_t cols, uint32_t box_rows) {
+                      uint64_t cols, uint32_t box_rows, int elem = 2) {
   EncodeTiledFn fn = get_encode_fn();
   if (!fn) return false;
-  cuuint64_t dims[3] = {cols, rows, n_mat};
-  cuuint64_t strides[2] = {cols * 2, rows * cols * 2};
-  cuuint32_t box[3] = {64, box_rows, 1};
+  cuuint64_t dims[3] = {cols * (uint64_t)elem / 2, rows, n_mat};
+  cuuint64_t strides[2] = {cols * (uint64_t)elem, rows * cols * (uint64_t)elem};
+  cuuint32_t box[3] = {64u, box_rows, 1};
   cuuint32_t es[3] = {1, 1, 1};
-  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides, box,
-            es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+  return fn(m, map_type(elem), 3, const_cast<void*>(ptr), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 

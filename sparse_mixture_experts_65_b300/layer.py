@@ -53,7 +53,8 @@ def _stream_handle(stream: Optional[torch.cuda.Stream]):
 def workspace_size(cfg: N.MoeConfig, kind: str = "forward") -> int:
     n = ctypes.c_size_t(0)
     fn = {"forward": N.lib().moe_workspace_size, "route": N.lib().moe_route_workspace_size,
-          "host_io": N.lib().moe_host_io_workspace_size}[kind]
+          "host_io": N.lib().moe_host_io_workspace_size,
+          "fp8": N.lib().moe_workspace_size_fp8}[kind]
     N.check(fn(ctypes.byref(cfg), ctypes.byref(n)), "moe_workspace_size")
     return n.value
 
@@ -70,9 +71,10 @@ def alloc_workspace(cfg: N.MoeConfig, device="cuda", kind: str = "forward") -> t
     return ws
 
 
-def launch_count(cfg: N.MoeConfig) -> int:
+def launch_count(cfg: N.MoeConfig, fp8: bool = False) -> int:
     n = ctypes.c_int32(0)
-    N.check(N.lib().moe_launch_count(ctypes.byref(cfg), ctypes.byref(n)), "moe_launch_count")
+    fn = N.lib().moe_launch_count_fp8 if fp8 else N.lib().moe_launch_count
+    N.check(fn(ctypes.byref(cfg), ctypes.byref(n)), "moe_launch_count")
     return n.value
 
 
@@ -128,6 +130,17 @@ def forward(cfg: N.MoeConfig, x, W_r, W1, W2, W3=None, logit_offset=None, sel_bi
         rc = N.lib().moe_forward_timed(*args, BoundForward.event_array(events, stream))
     N.check(rc, "moe_forward")
     return out
+
+
+def forward_fp8(cfg: N.MoeConfig, x, W_r, W1q, W1s, W3q, W3s, W2, logit_offset=None,
+                sel_bias=None, out: Optional[MoeOutputs] = None,
+                workspace: Optional[torch.Tensor] = None, stream=None) -> MoeOutputs:
+    """One call of moe_forward_fp8: e4m3 gate/up weights (uint8 codes) with
+    float32 channel scales, bf16 down weights."""
+    b = BoundForwardFp8(cfg, x, W_r, W1q, W1s, W3q, W3s, W2, logit_offset, sel_bias, out,
+                        workspace, stream)
+    b()
+    return b.out
 
 
 def route(cfg: N.MoeConfig, x, W_r, logit_offset=None, sel_bias=None,
@@ -252,6 +265,38 @@ class BoundForward:
         for e in events:
             e.record(s)
         return (ctypes.c_void_p * len(events))(*[ctypes.c_void_p(e.cuda_event) for e in events])
+
+
+class BoundForwardFp8(BoundForward):
+    """moe_forward_fp8 with every argument marshalled once."""
+
+    def __init__(self, cfg: N.MoeConfig, x, W_r, W1q, W1s, W3q, W3s, W2, logit_offset=None,
+                 sel_bias=None, out: Optional[MoeOutputs] = None,
+                 workspace: Optional[torch.Tensor] = None, stream=None):
+        self.cfg = cfg
+        self.out = out if out is not None else alloc_outputs(cfg, x.device, x.dtype)
+        self.workspace = (workspace if workspace is not None
+                          else alloc_workspace(cfg, x.device, "fp8"))
+        self._keep = (x, W_r, W1q, W1s, W3q, W3s, W2, logit_offset, sel_bias)
+        o = self.out
+        self.args = (ctypes.byref(cfg), _ptr(x), _ptr(W_r), _ptr(logit_offset), _ptr(sel_bias),
+                     _ptr(W1q), _ptr(W1s), _ptr(W3q), _ptr(W3s), _ptr(W2),
+                     _ptr(o.y), _ptr(o.topk_idx), _ptr(o.topk_w), _ptr(o.expert_counts),
+                     _ptr(o.aux_loss), _ptr(o.routed_counts), _ptr(o.offsets), _ptr(o.slot_pos),
+                     _ptr(o.f), _ptr(o.P), _ptr(self.workspace),
+                     ctypes.c_size_t(self.workspace.numel()), _stream_handle(stream))
+        self._fwd = N.lib().moe_forward_fp8
+        self._timed = N.lib().moe_forward_fp8_timed
+
+
+def bound_forward(cfg: N.MoeConfig, inp, stream=None, workspace=None) -> BoundForward:
+    """The bound call for a workload's inputs (fp8 gate/up weights or not)."""
+    if getattr(inp, "W1q", None) is not None:
+        return BoundForwardFp8(cfg, inp.x, inp.W_r, inp.W1q, inp.W1s, inp.W3q, inp.W3s, inp.W2,
+                               inp.logit_offset, inp.sel_bias, workspace=workspace, stream=stream)
+    return BoundForward(cfg, inp.x, inp.W_r, inp.W1, inp.W2, inp.W3, inp.logit_offset,
+                        inp.sel_bias, inp.Ws1, inp.Ws3, inp.Ws2, workspace=workspace,
+                        stream=stream)
 
 
 class BoundHostIO:

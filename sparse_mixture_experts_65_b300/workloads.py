@@ -44,6 +44,7 @@ class LayerShape:
     f_shared: int = 0
     logit_offset_var: float = 0.0       # variance of a per-expert logit skew
     sel_bias_halfwidth: float = 0.0     # sel bias ~ U(-h, h)
+    w_fp8: bool = False                 # gate/up expert weights as e4m3 codes + channel scales
 
     def with_T(self, T: int) -> "LayerShape":
         return replace(self, T=T)
@@ -68,6 +69,11 @@ WORKLOADS = {w.name: w for w in (TOY, SWITCH, MIXTRAL, DSV3, GPTOSS)}
 
 
 def get(name: str) -> LayerShape:
+    """A named workload; the suffix "_fp8" gives the same layer with e4m3
+    gate/up expert weights (SwiGLU layers)."""
+    if name.endswith("_fp8"):
+        base = get(name[:-len("_fp8")])
+        return replace(base, name=base.name + "_fp8", w_fp8=True)
     if name.startswith("gptoss") and name != "gptoss":
         return GPTOSS.with_T(int(name[len("gptoss"):].lstrip("_T")))
     return WORKLOADS[name]
@@ -109,13 +115,36 @@ class LayerInputs:
     Ws1: Optional[torch.Tensor] = None   # [f_s, d]
     Ws3: Optional[torch.Tensor] = None   # [f_s, d]
     Ws2: Optional[torch.Tensor] = None   # [d, f_s]
+    # e4m3 gate/up weights (W1, W3 are None then): codes [E, f, d] uint8 and
+    # one float32 scale per output channel [E, f]
+    W1q: Optional[torch.Tensor] = None
+    W1s: Optional[torch.Tensor] = None
+    W3q: Optional[torch.Tensor] = None
+    W3s: Optional[torch.Tensor] = None
 
     def weight_bytes(self) -> int:
         n = 0
-        for t in (self.W_r, self.W1, self.W2, self.W3, self.Ws1, self.Ws3, self.Ws2):
+        for t in (self.W_r, self.W1, self.W2, self.W3, self.Ws1, self.Ws3, self.Ws2, self.W1q,
+                  self.W1s, self.W3q, self.W3s):
             if t is not None:
                 n += t.numel() * t.element_size()
         return n
+
+
+def _fp8_channels(shape3, std, g, device):
+    """std * N(0,1) drawn in fp32 (slice by slice, the stream of _normal with
+    chunk_dim0), then stored per output channel (row) as e4m3 codes and a
+    float32 scale amax / 448, the codes rounded to nearest by torch's float8
+    conversion: input preparation, not the layer's arithmetic."""
+    E, n, c = shape3
+    codes = torch.empty(shape3, device=device, dtype=torch.uint8)
+    scales = torch.empty((E, n), device=device, dtype=torch.float32)
+    for i in range(E):
+        w = torch.randn((n, c), generator=g, device=device, dtype=torch.float32) * std
+        s = w.abs().amax(dim=1).clamp_min(1e-30) / 448.0
+        scales[i] = s
+        codes[i] = (w / s[:, None]).to(torch.float8_e4m3fn).view(torch.uint8)
+    return codes, scales
 
 
 def make_x(shape: LayerShape, device="cpu", seed: int = 0) -> torch.Tensor:
@@ -134,10 +163,15 @@ def make_inputs(shape: LayerShape, device="cpu", seed: int = 0) -> LayerInputs:
     big = E * f * d > (1 << 26)
     x = make_x(shape, device, seed)
     W_r = _normal((E, d), 1.0 / math.sqrt(d), _gen(device, base + 1), device, dt)
-    W1 = _normal((E, f, d), 1.0 / math.sqrt(d), _gen(device, base + 2), device, dt, big)
+    W1 = W3 = W1q = W1s = W3q = W3s = None
+    if shape.w_fp8:
+        W1q, W1s = _fp8_channels((E, f, d), 1.0 / math.sqrt(d), _gen(device, base + 2), device)
+    else:
+        W1 = _normal((E, f, d), 1.0 / math.sqrt(d), _gen(device, base + 2), device, dt, big)
     W2 = _normal((E, d, f), 1.0 / math.sqrt(f), _gen(device, base + 3), device, dt, big)
-    W3 = None
-    if shape.act == ACT_SWIGLU:
+    if shape.act == ACT_SWIGLU and shape.w_fp8:
+        W3q, W3s = _fp8_channels((E, f, d), 1.0 / math.sqrt(d), _gen(device, base + 4), device)
+    elif shape.act == ACT_SWIGLU:
         W3 = _normal((E, f, d), 1.0 / math.sqrt(d), _gen(device, base + 4), device, dt, big)
     logit_offset = None
     if shape.logit_offset_var > 0:
@@ -153,7 +187,8 @@ def make_inputs(shape: LayerShape, device="cpu", seed: int = 0) -> LayerInputs:
         Ws1 = _normal((fs, d), 1.0 / math.sqrt(d), _gen(device, base + 7), device, dt)
         Ws3 = _normal((fs, d), 1.0 / math.sqrt(d), _gen(device, base + 8), device, dt)
         Ws2 = _normal((d, fs), 1.0 / math.sqrt(fs), _gen(device, base + 9), device, dt)
-    return LayerInputs(shape, x, W_r, W1, W2, W3, logit_offset, sel_bias, Ws1, Ws3, Ws2)
+    return LayerInputs(shape, x, W_r, W1, W2, W3, logit_offset, sel_bias, Ws1, Ws3, Ws2,
+                       W1q, W1s, W3q, W3s)
 
 
 def make_logits(T: int, E: int, seed: int, scale: float = 1.0, shift: float = 0.0,

@@ -48,8 +48,12 @@ class LazyExperts:
 
 def run_gpu(inp, cfg=None, workspace=None):
     cfg = cfg if cfg is not None else L.config_for(inp.shape)
-    out = L.forward(cfg, inp.x, inp.W_r, inp.W1, inp.W2, inp.W3, inp.logit_offset, inp.sel_bias,
-                    inp.Ws1, inp.Ws3, inp.Ws2, workspace=workspace)
+    if inp.W1q is not None:
+        out = L.forward_fp8(cfg, inp.x, inp.W_r, inp.W1q, inp.W1s, inp.W3q, inp.W3s, inp.W2,
+                            inp.logit_offset, inp.sel_bias, workspace=workspace)
+    else:
+        out = L.forward(cfg, inp.x, inp.W_r, inp.W1, inp.W2, inp.W3, inp.logit_offset,
+                        inp.sel_bias, inp.Ws1, inp.Ws3, inp.Ws2, workspace=workspace)
     torch.cuda.synchronize()
     return cfg, out
 
@@ -68,6 +72,23 @@ def near_tie_mask(sel, k):
 def rel_l2(a, b):
     den = np.linalg.norm(b)
     return float(np.linalg.norm(a - b) / den) if den > 0 else float(np.linalg.norm(a - b))
+
+
+class LazyFp8Experts:
+    """e4m3 expert weights (codes + channel scales) dequantised to float64,
+    one expert at a time."""
+
+    def __init__(self, codes, scales):
+        self.codes, self.scales = codes, scales
+        self._e = None
+        self._v = None
+
+    def __getitem__(self, e):
+        if self._e != e:
+            self._v = O.dequantize_weights(self.codes[e].cpu().numpy(),
+                                           self.scales[e].cpu().numpy())
+            self._e = e
+        return self._v
 
 
 def check_layer(inp, out, sample=None, check_y=True):
@@ -96,13 +117,24 @@ def check_layer(inp, out, sample=None, check_y=True):
     bad = np.nonzero(diff & ~near)[0]
     assert bad.size == 0, f"{bad.size} tokens chose different experts outside the near-tie band: {bad[:10]}"
 
-    # oracle conditioned on the GPU's choice
-    W3 = LazyExperts(inp.W3) if inp.W3 is not None else None
+    # oracle conditioned on the GPU's choice (fp8 gate/up weights: the
+    # dequantised weights and the quantised token rows, as the oracle's fp8
+    # variant defines them)
+    xe = None
+    if inp.W1q is not None:
+        W1 = LazyFp8Experts(inp.W1q, inp.W1s)
+        W3 = LazyFp8Experts(inp.W3q, inp.W3s)
+        vals, scales = O.quantize_rows_e4m3(x64)
+        xe = vals * scales[:, None]
+    else:
+        W1 = LazyExperts(inp.W1)
+        W3 = LazyExperts(inp.W3) if inp.W3 is not None else None
     tokens = None if sample is None else np.asarray(sample)
-    r = O.moe_forward(x64, Wr, LazyExperts(inp.W1), LazyExperts(inp.W2), s.k, s.act, s.gate,
+    r = O.moe_forward(x64, Wr, W1, LazyExperts(inp.W2), s.k, s.act, s.gate,
                       W3=W3, logit_offset=off, sel_bias=bias, capacity_factor=s.capacity_factor,
                       alpha=s.alpha, Ws1=host64(inp.Ws1), Ws3=host64(inp.Ws3), Ws2=host64(inp.Ws2),
-                      tokens=tokens if check_y else np.zeros(0, np.int64), forced_idx=idx_gpu)
+                      tokens=tokens if check_y else np.zeros(0, np.int64), forced_idx=idx_gpu,
+                      x_experts=xe)
     a = r.asg
     np.testing.assert_array_equal(out.expert_counts.cpu().numpy(), a.kept)
     if out.routed_counts is not None:

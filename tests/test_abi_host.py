@@ -145,3 +145,40 @@ def test_balance_controls_check_arguments_without_gpu():
     assert lib.moe_bias_update(fake, 8, 4, 1, f(float("nan")), fake, None) == N.MOE_ERR_ARG
     assert lib.moe_bias_update(None, 8, 4, 1, f(1e-3), fake, None) == N.MOE_ERR_ARG
     assert lib.moe_bias_update(fake, 8, 4, 1, f(1e-3), odd, None) == N.MOE_ERR_ARG
+
+
+def test_fp8_entry_point_checks_without_gpu():
+    """moe_forward_fp8: unsupported layers and missing or misaligned scale
+    arrays are rejected before any device work; launch counts add the row
+    quantisation and drop the bf16 row copy."""
+    lib = N.lib()
+    fake = ctypes.c_void_p(1 << 20)
+    odd = ctypes.c_void_p((1 << 20) + 4)
+    size = ctypes.c_size_t(0)
+
+    def call(cfg, W1s=fake, W3s=fake):
+        args = [fake, fake, None, None, fake, W1s, fake, W3s, fake,
+                fake, fake, fake, fake, fake, None, None, None, None, None]
+        return lib.moe_forward_fp8(ctypes.byref(cfg), *args, None, ctypes.c_size_t(0), None)
+
+    ok = L.make_config(T=16, d=256, E=8, k=2, f=64)
+    assert lib.moe_workspace_size_fp8(ctypes.byref(ok), ctypes.byref(size)) == N.MOE_OK
+    plain = ctypes.c_size_t(0)
+    assert lib.moe_workspace_size(ctypes.byref(ok), ctypes.byref(plain)) == N.MOE_OK
+    assert size.value > 0
+    for bad in (L.make_config(T=16, d=256, E=8, k=2, f=64, act=L.ACT_GELU),
+                L.make_config(T=16, d=264, E=8, k=2, f=64),
+                L.make_config(T=16, d=256, E=8, k=2, f=64, dtype="f32"),
+                L.make_config(T=16, d=256, E=8, k=2, f=64, n_shared=1, f_shared=64)):
+        assert call(bad) == N.MOE_ERR_UNSUPPORTED
+        assert lib.moe_workspace_size_fp8(ctypes.byref(bad), ctypes.byref(size)) == \
+            N.MOE_ERR_UNSUPPORTED
+    assert call(ok, W1s=None) == N.MOE_ERR_ARG
+    assert call(ok, W3s=None) == N.MOE_ERR_ARG
+    assert call(ok, W1s=odd) == N.MOE_ERR_ARG
+    assert call(ok) == N.MOE_ERR_WORKSPACE          # everything else valid, no workspace
+    # decode batch: router, row quantisation, two projections, combine; the
+    # one-launch tensor-core router needs no row copy either
+    assert L.launch_count(L.config_for(W.get("gptoss16_fp8")), fp8=True) == 5
+    assert L.launch_count(L.config_for(W.get("gptoss256")), fp8=False) == 6
+    assert L.launch_count(L.config_for(W.get("gptoss256_fp8")), fp8=True) == 7

@@ -1,0 +1,83 @@
+"""The layer with fp8 (e4m3) gate/up expert weights (moe_forward_fp8) against
+the oracle's fp8 variant on the same seeded inputs: routing bit-exact (or a
+counted near tie), integers exact given the GPU's choice, y within the bf16
+tolerance.  The row quantisation is exact on both sides (power-of-two scales),
+so only the float32 accumulation and the bf16 roundings of h, o and y differ.
+"""
+import gc
+
+import pytest
+import torch
+
+from sparse_mixture_experts_65_b300 import layer as L
+from sparse_mixture_experts_65_b300 import workloads as W
+from sparse_mixture_experts_65_b300.workloads import LayerShape
+
+from gpu_harness import check_layer, run_gpu
+
+pytestmark = pytest.mark.gpu
+
+SW = W.ACT_SWIGLU
+TOPK, SIG, FULL = W.GATE_SOFTMAX_TOPK, W.GATE_SIGMOID_RENORM, W.GATE_SOFTMAX_FULL
+
+FP8 = [
+    # decode batches (one-launch small-batch router)
+    LayerShape("fp8_decode_t1", 70, T=1, d=256, E=16, k=4, f=192, act=SW, gate=TOPK,
+               dtype="bf16", w_fp8=True),
+    LayerShape("fp8_decode_ragged", 71, T=13, d=272, E=40, k=3, f=200, act=SW, gate=SIG,
+               dtype="bf16", sel_bias_halfwidth=0.05, w_fp8=True),
+    # tensor-core one-launch router; K (d) not a multiple of 128, N (f) ragged
+    LayerShape("fp8_one_launch", 72, T=700, d=400, E=24, k=2, f=328, act=SW, gate=TOPK,
+               dtype="bf16", w_fp8=True),
+    # split router (E > 64)
+    LayerShape("fp8_split_many", 73, T=300, d=256, E=100, k=4, f=128, act=SW, gate=SIG,
+               dtype="bf16", sel_bias_halfwidth=0.05, w_fp8=True),
+    # top-1 with capacity drops: the combine runs inside the down projection
+    LayerShape("fp8_capacity_top1", 74, T=517, d=192, E=16, k=1, f=256, act=SW, gate=FULL,
+               dtype="bf16", capacity_factor=1.0, logit_offset_var=1.5, w_fp8=True),
+]
+
+
+def _free():
+    gc.collect()
+    torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("shape", FP8, ids=lambda s: s.name)
+def test_fp8_layers(shape):
+    inp = W.make_inputs(shape, "cuda", seed=2)
+    _, out = run_gpu(inp)
+    rep = check_layer(inp, out)
+    print(shape.name, rep)
+
+
+@pytest.mark.parametrize("T", [1, 16])
+def test_fp8_gptoss_decode(T):
+    shape = W.get(f"gptoss{T}_fp8")
+    inp = W.make_inputs(shape, "cuda")
+    _, out = run_gpu(inp)
+    sample = None if T <= 16 else list(range(0, T, max(1, T // 32)))
+    rep = check_layer(inp, out, sample=sample)
+    print("gptoss_fp8", T, rep)
+    del inp, out
+    _free()
+
+
+def test_fp8_repeat_calls_bitwise_identical():
+    inp = W.make_inputs(FP8[2], "cuda", seed=3)
+    cfg = L.config_for(inp.shape)
+    ws = L.alloc_workspace(cfg, kind="fp8")
+    _, a = run_gpu(inp, cfg, ws)
+    _, b = run_gpu(inp, cfg, ws)
+    for name in ("y", "topk_idx", "topk_w", "expert_counts", "aux_loss", "slot_pos"):
+        assert torch.equal(getattr(a, name), getattr(b, name)), name
+    assert L.check_status(ws) == L.N.MOE_OK
+
+
+def test_fp8_zero_token_rows():
+    """An all-zero token row takes scale 1 and codes 0: its expert outputs are
+    the down projection of silu(0) * 0 = 0."""
+    inp = W.make_inputs(FP8[0], "cuda", seed=4)
+    inp.x.zero_()
+    _, out = run_gpu(inp)
+    assert torch.count_nonzero(out.y) == 0
