@@ -79,6 +79,34 @@ def test_roofline_bound_selection():
     assert r["bound"] == "tensor" and abs(r["achieved"] - 1000.0) < 1e-6
 
 
+def test_accounting_fp8_gate_up_weights():
+    """e4m3 gate/up weights count one byte each plus a float32 scale per
+    channel; the up projection reads one-byte rows; the down projection and
+    the layer's other bytes are those of the bf16 layer."""
+    bf = W.get("gptoss16")
+    f8 = W.get("gptoss16_fp8")
+    kept = [0] * bf.E
+    for e in range(0, 64, 4):
+        kept[e] = 4                   # 16 active experts, 64 kept rows
+    acc_b, lay_b = bench.accounting(bf, kept)
+    acc_f, lay_f = bench.accounting(f8, kept)
+    act, rows, d, f = 16, 64, bf.d, bf.f
+    assert acc_f["up"]["bytes"] == act * 2 * f * (d + 4) + rows * d + rows * f * 2
+    assert acc_b["up"]["bytes"] == act * 2 * f * d * 2 + rows * d * 2 + rows * f * 2
+    assert acc_f["down"] == acc_b["down"]
+    assert acc_f["up"]["flops"] == acc_b["up"]["flops"]
+    assert lay_b["bytes"] - lay_f["bytes"] == act * 2 * f * d * 2 - act * 2 * f * (d + 4)
+
+
+def test_fp8_up_projection_uses_the_fp8_tensor_peak():
+    peaks = dict(bench.FALLBACK_PEAKS)
+    acc = {"up": {"bytes": 1e6, "flops": 1e12}}
+    r8 = bench.roofline_for("up", acc, 1.0, peaks, "fallback", fp8=True)
+    r16 = bench.roofline_for("up", acc, 1.0, peaks, "fallback")
+    assert r8["bound"] == r16["bound"] == "tensor"
+    assert abs(r8["peak"] - 2 * r16["peak"]) < 0.2 and abs(r8["frac"] * 2 - r16["frac"]) < 1e-3
+
+
 def test_default_arguments_finish_within_minutes(monkeypatch):
     monkeypatch.setattr("sys.argv", ["bench.py"])
     a = bench.parse()
