@@ -188,18 +188,21 @@ int moe_router_scores(const moe_config* cfg, const void* x, const void* W_r,
  * entry point; it repackages stage 1 for such callers.
  * Inputs and output ([T, E] float32 logits, offset included) are those of
  * moe_router_scores; the logits come from the float32 FMA router (bit for bit
- * what moe_router_scores gives when MOE_ROUTER=simt selects that kernel, and
- * within 5e-6 of its default tensor-core router for large bf16 batches).  The
- * router GEMM's scratch (split partial logits and the counters of their
- * reduction) lives in one 8 MiB array
- * inside the library, which every GPU that loads libmoe.so holds until the
- * process exits.  A layer whose partials do not fit (4 KiB of counters plus
- * S*T*E*4 bytes, S the reduction split) returns MOE_ERR_UNSUPPORTED.  The
- * call allocates nothing.  The first call on a device looks up the array's
- * device address; make that first call before any stream capture.  All calls
- * share the one array and it keeps the last call's contents: calls that
- * overlap on the GPU (other streams, other threads) race, so the caller must
- * serialise them.
+ * what moe_router_scores gives when moe_set_tuning selects MOE_ROUTER_SIMT,
+ * and within 5e-6 of its default tensor-core router for large bf16 batches).
+ * The router GEMM's scratch (split partial logits and the counters of their
+ * reduction) lives in one 8 MiB array inside the library.  Each device on
+ * which the library's router module gets loaded (CUDA loads modules lazily:
+ * the first router or no-workspace call on that device loads it) holds those
+ * 8 MiB until the process exits.  A layer whose partials do not fit (4 KiB of
+ * counters plus S*T*E*4 bytes, S the reduction split) returns
+ * MOE_ERR_UNSUPPORTED.  The call allocates nothing.  The first call in a CUDA
+ * context looks up the array's device address in that context (and caches it
+ * under the context's id, so a device reset or another context gets its own
+ * lookup); make that first call before any stream capture.  All calls share
+ * the one array and it keeps the last call's contents: calls that overlap on
+ * the GPU (other streams, other threads) race, so the caller must serialise
+ * them.
  */
 int moe_router_scores_noalloc(const moe_config* cfg, const void* x, const void* W_r,
                               const float* logit_offset, float* scores, void* stream);
@@ -344,6 +347,35 @@ int moe_forward_timed(const moe_config* cfg,
 
 /* Number of kernels one moe_forward call launches for this layer. */
 int moe_launch_count(const moe_config* cfg, int32_t* launches);
+
+/*
+ * moe_set_tuning -- process-wide override of a kernel choice, for tests and
+ * tile sweeps only; production callers leave every knob at its default.
+ * Later calls of every entry point (on every thread and device) plan with
+ * the override; the results stay within the layer's parity tolerance whatever
+ * the choice, only the kernels and their speed change.  value -1 restores the
+ * library's own choice.
+ *   MOE_TUNE_ROUTER          MOE_ROUTER_SIMT (split float32 FMA logits),
+ *                            MOE_ROUTER_FUSED (fused float32 router),
+ *                            MOE_ROUTER_TC (tensor-core logits, bf16 only);
+ *   MOE_TUNE_GATHER          0: the up projection reads an expert-ordered copy
+ *                            of the rows; 1: it gathers the rows of x itself;
+ *   MOE_TUNE_TILE_N_UP / _DOWN  output columns per tensor-core tile (one of the
+ *                            compiled widths, else ignored);
+ *   MOE_TUNE_PARTIAL_A_ROWS  tiles with at most this many rows load only them.
+ * Errors: MOE_ERR_ARG for an unknown knob or a value out of range.  Not
+ * synchronised with calls in flight on other threads.
+ */
+enum {
+  MOE_TUNE_ROUTER = 0,
+  MOE_TUNE_GATHER = 1,
+  MOE_TUNE_TILE_N_UP = 2,
+  MOE_TUNE_TILE_N_DOWN = 3,
+  MOE_TUNE_PARTIAL_A_ROWS = 4,
+  MOE_TUNE_COUNT = 5
+};
+enum { MOE_ROUTER_SIMT = 1, MOE_ROUTER_FUSED = 2, MOE_ROUTER_TC = 3 };
+int moe_set_tuning(int32_t knob, int32_t value);
 
 /*
  * Self-test of the bounded device waits: launches one block that waits on

@@ -154,15 +154,35 @@ def topk_indices(sel, k: int) -> np.ndarray:
 
 
 def topk_gap(sel, k: int) -> np.ndarray:
-    """Per token: (k-th largest) - ((k+1)-th largest) selection score; +inf when k == E.
-    Tokens with a gap below the near-tie band may legitimately pick a different
-    set under a different (but valid) rounding of the scores."""
+    """Per token: the smallest difference between neighbouring scores among its
+    k+1 largest selection scores (all E of them when k == E); +inf when E == 1.
+
+    The chosen list (which experts, and their descending order) of a token is
+    decided by exactly those neighbouring comparisons: the k-th against the
+    (k+1)-th decides the set, the pairs inside the first k decide the order.
+    So if every score moves by less than half of this gap the list cannot
+    change, while moving the closest pair toward each other by more than half
+    of it swaps them.  A token whose gap lies below the near-tie band may
+    therefore legitimately be routed differently by another, equally valid,
+    rounding of its scores ([MoE-ch11] § Top-k routing: the k largest)."""
     sel = _f64(sel)
     T, E = sel.shape
-    if k >= E:
-        return np.full(T, np.inf)
-    srt = -np.sort(-sel, axis=1)
-    return srt[:, k - 1] - srt[:, k]
+    if not 1 <= k <= E:
+        raise ValueError("need 1 <= k <= E")
+    m = min(k + 1, E)
+    gap = np.full(T, np.inf)
+    for t in range(T):
+        best = np.sort(sel[t])[::-1][:m]          # the m largest, descending
+        for i in range(m - 1):
+            gap[t] = min(gap[t], best[i] - best[i + 1])
+    return gap
+
+
+def near_tie_tokens(sel, k: int, band: float = 1e-5) -> np.ndarray:
+    """Boolean [T]: tokens whose top-k list sits within `band` of a tie
+    (topk_gap below the band).  Such tokens are counted and reported when two
+    implementations route them differently."""
+    return topk_gap(sel, k) < band
 
 
 def gate_values(s, idx, gate_mode: str) -> np.ndarray:

@@ -24,6 +24,9 @@ MOE_F32, MOE_BF16 = 0, 1
 MOE_ACT_GELU, MOE_ACT_RELU, MOE_ACT_SWIGLU = 0, 1, 2
 MOE_GATE_SOFTMAX_TOPK, MOE_GATE_SIGMOID_RENORM, MOE_GATE_SOFTMAX_FULL = 0, 1, 2
 MOE_NUM_STAGES = 6
+MOE_TUNE_ROUTER, MOE_TUNE_GATHER, MOE_TUNE_TILE_N_UP, MOE_TUNE_TILE_N_DOWN = 0, 1, 2, 3
+MOE_TUNE_PARTIAL_A_ROWS = 4
+MOE_ROUTER_SIMT, MOE_ROUTER_FUSED, MOE_ROUTER_TC = 1, 2, 3
 STAGE_NAMES = ("router", "topk", "permute", "up", "down", "combine")
 
 EXPORTS = (
@@ -32,6 +35,7 @@ EXPORTS = (
     "moe_error_string", "moe_forward_timed", "moe_launch_count", "moe_selftest_wait_timeout",
     "moe_router_scores", "moe_router_scores_noalloc", "moe_router_z_loss", "moe_bias_update",
     "moe_workspace_size_fp8", "moe_forward_fp8", "moe_forward_fp8_timed", "moe_launch_count_fp8",
+    "moe_set_tuning",
 )
 
 
@@ -100,6 +104,8 @@ def lib() -> ctypes.CDLL:
         L.moe_error_string.restype = ctypes.c_char_p
         L.moe_launch_count.argtypes = [cfgp, I32P]
         L.moe_launch_count.restype = ctypes.c_int
+        L.moe_set_tuning.argtypes = [ctypes.c_int32, ctypes.c_int32]
+        L.moe_set_tuning.restype = ctypes.c_int
         L.moe_selftest_wait_timeout.argtypes = [P, SZ, ctypes.c_uint64, P]
         L.moe_selftest_wait_timeout.restype = ctypes.c_int
         _lib = L

@@ -38,9 +38,12 @@ static int choose_bn(const int* cands, int ncand, int N, long long est_mtiles, l
 
 int make_plan(const moe_config* cfg, WsKind kind, Plan* p, int num_sms);
 
-static int env_int(const char* name) {
-  const char* v = std::getenv(name);
-  return v ? std::atoi(v) : 0;
+// Process-wide overrides set through moe_set_tuning (tests and tile sweeps
+// only); -1 = no override.  Production calls never read the environment.
+static std::atomic<int> g_tune[MOE_TUNE_COUNT] = {-1, -1, -1, -1, -1};
+
+int tuning(int knob) {
+  return knob >= 0 && knob < MOE_TUNE_COUNT ? g_tune[knob].load(std::memory_order_relaxed) : -1;
 }
 
 int make_plan(const moe_config* cfg, WsKind kind, Plan* p) { return make_plan(cfg, kind, p, 0); }
@@ -88,23 +91,23 @@ int make_plan(const moe_config* cfg, WsKind kind, Plan* p, int num_sms) {
   // one kernel per 16*TM tokens computes all logits over the full width, then
   // routes; TN = experts per thread = next_pow2(E)/16.  Otherwise the split
   // path: a split-K logits kernel, then the top-k kernel.
-  // MOE_ROUTER=simt forces the split path, MOE_ROUTER=fused the fused one.
+  // A router override (moe_set_tuning) of SIMT forces the split path, FUSED
+  // the fused one.
+  const int router_tune = tuning(MOE_TUNE_ROUTER);
   {
-    const char* r = std::getenv("MOE_ROUTER");
-    const bool force_split = r && std::strcmp(r, "simt") == 0;
-    const bool force_fused = r && std::strcmp(r, "fused") == 0;
+    const bool force_split = router_tune == MOE_ROUTER_SIMT;
+    const bool force_fused = router_tune == MOE_ROUTER_FUSED;
     int ep = 32;
     while (ep < c.E) ep <<= 1;
     P.fu_tn = ep <= 256 ? ep / 16 : 0;
     P.fu_tm = ceil_div(c.T, 32) >= 64 ? 2 : 1;
     P.router_fused = P.fu_tn > 0 && !force_split && force_fused;
   }
-  // One-launch tensor-core routing (bf16, E <= 64, k <= 8) unless MOE_ROUTER
-  // forces another path; its routing blocks are its 128-token tiles.
+  // One-launch tensor-core routing (bf16, E <= 64, k <= 8) unless a router
+  // override forces another path; its routing blocks are its 128-token tiles.
   {
-    const char* r = std::getenv("MOE_ROUTER");
-    const bool forced = r && (std::strcmp(r, "simt") == 0 || std::strcmp(r, "fused") == 0 ||
-                              std::strcmp(r, "tc") == 0);
+    const bool forced = router_tune == MOE_ROUTER_SIMT || router_tune == MOE_ROUTER_FUSED ||
+                        router_tune == MOE_ROUTER_TC;
     // decode batches (T <= kSmallT): split-K logits, top-k, scan and
     // positions in one small launch
     P.route_small = !forced && c.T >= 1 && c.T <= kSmallT && c.E <= kSmallMaxE;
@@ -157,12 +160,10 @@ int make_plan(const moe_config* cfg, WsKind kind, Plan* p, int num_sms) {
   // tensor cores with 128-wide float32 chunks (max error ~2e-6 on a 7168-wide
   // router, measured; float32 FMA: ~8e-7); both stay inside half the 1e-5
   // band in which near-tied experts may swap.  Smaller batches and float32
-  // layers use the split float32 FMA kernel.  MOE_ROUTER=simt / fused / tc
-  // forces a path.
+  // layers use the split float32 FMA kernel.  A router override forces a path.
   {
-    const char* r = std::getenv("MOE_ROUTER");
-    const bool force_tc = r && std::strcmp(r, "tc") == 0;
-    const bool forced_other = r && (std::strcmp(r, "simt") == 0 || std::strcmp(r, "fused") == 0);
+    const bool force_tc = router_tune == MOE_ROUTER_TC;
+    const bool forced_other = router_tune == MOE_ROUTER_SIMT || router_tune == MOE_ROUTER_FUSED;
     P.router_tc = c.dtype == MOE_BF16 && (force_tc || (!forced_other && c.T >= kRouterTcMinT));
     if (P.router_tc) P.router_fused = false;
   }
@@ -187,9 +188,9 @@ int make_plan(const moe_config* cfg, WsKind kind, Plan* p, int num_sms) {
     else
       P.up_bn = choose_bn(single_c, 4, c.f, est, P.mt_sh, c.f_shared, P.num_sms, 1);
     P.dn_bn = choose_bn(down_c, 5, c.d, est, P.mt_sh, c.d, P.num_sms, 1);
-    // Tuning override (tile sweeps and tests): MOE_TILE_N_UP / MOE_TILE_N_DOWN
-    // select one of the compiled tile widths; other values are ignored.
-    const int up_env = env_int("MOE_TILE_N_UP"), dn_env = env_int("MOE_TILE_N_DOWN");
+    // Tuning override (tile sweeps and tests, moe_set_tuning): one of the
+    // compiled tile widths; other values are ignored.
+    const int up_env = tuning(MOE_TUNE_TILE_N_UP), dn_env = tuning(MOE_TUNE_TILE_N_DOWN);
     const int* up_list = c.act == MOE_ACT_SWIGLU ? dual_c : single_c;
     for (int i = 0; i < 4; ++i)
       if (up_env == up_list[i]) P.up_bn = up_env;
@@ -203,9 +204,9 @@ int make_plan(const moe_config* cfg, WsKind kind, Plan* p, int num_sms) {
     // Partial A tiles (<= 64 real rows loaded as 32-row boxes) measured
     // faster for the single-operand GEMMs (down projections, plain up
     // projections) and slower for the dual-operand SwiGLU up projection.
-    const char* v = std::getenv("MOE_PARTIAL_A_ROWS");   // tuning override
-    P.partial_rows = v ? std::atoi(v) : 64;
-    P.partial_rows_up = v ? P.partial_rows : (c.act == MOE_ACT_SWIGLU ? 0 : 64);
+    const int v = tuning(MOE_TUNE_PARTIAL_A_ROWS);
+    P.partial_rows = v >= 0 ? v : 64;
+    P.partial_rows_up = v >= 0 ? P.partial_rows : (c.act == MOE_ACT_SWIGLU ? 0 : 64);
   }
   P.combine_in_down = P.tc && c.k == 1 && c.n_shared == 0;
   // The up projection gathers the token rows itself (cp.async) for
@@ -213,12 +214,12 @@ int make_plan(const moe_config* cfg, WsKind kind, Plan* p, int num_sms) {
   // one 128-row tile: there the weights dominate and the gather costs
   // nothing (measured: Switch layer).  Wider experts (Mixtral-like) and the
   // split router read an expert-ordered copy through TMA, which keeps the
-  // compute-bound up projection fed.  MOE_GATHER=0/1 overrides.
+  // compute-bound up projection fed.  A gather override (0 / 1) forces either.
   {
     const long long per_expert = Tk / (c.E > 0 ? c.E : 1);
     P.gather = P.tc && P.route_tc && per_expert <= kTcBM;
-    const char* gv = std::getenv("MOE_GATHER");
-    if (gv && P.tc) P.gather = std::atoi(gv) != 0;
+    const int gv = tuning(MOE_TUNE_GATHER);
+    if (gv >= 0 && P.tc) P.gather = gv != 0;
     if (P.fp8) P.gather = false;   // the fp8 up projection reads the quantised rows by TMA
   }
   P.nt_up = ceil_div(c.f, P.up_bn);
@@ -640,6 +641,14 @@ int moe_launch_count_fp8(const moe_config* cfg, int32_t* launches) {
   // and the combine (folded into the down projection for top-1 layers)
   const int routing = p.route_small || p.route_tc ? 1 : (p.router_fused ? 2 : 3);
   *launches = cfg->T == 0 ? 0 : routing + 1 + 2 + (p.combine_in_down ? 0 : 1);
+  return MOE_OK;
+}
+
+int moe_set_tuning(int32_t knob, int32_t value) {
+  if (knob < 0 || knob >= MOE_TUNE_COUNT || value < -1) return MOE_ERR_ARG;
+  if (knob == MOE_TUNE_ROUTER && value > MOE_ROUTER_TC) return MOE_ERR_ARG;
+  if (knob == MOE_TUNE_GATHER && value > 1) return MOE_ERR_ARG;
+  g_tune[knob].store(value, std::memory_order_relaxed);
   return MOE_OK;
 }
 

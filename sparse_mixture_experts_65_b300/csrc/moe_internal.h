@@ -98,6 +98,9 @@ enum class WsKind { Forward, Route, HostIO, ForwardFp8 };
 
 int make_plan(const moe_config* cfg, WsKind kind, Plan* p);
 
+// Current override of a moe_set_tuning knob, -1 when none is set.
+int tuning(int knob);
+
 // Device pointers of the meta region.
 struct Meta {
   int* kept;

@@ -28,6 +28,8 @@
 #include <cstring>
 #include <mutex>
 
+#include <cuda.h>
+
 #include "bulk_rows.cuh"
 #include "common.cuh"
 #include "launch.cuh"
@@ -1129,8 +1131,7 @@ static cudaError_t launch_logits(const Plan& p, const void* x, const void* W_r,
 cudaError_t launch_router_scores(const Plan& p, const void* x, const void* W_r,
                                  const float* logit_offset, float* out, void* ws,
                                  cudaStream_t st) {
-  const char* r = std::getenv("MOE_ROUTER");
-  if (r && std::strcmp(r, "fused") == 0 && p.fu_tn > 0) {
+  if (tuning(MOE_TUNE_ROUTER) == MOE_ROUTER_FUSED && p.fu_tn > 0) {
     // the fused kernel's own logits, written out before its routing step
     FusedArgs f;
     std::memset(&f, 0, sizeof(f));
@@ -1157,13 +1158,16 @@ cudaError_t launch_router_scores(const Plan& p, const void* x, const void* W_r,
 // owns all device memory and gives none out per call, or code that must not
 // enter the CUDA allocator on its latency path.  The router GEMM's scratch
 // (split-K partial logits and the tile counters of its reduction) lives in the
-// file-scope array below instead.  The array costs every GPU that loads this
-// library kNoAllocScratchBytes of device memory until the process exits.
+// file-scope array below instead.  Each device on which this file's module is
+// loaded (under CUDA's lazy module loading: by the first router call or the
+// first no-workspace call on that device) holds kNoAllocScratchBytes of device
+// memory for it until the process exits.
 //
 // Host code must not pass `g_noalloc_scratch` itself to a kernel: in host code
 // that name is a host-side stand-in, not a device address.  The device address
-// is looked up once per device with cudaGetSymbolAddress (on the first call
-// made with that device current) and cached.
+// is looked up with cudaGetSymbolAddress once per CUDA context (the first call
+// made with that context current) and cached under the context's unique id,
+// so a device reset or another context gets its own lookup.
 namespace {
 
 constexpr size_t kNoAllocScratchBytes = 8u << 20;       // 8 MiB
@@ -1171,32 +1175,61 @@ constexpr size_t kNoAllocCounterBytes = moe::kWsHeaderBytes;   // tile counters,
 
 __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
 
-std::mutex g_noalloc_mu;
-void* g_noalloc_addr[64] = {};
-int g_noalloc_sms[64] = {};
+typedef CUresult (*CtxGetCurrentFn)(CUcontext*);
+typedef CUresult (*CtxGetIdFn)(CUcontext, unsigned long long*);
 
-// Device address of the scratch array (and the SM count) for the current
-// device; resolved once per device.
-int noalloc_setup(void** addr, int* sms) {
+std::mutex g_noalloc_mu;
+constexpr int kNoAllocCacheSlots = 64;
+unsigned long long g_noalloc_ctx[kNoAllocCacheSlots] = {};   // context ids (ids start at 1)
+void* g_noalloc_addr[kNoAllocCacheSlots] = {};
+int g_noalloc_next = 0;
+
+template <typename Fn>
+Fn driver_fn(const char* name) {
+  void* p = nullptr;
+  cudaDriverEntryPointQueryResult q;
+  if (cudaGetDriverEntryPointByVersion(name, &p, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+      q != cudaDriverEntryPointSuccess)
+    return nullptr;
+  return reinterpret_cast<Fn>(p);
+}
+
+// Device address of the scratch array in the current context; looked up once
+// per context.  Also rejects devices that are not sm_103.
+int noalloc_setup(void** addr) {
+  static CtxGetCurrentFn get_current = driver_fn<CtxGetCurrentFn>("cuCtxGetCurrent");
+  static CtxGetIdFn get_id = driver_fn<CtxGetIdFn>("cuCtxGetId");
+  if (!get_current || !get_id) return MOE_ERR_CUDA;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return MOE_ERR_CUDA;
-  if (dev < 0 || dev >= 64) return MOE_ERR_DEVICE;
-  std::lock_guard<std::mutex> lock(g_noalloc_mu);
-  if (g_noalloc_addr[dev] == nullptr) {
-    int major = 0, minor = 0, n = 0;
-    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+  int major = 0, minor = 0;
+  if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  if (major != 10 || minor != 3) return MOE_ERR_DEVICE;
+  CUcontext ctx = nullptr;
+  if (get_current(&ctx) != CUDA_SUCCESS) return MOE_ERR_CUDA;
+  if (ctx == nullptr) {   // no context yet: make the device's primary context current
+    if (cudaSetDevice(dev) != cudaSuccess || get_current(&ctx) != CUDA_SUCCESS || !ctx)
       return MOE_ERR_CUDA;
-    if (major != 10 || minor != 3) return MOE_ERR_DEVICE;
-    void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr)
-      return MOE_ERR_CUDA;
-    g_noalloc_sms[dev] = n;
-    g_noalloc_addr[dev] = p;
   }
-  *addr = g_noalloc_addr[dev];
-  *sms = g_noalloc_sms[dev];
+  unsigned long long id = 0;
+  if (get_id(ctx, &id) != CUDA_SUCCESS || id == 0) return MOE_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_noalloc_mu);
+  for (int i = 0; i < kNoAllocCacheSlots; ++i) {
+    if (g_noalloc_ctx[i] == id) {
+      *addr = g_noalloc_addr[i];
+      return MOE_OK;
+    }
+  }
+  void* p = nullptr;
+  if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr)
+    return MOE_ERR_CUDA;
+  const int slot = g_noalloc_next;                 // oldest entry replaced when full
+  g_noalloc_next = (g_noalloc_next + 1) % kNoAllocCacheSlots;
+  g_noalloc_ctx[slot] = id;
+  g_noalloc_addr[slot] = p;
+  *addr = p;
   return MOE_OK;
 }
 
@@ -1220,8 +1253,7 @@ extern "C" int moe_router_scores_noalloc(const moe_config* cfg, const void* x, c
   const size_t parts = p.sc_splits > 1 ? sizeof(float) * (size_t)p.sc_splits * cfg->T * cfg->E : 0;
   if (kNoAllocCounterBytes + parts > kNoAllocScratchBytes) return MOE_ERR_UNSUPPORTED;
   void* base = nullptr;
-  int sms = 0;
-  rc = noalloc_setup(&base, &sms);
+  rc = noalloc_setup(&base);
   if (rc != MOE_OK) return rc;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   // the array keeps the previous call's contents: start the counters at zero

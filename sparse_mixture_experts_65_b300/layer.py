@@ -6,6 +6,7 @@ device memory, streams and events.  Names follow the C ABI (include/moe.h).
 
 from __future__ import annotations
 
+import contextlib
 import ctypes
 from dataclasses import dataclass
 from typing import Optional
@@ -215,6 +216,32 @@ def forward_host_io(cfg: N.MoeConfig, x_host: torch.Tensor, y_host: torch.Tensor
         _stream_handle(stream))
     N.check(rc, "moe_forward_host_io")
     return y_host, aux_host
+
+
+_TUNE_KNOBS = {"router": N.MOE_TUNE_ROUTER, "gather": N.MOE_TUNE_GATHER,
+               "tile_n_up": N.MOE_TUNE_TILE_N_UP, "tile_n_down": N.MOE_TUNE_TILE_N_DOWN,
+               "partial_a_rows": N.MOE_TUNE_PARTIAL_A_ROWS}
+_ROUTERS = {"simt": N.MOE_ROUTER_SIMT, "fused": N.MOE_ROUTER_FUSED, "tc": N.MOE_ROUTER_TC}
+
+
+def set_tuning(knob: str, value) -> None:
+    """moe_set_tuning: a process-wide kernel-choice override for tests and tile
+    sweeps (None or -1 restores the library's choice; the router knob takes
+    "simt", "fused" or "tc")."""
+    v = -1 if value is None else (_ROUTERS[value] if isinstance(value, str) else int(value))
+    N.check(N.lib().moe_set_tuning(_TUNE_KNOBS[knob], v), "moe_set_tuning")
+
+
+@contextlib.contextmanager
+def tuning(**knobs):
+    """Overrides for the duration of a `with` block, restored afterwards."""
+    try:
+        for k, v in knobs.items():
+            set_tuning(k, v)
+        yield
+    finally:
+        for k in knobs:
+            set_tuning(k, None)
 
 
 def check_status(workspace: torch.Tensor, stream=None) -> int:

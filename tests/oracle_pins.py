@@ -76,6 +76,42 @@ def check_topk_ties():
     assert O.topk_indices(sel, 4)[1].tolist() == [0, 1, 2, 3]
 
 
+def check_topk_gap():
+    """The near-tie gap: the smallest neighbouring difference among the k+1
+    best scores.  Hand cases, then its meaning: moving every score by less than
+    half the gap never changes the ordered top-k list, and moving the closest
+    pair toward each other by a little more than half of it always does."""
+    g = O.topk_gap(np.array([[3.0, 1.0, 2.0, 0.0]]), 2)
+    assert g.tolist() == [1.0]                       # 3 | 2 | 1: both gaps are 1
+    sel = np.array([[5.0, 4.5, 1.0, 0.9]])
+    assert O.topk_gap(sel, 1).tolist() == [0.5]      # 5 vs 4.5 decides the set
+    assert O.topk_gap(sel, 2).tolist() == [0.5]      # inside the set: the order
+    np.testing.assert_allclose(O.topk_gap(sel, 3), [0.1], rtol=1e-12)   # 1 vs 0.9
+    far = np.array([[10.0, 5.0, 1.0, 1.0]])          # a tie below the (k+1)-th is irrelevant
+    assert O.topk_gap(far, 1).tolist() == [5.0]
+    assert O.topk_gap(np.array([[1.0, 2.0, 2.0, 0.0]]), 1).tolist() == [0.0]   # exact tie
+    assert O.topk_gap(np.array([[1.0, 3.0]]), 2).tolist() == [2.0]   # k = E: the order only
+    assert O.topk_gap(np.array([[0.7]]), 1).tolist() == [math.inf]   # E = 1: nothing to swap
+    assert O.near_tie_tokens(np.array([[1.0, 1.0 + 5e-6, 0.0], [3.0, 2.0, 1.0]]), 1).tolist() \
+        == [True, False]
+    rng = _rng(21)
+    for E, k in ((6, 2), (9, 4), (5, 5), (12, 1)):
+        sel = rng.normal(size=(40, E))
+        gap = O.topk_gap(sel, k)
+        base = O.topk_indices(sel, k)
+        for t in range(sel.shape[0]):
+            for _ in range(5):   # any perturbation below half the gap keeps the list
+                d = rng.uniform(-1, 1, size=E) * 0.49 * gap[t]
+                assert O.topk_indices(sel[t:t + 1] + d, k)[0].tolist() == base[t].tolist()
+            srt = np.argsort(-sel[t], kind="stable")[:min(k + 1, E)]
+            vals = sel[t, srt]
+            i = int(np.argmin(vals[:-1] - vals[1:]))
+            d = np.zeros(E)
+            d[srt[i]] -= 0.51 * gap[t]
+            d[srt[i + 1]] += 0.51 * gap[t]
+            assert O.topk_indices(sel[t:t + 1] + d, k)[0].tolist() != base[t].tolist()
+
+
 def check_gates_closed_form():
     """Hand-derived gates for logits [2, 1, 0, -1] with k = 2."""
     s = np.array([[2.0, 1.0, 0.0, -1.0]])
@@ -543,7 +579,7 @@ def check_fp8_layer():
 
 
 ALL_CHECKS = [
-    check_router_onehot, check_topk_bruteforce, check_topk_ties, check_gates_closed_form,
+    check_router_onehot, check_topk_bruteforce, check_topk_ties, check_topk_gap, check_gates_closed_form,
     check_gates_invariants, check_router_probs, check_selection_bias,
     check_capacity_formula, check_capacity_drops, check_offsets_and_permutation,
     check_sparse_equals_dense, check_drop_is_identity_branch, check_dense_ffn_special_case,

@@ -52,24 +52,23 @@ def test_small_layers(shape):
 
 
 @pytest.mark.parametrize("up_bn,dn_bn", [(32, 64), (64, 96), (96, 128), (128, 192), (128, 256)])
-def test_every_swiglu_tile_width(monkeypatch, up_bn, dn_bn):
+def test_every_swiglu_tile_width(up_bn, dn_bn):
     """Force each tile width of the tensor-core kernels on a ragged layer."""
-    monkeypatch.setenv("MOE_TILE_N_UP", str(up_bn))
-    monkeypatch.setenv("MOE_TILE_N_DOWN", str(dn_bn))
     shape = LayerShape("tiles", 20, T=211, d=200, E=6, k=2, f=416, act=SW, gate=TOPK,
                        dtype="bf16", n_shared=1, f_shared=136)
     inp = W.make_inputs(shape, "cuda", seed=2)
-    _, out = run_gpu(inp)
+    with L.tuning(tile_n_up=up_bn, tile_n_down=dn_bn):
+        _, out = run_gpu(inp)
     check_layer(inp, out)
 
 
 @pytest.mark.parametrize("act", [RE, GE])
 @pytest.mark.parametrize("up_bn", [64, 96, 128, 256])
-def test_every_plain_tile_width(monkeypatch, act, up_bn):
-    monkeypatch.setenv("MOE_TILE_N_UP", str(up_bn))
+def test_every_plain_tile_width(act, up_bn):
     shape = LayerShape("plain", 21, T=190, d=96, E=5, k=2, f=328, act=act, gate=TOPK, dtype="bf16")
     inp = W.make_inputs(shape, "cuda", seed=3)
-    _, out = run_gpu(inp)
+    with L.tuning(tile_n_up=up_bn):
+        _, out = run_gpu(inp)
     check_layer(inp, out)
 
 
@@ -277,17 +276,17 @@ def test_bad_arguments_rejected_on_device():
 # ---------------------------------------------------------------- router precision
 @pytest.mark.parametrize("path", ["simt", "fused", "tc"])
 @pytest.mark.parametrize("name", ["dsv3", "mixtral", "switch"])
-def test_router_logits_within_half_the_near_tie_band(monkeypatch, path, name):
+def test_router_logits_within_half_the_near_tie_band(path, name):
     """Every float32 logit lies within 5e-6 of the float64 value, half the
     1e-5 near-tie band, on each router path (float32 FMA split-K; fused float32
     FMA; tensor cores with 128-wide float32 chunks): two experts can then only
     swap order when their float64 scores are closer than the band."""
-    monkeypatch.setenv("MOE_ROUTER", path)
     shape = W.get(name)
     x = W.make_x(shape, "cuda")
     inp = W.make_inputs(shape.with_T(1), "cuda")      # W_r etc.; x replaced below
     cfg = L.config_for(shape)
-    s = L.router_scores(cfg, x, inp.W_r, inp.logit_offset)
+    with L.tuning(router=path):
+        s = L.router_scores(cfg, x, inp.W_r, inp.logit_offset)
     torch.cuda.synchronize()
     ref = host64(x) @ host64(inp.W_r).T
     if inp.logit_offset is not None:
@@ -346,29 +345,29 @@ def test_decode_batch_router(shape):
 
 
 @pytest.mark.parametrize("gather", ["0", "1"])
-def test_up_projection_row_source(monkeypatch, gather):
+def test_up_projection_row_source(gather):
     """Both row sources of the tensor-core up projection, on layers of every
     routing path (one-launch tensor-core router, split router with E > 64,
     decode-batch router): rows gathered from x inside the GEMM (cp.async),
     and an expert-ordered copy read through TMA."""
-    monkeypatch.setenv("MOE_GATHER", gather)
     for shape in (SMALL[0], SMALL[1], SMALL[2], SMALL[3], SMALL[4], ONE_LAUNCH[1], ONE_LAUNCH[3],
                   DECODE[1], DECODE[3]):
         inp = W.make_inputs(shape, "cuda", seed=12)
-        _, out = run_gpu(inp)
+        with L.tuning(gather=int(gather)):
+            _, out = run_gpu(inp)
         check_layer(inp, out)
 
 
 @pytest.mark.parametrize("path", ["simt", "fused", "tc"])
-def test_forced_router_path_parity(monkeypatch, path):
+def test_forced_router_path_parity(path):
     """The split router paths (split-K float32 logits, the fused float32
     router, tensor-core logits; each followed by the top-k and permute
     kernels) on small ragged layers, each routing as the oracle does."""
-    monkeypatch.setenv("MOE_ROUTER", path)
     shapes = (SMALL[0], SMALL[1], SMALL[2], SMALL[3], SMALL[4], SMALL[5], SMALL[6])
     for shape in shapes:
         if path == "fused" and shape.E > 256:
             continue
         inp = W.make_inputs(shape, "cuda", seed=11)
-        _, out = run_gpu(inp)
+        with L.tuning(router=path):
+            _, out = run_gpu(inp)
         check_layer(inp, out)

@@ -14,7 +14,7 @@ import oracle.moe_oracle as M
 import oracle_pins as P
 
 _orig = {name: getattr(M, name) for name in (
-    "router_logits", "topk_indices", "gate_values", "affinity", "expert_capacity",
+    "router_logits", "topk_indices", "topk_gap", "gate_values", "affinity", "expert_capacity",
     "assign_slots", "gelu_erf", "silu", "expert_ffn_rows", "balance_stats", "router_probs",
     "softmax_rows", "router_z_loss", "bias_update", "e4m3_round", "row_scale_exponent",
     "quantize_rows_e4m3", "moe_forward_fp8")}
@@ -37,6 +37,26 @@ def _topk_ties_high(sel, k):
     sel = np.asarray(sel, dtype=float)
     E = sel.shape[1]
     return (E - 1) - _orig["topk_indices"](sel[:, ::-1], k)
+
+
+def _gap_k_plus_2(sel, k):
+    sel = np.asarray(sel, dtype=float)
+    if k + 1 >= sel.shape[1]:
+        return _orig["topk_gap"](sel, k)
+    return _orig["topk_gap"](sel, k + 1)          # one score too many in the window
+
+
+def _gap_ascending(sel, k):
+    return _orig["topk_gap"](-np.asarray(sel, dtype=float), k)   # the smallest scores
+
+
+def _gap_set_boundary_only(sel, k):
+    sel = np.asarray(sel, dtype=float)
+    E = sel.shape[1]
+    if k >= E:
+        return np.full(sel.shape[0], np.inf)
+    srt = -np.sort(-sel, axis=1)
+    return srt[:, k - 1] - srt[:, k]              # ignores the order inside the set
 
 
 def _gates_full_softmax(s, idx, mode):
@@ -197,6 +217,10 @@ MUTATIONS = [
     ("router offset sign flipped", "router_logits", _router_offset_sign, P.check_router_onehot),
     ("top-k takes the smallest", "topk_indices", _topk_ascending, P.check_topk_bruteforce),
     ("ties go to the higher index", "topk_indices", _topk_ties_high, P.check_topk_ties),
+    ("near-tie window reaches the (k+2)-th score", "topk_gap", _gap_k_plus_2, P.check_topk_gap),
+    ("near-tie gap over the smallest scores", "topk_gap", _gap_ascending, P.check_topk_gap),
+    ("near-tie gap ignores the order inside the set", "topk_gap", _gap_set_boundary_only,
+     P.check_topk_gap),
     ("top-k gates use the full softmax", "gate_values", _gates_full_softmax, P.check_gates_closed_form),
     ("sigmoid gates not renormalised", "gate_values", _gates_sigmoid_unnormalised, P.check_gates_invariants),
     ("sigmoid affinity dropped", "affinity", _affinity_no_sigmoid, P.check_selection_bias),

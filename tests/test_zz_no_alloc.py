@@ -2,14 +2,17 @@
 device memory per call (a host framework that owns all device memory, or a
 latency path that must not enter the CUDA allocator).  Its scratch is an 8 MiB
 array inside the library; its results must equal moe_router_scores, which uses
-a caller workspace.  This file runs last so that a failure here comes after
-every other test has run; it also passes alone in a fresh process (the first
-call on the device does the array's set-up)."""
+a caller workspace, and lie within the router tolerance of the float64
+definition in the CPU oracle.  This file runs last so that a failure here
+comes after every other test has run; it also passes alone in a fresh process
+(the first call in the context does the array's set-up)."""
 import ctypes
 
 import numpy as np
 import pytest
 import torch
+
+import oracle.moe_oracle as O
 
 from sparse_mixture_experts_65_b300 import _native as N
 from sparse_mixture_experts_65_b300 import layer as L
@@ -43,7 +46,7 @@ def _noalloc(cfg, x, W_r, off, out):
 
 
 @pytest.mark.parametrize("order", [("switch", "gptoss256"), ("gptoss256", "switch")])
-def test_noalloc_matches_workspace_entry_point_on_two_calls_in_a_row(order, monkeypatch):
+def test_noalloc_matches_workspace_entry_point_on_two_calls_in_a_row(order):
     for name in order:                     # the second call finds the first one's leftovers
         shape = W.get(name)
         x, W_r, off = _router_inputs(shape, seed=3)
@@ -55,11 +58,16 @@ def test_noalloc_matches_workspace_entry_point_on_two_calls_in_a_row(order, monk
         diff = (out - ref).abs().max().item()
         assert np.isfinite(diff) and diff <= ROUTER_ATOL, (name, diff)
         # with moe_router_scores on the same float32 kernel the bits agree too
-        monkeypatch.setenv("MOE_ROUTER", "simt")
-        ref_same = L.router_scores(cfg, x, W_r, off)
-        monkeypatch.delenv("MOE_ROUTER")
+        with L.tuning(router="simt"):
+            ref_same = L.router_scores(cfg, x, W_r, off)
         torch.cuda.synchronize()
         assert torch.equal(out, ref_same), name
+        # and the logits are the float64 definition's within the router tolerance
+        def h(t):
+            return None if t is None else t.float().cpu().numpy().astype(np.float64)
+        exact = O.router_logits(h(x), h(W_r), h(off))
+        err = np.abs(out.cpu().numpy().astype(np.float64) - exact).max()
+        assert err <= ROUTER_ATOL, (name, err)
 
 
 def test_noalloc_rejects_layers_beyond_its_scratch():
