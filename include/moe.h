@@ -73,7 +73,11 @@ enum {
   MOE_ERR_WORKSPACE = 3,    /* workspace NULL, too small or not 256-byte aligned */
   MOE_ERR_CUDA = 4,         /* a CUDA runtime call or launch failed */
   MOE_ERR_TIMEOUT = 5,      /* a bounded device wait ran out (reported by moe_check_status) */
-  MOE_ERR_DEVICE = 6        /* current device is not a compute-capability 10.3 GPU */
+  MOE_ERR_DEVICE = 6,       /* current device is not a compute-capability 10.3 GPU */
+  MOE_ERR_BOUNDS = 7        /* bounds-checked build (libmoe_check.so) only: a routing-derived
+                               index (expert, capacity position, buffer row, token) was out
+                               of range; the access was skipped (reported by
+                               moe_check_status) */
 };
 
 typedef enum { MOE_F32 = 0, MOE_BF16 = 1 } moe_dtype;
@@ -305,8 +309,11 @@ int moe_forward_host_io(const moe_config* cfg,
 /*
  * Synchronises `stream`, then reads and clears the device status word in
  * `workspace`.  Returns MOE_OK, MOE_ERR_TIMEOUT when a bounded device wait
- * gave up since the last check, or MOE_ERR_CUDA if the synchronisation
- * itself failed.
+ * gave up since the last check, MOE_ERR_BOUNDS when the bounds-checked build
+ * (libmoe_check.so, the same ABI compiled with MOE_CHECK=1: every index that
+ * routing produces is range-tested before the access it drives, and a failed
+ * test skips the access instead of trapping) found an index out of range, or
+ * MOE_ERR_CUDA if the synchronisation itself failed.
  */
 int moe_check_status(void* workspace, void* stream);
 

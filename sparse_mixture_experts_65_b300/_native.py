@@ -11,6 +11,7 @@ import os
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libmoe.so")
+CHECK_LIB_PATH = os.path.join(_HERE, "libmoe_check.so")   # bounds-checked build
 
 MOE_OK = 0
 MOE_ERR_ARG = 1
@@ -19,6 +20,7 @@ MOE_ERR_WORKSPACE = 3
 MOE_ERR_CUDA = 4
 MOE_ERR_TIMEOUT = 5
 MOE_ERR_DEVICE = 6
+MOE_ERR_BOUNDS = 7
 
 MOE_F32, MOE_BF16 = 0, 1
 MOE_ACT_GELU, MOE_ACT_RELU, MOE_ACT_SWIGLU = 0, 1, 2
@@ -56,6 +58,7 @@ class MoeError(RuntimeError):
 
 
 _lib = None
+_libs = {}
 P = ctypes.c_void_p
 SZ = ctypes.c_size_t
 I32P = ctypes.POINTER(ctypes.c_int32)
@@ -64,52 +67,66 @@ I32P = ctypes.POINTER(ctypes.c_int32)
 def lib() -> ctypes.CDLL:
     global _lib
     if _lib is None:
-        if not os.path.exists(LIB_PATH):
-            raise RuntimeError(
-                f"{LIB_PATH} is missing: build it with `python -m sparse_mixture_experts_65_b300.build`"
-                " (or __graft_entry__.build()); this package has no non-CUDA fallback")
-        L = ctypes.CDLL(LIB_PATH)
-        cfgp = ctypes.POINTER(MoeConfig)
-        for name in ("moe_workspace_size", "moe_route_workspace_size", "moe_host_io_workspace_size",
-                     "moe_workspace_size_fp8"):
-            f = getattr(L, name)
-            f.argtypes = [cfgp, ctypes.POINTER(SZ)]
-            f.restype = ctypes.c_int
-        fwd_args = [cfgp, P, P, P, P, P, P, P, P, P, P, P, P, P, P, P, P, P, P, P, P, P, SZ, P]
-        L.moe_forward.argtypes = fwd_args
-        L.moe_forward.restype = ctypes.c_int
-        L.moe_forward_timed.argtypes = fwd_args + [ctypes.POINTER(P)]
-        L.moe_forward_timed.restype = ctypes.c_int
-        L.moe_route.argtypes = [cfgp, P, P, P, P, P, P, P, P, P, P, P, P, P, P, SZ, P]
-        L.moe_route.restype = ctypes.c_int
-        L.moe_forward_host_io.argtypes = [cfgp, P, P, P, P, P, P, P, P, P, P, P, P, P, SZ, P]
-        L.moe_forward_host_io.restype = ctypes.c_int
-        L.moe_router_scores.argtypes = [cfgp, P, P, P, P, P, SZ, P]
-        L.moe_router_scores.restype = ctypes.c_int
-        fp8_args = [cfgp] + [P] * 20 + [SZ, P]
-        L.moe_forward_fp8.argtypes = fp8_args
-        L.moe_forward_fp8.restype = ctypes.c_int
-        L.moe_forward_fp8_timed.argtypes = fp8_args + [ctypes.POINTER(P)]
-        L.moe_forward_fp8_timed.restype = ctypes.c_int
-        L.moe_launch_count_fp8.argtypes = [cfgp, I32P]
-        L.moe_launch_count_fp8.restype = ctypes.c_int
-        L.moe_router_z_loss.argtypes = [P, ctypes.c_int32, ctypes.c_int32, P, P]
-        L.moe_router_z_loss.restype = ctypes.c_int
-        L.moe_bias_update.argtypes = [P, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
-                                      ctypes.c_float, P, P]
-        L.moe_bias_update.restype = ctypes.c_int
-        L.moe_check_status.argtypes = [P, P]
-        L.moe_check_status.restype = ctypes.c_int
-        L.moe_error_string.argtypes = [ctypes.c_int]
-        L.moe_error_string.restype = ctypes.c_char_p
-        L.moe_launch_count.argtypes = [cfgp, I32P]
-        L.moe_launch_count.restype = ctypes.c_int
-        L.moe_set_tuning.argtypes = [ctypes.c_int32, ctypes.c_int32]
-        L.moe_set_tuning.restype = ctypes.c_int
-        L.moe_selftest_wait_timeout.argtypes = [P, SZ, ctypes.c_uint64, P]
-        L.moe_selftest_wait_timeout.restype = ctypes.c_int
-        _lib = L
+        _lib = _load(LIB_PATH)
     return _lib
+
+
+def use_library(variant: str) -> None:
+    """Routes every later call to `variant`: "default" (libmoe.so) or "check"
+    (libmoe_check.so, the bounds-checked build; tests only)."""
+    global _lib
+    _lib = _load(CHECK_LIB_PATH if variant == "check" else LIB_PATH)
+
+
+def _load(path: str) -> ctypes.CDLL:
+    if path in _libs:
+        return _libs[path]
+    if not os.path.exists(path):
+        raise RuntimeError(
+            f"{path} is missing: build it with `python -m sparse_mixture_experts_65_b300.build`"
+            " (or __graft_entry__.build()); this package has no non-CUDA fallback")
+    L = ctypes.CDLL(path)
+    cfgp = ctypes.POINTER(MoeConfig)
+    for name in ("moe_workspace_size", "moe_route_workspace_size", "moe_host_io_workspace_size",
+                 "moe_workspace_size_fp8"):
+        f = getattr(L, name)
+        f.argtypes = [cfgp, ctypes.POINTER(SZ)]
+        f.restype = ctypes.c_int
+    fwd_args = [cfgp, P, P, P, P, P, P, P, P, P, P, P, P, P, P, P, P, P, P, P, P, P, SZ, P]
+    L.moe_forward.argtypes = fwd_args
+    L.moe_forward.restype = ctypes.c_int
+    L.moe_forward_timed.argtypes = fwd_args + [ctypes.POINTER(P)]
+    L.moe_forward_timed.restype = ctypes.c_int
+    L.moe_route.argtypes = [cfgp, P, P, P, P, P, P, P, P, P, P, P, P, P, P, SZ, P]
+    L.moe_route.restype = ctypes.c_int
+    L.moe_forward_host_io.argtypes = [cfgp, P, P, P, P, P, P, P, P, P, P, P, P, P, SZ, P]
+    L.moe_forward_host_io.restype = ctypes.c_int
+    L.moe_router_scores.argtypes = [cfgp, P, P, P, P, P, SZ, P]
+    L.moe_router_scores.restype = ctypes.c_int
+    fp8_args = [cfgp] + [P] * 20 + [SZ, P]
+    L.moe_forward_fp8.argtypes = fp8_args
+    L.moe_forward_fp8.restype = ctypes.c_int
+    L.moe_forward_fp8_timed.argtypes = fp8_args + [ctypes.POINTER(P)]
+    L.moe_forward_fp8_timed.restype = ctypes.c_int
+    L.moe_launch_count_fp8.argtypes = [cfgp, I32P]
+    L.moe_launch_count_fp8.restype = ctypes.c_int
+    L.moe_router_z_loss.argtypes = [P, ctypes.c_int32, ctypes.c_int32, P, P]
+    L.moe_router_z_loss.restype = ctypes.c_int
+    L.moe_bias_update.argtypes = [P, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
+                                  ctypes.c_float, P, P]
+    L.moe_bias_update.restype = ctypes.c_int
+    L.moe_check_status.argtypes = [P, P]
+    L.moe_check_status.restype = ctypes.c_int
+    L.moe_error_string.argtypes = [ctypes.c_int]
+    L.moe_error_string.restype = ctypes.c_char_p
+    L.moe_launch_count.argtypes = [cfgp, I32P]
+    L.moe_launch_count.restype = ctypes.c_int
+    L.moe_set_tuning.argtypes = [ctypes.c_int32, ctypes.c_int32]
+    L.moe_set_tuning.restype = ctypes.c_int
+    L.moe_selftest_wait_timeout.argtypes = [P, SZ, ctypes.c_uint64, P]
+    L.moe_selftest_wait_timeout.restype = ctypes.c_int
+    _libs[path] = L
+    return L
 
 
 def error_string(code: int) -> str:

@@ -8,6 +8,7 @@
 // "Mixture-of-Experts" (neural networks visually) § Show the math: the layer
 // output is the gate-weighted sum over the chosen experts only; dropped
 // slots contribute nothing (ch. 11 § Expert capacity and dropped tokens).
+#include "check.cuh"
 #include "common.cuh"
 #include "launch.cuh"
 #include "moe_internal.h"
@@ -20,7 +21,8 @@ struct CombineArgs {
   const int* key_row;    // [T*k]
   const float* topk_w;   // [T*k]
   void* y;               // [T][d]
-  int T, d, k;
+  int T, d, k, R_cap;
+  uint32_t* status;
 };
 
 __device__ __forceinline__ void store4(float* y, size_t i, float4 v) {
@@ -53,7 +55,8 @@ __global__ void __launch_bounds__(kThreads) combine_kernel(const CombineArgs a) 
   pdl_wait();
   pdl_trigger();
   if (threadIdx.x < a.k) {
-    rows[threadIdx.x] = a.key_row[(size_t)t * a.k + threadIdx.x];
+    const int r = a.key_row[(size_t)t * a.k + threadIdx.x];
+    rows[threadIdx.x] = r >= 0 && in_bounds(r < a.R_cap, a.status) ? r : -1;
     gates[threadIdx.x] = a.topk_w[(size_t)t * a.k + threadIdx.x];
   }
   __syncthreads();
@@ -89,6 +92,8 @@ cudaError_t launch_combine(const Plan& p, const float* topk_w, void* y, void* ws
   a.T = p.cfg.T;
   a.d = p.cfg.d;
   a.k = p.cfg.k;
+  a.R_cap = p.R_cap;
+  a.status = reinterpret_cast<uint32_t*>(w + p.ws.status);
   if (p.cfg.dtype == MOE_BF16)
     return launch_pdl(combine_kernel<__nv_bfloat16>, dim3(p.cfg.T), dim3(kThreads), 0, st, a);
   return launch_pdl(combine_kernel<float>, dim3(p.cfg.T), dim3(kThreads), 0, st, a);

@@ -15,6 +15,7 @@
 #include <climits>
 #include <cmath>
 
+#include "check.cuh"
 #include "common.cuh"
 #include "launch.cuh"
 #include "moe_internal.h"
@@ -40,6 +41,8 @@ struct SimtArgs {
   int N, K, N_sh, K_sh;
   int act;               // routed activation
   int act_sh;
+  int R_cap;             // rows of the routed buffers
+  uint32_t* status;
 };
 
 constexpr int SB_M = kSimtBM, SB_N = kSimtBN, SB_K = 16;
@@ -74,7 +77,7 @@ __global__ void __launch_bounds__(kThreads) simt_grouped_gemm(const SimtArgs a) 
     const int act = sh ? a.act_sh : a.act;
     const float* A = sh ? a.A_sh : a.A;
     const int row0 = sh ? m_t * SB_M : a.seg_start[seg] + m_t * SB_M;
-    const int row_lim = sh ? a.A_sh_rows : INT_MAX;
+    const int row_lim = sh ? a.A_sh_rows : a.R_cap;
     const float* B0 = sh ? a.B0_sh : a.B0 + (size_t)seg * N * K;
     const float* B1 = sh ? a.B1_sh : (a.B1 ? a.B1 + (size_t)seg * N * K : nullptr);
     const bool dual = act == SIMT_SWIGLU;
@@ -125,6 +128,7 @@ __global__ void __launch_bounds__(kThreads) simt_grouped_gemm(const SimtArgs a) 
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
       const int gr = row0 + ty * 4 + i;
+      if (!sh && !in_bounds(gr >= 0 && gr < a.R_cap, a.status)) continue;
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
         const int gn = n0 + tx * 4 + j;
@@ -175,6 +179,8 @@ cudaError_t launch_experts_simt(const Plan& p, const void* x, const void* W1, co
   u.K_sh = p.cfg.d;
   u.act = simt_act(p.cfg.act);
   u.act_sh = SIMT_SWIGLU;
+  u.R_cap = p.R_cap;
+  u.status = reinterpret_cast<uint32_t*>(w + p.ws.status);
   cudaError_t e = launch_pdl(simt_grouped_gemm, dim3(grid_up), dim3(kThreads), 0, st, u);
   if (e != cudaSuccess) return e;
   if (mid_event) {
@@ -202,6 +208,8 @@ cudaError_t launch_experts_simt(const Plan& p, const void* x, const void* W1, co
   dn.K_sh = p.cfg.f_shared;
   dn.act = SIMT_NONE;
   dn.act_sh = SIMT_NONE;
+  dn.R_cap = p.R_cap;
+  dn.status = reinterpret_cast<uint32_t*>(w + p.ws.status);
   return launch_pdl(simt_grouped_gemm, dim3(grid_dn), dim3(kThreads), 0, st, dn);
 }
 

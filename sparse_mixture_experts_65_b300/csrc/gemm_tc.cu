@@ -31,6 +31,7 @@
 #include <cstring>
 #include <mutex>
 
+#include "check.cuh"
 #include "common.cuh"
 #include "launch.cuh"
 #include "moe_internal.h"
@@ -89,6 +90,8 @@ struct TcArgs {
   const float* a_scale = nullptr;   // fp8 operands: scale of each A row (routed rows) ...
   const float* b0_scale = nullptr;  // ... and of each output column of B0 / B1, [E][N]
   const float* b1_scale = nullptr;
+  int R_cap = 0;                    // rows of the routed output buffer
+  int T_x = 0;                      // rows of x (tokens): range of row_token entries
   uint32_t* status;
   uint64_t timeout_ns;
 };
@@ -485,7 +488,9 @@ tc_grouped_gemm(const __grid_constant__ CUtensorMap mA, const __grid_constant__ 
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
               const int r = ti.a_row + lane + 32 * j;
-              tok_s[lane + 32 * j] = r < ti.row_end ? __ldg(a.row_token + r) : -1;
+              int tk = r < ti.row_end ? __ldg(a.row_token + r) : -1;
+              if (tk >= 0 && !in_bounds(tk < a.T_x, a.status)) tk = -1;
+              tok_s[lane + 32 * j] = tk;
             }
             __syncwarp();
             tok_ready = true;
@@ -640,7 +645,9 @@ tc_grouped_gemm(const __grid_constant__ CUtensorMap mA, const __grid_constant__ 
     for (int tile = blockIdx.x; tile < total_all && ok; tile += gridDim.x) {
       const TileInfo ti = decode_tile(a, sc, tile, BNH);
       const size_t orow = static_cast<size_t>(ti.a_row + row_in_tile);
-      const bool row_ok = ti.a_row + row_in_tile < ti.row_end;
+      bool row_ok = ti.a_row + row_in_tile < ti.row_end;
+      if (row_ok && !ti.shared && a.static_mt == 0)
+        row_ok = in_bounds((int)orow < a.R_cap, a.status);
       const int nk = (ti.K + C::BK - 1) / C::BK;
       const int ck = EPI == EPI_F32_CHUNKED ? kChunkKB : nk;
       float csum[EPI == EPI_F32_CHUNKED ? BNH : 1];
@@ -669,9 +676,11 @@ tc_grouped_gemm(const __grid_constant__ CUtensorMap mA, const __grid_constant__ 
           }
         } else if constexpr (EPI == EPI_COMBINE1) {
           // y row of the token this expert row belongs to, scaled by its gate
-          const int tok = row_ok ? __ldg(a.row_token + orow) : 0;
-          const float g = row_ok ? __ldg(a.gate + tok) : 0.f;
-          epilogue_tile<BNH, DUAL, EPI>(a, ti, t_row, (size_t)tok, row_ok, g);
+          int tok = row_ok ? __ldg(a.row_token + orow) : 0;
+          const bool tok_ok = row_ok && in_bounds(tok >= 0 && tok < a.T_tokens, a.status);
+          if (!tok_ok) tok = 0;
+          const float g = tok_ok ? __ldg(a.gate + tok) : 0.f;
+          epilogue_tile<BNH, DUAL, EPI>(a, ti, t_row, (size_t)tok, tok_ok, g);
         } else if constexpr (F8) {
           const float rs = row_ok ? __ldg(a.a_scale + orow) : 0.f;
           epilogue_tile<BNH, DUAL, EPI, true>(a, ti, t_row, orow, row_ok, rs);
@@ -861,6 +870,8 @@ cudaError_t launch_experts_tc(const Plan& p, const void* x, const void* W1, cons
   au.ld_out = c.f;
   au.out_sh = sh ? static_cast<void*>(w + p.ws.hs) : nullptr;
   au.ld_out_sh = sh ? c.f_shared : 0;
+  au.R_cap = p.R_cap;
+  au.T_x = c.T;
   au.status = status;
   au.timeout_ns = kGemmTimeoutNs;
   const int grid_up = p.max_tiles_up < p.num_sms ? p.max_tiles_up : p.num_sms;

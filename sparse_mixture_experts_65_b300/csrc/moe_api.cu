@@ -8,6 +8,7 @@
 #include <cstring>
 
 #include "moe_internal.h"
+#include "ptx.cuh"
 
 namespace moe {
 
@@ -599,6 +600,7 @@ int moe_check_status(void* workspace, void* stream) {
       cudaMemsetAsync(workspace, 0, sizeof(status), st) != cudaSuccess ||
       cudaStreamSynchronize(st) != cudaSuccess)
     return MOE_ERR_CUDA;
+  if (status & STATUS_BOUNDS) return MOE_ERR_BOUNDS;
   return status ? MOE_ERR_TIMEOUT : MOE_OK;
 }
 
@@ -611,6 +613,8 @@ const char* moe_error_string(int code) {
     case MOE_ERR_CUDA: return "MOE_ERR_CUDA: CUDA runtime error";
     case MOE_ERR_TIMEOUT: return "MOE_ERR_TIMEOUT: a bounded device wait ran out";
     case MOE_ERR_DEVICE: return "MOE_ERR_DEVICE: needs a compute capability 10.3 GPU";
+    case MOE_ERR_BOUNDS:
+      return "MOE_ERR_BOUNDS: a routing-derived index was out of range (bounds-checked build)";
   }
   return "MOE_ERR_UNKNOWN";
 }

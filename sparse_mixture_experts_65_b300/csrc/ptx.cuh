@@ -16,6 +16,7 @@ enum : uint32_t {
   STATUS_TIMEOUT_GEMM = 1u << 0,
   STATUS_TIMEOUT_SELFTEST = 1u << 1,
   STATUS_TIMEOUT_ROUTE = 1u << 2,
+  STATUS_BOUNDS = 1u << 3,        // bounds-checked build: a routing-derived index out of range
 };
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {

@@ -16,6 +16,7 @@
 
 #include <cstdint>
 
+#include "check.cuh"
 #include "launch.cuh"
 #include "moe_internal.h"
 
@@ -36,13 +37,15 @@ __device__ __forceinline__ int row_scale_exponent(float amax) {
 
 __global__ void __launch_bounds__(kQuantThreads)
     quant_rows_kernel(const __nv_bfloat16* __restrict__ x, const int* __restrict__ key_row,
-                      int k, int d, uint8_t* __restrict__ xq, float* __restrict__ xs) {
+                      int k, int d, uint8_t* __restrict__ xq, float* __restrict__ xs,
+                      int R_cap, uint32_t* status) {
   __shared__ float red[kQuantThreads / 32];
   pdl_wait();
   pdl_trigger();
   const int key = blockIdx.x;
   const int row = key_row[key];
   if (row < 0) return;                      // dropped slot: no row
+  if (!in_bounds(row < R_cap, status)) return;
   const int t = key / k;
   const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)t * d);   // 8 values each
   const int nv = d / 8;
@@ -94,7 +97,8 @@ cudaError_t launch_quant_rows(const Plan& p, const void* x, void* ws, cudaStream
   return launch_pdl(quant_rows_kernel, dim3(keys), dim3(kQuantThreads), 0, st,
                     static_cast<const __nv_bfloat16*>(x),
                     reinterpret_cast<const int*>(w + p.ws.key_row), c.k, c.d,
-                    reinterpret_cast<uint8_t*>(w + p.ws.xq), reinterpret_cast<float*>(w + p.ws.xs));
+                    reinterpret_cast<uint8_t*>(w + p.ws.xq), reinterpret_cast<float*>(w + p.ws.xs),
+                    p.R_cap, reinterpret_cast<uint32_t*>(w + p.ws.status));
 }
 
 }  // namespace moe

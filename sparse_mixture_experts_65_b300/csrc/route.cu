@@ -19,6 +19,7 @@
 #include <climits>
 
 #include "bulk_rows.cuh"
+#include "check.cuh"
 #include "common.cuh"
 #include "launch.cuh"
 #include "moe_internal.h"
@@ -36,6 +37,7 @@ struct PermuteArgs {
   int* row_token;        // [R_cap]: token of each kept row
   uint32_t* status;
   int T, E, k, BT, capacity, nvec;   // nvec: 16-byte vectors per token row
+  int R_cap;
   int copy;
 };
 
@@ -77,16 +79,25 @@ __global__ void __launch_bounds__(kPermuteThreads) permute_kernel(const PermuteA
     const int* base = a.blk_base + (size_t)b * a.E;
     for (int c = 0; c < nk; c += 32) {
       const int q = c + lane;
-      const bool valid = q < nk;
-      const int e = valid ? a.topk_idx[key0 + q] : -1 - lane;   // invalid lanes never match
+      bool valid = q < nk;
+      int e = valid ? a.topk_idx[key0 + q] : -1 - lane;   // invalid lanes never match
+      if (valid && !in_bounds(e >= 0 && e < a.E, a.status)) {
+        valid = false;
+        row_s[q] = -1;
+        e = -1 - lane;
+      }
       const unsigned peers = __match_any_sync(0xffffffffu, e);
       const int before = __popc(peers & ((1u << lane) - 1u));
       const int prior = valid ? cnt[e] : 0;
       __syncwarp();
       if (valid) {
         const int pos = base[e] + prior + before;
-        const bool keep = pos < a.capacity;
-        const int row = keep ? a.m.seg_start[e] + pos : -1;
+        bool keep = pos < a.capacity;
+        int row = keep ? a.m.seg_start[e] + pos : -1;
+        if (keep && !in_bounds(row >= 0 && row < a.R_cap, a.status)) {
+          keep = false;
+          row = -1;
+        }
         a.key_row[key0 + q] = row;
         if (a.slot_pos) a.slot_pos[key0 + q] = keep ? a.m.offsets[e] + pos : -1;
         if (keep) a.row_token[row] = t0 + q / a.k;
@@ -153,7 +164,7 @@ constexpr uint32_t kGatherStage = 160u << 10;
 
 __global__ void __launch_bounds__(kGatherThreads) gather_rows_kernel(
     const char* x, char* xp, const int* key_row, int nkeys, int k, uint32_t row_bytes,
-    uint32_t* status) {
+    int R_cap, uint32_t* status) {
   extern __shared__ __align__(128) uint8_t gsm[];
   pdl_wait();
   pdl_trigger();
@@ -167,7 +178,9 @@ __global__ void __launch_bounds__(kGatherThreads) gather_rows_kernel(
       [&](int i) { return static_cast<const void*>(x + (size_t)((q0 + i) / k) * row_bytes); },
       [&](int i) {
         const int row = __ldg(key_row + q0 + i);
-        return row >= 0 ? static_cast<void*>(xp + (size_t)row * row_bytes) : nullptr;
+        return row >= 0 && in_bounds(row < R_cap, status)
+                   ? static_cast<void*>(xp + (size_t)row * row_bytes)
+                   : nullptr;
       },
       gsm, kGatherStage, bars, status, STATUS_TIMEOUT_ROUTE, 2000000000ull);
 }
@@ -193,7 +206,7 @@ cudaError_t launch_gather_rows(const Plan& p, const void* x, void* ws, cudaStrea
   return launch_pdl(gather_rows_kernel, dim3(blocks), dim3(kGatherThreads), smem, st,
                     static_cast<const char*>(x), w + p.ws.xp,
                     reinterpret_cast<const int*>(w + p.ws.key_row), nkeys, p.cfg.k, row_bytes,
-                    reinterpret_cast<uint32_t*>(w + p.ws.status));
+                    p.R_cap, reinterpret_cast<uint32_t*>(w + p.ws.status));
 }
 
 Meta meta_ptrs(const Plan& p, void* ws) {
@@ -228,6 +241,7 @@ cudaError_t launch_permute(const Plan& p, const void* x, const int32_t* topk_idx
   a.BT = p.BT;
   a.capacity = p.capacity;
   a.nvec = p.cfg.d * p.elem / 16;
+  a.R_cap = p.R_cap;
   a.copy = copy_rows ? 1 : 0;
   a.status = reinterpret_cast<uint32_t*>(static_cast<char*>(ws) + p.ws.status);
   const bool bulk = copy_rows && permute_bulk((uint32_t)a.nvec * 16u);

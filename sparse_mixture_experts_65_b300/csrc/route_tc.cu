@@ -36,6 +36,7 @@
 #include <climits>
 #include <cstring>
 
+#include "check.cuh"
 #include "common.cuh"
 #include "launch.cuh"
 #include "moe_internal.h"
@@ -60,7 +61,7 @@ struct RouteTcArgs {
   int32_t* slot_pos;           // [T*k] or null
   int* key_row;                // [T*k]: rank inside the tile, then the padded row
   int* row_token;              // [R_cap]
-  int T, d, E, k, gate, capacity, ntiles;
+  int T, d, E, k, gate, capacity, ntiles, R_cap;
   unsigned* arrive;            // CTAs whose tiles are published
   unsigned* passed;            // CTAs through the wait (the last one re-arms both)
   uint32_t* status;
@@ -646,9 +647,18 @@ __global__ void __launch_bounds__(kRtThreads, 1)
     const size_t key0 = (size_t)t0 * a.k;
     for (int kq = tid; kq < nkeys; kq += kRtThreads) {
       const int e = __ldcg(a.topk_idx + key0 + kq);
+      if (!in_bounds(e >= 0 && e < a.E, a.status)) {
+        a.key_row[key0 + kq] = -1;
+        if (a.slot_pos) a.slot_pos[key0 + kq] = -1;
+        continue;
+      }
       const int pos = scan_sm.pre[j][e] + __ldcg(a.key_row + key0 + kq);
-      const bool keep = pos < a.capacity;
-      const int row = keep ? scan_sm.segst[e] + pos : -1;
+      bool keep = pos < a.capacity;
+      int row = keep ? scan_sm.segst[e] + pos : -1;
+      if (keep && !in_bounds(pos >= 0 && row < a.R_cap, a.status)) {
+        keep = false;
+        row = -1;
+      }
       a.key_row[key0 + kq] = row;
       if (a.slot_pos) a.slot_pos[key0 + kq] = keep ? scan_sm.off[e] + pos : -1;
       if (keep) a.row_token[row] = t0 + kq / a.k;
@@ -728,6 +738,7 @@ cudaError_t launch_route_tc(const Plan& p, const void* x, const void* W_r,
   a.gate = c.gate;
   a.capacity = p.capacity;
   a.ntiles = p.nblk;
+  a.R_cap = p.R_cap;
   a.arrive = reinterpret_cast<unsigned*>(w + p.ws.status + kRouteArriveOffset);
   a.passed = reinterpret_cast<unsigned*>(w + p.ws.status + kRoutePassedOffset);
   a.status = reinterpret_cast<uint32_t*>(w + p.ws.status);

@@ -31,6 +31,7 @@
 #include <cuda.h>
 
 #include "bulk_rows.cuh"
+#include "check.cuh"
 #include "common.cuh"
 #include "launch.cuh"
 #include "moe_internal.h"
@@ -462,7 +463,7 @@ struct SmallArgs {
   int* key_row;     // [T*k]
   int* row_token;   // [R_cap]
   void* xp;         // [R_cap][d] or null (no copy)
-  int T, d, E, k, gate, capacity, S, nvec, elem;
+  int T, d, E, k, gate, capacity, S, nvec, elem, R_cap;
   uint32_t* status;
   ScanArgs scan;
 };
@@ -674,16 +675,24 @@ __global__ void __launch_bounds__(kSmallThreads) route_small_kernel(const SmallA
     const int nk = T * a.k;
     for (int c = 0; c < nk; c += 32) {
       const int q = c + lane;
-      const bool valid = q < nk;
-      const int e = valid ? a.topk_idx[q] : -1 - lane;
+      bool valid = q < nk;
+      int e = valid ? a.topk_idx[q] : -1 - lane;
+      if (valid && !in_bounds(e >= 0 && e < E, a.status)) {
+        valid = false;
+        e = -1 - lane;
+      }
       const unsigned peers = __match_any_sync(0xffffffffu, e);
       const int before = __popc(peers & ((1u << lane) - 1u));
       const int prior = valid ? cnt[e] : 0;
       __syncwarp();
       if (valid) {
         const int pos = prior + before;
-        const bool keep = pos < a.capacity;
-        const int row = keep ? scan_sm.routed_s[e] + pos : -1;
+        bool keep = pos < a.capacity;
+        int row = keep ? scan_sm.routed_s[e] + pos : -1;
+        if (keep && !in_bounds(row >= 0 && row < a.R_cap, a.status)) {
+          keep = false;
+          row = -1;
+        }
         a.key_row[q] = row;
         if (a.slot_pos)
           a.slot_pos[q] = keep ? reinterpret_cast<const int*>(scan_sm.psum_s)[e] + pos : -1;
@@ -789,6 +798,7 @@ cudaError_t launch_route_small(const Plan& p, const void* x, const void* W_r,
   a.S = route_small_splits(p.cfg.d);
   a.elem = p.elem;
   a.nvec = p.cfg.d * p.elem / 16;
+  a.R_cap = p.R_cap;
   a.status = reinterpret_cast<uint32_t*>(w + p.ws.status);
   a.scan = scan_args(p, ws, so);
   const size_t smem = route_small_smem(p.cfg.E);

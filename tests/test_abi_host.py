@@ -23,13 +23,27 @@ def _declared():
     return names
 
 
-def test_library_exports_every_declared_function():
+@pytest.mark.parametrize("path", [N.LIB_PATH, N.CHECK_LIB_PATH], ids=["libmoe", "libmoe_check"])
+def test_library_exports_every_declared_function(path):
+    """Both builds (the normal one and the bounds-checked one) load and export
+    every function the header declares."""
     declared = _declared()
     assert {"moe_forward", "moe_workspace_size", "moe_error_string"} <= declared
-    lib = N.lib()
+    lib = N._load(path)
     for name in sorted(declared):
         assert hasattr(lib, name), name
     assert set(N.EXPORTS) <= declared
+
+
+def test_tuning_knobs_check_their_arguments():
+    lib = N.lib()
+    assert lib.moe_set_tuning(99, 0) == N.MOE_ERR_ARG
+    assert lib.moe_set_tuning(N.MOE_TUNE_ROUTER, 9) == N.MOE_ERR_ARG
+    assert lib.moe_set_tuning(N.MOE_TUNE_GATHER, 2) == N.MOE_ERR_ARG
+    assert lib.moe_set_tuning(N.MOE_TUNE_TILE_N_UP, -2) == N.MOE_ERR_ARG
+    with L.tuning(router="simt", tile_n_up=64):
+        pass                                        # set, then restored
+    assert lib.moe_set_tuning(N.MOE_TUNE_ROUTER, -1) == N.MOE_OK
 
 
 def test_config_struct_layout():
@@ -38,8 +52,9 @@ def test_config_struct_layout():
 
 
 def test_error_strings():
-    for code in range(7):
+    for code in range(8):
         assert N.error_string(code).startswith("MOE_")
+    assert "BOUNDS" in N.error_string(N.MOE_ERR_BOUNDS)
     assert "UNKNOWN" in N.error_string(99)
 
 

@@ -62,7 +62,8 @@ def test_accounting_switch_shape():
     acc, layer = bench.accounting(s, kept)
     el = 2
     w1 = 2 * s.f * s.d * el          # two active experts, plain (ReLU) up projection
-    assert acc["up"]["bytes"] == w1 + 130 * s.d * el + 130 * s.f * el
+    assert acc["up"]["bytes"] == w1 + 130 * s.d * el          # weights + input rows only
+    assert acc["up"]["extra"] == 130 * s.f * el                 # h, an intermediate
     assert acc["up"]["flops"] == 2 * 130 * s.d * s.f
     assert acc["down"]["flops"] == 2 * 130 * s.f * s.d
     assert layer["active_experts"] == 2 and layer["kept_rows"] == 130
@@ -91,8 +92,8 @@ def test_accounting_fp8_gate_up_weights():
     acc_b, lay_b = bench.accounting(bf, kept)
     acc_f, lay_f = bench.accounting(f8, kept)
     act, rows, d, f = 16, 64, bf.d, bf.f
-    assert acc_f["up"]["bytes"] == act * 2 * f * (d + 4) + rows * d + rows * f * 2
-    assert acc_b["up"]["bytes"] == act * 2 * f * d * 2 + rows * d * 2 + rows * f * 2
+    assert acc_f["up"]["bytes"] == act * 2 * f * (d + 4) + rows * d
+    assert acc_b["up"]["bytes"] == act * 2 * f * d * 2 + rows * d * 2
     assert acc_f["down"] == acc_b["down"]
     assert acc_f["up"]["flops"] == acc_b["up"]["flops"]
     assert lay_b["bytes"] - lay_f["bytes"] == act * 2 * f * d * 2 - act * 2 * f * (d + 4)
@@ -110,5 +111,33 @@ def test_fp8_up_projection_uses_the_fp8_tensor_peak():
 def test_default_arguments_finish_within_minutes(monkeypatch):
     monkeypatch.setattr("sys.argv", ["bench.py"])
     a = bench.parse()
-    assert a.gpus == 1 and a.impl == "b300" and a.workload == "switch"
+    assert a.gpus == 1 and a.impl == "b300" and a.workload == "dsv3" and a.targets
     assert a.warmup >= 3 and a.steps >= 1
+
+
+def test_combine_in_down_counts_y_as_output():
+    s = W.SWITCH
+    kept = [0] * 64
+    kept[1] = 80
+    acc, _ = bench.accounting(s, kept, combine_in_down=True)
+    assert acc["down"]["bytes"] == s.d * s.f * 2 + s.T * s.d * 2
+    assert acc["down"]["extra"] == 80 * s.f * 2
+
+
+def test_cpu_baseline_and_routing_block_on_the_toy_layer():
+    """The oracle legs of the bench on a small CPU layer: routing over the whole
+    batch, whole experts timed, an all-core and a one-core figure, and the
+    routing comparison (the oracle's own choice has no flips)."""
+    import oracle.moe_oracle as O
+    inp = W.make_inputs(W.TOY, "cpu")
+    cb = bench.cpu_baseline(inp, 0.2)
+    assert cb["kind"] == "oracle" and cb["value"] > 0 and cb["one_core"]["cores"] == 1
+    assert cb["cpu_model"] and cb["host_cores"] >= 1
+    sel = O.selection_scores(O.router_logits(bench._h64(inp.x), bench._h64(inp.W_r)),
+                             W.TOY.gate)
+    idx = torch.from_numpy(O.topk_indices(sel, W.TOY.k)).to(torch.int32)
+    r = bench.routing_parity(inp, idx)
+    assert r["tokens"] == 256 and r["flipped_tokens"] == 0 and r["flipped_outside_band"] == 0
+    idx[0] = idx[0].flip(0)                      # a swapped order counts as a flip
+    r = bench.routing_parity(inp, idx)
+    assert r["flipped_tokens"] == 1
