@@ -41,7 +41,7 @@
 namespace moe {
 
 enum { EPI_SWIGLU = 0, EPI_GELU = 1, EPI_RELU = 2, EPI_OUT16 = 3, EPI_F32_CHUNKED = 4,
-       EPI_COMBINE1 = 5 };
+       EPI_COMBINE1 = 5, EPI_COMBINEK = 6 };
 
 // EPI_OUT16 (down projection when the combine is a separate kernel): the
 // expert output rows o are stored as bf16, rounded once from the float32
@@ -53,6 +53,16 @@ enum { EPI_SWIGLU = 0, EPI_GELU = 1, EPI_RELU = 2, EPI_OUT16 = 3, EPI_F32_CHUNKE
 // directly -- the same float32 product and the same single rounding as the
 // separate combine kernel.  The epilogue warps also write y = 0 for the
 // dropped tokens (key_row < 0).
+
+// EPI_COMBINEK (down projection of every other tensor-core layer): the
+// expert outputs o are stored as for EPI_OUT16, then each row counts itself in
+// for its token and column slice (one counter per token and N tile; the
+// shared expert's row counts too).  The row that completes the count sums the
+// slice, y[t] = bf16(os[t] + sum_j g_tj * o[row(t, j)]) in float32 in the
+// fixed order j = 0..k-1 over the kept slots -- the arithmetic of the
+// separate combine kernel, so the result is the same bit for bit whichever
+// row arrives last -- and re-arms the counter.  Tokens with no kept slot and
+// no shared expert get y = 0 up front.
 
 // EPI_F32_CHUNKED: the reduction runs in chunks of kChunkKB k-blocks (128 k),
 // each accumulated by the tensor cores from zero; the epilogue adds the chunk
@@ -91,6 +101,14 @@ struct TcArgs {
   const float* b0_scale = nullptr;  // ... and of each output column of B0 / B1, [E][N]
   const float* b1_scale = nullptr;
   int R_cap = 0;                    // rows of the routed output buffer
+  int a_rows = 0, a_rows_sh = 0;    // row extents of the routed / shared A maps
+  int zero_pad = 0;                 // partial A tiles: fill the unloaded rows with zeros
+  int m64 = 0;                      // routed tiles of <= 64 rows multiply with M = 64
+  unsigned* cmb_ctr = nullptr;      // EPI_COMBINEK: [T][cmb_nt] arrival counters
+  int cmb_nt = 0;                   // N tiles per token row
+  int k_slots = 1;                  // slots per token (key_row / gate are [T][k_slots])
+  unsigned* zero_ctr = nullptr;     // cleared by this launch (the next launch's counters)
+  int zero_ctr_n = 0;
   int T_x = 0;                      // rows of x (tokens): range of row_token entries
   uint32_t* status;
   uint64_t timeout_ns;
@@ -130,11 +148,14 @@ struct TcCfg {
   static constexpr int SMEM =
       1024 + STAGES * STAGE_BYTES + BAR_BYTES + 4 * SCHED_INTS + TOK_BYTES + CSCALE_BYTES;
   static constexpr uint32_t IDESC = F8 ? idesc_e4m3_f32(BM, MMA_N) : idesc_bf16_f32(BM, MMA_N);
+  // M = 64 for routed tiles with at most 64 rows (the first half of the A tile)
+  static constexpr uint32_t IDESC64 = F8 ? idesc_e4m3_f32(64, MMA_N) : idesc_bf16_f32(64, MMA_N);
 };
 
 struct TileInfo {
   int seg;
   bool shared;
+  bool m64;     // at most 64 rows, multiplied with M = 64
   int a_row;    // first A row (and output row)
   int row_end;  // rows at or past this index are segment padding: not stored
   int n0;       // first output column
@@ -162,6 +183,7 @@ __device__ __forceinline__ TileInfo decode_tile(const TcArgs& a, const Sched& sc
     ti.n0 = n_t * bnh;
     ti.K = a.K;
     ti.N = a.N;
+    ti.m64 = false;
     return ti;
   }
   const int nseg = a.E + a.has_shared;
@@ -182,6 +204,7 @@ __device__ __forceinline__ TileInfo decode_tile(const TcArgs& a, const Sched& sc
   ti.n0 = n_t * bnh;
   ti.K = ti.shared ? a.K_sh : a.K;
   ti.N = ti.shared ? a.N_sh : a.N;
+  ti.m64 = a.m64 && !ti.shared && ti.row_end - ti.a_row <= 64;
   return ti;
 }
 
@@ -265,6 +288,30 @@ __device__ __forceinline__ void epilogue_tile(const TcArgs& a, const TileInfo& t
 // epilogue never stores.
 constexpr int kABox = 32;
 
+// 32-row boxes a partial A tile loads (0: the whole 128-row box).
+__device__ __forceinline__ int a_real_boxes(int rows, int partial_rows) {
+  return rows > partial_rows ? 0 : (rows + kABox - 1) / kABox;
+}
+// Bytes the A loads of one stage deliver.  With zero_pad the boxes past the
+// real rows are loaded too, from a row coordinate past the map's extent: the
+// copy engine fills them with zeros without reading memory, so the padding
+// rows multiply zeros instead of stale data.
+__device__ __forceinline__ uint32_t a_stage_bytes(int boxes, bool zero_pad, uint32_t full) {
+  return boxes == 0 || zero_pad ? full : (uint32_t)boxes * kABox * 128u;
+}
+__device__ __forceinline__ void load_a_stage(uint32_t sa, const CUtensorMap* pA,
+                                             const CUtensorMap* pA32, uint32_t bar, int kx,
+                                             int a_row, int boxes, bool zero_pad, int oob_row) {
+  if (boxes == 0) {
+    tma_load_2d(sa, pA, bar, kx, a_row);
+    return;
+  }
+  for (int b = 0; b < boxes; ++b) tma_load_2d(sa + b * kABox * 128, pA32, bar, kx, a_row + b * kABox);
+  if (zero_pad)
+    for (int b = boxes; b < kTcBM / kABox; ++b)
+      tma_load_2d(sa + b * kABox * 128, pA32, bar, kx, oob_row);
+}
+
 // The A rows of one stage gathered from the token rows of x: 32 warp
 // instructions of 4 whole 128-byte row pieces each (lanes 8r..8r+7 take the
 // 8 16-byte chunks of row 4t + r), written in the 128-byte swizzle the MMA
@@ -287,25 +334,121 @@ __device__ __forceinline__ void gather_stage(uint32_t sa, const int* tok_s, cons
   cp_async_commit_group();
 }
 
+// EPI_COMBINEK: count this row's output slice in for its token.  Returns the
+// token when this row completed the count (its slice is then summed by the
+// whole warp, combine_slice), else -1.
+template <int BNH>
+__device__ __forceinline__ int combine_arrive(const TcArgs& a, const TileInfo& ti, size_t orow) {
+  const int t = ti.shared ? (int)orow : __ldg(a.row_token + orow);
+  if (!in_bounds(t >= 0 && t < a.T_tokens, a.status)) return -1;
+  const int* kr = a.key_row + (size_t)t * a.k_slots;
+  int expect = a.has_shared;
+  for (int j = 0; j < a.k_slots; ++j) expect += __ldg(kr + j) >= 0 ? 1 : 0;
+  unsigned* ctr = a.cmb_ctr + (size_t)t * a.cmb_nt + ti.n0 / BNH;
+  __threadfence();                        // this row's o slice before the count
+  if (atomicAdd(ctr, 1u) + 1u != (unsigned)expect) return -1;
+  __threadfence();                        // every counted slice before the reads
+  *ctr = 0u;                              // re-armed (the up projection also clears)
+  return t;
+}
+
+// y[t][n0 .. n0+BNH) of one token, by the whole warp: lane l takes the eight
+// columns from n0 + 8l on (BNH <= 256), loads the shared expert's slice and the
+// token's slot rows (all loads in flight together), and accumulates in the
+// fixed order os, then j = 0..k-1 -- the separate combine kernel's arithmetic.
+template <int BNH>
+__device__ __forceinline__ void combine_slice(const TcArgs& a, const TileInfo& ti, int t,
+                                              int lane) {
+  static_assert(BNH <= 256, "one 8-column chunk per lane");
+  const int c = lane * 8;
+  const int ncol = ti.N - ti.n0 < BNH ? ti.N - ti.n0 : BNH;
+  const bool act = c < ncol;
+  const __nv_bfloat16* o = static_cast<const __nv_bfloat16*>(a.out);
+  const __nv_bfloat16* os = static_cast<const __nv_bfloat16*>(a.out_sh);
+  const int* kr = a.key_row + (size_t)t * a.k_slots;
+  const float* gt = a.gate + (size_t)t * a.k_slots;
+  float acc[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) acc[i] = 0.f;
+  if (a.has_shared && act) {
+    const uint4 u =
+        __ldcg(reinterpret_cast<const uint4*>(os + (size_t)t * a.ld_out_sh + ti.n0 + c));
+    const __nv_bfloat162* b = reinterpret_cast<const __nv_bfloat162*>(&u);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float2 f = __bfloat1622float2(b[i]);
+      acc[2 * i] = f.x;
+      acc[2 * i + 1] = f.y;
+    }
+  }
+  for (int j0 = 0; j0 < a.k_slots; j0 += 8) {
+    int r[8];
+    float g[8];
+    uint4 v[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int j = j0 + u;
+      r[u] = j < a.k_slots ? __ldg(kr + j) : -1;
+      if (r[u] >= 0 && !in_bounds(r[u] < a.R_cap, a.status)) r[u] = -1;
+      g[u] = j < a.k_slots ? __ldg(gt + j) : 0.f;
+    }
+#pragma unroll
+    for (int u = 0; u < 8; ++u)
+      v[u] = (act && r[u] >= 0)
+                 ? __ldcg(reinterpret_cast<const uint4*>(o + (size_t)r[u] * a.ld_out + ti.n0 + c))
+                 : make_uint4(0, 0, 0, 0);
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      if (r[u] < 0) continue;
+      const __nv_bfloat162* b = reinterpret_cast<const __nv_bfloat162*>(&v[u]);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const float2 f = __bfloat1622float2(b[i]);
+        acc[2 * i] = fmaf(g[u], f.x, acc[2 * i]);
+        acc[2 * i + 1] = fmaf(g[u], f.y, acc[2 * i + 1]);
+      }
+    }
+  }
+  if (!act) return;
+  uint4 pk;
+  uint32_t* pw = reinterpret_cast<uint32_t*>(&pk);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    __nv_bfloat162 b2 = __floats2bfloat162_rn(acc[2 * i], acc[2 * i + 1]);
+    pw[i] = *reinterpret_cast<uint32_t*>(&b2);
+  }
+  *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.y) + (size_t)t * a.ld_y + ti.n0 + c) =
+      pk;
+}
+
+// Where the A rows of routed tiles come from:
+//   AS_TMA  an expert-ordered buffer (xp, h, ...) by 2-D TMA tiles;
+//   AS_CP   the token rows of x, gathered by four producer warps with cp.async;
+//   AS_G4   the token rows of x, gathered by TMA (tile::gather4: four rows of
+//           one 128-byte column slice per instruction, one instruction per lane
+//           of the producer warp).
+enum { AS_TMA = 0, AS_CP = 1, AS_G4 = 2 };
+
 // Warp roles: producer warps (one TMA warp, or four gathering warps), one MMA
 // warp, four epilogue warps.
-template <bool GATHER>
+template <int AS>
 struct TcWarps {
-  static constexpr int PROD = GATHER ? 4 : 1;
+  static constexpr int PROD = AS == AS_CP ? 4 : 1;
   static constexpr int MMA = PROD;
   static constexpr int EPI0 = PROD + 1;
   static constexpr int THREADS = (PROD + 5) * 32;
 };
 
-template <int BNH, bool DUAL, int EPI, bool GATHER, bool F8 = false>
-__global__ void __launch_bounds__(TcWarps<GATHER>::THREADS, 1)
+template <int BNH, bool DUAL, int EPI, int AS, bool F8 = false>
+__global__ void __launch_bounds__(TcWarps<AS>::THREADS, 1)
 tc_grouped_gemm(const __grid_constant__ CUtensorMap mA, const __grid_constant__ CUtensorMap mA_sh,
                 const __grid_constant__ CUtensorMap mA32, const __grid_constant__ CUtensorMap mA32_sh,
                 const __grid_constant__ CUtensorMap mB0, const __grid_constant__ CUtensorMap mB1,
                 const __grid_constant__ CUtensorMap mB0_sh,
                 const __grid_constant__ CUtensorMap mB1_sh, const TcArgs a) {
   using C = TcCfg<BNH, DUAL, EPI, F8>;
-  static_assert(!F8 || (EPI == EPI_SWIGLU && !GATHER), "fp8 operands: SwiGLU up projection");
+  constexpr bool GATHER = AS == AS_CP;
+  static_assert(!F8 || (EPI == EPI_SWIGLU && AS == AS_TMA), "fp8 operands: SwiGLU up projection");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -349,7 +492,7 @@ tc_grouped_gemm(const __grid_constant__ CUtensorMap mA, const __grid_constant__ 
       if (DUAL) tma_prefetch_desc(&mB1_sh);
     }
   }
-  using Wr = TcWarps<GATHER>;
+  using Wr = TcWarps<AS>;
   if (warp == Wr::MMA) {
     tmem_alloc(smem_u32(tmem_slot), C::TMEM_COLS);
     tmem_relinquish();
@@ -387,14 +530,14 @@ tc_grouped_gemm(const __grid_constant__ CUtensorMap mA, const __grid_constant__ 
   if (a.early_b) copy_sched();
   const int total = a.static_mt > 0 ? a.static_total : (a.early_b ? s_tp[a.E + a.has_shared] : 0);
   uint32_t npre = 0;   // uses whose B tiles were issued before the wait
-  if (!GATHER && a.early_b && warp == 0 && lane == 0) {
+  if (AS == AS_TMA && a.early_b && warp == 0 && lane == 0) {
     for (int tile = blockIdx.x; tile < total && npre < (uint32_t)C::STAGES; tile += gridDim.x) {
       const TileInfo ti = decode_tile(a, sc, tile, BNH);
       const int e = ti.shared ? 0 : ti.seg;
       const int nk = (ti.K + C::BK - 1) / C::BK;
       const int rows = ti.row_end - ti.a_row < kTcBM ? ti.row_end - ti.a_row : kTcBM;
-      const int a_boxes = rows > a.partial_rows ? 0 : (rows + kABox - 1) / kABox;
-      const uint32_t a_bytes = a_boxes ? a_boxes * kABox * 128u : (uint32_t)C::A_BYTES;
+      const int a_boxes = a_real_boxes(rows, a.partial_rows);
+      const uint32_t a_bytes = a_stage_bytes(a_boxes, a.zero_pad, C::A_BYTES);
       for (int kb = 0; kb < nk && npre < (uint32_t)C::STAGES; ++kb, ++npre) {
         const uint32_t sb = smem_base + npre * C::STAGE_BYTES + C::A_BYTES;
         mbar_arrive_expect_tx(full_bar(npre), a_bytes + C::B_BYTES);
@@ -407,6 +550,10 @@ tc_grouped_gemm(const __grid_constant__ CUtensorMap mA, const __grid_constant__ 
   }
   pdl_wait();      // everything above ran while the previous kernel finished
   pdl_trigger();
+  // counters the next launch (the down projection's combine) starts from
+  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < a.zero_ctr_n;
+       i += gridDim.x * blockDim.x)
+    a.zero_ctr[i] = 0u;
   if (!a.early_b) copy_sched();
   const int total_all =
       a.static_mt > 0 ? a.static_total : sc.tp[a.E + a.has_shared];
@@ -445,9 +592,8 @@ tc_grouped_gemm(const __grid_constant__ CUtensorMap mA, const __grid_constant__ 
         const CUtensorMap* pB1 = ti.shared ? &mB1_sh : &mB1;
         const int e = ti.shared ? 0 : ti.seg;
         const int rows = ti.row_end - ti.a_row < kTcBM ? ti.row_end - ti.a_row : kTcBM;
-        const int a_boxes = gat || rows > a.partial_rows ? 0 : (rows + kABox - 1) / kABox;
-        const uint32_t a_bytes =
-            gat ? 0u : (a_boxes ? a_boxes * kABox * 128u : (uint32_t)C::A_BYTES);
+        const int a_boxes = gat ? 0 : a_real_boxes(rows, a.partial_rows);
+        const uint32_t a_bytes = gat ? 0u : a_stage_bytes(a_boxes, a.zero_pad, C::A_BYTES);
         // token of every row of the tile (-1 for padding rows), per warp;
         // loaded after the warp's first B tile of the tile is in flight
         int* tok_s = reinterpret_cast<int*>(smem + C::STAGES * C::STAGE_BYTES + C::BAR_BYTES +
@@ -471,15 +617,9 @@ tc_grouped_gemm(const __grid_constant__ CUtensorMap mA, const __grid_constant__ 
           const uint32_t sb = sa + C::A_BYTES;
           if (lane == 0) {
             mbar_arrive_expect_tx(full_bar(s), a_bytes + C::B_BYTES);
-            if (!gat) {
-              if (a_boxes == 0) {
-                tma_load_2d(sa, &mA_sh, full_bar(s), kb * C::BKX, ti.a_row);
-              } else {
-                for (int b = 0; b < a_boxes; ++b)
-                  tma_load_2d(sa + b * kABox * 128, &mA32_sh, full_bar(s), kb * C::BKX,
-                              ti.a_row + b * kABox);
-              }
-            }
+            if (!gat)
+              load_a_stage(sa, &mA_sh, &mA32_sh, full_bar(s), kb * C::BKX, ti.a_row, a_boxes,
+                           a.zero_pad, a.a_rows_sh);
             tma_load_3d(sb, pB0, full_bar(s), kb * C::BKX, ti.n0, e);
             if (DUAL) tma_load_3d(sb + BNH * 128, pB1, full_bar(s), kb * C::BKX, ti.n0, e);
           }
@@ -519,6 +659,83 @@ tc_grouped_gemm(const __grid_constant__ CUtensorMap mA, const __grid_constant__ 
           }
         }
       }
+    } else if constexpr (AS == AS_G4) {
+      // ---------------- TMA row-gather producer (whole warp) ----------------
+      // Routed tiles: lane l gathers rows 4l .. 4l+3 of the tile (tokens
+      // row_token[a_row + 4l + i]; rows past the segment's last kept row
+      // repeat the tile's first token, they feed accumulator rows that are
+      // never stored) with one tile::gather4 copy per stage, into bytes
+      // 512l .. 512l+511 of the 128-byte-swizzled A tile -- the layout a
+      // 128-row box load produces.  Lane 0 sets the stage's transaction count
+      // and issues the B tiles (and the shared expert's A tiles) first.
+      uint32_t g = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; tile < total_all && ok; tile += gridDim.x) {
+        const TileInfo ti = decode_tile(a, sc, tile, BNH);
+        const CUtensorMap* pB0 = ti.shared ? &mB0_sh : &mB0;
+        const CUtensorMap* pB1 = ti.shared ? &mB1_sh : &mB1;
+        const int e = ti.shared ? 0 : ti.seg;
+        const int nk = (ti.K + C::BK - 1) / C::BK;
+        const int rows = ti.row_end - ti.a_row < kTcBM ? ti.row_end - ti.a_row : kTcBM;
+        const int a_boxes = a_real_boxes(rows, a.partial_rows);
+        const uint32_t a_sh_bytes = a_stage_bytes(a_boxes, a.zero_pad, C::A_BYTES);
+        int tk0 = 0, tk1 = 0, tk2 = 0, tk3 = 0;
+        if (!ti.shared) {
+          int tk[4];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const int r = ti.a_row + 4 * lane + i;
+            int v = r < ti.row_end ? __ldg(a.row_token + r) : -1;
+            if (v >= 0 && !in_bounds(v < a.T_x, a.status)) v = -1;
+            tk[i] = v;
+          }
+          int first = __shfl_sync(0xffffffffu, tk[0], 0);   // row a_row: always kept
+          if (first < 0) first = 0;
+          tk0 = tk[0] < 0 ? first : tk[0];
+          tk1 = tk[1] < 0 ? first : tk[1];
+          tk2 = tk[2] < 0 ? first : tk[2];
+          tk3 = tk[3] < 0 ? first : tk[3];
+        }
+        for (int kb = 0; kb < nk; ++kb, ++g) {
+          const int s = g % C::STAGES;
+          const uint32_t ph = (g / C::STAGES) & 1u;
+          int okw = 1;
+          if (lane == 0)
+            okw = mbar_wait_bounded(empty_bar(s), ph ^ 1u, a.timeout_ns, abort_flag) ? 1 : 0;
+          okw = __shfl_sync(0xffffffffu, okw, 0);
+          if (!okw) {
+            if (lane == 0) give_up();
+            ok = false;
+            break;
+          }
+          const uint32_t sa = smem_base + s * C::STAGE_BYTES;
+          const uint32_t sb = sa + C::A_BYTES;
+          if (lane == 0) {
+            mbar_arrive_expect_tx(full_bar(s),
+                                  (ti.shared ? a_sh_bytes : (uint32_t)C::A_BYTES) + C::B_BYTES);
+            if (ti.shared)
+              load_a_stage(sa, &mA_sh, &mA32_sh, full_bar(s), kb * C::BKX, ti.a_row, a_boxes,
+                           a.zero_pad, a.a_rows_sh);
+            tma_load_3d(sb, pB0, full_bar(s), kb * C::BKX, ti.n0, e);
+            if (DUAL) tma_load_3d(sb + BNH * 128, pB1, full_bar(s), kb * C::BKX, ti.n0, e);
+          }
+          __syncwarp();
+          if (!ti.shared)
+            tma_gather4(sa + lane * 512u, &mA, full_bar(s), kb * C::BKX, tk0, tk1, tk2, tk3);
+        }
+      }
+      // nothing asynchronous may still target shared memory at exit
+      if (lane == 0) {
+        for (int s = 0; s < C::STAGES; ++s) {
+          if (g > static_cast<uint32_t>(s)) {
+            const uint32_t issues = (g - 1 - s) / C::STAGES + 1;
+            if (ok)
+              mbar_wait_bounded(empty_bar(s), (issues - 1) & 1u, a.timeout_ns, abort_flag);
+            else
+              mbar_wait_bounded(full_bar(s), (issues - 1) & 1u, a.timeout_ns, nullptr);
+          }
+        }
+      }
     } else if (lane == 0) {
       // ---------------- TMA producer ----------------
       uint32_t g = 0;
@@ -532,8 +749,9 @@ tc_grouped_gemm(const __grid_constant__ CUtensorMap mA, const __grid_constant__ 
         const int e = ti.shared ? 0 : ti.seg;
         const int nk = (ti.K + C::BK - 1) / C::BK;
         const int rows = ti.row_end - ti.a_row < kTcBM ? ti.row_end - ti.a_row : kTcBM;
-        const int a_boxes = rows > a.partial_rows ? 0 : (rows + kABox - 1) / kABox;
-        const uint32_t a_bytes = a_boxes ? a_boxes * kABox * 128u : (uint32_t)C::A_BYTES;
+        const int a_boxes = a_real_boxes(rows, a.partial_rows);
+        const uint32_t a_bytes = a_stage_bytes(a_boxes, a.zero_pad, C::A_BYTES);
+        const int oob_row = ti.shared ? a.a_rows_sh : a.a_rows;
         for (int kb = 0; kb < nk; ++kb, ++g) {
           const int s = g % C::STAGES;
           const uint32_t ph = (g / C::STAGES) & 1u;
@@ -546,12 +764,8 @@ tc_grouped_gemm(const __grid_constant__ CUtensorMap mA, const __grid_constant__ 
           const uint32_t sa = smem_base + s * C::STAGE_BYTES;
           const uint32_t sb = sa + C::A_BYTES;
           if (!pre) mbar_arrive_expect_tx(full_bar(s), a_bytes + C::B_BYTES);
-          if (a_boxes == 0) {
-            tma_load_2d(sa, pA, full_bar(s), kb * C::BKX, ti.a_row);
-          } else {
-            for (int b = 0; b < a_boxes; ++b)
-              tma_load_2d(sa + b * kABox * 128, pA32, full_bar(s), kb * C::BKX, ti.a_row + b * kABox);
-          }
+          load_a_stage(sa, pA, pA32, full_bar(s), kb * C::BKX, ti.a_row, a_boxes, a.zero_pad,
+                       oob_row);
           if (!pre) {
             tma_load_3d(sb, pB0, full_bar(s), kb * C::BKX, ti.n0, e);
             if (DUAL) tma_load_3d(sb + BNH * 128, pB1, full_bar(s), kb * C::BKX, ti.n0, e);
@@ -593,6 +807,7 @@ tc_grouped_gemm(const __grid_constant__ CUtensorMap mA, const __grid_constant__ 
           tc_fence_after();
           const uint32_t d_tmem = tmem_base + ab * C::MMA_N;
           const int kb1 = kb0 + ck < nk ? kb0 + ck : nk;
+          const uint32_t idesc = ti.m64 ? C::IDESC64 : C::IDESC;
           for (int kb = kb0; kb < kb1; ++kb, ++g) {
             const int s = g % C::STAGES;
             const uint32_t ph = (g / C::STAGES) & 1u;
@@ -609,9 +824,9 @@ tc_grouped_gemm(const __grid_constant__ CUtensorMap mA, const __grid_constant__ 
               const uint64_t ad = smem_desc_k128(sa + kk * 32);
               const uint64_t bd = smem_desc_k128(sb + kk * 32);
               if constexpr (F8)
-                tc_mma_f8(d_tmem, ad, bd, C::IDESC, (kb != kb0 || kk != 0) ? 1u : 0u);
+                tc_mma_f8(d_tmem, ad, bd, idesc, (kb != kb0 || kk != 0) ? 1u : 0u);
               else
-                tc_mma_bf16(d_tmem, ad, bd, C::IDESC, (kb != kb0 || kk != 0) ? 1u : 0u);
+                tc_mma_bf16(d_tmem, ad, bd, idesc, (kb != kb0 || kk != 0) ? 1u : 0u);
             }
             tc_commit(empty_bar(s));
           }
@@ -640,12 +855,29 @@ tc_grouped_gemm(const __grid_constant__ CUtensorMap mA, const __grid_constant__ 
           for (int c = lane; c < nvec; c += 32) y[(size_t)t * nvec + c] = make_uint4(0, 0, 0, 0);
       }
     }
+    if constexpr (EPI == EPI_COMBINEK) {
+      // tokens that no row will count in for (every slot dropped, no shared
+      // expert) get y = 0
+      if (!a.has_shared) {
+        uint4* y = static_cast<uint4*>(a.y);
+        const int nvec = a.ld_y * 2 / 16;
+        const int gw = blockIdx.x * 4 + (warp - Wr::EPI0), nw = gridDim.x * 4;
+        for (int t = gw; t < a.T_tokens; t += nw) {
+          bool any = false;
+          for (int j = 0; j < a.k_slots; ++j) any |= __ldg(a.key_row + (size_t)t * a.k_slots + j) >= 0;
+          if (!any)
+            for (int c = lane; c < nvec; c += 32) y[(size_t)t * nvec + c] = make_uint4(0, 0, 0, 0);
+        }
+      }
+    }
     int it = 0;
     bool ok = true;
     for (int tile = blockIdx.x; tile < total_all && ok; tile += gridDim.x) {
       const TileInfo ti = decode_tile(a, sc, tile, BNH);
-      const size_t orow = static_cast<size_t>(ti.a_row + row_in_tile);
-      bool row_ok = ti.a_row + row_in_tile < ti.row_end;
+      // M = 64: rows 16q .. 16q+15 sit in the first 16 lanes of quarter q
+      const int rit = !ti.m64 ? row_in_tile : (lane < 16 ? q * 16 + lane : kTcBM);
+      const size_t orow = static_cast<size_t>(ti.a_row + rit);
+      bool row_ok = rit < kTcBM && ti.a_row + rit < ti.row_end;
       if (row_ok && !ti.shared && a.static_mt == 0)
         row_ok = in_bounds((int)orow < a.R_cap, a.status);
       const int nk = (ti.K + C::BK - 1) / C::BK;
@@ -689,6 +921,18 @@ tc_grouped_gemm(const __grid_constant__ CUtensorMap mA, const __grid_constant__ 
         }
         tc_fence_before();
         mbar_arrive(tempty_bar(ab));
+        if constexpr (EPI == EPI_COMBINEK) {
+          // rows that completed their token's count; the warp sums each one's
+          // slice together
+          const int tl = row_ok ? combine_arrive<BNH>(a, ti, orow) : -1;
+          const unsigned am = __activemask();
+          unsigned m = __ballot_sync(am, tl >= 0);
+          while (m) {
+            const int src = __ffs(m) - 1;
+            m &= m - 1u;
+            combine_slice<BNH>(a, ti, __shfl_sync(am, tl, src), lane);
+          }
+        }
       }
       if constexpr (EPI == EPI_F32_CHUNKED) {
         if (ok && row_ok) {
@@ -716,41 +960,41 @@ struct TcMaps {
   CUtensorMap A, A_sh, A32, A32_sh, B0, B1, B0_sh, B1_sh;
 };
 
-template <int BNH, bool DUAL, int EPI, bool GATHER = false, bool F8 = false>
+template <int BNH, bool DUAL, int EPI, int AS = AS_TMA, bool F8 = false>
 static cudaError_t run_tc(const TcMaps& m, const TcArgs& a, int grid, cudaStream_t st) {
   using C = TcCfg<BNH, DUAL, EPI, F8>;
   static std::atomic<uint64_t> attr_done{0};
-  auto kern = tc_grouped_gemm<BNH, DUAL, EPI, GATHER, F8>;
+  auto kern = tc_grouped_gemm<BNH, DUAL, EPI, AS, F8>;
   cudaError_t e = smem_attr_once(kern, C::SMEM, attr_done);
   if (e != cudaSuccess) return e;
-  return launch_pdl(kern, dim3(grid), dim3(TcWarps<GATHER>::THREADS), C::SMEM, st, m.A, m.A_sh,
+  return launch_pdl(kern, dim3(grid), dim3(TcWarps<AS>::THREADS), C::SMEM, st, m.A, m.A_sh,
                     m.A32, m.A32_sh, m.B0,
                     m.B1, m.B0_sh, m.B1_sh, a);
 }
 
-template <bool GATHER>
+template <int AS>
 static cudaError_t dispatch_up_t(int bn, int act, const TcMaps& m, const TcArgs& a, int grid,
                                  cudaStream_t st) {
   if (act == MOE_ACT_SWIGLU) {
     switch (bn) {
-      case 128: return run_tc<128, true, EPI_SWIGLU, GATHER>(m, a, grid, st);
-      case 96: return run_tc<96, true, EPI_SWIGLU, GATHER>(m, a, grid, st);
-      case 64: return run_tc<64, true, EPI_SWIGLU, GATHER>(m, a, grid, st);
-      case 32: return run_tc<32, true, EPI_SWIGLU, GATHER>(m, a, grid, st);
+      case 128: return run_tc<128, true, EPI_SWIGLU, AS>(m, a, grid, st);
+      case 96: return run_tc<96, true, EPI_SWIGLU, AS>(m, a, grid, st);
+      case 64: return run_tc<64, true, EPI_SWIGLU, AS>(m, a, grid, st);
+      case 32: return run_tc<32, true, EPI_SWIGLU, AS>(m, a, grid, st);
     }
   } else if (act == MOE_ACT_RELU) {
     switch (bn) {
-      case 256: return run_tc<256, false, EPI_RELU, GATHER>(m, a, grid, st);
-      case 128: return run_tc<128, false, EPI_RELU, GATHER>(m, a, grid, st);
-      case 96: return run_tc<96, false, EPI_RELU, GATHER>(m, a, grid, st);
-      case 64: return run_tc<64, false, EPI_RELU, GATHER>(m, a, grid, st);
+      case 256: return run_tc<256, false, EPI_RELU, AS>(m, a, grid, st);
+      case 128: return run_tc<128, false, EPI_RELU, AS>(m, a, grid, st);
+      case 96: return run_tc<96, false, EPI_RELU, AS>(m, a, grid, st);
+      case 64: return run_tc<64, false, EPI_RELU, AS>(m, a, grid, st);
     }
   } else {
     switch (bn) {
-      case 256: return run_tc<256, false, EPI_GELU, GATHER>(m, a, grid, st);
-      case 128: return run_tc<128, false, EPI_GELU, GATHER>(m, a, grid, st);
-      case 96: return run_tc<96, false, EPI_GELU, GATHER>(m, a, grid, st);
-      case 64: return run_tc<64, false, EPI_GELU, GATHER>(m, a, grid, st);
+      case 256: return run_tc<256, false, EPI_GELU, AS>(m, a, grid, st);
+      case 128: return run_tc<128, false, EPI_GELU, AS>(m, a, grid, st);
+      case 96: return run_tc<96, false, EPI_GELU, AS>(m, a, grid, st);
+      case 64: return run_tc<64, false, EPI_GELU, AS>(m, a, grid, st);
     }
   }
   return cudaErrorInvalidValue;
@@ -760,22 +1004,33 @@ static cudaError_t dispatch_up_t(int bn, int act, const TcMaps& m, const TcArgs&
 static cudaError_t dispatch_up_f8(int bn, const TcMaps& m, const TcArgs& a, int grid,
                                   cudaStream_t st) {
   switch (bn) {
-    case 128: return run_tc<128, true, EPI_SWIGLU, false, true>(m, a, grid, st);
-    case 96: return run_tc<96, true, EPI_SWIGLU, false, true>(m, a, grid, st);
-    case 64: return run_tc<64, true, EPI_SWIGLU, false, true>(m, a, grid, st);
-    case 32: return run_tc<32, true, EPI_SWIGLU, false, true>(m, a, grid, st);
+    case 128: return run_tc<128, true, EPI_SWIGLU, AS_TMA, true>(m, a, grid, st);
+    case 96: return run_tc<96, true, EPI_SWIGLU, AS_TMA, true>(m, a, grid, st);
+    case 64: return run_tc<64, true, EPI_SWIGLU, AS_TMA, true>(m, a, grid, st);
+    case 32: return run_tc<32, true, EPI_SWIGLU, AS_TMA, true>(m, a, grid, st);
   }
   return cudaErrorInvalidValue;
 }
 
-static cudaError_t dispatch_up(bool gather, int bn, int act, const TcMaps& m, const TcArgs& a,
+static cudaError_t dispatch_up(int as, int bn, int act, const TcMaps& m, const TcArgs& a,
                                int grid, cudaStream_t st) {
-  return gather ? dispatch_up_t<true>(bn, act, m, a, grid, st)
-                : dispatch_up_t<false>(bn, act, m, a, grid, st);
+  return as == AS_CP   ? dispatch_up_t<AS_CP>(bn, act, m, a, grid, st)
+         : as == AS_G4 ? dispatch_up_t<AS_G4>(bn, act, m, a, grid, st)
+                       : dispatch_up_t<AS_TMA>(bn, act, m, a, grid, st);
 }
 
-static cudaError_t dispatch_down(int bn, bool combine1, const TcMaps& m, const TcArgs& a,
-                                 int grid, cudaStream_t st) {
+static cudaError_t dispatch_down(int bn, bool combine1, bool combinek, const TcMaps& m,
+                                 const TcArgs& a, int grid, cudaStream_t st) {
+  if (combinek) {
+    switch (bn) {
+      case 256: return run_tc<256, false, EPI_COMBINEK>(m, a, grid, st);
+      case 192: return run_tc<192, false, EPI_COMBINEK>(m, a, grid, st);
+      case 128: return run_tc<128, false, EPI_COMBINEK>(m, a, grid, st);
+      case 96: return run_tc<96, false, EPI_COMBINEK>(m, a, grid, st);
+      case 64: return run_tc<64, false, EPI_COMBINEK>(m, a, grid, st);
+    }
+    return cudaErrorInvalidValue;
+  }
   if (combine1) {
     switch (bn) {
       case 256: return run_tc<256, false, EPI_COMBINE1>(m, a, grid, st);
@@ -818,11 +1073,13 @@ cudaError_t launch_experts_tc(const Plan& p, const void* x, const void* W1, cons
   // (fp8 gate/up weights: A is the e4m3 copy xq of the routed rows, one
   // scale per row in xs; B holds e4m3 codes with one scale per column)
   const int el = p.fp8 ? 1 : 2;
+  const bool from_x = p.gather || p.gather4;
   const void* a_src = p.fp8 ? static_cast<const void*>(w + p.ws.xq)
-                      : p.gather ? x : static_cast<const void*>(w + p.ws.xp);
-  const uint64_t a_rows = p.gather ? (uint64_t)c.T : (uint64_t)p.R_cap;
+                      : from_x ? x : static_cast<const void*>(w + p.ws.xp);
+  const uint64_t a_rows = from_x ? (uint64_t)c.T : (uint64_t)p.R_cap;
   TcMaps mu;
-  bool ok = encode_2d(&mu.A, a_src, a_rows, c.d, kTcBM, el);
+  // the row-gathering TMA reads boxes one row high
+  bool ok = encode_2d(&mu.A, a_src, a_rows, c.d, p.gather4 ? 1u : (uint32_t)kTcBM, el);
   ok = ok && encode_2d(&mu.A32, a_src, a_rows, c.d, kABox, el);
   ok = ok && encode_3d(&mu.B0, W1, c.E, c.f, c.d, p.up_bn, el);
   ok = ok && encode_3d(&mu.B1, dual ? W3 : W1, c.E, c.f, c.d, p.up_bn, el);
@@ -872,11 +1129,19 @@ cudaError_t launch_experts_tc(const Plan& p, const void* x, const void* W1, cons
   au.ld_out_sh = sh ? c.f_shared : 0;
   au.R_cap = p.R_cap;
   au.T_x = c.T;
+  au.a_rows = (int)a_rows;
+  au.a_rows_sh = c.T;
+  au.zero_pad = p.zero_pad ? 1 : 0;
+  au.m64 = p.m64 ? 1 : 0;
+  unsigned* cmb_ctr = p.combine_k ? reinterpret_cast<unsigned*>(w + p.ws.cmb_ctr) : nullptr;
+  au.zero_ctr = cmb_ctr;
+  au.zero_ctr_n = p.combine_k ? c.T * p.nt_dn : 0;
   au.status = status;
   au.timeout_ns = kGemmTimeoutNs;
   const int grid_up = p.max_tiles_up < p.num_sms ? p.max_tiles_up : p.num_sms;
+  const int as = p.gather ? AS_CP : p.gather4 ? AS_G4 : AS_TMA;
   cudaError_t e = p.fp8 ? dispatch_up_f8(p.up_bn, mu, au, grid_up, st)
-                        : dispatch_up(p.gather, p.up_bn, c.act, mu, au, grid_up, st);
+                        : dispatch_up(as, p.up_bn, c.act, mu, au, grid_up, st);
   if (e != cudaSuccess) return e;
   if (mid_event) {
     e = cudaEventRecord(mid_event, st);
@@ -902,14 +1167,21 @@ cudaError_t launch_experts_tc(const Plan& p, const void* x, const void* W1, cons
   if (!ok) return cudaErrorInvalidValue;
   TcArgs ad = au;
   ad.partial_rows = p.partial_rows;
+  ad.a_rows = p.R_cap;
+  ad.a_rows_sh = p.T_pad;
   ad.early_b = 1;   // the schedule comes from the routing kernel, two launches back
-  if (p.combine_in_down) {
+  ad.zero_ctr = nullptr;
+  ad.zero_ctr_n = 0;
+  if (p.combine_in_down || p.combine_k) {
     ad.row_token = reinterpret_cast<const int*>(w + p.ws.row_token);
     ad.gate = topk_w;
     ad.y = y;
     ad.ld_y = c.d;
     ad.key_row = reinterpret_cast<const int*>(w + p.ws.key_row);
     ad.T_tokens = c.T;
+    ad.k_slots = c.k;
+    ad.cmb_ctr = cmb_ctr;
+    ad.cmb_nt = p.nt_dn;
   }
   ad.tp = meta.tp_dn;
   ad.N = c.d;
@@ -921,7 +1193,7 @@ cudaError_t launch_experts_tc(const Plan& p, const void* x, const void* W1, cons
   ad.out_sh = sh ? static_cast<void*>(w + p.ws.os) : nullptr;
   ad.ld_out_sh = sh ? c.d : 0;
   const int grid_dn = p.max_tiles_dn < p.num_sms ? p.max_tiles_dn : p.num_sms;
-  return dispatch_down(p.dn_bn, p.combine_in_down, md, ad, grid_dn, st);
+  return dispatch_down(p.dn_bn, p.combine_in_down, p.combine_k, md, ad, grid_dn, st);
 }
 
 // ---------------------------------------------------------------- router
@@ -953,6 +1225,8 @@ cudaError_t launch_router_tc(const Plan& p, const void* x, const void* W_r,
   a.ld_out = c.E;
   a.rows_sh = c.T;
   a.static_mt = (c.T + kTcBM - 1) / kTcBM;
+  a.a_rows = c.T;
+  a.a_rows_sh = c.T;
   a.static_total = a.static_mt * ((c.E + bn - 1) / bn);
   a.col_bias = logit_offset;
   a.partial_rows = p.partial_rows;

@@ -41,7 +41,7 @@ int make_plan(const moe_config* cfg, WsKind kind, Plan* p, int num_sms);
 
 // Process-wide overrides set through moe_set_tuning (tests and tile sweeps
 // only); -1 = no override.  Production calls never read the environment.
-static std::atomic<int> g_tune[MOE_TUNE_COUNT] = {-1, -1, -1, -1, -1};
+static std::atomic<int> g_tune[MOE_TUNE_COUNT] = {-1, -1, -1, -1, -1, -1, -1, -1};
 
 int tuning(int knob) {
   return knob >= 0 && knob < MOE_TUNE_COUNT ? g_tune[knob].load(std::memory_order_relaxed) : -1;
@@ -208,20 +208,51 @@ int make_plan(const moe_config* cfg, WsKind kind, Plan* p, int num_sms) {
     const int v = tuning(MOE_TUNE_PARTIAL_A_ROWS);
     P.partial_rows = v >= 0 ? v : 64;
     P.partial_rows_up = v >= 0 ? P.partial_rows : (c.act == MOE_ACT_SWIGLU ? 0 : 64);
+    // the rows a partial tile does not load are filled with zeros by the copy
+    // engine (a box past the map's extent), so that padding rows multiply
+    // zeros rather than stale stage data
+    const int z = tuning(MOE_TUNE_ZERO_PAD);
+    P.zero_pad = z >= 0 ? z != 0 : false;
+    // routed tiles with at most 64 rows (the last tile of a segment, small
+    // segments) issue M = 64 MMAs: half the tensor work of an M = 128 tile
+    const int m = tuning(MOE_TUNE_MMA_M64);
+    P.m64 = m >= 0 ? m != 0 : true;
   }
   P.combine_in_down = P.tc && c.k == 1 && c.n_shared == 0;
+  // Other tensor-core layers can combine in the down projection's epilogue
+  // as well (the last row of a token's column slice sums it, in the fixed
+  // slot order: y is the separate kernel's bit for bit).  The rows it sums
+  // were written long before (a token's k slots lie in k different experts),
+  // so the fused form moves the same bytes as the separate combine kernel,
+  // inside an HBM-bound projection, and stalls its epilogue on the reads:
+  // measured slower on every layer shape (DeepSeek-V3-shaped 5.18 -> 5.37 ms,
+  // Mixtral-shaped 4.78 -> 4.81, gpt-oss-shaped T = 16 0.486 -> 0.492), so
+  // the separate kernel is the default and an override of 1 selects the fused
+  // form.
+  {
+    const int fc = tuning(MOE_TUNE_FUSED_COMBINE);
+    P.combine_k = P.tc && !P.combine_in_down && fc == 1;
+  }
   // The up projection gathers the token rows itself (cp.async) for
   // tensor-core layers routed in one launch whose experts average at most
   // one 128-row tile: there the weights dominate and the gather costs
-  // nothing (measured: Switch layer).  Wider experts (Mixtral-like) and the
-  // split router read an expert-ordered copy through TMA, which keeps the
-  // compute-bound up projection fed.  A gather override (0 / 1) forces either.
+  // nothing (measured: Switch layer).  Wider experts re-read each A tile for
+  // every N tile, and a gather per N tile costs more than one copy of the
+  // rows into expert order (measured on B300 for both the cp.async gather
+  // and the TMA row gather, tile::gather4: DeepSeek-V3-shaped up projection
+  // 2.96 -> 6.26 ms with the latter), so they read an expert-ordered copy
+  // through TMA.  A gather override forces a source: 0 the expert-ordered
+  // copy, 1 cp.async, 2 the TMA row gather.
   {
     const long long per_expert = Tk / (c.E > 0 ? c.E : 1);
     P.gather = P.tc && P.route_tc && per_expert <= kTcBM;
+    P.gather4 = false;
     const int gv = tuning(MOE_TUNE_GATHER);
-    if (gv >= 0 && P.tc) P.gather = gv != 0;
-    if (P.fp8) P.gather = false;   // the fp8 up projection reads the quantised rows by TMA
+    if (gv >= 0 && P.tc) {
+      P.gather = gv == 1;
+      P.gather4 = gv == 2;
+    }
+    if (P.fp8) P.gather = P.gather4 = false;   // fp8: the quantised rows are read by TMA
   }
   P.nt_up = ceil_div(c.f, P.up_bn);
   P.nt_dn = ceil_div(c.d, P.dn_bn);
@@ -257,7 +288,7 @@ int make_plan(const moe_config* cfg, WsKind kind, Plan* p, int num_sms) {
   L.row_token = take(sizeof(int) * (size_t)P.R_cap);
   if (kind != WsKind::Route) {
     const size_t act_elem = P.elem;   // h is bf16 on the tensor-core path, fp32 otherwise
-    L.xp = take(P.gather || P.fp8 ? 0 : (size_t)P.R_cap * c.d * P.elem);
+    L.xp = take(P.gather || P.gather4 || P.fp8 ? 0 : (size_t)P.R_cap * c.d * P.elem);
     L.xq = take(P.fp8 ? (size_t)P.R_cap * c.d : 0);
     L.xs = take(P.fp8 ? (size_t)P.R_cap * sizeof(float) : 0);
     L.h = take((size_t)P.R_cap * c.f * act_elem);
@@ -268,6 +299,9 @@ int make_plan(const moe_config* cfg, WsKind kind, Plan* p, int num_sms) {
       L.hs = take((size_t)P.T_pad * c.f_shared * act_elem);
       L.os = take((size_t)P.T_pad * c.d * P.elem);
     }
+    // sized for the narrowest down tile (64 columns), so that the layout does
+    // not depend on the tiling (which follows the GPU's SM count)
+    L.cmb_ctr = take(P.combine_k ? sizeof(unsigned) * (size_t)c.T * ceil_div(c.d, 64) : 0);
   }
   if (kind == WsKind::HostIO) {
     L.x_dev = take((size_t)c.T * c.d * P.elem);
@@ -398,7 +432,7 @@ static int forward_impl(const moe_config* cfg, const Tensors& t, void* ws, size_
   const ScanOutputs so{t.expert_counts, t.aux_loss, t.routed_counts, t.offsets, t.f_out, t.P_out};
   // expert-ordered bf16 copies of the rows, unless the up projection gathers
   // them or reads their e4m3 form
-  const bool copy = !route_only && !p.gather && !p.fp8;
+  const bool copy = !route_only && !p.gather && !p.gather4 && !p.fp8;
   if (p.route_small) {
     // stages 1-4 in one launch for a decode batch; top-k and permute are empty
     MOE_TRY_CUDA(launch_route_small(p, t.x, t.W_r, t.logit_offset, t.sel_bias, t.topk_idx,
@@ -430,7 +464,8 @@ static int forward_impl(const moe_config* cfg, const Tensors& t, void* ws, size_
   else
     MOE_TRY_CUDA(launch_experts_simt(p, t.x, t.W1, t.W3, t.W2, t.Ws1, t.Ws3, t.Ws2, ws, st, mid));
   if ((rc = record(events, MOE_STAGE_COMBINE, st)) != MOE_OK) return rc;
-  if (!p.combine_in_down) MOE_TRY_CUDA(launch_combine(p, t.topk_w, t.y, ws, st));
+  if (!p.combine_in_down && !p.combine_k)
+    MOE_TRY_CUDA(launch_combine(p, t.topk_w, t.y, ws, st));
   if ((rc = record(events, MOE_NUM_STAGES, st)) != MOE_OK) return rc;
   return MOE_OK;
 }
@@ -629,10 +664,11 @@ int moe_launch_count(const moe_config* cfg, int32_t* launches) {
   // permute) or three (logits, top-k, permute); then the two projections and
   // the combine, which top-1 bf16 layers without a shared expert fold into
   // the down projection
+  const bool copy = !p.gather && !p.gather4;   // the tensor-core router's row copy
   const int routing = p.route_small ? 1
-                      : p.route_tc  ? (p.gather ? 1 : 2)
+                      : p.route_tc  ? (copy ? 2 : 1)
                                     : (p.router_fused ? 2 : 3);
-  *launches = cfg->T == 0 ? 0 : routing + 2 + (p.combine_in_down ? 0 : 1);
+  *launches = cfg->T == 0 ? 0 : routing + 2 + (p.combine_in_down || p.combine_k ? 0 : 1);
   return MOE_OK;
 }
 
@@ -644,14 +680,17 @@ int moe_launch_count_fp8(const moe_config* cfg, int32_t* launches) {
   // routing without a row copy, the row quantisation, the two projections
   // and the combine (folded into the down projection for top-1 layers)
   const int routing = p.route_small || p.route_tc ? 1 : (p.router_fused ? 2 : 3);
-  *launches = cfg->T == 0 ? 0 : routing + 1 + 2 + (p.combine_in_down ? 0 : 1);
+  *launches = cfg->T == 0 ? 0 : routing + 1 + 2 + (p.combine_in_down || p.combine_k ? 0 : 1);
   return MOE_OK;
 }
 
 int moe_set_tuning(int32_t knob, int32_t value) {
   if (knob < 0 || knob >= MOE_TUNE_COUNT || value < -1) return MOE_ERR_ARG;
   if (knob == MOE_TUNE_ROUTER && value > MOE_ROUTER_TC) return MOE_ERR_ARG;
-  if (knob == MOE_TUNE_GATHER && value > 1) return MOE_ERR_ARG;
+  if (knob == MOE_TUNE_GATHER && value > 2) return MOE_ERR_ARG;
+  if ((knob == MOE_TUNE_ZERO_PAD || knob == MOE_TUNE_MMA_M64 ||
+       knob == MOE_TUNE_FUSED_COMBINE) && value > 1)
+    return MOE_ERR_ARG;
   g_tune[knob].store(value, std::memory_order_relaxed);
   return MOE_OK;
 }

@@ -56,6 +56,7 @@ struct WsLayout {
   size_t o;           // dtype  [R_cap][d] expert outputs
   size_t hs;          // dtype  [T_pad][f_s] shared-expert hidden
   size_t os;          // dtype  [T_pad][d]   shared-expert output
+  size_t cmb_ctr;     // uint32 [T][N tiles of the down projection]: combine arrival counters
   // host-io staging
   size_t x_dev, y_dev, topk_idx, topk_w, counts, aux;
   size_t total;
@@ -88,7 +89,11 @@ struct Plan {
   int partial_rows;           // A tiles with at most this many rows load only those rows
   int partial_rows_up;        // the same for the up projection
   bool combine_in_down;       // top-1, no shared expert, bf16: y written by the down epilogue
-  bool gather;                // the up projection gathers token rows (no expert-ordered copy)
+  bool combine_k;             // other bf16 layers: the down epilogue's last row per token sums y
+  bool gather;                // the up projection gathers token rows with cp.async
+  bool gather4;               // the up projection gathers token rows with TMA (tile::gather4)
+  bool zero_pad;              // partial A tiles load zeros (no memory read) into their padding rows
+  bool m64;                   // routed GEMM tiles of <= 64 rows multiply with M = 64
   bool fp8;                   // gate/up weights in e4m3: quantised rows, fp8 up projection
   int num_sms;
   WsLayout ws;

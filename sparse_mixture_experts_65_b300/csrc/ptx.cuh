@@ -101,6 +101,20 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map
       : "memory");
 }
 
+// Row gather (tile::gather4): one column slice (the map's box width) of four
+// arbitrary rows r0..r3 of a 2-D map whose box is one row high, written to
+// shared memory as rows 0..3 of a box at `dst` (swizzled like a tiled load).
+__device__ __forceinline__ void tma_gather4(uint32_t dst, const CUtensorMap* map, uint32_t bar,
+                                            int32_t col, int32_t r0, int32_t r1, int32_t r2,
+                                            int32_t r3) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4, %5, %6, %7}], [%2];"
+      ::"r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(col), "r"(r0), "r"(r1),
+        "r"(r2), "r"(r3)
+      : "memory");
+}
+
 // 16-byte cp.async into shared memory (L2 only); src_bytes = 0 fills zeros
 // and reads nothing.
 __device__ __forceinline__ void cp_async16_s(uint32_t dst, const void* src, uint32_t src_bytes) {

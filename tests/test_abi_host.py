@@ -39,8 +39,9 @@ def test_tuning_knobs_check_their_arguments():
     lib = N.lib()
     assert lib.moe_set_tuning(99, 0) == N.MOE_ERR_ARG
     assert lib.moe_set_tuning(N.MOE_TUNE_ROUTER, 9) == N.MOE_ERR_ARG
-    assert lib.moe_set_tuning(N.MOE_TUNE_GATHER, 2) == N.MOE_ERR_ARG
+    assert lib.moe_set_tuning(N.MOE_TUNE_GATHER, 3) == N.MOE_ERR_ARG
     assert lib.moe_set_tuning(N.MOE_TUNE_TILE_N_UP, -2) == N.MOE_ERR_ARG
+    assert lib.moe_set_tuning(N.MOE_TUNE_FUSED_COMBINE, 2) == N.MOE_ERR_ARG
     with L.tuning(router="simt", tile_n_up=64):
         pass                                        # set, then restored
     assert lib.moe_set_tuning(N.MOE_TUNE_ROUTER, -1) == N.MOE_OK
@@ -77,8 +78,11 @@ def test_workspace_sizes(name):
     # (plus a row copy unless the up projection gathers rows: Mixtral copies),
     # else three (logits, top-k, permute); two projections; the combine unless
     # a top-1 bf16 layer without a shared expert folds it into the down
-    # projection
+    # projection (the other bf16 layers do so only on request)
     expected = {"toy": 6, "switch": 3, "mixtral": 5, "dsv3": 6, "gptoss": 6}
+    with L.tuning(fused_combine=1):
+        fused = {"toy": 6, "switch": 3, "mixtral": 4, "dsv3": 5, "gptoss": 5}
+        assert L.launch_count(cfg) == fused[name]
     assert L.launch_count(cfg) == expected[name]
 
 
@@ -192,8 +196,8 @@ def test_fp8_entry_point_checks_without_gpu():
     assert call(ok, W3s=None) == N.MOE_ERR_ARG
     assert call(ok, W1s=odd) == N.MOE_ERR_ARG
     assert call(ok) == N.MOE_ERR_WORKSPACE          # everything else valid, no workspace
-    # decode batch: router, row quantisation, two projections, combine; the
-    # one-launch tensor-core router needs no row copy either
+    # decode batch: router, row quantisation, the two projections, combine;
+    # the split router of larger batches: logits, top-k, permute
     assert L.launch_count(L.config_for(W.get("gptoss16_fp8")), fp8=True) == 5
     assert L.launch_count(L.config_for(W.get("gptoss256")), fp8=False) == 6
     assert L.launch_count(L.config_for(W.get("gptoss256_fp8")), fp8=True) == 7

@@ -344,18 +344,48 @@ def test_decode_batch_router(shape):
     print(shape.name, rep)
 
 
-@pytest.mark.parametrize("gather", ["0", "1"])
+@pytest.mark.parametrize("gather", ["0", "1", "2"])
 def test_up_projection_row_source(gather):
-    """Both row sources of the tensor-core up projection, on layers of every
+    """Every row source of the tensor-core up projection, on layers of every
     routing path (one-launch tensor-core router, split router with E > 64,
-    decode-batch router): rows gathered from x inside the GEMM (cp.async),
-    and an expert-ordered copy read through TMA."""
+    decode-batch router): an expert-ordered copy read through TMA (0), rows
+    gathered from x inside the GEMM with cp.async (1) or with the TMA row
+    gather, four rows per instruction (2)."""
     for shape in (SMALL[0], SMALL[1], SMALL[2], SMALL[3], SMALL[4], ONE_LAUNCH[1], ONE_LAUNCH[3],
                   DECODE[1], DECODE[3]):
         inp = W.make_inputs(shape, "cuda", seed=12)
         with L.tuning(gather=int(gather)):
             _, out = run_gpu(inp)
         check_layer(inp, out)
+
+
+@pytest.mark.parametrize("shape", [SMALL[0], SMALL[2], SMALL[3], SMALL[4], ONE_LAUNCH[1],
+                                   ONE_LAUNCH[3], DECODE[1], DECODE[2]], ids=lambda s: s.name)
+def test_fused_combine_matches_the_separate_kernel_bitwise(shape):
+    """The down projection's epilogue combine (the last row of each token's
+    column slice sums it, fixed slot order) gives the separate combine
+    kernel's y bit for bit, with drops, shared experts and many experts."""
+    inp = W.make_inputs(shape, "cuda", seed=13)
+    with L.tuning(fused_combine=1):
+        _, fused = run_gpu(inp)
+    _, separate = run_gpu(inp)
+    assert torch.equal(fused.y, separate.y)
+    check_layer(inp, fused)
+
+
+def test_fused_combine_with_most_slots_dropped():
+    """k = 2 with a tiny capacity: most tokens lose both slots and get y = 0,
+    some keep one; every token's counters still complete."""
+    shape = LayerShape("drops_k2", 37, T=700, d=128, E=8, k=2, f=64, act=SW, gate=TOPK,
+                       dtype="bf16", capacity_factor=0.1)
+    inp = W.make_inputs(shape, "cuda", seed=14)
+    with L.tuning(fused_combine=1):
+        _, out = run_gpu(inp)
+    slot = out.slot_pos.cpu()
+    none = (slot < 0).all(dim=1)
+    assert none.any() and (~none).any()
+    assert torch.all(out.y[none.cuda()] == 0)
+    check_layer(inp, out)
 
 
 @pytest.mark.parametrize("path", ["simt", "fused", "tc"])
