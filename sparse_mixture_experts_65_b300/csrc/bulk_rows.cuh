@@ -64,4 +64,70 @@ __device__ __forceinline__ bool bulk_copy_rows(int n, uint32_t row_bytes, SrcF s
   return ok;
 }
 
+// Fan-out copy: source row i (i < n) goes to each non-null dst_of(i, j),
+// j < fan -- a token row to the expert segments of its kept slots.  Each row
+// is read once.  One issuing thread (thread 0) runs a pipeline over the
+// stage's slots: row i's stores are committed as one bulk group, loads run
+// nslot - kFanPend rows ahead of the stores, and a slot is refilled only once
+// the group that stored it has finished reading shared memory.  `bars` holds
+// kFanMaxSlots mbarriers (initialised here; the caller synchronises the block
+// before and after the call).  Returns false if a wait ran out.
+constexpr int kFanMaxSlots = 16;
+constexpr int kFanPend = 2;   // store groups allowed to still read shared memory
+
+template <typename SrcF, typename DstF>
+__device__ __forceinline__ bool bulk_fanout_rows(int n, int fan, uint32_t row_bytes, SrcF src_of,
+                                                 DstF dst_of, uint8_t* stage,
+                                                 uint32_t stage_bytes, uint64_t* bars,
+                                                 uint32_t* status, uint32_t timeout_bit,
+                                                 uint64_t timeout_ns) {
+  const uint32_t fit = stage_bytes / row_bytes;
+  const int nslot = (int)(fit < (uint32_t)kFanMaxSlots ? fit : (uint32_t)kFanMaxSlots);
+  if (threadIdx.x == 0) {
+    for (int w = 0; w < nslot; ++w) mbar_init(smem_u32(bars + w), 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
+  if (threadIdx.x != 0 || n <= 0) return true;
+  const uint32_t base = smem_u32(stage);
+  const int ahead = nslot - kFanPend;      // >= 1: the caller gives at least 3 slots
+  uint32_t phases = 0;
+  auto load = [&](int i) {
+    const int s = i % nslot;
+    mbar_arrive_expect_tx(smem_u32(bars + s), row_bytes);
+    bulk_load(base + (uint32_t)s * row_bytes, src_of(i), row_bytes, smem_u32(bars + s));
+  };
+  int next = 0;
+  for (; next < n && next < ahead; ++next) load(next);
+  bool ok = true;
+  int i = 0;
+  for (; i < n; ++i) {
+    const int s = i % nslot;
+    if (!mbar_wait_bounded(smem_u32(bars + s), (phases >> s) & 1u, timeout_ns, nullptr)) {
+      atomicOr(status, timeout_bit);
+      ok = false;
+      break;
+    }
+    phases ^= 1u << s;
+    for (int j = 0; j < fan; ++j) {
+      void* d = dst_of(i, j);
+      if (d != nullptr) bulk_store(d, base + (uint32_t)s * row_bytes, row_bytes);
+    }
+    bulk_commit();
+    bulk_wait_read<kFanPend>();           // rows <= i - kFanPend: slots free again
+    if (next < n) load(next++);
+  }
+  if (!ok) {
+    // loads issued ahead may still be landing in the stage
+    for (int r = i; r < next; ++r) {
+      const int s = r % nslot;
+      mbar_wait_bounded(smem_u32(bars + s), (phases >> s) & 1u, timeout_ns, nullptr);
+      phases ^= 1u << s;
+    }
+  }
+  bulk_commit();
+  bulk_wait_all();
+  return ok;
+}
+
 }  // namespace moe

@@ -54,10 +54,10 @@ constexpr uint64_t kPermuteTimeoutNs = 2000000000ull;
 // Rows of at least 1 KB (and at most a quarter of the stage) move by bulk
 // copies; shorter rows by 16-byte loads and stores.
 __host__ __device__ inline bool permute_bulk(uint32_t row_bytes) {
-  return row_bytes >= 1024u && row_bytes * kBulkIssuers <= kPermuteStage;
+  return row_bytes >= 1024u && row_bytes * 4u <= kPermuteStage;
 }
 
-// Shared memory: cnt[E] | row_s[BT*k] | (128-aligned) stage | 4 mbarriers.
+// Shared memory: cnt[E] | row_s[BT*k] | (128-aligned) stage | kFanMaxSlots mbarriers.
 __host__ __device__ inline size_t permute_stage_offset(int E, int keys) {
   return ((sizeof(int) * ((size_t)E + keys)) + 127) / 128 * 128;
 }
@@ -111,16 +111,17 @@ __global__ void __launch_bounds__(kPermuteThreads) permute_kernel(const PermuteA
   if (!a.copy) return;
   const uint32_t row_bytes = (uint32_t)a.nvec * 16u;
   if (permute_bulk(row_bytes)) {
-    // bulk row copies through shared memory: many kilobytes in flight per SM
+    // bulk copies through shared memory: each token row is read once and
+    // stored to the segments of its kept slots, loads running ahead of stores
     uint8_t* stage = reinterpret_cast<uint8_t*>(smi) + permute_stage_offset(a.E, a.BT * a.k);
     uint64_t* bars = reinterpret_cast<uint64_t*>(stage + kPermuteStage);
     const char* xs = static_cast<const char*>(a.x);
     char* xp = static_cast<char*>(a.xp);
-    bulk_copy_rows(
-        nk, row_bytes,
-        [&](int q) { return static_cast<const void*>(xs + (size_t)(t0 + q / a.k) * row_bytes); },
-        [&](int q) {
-          const int row = row_s[q];
+    bulk_fanout_rows(
+        nk / a.k, a.k, row_bytes,
+        [&](int i) { return static_cast<const void*>(xs + (size_t)(t0 + i) * row_bytes); },
+        [&](int i, int j) {
+          const int row = row_s[i * a.k + j];
           return row >= 0 ? static_cast<void*>(xp + (size_t)row * row_bytes) : nullptr;
         },
         stage, kPermuteStage, bars, a.status, STATUS_TIMEOUT_ROUTE, kPermuteTimeoutNs);
@@ -157,8 +158,9 @@ __global__ void __launch_bounds__(kPermuteThreads) permute_kernel(const PermuteA
 }
 
 // Copy of the kept token rows into expert order after the one-launch router
-// (key_row is final): every block takes a contiguous range of keys and moves
-// the kept rows with bulk copies through shared memory.
+// (key_row is final): every block takes a contiguous range of tokens and
+// copies each row once into shared memory and from there to the segments of
+// the token's kept slots (rows too wide for three stage slots go key by key).
 constexpr int kGatherThreads = 32 * kBulkIssuers;
 constexpr uint32_t kGatherStage = 160u << 10;
 
@@ -168,11 +170,29 @@ __global__ void __launch_bounds__(kGatherThreads) gather_rows_kernel(
   extern __shared__ __align__(128) uint8_t gsm[];
   pdl_wait();
   pdl_trigger();
+  uint64_t* bars = reinterpret_cast<uint64_t*>(gsm + kGatherStage);
+  if (row_bytes * 3u <= kGatherStage) {
+    const int ntok = nkeys / k;
+    const int per = (ntok + gridDim.x - 1) / gridDim.x;
+    const int t0 = blockIdx.x * per;
+    const int n = min(per, ntok - t0);
+    if (n <= 0) return;
+    bulk_fanout_rows(
+        n, k, row_bytes,
+        [&](int i) { return static_cast<const void*>(x + (size_t)(t0 + i) * row_bytes); },
+        [&](int i, int j) {
+          const int row = __ldg(key_row + (size_t)(t0 + i) * k + j);
+          return row >= 0 && in_bounds(row < R_cap, status)
+                     ? static_cast<void*>(xp + (size_t)row * row_bytes)
+                     : nullptr;
+        },
+        gsm, kGatherStage, bars, status, STATUS_TIMEOUT_ROUTE, 2000000000ull);
+    return;
+  }
   const int per = (nkeys + gridDim.x - 1) / gridDim.x;
   const int q0 = blockIdx.x * per;
   const int n = min(per, nkeys - q0);
   if (n <= 0) return;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(gsm + kGatherStage);
   bulk_copy_rows(
       n, row_bytes,
       [&](int i) { return static_cast<const void*>(x + (size_t)((q0 + i) / k) * row_bytes); },
@@ -190,7 +210,7 @@ cudaError_t launch_gather_rows(const Plan& p, const void* x, void* ws, cudaStrea
   const int nkeys = p.cfg.T * p.cfg.k;
   const uint32_t row_bytes = (uint32_t)p.cfg.d * p.elem;
   static std::atomic<uint64_t> attr_done{0};
-  const size_t smem = kGatherStage + 8 * kBulkIssuers;
+  const size_t smem = kGatherStage + 8 * kFanMaxSlots;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
@@ -247,7 +267,7 @@ cudaError_t launch_permute(const Plan& p, const void* x, const int32_t* topk_idx
   const bool bulk = copy_rows && permute_bulk((uint32_t)a.nvec * 16u);
   const size_t ints = sizeof(int) * ((size_t)p.cfg.E + (size_t)p.BT * p.cfg.k);
   const size_t smem =
-      bulk ? permute_stage_offset(p.cfg.E, p.BT * p.cfg.k) + kPermuteStage + 8 * kBulkIssuers
+      bulk ? permute_stage_offset(p.cfg.E, p.BT * p.cfg.k) + kPermuteStage + 8 * kFanMaxSlots
            : ints;
   if (bulk) {
     static std::atomic<uint64_t> attr_done{0};
