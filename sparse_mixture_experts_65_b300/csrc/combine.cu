@@ -80,6 +80,75 @@ __global__ void __launch_bounds__(kThreads) combine_kernel(const CombineArgs a) 
   }
 }
 
+// bf16 rows (d a multiple of 8): 16-byte loads, and every kept slot's row of
+// one 8-column chunk is requested before the first of them is used (U slots
+// at a time), so that each thread keeps up to U + 1 loads in flight.  The arithmetic and its order are those of
+// combine_kernel.
+template <int U>
+__global__ void __launch_bounds__(kThreads) combine_bf16x8_kernel(const CombineArgs a) {
+  __shared__ int rows[kMaxK];
+  __shared__ float gates[kMaxK];
+  const int t = blockIdx.x;
+  pdl_wait();
+  pdl_trigger();
+  if (threadIdx.x < a.k) {
+    const int r = a.key_row[(size_t)t * a.k + threadIdx.x];
+    rows[threadIdx.x] = r >= 0 && in_bounds(r < a.R_cap, a.status) ? r : -1;
+    gates[threadIdx.x] = a.topk_w[(size_t)t * a.k + threadIdx.x];
+  }
+  __syncthreads();
+  const __nv_bfloat16* o = static_cast<const __nv_bfloat16*>(a.o);
+  const __nv_bfloat16* os = static_cast<const __nv_bfloat16*>(a.os);
+  __nv_bfloat16* y = static_cast<__nv_bfloat16*>(a.y);
+  for (int c = threadIdx.x * 8; c < a.d; c += kThreads * 8) {
+    float acc[8];
+    if (os) {
+      const uint4 u = *reinterpret_cast<const uint4*>(os + (size_t)t * a.d + c);
+      const __nv_bfloat162* b = reinterpret_cast<const __nv_bfloat162*>(&u);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const float2 f = __bfloat1622float2(b[i]);
+        acc[2 * i] = f.x;
+        acc[2 * i + 1] = f.y;
+      }
+    } else {
+#pragma unroll
+      for (int i = 0; i < 8; ++i) acc[i] = 0.f;
+    }
+    for (int j0 = 0; j0 < a.k; j0 += U) {
+      uint4 v[U];
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int j = j0 + u;
+        const int r = j < a.k ? rows[j] : -1;
+        v[u] = r >= 0 ? *reinterpret_cast<const uint4*>(o + (size_t)r * a.d + c)
+                      : make_uint4(0, 0, 0, 0);
+      }
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int j = j0 + u;
+        if (j >= a.k || rows[j] < 0) continue;
+        const float g = gates[j];
+        const __nv_bfloat162* b = reinterpret_cast<const __nv_bfloat162*>(&v[u]);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const float2 f = __bfloat1622float2(b[i]);
+          acc[2 * i] = fmaf(g, f.x, acc[2 * i]);
+          acc[2 * i + 1] = fmaf(g, f.y, acc[2 * i + 1]);
+        }
+      }
+    }
+    uint4 pk;
+    uint32_t* pw = reinterpret_cast<uint32_t*>(&pk);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      __nv_bfloat162 b2 = __floats2bfloat162_rn(acc[2 * i], acc[2 * i + 1]);
+      pw[i] = *reinterpret_cast<uint32_t*>(&b2);
+    }
+    *reinterpret_cast<uint4*>(y + (size_t)t * a.d + c) = pk;
+  }
+}
+
 cudaError_t launch_combine(const Plan& p, const float* topk_w, void* y, void* ws,
                            cudaStream_t st) {
   CombineArgs a;
@@ -94,8 +163,15 @@ cudaError_t launch_combine(const Plan& p, const float* topk_w, void* y, void* ws
   a.k = p.cfg.k;
   a.R_cap = p.R_cap;
   a.status = reinterpret_cast<uint32_t*>(w + p.ws.status);
-  if (p.cfg.dtype == MOE_BF16)
-    return launch_pdl(combine_kernel<__nv_bfloat16>, dim3(p.cfg.T), dim3(kThreads), 0, st, a);
+  if (p.cfg.dtype == MOE_BF16) {
+    // many slots per token: all of a chunk's slot rows in flight at once
+    // (DeepSeek-V3-shaped layer 126 -> 120 us); with few slots the plain
+    // kernel measured faster (Mixtral-shaped 48 vs 52 us, gpt-oss-shaped
+    // decode 8 vs 10 us)
+    const dim3 g(p.cfg.T), b(kThreads);
+    if (p.cfg.k >= 8) return launch_pdl(combine_bf16x8_kernel<8>, g, b, 0, st, a);
+    return launch_pdl(combine_kernel<__nv_bfloat16>, g, b, 0, st, a);
+  }
   return launch_pdl(combine_kernel<float>, dim3(p.cfg.T), dim3(kThreads), 0, st, a);
 }
 

@@ -208,8 +208,10 @@ __device__ __forceinline__ TileInfo decode_tile(const TcArgs& a, const Sched& sc
   return ti;
 }
 
+// silu(g) * u with the hardware exponential and an approximate division
+// (relative error ~1e-7, far below the bf16 rounding of h)
 __device__ __forceinline__ float silu_mul(float g, float u) {
-  return g / (1.0f + __expf(-g)) * u;
+  return __fdividef(g, 1.0f + __expf(-g)) * u;
 }
 
 // Epilogue of one accumulator: activation (or none, or the gate of a top-1
@@ -217,9 +219,10 @@ __device__ __forceinline__ float silu_mul(float g, float u) {
 // row and the last column.
 template <int BNH, bool DUAL, int EPI, bool F8 = false>
 __device__ __forceinline__ void epilogue_tile(const TcArgs& a, const TileInfo& ti, uint32_t t_row,
-                                              size_t orow, bool row_ok, float scale) {
+                                              size_t orow, bool row_ok, float scale, int c_lo,
+                                              int c_hi) {
 #pragma unroll 1
-  for (int c = 0; c < BNH; c += 32) {
+  for (int c = c_lo; c < c_hi; c += 32) {
     uint32_t r0[32];
     tmem_ld32(t_row + c, r0);
     uint32_t r1[32];
@@ -338,12 +341,14 @@ __device__ __forceinline__ void gather_stage(uint32_t sa, const int* tok_s, cons
 // token when this row completed the count (its slice is then summed by the
 // whole warp, combine_slice), else -1.
 template <int BNH>
-__device__ __forceinline__ int combine_arrive(const TcArgs& a, const TileInfo& ti, size_t orow) {
+__device__ __forceinline__ int combine_arrive(const TcArgs& a, const TileInfo& ti, size_t orow,
+                                              int parts) {
   const int t = ti.shared ? (int)orow : __ldg(a.row_token + orow);
   if (!in_bounds(t >= 0 && t < a.T_tokens, a.status)) return -1;
   const int* kr = a.key_row + (size_t)t * a.k_slots;
   int expect = a.has_shared;
   for (int j = 0; j < a.k_slots; ++j) expect += __ldg(kr + j) >= 0 ? 1 : 0;
+  expect *= parts;                        // each row's slice arrives in `parts` column parts
   unsigned* ctr = a.cmb_ctr + (size_t)t * a.cmb_nt + ti.n0 / BNH;
   __threadfence();                        // this row's o slice before the count
   if (atomicAdd(ctr, 1u) + 1u != (unsigned)expect) return -1;
@@ -431,16 +436,24 @@ enum { AS_TMA = 0, AS_CP = 1, AS_G4 = 2 };
 
 // Warp roles: producer warps (one TMA warp, or four gathering warps), one MMA
 // warp, four epilogue warps.
-template <int AS>
+template <int AS, int EPI>
 struct TcWarps {
   static constexpr int PROD = AS == AS_CP ? 4 : 1;
   static constexpr int MMA = PROD;
   static constexpr int EPI0 = PROD + 1;
-  static constexpr int THREADS = (PROD + 5) * 32;
+  // Epilogues with an activation (SwiGLU, GELU) have two warps per TMEM lane
+  // quarter (warp w reads quarter w % 4), each taking half of a tile's
+  // columns: with one warp per scheduler their dependent chains (TMEM loads,
+  // exponentials, stores) put them on the critical path of short tiles
+  // (e4m3 decode up projection 288 -> 157 us).  The light epilogues keep one
+  // warp per quarter: extra waiting warps slowed the long-tile down
+  // projection (DeepSeek-V3-shaped 1.61 -> 1.75 ms).
+  static constexpr int EPIW = (EPI == EPI_SWIGLU || EPI == EPI_GELU) ? 8 : 4;
+  static constexpr int THREADS = (PROD + 1 + EPIW) * 32;
 };
 
 template <int BNH, bool DUAL, int EPI, int AS, bool F8 = false>
-__global__ void __launch_bounds__(TcWarps<AS>::THREADS, 1)
+__global__ void __launch_bounds__(TcWarps<AS, EPI>::THREADS, 1)
 tc_grouped_gemm(const __grid_constant__ CUtensorMap mA, const __grid_constant__ CUtensorMap mA_sh,
                 const __grid_constant__ CUtensorMap mA32, const __grid_constant__ CUtensorMap mA32_sh,
                 const __grid_constant__ CUtensorMap mB0, const __grid_constant__ CUtensorMap mB1,
@@ -474,7 +487,7 @@ tc_grouped_gemm(const __grid_constant__ CUtensorMap mA, const __grid_constant__ 
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(tfull_bar(b), 1);
-      mbar_init(tempty_bar(b), 128);
+      mbar_init(tempty_bar(b), 32 * TcWarps<AS, EPI>::EPIW);
     }
     mbar_init(drain_bar, 1);
     *abort_flag = 0;
@@ -492,7 +505,7 @@ tc_grouped_gemm(const __grid_constant__ CUtensorMap mA, const __grid_constant__ 
       if (DUAL) tma_prefetch_desc(&mB1_sh);
     }
   }
-  using Wr = TcWarps<AS>;
+  using Wr = TcWarps<AS, EPI>;
   if (warp == Wr::MMA) {
     tmem_alloc(smem_u32(tmem_slot), C::TMEM_COLS);
     tmem_relinquish();
@@ -840,16 +853,24 @@ tc_grouped_gemm(const __grid_constant__ CUtensorMap mA, const __grid_constant__ 
       }
     }
   } else {
-    // ---------------- epilogue (the last four warps) ----------------
+    // ---------------- epilogue (the last eight warps) ----------------
     const int q = warp & 3;                  // TMEM lane quarter this warp may read
     const int row_in_tile = q * 32 + lane;
+    const int ew = warp - Wr::EPI0;          // 0 .. EPIW-1
+    // columns of this warp: a half of the tile when the halves are whole
+    // 32-column chunks, else the first warp of the quarter takes all of them
+    constexpr bool kSplit = Wr::EPIW == 8 && BNH % 64 == 0;
+    const int half = ew >> 2;
+    const int c_lo = kSplit ? half * (BNH / 2) : 0;
+    const int c_hi = kSplit ? c_lo + BNH / 2 : (half == 0 ? BNH : 0);
+    const bool has_cols = c_hi > c_lo;
     if constexpr (EPI == EPI_COMBINE1) {
       // a dropped token (key_row < 0, top-1) gets y = 0: its rows are spread
       // over all epilogue warps of the grid, written while the first
       // accumulator is still being computed
       uint4* y = static_cast<uint4*>(a.y);
       const int nvec = a.ld_y * 2 / 16;
-      const int gw = blockIdx.x * 4 + (warp - Wr::EPI0), nw = gridDim.x * 4;
+      const int gw = blockIdx.x * Wr::EPIW + ew, nw = gridDim.x * Wr::EPIW;
       for (int t = gw; t < a.T_tokens; t += nw) {
         if (__ldg(a.key_row + t) < 0)
           for (int c = lane; c < nvec; c += 32) y[(size_t)t * nvec + c] = make_uint4(0, 0, 0, 0);
@@ -861,7 +882,7 @@ tc_grouped_gemm(const __grid_constant__ CUtensorMap mA, const __grid_constant__ 
       if (!a.has_shared) {
         uint4* y = static_cast<uint4*>(a.y);
         const int nvec = a.ld_y * 2 / 16;
-        const int gw = blockIdx.x * 4 + (warp - Wr::EPI0), nw = gridDim.x * 4;
+        const int gw = blockIdx.x * Wr::EPIW + ew, nw = gridDim.x * Wr::EPIW;
         for (int t = gw; t < a.T_tokens; t += nw) {
           bool any = false;
           for (int j = 0; j < a.k_slots; ++j) any |= __ldg(a.key_row + (size_t)t * a.k_slots + j) >= 0;
@@ -898,13 +919,15 @@ tc_grouped_gemm(const __grid_constant__ CUtensorMap mA, const __grid_constant__ 
         tc_fence_after();
         const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + ab * C::MMA_N;
         if constexpr (EPI == EPI_F32_CHUNKED) {
+          if (has_cols) {
 #pragma unroll
-          for (int c = 0; c < BNH; c += 32) {
-            uint32_t r0[32];
-            tmem_ld32(t_row + c, r0);
-            tmem_ld_wait();
+            for (int c = 0; c < BNH; c += 32) {
+              uint32_t r0[32];
+              tmem_ld32(t_row + c, r0);
+              tmem_ld_wait();
 #pragma unroll
-            for (int i = 0; i < 32; ++i) csum[c + i] += __uint_as_float(r0[i]);
+              for (int i = 0; i < 32; ++i) csum[c + i] += __uint_as_float(r0[i]);
+            }
           }
         } else if constexpr (EPI == EPI_COMBINE1) {
           // y row of the token this expert row belongs to, scaled by its gate
@@ -912,19 +935,19 @@ tc_grouped_gemm(const __grid_constant__ CUtensorMap mA, const __grid_constant__ 
           const bool tok_ok = row_ok && in_bounds(tok >= 0 && tok < a.T_tokens, a.status);
           if (!tok_ok) tok = 0;
           const float g = tok_ok ? __ldg(a.gate + tok) : 0.f;
-          epilogue_tile<BNH, DUAL, EPI>(a, ti, t_row, (size_t)tok, tok_ok, g);
+          epilogue_tile<BNH, DUAL, EPI>(a, ti, t_row, (size_t)tok, tok_ok, g, c_lo, c_hi);
         } else if constexpr (F8) {
           const float rs = row_ok ? __ldg(a.a_scale + orow) : 0.f;
-          epilogue_tile<BNH, DUAL, EPI, true>(a, ti, t_row, orow, row_ok, rs);
+          epilogue_tile<BNH, DUAL, EPI, true>(a, ti, t_row, orow, row_ok, rs, c_lo, c_hi);
         } else {
-          epilogue_tile<BNH, DUAL, EPI>(a, ti, t_row, orow, row_ok, 1.f);
+          epilogue_tile<BNH, DUAL, EPI>(a, ti, t_row, orow, row_ok, 1.f, c_lo, c_hi);
         }
         tc_fence_before();
         mbar_arrive(tempty_bar(ab));
         if constexpr (EPI == EPI_COMBINEK) {
           // rows that completed their token's count; the warp sums each one's
           // slice together
-          const int tl = row_ok ? combine_arrive<BNH>(a, ti, orow) : -1;
+          const int tl = row_ok && has_cols ? combine_arrive<BNH>(a, ti, orow, kSplit ? 2 : 1) : -1;
           const unsigned am = __activemask();
           unsigned m = __ballot_sync(am, tl >= 0);
           while (m) {
@@ -935,7 +958,7 @@ tc_grouped_gemm(const __grid_constant__ CUtensorMap mA, const __grid_constant__ 
         }
       }
       if constexpr (EPI == EPI_F32_CHUNKED) {
-        if (ok && row_ok) {
+        if (ok && row_ok && has_cols) {
           float* dst = static_cast<float*>(a.out) + orow * a.ld_out + ti.n0;
 #pragma unroll
           for (int i = 0; i < BNH; ++i) {
@@ -967,7 +990,7 @@ static cudaError_t run_tc(const TcMaps& m, const TcArgs& a, int grid, cudaStream
   auto kern = tc_grouped_gemm<BNH, DUAL, EPI, AS, F8>;
   cudaError_t e = smem_attr_once(kern, C::SMEM, attr_done);
   if (e != cudaSuccess) return e;
-  return launch_pdl(kern, dim3(grid), dim3(TcWarps<AS>::THREADS), C::SMEM, st, m.A, m.A_sh,
+  return launch_pdl(kern, dim3(grid), dim3(TcWarps<AS, EPI>::THREADS), C::SMEM, st, m.A, m.A_sh,
                     m.A32, m.A32_sh, m.B0,
                     m.B1, m.B0_sh, m.B1_sh, a);
 }
