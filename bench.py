@@ -727,16 +727,17 @@ def run_b300(args):
     layer_roof = layer_roofline(layer, ms_step, peaks)
 
     e2e = None
-    if fp8 and not args.no_e2e:
-        e2e = {"value": None, "unavailable": "the host-memory entry point serves the bf16 "
-               "weights only; moe_forward_fp8 takes device tensors"}
-    elif not args.no_e2e:
+    if not args.no_e2e:
         x_h = inp.x.cpu().pin_memory()
         y_h = torch.empty_like(x_h).pin_memory()
         aux_h = torch.empty(1, dtype=torch.float32).pin_memory()
-        hio = L.BoundHostIO(cfg, x_h, y_h, aux_h, inp.W_r, inp.W1, inp.W2, inp.W3,
-                            inp.logit_offset, inp.sel_bias, inp.Ws1, inp.Ws3, inp.Ws2,
-                            stream=stream)
+        if fp8:
+            hio = L.BoundHostIOFp8(cfg, x_h, y_h, aux_h, inp.W_r, inp.W1q, inp.W1s, inp.W3q,
+                                   inp.W3s, inp.W2, inp.logit_offset, inp.sel_bias, stream=stream)
+        else:
+            hio = L.BoundHostIO(cfg, x_h, y_h, aux_h, inp.W_r, inp.W1, inp.W2, inp.W3,
+                                inp.logit_offset, inp.sel_bias, inp.Ws1, inp.Ws3, inp.Ws2,
+                                stream=stream)
         for _ in range(Wm):
             hio()
         barrier()
@@ -751,7 +752,8 @@ def run_b300(args):
         io = shape.T * shape.d * x_h.element_size()
         e2e = {"value": round(world * shape.T * K / (ms_e2e / 1e3), 1), "unit": "tokens/s",
                "h2d_bytes_per_step": io, "d2h_bytes_per_step": io + 4,
-               "ms_per_step": round(ms_e2e / K, 5), "api": "moe_forward_host_io"}
+               "ms_per_step": round(ms_e2e / K, 5),
+               "api": "moe_forward_fp8_host_io" if fp8 else "moe_forward_host_io"}
         del hio, x_h, y_h
 
     cpu = routing = None

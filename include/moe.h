@@ -307,6 +307,22 @@ int moe_forward_host_io(const moe_config* cfg,
                         void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * moe_forward_fp8_host_io -- moe_forward_fp8 with the activations in HOST
+ * memory, as moe_forward_host_io is to moe_forward: x_host [T, d] bf16 is
+ * copied to the device, the layer runs with the e4m3 gate/up weights, and
+ * y_host [T, d] bf16 and aux_loss_host [1] are copied back, all enqueued on
+ * `stream`.  Weights, scales, logit_offset and sel_bias are device pointers
+ * as in moe_forward_fp8.  Needs moe_host_io_workspace_size_fp8() bytes.
+ */
+int moe_host_io_workspace_size_fp8(const moe_config* cfg, size_t* bytes);
+int moe_forward_fp8_host_io(const moe_config* cfg, const void* x_host, const void* W_r,
+                            const float* logit_offset, const float* sel_bias,
+                            const uint8_t* W1q, const float* W1s, const uint8_t* W3q,
+                            const float* W3s, const void* W2, void* y_host,
+                            float* aux_loss_host, void* workspace, size_t workspace_bytes,
+                            void* stream);
+
+/*
  * Synchronises `stream`, then reads and clears the device status word in
  * `workspace`.  Returns MOE_OK, MOE_ERR_TIMEOUT when a bounded device wait
  * gave up since the last check, MOE_ERR_BOUNDS when the bounds-checked build

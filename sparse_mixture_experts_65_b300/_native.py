@@ -38,7 +38,7 @@ EXPORTS = (
     "moe_error_string", "moe_forward_timed", "moe_launch_count", "moe_selftest_wait_timeout",
     "moe_router_scores", "moe_router_scores_noalloc", "moe_router_z_loss", "moe_bias_update",
     "moe_workspace_size_fp8", "moe_forward_fp8", "moe_forward_fp8_timed", "moe_launch_count_fp8",
-    "moe_set_tuning",
+    "moe_set_tuning", "moe_host_io_workspace_size_fp8", "moe_forward_fp8_host_io",
 )
 
 
@@ -89,7 +89,7 @@ def _load(path: str) -> ctypes.CDLL:
     L = ctypes.CDLL(path)
     cfgp = ctypes.POINTER(MoeConfig)
     for name in ("moe_workspace_size", "moe_route_workspace_size", "moe_host_io_workspace_size",
-                 "moe_workspace_size_fp8"):
+                 "moe_workspace_size_fp8", "moe_host_io_workspace_size_fp8"):
         f = getattr(L, name)
         f.argtypes = [cfgp, ctypes.POINTER(SZ)]
         f.restype = ctypes.c_int
@@ -102,6 +102,8 @@ def _load(path: str) -> ctypes.CDLL:
     L.moe_route.restype = ctypes.c_int
     L.moe_forward_host_io.argtypes = [cfgp, P, P, P, P, P, P, P, P, P, P, P, P, P, SZ, P]
     L.moe_forward_host_io.restype = ctypes.c_int
+    L.moe_forward_fp8_host_io.argtypes = [cfgp] + [P] * 12 + [SZ, P]
+    L.moe_forward_fp8_host_io.restype = ctypes.c_int
     L.moe_router_scores.argtypes = [cfgp, P, P, P, P, P, SZ, P]
     L.moe_router_scores.restype = ctypes.c_int
     fp8_args = [cfgp] + [P] * 20 + [SZ, P]

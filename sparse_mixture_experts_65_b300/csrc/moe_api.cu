@@ -69,7 +69,8 @@ int make_plan(const moe_config* cfg, WsKind kind, Plan* p, int num_sms) {
   // fp8 gate/up weights: a bf16 SwiGLU layer without a shared expert; rows of
   // d e4m3 bytes must be 16-byte multiples (TMA) and the column scales are
   // read in pairs
-  if (kind == WsKind::ForwardFp8 &&
+  const bool fp8_kind = kind == WsKind::ForwardFp8 || kind == WsKind::HostIOFp8;
+  if (fp8_kind &&
       (c.dtype != MOE_BF16 || c.act != MOE_ACT_SWIGLU || c.n_shared != 0 || c.d % 16 ||
        c.f % 4))
     return MOE_ERR_UNSUPPORTED;
@@ -80,7 +81,7 @@ int make_plan(const moe_config* cfg, WsKind kind, Plan* p, int num_sms) {
   Plan& P = *p;
   std::memset(&P, 0, sizeof(P));
   P.cfg = c;
-  P.fp8 = kind == WsKind::ForwardFp8;
+  P.fp8 = fp8_kind;
   P.elem = c.dtype == MOE_BF16 ? 2 : 4;
   if (c.capacity_factor > 0) {
     const double cap = std::ceil(static_cast<double>(Tk) * c.capacity_factor / c.E);
@@ -303,7 +304,7 @@ int make_plan(const moe_config* cfg, WsKind kind, Plan* p, int num_sms) {
     // not depend on the tiling (which follows the GPU's SM count)
     L.cmb_ctr = take(P.combine_k ? sizeof(unsigned) * (size_t)c.T * ceil_div(c.d, 64) : 0);
   }
-  if (kind == WsKind::HostIO) {
+  if (kind == WsKind::HostIO || kind == WsKind::HostIOFp8) {
     L.x_dev = take((size_t)c.T * c.d * P.elem);
     L.y_dev = take((size_t)c.T * c.d * P.elem);
     L.topk_idx = take(sizeof(int) * (size_t)Tk);
@@ -620,6 +621,46 @@ int moe_forward_host_io(const moe_config* cfg, const void* x_host, const void* W
   if (rc != MOE_OK) return rc;
   if (io_bytes) MOE_TRY_CUDA(cudaMemcpyAsync(x_dev, x_host, io_bytes, cudaMemcpyHostToDevice, st));
   rc = forward_impl(cfg, t, workspace, workspace_bytes, st, nullptr, false, WsKind::HostIO);
+  if (rc != MOE_OK) return rc;
+  if (io_bytes) MOE_TRY_CUDA(cudaMemcpyAsync(y_host, y_dev, io_bytes, cudaMemcpyDeviceToHost, st));
+  MOE_TRY_CUDA(cudaMemcpyAsync(aux_loss_host, aux_dev, sizeof(float), cudaMemcpyDeviceToHost, st));
+  return MOE_OK;
+}
+
+int moe_host_io_workspace_size_fp8(const moe_config* cfg, size_t* bytes) {
+  if (!bytes) return MOE_ERR_ARG;
+  Plan p;
+  const int rc = make_plan(cfg, WsKind::HostIOFp8, &p);
+  if (rc == MOE_OK) *bytes = p.ws.total;
+  return rc;
+}
+
+int moe_forward_fp8_host_io(const moe_config* cfg, const void* x_host, const void* W_r,
+                            const float* logit_offset, const float* sel_bias,
+                            const uint8_t* W1q, const float* W1s, const uint8_t* W3q,
+                            const float* W3s, const void* W2, void* y_host,
+                            float* aux_loss_host, void* workspace, size_t workspace_bytes,
+                            void* stream) {
+  if (!cfg || !x_host || !y_host || !aux_loss_host || !W1s || !W3s) return MOE_ERR_ARG;
+  Plan p;
+  int rc = make_plan(cfg, WsKind::HostIOFp8, &p);
+  if (rc != MOE_OK) return rc;
+  rc = check_workspace(p, workspace, workspace_bytes);
+  if (rc != MOE_OK) return rc;
+  char* w = static_cast<char*>(workspace);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const size_t io_bytes = (size_t)cfg->T * cfg->d * p.elem;
+  void* x_dev = w + p.ws.x_dev;
+  void* y_dev = w + p.ws.y_dev;
+  float* aux_dev = reinterpret_cast<float*>(w + p.ws.aux);
+  Tensors t{x_dev, W_r, logit_offset, sel_bias, W1q, W3q, W2, nullptr, nullptr, nullptr, y_dev,
+            reinterpret_cast<int32_t*>(w + p.ws.topk_idx), reinterpret_cast<float*>(w + p.ws.topk_w),
+            reinterpret_cast<int32_t*>(w + p.ws.counts), aux_dev, nullptr, nullptr, nullptr,
+            nullptr, nullptr, W1s, W3s};
+  rc = check_tensors(*cfg, t, false);
+  if (rc != MOE_OK) return rc;
+  if (io_bytes) MOE_TRY_CUDA(cudaMemcpyAsync(x_dev, x_host, io_bytes, cudaMemcpyHostToDevice, st));
+  rc = forward_impl(cfg, t, workspace, workspace_bytes, st, nullptr, false, WsKind::HostIOFp8);
   if (rc != MOE_OK) return rc;
   if (io_bytes) MOE_TRY_CUDA(cudaMemcpyAsync(y_host, y_dev, io_bytes, cudaMemcpyDeviceToHost, st));
   MOE_TRY_CUDA(cudaMemcpyAsync(aux_loss_host, aux_dev, sizeof(float), cudaMemcpyDeviceToHost, st));

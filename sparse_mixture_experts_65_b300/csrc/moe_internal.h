@@ -99,7 +99,7 @@ struct Plan {
   WsLayout ws;
 };
 
-enum class WsKind { Forward, Route, HostIO, ForwardFp8 };
+enum class WsKind { Forward, Route, HostIO, ForwardFp8, HostIOFp8 };
 
 int make_plan(const moe_config* cfg, WsKind kind, Plan* p);
 

@@ -55,7 +55,8 @@ def workspace_size(cfg: N.MoeConfig, kind: str = "forward") -> int:
     n = ctypes.c_size_t(0)
     fn = {"forward": N.lib().moe_workspace_size, "route": N.lib().moe_route_workspace_size,
           "host_io": N.lib().moe_host_io_workspace_size,
-          "fp8": N.lib().moe_workspace_size_fp8}[kind]
+          "fp8": N.lib().moe_workspace_size_fp8,
+          "host_io_fp8": N.lib().moe_host_io_workspace_size_fp8}[kind]
     N.check(fn(ctypes.byref(cfg), ctypes.byref(n)), "moe_workspace_size")
     return n.value
 
@@ -325,6 +326,29 @@ def bound_forward(cfg: N.MoeConfig, inp, stream=None, workspace=None) -> BoundFo
     return BoundForward(cfg, inp.x, inp.W_r, inp.W1, inp.W2, inp.W3, inp.logit_offset,
                         inp.sel_bias, inp.Ws1, inp.Ws3, inp.Ws2, workspace=workspace,
                         stream=stream)
+
+
+class BoundHostIOFp8:
+    """moe_forward_fp8_host_io with every argument marshalled once: host x in,
+    host y and loss out, e4m3 gate/up weights on the device."""
+
+    def __init__(self, cfg: N.MoeConfig, x_host, y_host, aux_host, W_r, W1q, W1s, W3q, W3s, W2,
+                 logit_offset=None, sel_bias=None, workspace: Optional[torch.Tensor] = None,
+                 stream=None):
+        self.workspace = (workspace if workspace is not None
+                          else alloc_workspace(cfg, W_r.device, "host_io_fp8"))
+        self._keep = (x_host, y_host, aux_host, W_r, W1q, W1s, W3q, W3s, W2, logit_offset,
+                      sel_bias)
+        self.args = (ctypes.byref(cfg), _ptr(x_host), _ptr(W_r), _ptr(logit_offset),
+                     _ptr(sel_bias), _ptr(W1q), _ptr(W1s), _ptr(W3q), _ptr(W3s), _ptr(W2),
+                     _ptr(y_host), _ptr(aux_host), _ptr(self.workspace),
+                     ctypes.c_size_t(self.workspace.numel()), _stream_handle(stream))
+        self._fn = N.lib().moe_forward_fp8_host_io
+
+    def __call__(self) -> None:
+        rc = self._fn(*self.args)
+        if rc != N.MOE_OK:
+            raise N.MoeError(rc, "moe_forward_fp8_host_io")
 
 
 class BoundHostIO:

@@ -35,6 +35,25 @@ def test_library_exports_every_declared_function(path):
     assert set(N.EXPORTS) <= declared
 
 
+def test_fp8_host_io_checks_arguments_without_gpu():
+    cfg = L.config_for(W.get("gptoss16_fp8"))
+    fp8 = L.workspace_size(cfg, "fp8")
+    hio = L.workspace_size(cfg, "host_io_fp8")
+    assert hio > fp8
+    fake = ctypes.c_void_p(4096)
+    lib = N.lib()
+    args = [ctypes.byref(cfg)] + [fake] * 12 + [ctypes.c_size_t(hio), None]
+    bad = list(args)
+    bad[1] = None                                      # no host x
+    assert lib.moe_forward_fp8_host_io(*bad) == N.MOE_ERR_ARG
+    bad = list(args)
+    bad[6] = None                                      # no W1 scales
+    assert lib.moe_forward_fp8_host_io(*bad) == N.MOE_ERR_ARG
+    bad = list(args)
+    bad[11] = None                                     # no host loss
+    assert lib.moe_forward_fp8_host_io(*bad) == N.MOE_ERR_ARG
+
+
 def test_tuning_knobs_check_their_arguments():
     lib = N.lib()
     assert lib.moe_set_tuning(99, 0) == N.MOE_ERR_ARG

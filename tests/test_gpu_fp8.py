@@ -81,3 +81,21 @@ def test_fp8_zero_token_rows():
     inp.x.zero_()
     _, out = run_gpu(inp)
     assert torch.count_nonzero(out.y) == 0
+
+
+@pytest.mark.parametrize("shape", [FP8[1], FP8[2]], ids=lambda s: s.name)
+def test_fp8_host_io_entry_point_matches_device_entry_point(shape):
+    """moe_forward_fp8_host_io (x from pinned host memory, y and the loss back
+    to the host) gives exactly moe_forward_fp8's y and loss."""
+    inp = W.make_inputs(shape, "cuda", seed=6)
+    cfg, dev = run_gpu(inp)
+    x_h = inp.x.cpu().pin_memory()
+    y_h = torch.empty_like(x_h).pin_memory()
+    aux_h = torch.empty(1, dtype=torch.float32).pin_memory()
+    hio = L.BoundHostIOFp8(cfg, x_h, y_h, aux_h, inp.W_r, inp.W1q, inp.W1s, inp.W3q, inp.W3s,
+                           inp.W2, inp.logit_offset, inp.sel_bias)
+    hio()
+    torch.cuda.synchronize()
+    assert L.check_status(hio.workspace) == 0
+    assert torch.equal(y_h, dev.y.cpu())
+    assert torch.equal(aux_h, dev.aux_loss.cpu())
