@@ -387,8 +387,6 @@ int moe_launch_count(const moe_config* cfg, int32_t* launches);
  *   MOE_TUNE_TILE_N_UP / _DOWN  output columns per tensor-core tile (one of the
  *                            compiled widths, else ignored);
  *   MOE_TUNE_PARTIAL_A_ROWS  tiles with at most this many rows load only them;
- *   MOE_TUNE_ZERO_PAD        1: the rows such a tile does not load are zeros,
- *                            0 (the default): they keep stale stage data;
  *   MOE_TUNE_MMA_M64         1 (the default): expert tiles of at most 64 rows
  *                            multiply with M = 64, 0: always M = 128;
  *   MOE_TUNE_FUSED_COMBINE   1: bf16 layers with k > 1 or a shared expert
@@ -405,10 +403,9 @@ enum {
   MOE_TUNE_TILE_N_UP = 2,
   MOE_TUNE_TILE_N_DOWN = 3,
   MOE_TUNE_PARTIAL_A_ROWS = 4,
-  MOE_TUNE_ZERO_PAD = 5,
-  MOE_TUNE_MMA_M64 = 6,
-  MOE_TUNE_FUSED_COMBINE = 7,
-  MOE_TUNE_COUNT = 8
+  MOE_TUNE_MMA_M64 = 5,
+  MOE_TUNE_FUSED_COMBINE = 6,
+  MOE_TUNE_COUNT = 7
 };
 enum { MOE_ROUTER_SIMT = 1, MOE_ROUTER_FUSED = 2, MOE_ROUTER_TC = 3 };
 int moe_set_tuning(int32_t knob, int32_t value);

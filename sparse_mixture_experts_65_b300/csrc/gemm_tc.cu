@@ -101,8 +101,6 @@ struct TcArgs {
   const float* b0_scale = nullptr;  // ... and of each output column of B0 / B1, [E][N]
   const float* b1_scale = nullptr;
   int R_cap = 0;                    // rows of the routed output buffer
-  int a_rows = 0, a_rows_sh = 0;    // row extents of the routed / shared A maps
-  int zero_pad = 0;                 // partial A tiles: fill the unloaded rows with zeros
   int m64 = 0;                      // routed tiles of <= 64 rows multiply with M = 64
   unsigned* cmb_ctr = nullptr;      // EPI_COMBINEK: [T][cmb_nt] arrival counters
   int cmb_nt = 0;                   // N tiles per token row
@@ -295,24 +293,18 @@ constexpr int kABox = 32;
 __device__ __forceinline__ int a_real_boxes(int rows, int partial_rows) {
   return rows > partial_rows ? 0 : (rows + kABox - 1) / kABox;
 }
-// Bytes the A loads of one stage deliver.  With zero_pad the boxes past the
-// real rows are loaded too, from a row coordinate past the map's extent: the
-// copy engine fills them with zeros without reading memory, so the padding
-// rows multiply zeros instead of stale data.
-__device__ __forceinline__ uint32_t a_stage_bytes(int boxes, bool zero_pad, uint32_t full) {
-  return boxes == 0 || zero_pad ? full : (uint32_t)boxes * kABox * 128u;
+// Bytes the A loads of one stage deliver.
+__device__ __forceinline__ uint32_t a_stage_bytes(int boxes, uint32_t full) {
+  return boxes == 0 ? full : (uint32_t)boxes * kABox * 128u;
 }
 __device__ __forceinline__ void load_a_stage(uint32_t sa, const CUtensorMap* pA,
                                              const CUtensorMap* pA32, uint32_t bar, int kx,
-                                             int a_row, int boxes, bool zero_pad, int oob_row) {
+                                             int a_row, int boxes) {
   if (boxes == 0) {
     tma_load_2d(sa, pA, bar, kx, a_row);
     return;
   }
   for (int b = 0; b < boxes; ++b) tma_load_2d(sa + b * kABox * 128, pA32, bar, kx, a_row + b * kABox);
-  if (zero_pad)
-    for (int b = boxes; b < kTcBM / kABox; ++b)
-      tma_load_2d(sa + b * kABox * 128, pA32, bar, kx, oob_row);
 }
 
 // The A rows of one stage gathered from the token rows of x: 32 warp
@@ -550,7 +542,7 @@ tc_grouped_gemm(const __grid_constant__ CUtensorMap mA, const __grid_constant__ 
       const int nk = (ti.K + C::BK - 1) / C::BK;
       const int rows = ti.row_end - ti.a_row < kTcBM ? ti.row_end - ti.a_row : kTcBM;
       const int a_boxes = a_real_boxes(rows, a.partial_rows);
-      const uint32_t a_bytes = a_stage_bytes(a_boxes, a.zero_pad, C::A_BYTES);
+      const uint32_t a_bytes = a_stage_bytes(a_boxes, C::A_BYTES);
       for (int kb = 0; kb < nk && npre < (uint32_t)C::STAGES; ++kb, ++npre) {
         const uint32_t sb = smem_base + npre * C::STAGE_BYTES + C::A_BYTES;
         mbar_arrive_expect_tx(full_bar(npre), a_bytes + C::B_BYTES);
@@ -606,7 +598,7 @@ tc_grouped_gemm(const __grid_constant__ CUtensorMap mA, const __grid_constant__ 
         const int e = ti.shared ? 0 : ti.seg;
         const int rows = ti.row_end - ti.a_row < kTcBM ? ti.row_end - ti.a_row : kTcBM;
         const int a_boxes = gat ? 0 : a_real_boxes(rows, a.partial_rows);
-        const uint32_t a_bytes = gat ? 0u : a_stage_bytes(a_boxes, a.zero_pad, C::A_BYTES);
+        const uint32_t a_bytes = gat ? 0u : a_stage_bytes(a_boxes, C::A_BYTES);
         // token of every row of the tile (-1 for padding rows), per warp;
         // loaded after the warp's first B tile of the tile is in flight
         int* tok_s = reinterpret_cast<int*>(smem + C::STAGES * C::STAGE_BYTES + C::BAR_BYTES +
@@ -631,8 +623,7 @@ tc_grouped_gemm(const __grid_constant__ CUtensorMap mA, const __grid_constant__ 
           if (lane == 0) {
             mbar_arrive_expect_tx(full_bar(s), a_bytes + C::B_BYTES);
             if (!gat)
-              load_a_stage(sa, &mA_sh, &mA32_sh, full_bar(s), kb * C::BKX, ti.a_row, a_boxes,
-                           a.zero_pad, a.a_rows_sh);
+              load_a_stage(sa, &mA_sh, &mA32_sh, full_bar(s), kb * C::BKX, ti.a_row, a_boxes);
             tma_load_3d(sb, pB0, full_bar(s), kb * C::BKX, ti.n0, e);
             if (DUAL) tma_load_3d(sb + BNH * 128, pB1, full_bar(s), kb * C::BKX, ti.n0, e);
           }
@@ -691,7 +682,7 @@ tc_grouped_gemm(const __grid_constant__ CUtensorMap mA, const __grid_constant__ 
         const int nk = (ti.K + C::BK - 1) / C::BK;
         const int rows = ti.row_end - ti.a_row < kTcBM ? ti.row_end - ti.a_row : kTcBM;
         const int a_boxes = a_real_boxes(rows, a.partial_rows);
-        const uint32_t a_sh_bytes = a_stage_bytes(a_boxes, a.zero_pad, C::A_BYTES);
+        const uint32_t a_sh_bytes = a_stage_bytes(a_boxes, C::A_BYTES);
         int tk0 = 0, tk1 = 0, tk2 = 0, tk3 = 0;
         if (!ti.shared) {
           int tk[4];
@@ -727,8 +718,7 @@ tc_grouped_gemm(const __grid_constant__ CUtensorMap mA, const __grid_constant__ 
             mbar_arrive_expect_tx(full_bar(s),
                                   (ti.shared ? a_sh_bytes : (uint32_t)C::A_BYTES) + C::B_BYTES);
             if (ti.shared)
-              load_a_stage(sa, &mA_sh, &mA32_sh, full_bar(s), kb * C::BKX, ti.a_row, a_boxes,
-                           a.zero_pad, a.a_rows_sh);
+              load_a_stage(sa, &mA_sh, &mA32_sh, full_bar(s), kb * C::BKX, ti.a_row, a_boxes);
             tma_load_3d(sb, pB0, full_bar(s), kb * C::BKX, ti.n0, e);
             if (DUAL) tma_load_3d(sb + BNH * 128, pB1, full_bar(s), kb * C::BKX, ti.n0, e);
           }
@@ -763,8 +753,7 @@ tc_grouped_gemm(const __grid_constant__ CUtensorMap mA, const __grid_constant__ 
         const int nk = (ti.K + C::BK - 1) / C::BK;
         const int rows = ti.row_end - ti.a_row < kTcBM ? ti.row_end - ti.a_row : kTcBM;
         const int a_boxes = a_real_boxes(rows, a.partial_rows);
-        const uint32_t a_bytes = a_stage_bytes(a_boxes, a.zero_pad, C::A_BYTES);
-        const int oob_row = ti.shared ? a.a_rows_sh : a.a_rows;
+        const uint32_t a_bytes = a_stage_bytes(a_boxes, C::A_BYTES);
         for (int kb = 0; kb < nk; ++kb, ++g) {
           const int s = g % C::STAGES;
           const uint32_t ph = (g / C::STAGES) & 1u;
@@ -777,8 +766,7 @@ tc_grouped_gemm(const __grid_constant__ CUtensorMap mA, const __grid_constant__ 
           const uint32_t sa = smem_base + s * C::STAGE_BYTES;
           const uint32_t sb = sa + C::A_BYTES;
           if (!pre) mbar_arrive_expect_tx(full_bar(s), a_bytes + C::B_BYTES);
-          load_a_stage(sa, pA, pA32, full_bar(s), kb * C::BKX, ti.a_row, a_boxes, a.zero_pad,
-                       oob_row);
+          load_a_stage(sa, pA, pA32, full_bar(s), kb * C::BKX, ti.a_row, a_boxes);
           if (!pre) {
             tma_load_3d(sb, pB0, full_bar(s), kb * C::BKX, ti.n0, e);
             if (DUAL) tma_load_3d(sb + BNH * 128, pB1, full_bar(s), kb * C::BKX, ti.n0, e);
@@ -1152,9 +1140,6 @@ cudaError_t launch_experts_tc(const Plan& p, const void* x, const void* W1, cons
   au.ld_out_sh = sh ? c.f_shared : 0;
   au.R_cap = p.R_cap;
   au.T_x = c.T;
-  au.a_rows = (int)a_rows;
-  au.a_rows_sh = c.T;
-  au.zero_pad = p.zero_pad ? 1 : 0;
   au.m64 = p.m64 ? 1 : 0;
   unsigned* cmb_ctr = p.combine_k ? reinterpret_cast<unsigned*>(w + p.ws.cmb_ctr) : nullptr;
   au.zero_ctr = cmb_ctr;
@@ -1190,8 +1175,6 @@ cudaError_t launch_experts_tc(const Plan& p, const void* x, const void* W1, cons
   if (!ok) return cudaErrorInvalidValue;
   TcArgs ad = au;
   ad.partial_rows = p.partial_rows;
-  ad.a_rows = p.R_cap;
-  ad.a_rows_sh = p.T_pad;
   ad.early_b = 1;   // the schedule comes from the routing kernel, two launches back
   ad.zero_ctr = nullptr;
   ad.zero_ctr_n = 0;
@@ -1248,8 +1231,6 @@ cudaError_t launch_router_tc(const Plan& p, const void* x, const void* W_r,
   a.ld_out = c.E;
   a.rows_sh = c.T;
   a.static_mt = (c.T + kTcBM - 1) / kTcBM;
-  a.a_rows = c.T;
-  a.a_rows_sh = c.T;
   a.static_total = a.static_mt * ((c.E + bn - 1) / bn);
   a.col_bias = logit_offset;
   a.partial_rows = p.partial_rows;

@@ -41,7 +41,7 @@ int make_plan(const moe_config* cfg, WsKind kind, Plan* p, int num_sms);
 
 // Process-wide overrides set through moe_set_tuning (tests and tile sweeps
 // only); -1 = no override.  Production calls never read the environment.
-static std::atomic<int> g_tune[MOE_TUNE_COUNT] = {-1, -1, -1, -1, -1, -1, -1, -1};
+static std::atomic<int> g_tune[MOE_TUNE_COUNT] = {-1, -1, -1, -1, -1, -1, -1};
 
 int tuning(int knob) {
   return knob >= 0 && knob < MOE_TUNE_COUNT ? g_tune[knob].load(std::memory_order_relaxed) : -1;
@@ -209,11 +209,6 @@ int make_plan(const moe_config* cfg, WsKind kind, Plan* p, int num_sms) {
     const int v = tuning(MOE_TUNE_PARTIAL_A_ROWS);
     P.partial_rows = v >= 0 ? v : 64;
     P.partial_rows_up = v >= 0 ? P.partial_rows : (c.act == MOE_ACT_SWIGLU ? 0 : 64);
-    // the rows a partial tile does not load are filled with zeros by the copy
-    // engine (a box past the map's extent), so that padding rows multiply
-    // zeros rather than stale stage data
-    const int z = tuning(MOE_TUNE_ZERO_PAD);
-    P.zero_pad = z >= 0 ? z != 0 : false;
     // routed tiles with at most 64 rows (the last tile of a segment, small
     // segments) issue M = 64 MMAs: half the tensor work of an M = 128 tile
     const int m = tuning(MOE_TUNE_MMA_M64);
@@ -729,8 +724,7 @@ int moe_set_tuning(int32_t knob, int32_t value) {
   if (knob < 0 || knob >= MOE_TUNE_COUNT || value < -1) return MOE_ERR_ARG;
   if (knob == MOE_TUNE_ROUTER && value > MOE_ROUTER_TC) return MOE_ERR_ARG;
   if (knob == MOE_TUNE_GATHER && value > 2) return MOE_ERR_ARG;
-  if ((knob == MOE_TUNE_ZERO_PAD || knob == MOE_TUNE_MMA_M64 ||
-       knob == MOE_TUNE_FUSED_COMBINE) && value > 1)
+  if ((knob == MOE_TUNE_MMA_M64 || knob == MOE_TUNE_FUSED_COMBINE) && value > 1)
     return MOE_ERR_ARG;
   g_tune[knob].store(value, std::memory_order_relaxed);
   return MOE_OK;

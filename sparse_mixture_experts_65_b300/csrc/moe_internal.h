@@ -92,7 +92,6 @@ struct Plan {
   bool combine_k;             // other bf16 layers: the down epilogue's last row per token sums y
   bool gather;                // the up projection gathers token rows with cp.async
   bool gather4;               // the up projection gathers token rows with TMA (tile::gather4)
-  bool zero_pad;              // partial A tiles load zeros (no memory read) into their padding rows
   bool m64;                   // routed GEMM tiles of <= 64 rows multiply with M = 64
   bool fp8;                   // gate/up weights in e4m3: quantised rows, fp8 up projection
   int num_sms;
