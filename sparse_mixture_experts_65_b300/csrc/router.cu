@@ -279,13 +279,17 @@ __device__ __forceinline__ void route_one_token(const float (&sv)[NPL_MAX], int 
                                                 float (&psum)[NPL_MAX]) {
   const int lane = threadIdx.x & 31;
   const bool sigm = gate == MOE_GATE_SIGMOID_RENORM;
-  float sel[NPL_MAX];
+  // affinities, once per score: the logit, or its sigmoid with the hardware
+  // exponential and an approximate reciprocal (relative error ~1e-7, far
+  // inside the 1e-5 near-tie band and the gate tolerance)
+  float aff[NPL_MAX], sel[NPL_MAX];
 #pragma unroll
   for (int i = 0; i < NPL_MAX; ++i) {
     const int e = lane + 32 * i;
+    aff[i] = sigm ? __fdividef(1.0f, 1.0f + __expf(-sv[i])) : sv[i];
     sel[i] = -INFINITY;
     if (e < E) {
-      float v = sigm ? sigmoidf_(sv[i]) : sv[i];
+      float v = aff[i];
       if (sel_bias) v += sel_bias[e];
       sel[i] = (v != v) ? -INFINITY : v;
     }
@@ -333,7 +337,7 @@ __device__ __forceinline__ void route_one_token(const float (&sv)[NPL_MAX], int 
   float z_all = 0.f;
 #pragma unroll
   for (int i = 0; i < NPL_MAX; ++i)
-    if (lane + 32 * i < E) z_all += sigm ? sigmoidf_(sv[i]) : expf(sv[i] - m_all);
+    if (lane + 32 * i < E) z_all += sigm ? aff[i] : expf(sv[i] - m_all);
   z_all = warp_sum(z_all);
   float g;
   if (gate == MOE_GATE_SOFTMAX_TOPK) {
@@ -341,7 +345,7 @@ __device__ __forceinline__ void route_one_token(const float (&sv)[NPL_MAX], int 
     const float ek = mine ? expf(s_me - m_k) : 0.f;
     g = ek / warp_sum(ek);
   } else if (sigm) {
-    const float ak = mine ? sigmoidf_(s_me) : 0.f;
+    const float ak = mine ? __fdividef(1.0f, 1.0f + __expf(-s_me)) : 0.f;
     g = ak / warp_sum(ak);
   } else {
     g = expf(s_me - m_all) / z_all;
@@ -354,7 +358,7 @@ __device__ __forceinline__ void route_one_token(const float (&sv)[NPL_MAX], int 
 #pragma unroll
   for (int i = 0; i < NPL_MAX; ++i)
     if (lane + 32 * i < E)
-      psum[i] += sigm ? sigmoidf_(sv[i]) / z_all : expf(sv[i] - m_all) / z_all;
+      psum[i] += sigm ? aff[i] / z_all : expf(sv[i] - m_all) / z_all;
 }
 
 // Block epilogue of a routing block: the per-warp probability sums (fixed
