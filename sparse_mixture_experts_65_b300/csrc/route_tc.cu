@@ -48,7 +48,16 @@ namespace moe {
 
 constexpr int kRtThreads = 192;
 constexpr int kRtBK = 64;          // k per stage (128 bytes of bf16: one swizzle row)
-constexpr int kRtChunkKB = 2;      // stages per TMEM accumulator (128-wide chunks)
+// Stages per TMEM accumulator: 128-wide chunks of the model width, whose
+// float32 sums the epilogue adds in chunk order (the tensor cores' own
+// accumulation then spans at most 8 MMA steps: ~2e-6 on a 7168-wide router).
+// Narrow routers (d <= 768) take two chunks of at most 384: at most 24 steps
+// each, ~2e-6 on a 768-wide router as well, with a third of the epilogue's
+// chunk passes on the latency-bound path of the routing kernel.
+constexpr int kRtChunkKB = 2;
+__host__ __device__ inline int rt_chunk_kb(int nk) {
+  return nk <= 12 ? ((nk + 1) / 2 > kRtChunkKB ? (nk + 1) / 2 : kRtChunkKB) : kRtChunkKB;
+}
 constexpr int kRtMaxK = 8;
 constexpr int kRtLds = kTcBM + 1;  // row stride of the logit columns (odd: no bank conflicts)
 constexpr uint64_t kRtTimeoutNs = 2000000000ull;   // 2 s
@@ -436,6 +445,7 @@ __global__ void __launch_bounds__(kRtThreads, 1)
   __syncthreads();
 
   const int nk = (a.d + kRtBK - 1) / kRtBK;
+  const int ckb = rt_chunk_kb(nk);
   auto give_up = [&]() {
     atomicOr(a.status, STATUS_TIMEOUT_ROUTE);
     *abort_flag = 1;
@@ -479,7 +489,7 @@ __global__ void __launch_bounds__(kRtThreads, 1)
       int it = 0;
       bool ok = true;
       for (int tile = blockIdx.x; tile < a.ntiles && ok; tile += gridDim.x) {
-        for (int kb0 = 0; kb0 < nk && ok; kb0 += kRtChunkKB, ++it) {
+        for (int kb0 = 0; kb0 < nk && ok; kb0 += ckb, ++it) {
           const int ab = it & 1;
           const uint32_t aph = (it >> 1) & 1;
           if (!mbar_wait_bounded(tempty_bar(ab), aph ^ 1u, a.timeout_ns, abort_flag)) {
@@ -489,7 +499,7 @@ __global__ void __launch_bounds__(kRtThreads, 1)
           }
           tc_fence_after();
           const uint32_t d_tmem = tmem_base + ab * EP;
-          const int kb1 = kb0 + kRtChunkKB < nk ? kb0 + kRtChunkKB : nk;
+          const int kb1 = kb0 + ckb < nk ? kb0 + ckb : nk;
           for (int kb = kb0; kb < kb1; ++kb, ++g) {
             const int s = g % C::STAGES;
             const uint32_t ph = (g / C::STAGES) & 1u;
@@ -528,7 +538,7 @@ __global__ void __launch_bounds__(kRtThreads, 1)
       float s[EP];
 #pragma unroll
       for (int e = 0; e < EP; ++e) s[e] = 0.f;
-      for (int kb0 = 0; kb0 < nk; kb0 += kRtChunkKB, ++it) {
+      for (int kb0 = 0; kb0 < nk; kb0 += ckb, ++it) {
         const int ab = it & 1;
         const uint32_t aph = (it >> 1) & 1;
         if (!mbar_wait_bounded(tfull_bar(ab), aph, a.timeout_ns, abort_flag)) {
