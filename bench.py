@@ -21,8 +21,9 @@ Also reported:
   roofline     the dominant kernel's algorithmic bytes (or FLOPs) per launch
                over its average duration, from per-stage CUDA events recorded
                inside the timed region, against the measured peak;
-  e2e          the same metric through moe_forward_host_io: x copied from
-               pinned host memory and y copied back inside every step;
+  e2e          the same metric through moe_forward_host_io_batches: every step's
+               x copied from pinned host memory and its y and loss copied back,
+               the copies overlapping the neighbouring steps' layers;
   cpu_baseline the fp64 CPU oracle on the host cores, all BLAS threads and one
                (rank 0, N = 1 only): routing of the whole batch, whole experts
                timed on a seeded sample, the whole-layer time scaled from it;
@@ -728,33 +729,39 @@ def run_b300(args):
 
     e2e = None
     if not args.no_e2e:
-        x_h = inp.x.cpu().pin_memory()
-        y_h = torch.empty_like(x_h).pin_memory()
-        aux_h = torch.empty(1, dtype=torch.float32).pin_memory()
-        if fp8:
-            hio = L.BoundHostIOFp8(cfg, x_h, y_h, aux_h, inp.W_r, inp.W1q, inp.W1s, inp.W3q,
-                                   inp.W3s, inp.W2, inp.logit_offset, inp.sel_bias, stream=stream)
-        else:
-            hio = L.BoundHostIO(cfg, x_h, y_h, aux_h, inp.W_r, inp.W1, inp.W2, inp.W3,
-                                inp.logit_offset, inp.sel_bias, inp.Ws1, inp.Ws3, inp.Ws2,
-                                stream=stream)
-        for _ in range(Wm):
-            hio()
+        # The user's call for a stream of batches in host memory: each step is
+        # one batch, its x copied in from pinned host memory and its y and loss
+        # copied back, the copies overlapping the layer of the neighbouring
+        # batches (moe_forward_host_io_batches).  A ring of 4 pinned buffers
+        # holds the batches (every step copies its full batch both ways).
+        ring = 4
+        x_h = [inp.x.cpu().pin_memory() for _ in range(ring)]
+        y_h = [torch.empty_like(x_h[0]).pin_memory() for _ in range(ring)]
+        aux_h = torch.empty(max(K, Wm), dtype=torch.float32).pin_memory()
+        cin, cout = torch.cuda.Stream(), torch.cuda.Stream()
+        warm = L.BoundHostIOBatches(cfg, [x_h[i % ring] for i in range(Wm)],
+                                    [y_h[i % ring] for i in range(Wm)], aux_h, inp,
+                                    stream=stream, copy_in_stream=cin, copy_out_stream=cout)
+        hio = L.BoundHostIOBatches(cfg, [x_h[i % ring] for i in range(K)],
+                                   [y_h[i % ring] for i in range(K)], aux_h, inp, stream=stream,
+                                   copy_in_stream=cin, copy_out_stream=cout,
+                                   workspace=warm.workspace)
+        warm()
         barrier()
         s2, e2 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         s2.record(stream)
-        for _ in range(K):
-            hio()
+        hio()
         e2.record(stream)
         torch.cuda.synchronize()
         barrier()
+        assert L.check_status(hio.workspace) == 0, "device status after the host-memory batches"
         ms_e2e = max_over_ranks(s2.elapsed_time(e2), dist, "cuda")
-        io = shape.T * shape.d * x_h.element_size()
+        io = shape.T * shape.d * x_h[0].element_size()
         e2e = {"value": round(world * shape.T * K / (ms_e2e / 1e3), 1), "unit": "tokens/s",
                "h2d_bytes_per_step": io, "d2h_bytes_per_step": io + 4,
                "ms_per_step": round(ms_e2e / K, 5),
-               "api": "moe_forward_fp8_host_io" if fp8 else "moe_forward_host_io"}
-        del hio, x_h, y_h
+               "api": "moe_forward_fp8_host_io_batches" if fp8 else "moe_forward_host_io_batches"}
+        del hio, warm, x_h, y_h
 
     cpu = routing = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

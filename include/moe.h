@@ -323,6 +323,40 @@ int moe_forward_fp8_host_io(const moe_config* cfg, const void* x_host, const voi
                             void* stream);
 
 /*
+ * moe_forward_host_io_batches / moe_forward_fp8_host_io_batches -- n_batches
+ * layer calls on host-memory batches (x_host[i] -> y_host[i], aux_loss_host[i]),
+ * with the copies of one batch overlapping the layer of another: batch i+1's
+ * x travels to the device while batch i computes, and batch i's y travels back
+ * while batch i+1 computes.  The layer runs on `stream`, the copies to the
+ * device on `copy_in_stream` and the copies back on `copy_out_stream` (both
+ * different from `stream`; they may be the same stream, in which case the two
+ * directions take turns).  All three streams are the caller's.  Every other
+ * argument is that of moe_forward_host_io (resp. moe_forward_fp8_host_io),
+ * with arrays of n_batches host pointers in place of x_host / y_host and
+ * n_batches floats at aux_loss_host; pinned host memory makes the copies
+ * asynchronous.  The workspace (moe_host_io_workspace_size, resp. _fp8) holds
+ * two staging slots.  When the call returns, `stream` waits for every copy:
+ * synchronising `stream` makes all y_host and losses valid.
+ * Errors: MOE_ERR_ARG for n_batches < 0, NULL arrays or entries, or a copy
+ * stream equal to `stream`; otherwise those of moe_forward_host_io.
+ */
+int moe_forward_host_io_batches(const moe_config* cfg, int32_t n_batches,
+                                const void* const* x_host, const void* W_r,
+                                const float* logit_offset, const float* sel_bias, const void* W1,
+                                const void* W3, const void* W2, const void* Ws1, const void* Ws3,
+                                const void* Ws2, void* const* y_host, float* aux_loss_host,
+                                void* workspace, size_t workspace_bytes, void* stream,
+                                void* copy_in_stream, void* copy_out_stream);
+int moe_forward_fp8_host_io_batches(const moe_config* cfg, int32_t n_batches,
+                                    const void* const* x_host, const void* W_r,
+                                    const float* logit_offset, const float* sel_bias,
+                                    const uint8_t* W1q, const float* W1s, const uint8_t* W3q,
+                                    const float* W3s, const void* W2, void* const* y_host,
+                                    float* aux_loss_host, void* workspace,
+                                    size_t workspace_bytes, void* stream, void* copy_in_stream,
+                                    void* copy_out_stream);
+
+/*
  * Synchronises `stream`, then reads and clears the device status word in
  * `workspace`.  Returns MOE_OK, MOE_ERR_TIMEOUT when a bounded device wait
  * gave up since the last check, MOE_ERR_BOUNDS when the bounds-checked build

@@ -38,6 +38,7 @@ EXPORTS = (
     "moe_router_scores", "moe_router_scores_noalloc", "moe_router_z_loss", "moe_bias_update",
     "moe_workspace_size_fp8", "moe_forward_fp8", "moe_forward_fp8_timed", "moe_launch_count_fp8",
     "moe_set_tuning", "moe_host_io_workspace_size_fp8", "moe_forward_fp8_host_io",
+    "moe_forward_host_io_batches", "moe_forward_fp8_host_io_batches",
 )
 
 
@@ -103,6 +104,10 @@ def _load(path: str) -> ctypes.CDLL:
     L.moe_forward_host_io.restype = ctypes.c_int
     L.moe_forward_fp8_host_io.argtypes = [cfgp] + [P] * 12 + [SZ, P]
     L.moe_forward_fp8_host_io.restype = ctypes.c_int
+    L.moe_forward_host_io_batches.argtypes = [cfgp, ctypes.c_int32] + [P] * 13 + [SZ, P, P, P]
+    L.moe_forward_host_io_batches.restype = ctypes.c_int
+    L.moe_forward_fp8_host_io_batches.argtypes = [cfgp, ctypes.c_int32] + [P] * 12 + [SZ, P, P, P]
+    L.moe_forward_fp8_host_io_batches.restype = ctypes.c_int
     L.moe_router_scores.argtypes = [cfgp, P, P, P, P, P, SZ, P]
     L.moe_router_scores.restype = ctypes.c_int
     fp8_args = [cfgp] + [P] * 20 + [SZ, P]

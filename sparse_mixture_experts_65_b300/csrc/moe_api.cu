@@ -306,6 +306,9 @@ int make_plan(const moe_config* cfg, WsKind kind, Plan* p, int num_sms) {
     L.topk_w = take(sizeof(float) * (size_t)Tk);
     L.counts = take(sizeof(int) * E);
     L.aux = take(sizeof(float));
+    L.x_dev2 = take((size_t)c.T * c.d * P.elem);
+    L.y_dev2 = take((size_t)c.T * c.d * P.elem);
+    L.aux2 = take(sizeof(float));
   }
   L.total = off;
   return MOE_OK;
@@ -464,6 +467,93 @@ static int forward_impl(const moe_config* cfg, const Tensors& t, void* ws, size_
     MOE_TRY_CUDA(launch_combine(p, t.topk_w, t.y, ws, st));
   if ((rc = record(events, MOE_NUM_STAGES, st)) != MOE_OK) return rc;
   return MOE_OK;
+}
+
+// A sequence of batches from and to host memory, with the copies of one batch
+// overlapping the layer of another.  The workspace holds two staging slots for
+// x, y and the loss.  `ci` carries the copies in (H2D 0, H2D 1, then H2D i+2
+// into the slot batch i used, once batch i's layer has read it), `co` the
+// copies back (D2H i after batch i's layer); `st` runs the layers, batch i
+// after H2D i and after D2H i-2 has read the slot's y.  With ci == co the
+// copies share one stream in the order H2D 0, H2D 1, D2H 0, H2D 2, D2H 1, ...
+// At the end `st` waits for both copy streams, so that synchronising `st`
+// covers every copy.
+static int host_io_batches(const moe_config* cfg, int n, const void* const* x_host,
+                           void* const* y_host, float* aux_host, Tensors t, WsKind kind,
+                           void* workspace, size_t workspace_bytes, cudaStream_t st,
+                           cudaStream_t ci, cudaStream_t co) {
+  if (!cfg || n < 0) return MOE_ERR_ARG;
+  if (n > 0 && (!x_host || !y_host || !aux_host)) return MOE_ERR_ARG;
+  if (ci == st || co == st) return MOE_ERR_ARG;   // the copies need streams of their own
+  for (int i = 0; i < n; ++i)
+    if (!x_host[i] || !y_host[i]) return MOE_ERR_ARG;
+  Plan p;
+  int rc = make_plan(cfg, kind, &p);
+  if (rc != MOE_OK) return rc;
+  rc = check_workspace(p, workspace, workspace_bytes);
+  if (rc != MOE_OK) return rc;
+  char* w = static_cast<char*>(workspace);
+  void* xd[2] = {w + p.ws.x_dev, w + p.ws.x_dev2};
+  void* yd[2] = {w + p.ws.y_dev, w + p.ws.y_dev2};
+  float* ad[2] = {reinterpret_cast<float*>(w + p.ws.aux), reinterpret_cast<float*>(w + p.ws.aux2)};
+  t.x = xd[0];
+  t.y = yd[0];
+  t.topk_idx = reinterpret_cast<int32_t*>(w + p.ws.topk_idx);
+  t.topk_w = reinterpret_cast<float*>(w + p.ws.topk_w);
+  t.expert_counts = reinterpret_cast<int32_t*>(w + p.ws.counts);
+  t.aux_loss = ad[0];
+  rc = check_tensors(*cfg, t, false);
+  if (rc != MOE_OK) return rc;
+  if (n == 0) return MOE_OK;
+  const size_t io = (size_t)cfg->T * cfg->d * p.elem;
+  // in[2], layer[2], out[2], joins of ci and co
+  cudaEvent_t ev[8] = {};
+  for (auto& e : ev)
+    if (cudaEventCreateWithFlags(&e, cudaEventDisableTiming) != cudaSuccess) {
+      for (auto& f : ev)
+        if (f) cudaEventDestroy(f);
+      return MOE_ERR_CUDA;
+    }
+  cudaEvent_t* ev_in = ev;
+  cudaEvent_t* ev_layer = ev + 2;
+  cudaEvent_t* ev_out = ev + 4;
+  auto run = [&]() -> int {
+    auto h2d = [&](int i) -> int {
+      const int s = i & 1;
+      if (i >= 2) MOE_TRY_CUDA(cudaStreamWaitEvent(ci, ev_layer[s], 0));
+      if (io) MOE_TRY_CUDA(cudaMemcpyAsync(xd[s], x_host[i], io, cudaMemcpyHostToDevice, ci));
+      MOE_TRY_CUDA(cudaEventRecord(ev_in[s], ci));
+      return MOE_OK;
+    };
+    int r = h2d(0);
+    if (r == MOE_OK && n > 1) r = h2d(1);
+    for (int i = 0; i < n && r == MOE_OK; ++i) {
+      const int s = i & 1;
+      MOE_TRY_CUDA(cudaStreamWaitEvent(st, ev_in[s], 0));
+      if (i >= 2) MOE_TRY_CUDA(cudaStreamWaitEvent(st, ev_out[s], 0));
+      Tensors ti = t;
+      ti.x = xd[s];
+      ti.y = yd[s];
+      ti.aux_loss = ad[s];
+      r = forward_impl(cfg, ti, workspace, workspace_bytes, st, nullptr, false, kind);
+      if (r != MOE_OK) break;
+      MOE_TRY_CUDA(cudaEventRecord(ev_layer[s], st));
+      MOE_TRY_CUDA(cudaStreamWaitEvent(co, ev_layer[s], 0));
+      if (io) MOE_TRY_CUDA(cudaMemcpyAsync(y_host[i], yd[s], io, cudaMemcpyDeviceToHost, co));
+      MOE_TRY_CUDA(cudaMemcpyAsync(aux_host + i, ad[s], sizeof(float), cudaMemcpyDeviceToHost, co));
+      MOE_TRY_CUDA(cudaEventRecord(ev_out[s], co));
+      if (i + 2 < n) r = h2d(i + 2);
+    }
+    if (r != MOE_OK) return r;
+    MOE_TRY_CUDA(cudaEventRecord(ev[6], ci));
+    MOE_TRY_CUDA(cudaEventRecord(ev[7], co));
+    MOE_TRY_CUDA(cudaStreamWaitEvent(st, ev[6], 0));
+    MOE_TRY_CUDA(cudaStreamWaitEvent(st, ev[7], 0));
+    return MOE_OK;
+  };
+  rc = run();
+  for (auto& e : ev) cudaEventDestroy(e);   // released once their work completes
+  return rc;
 }
 
 }  // namespace moe
@@ -660,6 +750,39 @@ int moe_forward_fp8_host_io(const moe_config* cfg, const void* x_host, const voi
   if (io_bytes) MOE_TRY_CUDA(cudaMemcpyAsync(y_host, y_dev, io_bytes, cudaMemcpyDeviceToHost, st));
   MOE_TRY_CUDA(cudaMemcpyAsync(aux_loss_host, aux_dev, sizeof(float), cudaMemcpyDeviceToHost, st));
   return MOE_OK;
+}
+
+int moe_forward_host_io_batches(const moe_config* cfg, int32_t n_batches,
+                                const void* const* x_host, const void* W_r,
+                                const float* logit_offset, const float* sel_bias, const void* W1,
+                                const void* W3, const void* W2, const void* Ws1, const void* Ws3,
+                                const void* Ws2, void* const* y_host, float* aux_loss_host,
+                                void* workspace, size_t workspace_bytes, void* stream,
+                                void* copy_in_stream, void* copy_out_stream) {
+  Tensors t{nullptr, W_r, logit_offset, sel_bias, W1, W3, W2, Ws1, Ws3, Ws2, nullptr,
+            nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr};
+  return host_io_batches(cfg, n_batches, x_host, y_host, aux_loss_host, t, WsKind::HostIO,
+                         workspace, workspace_bytes, static_cast<cudaStream_t>(stream),
+                         static_cast<cudaStream_t>(copy_in_stream),
+                         static_cast<cudaStream_t>(copy_out_stream));
+}
+
+int moe_forward_fp8_host_io_batches(const moe_config* cfg, int32_t n_batches,
+                                    const void* const* x_host, const void* W_r,
+                                    const float* logit_offset, const float* sel_bias,
+                                    const uint8_t* W1q, const float* W1s, const uint8_t* W3q,
+                                    const float* W3s, const void* W2, void* const* y_host,
+                                    float* aux_loss_host, void* workspace,
+                                    size_t workspace_bytes, void* stream, void* copy_in_stream,
+                                    void* copy_out_stream) {
+  if (!W1s || !W3s) return MOE_ERR_ARG;
+  Tensors t{nullptr, W_r, logit_offset, sel_bias, W1q, W3q, W2, nullptr, nullptr, nullptr,
+            nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr,
+            nullptr, W1s, W3s};
+  return host_io_batches(cfg, n_batches, x_host, y_host, aux_loss_host, t, WsKind::HostIOFp8,
+                         workspace, workspace_bytes, static_cast<cudaStream_t>(stream),
+                         static_cast<cudaStream_t>(copy_in_stream),
+                         static_cast<cudaStream_t>(copy_out_stream));
 }
 
 int moe_check_status(void* workspace, void* stream) {

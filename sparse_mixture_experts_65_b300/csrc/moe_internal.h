@@ -59,6 +59,7 @@ struct WsLayout {
   size_t cmb_ctr;     // uint32 [T][N tiles of the down projection]: combine arrival counters
   // host-io staging
   size_t x_dev, y_dev, topk_idx, topk_w, counts, aux;
+  size_t x_dev2, y_dev2, aux2;   // second staging slot (pipelined batches)
   size_t total;
 };
 

@@ -351,6 +351,49 @@ class BoundHostIOFp8:
             raise N.MoeError(rc, "moe_forward_fp8_host_io")
 
 
+class BoundHostIOBatches:
+    """moe_forward_host_io_batches (or the fp8 form) with every argument
+    marshalled once: calling it runs one layer call per host batch, the copies
+    of one batch overlapping the layer of another.  x_hosts / y_hosts: lists
+    of pinned host tensors (a list may repeat a buffer); aux_host: a pinned
+    float32 host tensor with one entry per batch.  `inp` is a workload's
+    LayerInputs (device weights, bf16 or e4m3 gate/up)."""
+
+    def __init__(self, cfg: N.MoeConfig, x_hosts, y_hosts, aux_host, inp, stream=None,
+                 copy_in_stream=None, copy_out_stream=None,
+                 workspace: Optional[torch.Tensor] = None):
+        n = len(x_hosts)
+        if len(y_hosts) != n or aux_host.numel() < n:
+            raise ValueError("one y buffer and one loss entry per batch")
+        fp8 = getattr(inp, "W1q", None) is not None
+        dev = inp.W_r.device
+        self.workspace = (workspace if workspace is not None
+                          else alloc_workspace(cfg, dev, "host_io_fp8" if fp8 else "host_io"))
+        self.copy_in = copy_in_stream if copy_in_stream is not None else torch.cuda.Stream(dev)
+        self.copy_out = copy_out_stream if copy_out_stream is not None else torch.cuda.Stream(dev)
+        self._xs = (ctypes.c_void_p * n)(*[x.data_ptr() for x in x_hosts])
+        self._ys = (ctypes.c_void_p * n)(*[y.data_ptr() for y in y_hosts])
+        self._keep = (x_hosts, y_hosts, aux_host, inp)
+        head = (ctypes.byref(cfg), ctypes.c_int32(n), self._xs, _ptr(inp.W_r),
+                _ptr(inp.logit_offset), _ptr(inp.sel_bias))
+        tail = (self._ys, _ptr(aux_host), _ptr(self.workspace),
+                ctypes.c_size_t(self.workspace.numel()), _stream_handle(stream),
+                _stream_handle(self.copy_in), _stream_handle(self.copy_out))
+        if fp8:
+            self.args = head + (_ptr(inp.W1q), _ptr(inp.W1s), _ptr(inp.W3q), _ptr(inp.W3s),
+                                _ptr(inp.W2)) + tail
+            self._fn = N.lib().moe_forward_fp8_host_io_batches
+        else:
+            self.args = head + (_ptr(inp.W1), _ptr(inp.W3), _ptr(inp.W2), _ptr(inp.Ws1),
+                                _ptr(inp.Ws3), _ptr(inp.Ws2)) + tail
+            self._fn = N.lib().moe_forward_host_io_batches
+
+    def __call__(self) -> None:
+        rc = self._fn(*self.args)
+        if rc != N.MOE_OK:
+            raise N.MoeError(rc, "moe_forward_host_io_batches")
+
+
 class BoundHostIO:
     """moe_forward_host_io with every argument marshalled once."""
 

@@ -54,6 +54,28 @@ def test_fp8_host_io_checks_arguments_without_gpu():
     assert lib.moe_forward_fp8_host_io(*bad) == N.MOE_ERR_ARG
 
 
+def test_host_io_batches_check_arguments_without_gpu():
+    cfg = L.config_for(W.get("gptoss16"))
+    n = L.workspace_size(cfg, "host_io")
+    fake = ctypes.c_void_p(4096)
+    arr = (ctypes.c_void_p * 2)(4096, 8192)
+    lib = N.lib()
+    s1, s2 = ctypes.c_void_p(1), ctypes.c_void_p(2)
+
+    def call(count=2, xs=arr, ys=arr, aux=fake, st=s1, cs=s2):
+        return lib.moe_forward_host_io_batches(ctypes.byref(cfg), count, xs, fake, None, None,
+                                               fake, fake, fake, None, None, None, ys, aux, fake,
+                                               ctypes.c_size_t(n), st, cs, cs)
+    assert call(count=-1) == N.MOE_ERR_ARG
+    assert call(xs=None) == N.MOE_ERR_ARG
+    assert call(ys=None) == N.MOE_ERR_ARG
+    assert call(aux=None) == N.MOE_ERR_ARG
+    assert call(cs=s1) == N.MOE_ERR_ARG               # the copies need their own stream
+    bad = (ctypes.c_void_p * 2)(4096, None)
+    assert call(xs=bad) == N.MOE_ERR_ARG
+    assert call(count=0) == N.MOE_OK                  # nothing to do, nothing enqueued
+
+
 def test_tuning_knobs_check_their_arguments():
     lib = N.lib()
     assert lib.moe_set_tuning(99, 0) == N.MOE_ERR_ARG

@@ -99,3 +99,18 @@ def test_fp8_host_io_entry_point_matches_device_entry_point(shape):
     assert L.check_status(hio.workspace) == 0
     assert torch.equal(y_h, dev.y.cpu())
     assert torch.equal(aux_h, dev.aux_loss.cpu())
+
+
+def test_fp8_host_io_batches_match_device_entry_point():
+    shape = FP8[1]
+    inp = W.make_inputs(shape, "cuda", seed=7)
+    cfg, dev = run_gpu(inp)
+    x_h = [inp.x.cpu().pin_memory() for _ in range(3)]
+    y_h = [torch.empty_like(x).pin_memory() for x in x_h]
+    aux_h = torch.empty(3, dtype=torch.float32).pin_memory()
+    b = L.BoundHostIOBatches(cfg, x_h, y_h, aux_h, inp)
+    b()
+    torch.cuda.synchronize()
+    for y in y_h:
+        assert torch.equal(y, dev.y.cpu())
+    assert torch.all(aux_h == dev.aux_loss.cpu()[0])

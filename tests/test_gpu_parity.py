@@ -401,3 +401,35 @@ def test_forced_router_path_parity(path):
         with L.tuning(router=path):
             _, out = run_gpu(inp)
         check_layer(inp, out)
+
+
+@pytest.mark.parametrize("one_copy_stream", [False, True], ids=["in_out_streams", "one_stream"])
+@pytest.mark.parametrize("shape", [SMALL[0], SMALL[2], DECODE[1]], ids=lambda s: s.name)
+def test_host_io_batches_match_forward_per_batch(shape, one_copy_stream):
+    """moe_forward_host_io_batches: five host batches (different x), the copies
+    of one overlapping the layer of another through two staging slots (copies
+    in and out on two streams, or taking turns on one), give exactly what
+    moe_forward gives for each batch."""
+    base = W.make_inputs(shape, "cuda", seed=15)
+    cfg = L.config_for(shape)
+    xs = [W.make_x(shape, "cuda", seed=40 + i) for i in range(5)]
+    refs = []
+    for x in xs:
+        inp = W.make_inputs(shape, "cuda", seed=15)
+        inp.x = x
+        _, out = run_gpu(inp, cfg)
+        refs.append((out.y.cpu(), out.aux_loss.cpu()))
+    x_h = [x.cpu().pin_memory() for x in xs]
+    y_h = [torch.empty_like(x).pin_memory() for x in x_h]
+    aux_h = torch.empty(5, dtype=torch.float32).pin_memory()
+    cs = torch.cuda.Stream() if one_copy_stream else None
+    b = L.BoundHostIOBatches(cfg, x_h, y_h, aux_h, base, copy_in_stream=cs, copy_out_stream=cs)
+    b()
+    torch.cuda.synchronize()
+    assert L.check_status(b.workspace) == 0
+    for i, (y, aux) in enumerate(refs):
+        assert torch.equal(y_h[i], y), i
+        assert aux_h[i].item() == aux.item(), i
+    b()                                       # a second call on the same workspace
+    torch.cuda.synchronize()
+    assert torch.equal(y_h[4], refs[4][0])
