@@ -438,11 +438,13 @@ __global__ void __launch_bounds__(kRtThreads, 1)
   const uint32_t tmem_base = *tmem_slot;
   pdl_wait();
   pdl_trigger();
-  if (tid < EP) {
-    bias_s[tid] = (a.sel_bias && tid < a.E) ? a.sel_bias[tid] : 0.f;
-    offs_s[tid] = (a.logit_offset && tid < a.E) ? a.logit_offset[tid] : 0.f;
+  // the selection bias and the logit offset are read by the epilogue warps
+  // only (after their first named barrier), so the producer and the MMA
+  // issuer start streaming without waiting for these loads
+  if (tid >= 64 && tid - 64 < EP) {
+    bias_s[tid - 64] = (a.sel_bias && tid - 64 < a.E) ? a.sel_bias[tid - 64] : 0.f;
+    offs_s[tid - 64] = (a.logit_offset && tid - 64 < a.E) ? a.logit_offset[tid - 64] : 0.f;
   }
-  __syncthreads();
 
   const int nk = (a.d + kRtBK - 1) / kRtBK;
   const int ckb = rt_chunk_kb(nk);
@@ -575,13 +577,20 @@ __global__ void __launch_bounds__(kRtThreads, 1)
       route_token<EP>(s, a.E, a.k, a.gate, bias_s, valid, a.topk_idx + (size_t)t * a.k,
                       a.topk_w + (size_t)t * a.k, keys_s + tl * a.k, ca_s + tl * a.k, lg + tl);
       epi_bar();
-      // probability sums of the tile: two halves of 64 tokens, in token order
+      // probability sums of the tile: two halves of 64 tokens, each as eight
+      // interleaved partial sums added in a fixed tree (independent loads)
       if (ep_tid < 2 * a.E) {
         const int e = ep_tid >> 1, half = ep_tid & 1;
         const float* row = lg + e * kRtLds + half * (kTcBM / 2);
-        float acc = 0.f;
-        for (int i = 0; i < kTcBM / 2; ++i) acc += row[i];
-        ph[half * EP + e] = acc;
+        float acc[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) acc[u] = row[u];
+#pragma unroll
+        for (int i = 8; i < kTcBM / 2; i += 8)
+#pragma unroll
+          for (int u = 0; u < 8; ++u) acc[u] += row[i + u];
+        ph[half * EP + e] = ((acc[0] + acc[1]) + (acc[2] + acc[3])) +
+                            ((acc[4] + acc[5]) + (acc[6] + acc[7]));
       }
       const int ntok = a.T - t0 < kTcBM ? a.T - t0 : kTcBM;
       const int nkeys = ntok * a.k;
