@@ -433,3 +433,43 @@ def test_host_io_batches_match_forward_per_batch(shape, one_copy_stream):
     b()                                       # a second call on the same workspace
     torch.cuda.synchronize()
     assert torch.equal(y_h[4], refs[4][0])
+
+
+# ---------------------------------------------------------------- limits
+LIMITS = [
+    # the largest expert count and k the ABI takes (split router, sigmoid gates, bias)
+    LayerShape("max_e512_k32", 60, T=100, d=128, E=512, k=32, f=64, act=SW, gate=SIG,
+               dtype="bf16", sel_bias_halfwidth=0.05),
+    LayerShape("max_e512_k32_f32", 61, T=40, d=32, E=512, k=32, f=16, act=GE, gate=TOPK,
+               dtype="f32"),
+    # either side of the decode-batch threshold (16 tokens) and of the
+    # tensor-core router threshold (256 tokens), with E > 64
+    LayerShape("decode_edge_t16", 62, T=16, d=192, E=96, k=4, f=64, act=SW, gate=TOPK,
+               dtype="bf16"),
+    LayerShape("decode_edge_t17", 63, T=17, d=192, E=96, k=4, f=64, act=SW, gate=TOPK,
+               dtype="bf16"),
+    LayerShape("router_tc_edge_t255", 64, T=255, d=256, E=80, k=2, f=64, act=RE, gate=FULL,
+               dtype="bf16", capacity_factor=1.25, logit_offset_var=1.5),
+    LayerShape("router_tc_edge_t256", 65, T=256, d=256, E=80, k=2, f=64, act=RE, gate=FULL,
+               dtype="bf16", capacity_factor=1.25, logit_offset_var=1.5),
+]
+
+
+@pytest.mark.parametrize("shape", LIMITS, ids=lambda s: s.name)
+def test_limits_and_thresholds(shape):
+    inp = W.make_inputs(shape, "cuda", seed=17)
+    _, out = run_gpu(inp)
+    check_layer(inp, out)
+
+
+def test_one_launch_router_largest_batch():
+    """65 536 tokens: the largest batch of the one-launch router (512 tiles on
+    at most 148 CTAs, several tiles per CTA), Switch-like skew and drops;
+    routing over the whole batch, y on a sample."""
+    shape = LayerShape("route_t65536", 66, T=65536, d=128, E=64, k=1, f=128, act=RE, gate=FULL,
+                       dtype="bf16", capacity_factor=1.25, logit_offset_var=1.5)
+    inp = W.make_inputs(shape, "cuda", seed=18)
+    _, out = run_gpu(inp)
+    sample = np.sort(np.random.default_rng(19).choice(shape.T, 256, replace=False))
+    rep = check_layer(inp, out, sample=sample)
+    assert rep["dropped"] > 0
