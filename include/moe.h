@@ -427,7 +427,10 @@ int moe_launch_count(const moe_config* cfg, int32_t* launches);
  *                            combine in the down projection's epilogue (the
  *                            last row of each token's column slice sums it, in
  *                            the fixed slot order); 0 (the default): a separate
- *                            combine kernel.  y is the same bit for bit.
+ *                            combine kernel.  y is the same bit for bit;
+ *   MOE_TUNE_CLUSTER         1: the TMA-fed expert projections run as clusters
+ *                            of two CTAs on adjacent column tiles sharing one
+ *                            multicast A tile; 0 (the default): single CTAs.
  * Errors: MOE_ERR_ARG for an unknown knob or a value out of range.  Not
  * synchronised with calls in flight on other threads.
  */
@@ -439,7 +442,8 @@ enum {
   MOE_TUNE_PARTIAL_A_ROWS = 4,
   MOE_TUNE_MMA_M64 = 5,
   MOE_TUNE_FUSED_COMBINE = 6,
-  MOE_TUNE_COUNT = 7
+  MOE_TUNE_CLUSTER = 7,
+  MOE_TUNE_COUNT = 8
 };
 enum { MOE_ROUTER_SIMT = 1, MOE_ROUTER_FUSED = 2, MOE_ROUTER_TC = 3 };
 int moe_set_tuning(int32_t knob, int32_t value);

@@ -28,6 +28,7 @@ MOE_GATE_SOFTMAX_TOPK, MOE_GATE_SIGMOID_RENORM, MOE_GATE_SOFTMAX_FULL = 0, 1, 2
 MOE_NUM_STAGES = 6
 MOE_TUNE_ROUTER, MOE_TUNE_GATHER, MOE_TUNE_TILE_N_UP, MOE_TUNE_TILE_N_DOWN = 0, 1, 2, 3
 MOE_TUNE_PARTIAL_A_ROWS, MOE_TUNE_MMA_M64, MOE_TUNE_FUSED_COMBINE = 4, 5, 6
+MOE_TUNE_CLUSTER = 7
 MOE_ROUTER_SIMT, MOE_ROUTER_FUSED, MOE_ROUTER_TC = 1, 2, 3
 STAGE_NAMES = ("router", "topk", "permute", "up", "down", "combine")
 

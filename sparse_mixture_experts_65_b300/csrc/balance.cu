@@ -31,12 +31,6 @@ namespace moe {
 constexpr int kZlCluster = 8;     // CTAs of the one cluster (portable size)
 constexpr int kZlThreads = 512;
 
-__device__ __forceinline__ uint32_t cluster_ctarank() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-  return r;
-}
-
 // Every thread of every CTA of the cluster arrives; release/acquire order the
 // shared-memory writes before the barrier with the reads after it.
 __device__ __forceinline__ void cluster_barrier() {

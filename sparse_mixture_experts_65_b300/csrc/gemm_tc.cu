@@ -208,6 +208,60 @@ __device__ __forceinline__ TileInfo decode_tile(const TcArgs& a, const Sched& sc
 
 // silu(g) * u with the hardware exponential and an approximate division
 // (relative error ~1e-7, far below the bf16 rounding of h)
+// Work item of a 2-CTA cluster: a pair of adjacent N tiles of one M tile;
+// CTA rank r of the cluster takes N tile 2*np + r (past the segment's last N
+// tile for an odd count: a phantom tile whose B loads fall outside the weight
+// map -- zeros -- and whose results are never stored).  Pairs are numbered
+// like tiles, N-major inside a segment; since every routed segment has the
+// same number of N tiles, the pair prefix of segment s is (tp[s] / nt) * ntp.
+__device__ __forceinline__ int pair_prefix(const TcArgs& a, const Sched& sc, int s, int nt,
+                                           int ntp) {
+  return (sc.tp[s] / nt) * ntp;
+}
+
+__device__ __forceinline__ int total_pairs(const TcArgs& a, const Sched& sc, int bnh) {
+  const int nt = (a.N + bnh - 1) / bnh, ntp = (nt + 1) / 2;
+  int tot = pair_prefix(a, sc, a.E, nt, ntp);
+  if (a.has_shared) {
+    const int nt_sh = (a.N_sh + bnh - 1) / bnh;
+    tot += sc.mtiles[a.E] * ((nt_sh + 1) / 2);
+  }
+  return tot;
+}
+
+__device__ __forceinline__ TileInfo decode_pair(const TcArgs& a, const Sched& sc, int pair,
+                                                int bnh, int rank) {
+  const int nt = (a.N + bnh - 1) / bnh, ntp = (nt + 1) / 2;
+  const int routed = pair_prefix(a, sc, a.E, nt, ntp);
+  TileInfo ti;
+  int local, mt;
+  if (pair >= routed) {
+    ti.seg = a.E;
+    ti.shared = true;
+    local = pair - routed;
+    mt = sc.mtiles[a.E];
+  } else {
+    int lo = 0, hi = a.E - 1;
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (pair_prefix(a, sc, mid, nt, ntp) <= pair) lo = mid; else hi = mid - 1;
+    }
+    ti.seg = lo;
+    ti.shared = false;
+    local = pair - pair_prefix(a, sc, lo, nt, ntp);
+    mt = sc.mtiles[lo];
+  }
+  const int np = local / mt, m_t = local - np * mt;
+  const int seg0 = ti.shared ? 0 : sc.seg_start[ti.seg];
+  ti.a_row = seg0 + m_t * kTcBM;
+  ti.row_end = ti.shared ? a.rows_sh : seg0 + sc.kept[ti.seg];
+  ti.n0 = (2 * np + rank) * bnh;
+  ti.K = ti.shared ? a.K_sh : a.K;
+  ti.N = ti.shared ? a.N_sh : a.N;
+  ti.m64 = a.m64 && !ti.shared && ti.row_end - ti.a_row <= 64;
+  return ti;
+}
+
 __device__ __forceinline__ float silu_mul(float g, float u) {
   return __fdividef(g, 1.0f + __expf(-g)) * u;
 }
@@ -444,7 +498,7 @@ struct TcWarps {
   static constexpr int THREADS = (PROD + 1 + EPIW) * 32;
 };
 
-template <int BNH, bool DUAL, int EPI, int AS, bool F8 = false>
+template <int BNH, bool DUAL, int EPI, int AS, bool F8 = false, int CL = 1>
 __global__ void __launch_bounds__(TcWarps<AS, EPI>::THREADS, 1)
 tc_grouped_gemm(const __grid_constant__ CUtensorMap mA, const __grid_constant__ CUtensorMap mA_sh,
                 const __grid_constant__ CUtensorMap mA32, const __grid_constant__ CUtensorMap mA32_sh,
@@ -453,6 +507,14 @@ tc_grouped_gemm(const __grid_constant__ CUtensorMap mA, const __grid_constant__ 
                 const __grid_constant__ CUtensorMap mB1_sh, const TcArgs a) {
   using C = TcCfg<BNH, DUAL, EPI, F8>;
   constexpr bool GATHER = AS == AS_CP;
+  // CL = 2: a cluster of two CTAs takes pairs of adjacent N tiles of one M
+  // tile; each CTA loads half of the A rows and multicasts them to both, so
+  // the A tile crosses from L2 once per pair; the stage's empty barrier then
+  // waits for both CTAs' MMAs.
+  static_assert(CL == 1 || (CL == 2 && AS == AS_TMA), "clusters: TMA-fed A tiles");
+  const int cl_rank = CL == 2 ? (int)(blockIdx.x & 1) : 0;
+  const int item0 = CL == 2 ? (int)(blockIdx.x >> 1) : (int)blockIdx.x;
+  const int istep = CL == 2 ? (int)(gridDim.x >> 1) : (int)gridDim.x;
   static_assert(!F8 || (EPI == EPI_SWIGLU && AS == AS_TMA), "fp8 operands: SwiGLU up projection");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -475,7 +537,7 @@ tc_grouped_gemm(const __grid_constant__ CUtensorMap mA, const __grid_constant__ 
       // gathering: the transaction arrive of the stage's warp, then its
       // second arrive once the warp's row copies have landed
       mbar_init(full_bar(s), GATHER ? 2 : 1);
-      mbar_init(empty_bar(s), 1);
+      mbar_init(empty_bar(s), CL);   // the MMA commit of every CTA that reads the stage
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(tfull_bar(b), 1);
@@ -504,6 +566,7 @@ tc_grouped_gemm(const __grid_constant__ CUtensorMap mA, const __grid_constant__ 
   }
   tc_fence_before();
   __syncthreads();
+  if constexpr (CL == 2) cluster_sync();   // both CTAs' barriers exist before any multicast
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
   // The tile schedule is copied to shared memory.  With early_b it was
@@ -532,17 +595,28 @@ tc_grouped_gemm(const __grid_constant__ CUtensorMap mA, const __grid_constant__ 
     sc.mtiles = s_mt;
     sc.kept = s_kept;
   };
+  auto decode = [&](int item) -> TileInfo {
+    if constexpr (CL == 2) return decode_pair(a, sc, item, BNH, cl_rank);
+    else return decode_tile(a, sc, item, BNH);
+  };
+  auto count_items = [&]() -> int {
+    if (a.static_mt > 0) return a.static_total;
+    if constexpr (CL == 2) return total_pairs(a, sc, BNH);
+    else return sc.tp[a.E + a.has_shared];
+  };
   if (a.early_b) copy_sched();
-  const int total = a.static_mt > 0 ? a.static_total : (a.early_b ? s_tp[a.E + a.has_shared] : 0);
+  const int total = a.static_mt > 0 ? a.static_total : (a.early_b ? count_items() : 0);
   uint32_t npre = 0;   // uses whose B tiles were issued before the wait
   if (AS == AS_TMA && a.early_b && warp == 0 && lane == 0) {
-    for (int tile = blockIdx.x; tile < total && npre < (uint32_t)C::STAGES; tile += gridDim.x) {
-      const TileInfo ti = decode_tile(a, sc, tile, BNH);
+    for (int tile = item0; tile < total && npre < (uint32_t)C::STAGES; tile += istep) {
+      const TileInfo ti = decode(tile);
       const int e = ti.shared ? 0 : ti.seg;
       const int nk = (ti.K + C::BK - 1) / C::BK;
       const int rows = ti.row_end - ti.a_row < kTcBM ? ti.row_end - ti.a_row : kTcBM;
-      const int a_boxes = a_real_boxes(rows, a.partial_rows);
-      const uint32_t a_bytes = a_stage_bytes(a_boxes, C::A_BYTES);
+      const int a_boxes = CL == 2 ? 0 : a_real_boxes(rows, a.partial_rows);
+      const uint32_t a_bytes =
+          CL == 2 ? (ti.m64 ? (uint32_t)C::A_BYTES / 2 : (uint32_t)C::A_BYTES)
+                  : a_stage_bytes(a_boxes, C::A_BYTES);
       for (int kb = 0; kb < nk && npre < (uint32_t)C::STAGES; ++kb, ++npre) {
         const uint32_t sb = smem_base + npre * C::STAGE_BYTES + C::A_BYTES;
         mbar_arrive_expect_tx(full_bar(npre), a_bytes + C::B_BYTES);
@@ -560,8 +634,7 @@ tc_grouped_gemm(const __grid_constant__ CUtensorMap mA, const __grid_constant__ 
        i += gridDim.x * blockDim.x)
     a.zero_ctr[i] = 0u;
   if (!a.early_b) copy_sched();
-  const int total_all =
-      a.static_mt > 0 ? a.static_total : sc.tp[a.E + a.has_shared];
+  const int total_all = count_items();
   (void)total;
 
   auto give_up = [&]() {
@@ -584,8 +657,8 @@ tc_grouped_gemm(const __grid_constant__ CUtensorMap mA, const __grid_constant__ 
       uint32_t g = 0;
       bool ok = true;
       const int sub = lane >> 3, chunk = lane & 7;
-      for (int tile = blockIdx.x; tile < total_all && ok; tile += gridDim.x) {
-        const TileInfo ti = decode_tile(a, sc, tile, BNH);
+      for (int tile = item0; tile < total_all && ok; tile += istep) {
+        const TileInfo ti = decode(tile);
         const int nk = (ti.K + C::BK - 1) / C::BK;
         // does this warp fill any stage of the tile?
         if (nk < Wr::PROD && (int)((uint32_t)(warp - (int)(g & 3u)) & 3u) >= nk) {
@@ -674,8 +747,8 @@ tc_grouped_gemm(const __grid_constant__ CUtensorMap mA, const __grid_constant__ 
       // and issues the B tiles (and the shared expert's A tiles) first.
       uint32_t g = 0;
       bool ok = true;
-      for (int tile = blockIdx.x; tile < total_all && ok; tile += gridDim.x) {
-        const TileInfo ti = decode_tile(a, sc, tile, BNH);
+      for (int tile = item0; tile < total_all && ok; tile += istep) {
+        const TileInfo ti = decode(tile);
         const CUtensorMap* pB0 = ti.shared ? &mB0_sh : &mB0;
         const CUtensorMap* pB1 = ti.shared ? &mB1_sh : &mB1;
         const int e = ti.shared ? 0 : ti.seg;
@@ -743,8 +816,8 @@ tc_grouped_gemm(const __grid_constant__ CUtensorMap mA, const __grid_constant__ 
       // ---------------- TMA producer ----------------
       uint32_t g = 0;
       bool ok = true;
-      for (int tile = blockIdx.x; tile < total_all && ok; tile += gridDim.x) {
-        const TileInfo ti = decode_tile(a, sc, tile, BNH);
+      for (int tile = item0; tile < total_all && ok; tile += istep) {
+        const TileInfo ti = decode(tile);
         const CUtensorMap* pA = ti.shared ? &mA_sh : &mA;
         const CUtensorMap* pA32 = ti.shared ? &mA32_sh : &mA32;
         const CUtensorMap* pB0 = ti.shared ? &mB0_sh : &mB0;
@@ -752,8 +825,10 @@ tc_grouped_gemm(const __grid_constant__ CUtensorMap mA, const __grid_constant__ 
         const int e = ti.shared ? 0 : ti.seg;
         const int nk = (ti.K + C::BK - 1) / C::BK;
         const int rows = ti.row_end - ti.a_row < kTcBM ? ti.row_end - ti.a_row : kTcBM;
-        const int a_boxes = a_real_boxes(rows, a.partial_rows);
-        const uint32_t a_bytes = a_stage_bytes(a_boxes, C::A_BYTES);
+        const int a_boxes = CL == 2 ? 0 : a_real_boxes(rows, a.partial_rows);
+        const uint32_t a_bytes =
+            CL == 2 ? (ti.m64 ? (uint32_t)C::A_BYTES / 2 : (uint32_t)C::A_BYTES)
+                    : a_stage_bytes(a_boxes, C::A_BYTES);
         for (int kb = 0; kb < nk; ++kb, ++g) {
           const int s = g % C::STAGES;
           const uint32_t ph = (g / C::STAGES) & 1u;
@@ -766,7 +841,15 @@ tc_grouped_gemm(const __grid_constant__ CUtensorMap mA, const __grid_constant__ 
           const uint32_t sa = smem_base + s * C::STAGE_BYTES;
           const uint32_t sb = sa + C::A_BYTES;
           if (!pre) mbar_arrive_expect_tx(full_bar(s), a_bytes + C::B_BYTES);
-          load_a_stage(sa, pA, pA32, full_bar(s), kb * C::BKX, ti.a_row, a_boxes);
+          if constexpr (CL == 2) {
+            // this CTA's half of the A rows (one 64-row box, the map's box in
+            // cluster mode) to both CTAs; an M = 64 tile needs the first half only
+            if (!(ti.m64 && cl_rank == 1))
+              tma_load_2d_mc(sa + cl_rank * (kTcBM / 2) * 128, pA, full_bar(s), kb * C::BKX,
+                             ti.a_row + cl_rank * (kTcBM / 2), 0x3);
+          } else {
+            load_a_stage(sa, pA, pA32, full_bar(s), kb * C::BKX, ti.a_row, a_boxes);
+          }
           if (!pre) {
             tma_load_3d(sb, pB0, full_bar(s), kb * C::BKX, ti.n0, e);
             if (DUAL) tma_load_3d(sb + BNH * 128, pB1, full_bar(s), kb * C::BKX, ti.n0, e);
@@ -793,8 +876,8 @@ tc_grouped_gemm(const __grid_constant__ CUtensorMap mA, const __grid_constant__ 
       uint32_t g = 0;
       int it = 0;
       bool ok = true;
-      for (int tile = blockIdx.x; tile < total_all && ok; tile += gridDim.x) {
-        const TileInfo ti = decode_tile(a, sc, tile, BNH);
+      for (int tile = item0; tile < total_all && ok; tile += istep) {
+        const TileInfo ti = decode(tile);
         const int nk = (ti.K + C::BK - 1) / C::BK;
         const int ck = EPI == EPI_F32_CHUNKED ? kChunkKB : nk;   // k-blocks per accumulator
         for (int kb0 = 0; kb0 < nk && ok; kb0 += ck, ++it) {
@@ -829,7 +912,10 @@ tc_grouped_gemm(const __grid_constant__ CUtensorMap mA, const __grid_constant__ 
               else
                 tc_mma_bf16(d_tmem, ad, bd, idesc, (kb != kb0 || kk != 0) ? 1u : 0u);
             }
-            tc_commit(empty_bar(s));
+            if constexpr (CL == 2)
+              tc_commit_mc(empty_bar(s), 0x3);   // both CTAs' copies of the stage are free
+            else
+              tc_commit(empty_bar(s));
           }
           if (!ok) break;
           tc_commit(tfull_bar(ab));
@@ -881,8 +967,8 @@ tc_grouped_gemm(const __grid_constant__ CUtensorMap mA, const __grid_constant__ 
     }
     int it = 0;
     bool ok = true;
-    for (int tile = blockIdx.x; tile < total_all && ok; tile += gridDim.x) {
-      const TileInfo ti = decode_tile(a, sc, tile, BNH);
+    for (int tile = item0; tile < total_all && ok; tile += istep) {
+      const TileInfo ti = decode(tile);
       // M = 64: rows 16q .. 16q+15 sit in the first 16 lanes of quarter q
       const int rit = !ti.m64 ? row_in_tile : (lane < 16 ? q * 16 + lane : kTcBM);
       const size_t orow = static_cast<size_t>(ti.a_row + rit);
@@ -964,6 +1050,9 @@ tc_grouped_gemm(const __grid_constant__ CUtensorMap mA, const __grid_constant__ 
     tc_fence_after();
     tmem_dealloc(tmem_base, C::TMEM_COLS);
   }
+  // no CTA leaves while its peer may still multicast into it or commit to
+  // its barriers
+  if constexpr (CL == 2) cluster_sync();
 }
 
 // ---------------------------------------------------------------- host side
@@ -971,21 +1060,45 @@ struct TcMaps {
   CUtensorMap A, A_sh, A32, A32_sh, B0, B1, B0_sh, B1_sh;
 };
 
-template <int BNH, bool DUAL, int EPI, int AS = AS_TMA, bool F8 = false>
+template <int BNH, bool DUAL, int EPI, int AS = AS_TMA, bool F8 = false, int CL = 1>
 static cudaError_t run_tc(const TcMaps& m, const TcArgs& a, int grid, cudaStream_t st) {
   using C = TcCfg<BNH, DUAL, EPI, F8>;
   static std::atomic<uint64_t> attr_done{0};
-  auto kern = tc_grouped_gemm<BNH, DUAL, EPI, AS, F8>;
+  auto kern = tc_grouped_gemm<BNH, DUAL, EPI, AS, F8, CL>;
   cudaError_t e = smem_attr_once(kern, C::SMEM, attr_done);
   if (e != cudaSuccess) return e;
-  return launch_pdl(kern, dim3(grid), dim3(TcWarps<AS, EPI>::THREADS), C::SMEM, st, m.A, m.A_sh,
-                    m.A32, m.A32_sh, m.B0,
-                    m.B1, m.B0_sh, m.B1_sh, a);
+  if constexpr (CL == 1) {
+    return launch_pdl(kern, dim3(grid), dim3(TcWarps<AS, EPI>::THREADS), C::SMEM, st, m.A,
+                      m.A_sh, m.A32, m.A32_sh, m.B0, m.B1, m.B0_sh, m.B1_sh, a);
+  } else {
+    // clusters of CL CTAs along x (the grid a multiple of CL), with
+    // programmatic dependent launch
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid < CL ? CL : (grid / CL) * CL);
+    cfg.blockDim = dim3(TcWarps<AS, EPI>::THREADS);
+    cfg.dynamicSmemBytes = C::SMEM;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = CL;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 2;
+    return cudaLaunchKernelEx(&cfg, kern, m.A, m.A_sh, m.A32, m.A32_sh, m.B0, m.B1, m.B0_sh,
+                              m.B1_sh, a);
+  }
 }
 
 template <int AS>
 static cudaError_t dispatch_up_t(int bn, int act, const TcMaps& m, const TcArgs& a, int grid,
-                                 cudaStream_t st) {
+                                 cudaStream_t st, bool cl2 = false) {
+  if constexpr (AS == AS_TMA) {
+    if (cl2 && act == MOE_ACT_SWIGLU && bn == 128)
+      return run_tc<128, true, EPI_SWIGLU, AS_TMA, false, 2>(m, a, grid, st);
+  }
   if (act == MOE_ACT_SWIGLU) {
     switch (bn) {
       case 128: return run_tc<128, true, EPI_SWIGLU, AS>(m, a, grid, st);
@@ -1024,14 +1137,23 @@ static cudaError_t dispatch_up_f8(int bn, const TcMaps& m, const TcArgs& a, int 
 }
 
 static cudaError_t dispatch_up(int as, int bn, int act, const TcMaps& m, const TcArgs& a,
-                               int grid, cudaStream_t st) {
+                               int grid, cudaStream_t st, bool cl2) {
   return as == AS_CP   ? dispatch_up_t<AS_CP>(bn, act, m, a, grid, st)
          : as == AS_G4 ? dispatch_up_t<AS_G4>(bn, act, m, a, grid, st)
-                       : dispatch_up_t<AS_TMA>(bn, act, m, a, grid, st);
+                       : dispatch_up_t<AS_TMA>(bn, act, m, a, grid, st, cl2);
 }
 
 static cudaError_t dispatch_down(int bn, bool combine1, bool combinek, const TcMaps& m,
-                                 const TcArgs& a, int grid, cudaStream_t st) {
+                                 const TcArgs& a, int grid, cudaStream_t st, bool cl2 = false) {
+  if (cl2 && !combinek) {
+    if (combine1) {
+      if (bn == 256) return run_tc<256, false, EPI_COMBINE1, AS_TMA, false, 2>(m, a, grid, st);
+      if (bn == 192) return run_tc<192, false, EPI_COMBINE1, AS_TMA, false, 2>(m, a, grid, st);
+    } else {
+      if (bn == 256) return run_tc<256, false, EPI_OUT16, AS_TMA, false, 2>(m, a, grid, st);
+      if (bn == 192) return run_tc<192, false, EPI_OUT16, AS_TMA, false, 2>(m, a, grid, st);
+    }
+  }
   if (combinek) {
     switch (bn) {
       case 256: return run_tc<256, false, EPI_COMBINEK>(m, a, grid, st);
@@ -1090,12 +1212,14 @@ cudaError_t launch_experts_tc(const Plan& p, const void* x, const void* W1, cons
   const uint64_t a_rows = from_x ? (uint64_t)c.T : (uint64_t)p.R_cap;
   TcMaps mu;
   // the row-gathering TMA reads boxes one row high
-  bool ok = encode_2d(&mu.A, a_src, a_rows, c.d, p.gather4 ? 1u : (uint32_t)kTcBM, el);
+  // (2-CTA clusters load A in halves of 64 rows, each CTA one half)
+  const uint32_t a_box = p.gather4 ? 1u : (p.cluster2_up ? (uint32_t)kTcBM / 2 : (uint32_t)kTcBM);
+  bool ok = encode_2d(&mu.A, a_src, a_rows, c.d, a_box, el);
   ok = ok && encode_2d(&mu.A32, a_src, a_rows, c.d, kABox, el);
   ok = ok && encode_3d(&mu.B0, W1, c.E, c.f, c.d, p.up_bn, el);
   ok = ok && encode_3d(&mu.B1, dual ? W3 : W1, c.E, c.f, c.d, p.up_bn, el);
   if (sh) {
-    ok = ok && encode_2d(&mu.A_sh, x, c.T, c.d, kTcBM);
+    ok = ok && encode_2d(&mu.A_sh, x, c.T, c.d, a_box);
     ok = ok && encode_2d(&mu.A32_sh, x, c.T, c.d, kABox);
     ok = ok && encode_3d(&mu.B0_sh, Ws1, 1, c.f_shared, c.d, p.up_bn);
     ok = ok && encode_3d(&mu.B1_sh, Ws3, 1, c.f_shared, c.d, p.up_bn);
@@ -1149,7 +1273,7 @@ cudaError_t launch_experts_tc(const Plan& p, const void* x, const void* W1, cons
   const int grid_up = p.max_tiles_up < p.num_sms ? p.max_tiles_up : p.num_sms;
   const int as = p.gather ? AS_CP : p.gather4 ? AS_G4 : AS_TMA;
   cudaError_t e = p.fp8 ? dispatch_up_f8(p.up_bn, mu, au, grid_up, st)
-                        : dispatch_up(as, p.up_bn, c.act, mu, au, grid_up, st);
+                        : dispatch_up(as, p.up_bn, c.act, mu, au, grid_up, st, p.cluster2_up);
   if (e != cudaSuccess) return e;
   if (mid_event) {
     e = cudaEventRecord(mid_event, st);
@@ -1158,12 +1282,12 @@ cudaError_t launch_experts_tc(const Plan& p, const void* x, const void* W1, cons
 
   // ---- down projection: o = h W2^T (fp32) ----
   TcMaps md;
-  ok = encode_2d(&md.A, h, p.R_cap, c.f, kTcBM);
+  ok = encode_2d(&md.A, h, p.R_cap, c.f, p.cluster2_dn ? kTcBM / 2 : kTcBM);
   ok = ok && encode_2d(&md.A32, h, p.R_cap, c.f, kABox);
   ok = ok && encode_3d(&md.B0, W2, c.E, c.d, c.f, p.dn_bn);
   md.B1 = md.B0;
   if (sh) {
-    ok = ok && encode_2d(&md.A_sh, hs, p.T_pad, c.f_shared, kTcBM);
+    ok = ok && encode_2d(&md.A_sh, hs, p.T_pad, c.f_shared, p.cluster2_dn ? kTcBM / 2 : kTcBM);
     ok = ok && encode_2d(&md.A32_sh, hs, p.T_pad, c.f_shared, kABox);
     ok = ok && encode_3d(&md.B0_sh, Ws2, 1, c.d, c.f_shared, p.dn_bn);
   } else {
@@ -1199,7 +1323,8 @@ cudaError_t launch_experts_tc(const Plan& p, const void* x, const void* W1, cons
   ad.out_sh = sh ? static_cast<void*>(w + p.ws.os) : nullptr;
   ad.ld_out_sh = sh ? c.d : 0;
   const int grid_dn = p.max_tiles_dn < p.num_sms ? p.max_tiles_dn : p.num_sms;
-  return dispatch_down(p.dn_bn, p.combine_in_down, p.combine_k, md, ad, grid_dn, st);
+  return dispatch_down(p.dn_bn, p.combine_in_down, p.combine_k, md, ad, grid_dn, st,
+                       p.cluster2_dn);
 }
 
 // ---------------------------------------------------------------- router

@@ -41,7 +41,7 @@ int make_plan(const moe_config* cfg, WsKind kind, Plan* p, int num_sms);
 
 // Process-wide overrides set through moe_set_tuning (tests and tile sweeps
 // only); -1 = no override.  Production calls never read the environment.
-static std::atomic<int> g_tune[MOE_TUNE_COUNT] = {-1, -1, -1, -1, -1, -1, -1};
+static std::atomic<int> g_tune[MOE_TUNE_COUNT] = {-1, -1, -1, -1, -1, -1, -1, -1};
 
 int tuning(int knob) {
   return knob >= 0 && knob < MOE_TUNE_COUNT ? g_tune[knob].load(std::memory_order_relaxed) : -1;
@@ -213,6 +213,7 @@ int make_plan(const moe_config* cfg, WsKind kind, Plan* p, int num_sms) {
     // segments) issue M = 64 MMAs: half the tensor work of an M = 128 tile
     const int m = tuning(MOE_TUNE_MMA_M64);
     P.m64 = m >= 0 ? m != 0 : true;
+
   }
   P.combine_in_down = P.tc && c.k == 1 && c.n_shared == 0;
   // Other tensor-core layers can combine in the down projection's epilogue
@@ -249,6 +250,22 @@ int make_plan(const moe_config* cfg, WsKind kind, Plan* p, int num_sms) {
       P.gather4 = gv == 2;
     }
     if (P.fp8) P.gather = P.gather4 = false;   // fp8: the quantised rows are read by TMA
+  }
+  // On request, the TMA-fed projections run as clusters of two CTAs on
+  // adjacent N tiles, each loading half of the shared A tile and multicasting
+  // it (the compiled cluster forms: SwiGLU up projections of 128-column tiles,
+  // down projections of 192 or 256 columns).  The A tile then crosses from L2
+  // once per pair and the power draw drops (SM clock under the cap 1237 ->
+  // 1297 MHz on the DeepSeek-V3-shaped layer), but the pair's stages are
+  // refilled only when both CTAs have consumed them, and that coupling costs
+  // more (DeepSeek-V3-shaped 5.14 -> 5.23 ms; Mixtral-shaped 4.70 -> 4.66),
+  // so single CTAs are the default.
+  {
+    const int cl = tuning(MOE_TUNE_CLUSTER);
+    const bool on = cl == 1;
+    P.cluster2_up = on && P.tc && !P.fp8 && !P.gather && !P.gather4 &&
+                    c.act == MOE_ACT_SWIGLU && P.up_bn == 128;
+    P.cluster2_dn = on && P.tc && !P.combine_k && (P.dn_bn == 256 || P.dn_bn == 192);
   }
   P.nt_up = ceil_div(c.f, P.up_bn);
   P.nt_dn = ceil_div(c.d, P.dn_bn);
@@ -847,7 +864,8 @@ int moe_set_tuning(int32_t knob, int32_t value) {
   if (knob < 0 || knob >= MOE_TUNE_COUNT || value < -1) return MOE_ERR_ARG;
   if (knob == MOE_TUNE_ROUTER && value > MOE_ROUTER_TC) return MOE_ERR_ARG;
   if (knob == MOE_TUNE_GATHER && value > 2) return MOE_ERR_ARG;
-  if ((knob == MOE_TUNE_MMA_M64 || knob == MOE_TUNE_FUSED_COMBINE) && value > 1)
+  if ((knob == MOE_TUNE_MMA_M64 || knob == MOE_TUNE_FUSED_COMBINE ||
+       knob == MOE_TUNE_CLUSTER) && value > 1)
     return MOE_ERR_ARG;
   g_tune[knob].store(value, std::memory_order_relaxed);
   return MOE_OK;

@@ -94,6 +94,8 @@ struct Plan {
   bool gather;                // the up projection gathers token rows with cp.async
   bool gather4;               // the up projection gathers token rows with TMA (tile::gather4)
   bool m64;                   // routed GEMM tiles of <= 64 rows multiply with M = 64
+  bool cluster2_up;           // the up projection runs as 2-CTA clusters sharing the A tile
+  bool cluster2_dn;           // the same for the down projection
   bool fp8;                   // gate/up weights in e4m3: quantised rows, fp8 up projection
   int num_sms;
   WsLayout ws;

@@ -473,3 +473,22 @@ def test_one_launch_router_largest_batch():
     sample = np.sort(np.random.default_rng(19).choice(shape.T, 256, replace=False))
     rep = check_layer(inp, out, sample=sample)
     assert rep["dropped"] > 0
+
+
+CLUSTER_SHAPES = [SMALL[0], SMALL[2], ONE_LAUNCH[2], DECODE[1], LIMITS[4],
+                  LayerShape("cluster_odd_ntiles", 67, T=600, d=256, E=6, k=2, f=640, act=SW,
+                             gate=TOPK, dtype="bf16", n_shared=1, f_shared=384)]
+
+
+@pytest.mark.parametrize("shape", CLUSTER_SHAPES, ids=lambda s: s.name)
+def test_two_cta_cluster_projections(shape):
+    """The projections as clusters of two CTAs sharing a multicast A tile
+    (odd column-tile counts leave a phantom tile that stores nothing; M = 64
+    tails load one half): the same parity as single CTAs, and the same y."""
+    inp = W.make_inputs(shape, "cuda", seed=23)
+    with L.tuning(tile_n_up=128, tile_n_down=256):     # the compiled cluster forms
+        _, single = run_gpu(inp)
+        with L.tuning(cluster=1):
+            _, pair = run_gpu(inp)
+    check_layer(inp, pair)
+    assert torch.equal(pair.y, single.y)
