@@ -21,7 +21,7 @@ LIB = os.path.join(PKG, "libmoe.so")
 BUILD_CHECK = os.path.join(PKG, "_build_check")
 LIB_CHECK = os.path.join(PKG, "libmoe_check.so")
 INCLUDE = os.path.join(os.path.dirname(PKG), "include")
-SOURCES = ["router.cu", "route.cu", "route_tc.cu", "gemm_tc.cu", "gemm_simt.cu", "combine.cu", "balance.cu", "quant.cu", "moe_api.cu"]
+SOURCES = ["router.cu", "route.cu", "route_tc.cu", "route_wide.cu", "gemm_tc.cu", "gemm_simt.cu", "combine.cu", "balance.cu", "quant.cu", "moe_api.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC,-O3",
               "--expt-relaxed-constexpr", "-I", INCLUDE]

@@ -130,4 +130,86 @@ __device__ __forceinline__ bool bulk_fanout_rows(int n, int fan, uint32_t row_by
   return ok;
 }
 
+// The same fan-out copy over rows handed out while the copy runs: claim()
+// (called by the issuing thread only) returns the first of up to `batch`
+// rows [r, r + batch) the block may copy next, or a negative value when none
+// are left; `n` bounds the row indices.  Blocks that finish early take more
+// rows, so that the copy ends at about the same time on every block.
+template <typename ClaimF, typename SrcF, typename DstF>
+__device__ __forceinline__ bool bulk_fanout_claimed(ClaimF claim, int batch, int n, int fan,
+                                                    uint32_t row_bytes, SrcF src_of, DstF dst_of,
+                                                    uint8_t* stage, uint32_t stage_bytes,
+                                                    uint64_t* bars, uint32_t* status,
+                                                    uint32_t timeout_bit, uint64_t timeout_ns) {
+  const uint32_t fit = stage_bytes / row_bytes;
+  const int nslot = (int)(fit < (uint32_t)kFanMaxSlots ? fit : (uint32_t)kFanMaxSlots);
+  if (threadIdx.x == 0) {
+    for (int w = 0; w < nslot; ++w) mbar_init(smem_u32(bars + w), 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
+  if (threadIdx.x != 0) return true;
+  const uint32_t base = smem_u32(stage);
+  const int ahead = nslot - kFanPend;      // >= 1: the caller gives at least 3 slots
+  int slot_row[kFanMaxSlots];
+  uint32_t phases = 0;
+  int cur = 0, end = 0;                    // rows claimed and not yet loaded
+  bool more = true;
+  auto next_row = [&]() -> int {
+    if (cur == end && more) {
+      const int r = claim();
+      if (r < 0 || r >= n) {
+        more = false;
+      } else {
+        cur = r;
+        end = r + batch < n ? r + batch : n;
+      }
+    }
+    return cur < end ? cur++ : -1;
+  };
+  int issued = 0;
+  auto load = [&](int row) {
+    const int s = issued % nslot;
+    slot_row[s] = row;
+    mbar_arrive_expect_tx(smem_u32(bars + s), row_bytes);
+    bulk_load(base + (uint32_t)s * row_bytes, src_of(row), row_bytes, smem_u32(bars + s));
+    ++issued;
+  };
+  while (issued < ahead) {
+    const int r = next_row();
+    if (r < 0) break;
+    load(r);
+  }
+  bool ok = true;
+  int done = 0;
+  for (; done < issued; ++done) {
+    const int s = done % nslot;
+    if (!mbar_wait_bounded(smem_u32(bars + s), (phases >> s) & 1u, timeout_ns, nullptr)) {
+      atomicOr(status, timeout_bit);
+      ok = false;
+      break;
+    }
+    phases ^= 1u << s;
+    for (int j = 0; j < fan; ++j) {
+      void* d = dst_of(slot_row[s], j);
+      if (d != nullptr) bulk_store(d, base + (uint32_t)s * row_bytes, row_bytes);
+    }
+    bulk_commit();
+    bulk_wait_read<kFanPend>();            // rows <= done - kFanPend: slots free again
+    const int r = next_row();
+    if (r >= 0) load(r);
+  }
+  if (!ok) {
+    // loads issued ahead may still be landing in the stage
+    for (int r = done; r < issued; ++r) {
+      const int s = r % nslot;
+      mbar_wait_bounded(smem_u32(bars + s), (phases >> s) & 1u, timeout_ns, nullptr);
+      phases ^= 1u << s;
+    }
+  }
+  bulk_commit();
+  bulk_wait_all();
+  return ok;
+}
+
 }  // namespace moe

@@ -1219,7 +1219,10 @@ cudaError_t launch_experts_tc(const Plan& p, const void* x, const void* W1, cons
   ok = ok && encode_3d(&mu.B0, W1, c.E, c.f, c.d, p.up_bn, el);
   ok = ok && encode_3d(&mu.B1, dual ? W3 : W1, c.E, c.f, c.d, p.up_bn, el);
   if (sh) {
-    ok = ok && encode_2d(&mu.A_sh, x, c.T, c.d, a_box);
+    // the shared expert's rows are x itself, loaded as 128-row boxes (64-row
+    // halves in cluster mode) whatever the routed rows' source
+    const uint32_t a_box_sh = p.cluster2_up ? (uint32_t)kTcBM / 2 : (uint32_t)kTcBM;
+    ok = ok && encode_2d(&mu.A_sh, x, c.T, c.d, a_box_sh);
     ok = ok && encode_2d(&mu.A32_sh, x, c.T, c.d, kABox);
     ok = ok && encode_3d(&mu.B0_sh, Ws1, 1, c.f_shared, c.d, p.up_bn);
     ok = ok && encode_3d(&mu.B1_sh, Ws3, 1, c.f_shared, c.d, p.up_bn);

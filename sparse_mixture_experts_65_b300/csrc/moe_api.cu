@@ -114,12 +114,17 @@ int make_plan(const moe_config* cfg, WsKind kind, Plan* p, int num_sms) {
     // positions in one small launch
     P.route_small = !forced && c.T >= 1 && c.T <= kSmallT && c.E <= kSmallMaxE;
     P.route_tc = route_tc_eligible(c) && !forced && !P.route_small;
-    if (P.route_tc || P.route_small) P.router_fused = false;
+    // 64 < E <= 256: the one-launch cluster router (route_wide.cu)
+    P.route_wide = route_wide_eligible(c) && !forced && !P.route_small && !P.route_tc;
+    if (P.route_tc || P.route_small || P.route_wide) P.router_fused = false;
   }
   if (P.route_small) {
     P.BT = c.T;
   } else if (P.route_tc) {
     P.BT = kTcBM;
+  } else if (P.route_wide) {
+    P.rw_ks = route_wide_ks(c);
+    P.BT = kTcBM / P.rw_ks;
   } else if (P.router_fused) {
     P.BT = 16 * P.fu_tm;
   } else {
@@ -129,7 +134,8 @@ int make_plan(const moe_config* cfg, WsKind kind, Plan* p, int num_sms) {
     const int bt = kRouteTokensPerPass * (passes < 1 ? 1 : passes);
     P.BT = bt > kRouteMaxBT ? kRouteMaxBT : bt;
   }
-  P.nblk = ceil_div(c.T, P.BT);
+  P.nblk = P.route_wide ? ceil_div(c.T, kTcBM) * P.rw_ks : ceil_div(c.T, P.BT);
+  P.blk_stride = (c.E + 3) / 4 * 4;
   P.num_sms = num_sms > 0 ? num_sms : 148;
   // router GEMM: 128-token x (16*TN)-expert tiles, K split until >= 2 blocks per SM
   P.sc_tn = c.E > 32 ? 4 : 2;
@@ -242,7 +248,8 @@ int make_plan(const moe_config* cfg, WsKind kind, Plan* p, int num_sms) {
   // copy, 1 cp.async, 2 the TMA row gather.
   {
     const long long per_expert = Tk / (c.E > 0 ? c.E : 1);
-    P.gather = P.tc && P.route_tc && per_expert <= kTcBM;
+    P.gather = P.tc && ((P.route_tc && per_expert <= kTcBM) ||
+                        (P.route_wide && per_expert <= kWideGatherRows));
     P.gather4 = false;
     const int gv = tuning(MOE_TUNE_GATHER);
     if (gv >= 0 && P.tc) {
@@ -294,8 +301,8 @@ int make_plan(const moe_config* cfg, WsKind kind, Plan* p, int num_sms) {
     if (small > parts) parts = small;
   }
   L.score_parts = take(parts);
-  L.blk_cnt = take(sizeof(int) * (size_t)P.nblk * E);
-  L.blk_prob = take(sizeof(float) * (size_t)P.nblk * E);
+  L.blk_cnt = take(sizeof(int) * (size_t)P.nblk * P.blk_stride);
+  L.blk_prob = take(sizeof(float) * (size_t)P.nblk * P.blk_stride);
   L.meta = take(sizeof(int) * (E + (E + 1) * 3 + (E + 2) * 2));
   L.key_row = take(sizeof(int) * (size_t)Tk);
   L.row_token = take(sizeof(int) * (size_t)P.R_cap);
@@ -462,6 +469,12 @@ static int forward_impl(const moe_config* cfg, const Tensors& t, void* ws, size_
     if ((rc = record(events, MOE_STAGE_TOPK, st)) != MOE_OK) return rc;
     if ((rc = record(events, MOE_STAGE_PERMUTE, st)) != MOE_OK) return rc;
     if (copy) MOE_TRY_CUDA(launch_gather_rows(p, t.x, ws, st));
+  } else if (p.route_wide) {
+    // stages 1-4 and the row copy in one launch; top-k and permute are empty
+    MOE_TRY_CUDA(launch_route_wide(p, t.x, t.W_r, t.logit_offset, t.sel_bias, t.topk_idx,
+                                   t.topk_w, t.slot_pos, copy, ws, so, st));
+    if ((rc = record(events, MOE_STAGE_TOPK, st)) != MOE_OK) return rc;
+    if ((rc = record(events, MOE_STAGE_PERMUTE, st)) != MOE_OK) return rc;
   } else {
     cudaEvent_t topk_ev = events ? static_cast<cudaEvent_t>(events[MOE_STAGE_TOPK]) : nullptr;
     MOE_TRY_CUDA(launch_router(p, t.x, t.W_r, t.logit_offset, t.sel_bias, t.topk_idx, t.topk_w,
@@ -843,6 +856,7 @@ int moe_launch_count(const moe_config* cfg, int32_t* launches) {
   const bool copy = !p.gather && !p.gather4;   // the tensor-core router's row copy
   const int routing = p.route_small ? 1
                       : p.route_tc  ? (copy ? 2 : 1)
+                      : p.route_wide ? (copy && !route_wide_copies_rows(p) ? 2 : 1)
                                     : (p.router_fused ? 2 : 3);
   *launches = cfg->T == 0 ? 0 : routing + 2 + (p.combine_in_down || p.combine_k ? 0 : 1);
   return MOE_OK;
@@ -855,7 +869,7 @@ int moe_launch_count_fp8(const moe_config* cfg, int32_t* launches) {
   if (rc != MOE_OK) return rc;
   // routing without a row copy, the row quantisation, the two projections
   // and the combine (folded into the down projection for top-1 layers)
-  const int routing = p.route_small || p.route_tc ? 1 : (p.router_fused ? 2 : 3);
+  const int routing = p.route_small || p.route_tc || p.route_wide ? 1 : (p.router_fused ? 2 : 3);
   *launches = cfg->T == 0 ? 0 : routing + 1 + 2 + (p.combine_in_down || p.combine_k ? 0 : 1);
   return MOE_OK;
 }

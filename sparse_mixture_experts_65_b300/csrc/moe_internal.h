@@ -23,15 +23,33 @@ constexpr int kTcBM = 128;           // rows per tensor-core tile
 constexpr int kSimtBM = 64;          // rows per SIMT tile (fp32 path)
 constexpr int kSimtBN = 64;
 // Workspace header (zeroed once by the caller): status word at 0, routing
-// block-completion counter at 16, the one-launch router's grid-wait
-// counters (arrivals, passes) at 32 and 48, router split-reduction tile
+// block-completion counter at 16, the one-launch routers' grid-wait
+// counters (arrivals, passes) at 32 and 48 (and 96 and 112, with the row
+// copy's counters at 64 and 80), router split-reduction tile
 // counters from kTileCounterOffset on.  Every counter is back at zero when a
 // call has finished without a timeout.
 constexpr int kWsHeaderBytes = 4096;
 constexpr int kRouteDoneOffset = 16;
 constexpr int kRouteArriveOffset = 32;
 constexpr int kRoutePassedOffset = 48;
+// The one-launch router for E <= 256: its row-copy work counter and finished
+// count, and the counters of its second grid-wide wait.
+constexpr int kRouteCopyNextOffset = 64;
+constexpr int kRouteCopyDoneOffset = 80;
+constexpr int kRouteArrive2Offset = 96;
+constexpr int kRoutePassed2Offset = 112;
 constexpr int kRouteTcMaxOwn = 16;        // 128-token tiles per CTA of the one-launch router
+// One-launch router for 64 < E <= 256 (route_wide.cu): top-k of at most
+// kRouteWideMaxK, at most kRouteWideMaxOwn tiles per cluster, a grid of at
+// most kRouteWideMaxCtas CTAs, and clusters sized for one wave of
+// kRouteWideSlots SMs.
+constexpr int kRouteWideMaxK = 8;
+constexpr int kRouteWideMaxOwn = 16;
+constexpr int kRouteWideMaxCtas = 160;
+constexpr int kRouteWideSlots = 148;
+// Layers routed by it whose experts average at most this many rows gather
+// their rows in the up projection instead of copying them.
+constexpr int kWideGatherRows = 32;
 constexpr int kSmallT = 16;               // batches up to this size route in one small launch
 constexpr int kSmallMaxE = 256;
 constexpr int kTileCounterOffset = 256;
@@ -42,8 +60,8 @@ struct WsLayout {
   size_t status;      // uint32 status word (+ padding)
   size_t scores;      // float  [T][E]     router logits
   size_t score_parts; // float  [S][T][E]  split partial router logits (S > 1)
-  size_t blk_cnt;     // int32  [nblk][E]  per-block expert histogram, then its exclusive scan
-  size_t blk_prob;    // float  [nblk][E]  per-block sums of the router distribution
+  size_t blk_cnt;     // int32  [nblk][Es] per-block expert histogram (Es = E rounded up to 4)
+  size_t blk_prob;    // float  [nblk][Es] per-block sums of the router distribution
   size_t meta;        // int32  kept[E] | offsets[E+1] | seg_start[E+1] | mtiles[E+1]
                       //        | tp_up[E+2] | tp_dn[E+2]
   size_t key_row;     // int32  [T*k]      padded row of each assignment, -1 if dropped
@@ -72,6 +90,9 @@ struct Plan {
   bool router_tc;     // router logits on the tensor cores
   bool route_tc;      // stages 1-4 in one tensor-core launch (bf16, E <= 64, k <= 8)
   bool route_small;   // stages 1-4 in one launch for decode batches (T <= kSmallT)
+  bool route_wide;    // stages 1-4 and the row copy in one launch (bf16, 64 < E <= 256, k <= 8)
+  int rw_ks;          // that router's CTAs per 128-token tile
+  int blk_stride;     // row stride of blk_cnt / blk_prob (E rounded up to 4)
   bool router_fused;  // one kernel: logits, top-k, histogram, scan (E <= 256)
   int fu_tm, fu_tn;   // fused router: tokens per thread (1, 2), experts per thread
   int sc_tn;          // router GEMM: experts per thread (2 or 4)
@@ -139,6 +160,16 @@ cudaError_t launch_route_tc(const Plan& p, const void* x, const void* W_r,
                             float* topk_w, int32_t* slot_pos, void* ws, const ScanOutputs& so,
                             cudaStream_t st);
 cudaError_t launch_gather_rows(const Plan& p, const void* x, void* ws, cudaStream_t st);
+bool route_wide_eligible(const moe_config& c);
+int route_wide_ks(const moe_config& c);
+bool route_wide_copies_rows(const Plan& p);
+// Stages 1-4 and, when `copy`, the expert-ordered row copies (in the same
+// launch when a row fits the kernel's staging three times, else by the row
+// copy kernel after it).
+cudaError_t launch_route_wide(const Plan& p, const void* x, const void* W_r,
+                              const float* logit_offset, const float* sel_bias,
+                              int32_t* topk_idx, float* topk_w, int32_t* slot_pos, bool copy,
+                              void* ws, const ScanOutputs& so, cudaStream_t st);
 size_t route_small_smem(int E);
 int route_small_splits(int d);
 cudaError_t launch_route_small(const Plan& p, const void* x, const void* W_r,

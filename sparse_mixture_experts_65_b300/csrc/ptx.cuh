@@ -125,6 +125,60 @@ __device__ __forceinline__ uint32_t cluster_ctarank() {
   return r;
 }
 
+// Address of the shared-memory location `addr` (of this CTA) in CTA `rank`
+// of the cluster.
+__device__ __forceinline__ uint32_t mapa_shared(uint32_t addr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
+  return r;
+}
+
+// 16-byte load from the shared memory of any CTA of the cluster (an address
+// from mapa_shared).
+__device__ __forceinline__ float4 ld_dsmem_f4(uint32_t addr) {
+  float4 v;
+  asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "r"(addr));
+  return v;
+}
+
+// One arrival, with release semantics at cluster scope, on an mbarrier of any
+// CTA of the cluster (an address from mapa_shared).
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t bar_cluster) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];"
+               ::"r"(bar_cluster) : "memory");
+}
+
+// Wait (bounded, like mbar_wait_bounded) for a phase of a barrier of this CTA
+// whose arrivals come from other CTAs of the cluster, with acquire semantics
+// at cluster scope: what the arriving threads wrote before their release is
+// visible afterwards.
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+__device__ __forceinline__ bool mbar_wait_cluster_bounded(uint32_t bar, uint32_t parity,
+                                                          uint64_t limit_ns,
+                                                          const volatile int* abort_flag) {
+  if (mbar_try_wait_cluster(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (uint32_t i = 1;; ++i) {
+    if (mbar_try_wait_cluster(bar, parity)) return true;
+    if ((i & 63u) == 0) {
+      if (abort_flag != nullptr && *abort_flag) return false;
+      if (globaltimer_ns() - t0 > limit_ns) return false;
+    }
+  }
+}
+
 // Row gather (tile::gather4): one column slice (the map's box width) of four
 // arbitrary rows r0..r3 of a 2-D map whose box is one row high, written to
 // shared memory as rows 0..3 of a box at `dst` (swizzled like a tiled load).

@@ -47,14 +47,21 @@ class LazyExperts:
 
 
 def run_gpu(inp, cfg=None, workspace=None):
+    """One layer call; the device status (bounded waits, bounds checks) must
+    come back clean."""
     cfg = cfg if cfg is not None else L.config_for(inp.shape)
-    if inp.W1q is not None:
+    fp8 = inp.W1q is not None
+    ws = workspace if workspace is not None else L.alloc_workspace(
+        cfg, inp.x.device, "fp8" if fp8 else "forward")
+    if fp8:
         out = L.forward_fp8(cfg, inp.x, inp.W_r, inp.W1q, inp.W1s, inp.W3q, inp.W3s, inp.W2,
-                            inp.logit_offset, inp.sel_bias, workspace=workspace)
+                            inp.logit_offset, inp.sel_bias, workspace=ws)
     else:
         out = L.forward(cfg, inp.x, inp.W_r, inp.W1, inp.W2, inp.W3, inp.logit_offset,
-                        inp.sel_bias, inp.Ws1, inp.Ws3, inp.Ws2, workspace=workspace)
+                        inp.sel_bias, inp.Ws1, inp.Ws3, inp.Ws2, workspace=ws)
     torch.cuda.synchronize()
+    status = L.check_status(ws)
+    assert status == 0, f"device status {status} ({inp.shape.name})"
     return cfg, out
 
 

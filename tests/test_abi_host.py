@@ -112,17 +112,19 @@ def test_workspace_sizes(name):
     elem = 4 if s.dtype == "f32" else 2
     # the expert-ordered buffers alone: at least T*k rows of h and o, both in
     # the layer dtype (and of x unless the up projection gathers rows: the
-    # Switch layer)
-    x_rows = 0 if name == "switch" else s.d * elem
+    # Switch layer, and the gpt-oss-shaped batch of 8 rows per expert)
+    x_rows = 0 if name in ("switch", "gptoss") else s.d * elem
     assert fw >= s.T * s.k * (x_rows + s.f * elem + s.d * elem)
     # routing: one tensor-core launch for bf16 layers with E <= 64 and k <= 8
     # (plus a row copy unless the up projection gathers rows: Mixtral copies),
-    # else three (logits, top-k, permute); two projections; the combine unless
-    # a top-1 bf16 layer without a shared expert folds it into the down
+    # one launch with the row copy inside for bf16 layers with 64 < E <= 256
+    # and k <= 8 (DeepSeek-V3- and gpt-oss-shaped), else three (logits, top-k,
+    # permute: the float32 toy layer); two projections; the combine unless a
+    # top-1 bf16 layer without a shared expert folds it into the down
     # projection (the other bf16 layers do so only on request)
-    expected = {"toy": 6, "switch": 3, "mixtral": 5, "dsv3": 6, "gptoss": 6}
+    expected = {"toy": 6, "switch": 3, "mixtral": 5, "dsv3": 4, "gptoss": 4}
     with L.tuning(fused_combine=1):
-        fused = {"toy": 6, "switch": 3, "mixtral": 4, "dsv3": 5, "gptoss": 5}
+        fused = {"toy": 6, "switch": 3, "mixtral": 4, "dsv3": 3, "gptoss": 3}
         assert L.launch_count(cfg) == fused[name]
     assert L.launch_count(cfg) == expected[name]
 
@@ -238,7 +240,12 @@ def test_fp8_entry_point_checks_without_gpu():
     assert call(ok, W1s=odd) == N.MOE_ERR_ARG
     assert call(ok) == N.MOE_ERR_WORKSPACE          # everything else valid, no workspace
     # decode batch: router, row quantisation, the two projections, combine;
-    # the split router of larger batches: logits, top-k, permute
+    # larger batches route in one launch as well (64 < E <= 256), the bf16
+    # layer with its row copy inside it
     assert L.launch_count(L.config_for(W.get("gptoss16_fp8")), fp8=True) == 5
-    assert L.launch_count(L.config_for(W.get("gptoss256")), fp8=False) == 6
-    assert L.launch_count(L.config_for(W.get("gptoss256_fp8")), fp8=True) == 7
+    assert L.launch_count(L.config_for(W.get("gptoss256")), fp8=False) == 4
+    assert L.launch_count(L.config_for(W.get("gptoss256_fp8")), fp8=True) == 5
+    # forcing the split router (tensor-core logits, top-k, permute)
+    with L.tuning(router="tc"):
+        assert L.launch_count(L.config_for(W.get("gptoss256")), fp8=False) == 6
+        assert L.launch_count(L.config_for(W.get("gptoss256_fp8")), fp8=True) == 7

@@ -93,7 +93,7 @@ def test_switch_layer_full():
 def test_mixtral_layer_sampled():
     inp = W.make_inputs(W.MIXTRAL, "cuda")
     _, out = run_gpu(inp)
-    sample = np.sort(np.random.default_rng(7).choice(W.MIXTRAL.T, 192, replace=False))
+    sample = np.sort(np.random.default_rng(7).choice(W.MIXTRAL.T, 1024, replace=False))
     rep = check_layer(inp, out, sample=sample)
     print("mixtral", rep)
     del inp, out
@@ -103,7 +103,7 @@ def test_mixtral_layer_sampled():
 def test_dsv3_layer_sampled():
     inp = W.make_inputs(W.DSV3, "cuda")
     _, out = run_gpu(inp)
-    sample = np.sort(np.random.default_rng(8).choice(W.DSV3.T, 48, replace=False))
+    sample = np.sort(np.random.default_rng(8).choice(W.DSV3.T, 512, replace=False))
     rep = check_layer(inp, out, sample=sample)
     print("dsv3", rep)
     del inp, out
@@ -492,3 +492,91 @@ def test_two_cta_cluster_projections(shape):
             _, pair = run_gpu(inp)
     check_layer(inp, pair)
     assert torch.equal(pair.y, single.y)
+
+
+# ---------------------------------------------------------------- one-launch router, 64 < E <= 256
+# Clusters of KS CTAs per 128-token tile, each CTA on a share of the model
+# width; KS = 8, 4, 2, 1 by tile count and width (tiles x KS within one wave
+# of 148 SMs, at least one 128-wide chunk per CTA).
+ROUTE_WIDE = [
+    # KS = 4 (6 tiles, 4 chunks), sigmoid gates with a selection bias, drops,
+    # the shared expert
+    LayerShape("wide_e256_k8_sig_cap", 70, T=700, d=512, E=256, k=8, f=64, act=SW, gate=SIG,
+               dtype="bf16", capacity_factor=1.0, sel_bias_halfwidth=0.05, n_shared=1,
+               f_shared=64),
+    # KS = 1 (one chunk), E = 130: 256-wide expert tile with a ragged tail and
+    # a histogram row stride of 132; full-softmax gates, skewed offsets
+    LayerShape("wide_e130_ks1_full", 71, T=1000, d=96, E=130, k=3, f=64, act=GE, gate=FULL,
+               dtype="bf16", capacity_factor=1.0, logit_offset_var=1.5),
+    # KS = 8 (3 tiles, 8 chunks), E = 100 (128-wide expert tile), a ragged
+    # last k-block (d = 1000), top-k softmax gates
+    LayerShape("wide_e100_ks8_ragged_d", 72, T=333, d=1000, E=100, k=2, f=64, act=SW,
+               gate=TOPK, dtype="bf16"),
+    # KS = 8 with 18 tiles: more tiles than clusters of 8 that fit at once,
+    # so some clusters take two tiles (both partial-logit slots)
+    LayerShape("wide_e160_ks8_two_tiles", 73, T=2200, d=2048, E=160, k=4, f=64, act=RE,
+               gate=TOPK, dtype="bf16", capacity_factor=1.25),
+    # KS = 1 with 313 tiles on at most 148 clusters: several tiles per CTA,
+    # Switch-like skew and drops, k = 1
+    LayerShape("wide_e72_persistent", 74, T=40000, d=64, E=72, k=1, f=64, act=RE, gate=FULL,
+               dtype="bf16", capacity_factor=1.25, logit_offset_var=1.5),
+    # KS = 2 (71 tiles, 2 chunks)
+    LayerShape("wide_e192_ks2", 75, T=9000, d=256, E=192, k=6, f=64, act=SW, gate=SIG,
+               dtype="bf16", sel_bias_halfwidth=0.05),
+]
+
+
+@pytest.mark.parametrize("shape", ROUTE_WIDE, ids=lambda s: s.name)
+def test_wide_router_layers(shape):
+    """Layers routed by the one-launch cluster router: routing over the whole
+    batch (indices, gates, counts, positions, f, P, L) and y against the
+    oracle (sampled for the largest batch)."""
+    inp = W.make_inputs(shape, "cuda", seed=24)
+    cfg = L.config_for(shape)
+    assert L.launch_count(cfg) == 4 - (shape.k == 1)       # router, up, down (+ combine)
+    _, out = run_gpu(inp)
+    sample = None
+    if shape.T > 5000:
+        sample = np.sort(np.random.default_rng(25).choice(shape.T, 384, replace=False))
+    rep = check_layer(inp, out, sample=sample)
+    print(shape.name, rep)
+    if shape.capacity_factor > 0 and shape.k == 1:
+        assert rep["dropped"] > 0
+    del inp, out
+    _free()
+
+
+def test_wide_router_repeat_and_route_entry_point():
+    """Bitwise repeatable (same workspace, twice), and moe_route gives the
+    forward pass's routing outputs bit for bit."""
+    shape = ROUTE_WIDE[0]
+    inp = W.make_inputs(shape, "cuda", seed=26)
+    cfg = L.config_for(shape)
+    ws = L.alloc_workspace(cfg)
+    _, a = run_gpu(inp, cfg, ws)
+    _, b = run_gpu(inp, cfg, ws)
+    for name in ("y", "topk_idx", "topk_w", "expert_counts", "aux_loss", "slot_pos", "P"):
+        assert torch.equal(getattr(a, name), getattr(b, name)), name
+    assert L.check_status(ws) == 0
+    rt = L.route(cfg, inp.x, inp.W_r, inp.logit_offset, inp.sel_bias)
+    torch.cuda.synchronize()
+    for name in ("topk_idx", "topk_w", "expert_counts", "aux_loss", "routed_counts", "offsets",
+                 "slot_pos", "f", "P"):
+        assert torch.equal(getattr(rt, name), getattr(a, name)), name
+
+
+def test_wide_router_agrees_with_split_router():
+    """The one-launch router and the split tensor-core router (logits GEMM,
+    top-k kernel, permute) add the same 128-wide float32 chunks in different
+    groupings: the same choices away from near-ties, gates within float32
+    rounding, and the same y within the layer tolerance."""
+    shape = ROUTE_WIDE[1]
+    inp = W.make_inputs(shape, "cuda", seed=27)
+    _, wide = run_gpu(inp)
+    with L.tuning(router="tc"):
+        _, split = run_gpu(inp)
+    same = (wide.topk_idx == split.topk_idx).all(dim=1)
+    assert same.float().mean().item() > 0.99
+    g = (wide.topk_w - split.topk_w)[same].abs().max().item()
+    assert g < 1e-5, g
+    check_layer(inp, split)
