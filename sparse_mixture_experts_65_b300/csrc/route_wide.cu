@@ -29,7 +29,8 @@
 // order plus the logit offset, selection, top-k, gates, the router
 // distribution, and the rank of every key among the earlier keys of the
 // block with the same expert; the block's histogram and probability sums are
-// published.  A grid-wide wait (bounded; every CTA is resident) follows,
+// published.  A grid-wide wait (bounded; the grid is sized to the clusters
+// the GPU holds at once, so every CTA is resident) follows,
 // after which every CTA derives the routed totals, the exclusive prefix of
 // its own blocks and the expert segments (CTA 0 also writes the meta data
 // and the balance statistics), turns its keys' ranks into positions and
@@ -80,12 +81,12 @@ struct RwCfg {
   static_assert(kTcBM * PITCH * 4 <= STAGE_AREA, "partial logits fit the stage area");
   static constexpr int BAR_BYTES = al16(8 * NBARS);
   static constexpr int FAN_BAR_BYTES = 8 * kFanMaxSlots;
-  static constexpr int KEYS_BYTES = 4 * kTcBM * kRouteWideMaxK;
+  static constexpr int KEYS_BYTES = 4 * kTcBM * kRouteWideMaxK;   // keys of a block, then ranks
   static constexpr int PW_BYTES = 4 * kRwEpiWarps * EPN;
   static constexpr int CNT_BYTES = 4 * EPN;
   static constexpr int VEC_BYTES = 4 * 2 * EPN;             // selection bias and logit offset
   static constexpr int MISC_BYTES = 64;
-  static constexpr int SMEM = 1024 + STAGE_AREA + BAR_BYTES + FAN_BAR_BYTES + KEYS_BYTES +
+  static constexpr int SMEM = 1024 + STAGE_AREA + BAR_BYTES + FAN_BAR_BYTES + 2 * KEYS_BYTES +
                               PW_BYTES + CNT_BYTES + VEC_BYTES + MISC_BYTES;
 };
 
@@ -278,9 +279,10 @@ __device__ __forceinline__ void rw_route_tokens(const float (&sv)[NT][NPL], cons
         w_out[t][lane] = g;
         keys[t][lane] = my_idx[t];
       }
+      const float inv_z = 1.0f / z_all;
 #pragma unroll
       for (int i = 0; i < NPL; ++i)
-        if (rw_expert(lane, i) < E) psum[i] += ex[i] / z_all;
+        if (rw_expert(lane, i) < E) psum[i] += ex[i] * inv_z;
     }
   }
 }
@@ -501,7 +503,9 @@ __global__ void __launch_bounds__(kRwThreads, 1)
   p += C::BAR_BYTES;
   uint64_t* fan_bars = reinterpret_cast<uint64_t*>(p);
   p += C::FAN_BAR_BYTES;
-  int* keys_s = reinterpret_cast<int*>(p);     // [BT][k] keys of the routed block
+  int* keys_s = reinterpret_cast<int*>(p);     // [BT][k] experts of the routed block's keys
+  p += C::KEYS_BYTES;
+  int* rank_s = reinterpret_cast<int*>(p);     // [BT][k] their ranks inside the block
   p += C::KEYS_BYTES;
   float* Pw = reinterpret_cast<float*>(p);     // [8][EPN] per-warp probability sums
   p += C::PW_BYTES;
@@ -829,6 +833,7 @@ __global__ void __launch_bounds__(kRwThreads, 1)
           __syncwarp();
           if (kv) {
             a.key_row[key0 + kq] = prior + before;
+            rank_s[kq] = prior + before;
             if (before == 0) cnt[e] = prior + __popc(peers);
           }
           __syncwarp();
@@ -865,14 +870,16 @@ __global__ void __launch_bounds__(kRwThreads, 1)
     ntok = ntok < 0 ? 0 : (ntok > BT ? BT : ntok);
     const int nkeys = ntok * a.k;
     const size_t key0 = (size_t)t_base * a.k;
+    // the last tile's keys and ranks are still in shared memory
+    const bool last = j == nown - 1;
     for (int kq = tid; kq < nkeys; kq += kRwThreads) {
-      const int e = __ldcg(a.topk_idx + key0 + kq);
+      const int e = last ? keys_s[kq] : __ldcg(a.topk_idx + key0 + kq);
       if (!in_bounds(e >= 0 && e < a.E, a.status)) {
         a.key_row[key0 + kq] = -1;
         if (a.slot_pos) a.slot_pos[key0 + kq] = -1;
         continue;
       }
-      const int pos = ssm.pre[j][e] + __ldcg(a.key_row + key0 + kq);
+      const int pos = ssm.pre[j][e] + (last ? rank_s[kq] : __ldcg(a.key_row + key0 + kq));
       bool keep = pos < a.capacity;
       int rw = keep ? ssm.segst[e] + pos : -1;
       if (keep && !in_bounds(pos >= 0 && rw < a.R_cap, a.status)) {
@@ -934,12 +941,6 @@ bool route_wide_copies_rows(const Plan& p) {
   return row_bytes * 3u <= (uint32_t)area;
 }
 
-// Launch modes the runtime accepted, per kernel form: bit 0 = cooperative
-// cluster launch with programmatic dependent launch worked, bit 1 = that was
-// refused and the cluster launch without the cooperative attribute is used
-// (co-residency then rests on the grid not exceeding the clusters the GPU
-// holds at once, which the launcher checks).
-static std::atomic<int> g_rw_launch_mode[2]{{0}, {0}};
 // Clusters of each size that fit on the GPU at once, per device.
 static std::atomic<int> g_rw_max_clusters[2][4][64];
 
@@ -995,28 +996,17 @@ static cudaError_t launch_route_wide_t(const CUtensorMap& mX, const CUtensorMap&
   cfg.blockDim = dim3(kRwThreads);
   cfg.dynamicSmemBytes = C::SMEM;
   cfg.stream = st;
-  cudaLaunchAttribute attr[3];
+  // a cluster launch (no cooperative attribute): the grid holds at most the
+  // clusters the GPU keeps resident at once, so every CTA reaches the
+  // grid-wide waits (which are bounded in any case)
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = a.ks;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
   attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[1].val.programmaticStreamSerializationAllowed = 1;
-  attr[2].id = cudaLaunchAttributeCooperative;
-  attr[2].val.cooperative = 1;
   cfg.attrs = attr;
-  std::atomic<int>& mode = g_rw_launch_mode[EPN == 256];
-  if ((mode.load(std::memory_order_relaxed) & 2) == 0) {
-    cfg.numAttrs = 3;
-    e = cudaLaunchKernelEx(&cfg, kern, mX, mW, a);
-    if (e == cudaSuccess) {
-      mode.fetch_or(1, std::memory_order_relaxed);
-      return e;
-    }
-    if (mode.load(std::memory_order_relaxed) & 1) return e;   // worked before
-    (void)cudaGetLastError();   // a refused attribute combination is not sticky
-    mode.fetch_or(2, std::memory_order_relaxed);
-  }
   cfg.numAttrs = 2;
   return cudaLaunchKernelEx(&cfg, kern, mX, mW, a);
 }
