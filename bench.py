@@ -120,9 +120,10 @@ def source_sha():
 
 
 # ----------------------------------------------------------------- accounting
-def accounting(shape, kept, combine_in_down=False):
+def accounting(shape, kept, combine_in_down=False, fused=False):
     """Algorithmic bytes and FLOPs per launch of each kernel and of the layer,
-    from the kept assignments per expert.
+    from the kept assignments per expert.  With `fused` the up and down
+    projections are one launch: its figures are their sum, under "up".
 
     "bytes" counts only what the definition must move: the weights of the
     experts with at least one kept row (e4m3 gate/up weights at one byte plus a
@@ -160,6 +161,11 @@ def accounting(shape, kept, combine_in_down=False):
                  "extra": h_bytes + (0 if combine_in_down else o_bytes)},
         "combine": {"bytes": y_bytes, "flops": 2 * rows * d, "extra": o_bytes},
     }
+    if fused:
+        up, dn = acc["up"], acc["down"]
+        acc["up"] = {"bytes": up["bytes"] + dn["bytes"], "flops": up["flops"] + dn["flops"],
+                     "extra": up["extra"] + dn["extra"]}
+        acc["down"] = {"bytes": 0, "flops": 0, "extra": 0}
     layer_bytes = (w_up + w_dn + E * d * el + 2 * T * d * el)
     layer_flops = 2 * rows * (m_up + 1) * d * f + S * 2 * T * 3 * d * fs + 2 * T * d * E
     return acc, {"bytes": layer_bytes, "flops": layer_flops, "active_experts": active,
@@ -601,8 +607,10 @@ def measure_layer(shape, K, Wm, stream, dist=None, sample_clocks=True):
     torch.cuda.synchronize()
     assert L.check_status(fwd.workspace) == 0, "device status after warm-up"
     kept = fwd.out.expert_counts.cpu().tolist()
-    combine_in_down = shape.dtype == "bf16" and shape.k == 1 and shape.n_shared == 0
-    acc, layer = accounting(shape, kept, combine_in_down)
+    flags = L.plan_flags(cfg)
+    combine_in_down = "combine_in_down" in flags
+    fused = "fused_projections" in flags
+    acc, layer = accounting(shape, kept, combine_in_down, fused)
 
     # The timed region runs the plain forward call, exactly as a user issues
     # it (no per-stage events: an event between two kernels would stop the
@@ -637,6 +645,7 @@ def measure_layer(shape, K, Wm, stream, dist=None, sample_clocks=True):
     stage_ms = {s: statistics.fmean(evs[i][j].elapsed_time(evs[i][j + 1]) for i in range(K_st))
                 for j, s in enumerate(STAGES)}
     return {"inp": inp, "cfg": cfg, "fwd": fwd, "fp8": fp8, "acc": acc, "layer": layer,
+            "fused": fused,
             "ms_total": ms_total, "ms_step": ms_total / K, "stage_ms": stage_ms,
             "clocks": clocks.summary() if clocks else None,
             "launches_per_step": L.launch_count(cfg, fp8)}
@@ -725,6 +734,8 @@ def run_b300(args):
     roof = roofline_for(dominant, acc, stage_ms[dominant], peaks, peak_kind, fp8)
     roof["traffic"] = ncu_traffic(dominant, shape.name)
     roof["share_of_step"] = round(stage_ms[dominant] / sum(stage_ms.values()), 4)
+    if m["fused"] and dominant == "up":
+        roof["kernel"] = "up+down (one launch)"
     layer_roof = layer_roofline(layer, ms_step, peaks)
 
     e2e = None

@@ -406,6 +406,25 @@ int moe_forward_timed(const moe_config* cfg,
 int moe_launch_count(const moe_config* cfg, int32_t* launches);
 
 /*
+ * The kernel path a moe_forward call takes for this layer (under the current
+ * moe_set_tuning overrides), as a set of MOE_PLAN_* bits: routing in one
+ * launch (E <= 64), in one launch of thread-block clusters (64 < E <= 256),
+ * or by the decode-batch router (T <= 16); the routed token rows gathered by
+ * the up projection instead of copied; the combine inside the down
+ * projection; the up and down projections in one launch.  Host only: plans,
+ * launches nothing.  Errors: those of moe_workspace_size.
+ */
+enum {
+  MOE_PLAN_ROUTE_ONE_LAUNCH = 1,
+  MOE_PLAN_ROUTE_CLUSTER = 2,
+  MOE_PLAN_ROUTE_DECODE = 4,
+  MOE_PLAN_GATHER_ROWS = 8,
+  MOE_PLAN_COMBINE_IN_DOWN = 16,
+  MOE_PLAN_FUSED_PROJECTIONS = 32
+};
+int moe_plan_flags(const moe_config* cfg, uint32_t* flags);
+
+/*
  * moe_set_tuning -- process-wide override of a kernel choice, for tests and
  * tile sweeps only; production callers leave every knob at its default.
  * Later calls of every entry point (on every thread and device) plan with
@@ -430,7 +449,15 @@ int moe_launch_count(const moe_config* cfg, int32_t* launches);
  *                            combine kernel.  y is the same bit for bit;
  *   MOE_TUNE_CLUSTER         1: the TMA-fed expert projections run as clusters
  *                            of two CTAs on adjacent column tiles sharing one
- *                            multicast A tile; 0 (the default): single CTAs.
+ *                            multicast A tile; 0 (the default): single CTAs;
+ *   MOE_TUNE_FUSED_PROJ      1: the up and down projections run as one
+ *                            persistent launch wherever a form is compiled for
+ *                            the layer's tiling (down tiles wait, bounded, for
+ *                            the up tiles of their rows); 0: always two
+ *                            launches; the default takes one launch for the
+ *                            forms that measured faster (gathered ReLU up
+ *                            projection with the combine in the down
+ *                            projection, the 96-column decode tiling).
  * Errors: MOE_ERR_ARG for an unknown knob or a value out of range.  Not
  * synchronised with calls in flight on other threads.
  */
@@ -443,7 +470,8 @@ enum {
   MOE_TUNE_MMA_M64 = 5,
   MOE_TUNE_FUSED_COMBINE = 6,
   MOE_TUNE_CLUSTER = 7,
-  MOE_TUNE_COUNT = 8
+  MOE_TUNE_FUSED_PROJ = 8,
+  MOE_TUNE_COUNT = 9
 };
 enum { MOE_ROUTER_SIMT = 1, MOE_ROUTER_FUSED = 2, MOE_ROUTER_TC = 3 };
 int moe_set_tuning(int32_t knob, int32_t value);

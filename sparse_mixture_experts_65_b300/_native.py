@@ -28,7 +28,9 @@ MOE_GATE_SOFTMAX_TOPK, MOE_GATE_SIGMOID_RENORM, MOE_GATE_SOFTMAX_FULL = 0, 1, 2
 MOE_NUM_STAGES = 6
 MOE_TUNE_ROUTER, MOE_TUNE_GATHER, MOE_TUNE_TILE_N_UP, MOE_TUNE_TILE_N_DOWN = 0, 1, 2, 3
 MOE_TUNE_PARTIAL_A_ROWS, MOE_TUNE_MMA_M64, MOE_TUNE_FUSED_COMBINE = 4, 5, 6
-MOE_TUNE_CLUSTER = 7
+MOE_TUNE_CLUSTER, MOE_TUNE_FUSED_PROJ = 7, 8
+MOE_PLAN_ROUTE_ONE_LAUNCH, MOE_PLAN_ROUTE_CLUSTER, MOE_PLAN_ROUTE_DECODE = 1, 2, 4
+MOE_PLAN_GATHER_ROWS, MOE_PLAN_COMBINE_IN_DOWN, MOE_PLAN_FUSED_PROJECTIONS = 8, 16, 32
 MOE_ROUTER_SIMT, MOE_ROUTER_FUSED, MOE_ROUTER_TC = 1, 2, 3
 STAGE_NAMES = ("router", "topk", "permute", "up", "down", "combine")
 
@@ -39,7 +41,7 @@ EXPORTS = (
     "moe_router_scores", "moe_router_scores_noalloc", "moe_router_z_loss", "moe_bias_update",
     "moe_workspace_size_fp8", "moe_forward_fp8", "moe_forward_fp8_timed", "moe_launch_count_fp8",
     "moe_set_tuning", "moe_host_io_workspace_size_fp8", "moe_forward_fp8_host_io",
-    "moe_forward_host_io_batches", "moe_forward_fp8_host_io_batches",
+    "moe_forward_host_io_batches", "moe_forward_fp8_host_io_batches", "moe_plan_flags",
 )
 
 
@@ -129,6 +131,8 @@ def _load(path: str) -> ctypes.CDLL:
     L.moe_error_string.restype = ctypes.c_char_p
     L.moe_launch_count.argtypes = [cfgp, I32P]
     L.moe_launch_count.restype = ctypes.c_int
+    L.moe_plan_flags.argtypes = [cfgp, ctypes.POINTER(ctypes.c_uint32)]
+    L.moe_plan_flags.restype = ctypes.c_int
     L.moe_set_tuning.argtypes = [ctypes.c_int32, ctypes.c_int32]
     L.moe_set_tuning.restype = ctypes.c_int
     L.moe_selftest_wait_timeout.argtypes = [P, SZ, ctypes.c_uint64, P]

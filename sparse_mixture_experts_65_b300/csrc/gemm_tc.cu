@@ -1055,6 +1055,528 @@ tc_grouped_gemm(const __grid_constant__ CUtensorMap mA, const __grid_constant__ 
   if constexpr (CL == 2) cluster_sync();
 }
 
+// ---------------------------------------------------------------- up + down in one launch
+// The up and down projections of a layer as one persistent launch over one
+// work list: every up tile, then every down tile, dealt to the CTAs in turn.
+// A down tile reads the h rows of its M tile, which exist once every up tile
+// of that M tile has stored them: each up tile, after its stores, adds one to
+// the M tile's counter (release), and the producer of a down tile issues its
+// weight (W2) tiles for the first stages, waits for the count (acquire,
+// bounded), then issues the h rows.  So W2 streams while the up projection's
+// last wave finishes, and no SM idles between the two projections.  Deadlock
+// cannot arise: every CTA runs all its up tiles before its first down tile,
+// and the grid holds at most one CTA per SM (all resident).  The counters sit
+// in the workspace header and the last CTA to finish clears them.
+template <int BNH_, bool DUAL_, int EPI_>
+struct TcPhase {
+  static constexpr int BNH = BNH_;
+  static constexpr bool DUAL = DUAL_;
+  static constexpr int EPI = EPI_;
+  using C = TcCfg<BNH_, DUAL_, EPI_>;
+  static constexpr int EPIW = (EPI_ == EPI_SWIGLU || EPI_ == EPI_GELU) ? 8 : 4;
+  // columns of an epilogue warp: a half of the tile for the activation
+  // epilogues (when the halves are whole 32-column chunks), else all of them
+  // for the first warp of each TMEM quarter
+  static constexpr bool SPLIT = EPIW == 8 && BNH_ % 64 == 0;
+};
+
+template <class PU, class PD, int ASU>
+struct UdCfg {
+  static constexpr int SB = PU::C::STAGE_BYTES > PD::C::STAGE_BYTES ? PU::C::STAGE_BYTES
+                                                                    : PD::C::STAGE_BYTES;
+  static constexpr int A_BYTES = kTcBM * 128;
+  static constexpr int STAGES_FIT = (200 * 1024) / SB;
+  static constexpr int STAGES = STAGES_FIT > 8 ? 8 : STAGES_FIT;
+  static constexpr int ACC = PU::C::MMA_N > PD::C::MMA_N ? PU::C::MMA_N : PD::C::MMA_N;
+  static constexpr int TMEM_COLS = pow2_at_least(2 * ACC);
+  static_assert(TMEM_COLS <= 512, "two accumulators must fit in tensor memory");
+  static constexpr int PROD = ASU == AS_CP ? 4 : 1;
+  static constexpr int MMA = PROD;
+  static constexpr int EPI0 = PROD + 1;
+  static constexpr int EPIW = PU::EPIW > PD::EPIW ? PU::EPIW : PD::EPIW;
+  static constexpr int THREADS = (PROD + 1 + EPIW) * 32;
+  static constexpr int BAR_BYTES = 8 * (2 * STAGES + 5) + 16;
+  // tp_up[E+2] | tp_dn[E+2] | seg_start[E] | mtiles[E+1] | kept[E]
+  static constexpr int SCHED_INTS = 5 * (kMaxE + 2);
+  static constexpr int TOK_BYTES = 4 * 128 * 4;
+  static constexpr int SMEM = 1024 + STAGES * SB + BAR_BYTES + 4 * SCHED_INTS + TOK_BYTES;
+};
+
+struct UdArgs {
+  unsigned* done;    // [n_done] up tiles stored per M tile (routed M tiles, then shared)
+  unsigned* up_all;  // up tiles stored in all
+  unsigned* fin;     // CTAs finished (the last one clears the counters and itself)
+  int n_done;
+  int sh_base;       // index of the shared segment's first M tile (R_cap / 128)
+  int nt_up, nt_up_sh;   // up tiles per routed / shared M tile
+};
+
+__device__ __forceinline__ int ud_mtile(const TileInfo& ti, int sh_base) {
+  return (ti.shared ? sh_base : 0) + ti.a_row / kTcBM;
+}
+
+__device__ __forceinline__ void ud_epi_bar(int nthreads) {
+  asm volatile("bar.sync 1, %0;" ::"r"(nthreads) : "memory");
+}
+
+template <class PU, class PD, int ASU>
+__global__ void __launch_bounds__(UdCfg<PU, PD, ASU>::THREADS, 1)
+tc_updown(const __grid_constant__ CUtensorMap mA, const __grid_constant__ CUtensorMap mA_sh,
+          const __grid_constant__ CUtensorMap mA32, const __grid_constant__ CUtensorMap mA32_sh,
+          const __grid_constant__ CUtensorMap mB0, const __grid_constant__ CUtensorMap mB1,
+          const __grid_constant__ CUtensorMap mB0_sh, const __grid_constant__ CUtensorMap mB1_sh,
+          const __grid_constant__ CUtensorMap mH, const __grid_constant__ CUtensorMap mH_sh,
+          const __grid_constant__ CUtensorMap mH32, const __grid_constant__ CUtensorMap mH32_sh,
+          const __grid_constant__ CUtensorMap mW2, const __grid_constant__ CUtensorMap mW2_sh,
+          const TcArgs au, const TcArgs ad, const UdArgs ud) {
+  using U = UdCfg<PU, PD, ASU>;
+  constexpr bool GATHER = ASU == AS_CP;
+  static_assert(ASU == AS_TMA || ASU == AS_CP, "up rows: TMA or cp.async gather");
+  static_assert(!PD::DUAL && (PD::EPI == EPI_OUT16 || PD::EPI == EPI_COMBINE1), "down epilogues");
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + U::STAGES * U::SB);
+  const uint32_t bar0 = smem_u32(bars);
+  auto full_bar = [&](int s) { return bar0 + 8u * s; };
+  auto empty_bar = [&](int s) { return bar0 + 8u * (U::STAGES + s); };
+  auto tfull_bar = [&](int b) { return bar0 + 8u * (2 * U::STAGES + b); };
+  auto tempty_bar = [&](int b) { return bar0 + 8u * (2 * U::STAGES + 2 + b); };
+  const uint32_t drain_bar = bar0 + 8u * (2 * U::STAGES + 4);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * U::STAGES + 5);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  volatile int* s_stop = reinterpret_cast<volatile int*>(tmem_slot + 2);
+  const uint32_t smem_base = smem_u32(smem);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < U::STAGES; ++s) {
+      mbar_init(full_bar(s), GATHER ? 2 : 1);
+      mbar_init(empty_bar(s), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(tfull_bar(b), 1);
+      mbar_init(tempty_bar(b), 32 * U::EPIW);
+    }
+    mbar_init(drain_bar, 1);
+    *abort_flag = 0;
+    *s_stop = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&mA);
+    tma_prefetch_desc(&mA32);
+    tma_prefetch_desc(&mB0);
+    if (PU::DUAL) tma_prefetch_desc(&mB1);
+    tma_prefetch_desc(&mH);
+    tma_prefetch_desc(&mH32);
+    tma_prefetch_desc(&mW2);
+    if (au.has_shared) {
+      tma_prefetch_desc(&mA_sh);
+      tma_prefetch_desc(&mA32_sh);
+      tma_prefetch_desc(&mB0_sh);
+      if (PU::DUAL) tma_prefetch_desc(&mB1_sh);
+      tma_prefetch_desc(&mH_sh);
+      tma_prefetch_desc(&mH32_sh);
+      tma_prefetch_desc(&mW2_sh);
+    }
+  }
+  if (warp == U::MMA) {
+    tmem_alloc(smem_u32(tmem_slot), U::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  pdl_wait();     // the schedule and the routed rows come from the routing kernels
+  pdl_trigger();
+  // both projections' tile schedules in shared memory (the segments are the
+  // same; only the tile prefixes differ)
+  int* s_tpu = reinterpret_cast<int*>(smem + U::STAGES * U::SB + U::BAR_BYTES);
+  int* s_tpd = s_tpu + (kMaxE + 2);
+  int* s_seg = s_tpd + (kMaxE + 2);
+  int* s_mt = s_seg + (kMaxE + 2);
+  int* s_kept = s_mt + (kMaxE + 2);
+  const int nseg = au.E + au.has_shared;
+  for (int i = threadIdx.x; i <= nseg; i += blockDim.x) {
+    s_tpu[i] = __ldg(au.tp + i);
+    s_tpd[i] = __ldg(ad.tp + i);
+  }
+  for (int i = threadIdx.x; i < nseg; i += blockDim.x) s_mt[i] = __ldg(au.mtiles + i);
+  for (int i = threadIdx.x; i < au.E; i += blockDim.x) {
+    s_seg[i] = __ldg(au.seg_start + i);
+    s_kept[i] = __ldg(au.kept + i);
+  }
+  __syncthreads();
+  const Sched su{s_tpu, s_seg, s_mt, s_kept};
+  const Sched sd{s_tpd, s_seg, s_mt, s_kept};
+  const int n_up = s_tpu[nseg];
+  const int total = n_up + s_tpd[nseg];
+  auto decode = [&](int item, bool& dn) -> TileInfo {
+    dn = item >= n_up;
+    return dn ? decode_tile(ad, sd, item - n_up, PD::BNH) : decode_tile(au, su, item, PU::BNH);
+  };
+  auto give_up = [&]() {
+    atomicOr(au.status, STATUS_TIMEOUT_GEMM);
+    *abort_flag = 1;
+  };
+  // have the up tiles of a down tile's M tile stored its h rows?
+  auto dep_met = [&](const TileInfo& ti) {
+    return ld_acquire_gpu_u32(ud.done + ud_mtile(ti, ud.sh_base)) >=
+           (unsigned)(ti.shared ? ud.nt_up_sh : ud.nt_up);
+  };
+  auto dep_wait = [&](const TileInfo& ti) -> bool {
+    if (dep_met(ti)) return true;
+    const uint64_t t0 = globaltimer_ns();
+    for (uint32_t i = 1;; ++i) {
+      if (dep_met(ti)) return true;
+      if ((i & 63u) == 0) {
+        if (*abort_flag) return false;
+        if (globaltimer_ns() - t0 > au.timeout_ns) return false;
+      }
+    }
+  };
+
+  if (warp < U::PROD) {
+    if constexpr (GATHER) {
+      // ---------------- four producer warps (gathered up rows) ----------------
+      // As in tc_grouped_gemm: warp w fills the stages of uses g = w, w + 4, ...;
+      // routed up tiles gather their rows of x with cp.async, every other tile
+      // (the shared expert's up tiles, all down tiles) loads A by TMA.  A down
+      // stage's weight tile goes out before the warp waits for the h rows.
+      uint32_t g = 0;
+      bool ok = true;
+      bool all_up = false;   // (lane 0's view)
+      const int sub = lane >> 3, chunk = lane & 7;
+      for (int item = blockIdx.x; item < total && ok; item += gridDim.x) {
+        bool dn;
+        const TileInfo ti = decode(item, dn);
+        const int nk = (ti.K + 63) / 64;
+        if (nk < U::PROD && (int)((uint32_t)(warp - (int)(g & 3u)) & 3u) >= nk) {
+          g += nk;
+          continue;
+        }
+        const TcArgs& a = dn ? ad : au;
+        const bool gat = !dn && !ti.shared;
+        const CUtensorMap* pA = dn ? (ti.shared ? &mH_sh : &mH) : &mA_sh;
+        const CUtensorMap* pA32 = dn ? (ti.shared ? &mH32_sh : &mH32) : &mA32_sh;
+        const CUtensorMap* pB0 = dn ? (ti.shared ? &mW2_sh : &mW2) : (ti.shared ? &mB0_sh : &mB0);
+        const CUtensorMap* pB1 = ti.shared ? &mB1_sh : &mB1;
+        const bool dual = !dn && PU::DUAL;
+        const int bnh = dn ? PD::BNH : PU::BNH;
+        const uint32_t b_bytes = dn ? (uint32_t)PD::C::B_BYTES : (uint32_t)PU::C::B_BYTES;
+        const int e = ti.shared ? 0 : ti.seg;
+        const int rows = ti.row_end - ti.a_row < kTcBM ? ti.row_end - ti.a_row : kTcBM;
+        const int a_boxes = gat ? 0 : a_real_boxes(rows, a.partial_rows);
+        const uint32_t a_bytes = gat ? 0u : a_stage_bytes(a_boxes, U::A_BYTES);
+        int* tok_s = reinterpret_cast<int*>(smem + U::STAGES * U::SB + U::BAR_BYTES +
+                                            4 * U::SCHED_INTS) + warp * 128;
+        bool tok_ready = !gat;
+        bool dep_ok = !dn || all_up;
+        for (int kb = 0; kb < nk; ++kb, ++g) {
+          if ((int)(g & 3u) != warp) continue;
+          const int s = g % U::STAGES;
+          const uint32_t ph = (g / U::STAGES) & 1u;
+          int okw = 1;
+          if (lane == 0)
+            okw = mbar_wait_bounded(empty_bar(s), ph ^ 1u, au.timeout_ns, abort_flag) ? 1 : 0;
+          okw = __shfl_sync(0xffffffffu, okw, 0);
+          __syncwarp();
+          if (!okw) {
+            if (lane == 0) give_up();
+            ok = false;
+            break;
+          }
+          const uint32_t sa = smem_base + s * U::SB;
+          const uint32_t sb = sa + U::A_BYTES;
+          if (lane == 0) {
+            mbar_arrive_expect_tx(full_bar(s), a_bytes + b_bytes);
+            tma_load_3d(sb, pB0, full_bar(s), kb * 64, ti.n0, e);
+            if (dual) tma_load_3d(sb + bnh * 128, pB1, full_bar(s), kb * 64, ti.n0, e);
+            if (!gat) {
+              if (!dep_ok && ld_acquire_gpu_u32(ud.up_all) >= (unsigned)n_up) {
+                fence_proxy_async_global();   // every up tile is stored: no more checks
+                all_up = true;
+                dep_ok = true;
+              }
+              if (!dep_ok) {
+                // on a give-up the rows are loaded all the same (the call's
+                // status reports the timeout), so that every issued stage completes
+                if (!dep_wait(ti)) give_up();
+                fence_proxy_async_global();
+                dep_ok = true;
+              }
+              load_a_stage(sa, pA, pA32, full_bar(s), kb * 64, ti.a_row, a_boxes);
+            }
+          }
+          if (!tok_ready) {
+            __syncwarp();
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              const int r = ti.a_row + lane + 32 * j;
+              int tk = r < ti.row_end ? __ldg(au.row_token + r) : -1;
+              if (tk >= 0 && !in_bounds(tk < au.T_x, au.status)) tk = -1;
+              tok_s[lane + 32 * j] = tk;
+            }
+            __syncwarp();
+            tok_ready = true;
+          }
+          if (gat) {
+            const int col = kb * 64 + chunk * 8;
+            gather_stage(sa, tok_s, au.gx, au.gx_row_bytes, col, col < ti.K, sub, chunk);
+            cp_async_wait_group<0>();
+            fence_proxy_async_smem();
+          }
+          __syncwarp();
+          if (lane == 0) mbar_arrive(full_bar(s));
+        }
+      }
+      if (warp == 0 && lane == 0) {
+        for (int s = 0; s < U::STAGES; ++s) {
+          if (g > static_cast<uint32_t>(s)) {
+            const uint32_t issues = (g - 1 - s) / U::STAGES + 1;
+            if (ok)
+              mbar_wait_bounded(empty_bar(s), (issues - 1) & 1u, au.timeout_ns, abort_flag);
+            else
+              mbar_wait_bounded(full_bar(s), (issues - 1) & 1u, au.timeout_ns, nullptr);
+          }
+        }
+      }
+    } else if (lane == 0) {
+      // ---------------- TMA producer ----------------
+      uint32_t g = 0;   // stage uses issued
+      bool ok = true;
+      bool all_up = false;
+      for (int item = blockIdx.x; item < total && ok; item += gridDim.x) {
+        bool dn;
+        const TileInfo ti = decode(item, dn);
+        const TcArgs& a = dn ? ad : au;
+        const CUtensorMap* pA = dn ? (ti.shared ? &mH_sh : &mH) : (ti.shared ? &mA_sh : &mA);
+        const CUtensorMap* pA32 =
+            dn ? (ti.shared ? &mH32_sh : &mH32) : (ti.shared ? &mA32_sh : &mA32);
+        const CUtensorMap* pB0 = dn ? (ti.shared ? &mW2_sh : &mW2) : (ti.shared ? &mB0_sh : &mB0);
+        const CUtensorMap* pB1 = ti.shared ? &mB1_sh : &mB1;
+        const bool dual = !dn && PU::DUAL;
+        const int bnh = dn ? PD::BNH : PU::BNH;
+        const uint32_t b_bytes = dn ? (uint32_t)PD::C::B_BYTES : (uint32_t)PU::C::B_BYTES;
+        const int e = ti.shared ? 0 : ti.seg;
+        const int nk = (ti.K + 63) / 64;
+        const int rows = ti.row_end - ti.a_row < kTcBM ? ti.row_end - ti.a_row : kTcBM;
+        const int a_boxes = a_real_boxes(rows, a.partial_rows);
+        const uint32_t a_bytes = a_stage_bytes(a_boxes, U::A_BYTES);
+        int kb = 0;
+        if (dn && !all_up) {
+          // once every up tile is stored (observed through an acquire, then one
+          // proxy fence), no down tile needs its own check
+          if (ld_acquire_gpu_u32(ud.up_all) >= (unsigned)n_up) {
+            fence_proxy_async_global();
+            all_up = true;
+          }
+        }
+        if (dn && !all_up) {
+          if (!dep_met(ti)) {
+            // the h rows are not all stored yet: the weight tiles of the first
+            // stages go out now, their h rows after the wait (loaded even on a
+            // give-up, so that every issued stage completes; the call's status
+            // then reports the timeout)
+            int nb = 0;
+            for (; nb < nk && nb < U::STAGES; ++nb) {
+              const uint32_t gg = g + nb;
+              const int s = gg % U::STAGES;
+              const uint32_t ph = (gg / U::STAGES) & 1u;
+              if (!mbar_wait_bounded(empty_bar(s), ph ^ 1u, au.timeout_ns, abort_flag)) {
+                give_up();
+                ok = false;
+                break;
+              }
+              mbar_arrive_expect_tx(full_bar(s), a_bytes + b_bytes);
+              tma_load_3d(smem_base + s * U::SB + U::A_BYTES, pB0, full_bar(s), nb * 64, ti.n0, e);
+            }
+            if (ok && !dep_wait(ti)) give_up();
+            fence_proxy_async_global();
+            for (int j = 0; j < nb; ++j) {
+              const int s = (g + j) % U::STAGES;
+              load_a_stage(smem_base + s * U::SB, pA, pA32, full_bar(s), j * 64, ti.a_row, a_boxes);
+            }
+            kb = nb;
+            if (!ok) {
+              g += nb;
+              break;
+            }
+          } else {
+            fence_proxy_async_global();   // the count was observed through an acquire
+          }
+        }
+        for (; kb < nk; ++kb) {
+          const uint32_t gg = g + kb;
+          const int s = gg % U::STAGES;
+          const uint32_t ph = (gg / U::STAGES) & 1u;
+          if (!mbar_wait_bounded(empty_bar(s), ph ^ 1u, au.timeout_ns, abort_flag)) {
+            give_up();
+            ok = false;
+            break;
+          }
+          const uint32_t sa = smem_base + s * U::SB;
+          const uint32_t sb = sa + U::A_BYTES;
+          mbar_arrive_expect_tx(full_bar(s), a_bytes + b_bytes);
+          load_a_stage(sa, pA, pA32, full_bar(s), kb * 64, ti.a_row, a_boxes);
+          tma_load_3d(sb, pB0, full_bar(s), kb * 64, ti.n0, e);
+          if (dual) tma_load_3d(sb + bnh * 128, pB1, full_bar(s), kb * 64, ti.n0, e);
+        }
+        g += kb;
+      }
+      // nothing asynchronous may still target shared memory at exit
+      for (int s = 0; s < U::STAGES; ++s) {
+        if (g > static_cast<uint32_t>(s)) {
+          const uint32_t issues = (g - 1 - s) / U::STAGES + 1;
+          if (ok)
+            mbar_wait_bounded(empty_bar(s), (issues - 1) & 1u, au.timeout_ns, abort_flag);
+          else
+            mbar_wait_bounded(full_bar(s), (issues - 1) & 1u, au.timeout_ns, nullptr);
+        }
+      }
+    }
+  } else if (warp == U::MMA) {
+    if (lane == 0) {
+      // ---------------- MMA issuer: one accumulator per tile ----------------
+      uint32_t g = 0;
+      int it = 0;
+      bool ok = true;
+      for (int item = blockIdx.x; item < total && ok; item += gridDim.x, ++it) {
+        bool dn;
+        const TileInfo ti = decode(item, dn);
+        const int nk = (ti.K + 63) / 64;
+        const int ab = it & 1;
+        const uint32_t aph = (it >> 1) & 1;
+        if (!mbar_wait_bounded(tempty_bar(ab), aph ^ 1u, au.timeout_ns, abort_flag)) {
+          give_up();
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + ab * U::ACC;
+        const uint32_t idesc = dn ? (ti.m64 ? PD::C::IDESC64 : PD::C::IDESC)
+                                  : (ti.m64 ? PU::C::IDESC64 : PU::C::IDESC);
+        for (int kb = 0; kb < nk; ++kb, ++g) {
+          const int s = g % U::STAGES;
+          const uint32_t ph = (g / U::STAGES) & 1u;
+          if (!mbar_wait_bounded(full_bar(s), ph, au.timeout_ns, abort_flag)) {
+            give_up();
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t sa = smem_base + s * U::SB;
+          const uint32_t sb = sa + U::A_BYTES;
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)
+            tc_mma_bf16(d_tmem, smem_desc_k128(sa + kk * 32), smem_desc_k128(sb + kk * 32), idesc,
+                        (kb != 0 || kk != 0) ? 1u : 0u);
+          tc_commit(empty_bar(s));
+        }
+        if (!ok) break;
+        tc_commit(tfull_bar(ab));
+      }
+      if (!ok) {
+        tc_commit(drain_bar);
+        mbar_wait_bounded(drain_bar, 0, au.timeout_ns, nullptr);
+      }
+    }
+  } else {
+    // ---------------- epilogue ----------------
+    const int q = warp & 3;
+    const int row_in_tile = q * 32 + lane;
+    const int ew = warp - U::EPI0;
+    const int ep_tid = ew * 32 + lane;
+    const int half = ew >> 2;
+    const int cu_lo = PU::SPLIT ? half * (PU::BNH / 2) : 0;
+    const int cu_hi = PU::SPLIT ? cu_lo + PU::BNH / 2 : (half == 0 ? PU::BNH : 0);
+    const int cd_lo = PD::SPLIT ? half * (PD::BNH / 2) : 0;
+    const int cd_hi = PD::SPLIT ? cd_lo + PD::BNH / 2 : (half == 0 ? PD::BNH : 0);
+    if constexpr (PD::EPI == EPI_COMBINE1) {
+      // a dropped token (key_row < 0, top-1) gets y = 0
+      uint4* y = static_cast<uint4*>(ad.y);
+      const int nvec = ad.ld_y * 2 / 16;
+      const int gw = blockIdx.x * U::EPIW + ew, nw = gridDim.x * U::EPIW;
+      for (int t = gw; t < ad.T_tokens; t += nw) {
+        if (__ldg(ad.key_row + t) < 0)
+          for (int c = lane; c < nvec; c += 32) y[(size_t)t * nvec + c] = make_uint4(0, 0, 0, 0);
+      }
+    }
+    int it = 0;
+    for (int item = blockIdx.x; item < total; item += gridDim.x, ++it) {
+      bool dn;
+      const TileInfo ti = decode(item, dn);
+      const TcArgs& a = dn ? ad : au;
+      const int rit = !ti.m64 ? row_in_tile : (lane < 16 ? q * 16 + lane : kTcBM);
+      const size_t orow = static_cast<size_t>(ti.a_row + rit);
+      bool row_ok = rit < kTcBM && ti.a_row + rit < ti.row_end;
+      if (row_ok && !ti.shared) row_ok = in_bounds((int)orow < a.R_cap, a.status);
+      const int ab = it & 1;
+      const uint32_t aph = (it >> 1) & 1;
+      bool ok = mbar_wait_sleep_bounded(tfull_bar(ab), aph, au.timeout_ns, abort_flag);
+      if (!ok) give_up();
+      tc_fence_after();
+      const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + ab * U::ACC;
+      if (ok) {
+        if (dn) {
+          if constexpr (PD::EPI == EPI_COMBINE1) {
+            int tok = row_ok ? __ldg(ad.row_token + orow) : 0;
+            const bool tok_ok = row_ok && in_bounds(tok >= 0 && tok < ad.T_tokens, ad.status);
+            if (!tok_ok) tok = 0;
+            const float gt = tok_ok ? __ldg(ad.gate + tok) : 0.f;
+            epilogue_tile<PD::BNH, false, PD::EPI>(ad, ti, t_row, (size_t)tok, tok_ok, gt, cd_lo,
+                                                   cd_hi);
+          } else {
+            epilogue_tile<PD::BNH, false, PD::EPI>(ad, ti, t_row, orow, row_ok, 1.f, cd_lo, cd_hi);
+          }
+        } else {
+          epilogue_tile<PU::BNH, PU::DUAL, PU::EPI>(au, ti, t_row, orow, row_ok, 1.f, cu_lo,
+                                                    cu_hi);
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(tempty_bar(ab));
+      if (!dn) {
+        // this up tile's h rows are stored: count them in for their M tile
+        // (every epilogue thread's stores, then one release); all epilogue
+        // threads stop together if any role gave up
+        __threadfence();
+        ud_epi_bar(32 * U::EPIW);
+        if (ep_tid == 0) {
+          if (*abort_flag == 0) {
+            red_add_release_gpu(ud.done + ud_mtile(ti, ud.sh_base), 1u);
+            red_add_release_gpu(ud.up_all, 1u);
+          }
+          *s_stop = *abort_flag;
+        }
+        ud_epi_bar(32 * U::EPIW);
+        if (*s_stop) break;
+      } else if (!ok) {
+        break;   // down tiles have no barriers: leave at once
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == U::MMA) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, U::TMEM_COLS);
+  }
+  // the last CTA to finish clears the counters for the next call
+  if (threadIdx.x == 0) {
+    __threadfence();
+    if (atomicAdd(ud.fin, 1u) == gridDim.x - 1u) {
+      for (int i = 0; i < ud.n_done; ++i) ud.done[i] = 0u;
+      *ud.up_all = 0u;
+      __threadfence();
+      *ud.fin = 0u;
+    }
+  }
+}
+
 // ---------------------------------------------------------------- host side
 struct TcMaps {
   CUtensorMap A, A_sh, A32, A32_sh, B0, B1, B0_sh, B1_sh;
@@ -1186,6 +1708,84 @@ static cudaError_t dispatch_down(int bn, bool combine1, bool combinek, const TcM
 
 constexpr uint64_t kGemmTimeoutNs = 2000000000ull;   // 2 s
 
+// ---- up + down in one launch: the compiled forms ----
+template <class PU, class PD, int ASU>
+static cudaError_t run_ud(const TcMaps& mu, const TcMaps& md, const TcArgs& au, const TcArgs& ad,
+                          const UdArgs& ud, int grid, cudaStream_t st) {
+  using U = UdCfg<PU, PD, ASU>;
+  static std::atomic<uint64_t> attr_done{0};
+  auto kern = tc_updown<PU, PD, ASU>;
+  cudaError_t e = smem_attr_once(kern, U::SMEM, attr_done);
+  if (e != cudaSuccess) return e;
+  return launch_pdl(kern, dim3(grid), dim3(U::THREADS), U::SMEM, st, mu.A, mu.A_sh, mu.A32,
+                    mu.A32_sh, mu.B0, mu.B1, mu.B0_sh, mu.B1_sh, md.A, md.A_sh, md.A32,
+                    md.A32_sh, md.B0, md.B0_sh, au, ad, ud);
+}
+
+using UdSw128 = TcPhase<128, true, EPI_SWIGLU>;
+using UdSw96 = TcPhase<96, true, EPI_SWIGLU>;
+using UdRelu256 = TcPhase<256, false, EPI_RELU>;
+using UdOut256 = TcPhase<256, false, EPI_OUT16>;
+using UdOut192 = TcPhase<192, false, EPI_OUT16>;
+using UdOut96 = TcPhase<96, false, EPI_OUT16>;
+using UdCmb256 = TcPhase<256, false, EPI_COMBINE1>;
+using UdCmb192 = TcPhase<192, false, EPI_COMBINE1>;
+
+// The forms compiled for one launch (the tilings the bench workloads take:
+// SwiGLU up tiles of 128 columns fed by TMA or gathered, of 96 for the
+// smallest decode batch; ReLU up tiles of 256 gathered, with the combine in
+// the down epilogue); any other layer runs the two launches.
+bool updown_compiled(int as, int act, int up_bn, int dn_bn, bool combine1) {
+  if (act == MOE_ACT_SWIGLU && !combine1) {
+    if (up_bn == 128 && (as == AS_TMA || as == AS_CP)) return dn_bn == 256 || dn_bn == 192;
+    if (up_bn == 96 && as == AS_TMA) return dn_bn == 96;
+  }
+  if (act == MOE_ACT_RELU && combine1 && up_bn == 256 && as == AS_CP)
+    return dn_bn == 192 || dn_bn == 256;
+  return false;
+}
+
+static cudaError_t dispatch_updown(int as, int act, int up_bn, int dn_bn, bool combine1,
+                                   const TcMaps& mu, const TcMaps& md, const TcArgs& au,
+                                   const TcArgs& ad, const UdArgs& ud, int grid, cudaStream_t st) {
+  if (act == MOE_ACT_SWIGLU && !combine1 && up_bn == 128) {
+    if (as == AS_TMA) {
+      if (dn_bn == 256) return run_ud<UdSw128, UdOut256, AS_TMA>(mu, md, au, ad, ud, grid, st);
+      if (dn_bn == 192) return run_ud<UdSw128, UdOut192, AS_TMA>(mu, md, au, ad, ud, grid, st);
+    } else if (as == AS_CP) {
+      if (dn_bn == 256) return run_ud<UdSw128, UdOut256, AS_CP>(mu, md, au, ad, ud, grid, st);
+      if (dn_bn == 192) return run_ud<UdSw128, UdOut192, AS_CP>(mu, md, au, ad, ud, grid, st);
+    }
+  }
+  if (act == MOE_ACT_SWIGLU && !combine1 && up_bn == 96 && as == AS_TMA && dn_bn == 96)
+    return run_ud<UdSw96, UdOut96, AS_TMA>(mu, md, au, ad, ud, grid, st);
+  if (act == MOE_ACT_RELU && combine1 && up_bn == 256 && as == AS_CP) {
+    if (dn_bn == 192) return run_ud<UdRelu256, UdCmb192, AS_CP>(mu, md, au, ad, ud, grid, st);
+    if (dn_bn == 256) return run_ud<UdRelu256, UdCmb256, AS_CP>(mu, md, au, ad, ud, grid, st);
+  }
+  return cudaErrorInvalidValue;
+}
+
+int updown_counters(const Plan& p) { return p.R_cap / kTcBM + p.mt_sh; }
+
+bool updown_eligible(const Plan& p) {
+  if (!p.tc || p.fp8 || p.combine_k || p.cluster2_up || p.cluster2_dn || p.gather4) return false;
+  if (updown_counters(p) > kMaxTileCounters) return false;   // the counters live in the header
+  return updown_compiled(p.gather ? AS_CP : AS_TMA, p.cfg.act, p.up_bn, p.dn_bn,
+                         p.combine_in_down);
+}
+
+// The forms that measured faster as one launch (same box, A/B in one call):
+// the gathered ReLU up projection with the combine in the down epilogue
+// (Switch-shaped layer 95.0 -> 89.5 us per step) and the 96-column decode
+// form (gpt-oss-shaped T = 1: 65.2 -> 64.6 us).  The 128-column SwiGLU forms
+// did not (DeepSeek-V3-shaped +0.5 %, Mixtral-shaped +1.3 %, gpt-oss-shaped
+// T = 16 +1.2 %): those layers run under the power cap, where closing the
+// idle gap between the projections saves no energy and so no time.
+bool updown_default(const Plan& p) {
+  return (p.cfg.act == MOE_ACT_RELU && p.combine_in_down) || p.up_bn == 96;
+}
+
 cudaError_t launch_experts_tc(const Plan& p, const void* x, const void* W1, const void* W3,
                               const void* W2, const void* Ws1, const void* Ws3, const void* Ws2,
                               void* ws, cudaStream_t st, cudaEvent_t mid_event, void* y,
@@ -1275,13 +1875,6 @@ cudaError_t launch_experts_tc(const Plan& p, const void* x, const void* W1, cons
   au.timeout_ns = kGemmTimeoutNs;
   const int grid_up = p.max_tiles_up < p.num_sms ? p.max_tiles_up : p.num_sms;
   const int as = p.gather ? AS_CP : p.gather4 ? AS_G4 : AS_TMA;
-  cudaError_t e = p.fp8 ? dispatch_up_f8(p.up_bn, mu, au, grid_up, st)
-                        : dispatch_up(as, p.up_bn, c.act, mu, au, grid_up, st, p.cluster2_up);
-  if (e != cudaSuccess) return e;
-  if (mid_event) {
-    e = cudaEventRecord(mid_event, st);
-    if (e != cudaSuccess) return e;
-  }
 
   // ---- down projection: o = h W2^T (fp32) ----
   TcMaps md;
@@ -1326,6 +1919,30 @@ cudaError_t launch_experts_tc(const Plan& p, const void* x, const void* W1, cons
   ad.out_sh = sh ? static_cast<void*>(w + p.ws.os) : nullptr;
   ad.ld_out_sh = sh ? c.d : 0;
   const int grid_dn = p.max_tiles_dn < p.num_sms ? p.max_tiles_dn : p.num_sms;
+  if (p.fused) {
+    // both projections in one launch; the up stage event then covers both
+    UdArgs ud;
+    ud.done = reinterpret_cast<unsigned*>(w + p.ws.status + kTileCounterOffset);
+    ud.fin = reinterpret_cast<unsigned*>(w + p.ws.status + kUpDownFinOffset);
+    ud.up_all = reinterpret_cast<unsigned*>(w + p.ws.status + kUpDownAllOffset);
+    ud.n_done = updown_counters(p);
+    ud.sh_base = p.R_cap / kTcBM;
+    ud.nt_up = p.nt_up;
+    ud.nt_up_sh = p.nt_up_sh;
+    const long long tiles = (long long)p.max_tiles_up + p.max_tiles_dn;
+    const int grid = tiles < p.num_sms ? (int)tiles : p.num_sms;
+    cudaError_t e = dispatch_updown(as, c.act, p.up_bn, p.dn_bn, p.combine_in_down, mu, md, au,
+                                    ad, ud, grid, st);
+    if (e != cudaSuccess) return e;
+    return mid_event ? cudaEventRecord(mid_event, st) : cudaSuccess;
+  }
+  cudaError_t e = p.fp8 ? dispatch_up_f8(p.up_bn, mu, au, grid_up, st)
+                        : dispatch_up(as, p.up_bn, c.act, mu, au, grid_up, st, p.cluster2_up);
+  if (e != cudaSuccess) return e;
+  if (mid_event) {
+    e = cudaEventRecord(mid_event, st);
+    if (e != cudaSuccess) return e;
+  }
   return dispatch_down(p.dn_bn, p.combine_in_down, p.combine_k, md, ad, grid_dn, st,
                        p.cluster2_dn);
 }

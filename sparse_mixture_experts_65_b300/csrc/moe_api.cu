@@ -41,7 +41,7 @@ int make_plan(const moe_config* cfg, WsKind kind, Plan* p, int num_sms);
 
 // Process-wide overrides set through moe_set_tuning (tests and tile sweeps
 // only); -1 = no override.  Production calls never read the environment.
-static std::atomic<int> g_tune[MOE_TUNE_COUNT] = {-1, -1, -1, -1, -1, -1, -1, -1};
+static std::atomic<int> g_tune[MOE_TUNE_COUNT] = {-1, -1, -1, -1, -1, -1, -1, -1, -1};
 
 int tuning(int knob) {
   return knob >= 0 && knob < MOE_TUNE_COUNT ? g_tune[knob].load(std::memory_order_relaxed) : -1;
@@ -275,11 +275,19 @@ int make_plan(const moe_config* cfg, WsKind kind, Plan* p, int num_sms) {
     P.cluster2_dn = on && P.tc && !P.combine_k && (P.dn_bn == 256 || P.dn_bn == 192);
   }
   P.nt_up = ceil_div(c.f, P.up_bn);
-  P.nt_dn = ceil_div(c.d, P.dn_bn);
   P.nt_up_sh = c.n_shared ? ceil_div(c.f_shared, P.up_bn) : 0;
+  P.nt_dn = ceil_div(c.d, P.dn_bn);
   P.nt_dn_sh = c.n_shared ? ceil_div(c.d, P.dn_bn) : 0;
   P.max_tiles_up = (P.R_cap / P.bm) * P.nt_up + P.mt_sh * P.nt_up_sh;
   P.max_tiles_dn = (P.R_cap / P.bm) * P.nt_dn + P.mt_sh * P.nt_dn_sh;
+  // Up and down projections in one persistent launch (down tiles wait for
+  // their M tile's up tiles through counters), where a form is compiled for
+  // the tiling and measured faster than two launches; a tuning override of 1
+  // takes every compiled form, 0 none.
+  {
+    const int fp = tuning(MOE_TUNE_FUSED_PROJ);
+    P.fused = updown_eligible(P) && (fp == 1 || (fp < 0 && updown_default(P)));
+  }
 
   // ---- workspace layout ----
   WsLayout& L = P.ws;
@@ -858,7 +866,24 @@ int moe_launch_count(const moe_config* cfg, int32_t* launches) {
                       : p.route_tc  ? (copy ? 2 : 1)
                       : p.route_wide ? (copy && !route_wide_copies_rows(p) ? 2 : 1)
                                     : (p.router_fused ? 2 : 3);
-  *launches = cfg->T == 0 ? 0 : routing + 2 + (p.combine_in_down || p.combine_k ? 0 : 1);
+  *launches = cfg->T == 0 ? 0
+                          : routing + (p.fused ? 1 : 2) + (p.combine_in_down || p.combine_k ? 0 : 1);
+  return MOE_OK;
+}
+
+int moe_plan_flags(const moe_config* cfg, uint32_t* flags) {
+  if (!flags) return MOE_ERR_ARG;
+  Plan p;
+  const int rc = make_plan(cfg, WsKind::Forward, &p);
+  if (rc != MOE_OK) return rc;
+  uint32_t f = 0;
+  if (p.route_tc) f |= MOE_PLAN_ROUTE_ONE_LAUNCH;
+  if (p.route_wide) f |= MOE_PLAN_ROUTE_CLUSTER;
+  if (p.route_small) f |= MOE_PLAN_ROUTE_DECODE;
+  if (p.gather || p.gather4) f |= MOE_PLAN_GATHER_ROWS;
+  if (p.combine_in_down || p.combine_k) f |= MOE_PLAN_COMBINE_IN_DOWN;
+  if (p.fused) f |= MOE_PLAN_FUSED_PROJECTIONS;
+  *flags = f;
   return MOE_OK;
 }
 
@@ -879,7 +904,7 @@ int moe_set_tuning(int32_t knob, int32_t value) {
   if (knob == MOE_TUNE_ROUTER && value > MOE_ROUTER_TC) return MOE_ERR_ARG;
   if (knob == MOE_TUNE_GATHER && value > 2) return MOE_ERR_ARG;
   if ((knob == MOE_TUNE_MMA_M64 || knob == MOE_TUNE_FUSED_COMBINE ||
-       knob == MOE_TUNE_CLUSTER) && value > 1)
+       knob == MOE_TUNE_CLUSTER || knob == MOE_TUNE_FUSED_PROJ) && value > 1)
     return MOE_ERR_ARG;
   g_tune[knob].store(value, std::memory_order_relaxed);
   return MOE_OK;

@@ -38,6 +38,12 @@ constexpr int kRouteCopyNextOffset = 64;
 constexpr int kRouteCopyDoneOffset = 80;
 constexpr int kRouteArrive2Offset = 96;
 constexpr int kRoutePassed2Offset = 112;
+// Up and down projections in one launch: the CTAs that have finished, the
+// up tiles stored in all; the per-M-tile counts of stored up tiles use the
+// tile-counter area (only one of
+// the two is in use at a time, and both are zero between launches).
+constexpr int kUpDownFinOffset = 128;
+constexpr int kUpDownAllOffset = 144;   // up tiles stored in all
 constexpr int kRouteTcMaxOwn = 16;        // 128-token tiles per CTA of the one-launch router
 // One-launch router for 64 < E <= 256 (route_wide.cu): top-k of at most
 // kRouteWideMaxK, at most kRouteWideMaxOwn tiles per cluster, a grid of at
@@ -118,6 +124,7 @@ struct Plan {
   bool cluster2_up;           // the up projection runs as 2-CTA clusters sharing the A tile
   bool cluster2_dn;           // the same for the down projection
   bool fp8;                   // gate/up weights in e4m3: quantised rows, fp8 up projection
+  bool fused;                 // up and down projections in one persistent launch
   int num_sms;
   WsLayout ws;
 };
@@ -191,6 +198,11 @@ cudaError_t launch_experts_tc(const Plan& p, const void* x, const void* W1, cons
                               const float* topk_w, const float* W1s = nullptr,
                               const float* W3s = nullptr);
 cudaError_t launch_quant_rows(const Plan& p, const void* x, void* ws, cudaStream_t st);
+// Up and down projections in one launch: compiled for this tiling and the
+// counters fit the workspace header.
+bool updown_eligible(const Plan& p);
+bool updown_default(const Plan& p);   // eligible forms that run as one launch by default
+int updown_counters(const Plan& p);
 cudaError_t launch_experts_simt(const Plan& p, const void* x, const void* W1, const void* W3,
                                 const void* W2, const void* Ws1, const void* Ws3,
                                 const void* Ws2, void* ws, cudaStream_t st,

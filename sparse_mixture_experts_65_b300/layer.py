@@ -73,6 +73,22 @@ def alloc_workspace(cfg: N.MoeConfig, device="cuda", kind: str = "forward") -> t
     return ws
 
 
+_PLAN_FLAGS = {"route_one_launch": N.MOE_PLAN_ROUTE_ONE_LAUNCH,
+               "route_cluster": N.MOE_PLAN_ROUTE_CLUSTER,
+               "route_decode": N.MOE_PLAN_ROUTE_DECODE,
+               "gather_rows": N.MOE_PLAN_GATHER_ROWS,
+               "combine_in_down": N.MOE_PLAN_COMBINE_IN_DOWN,
+               "fused_projections": N.MOE_PLAN_FUSED_PROJECTIONS}
+
+
+def plan_flags(cfg: N.MoeConfig) -> set:
+    """moe_plan_flags: the names of the kernel-path choices a forward call of
+    this layer makes (under the current tuning overrides)."""
+    f = ctypes.c_uint32(0)
+    N.check(N.lib().moe_plan_flags(ctypes.byref(cfg), ctypes.byref(f)), "moe_plan_flags")
+    return {name for name, bit in _PLAN_FLAGS.items() if f.value & bit}
+
+
 def launch_count(cfg: N.MoeConfig, fp8: bool = False) -> int:
     n = ctypes.c_int32(0)
     fn = N.lib().moe_launch_count_fp8 if fp8 else N.lib().moe_launch_count
@@ -223,7 +239,7 @@ _TUNE_KNOBS = {"router": N.MOE_TUNE_ROUTER, "gather": N.MOE_TUNE_GATHER,
                "tile_n_up": N.MOE_TUNE_TILE_N_UP, "tile_n_down": N.MOE_TUNE_TILE_N_DOWN,
                "partial_a_rows": N.MOE_TUNE_PARTIAL_A_ROWS,
                "mma_m64": N.MOE_TUNE_MMA_M64, "fused_combine": N.MOE_TUNE_FUSED_COMBINE,
-               "cluster": N.MOE_TUNE_CLUSTER}
+               "cluster": N.MOE_TUNE_CLUSTER, "fused_proj": N.MOE_TUNE_FUSED_PROJ}
 _ROUTERS = {"simt": N.MOE_ROUTER_SIMT, "fused": N.MOE_ROUTER_FUSED, "tc": N.MOE_ROUTER_TC}
 
 

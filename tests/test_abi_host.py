@@ -119,14 +119,30 @@ def test_workspace_sizes(name):
     # (plus a row copy unless the up projection gathers rows: Mixtral copies),
     # one launch with the row copy inside for bf16 layers with 64 < E <= 256
     # and k <= 8 (DeepSeek-V3- and gpt-oss-shaped), else three (logits, top-k,
-    # permute: the float32 toy layer); two projections; the combine unless a
-    # top-1 bf16 layer without a shared expert folds it into the down
-    # projection (the other bf16 layers do so only on request)
-    expected = {"toy": 6, "switch": 3, "mixtral": 5, "dsv3": 4, "gptoss": 4}
+    # permute: the float32 toy layer); two projections, or one launch for
+    # both (by default the Switch layer's form; every compiled form on
+    # request); the combine unless a top-1 bf16 layer without a shared expert
+    # folds it into the down projection (the other bf16 layers do so only on
+    # request)
+    expected = {"toy": 6, "switch": 2, "mixtral": 5, "dsv3": 4, "gptoss": 4}
     with L.tuning(fused_combine=1):
-        fused = {"toy": 6, "switch": 3, "mixtral": 4, "dsv3": 3, "gptoss": 3}
+        fused = {"toy": 6, "switch": 2, "mixtral": 4, "dsv3": 3, "gptoss": 3}
         assert L.launch_count(cfg) == fused[name]
+    with L.tuning(fused_proj=0):
+        two = {"toy": 6, "switch": 3, "mixtral": 5, "dsv3": 4, "gptoss": 4}
+        assert L.launch_count(cfg) == two[name]
+        assert "fused_projections" not in L.plan_flags(cfg)
+    with L.tuning(fused_proj=1):
+        one = {"toy": 6, "switch": 2, "mixtral": 4, "dsv3": 3, "gptoss": 3}
+        assert L.launch_count(cfg) == one[name]
+        assert ("fused_projections" in L.plan_flags(cfg)) == (name != "toy")
     assert L.launch_count(cfg) == expected[name]
+    flags = L.plan_flags(cfg)
+    route = {"toy": set(), "switch": {"route_one_launch", "gather_rows", "combine_in_down",
+                                      "fused_projections"},
+             "mixtral": {"route_one_launch"}, "dsv3": {"route_cluster"},
+             "gptoss": {"route_cluster", "gather_rows"}}
+    assert flags == route[name], flags
 
 
 def _rc_size(cfg):

@@ -141,3 +141,17 @@ def test_cpu_baseline_and_routing_block_on_the_toy_layer():
     idx[0] = idx[0].flip(0)                      # a swapped order counts as a flip
     r = bench.routing_parity(inp, idx)
     assert r["flipped_tokens"] == 1
+
+
+def test_fused_projections_count_as_one_kernel():
+    """With the up and down projections in one launch, the "up" kernel's
+    algorithmic bytes and FLOPs are the two projections' sums and "down" is
+    empty; the layer's figures do not change."""
+    s = W.SWITCH
+    kept = [0] * 64
+    kept[3], kept[7] = 80, 50
+    two, lay2 = bench.accounting(s, kept, combine_in_down=True)
+    one, lay1 = bench.accounting(s, kept, combine_in_down=True, fused=True)
+    assert one["up"]["bytes"] == two["up"]["bytes"] + two["down"]["bytes"]
+    assert one["up"]["flops"] == two["up"]["flops"] + two["down"]["flops"]
+    assert one["down"]["bytes"] == 0 and lay1 == lay2

@@ -580,3 +580,43 @@ def test_wide_router_agrees_with_split_router():
     g = (wide.topk_w - split.topk_w)[same].abs().max().item()
     assert g < 1e-5, g
     check_layer(inp, split)
+
+
+# ---------------------------------------------------------------- up + down in one launch
+FUSED_CASES = [
+    # (shape, tile widths forced so that a compiled fused form applies, one launch?)
+    (SMALL[0], dict(tile_n_up=128, tile_n_down=256), True),    # SwiGLU, TMA rows
+    (SMALL[2], dict(tile_n_up=128, tile_n_down=192), True),    # + shared expert, sigmoid gates
+    (SMALL[1], dict(tile_n_up=256, tile_n_down=192), True),    # ReLU top-1: gathered rows, combine in down
+    (ROUTE_WIDE[0], dict(tile_n_up=128, tile_n_down=256), True),  # cluster router, shared expert, drops
+    (ROUTE_WIDE[3], dict(tile_n_up=128, tile_n_down=192), False),  # ReLU k = 4: no compiled form
+    (DECODE[1], dict(tile_n_up=96, tile_n_down=96), True),     # decode batch, E = 256, shared expert
+    (ONE_LAUNCH[0], dict(tile_n_up=256, tile_n_down=256), False),  # ReLU rows by TMA: not compiled
+    # 512 up and 128 down tiles on at most 148 CTAs: several of each per CTA
+    (LayerShape("fused_many_tiles", 76, T=4096, d=512, E=16, k=2, f=1024, act=SW, gate=TOPK,
+                dtype="bf16", capacity_factor=1.25),
+     dict(tile_n_up=128, tile_n_down=256), True),
+]
+
+
+@pytest.mark.parametrize("case", FUSED_CASES, ids=lambda c: c[0].name)
+def test_fused_projections_match_two_launches_bitwise(case):
+    """The up and down projections as one persistent launch (down tiles wait
+    for their M tile's up tiles through counters) give y bit for bit equal to
+    the two launches, and pass the oracle comparison; the counters are back at
+    zero afterwards (a second call on the same workspace agrees)."""
+    shape, tiles, expect = case
+    inp = W.make_inputs(shape, "cuda", seed=28)
+    cfg = L.config_for(shape)
+    with L.tuning(fused_proj=1, **tiles):
+        fused = "fused_projections" in L.plan_flags(cfg)
+        assert fused == expect, L.plan_flags(cfg)
+        ws = L.alloc_workspace(cfg)
+        _, one = run_gpu(inp, cfg, ws)
+        _, again = run_gpu(inp, cfg, ws)
+        with L.tuning(fused_proj=0):
+            assert "fused_projections" not in L.plan_flags(cfg)
+            _, two = run_gpu(inp, cfg)
+    assert torch.equal(one.y, two.y)
+    assert torch.equal(again.y, one.y)
+    check_layer(inp, one)
