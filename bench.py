@@ -682,6 +682,8 @@ def measure_targets(stream, peaks, peak_kind):
         m = measure_layer(shape, K, 5, stream)
         acc = m["acc"]
         roof = roofline_for(stage, acc, m["stage_ms"][stage], peaks, peak_kind, m["fp8"])
+        if m["fused"] and stage == "up":
+            roof["kernel"] = "up+down (one launch)"
         ent = {"target": target, "steps": K, "ms_per_step": round(m["ms_step"], 5),
                "tokens_per_s": round(shape.T / (m["ms_step"] / 1e3), 1),
                "stage_ms": {s: round(v, 5) for s, v in m["stage_ms"].items()},
@@ -689,8 +691,10 @@ def measure_targets(stream, peaks, peak_kind):
                "clocks": m["clocks"]}
         if shape.T <= 256:
             # decode: the active experts' gate/up weights streamed by the up
-            # projection, over its duration
-            gbs = m["layer"]["w_up"] / (m["stage_ms"][stage] / 1e3) / 1e9
+            # projection, over its duration (with both projections in one
+            # launch: all their weights, over that launch)
+            w = m["layer"]["w_up"] + (m["layer"]["w_dn"] if m["fused"] else 0)
+            gbs = w / (m["stage_ms"][stage] / 1e3) / 1e9
             ent["weight_stream_gbs"] = round(gbs, 1)
             ent["weight_stream_frac"] = round(gbs / peaks["hbm_gbs"], 4)
         out[name] = ent
