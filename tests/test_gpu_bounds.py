@@ -1,9 +1,10 @@
 """The bounds-checked build (libmoe_check.so: every index routing produces is
 range-tested on the device before the access it drives; a failure is recorded
 as MOE_ERR_BOUNDS and the access skipped, never a trap).  Over the parity
-shapes -- ragged tiles, capacity drops, many experts, every routing path, the
-decode batches and a full-size layer -- it must report no out-of-range index
-and still match the oracle."""
+shapes -- ragged tiles, capacity drops, many experts, every routing path
+(including the cluster router for 64 < E <= 256), the decode batches, the
+projections as one launch and a full-size layer -- it must report no
+out-of-range index and still match the oracle."""
 import pytest
 import torch
 
@@ -16,7 +17,7 @@ import test_gpu_parity as TP
 
 pytestmark = pytest.mark.gpu
 
-SHAPES = TP.SMALL + TP.ONE_LAUNCH + TP.DECODE
+SHAPES = TP.SMALL + TP.ONE_LAUNCH + TP.DECODE + TP.ROUTE_WIDE
 
 
 @pytest.fixture
@@ -60,3 +61,15 @@ def test_checked_build_full_switch_layer(checked_library):
     assert rep["dropped"] > 0
     del inp, out, ws
     torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("case", TP.FUSED_CASES, ids=lambda c: c[0].name)
+def test_checked_build_on_the_one_launch_projections(checked_library, case):
+    shape, tiles, _ = case
+    inp = W.make_inputs(shape, "cuda", seed=29)
+    with L.tuning(fused_proj=1, **tiles):
+        cfg = L.config_for(shape)
+        ws = L.alloc_workspace(cfg)
+        _, out = run_gpu(inp, cfg, ws)
+    assert L.check_status(ws) == N.MOE_OK
+    check_layer(inp, out)
