@@ -2,7 +2,7 @@
 """Throughput of the B300 MoE layer forward pass (tokens/s), one JSON line.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl b300|reference]
-                    [--workload dsv3|switch|mixtral|gptoss<T>|toy|<name>_fp8]
+                    [--workload dsv3|switch|mixtral|gptoss<T>|toy|<name>_fp8|<name>_fp8all]
                     [--no-targets] [--no-cpu-baseline] [--no-e2e]
 
 The default workload is the largest single-GPU layer, the DeepSeek-V3-shaped
@@ -126,8 +126,8 @@ def accounting(shape, kept, combine_in_down=False, fused=False):
     projections are one launch: its figures are their sum, under "up".
 
     "bytes" counts only what the definition must move: the weights of the
-    experts with at least one kept row (e4m3 gate/up weights at one byte plus a
-    float32 scale per channel), the router weights, the kernel's input rows of
+    experts with at least one kept row (e4m3 gate/up, and with w2_fp8 down,
+    weights at one byte plus a float32 scale per channel), the router weights, the kernel's input rows of
     x and the layer's outputs.  Intermediates that this implementation stores
     between kernels (the expert-ordered row copy, h, the expert outputs o, the
     float32 logits of the split router) are reported apart as "extra"."""
@@ -141,7 +141,8 @@ def accounting(shape, kept, combine_in_down=False, fused=False):
     fp8 = getattr(shape, "w_fp8", False)
     w_el = 1 if fp8 else el                      # bytes per gate/up weight
     w_up = active * m_up * f * (d * w_el + (4 if fp8 else 0)) + S * 2 * fs * d * el
-    w_dn = active * d * f * el + S * d * fs * el
+    fp8_dn = getattr(shape, "w2_fp8", False)
+    w_dn = active * d * (f * (1 if fp8_dn else el) + (4 if fp8_dn else 0)) + S * d * fs * el
     a_el = 1 if fp8 else el                      # bytes per up-projection input element
     h_bytes = (rows * f + S * T * fs) * el
     o_bytes = (rows + S * T) * d * el
@@ -447,7 +448,11 @@ class OracleLayer:
         else:
             w1 = _h64(inp.W1[e])
             w3 = _h64(inp.W3[e]) if inp.W3 is not None else None
-        return w1, w3, _h64(inp.W2[e])
+        if getattr(inp, "W2q", None) is not None:
+            w2 = O.dequantize_weights(inp.W2q[e].cpu().numpy(), inp.W2s[e].cpu().numpy())
+        else:
+            w2 = _h64(inp.W2[e])
+        return w1, w3, w2
 
     def estimate(self, seconds, seed=0):
         """Seconds the oracle needs for the whole layer on this batch: routing
@@ -541,7 +546,9 @@ def workload_config(shape, extra=None):
          "k": shape.k, "f": shape.f, "act": shape.act, "gate": shape.gate,
          "capacity_factor": shape.capacity_factor or None, "n_shared": shape.n_shared,
          "f_shared": shape.f_shared or None, "alpha": shape.alpha}
-    if getattr(shape, "w_fp8", False):
+    if getattr(shape, "w2_fp8", False):
+        c["expert_weights"] = "gate/up/down e4m3 + float32 channel scales"
+    elif getattr(shape, "w_fp8", False):
         c["expert_weights"] = "gate/up e4m3 + float32 channel scales, down bf16"
     if extra:
         c.update(extra)
@@ -607,7 +614,7 @@ def measure_layer(shape, K, Wm, stream, dist=None, sample_clocks=True):
     torch.cuda.synchronize()
     assert L.check_status(fwd.workspace) == 0, "device status after warm-up"
     kept = fwd.out.expert_counts.cpu().tolist()
-    flags = L.plan_flags(cfg)
+    flags = L.plan_flags(cfg, fp8)
     combine_in_down = "combine_in_down" in flags
     fused = "fused_projections" in flags
     acc, layer = accounting(shape, kept, combine_in_down, fused)
@@ -775,7 +782,7 @@ def run_b300(args):
         e2e = {"value": round(world * shape.T * K / (ms_e2e / 1e3), 1), "unit": "tokens/s",
                "h2d_bytes_per_step": io, "d2h_bytes_per_step": io + 4,
                "ms_per_step": round(ms_e2e / K, 5),
-               "api": "moe_forward_fp8_host_io_batches" if fp8 else "moe_forward_host_io_batches"}
+               "api": hio._fn.__name__}
         del hio, warm, x_h, y_h
 
     cpu = routing = None

@@ -255,6 +255,43 @@ int moe_forward_fp8_timed(const moe_config* cfg, const void* x, const void* W_r,
 int moe_launch_count_fp8(const moe_config* cfg, int32_t* launches);
 
 /*
+ * moe_forward_fp8_all -- moe_forward_fp8 with the down expert weights stored
+ * as e4m3 as well:
+ *   W2q  [E, d, f] uint8: e4m3 codes (the encoding of W1q);
+ *   W2s  [E, d] float32: one scale per output channel, so that
+ *        W2[e][n][c] = W2s[e][n] * e4m3(W2q[e][n][c]).
+ * The down projection reads h in bf16 as moe_forward_fp8 does; the codes are
+ * expanded to bf16 on chip (exactly: every e4m3 value is a bf16 value), the
+ * products accumulate in float32 and each accumulator is multiplied by its
+ * channel's scale before the bf16 rounding of the expert output.  So no
+ * rounding decision moves to the activations and the parity bar stays that
+ * of moe_forward_fp8; the down weights stream at one byte each.  Every other
+ * argument, requirement, workspace size (moe_workspace_size_fp8) and launch
+ * count (moe_launch_count_fp8) is moe_forward_fp8's; W2q and W2s 16-byte
+ * aligned, else MOE_ERR_ARG; f a multiple of 16 (a row of codes is read by
+ * TMA) and no MOE_TUNE_FUSED_COMBINE override of 1, else
+ * MOE_ERR_UNSUPPORTED.  moe_forward_fp8_all_timed takes the stage events
+ * of moe_forward_fp8_timed; moe_forward_fp8_all_host_io_batches is
+ * moe_forward_fp8_host_io_batches for this layer.
+ */
+int moe_forward_fp8_all(const moe_config* cfg, const void* x, const void* W_r,
+                        const float* logit_offset, const float* sel_bias,
+                        const uint8_t* W1q, const float* W1s, const uint8_t* W3q, const float* W3s,
+                        const uint8_t* W2q, const float* W2s, void* y, int32_t* topk_idx,
+                        float* topk_w, int32_t* expert_counts, float* aux_loss,
+                        int32_t* routed_counts, int32_t* offsets, int32_t* slot_pos,
+                        float* f_out, float* P_out, void* workspace, size_t workspace_bytes,
+                        void* stream);
+int moe_forward_fp8_all_timed(const moe_config* cfg, const void* x, const void* W_r,
+                              const float* logit_offset, const float* sel_bias,
+                              const uint8_t* W1q, const float* W1s, const uint8_t* W3q,
+                              const float* W3s, const uint8_t* W2q, const float* W2s, void* y,
+                              int32_t* topk_idx, float* topk_w, int32_t* expert_counts,
+                              float* aux_loss, int32_t* routed_counts, int32_t* offsets,
+                              int32_t* slot_pos, float* f_out, float* P_out, void* workspace,
+                              size_t workspace_bytes, void* stream, void* const* events);
+
+/*
  * moe_router_z_loss -- the router z-loss of a batch of router logits:
  *     z_loss[0] = (1/T) * sum_t ( log sum_e exp(scores[t, e]) )^2
  * "Mixture of Experts" (llm-tutorial ch. 11) § Why MoE is hard names the
@@ -355,6 +392,15 @@ int moe_forward_fp8_host_io_batches(const moe_config* cfg, int32_t n_batches,
                                     float* aux_loss_host, void* workspace,
                                     size_t workspace_bytes, void* stream, void* copy_in_stream,
                                     void* copy_out_stream);
+int moe_forward_fp8_all_host_io_batches(const moe_config* cfg, int32_t n_batches,
+                                        const void* const* x_host, const void* W_r,
+                                        const float* logit_offset, const float* sel_bias,
+                                        const uint8_t* W1q, const float* W1s,
+                                        const uint8_t* W3q, const float* W3s,
+                                        const uint8_t* W2q, const float* W2s,
+                                        void* const* y_host, float* aux_loss_host,
+                                        void* workspace, size_t workspace_bytes, void* stream,
+                                        void* copy_in_stream, void* copy_out_stream);
 
 /*
  * Synchronises `stream`, then reads and clears the device status word in
@@ -423,6 +469,9 @@ enum {
   MOE_PLAN_FUSED_PROJECTIONS = 32
 };
 int moe_plan_flags(const moe_config* cfg, uint32_t* flags);
+/* The same for a moe_forward_fp8 / moe_forward_fp8_all call (errors: those of
+ * moe_workspace_size_fp8). */
+int moe_plan_flags_fp8(const moe_config* cfg, uint32_t* flags);
 
 /*
  * moe_set_tuning -- process-wide override of a kernel choice, for tests and

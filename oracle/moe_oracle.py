@@ -483,13 +483,19 @@ def dequantize_weights(codes, scales) -> np.ndarray:
 
 def moe_forward_fp8(x, W_r, W1q, W1s, W3q, W3s, W2, k: int, gate_mode: str,
                     logit_offset=None, sel_bias=None, capacity_factor=None,
-                    alpha: float = 0.01, tokens=None, forced_idx=None) -> OracleResult:
+                    alpha: float = 0.01, tokens=None, forced_idx=None,
+                    W2s=None) -> OracleResult:
     """The SwiGLU layer with e4m3 gate/up weights (codes + per-channel scales):
-    routing on x, the up projection on the quantised rows of x."""
+    routing on x, the up projection on the quantised rows of x.  With W2s
+    given, W2 holds e4m3 codes [E, d, f] too and W2s [E, d] one scale per
+    output channel: the down weights are those codes times their channel's
+    scale (the activations h are not quantised)."""
     vals, scales = quantize_rows_e4m3(x)
     xq = vals * scales[:, None]
     W1 = dequantize_weights(W1q, W1s)
     W3 = dequantize_weights(W3q, W3s)
+    if W2s is not None:
+        W2 = dequantize_weights(W2, W2s)
     return moe_forward(x, W_r, W1, W2, k, ACT_SWIGLU, gate_mode, W3=W3,
                        logit_offset=logit_offset, sel_bias=sel_bias,
                        capacity_factor=capacity_factor, alpha=alpha, tokens=tokens,

@@ -42,6 +42,8 @@ EXPORTS = (
     "moe_workspace_size_fp8", "moe_forward_fp8", "moe_forward_fp8_timed", "moe_launch_count_fp8",
     "moe_set_tuning", "moe_host_io_workspace_size_fp8", "moe_forward_fp8_host_io",
     "moe_forward_host_io_batches", "moe_forward_fp8_host_io_batches", "moe_plan_flags",
+    "moe_forward_fp8_all", "moe_forward_fp8_all_timed", "moe_forward_fp8_all_host_io_batches",
+    "moe_plan_flags_fp8",
 )
 
 
@@ -118,6 +120,14 @@ def _load(path: str) -> ctypes.CDLL:
     L.moe_forward_fp8.restype = ctypes.c_int
     L.moe_forward_fp8_timed.argtypes = fp8_args + [ctypes.POINTER(P)]
     L.moe_forward_fp8_timed.restype = ctypes.c_int
+    fp8_all_args = [cfgp] + [P] * 21 + [SZ, P]
+    L.moe_forward_fp8_all.argtypes = fp8_all_args
+    L.moe_forward_fp8_all.restype = ctypes.c_int
+    L.moe_forward_fp8_all_timed.argtypes = fp8_all_args + [ctypes.POINTER(P)]
+    L.moe_forward_fp8_all_timed.restype = ctypes.c_int
+    L.moe_forward_fp8_all_host_io_batches.argtypes = ([cfgp, ctypes.c_int32] + [P] * 13
+                                                      + [SZ, P, P, P])
+    L.moe_forward_fp8_all_host_io_batches.restype = ctypes.c_int
     L.moe_launch_count_fp8.argtypes = [cfgp, I32P]
     L.moe_launch_count_fp8.restype = ctypes.c_int
     L.moe_router_z_loss.argtypes = [P, ctypes.c_int32, ctypes.c_int32, P, P]
@@ -133,6 +143,8 @@ def _load(path: str) -> ctypes.CDLL:
     L.moe_launch_count.restype = ctypes.c_int
     L.moe_plan_flags.argtypes = [cfgp, ctypes.POINTER(ctypes.c_uint32)]
     L.moe_plan_flags.restype = ctypes.c_int
+    L.moe_plan_flags_fp8.argtypes = [cfgp, ctypes.POINTER(ctypes.c_uint32)]
+    L.moe_plan_flags_fp8.restype = ctypes.c_int
     L.moe_set_tuning.argtypes = [ctypes.c_int32, ctypes.c_int32]
     L.moe_set_tuning.restype = ctypes.c_int
     L.moe_selftest_wait_timeout.argtypes = [P, SZ, ctypes.c_uint64, P]

@@ -1581,6 +1581,440 @@ tc_updown(const __grid_constant__ CUtensorMap mA, const __grid_constant__ CUtens
   }
 }
 
+// ---------------------------------------------------------------- down projection, e4m3 weights
+// o = h W2^T with W2 stored as e4m3 codes and one float32 scale per output
+// channel (W2[e][n][c] = W2s[e][n] * e4m3(W2q[e][n][c])).  The tensor cores
+// take no bf16 x e4m3 product, and quantising h would add rounding decisions
+// on activations, so the codes are expanded to bf16 on chip -- exactly: every
+// e4m3 value is a bf16 value -- and the product runs as the bf16 kernel's,
+// the channel scale multiplying the float32 accumulator in the epilogue.  The
+// weights then stream at one byte each.
+//
+// Three rings per CTA, each with its own depth: the codes (64 bytes per
+// weight row and K block, no swizzle; loaded by the code producer, the only
+// HBM stream that matters, so the deepest ring and issued ahead of the
+// previous kernel's end), the h rows (bf16, 128-byte swizzle; loaded by the
+// A producer, mostly L2 hits) and the expanded bf16 weight tiles (written by
+// four converter warps in the layout the MMA descriptors read).  A code
+// stage is freed as soon as the converters have read it, so the code ring
+// does not wait for the tensor cores; the MMA's commits free the A and bf16
+// stages.
+template <int BNH, int EPI>
+struct F8wCfg {
+  static constexpr int A_BYTES = kTcBM * 128;
+  static constexpr int B_BYTES = BNH * 128;       // expanded weights, bf16
+  static constexpr int R_BYTES = BNH * 64;        // codes
+  static constexpr int AST = 4;
+  static constexpr int BST = 2;
+  static constexpr int RING_BUDGET = 208 * 1024;
+  static constexpr int CST_FIT = (RING_BUDGET - AST * A_BYTES - BST * B_BYTES) / R_BYTES;
+  static constexpr int CST = CST_FIT > 12 ? 12 : CST_FIT;
+  static constexpr int R_OFF = 0;
+  static constexpr int A_OFF = CST * R_BYTES;
+  static constexpr int B_OFF = A_OFF + AST * A_BYTES;
+  static constexpr int RING_BYTES = B_OFF + BST * B_BYTES;
+  static constexpr int TMEM_COLS = pow2_at_least(2 * BNH);
+  static constexpr int EPIW = 4;
+  static constexpr int CONVW = 4;
+  static constexpr int EPI0 = 2;
+  static constexpr int CONV0 = EPI0 + EPIW;
+  static constexpr int APROD = CONV0 + CONVW;     // the A producer's warp
+  static constexpr int THREADS = (APROD + 1) * 32;
+  static constexpr int NBARS = 2 * (CST + AST + BST) + 5;
+  static constexpr int BAR_BYTES = 8 * NBARS + 16;
+  static constexpr int SCHED_INTS = 4 * (kMaxE + 2);
+  static constexpr int SMEM = 1024 + RING_BYTES + BAR_BYTES + 4 * SCHED_INTS;
+  static constexpr uint32_t IDESC = idesc_bf16_f32(kTcBM, BNH);
+  static constexpr uint32_t IDESC64 = idesc_bf16_f32(64, BNH);
+  static_assert(BNH % 32 == 0 && BNH <= 256, "tile width");
+  static_assert(CST >= 4, "code ring depth");
+  static_assert(R_BYTES % 1024 == 0 && A_BYTES % 1024 == 0 && B_BYTES % 1024 == 0,
+                "swizzled tiles start on 1024-byte boundaries");
+  static_assert(SMEM <= 227 * 1024, "shared memory");
+};
+
+// Four e4m3 codes (one 32-bit word, lowest byte first) as two bf16 pairs
+// (codes 0, 1 and codes 2, 3; lower code in the lower half), exactly, on the
+// integer and FMA pipes.  A byte permute spreads each code into its own
+// sign-extended 16-bit half; shifted left by 4 and masked, the half keeps the
+// sign in bit 15 and the code's 4 exponent and 3 mantissa bits in bits 10..4:
+// the bf16 whose value is the code's value times 2^-120 (the bf16 exponent is
+// the e4m3 one, bias 127 instead of 7; an e4m3 subnormal, exponent 0, lands
+// on the bf16 subnormal of the same mantissa).  One bf16 multiply by 2^120
+// (exact: every e4m3 value is a normal bf16 value) gives the value.  The NaN
+// codes 0x7F / 0xFF come out as +-480.
+__device__ __forceinline__ uint2 e4m3x4_to_bf16x4(uint32_t w) {
+  uint32_t lo, hi;
+  asm("prmt.b32 %0, %1, 0, 0x9180;" : "=r"(lo) : "r"(w));   // s(c1) c1 s(c0) c0
+  asm("prmt.b32 %0, %1, 0, 0xB3A2;" : "=r"(hi) : "r"(w));   // s(c3) c3 s(c2) c2
+  lo = (lo << 4) & 0x87F087F0u;
+  hi = (hi << 4) & 0x87F087F0u;
+  uint2 r;
+  asm("fma.rn.bf16x2 %0, %1, %2, %3;" : "=r"(r.x) : "r"(lo), "r"(0x7B807B80u), "r"(0x80008000u));
+  asm("fma.rn.bf16x2 %0, %1, %2, %3;" : "=r"(r.y) : "r"(hi), "r"(0x7B807B80u), "r"(0x80008000u));
+  return r;
+}
+
+// Epilogue of the e4m3-weight down projection: the accumulator times the
+// output channel's scale, then as epilogue_tile (bf16 o rows, or the top-1
+// combine y = bf16(g * value)).
+template <int BNH, int EPI>
+__device__ __forceinline__ void epilogue_tile_f8w(const TcArgs& a, const TileInfo& ti,
+                                                  uint32_t t_row, size_t orow, bool row_ok,
+                                                  float gate, int c_lo, int c_hi) {
+#pragma unroll 1
+  for (int c = c_lo; c < c_hi; c += 32) {
+    uint32_t r0[32];
+    tmem_ld32(t_row + c, r0);
+    tmem_ld_wait();
+    const int col = ti.n0 + c;
+    __nv_bfloat16* out =
+        static_cast<__nv_bfloat16*>(EPI == EPI_COMBINE1 ? a.y : a.out);
+    const int ld = EPI == EPI_COMBINE1 ? a.ld_y : a.ld_out;
+    __nv_bfloat16* dst = out + orow * ld + col;
+    const float* cs = a.b0_scale + (size_t)ti.seg * a.N;
+    uint32_t pk[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      const int cc = col + 2 * i;
+      const float s0 = cc < ti.N ? __ldg(cs + cc) : 0.f;
+      const float s1 = cc + 1 < ti.N ? __ldg(cs + cc + 1) : 0.f;
+      float v0 = __uint_as_float(r0[2 * i]) * s0, v1 = __uint_as_float(r0[2 * i + 1]) * s1;
+      if (EPI == EPI_COMBINE1) {
+        v0 = fmaf(gate, v0, 0.f);
+        v1 = fmaf(gate, v1, 0.f);
+      }
+      __nv_bfloat162 b2 = __floats2bfloat162_rn(v0, v1);
+      pk[i] = *reinterpret_cast<uint32_t*>(&b2);
+    }
+    if (!row_ok) {
+    } else if (col + 32 <= ti.N) {
+#pragma unroll
+      for (int v = 0; v < 4; ++v)
+        reinterpret_cast<uint4*>(dst)[v] =
+            make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
+    } else {
+#pragma unroll
+      for (int i = 0; i < 32; ++i) {
+        if (col + i < ti.N) {
+          const uint32_t w = pk[i >> 1];
+          reinterpret_cast<uint16_t*>(dst)[i] =
+              (i & 1) ? static_cast<uint16_t>(w >> 16) : static_cast<uint16_t>(w);
+        }
+      }
+    }
+  }
+}
+
+template <int BNH, int EPI>
+__global__ void __launch_bounds__(F8wCfg<BNH, EPI>::THREADS, 1)
+tc_down_f8w(const __grid_constant__ CUtensorMap mA, const __grid_constant__ CUtensorMap mA32,
+            const __grid_constant__ CUtensorMap mW, const TcArgs a) {
+  using C = F8wCfg<BNH, EPI>;
+  static_assert(EPI == EPI_OUT16 || EPI == EPI_COMBINE1, "down epilogues");
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::RING_BYTES);
+  const uint32_t bar0 = smem_u32(bars);
+  // barriers: codes full / empty, A full / empty, bf16 tiles full / empty,
+  // accumulators full / empty, drain
+  auto cfull = [&](int s) { return bar0 + 8u * s; };
+  auto cempty = [&](int s) { return bar0 + 8u * (C::CST + s); };
+  auto afull = [&](int s) { return bar0 + 8u * (2 * C::CST + s); };
+  auto aempty = [&](int s) { return bar0 + 8u * (2 * C::CST + C::AST + s); };
+  auto bfull = [&](int s) { return bar0 + 8u * (2 * (C::CST + C::AST) + s); };
+  auto bempty = [&](int s) { return bar0 + 8u * (2 * (C::CST + C::AST) + C::BST + s); };
+  const uint32_t tb0 = bar0 + 8u * (2 * (C::CST + C::AST + C::BST));
+  auto tfull_bar = [&](int b) { return tb0 + 8u * b; };
+  auto tempty_bar = [&](int b) { return tb0 + 8u * (2 + b); };
+  const uint32_t drain_bar = tb0 + 8u * 4;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + C::NBARS);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  const uint32_t smem_base = smem_u32(smem);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  auto stage_r = [&](int s) { return smem_base + C::R_OFF + s * C::R_BYTES; };
+  auto stage_a = [&](int s) { return smem_base + C::A_OFF + s * C::A_BYTES; };
+  auto stage_b = [&](int s) { return smem_base + C::B_OFF + s * C::B_BYTES; };
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < C::CST; ++s) {
+      mbar_init(cfull(s), 1);
+      mbar_init(cempty(s), C::CONVW);
+    }
+    for (int s = 0; s < C::AST; ++s) {
+      mbar_init(afull(s), 1);
+      mbar_init(aempty(s), 1);
+    }
+    for (int s = 0; s < C::BST; ++s) {
+      mbar_init(bfull(s), C::CONVW);
+      mbar_init(bempty(s), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(tfull_bar(b), 1);
+      mbar_init(tempty_bar(b), 32 * C::EPIW);
+    }
+    mbar_init(drain_bar, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&mA);
+    tma_prefetch_desc(&mA32);
+    tma_prefetch_desc(&mW);
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_slot), C::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  // The tile schedule was written by the routing kernel, two launches back
+  // (complete before the previous grid could start this one): it is read
+  // before the wait, and the code producer streams the first stages' codes
+  // meanwhile; h (written by the previous kernel) waits.
+  int* s_tp = reinterpret_cast<int*>(smem + C::RING_BYTES + C::BAR_BYTES);
+  int* s_seg = s_tp + (kMaxE + 2);
+  int* s_mt = s_seg + (kMaxE + 2);
+  int* s_kept = s_mt + (kMaxE + 2);
+  const int nseg = a.E + a.has_shared;
+  for (int i = threadIdx.x; i <= nseg; i += blockDim.x) s_tp[i] = __ldg(a.tp + i);
+  for (int i = threadIdx.x; i < nseg; i += blockDim.x) s_mt[i] = __ldg(a.mtiles + i);
+  for (int i = threadIdx.x; i < a.E; i += blockDim.x) {
+    s_seg[i] = __ldg(a.seg_start + i);
+    s_kept[i] = __ldg(a.kept + i);
+  }
+  __syncthreads();
+  const Sched sc{s_tp, s_seg, s_mt, s_kept};
+  const int total = s_tp[nseg];
+  auto give_up = [&]() {
+    atomicOr(a.status, STATUS_TIMEOUT_GEMM);
+    *abort_flag = 1;
+  };
+  // Waits until every load this thread issued into a ring has landed: on the
+  // consumers' release of each stage's last use when all went well, else on
+  // the load itself.
+  auto drain_ring = [&](uint32_t issued, int depth, auto full, auto empty, bool ok) {
+    for (int s = 0; s < depth; ++s) {
+      if (issued > static_cast<uint32_t>(s)) {
+        const uint32_t uses = (issued - 1 - s) / depth + 1;
+        if (ok)
+          mbar_wait_sleep_bounded(empty(s), (uses - 1) & 1u, a.timeout_ns, abort_flag);
+        else
+          mbar_wait_bounded(full(s), (uses - 1) & 1u, a.timeout_ns, nullptr);
+      }
+    }
+  };
+  uint32_t npre = 0;   // code stages issued before the wait
+  if (warp == 0 && lane == 0) {
+    for (int tile = blockIdx.x; tile < total && npre < (uint32_t)C::CST; tile += gridDim.x) {
+      const TileInfo ti = decode_tile(a, sc, tile, BNH);
+      const int nk = (ti.K + 63) / 64;
+      for (int kb = 0; kb < nk && npre < (uint32_t)C::CST; ++kb, ++npre) {
+        mbar_arrive_expect_tx(cfull(npre), C::R_BYTES);
+        tma_load_3d(stage_r(npre), &mW, cfull(npre), kb * 32, ti.n0, ti.seg);
+      }
+    }
+  }
+  pdl_wait();
+  pdl_trigger();
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ---------------- code producer ----------------
+      uint32_t g = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
+        const TileInfo ti = decode_tile(a, sc, tile, BNH);
+        const int nk = (ti.K + 63) / 64;
+        for (int kb = 0; kb < nk; ++kb, ++g) {
+          if (g < npre) continue;   // in flight since the prologue
+          const int s = g % C::CST;
+          const uint32_t ph = (g / C::CST) & 1u;
+          if (!mbar_wait_sleep_bounded(cempty(s), ph ^ 1u, a.timeout_ns, abort_flag)) {
+            give_up();
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(cfull(s), C::R_BYTES);
+          tma_load_3d(stage_r(s), &mW, cfull(s), kb * 32, ti.n0, ti.seg);
+        }
+      }
+      drain_ring(g, C::CST, cfull, cempty, ok);
+    }
+  } else if (warp == C::APROD) {
+    if (lane == 0) {
+      // ---------------- A (h rows) producer ----------------
+      uint32_t g = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
+        const TileInfo ti = decode_tile(a, sc, tile, BNH);
+        const int nk = (ti.K + 63) / 64;
+        const int rows = ti.row_end - ti.a_row < kTcBM ? ti.row_end - ti.a_row : kTcBM;
+        const int a_boxes = a_real_boxes(rows, a.partial_rows);
+        const uint32_t a_bytes = a_stage_bytes(a_boxes, C::A_BYTES);
+        for (int kb = 0; kb < nk; ++kb, ++g) {
+          const int s = g % C::AST;
+          const uint32_t ph = (g / C::AST) & 1u;
+          if (!mbar_wait_sleep_bounded(aempty(s), ph ^ 1u, a.timeout_ns, abort_flag)) {
+            give_up();
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(afull(s), a_bytes);
+          load_a_stage(stage_a(s), &mA, &mA32, afull(s), kb * 64, ti.a_row, a_boxes);
+        }
+      }
+      drain_ring(g, C::AST, afull, aempty, ok);
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ---------------- MMA issuer ----------------
+      uint32_t g = 0;
+      int it = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x, ++it) {
+        const TileInfo ti = decode_tile(a, sc, tile, BNH);
+        const int nk = (ti.K + 63) / 64;
+        const int ab = it & 1;
+        const uint32_t aph = (it >> 1) & 1;
+        if (!mbar_wait_sleep_bounded(tempty_bar(ab), aph ^ 1u, a.timeout_ns, abort_flag)) {
+          give_up();
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + ab * BNH;
+        const uint32_t idesc = ti.m64 ? C::IDESC64 : C::IDESC;
+        for (int kb = 0; kb < nk; ++kb, ++g) {
+          const int sa = g % C::AST, sb = g % C::BST;
+          // the stage's h rows have landed and its weights are expanded
+          if (!mbar_wait_sleep_bounded(afull(sa), (g / C::AST) & 1u, a.timeout_ns, abort_flag) ||
+              !mbar_wait_sleep_bounded(bfull(sb), (g / C::BST) & 1u, a.timeout_ns, abort_flag)) {
+            give_up();
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)
+            tc_mma_bf16(d_tmem, smem_desc_k128(stage_a(sa) + kk * 32),
+                        smem_desc_k128(stage_b(sb) + kk * 32), idesc,
+                        (kb != 0 || kk != 0) ? 1u : 0u);
+          tc_commit(aempty(sa));
+          tc_commit(bempty(sb));
+        }
+        if (!ok) break;
+        tc_commit(tfull_bar(ab));
+      }
+      if (!ok) {
+        tc_commit(drain_bar);
+        mbar_wait_bounded(drain_bar, 0, a.timeout_ns, nullptr);
+      }
+    }
+  } else if (warp >= C::CONV0) {
+    // ---------------- converter warps ----------------
+    // item i of a stage: weight row i / 8, 16-byte chunk i % 8 of its bf16
+    // row (eight codes); the bf16 tile is written in the 128-byte swizzle
+    // (chunk c of row n at n*128 + (c ^ (n & 7))*16)
+    const int ct = (warp - C::CONV0) * 32 + lane;
+    uint32_t g = 0;
+    bool ok = true;
+    for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
+      const TileInfo ti = decode_tile(a, sc, tile, BNH);
+      const int nk = (ti.K + 63) / 64;
+      for (int kb = 0; kb < nk; ++kb, ++g) {
+        const int sr = g % C::CST, sb = g % C::BST;
+        // every lane waits (it reads what the TMA wrote and overwrites what
+        // the tensor cores read)
+        const bool okl =
+            mbar_wait_sleep_bounded(cfull(sr), (g / C::CST) & 1u, a.timeout_ns, abort_flag) &&
+            mbar_wait_sleep_bounded(bempty(sb), ((g / C::BST) & 1u) ^ 1u, a.timeout_ns,
+                                    abort_flag);
+        if (!__all_sync(0xffffffffu, okl)) {
+          if (lane == 0) give_up();
+          ok = false;
+          break;
+        }
+        const uint8_t* raw = smem + C::R_OFF + sr * C::R_BYTES;
+        uint8_t* bt = smem + C::B_OFF + sb * C::B_BYTES;
+        constexpr int PER = (BNH * 8) / (C::CONVW * 32);
+        static_assert(PER * C::CONVW * 32 == BNH * 8, "items per converter thread");
+        uint2 codes[PER];
+#pragma unroll
+        for (int j = 0; j < PER; ++j) {
+          const int i = ct + j * 32 * C::CONVW;
+          codes[j] = *reinterpret_cast<const uint2*>(raw + (i >> 3) * 64 + (i & 7) * 8);
+        }
+        // the codes are in registers: the code stage can be refilled
+        __syncwarp();
+        if (lane == 0) mbar_arrive(cempty(sr));
+#pragma unroll
+        for (int j = 0; j < PER; ++j) {
+          const int i = ct + j * 32 * C::CONVW;
+          const int n = i >> 3, c = i & 7;
+          const uint2 b01 = e4m3x4_to_bf16x4(codes[j].x), b23 = e4m3x4_to_bf16x4(codes[j].y);
+          *reinterpret_cast<uint4*>(bt + n * 128 + ((c ^ (n & 7)) << 4)) =
+              make_uint4(b01.x, b01.y, b23.x, b23.y);
+        }
+        fence_proxy_async_smem();   // the tensor cores read what these threads wrote
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bfull(sb));
+      }
+    }
+  } else {
+    // ---------------- epilogue (four warps, one per TMEM lane quarter) ----------------
+    const int q = warp & 3;
+    const int row_in_tile = q * 32 + lane;
+    if constexpr (EPI == EPI_COMBINE1) {
+      // a dropped token (key_row < 0, top-1) gets y = 0
+      uint4* y = static_cast<uint4*>(a.y);
+      const int nvec = a.ld_y * 2 / 16;
+      const int gw = blockIdx.x * C::EPIW + (warp - C::EPI0), nw = gridDim.x * C::EPIW;
+      for (int t = gw; t < a.T_tokens; t += nw) {
+        if (__ldg(a.key_row + t) < 0)
+          for (int c = lane; c < nvec; c += 32) y[(size_t)t * nvec + c] = make_uint4(0, 0, 0, 0);
+      }
+    }
+    int it = 0;
+    for (int tile = blockIdx.x; tile < total; tile += gridDim.x, ++it) {
+      const TileInfo ti = decode_tile(a, sc, tile, BNH);
+      const int rit = !ti.m64 ? row_in_tile : (lane < 16 ? q * 16 + lane : kTcBM);
+      const size_t orow = static_cast<size_t>(ti.a_row + rit);
+      bool row_ok = rit < kTcBM && ti.a_row + rit < ti.row_end;
+      if (row_ok) row_ok = in_bounds((int)orow < a.R_cap, a.status);
+      const int ab = it & 1;
+      const uint32_t aph = (it >> 1) & 1;
+      if (!mbar_wait_sleep_bounded(tfull_bar(ab), aph, a.timeout_ns, abort_flag)) {
+        give_up();
+        break;
+      }
+      tc_fence_after();
+      const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + ab * BNH;
+      if constexpr (EPI == EPI_COMBINE1) {
+        int tok = row_ok ? __ldg(a.row_token + orow) : 0;
+        const bool tok_ok = row_ok && in_bounds(tok >= 0 && tok < a.T_tokens, a.status);
+        if (!tok_ok) tok = 0;
+        const float gt = tok_ok ? __ldg(a.gate + tok) : 0.f;
+        epilogue_tile_f8w<BNH, EPI>(a, ti, t_row, (size_t)tok, tok_ok, gt, 0, BNH);
+      } else {
+        epilogue_tile_f8w<BNH, EPI>(a, ti, t_row, orow, row_ok, 1.f, 0, BNH);
+      }
+      tc_fence_before();
+      mbar_arrive(tempty_bar(ab));
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, C::TMEM_COLS);
+  }
+}
+
 // ---------------------------------------------------------------- host side
 struct TcMaps {
   CUtensorMap A, A_sh, A32, A32_sh, B0, B1, B0_sh, B1_sh;
@@ -1712,6 +2146,40 @@ static cudaError_t dispatch_down(int bn, bool combine1, bool combinek, const TcM
 
 constexpr uint64_t kGemmTimeoutNs = 2000000000ull;   // 2 s
 
+// ---- the down projection with e4m3 weights ----
+template <int BNH, int EPI>
+static cudaError_t run_f8w(const TcMaps& m, const CUtensorMap& mW, const TcArgs& a, int grid,
+                           cudaStream_t st) {
+  using C = F8wCfg<BNH, EPI>;
+  static std::atomic<uint64_t> attr_done{0};
+  auto kern = tc_down_f8w<BNH, EPI>;
+  cudaError_t e = smem_attr_once(kern, C::SMEM, attr_done);
+  if (e != cudaSuccess) return e;
+  return launch_pdl(kern, dim3(grid), dim3(C::THREADS), C::SMEM, st, m.A, m.A32, mW, a);
+}
+
+static cudaError_t dispatch_down_f8w(int bn, bool combine1, const TcMaps& m, const CUtensorMap& mW,
+                                     const TcArgs& a, int grid, cudaStream_t st) {
+  if (combine1) {
+    switch (bn) {
+      case 256: return run_f8w<256, EPI_COMBINE1>(m, mW, a, grid, st);
+      case 192: return run_f8w<192, EPI_COMBINE1>(m, mW, a, grid, st);
+      case 128: return run_f8w<128, EPI_COMBINE1>(m, mW, a, grid, st);
+      case 96: return run_f8w<96, EPI_COMBINE1>(m, mW, a, grid, st);
+      case 64: return run_f8w<64, EPI_COMBINE1>(m, mW, a, grid, st);
+    }
+    return cudaErrorInvalidValue;
+  }
+  switch (bn) {
+    case 256: return run_f8w<256, EPI_OUT16>(m, mW, a, grid, st);
+    case 192: return run_f8w<192, EPI_OUT16>(m, mW, a, grid, st);
+    case 128: return run_f8w<128, EPI_OUT16>(m, mW, a, grid, st);
+    case 96: return run_f8w<96, EPI_OUT16>(m, mW, a, grid, st);
+    case 64: return run_f8w<64, EPI_OUT16>(m, mW, a, grid, st);
+  }
+  return cudaErrorInvalidValue;
+}
+
 // ---- up + down in one launch: the compiled forms ----
 template <class PU, class PD, int ASU>
 static cudaError_t run_ud(const TcMaps& mu, const TcMaps& md, const TcArgs& au, const TcArgs& ad,
@@ -1793,7 +2261,8 @@ bool updown_default(const Plan& p) {
 cudaError_t launch_experts_tc(const Plan& p, const void* x, const void* W1, const void* W3,
                               const void* W2, const void* Ws1, const void* Ws3, const void* Ws2,
                               void* ws, cudaStream_t st, cudaEvent_t mid_event, void* y,
-                              const float* topk_w, const float* W1s, const float* W3s) {
+                              const float* topk_w, const float* W1s, const float* W3s,
+                              const float* W2s) {
   const moe_config& c = p.cfg;
   char* w = static_cast<char*>(ws);
   const Meta meta = meta_ptrs(p, ws);
@@ -1923,6 +2392,19 @@ cudaError_t launch_experts_tc(const Plan& p, const void* x, const void* W1, cons
   ad.out_sh = sh ? static_cast<void*>(w + p.ws.os) : nullptr;
   ad.ld_out_sh = sh ? c.d : 0;
   const int grid_dn = p.max_tiles_dn < p.num_sms ? p.max_tiles_dn : p.num_sms;
+  if (W2s != nullptr) {
+    // e4m3 down weights: the codes by 64-byte tiles, expanded on chip
+    if (sh || p.fused || p.combine_k) return cudaErrorInvalidValue;
+    CUtensorMap mW;
+    if (!encode_3d_codes(&mW, W2, c.E, c.d, c.f, p.dn_bn)) return cudaErrorInvalidValue;
+    TcArgs a8 = ad;
+    a8.b0_scale = W2s;
+    cudaError_t e = p.fp8 ? dispatch_up_f8(p.up_bn, mu, au, grid_up, st)
+                          : dispatch_up(as, p.up_bn, c.act, mu, au, grid_up, st, p.cluster2_up);
+    if (e != cudaSuccess) return e;
+    if (mid_event && (e = cudaEventRecord(mid_event, st)) != cudaSuccess) return e;
+    return dispatch_down_f8w(p.dn_bn, p.combine_in_down, md, mW, a8, grid_dn, st);
+  }
   if (p.fused) {
     // both projections in one launch; the up stage event then covers both
     UdArgs ud;

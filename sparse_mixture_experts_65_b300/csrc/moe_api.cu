@@ -386,6 +386,7 @@ struct Tensors {
   int32_t *routed_counts, *offsets, *slot_pos;
   float *f_out, *P_out;
   const float *W1s = nullptr, *W3s = nullptr;   // fp8 gate/up weights: column scales
+  const float* W2s = nullptr;   // fp8 down weights too (W2 holds e4m3 codes): column scales
 };
 
 static int check_tensors(const moe_config& c, const Tensors& t, bool route_only) {
@@ -401,6 +402,7 @@ static int check_tensors(const moe_config& c, const Tensors& t, bool route_only)
   if (c.act == MOE_ACT_SWIGLU ? (!t.W3 || !aligned16(t.W3)) : t.W3 != nullptr) return MOE_ERR_ARG;
   if ((t.W1s != nullptr) != (t.W3s != nullptr)) return MOE_ERR_ARG;
   if (t.W1s && (!aligned16(t.W1s) || !aligned16(t.W3s))) return MOE_ERR_ARG;
+  if (t.W2s && (!t.W1s || !aligned16(t.W2s))) return MOE_ERR_ARG;
   if (c.n_shared) {
     if (!t.Ws1 || !t.Ws3 || !t.Ws2) return MOE_ERR_ARG;
     if (!aligned16(t.Ws1) || !aligned16(t.Ws3) || !aligned16(t.Ws2)) return MOE_ERR_ARG;
@@ -457,6 +459,10 @@ static int forward_impl(const moe_config* cfg, const Tensors& t, void* ws, size_
     if (rc != MOE_OK) return rc;
   }
   const moe_config& c = *cfg;
+  // e4m3 down weights: rows of f code bytes are TMA rows (16-byte multiples);
+  // the down kernel writes the expert outputs or combines a top-1 layer in
+  // its epilogue, so the k-slot combine override has no form with them
+  if (t.W2s && (c.f % 16 || p.combine_k || p.fused)) return MOE_ERR_UNSUPPORTED;
   if (c.T == 0) return zero_outputs(c, t, st);
 
   if ((rc = record(events, MOE_STAGE_ROUTER, st)) != MOE_OK) return rc;
@@ -497,7 +503,7 @@ static int forward_impl(const moe_config* cfg, const Tensors& t, void* ws, size_
   cudaEvent_t mid = events ? static_cast<cudaEvent_t>(events[MOE_STAGE_DOWN]) : nullptr;
   if (p.tc)
     MOE_TRY_CUDA(launch_experts_tc(p, t.x, t.W1, t.W3, t.W2, t.Ws1, t.Ws3, t.Ws2, ws, st, mid,
-                                   t.y, t.topk_w, t.W1s, t.W3s));
+                                   t.y, t.topk_w, t.W1s, t.W3s, t.W2s));
   else
     MOE_TRY_CUDA(launch_experts_simt(p, t.x, t.W1, t.W3, t.W2, t.Ws1, t.Ws3, t.Ws2, ws, st, mid));
   if ((rc = record(events, MOE_STAGE_COMBINE, st)) != MOE_OK) return rc;
@@ -686,6 +692,36 @@ int moe_forward_fp8(const moe_config* cfg, const void* x, const void* W_r,
                                nullptr);
 }
 
+int moe_forward_fp8_all_timed(const moe_config* cfg, const void* x, const void* W_r,
+                              const float* logit_offset, const float* sel_bias,
+                              const uint8_t* W1q, const float* W1s, const uint8_t* W3q,
+                              const float* W3s, const uint8_t* W2q, const float* W2s, void* y,
+                              int32_t* topk_idx, float* topk_w, int32_t* expert_counts,
+                              float* aux_loss, int32_t* routed_counts, int32_t* offsets,
+                              int32_t* slot_pos, float* f_out, float* P_out, void* workspace,
+                              size_t workspace_bytes, void* stream, void* const* events) {
+  if (!W1s || !W3s || !W2s) return MOE_ERR_ARG;
+  Tensors t{x,  W_r, logit_offset, sel_bias, W1q,     W3q,     W2q,     nullptr,  nullptr, nullptr,
+            y,  topk_idx, topk_w, expert_counts, aux_loss, routed_counts, offsets, slot_pos,
+            f_out, P_out, W1s, W3s, W2s};
+  return forward_impl(cfg, t, workspace, workspace_bytes, static_cast<cudaStream_t>(stream),
+                      events, false, WsKind::ForwardFp8);
+}
+
+int moe_forward_fp8_all(const moe_config* cfg, const void* x, const void* W_r,
+                        const float* logit_offset, const float* sel_bias, const uint8_t* W1q,
+                        const float* W1s, const uint8_t* W3q, const float* W3s,
+                        const uint8_t* W2q, const float* W2s, void* y, int32_t* topk_idx,
+                        float* topk_w, int32_t* expert_counts, float* aux_loss,
+                        int32_t* routed_counts, int32_t* offsets, int32_t* slot_pos,
+                        float* f_out, float* P_out, void* workspace, size_t workspace_bytes,
+                        void* stream) {
+  return moe_forward_fp8_all_timed(cfg, x, W_r, logit_offset, sel_bias, W1q, W1s, W3q, W3s, W2q,
+                                   W2s, y, topk_idx, topk_w, expert_counts, aux_loss,
+                                   routed_counts, offsets, slot_pos, f_out, P_out, workspace,
+                                   workspace_bytes, stream, nullptr);
+}
+
 int moe_route(const moe_config* cfg, const void* x, const void* W_r, const float* logit_offset,
               const float* sel_bias, int32_t* topk_idx, float* topk_w, int32_t* expert_counts,
               float* aux_loss, int32_t* routed_counts, int32_t* offsets, int32_t* slot_pos,
@@ -823,6 +859,25 @@ int moe_forward_fp8_host_io_batches(const moe_config* cfg, int32_t n_batches,
                          static_cast<cudaStream_t>(copy_out_stream));
 }
 
+int moe_forward_fp8_all_host_io_batches(const moe_config* cfg, int32_t n_batches,
+                                        const void* const* x_host, const void* W_r,
+                                        const float* logit_offset, const float* sel_bias,
+                                        const uint8_t* W1q, const float* W1s,
+                                        const uint8_t* W3q, const float* W3s,
+                                        const uint8_t* W2q, const float* W2s,
+                                        void* const* y_host, float* aux_loss_host,
+                                        void* workspace, size_t workspace_bytes, void* stream,
+                                        void* copy_in_stream, void* copy_out_stream) {
+  if (!W1s || !W3s || !W2s) return MOE_ERR_ARG;
+  Tensors t{nullptr, W_r, logit_offset, sel_bias, W1q, W3q, W2q, nullptr, nullptr, nullptr,
+            nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr,
+            nullptr, W1s, W3s, W2s};
+  return host_io_batches(cfg, n_batches, x_host, y_host, aux_loss_host, t, WsKind::HostIOFp8,
+                         workspace, workspace_bytes, static_cast<cudaStream_t>(stream),
+                         static_cast<cudaStream_t>(copy_in_stream),
+                         static_cast<cudaStream_t>(copy_out_stream));
+}
+
 int moe_check_status(void* workspace, void* stream) {
   if (!workspace) return MOE_ERR_WORKSPACE;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
@@ -871,10 +926,10 @@ int moe_launch_count(const moe_config* cfg, int32_t* launches) {
   return MOE_OK;
 }
 
-int moe_plan_flags(const moe_config* cfg, uint32_t* flags) {
+static int plan_flags(const moe_config* cfg, WsKind kind, uint32_t* flags) {
   if (!flags) return MOE_ERR_ARG;
   Plan p;
-  const int rc = make_plan(cfg, WsKind::Forward, &p);
+  const int rc = make_plan(cfg, kind, &p);
   if (rc != MOE_OK) return rc;
   uint32_t f = 0;
   if (p.route_tc) f |= MOE_PLAN_ROUTE_ONE_LAUNCH;
@@ -885,6 +940,14 @@ int moe_plan_flags(const moe_config* cfg, uint32_t* flags) {
   if (p.fused) f |= MOE_PLAN_FUSED_PROJECTIONS;
   *flags = f;
   return MOE_OK;
+}
+
+int moe_plan_flags(const moe_config* cfg, uint32_t* flags) {
+  return plan_flags(cfg, WsKind::Forward, flags);
+}
+
+int moe_plan_flags_fp8(const moe_config* cfg, uint32_t* flags) {
+  return plan_flags(cfg, WsKind::ForwardFp8, flags);
 }
 
 int moe_launch_count_fp8(const moe_config* cfg, int32_t* launches) {

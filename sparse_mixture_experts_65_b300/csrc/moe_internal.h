@@ -196,7 +196,7 @@ cudaError_t launch_experts_tc(const Plan& p, const void* x, const void* W1, cons
                               const void* W2, const void* Ws1, const void* Ws3, const void* Ws2,
                               void* ws, cudaStream_t st, cudaEvent_t mid_event, void* y,
                               const float* topk_w, const float* W1s = nullptr,
-                              const float* W3s = nullptr);
+                              const float* W3s = nullptr, const float* W2s = nullptr);
 cudaError_t launch_quant_rows(const Plan& p, const void* x, void* ws, cudaStream_t st);
 // Up and down projections in one launch: compiled for this tiling and the
 // counters fit the workspace header.

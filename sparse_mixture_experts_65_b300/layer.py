@@ -81,11 +81,13 @@ _PLAN_FLAGS = {"route_one_launch": N.MOE_PLAN_ROUTE_ONE_LAUNCH,
                "fused_projections": N.MOE_PLAN_FUSED_PROJECTIONS}
 
 
-def plan_flags(cfg: N.MoeConfig) -> set:
-    """moe_plan_flags: the names of the kernel-path choices a forward call of
-    this layer makes (under the current tuning overrides)."""
+def plan_flags(cfg: N.MoeConfig, fp8: bool = False) -> set:
+    """moe_plan_flags (moe_plan_flags_fp8 with fp8): the names of the
+    kernel-path choices a forward call of this layer makes (under the current
+    tuning overrides)."""
     f = ctypes.c_uint32(0)
-    N.check(N.lib().moe_plan_flags(ctypes.byref(cfg), ctypes.byref(f)), "moe_plan_flags")
+    fn = N.lib().moe_plan_flags_fp8 if fp8 else N.lib().moe_plan_flags
+    N.check(fn(ctypes.byref(cfg), ctypes.byref(f)), "moe_plan_flags")
     return {name for name, bit in _PLAN_FLAGS.items() if f.value & bit}
 
 
@@ -152,11 +154,13 @@ def forward(cfg: N.MoeConfig, x, W_r, W1, W2, W3=None, logit_offset=None, sel_bi
 
 def forward_fp8(cfg: N.MoeConfig, x, W_r, W1q, W1s, W3q, W3s, W2, logit_offset=None,
                 sel_bias=None, out: Optional[MoeOutputs] = None,
-                workspace: Optional[torch.Tensor] = None, stream=None) -> MoeOutputs:
+                workspace: Optional[torch.Tensor] = None, stream=None,
+                W2s=None) -> MoeOutputs:
     """One call of moe_forward_fp8: e4m3 gate/up weights (uint8 codes) with
-    float32 channel scales, bf16 down weights."""
+    float32 channel scales, bf16 down weights; with W2s given, W2 is the
+    e4m3 codes of the down weights too (moe_forward_fp8_all)."""
     b = BoundForwardFp8(cfg, x, W_r, W1q, W1s, W3q, W3s, W2, logit_offset, sel_bias, out,
-                        workspace, stream)
+                        workspace, stream, W2s)
     b()
     return b.out
 
@@ -314,29 +318,41 @@ class BoundForward:
 
 
 class BoundForwardFp8(BoundForward):
-    """moe_forward_fp8 with every argument marshalled once."""
+    """moe_forward_fp8 with every argument marshalled once; with W2s given, W2
+    holds the e4m3 codes of the down weights and the call is
+    moe_forward_fp8_all."""
 
     def __init__(self, cfg: N.MoeConfig, x, W_r, W1q, W1s, W3q, W3s, W2, logit_offset=None,
                  sel_bias=None, out: Optional[MoeOutputs] = None,
-                 workspace: Optional[torch.Tensor] = None, stream=None):
+                 workspace: Optional[torch.Tensor] = None, stream=None, W2s=None):
         self.cfg = cfg
         self.out = out if out is not None else alloc_outputs(cfg, x.device, x.dtype)
         self.workspace = (workspace if workspace is not None
                           else alloc_workspace(cfg, x.device, "fp8"))
-        self._keep = (x, W_r, W1q, W1s, W3q, W3s, W2, logit_offset, sel_bias)
+        self._keep = (x, W_r, W1q, W1s, W3q, W3s, W2, W2s, logit_offset, sel_bias)
         o = self.out
-        self.args = (ctypes.byref(cfg), _ptr(x), _ptr(W_r), _ptr(logit_offset), _ptr(sel_bias),
-                     _ptr(W1q), _ptr(W1s), _ptr(W3q), _ptr(W3s), _ptr(W2),
-                     _ptr(o.y), _ptr(o.topk_idx), _ptr(o.topk_w), _ptr(o.expert_counts),
-                     _ptr(o.aux_loss), _ptr(o.routed_counts), _ptr(o.offsets), _ptr(o.slot_pos),
-                     _ptr(o.f), _ptr(o.P), _ptr(self.workspace),
-                     ctypes.c_size_t(self.workspace.numel()), _stream_handle(stream))
-        self._fwd = N.lib().moe_forward_fp8
-        self._timed = N.lib().moe_forward_fp8_timed
+        down = (_ptr(W2),) if W2s is None else (_ptr(W2), _ptr(W2s))
+        self.args = ((ctypes.byref(cfg), _ptr(x), _ptr(W_r), _ptr(logit_offset),
+                      _ptr(sel_bias), _ptr(W1q), _ptr(W1s), _ptr(W3q), _ptr(W3s)) + down
+                     + (_ptr(o.y), _ptr(o.topk_idx), _ptr(o.topk_w), _ptr(o.expert_counts),
+                        _ptr(o.aux_loss), _ptr(o.routed_counts), _ptr(o.offsets),
+                        _ptr(o.slot_pos), _ptr(o.f), _ptr(o.P), _ptr(self.workspace),
+                        ctypes.c_size_t(self.workspace.numel()), _stream_handle(stream)))
+        if W2s is None:
+            self._fwd = N.lib().moe_forward_fp8
+            self._timed = N.lib().moe_forward_fp8_timed
+        else:
+            self._fwd = N.lib().moe_forward_fp8_all
+            self._timed = N.lib().moe_forward_fp8_all_timed
 
 
 def bound_forward(cfg: N.MoeConfig, inp, stream=None, workspace=None) -> BoundForward:
-    """The bound call for a workload's inputs (fp8 gate/up weights or not)."""
+    """The bound call for a workload's inputs (fp8 gate/up weights or not;
+    fp8 down weights when the inputs carry W2q)."""
+    if getattr(inp, "W2q", None) is not None:
+        return BoundForwardFp8(cfg, inp.x, inp.W_r, inp.W1q, inp.W1s, inp.W3q, inp.W3s, inp.W2q,
+                               inp.logit_offset, inp.sel_bias, workspace=workspace, stream=stream,
+                               W2s=inp.W2s)
     if getattr(inp, "W1q", None) is not None:
         return BoundForwardFp8(cfg, inp.x, inp.W_r, inp.W1q, inp.W1s, inp.W3q, inp.W3s, inp.W2,
                                inp.logit_offset, inp.sel_bias, workspace=workspace, stream=stream)
@@ -374,7 +390,7 @@ class BoundHostIOBatches:
     of one batch overlapping the layer of another.  x_hosts / y_hosts: lists
     of pinned host tensors (a list may repeat a buffer); aux_host: a pinned
     float32 host tensor with one entry per batch.  `inp` is a workload's
-    LayerInputs (device weights, bf16 or e4m3 gate/up)."""
+    LayerInputs (device weights, bf16 or e4m3 gate/up, bf16 or e4m3 down)."""
 
     def __init__(self, cfg: N.MoeConfig, x_hosts, y_hosts, aux_host, inp, stream=None,
                  copy_in_stream=None, copy_out_stream=None,
@@ -396,7 +412,11 @@ class BoundHostIOBatches:
         tail = (self._ys, _ptr(aux_host), _ptr(self.workspace),
                 ctypes.c_size_t(self.workspace.numel()), _stream_handle(stream),
                 _stream_handle(self.copy_in), _stream_handle(self.copy_out))
-        if fp8:
+        if fp8 and getattr(inp, "W2q", None) is not None:
+            self.args = head + (_ptr(inp.W1q), _ptr(inp.W1s), _ptr(inp.W3q), _ptr(inp.W3s),
+                                _ptr(inp.W2q), _ptr(inp.W2s)) + tail
+            self._fn = N.lib().moe_forward_fp8_all_host_io_batches
+        elif fp8:
             self.args = head + (_ptr(inp.W1q), _ptr(inp.W1s), _ptr(inp.W3q), _ptr(inp.W3s),
                                 _ptr(inp.W2)) + tail
             self._fn = N.lib().moe_forward_fp8_host_io_batches

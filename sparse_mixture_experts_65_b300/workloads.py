@@ -45,6 +45,7 @@ class LayerShape:
     logit_offset_var: float = 0.0       # variance of a per-expert logit skew
     sel_bias_halfwidth: float = 0.0     # sel bias ~ U(-h, h)
     w_fp8: bool = False                 # gate/up expert weights as e4m3 codes + channel scales
+    w2_fp8: bool = False                # down expert weights as e4m3 codes + channel scales too
 
     def with_T(self, T: int) -> "LayerShape":
         return replace(self, T=T)
@@ -70,7 +71,11 @@ WORKLOADS = {w.name: w for w in (TOY, SWITCH, MIXTRAL, DSV3, GPTOSS)}
 
 def get(name: str) -> LayerShape:
     """A named workload; the suffix "_fp8" gives the same layer with e4m3
-    gate/up expert weights (SwiGLU layers)."""
+    gate/up expert weights (SwiGLU layers), "_fp8all" with e4m3 down expert
+    weights as well."""
+    if name.endswith("_fp8all"):
+        base = get(name[:-len("_fp8all")])
+        return replace(base, name=base.name + "_fp8all", w_fp8=True, w2_fp8=True)
     if name.endswith("_fp8"):
         base = get(name[:-len("_fp8")])
         return replace(base, name=base.name + "_fp8", w_fp8=True)
@@ -121,11 +126,15 @@ class LayerInputs:
     W1s: Optional[torch.Tensor] = None
     W3q: Optional[torch.Tensor] = None
     W3s: Optional[torch.Tensor] = None
+    # e4m3 down weights (W2 is None then): codes [E, d, f] uint8 and one
+    # float32 scale per output channel [E, d]
+    W2q: Optional[torch.Tensor] = None
+    W2s: Optional[torch.Tensor] = None
 
     def weight_bytes(self) -> int:
         n = 0
         for t in (self.W_r, self.W1, self.W2, self.W3, self.Ws1, self.Ws3, self.Ws2, self.W1q,
-                  self.W1s, self.W3q, self.W3s):
+                  self.W1s, self.W3q, self.W3s, self.W2q, self.W2s):
             if t is not None:
                 n += t.numel() * t.element_size()
         return n
@@ -168,7 +177,11 @@ def make_inputs(shape: LayerShape, device="cpu", seed: int = 0) -> LayerInputs:
         W1q, W1s = _fp8_channels((E, f, d), 1.0 / math.sqrt(d), _gen(device, base + 2), device)
     else:
         W1 = _normal((E, f, d), 1.0 / math.sqrt(d), _gen(device, base + 2), device, dt, big)
-    W2 = _normal((E, d, f), 1.0 / math.sqrt(f), _gen(device, base + 3), device, dt, big)
+    W2 = W2q = W2s = None
+    if shape.w2_fp8:
+        W2q, W2s = _fp8_channels((E, d, f), 1.0 / math.sqrt(f), _gen(device, base + 3), device)
+    else:
+        W2 = _normal((E, d, f), 1.0 / math.sqrt(f), _gen(device, base + 3), device, dt, big)
     if shape.act == ACT_SWIGLU and shape.w_fp8:
         W3q, W3s = _fp8_channels((E, f, d), 1.0 / math.sqrt(d), _gen(device, base + 4), device)
     elif shape.act == ACT_SWIGLU:
@@ -188,7 +201,7 @@ def make_inputs(shape: LayerShape, device="cpu", seed: int = 0) -> LayerInputs:
         Ws3 = _normal((fs, d), 1.0 / math.sqrt(d), _gen(device, base + 8), device, dt)
         Ws2 = _normal((d, fs), 1.0 / math.sqrt(fs), _gen(device, base + 9), device, dt)
     return LayerInputs(shape, x, W_r, W1, W2, W3, logit_offset, sel_bias, Ws1, Ws3, Ws2,
-                       W1q, W1s, W3q, W3s)
+                       W1q, W1s, W3q, W3s, W2q, W2s)
 
 
 def make_logits(T: int, E: int, seed: int, scale: float = 1.0, shift: float = 0.0,

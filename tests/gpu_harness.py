@@ -53,7 +53,10 @@ def run_gpu(inp, cfg=None, workspace=None):
     fp8 = inp.W1q is not None
     ws = workspace if workspace is not None else L.alloc_workspace(
         cfg, inp.x.device, "fp8" if fp8 else "forward")
-    if fp8:
+    if fp8 and getattr(inp, "W2q", None) is not None:
+        out = L.forward_fp8(cfg, inp.x, inp.W_r, inp.W1q, inp.W1s, inp.W3q, inp.W3s, inp.W2q,
+                            inp.logit_offset, inp.sel_bias, workspace=ws, W2s=inp.W2s)
+    elif fp8:
         out = L.forward_fp8(cfg, inp.x, inp.W_r, inp.W1q, inp.W1s, inp.W3q, inp.W3s, inp.W2,
                             inp.logit_offset, inp.sel_bias, workspace=ws)
     else:
@@ -135,7 +138,7 @@ def check_layer(inp, out, sample=None, check_y=True):
 
     # oracle conditioned on the GPU's choice (fp8 gate/up weights: the
     # dequantised weights and the quantised token rows, as the oracle's fp8
-    # variant defines them)
+    # variant defines them; fp8 down weights: their dequantised values)
     xe = None
     if inp.W1q is not None:
         W1 = LazyFp8Experts(inp.W1q, inp.W1s)
@@ -145,8 +148,10 @@ def check_layer(inp, out, sample=None, check_y=True):
     else:
         W1 = LazyExperts(inp.W1)
         W3 = LazyExperts(inp.W3) if inp.W3 is not None else None
+    W2 = (LazyFp8Experts(inp.W2q, inp.W2s) if getattr(inp, "W2q", None) is not None
+          else LazyExperts(inp.W2))
     tokens = None if sample is None else np.asarray(sample)
-    r = O.moe_forward(x64, Wr, W1, LazyExperts(inp.W2), s.k, s.act, s.gate,
+    r = O.moe_forward(x64, Wr, W1, W2, s.k, s.act, s.gate,
                       W3=W3, logit_offset=off, sel_bias=bias, capacity_factor=s.capacity_factor,
                       alpha=s.alpha, Ws1=host64(inp.Ws1), Ws3=host64(inp.Ws3), Ws2=host64(inp.Ws2),
                       tokens=tokens if check_y else np.zeros(0, np.int64), forced_idx=idx_gpu,

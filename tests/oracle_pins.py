@@ -578,6 +578,53 @@ def check_fp8_layer():
     np.testing.assert_array_equal(a.y, b.y)
 
 
+def _e4m3_value_by_definition(code: int) -> float:
+    """OCP e4m3 (fn): sign, 4 exponent bits with bias 7, 3 mantissa bits;
+    exponent 0 is subnormal (2^-6 * m/8); 0x7F / 0xFF are NaN."""
+    sign = -1.0 if code & 0x80 else 1.0
+    e, m = (code >> 3) & 0xF, code & 0x7
+    if e == 0xF and m == 0x7:
+        return math.nan
+    if e == 0:
+        return sign * 2.0 ** -6 * (m / 8.0)
+    return sign * 2.0 ** (e - 7) * (1.0 + m / 8.0)
+
+
+def check_fp8_down_weights():
+    """e4m3 down weights: a hand-computed one-expert case (d = f = 2; the codes
+    of the down matrix are 1, 1 / 4, 0 on two output channels with scales
+    1/2 and 1/4: y = ((h0 + h1) / 2, h0)), and a square random case (d = f,
+    so a scale applied along the wrong axis keeps the shapes) against weights
+    decoded element by element from the e4m3 definition and scaled per output
+    channel."""
+    x = np.array([[1.1, 0.5]])
+    W13 = np.array([[[0x38, 0x00], [0x00, 0x38]]])     # identity: gate = up = (1.125, 0.5)
+    r = O.moe_forward_fp8(x, np.ones((1, 2)), W13, np.ones((1, 2)), W13, np.ones((1, 2)),
+                          np.array([[[0x38, 0x38], [0x48, 0x00]]]), 1, O.GATE_SOFTMAX_TOPK,
+                          W2s=np.array([[0.5, 0.25]], dtype=np.float32))
+    h0, h1 = (g * g / (1 + math.exp(-g)) for g in (1.125, 0.5))
+    assert abs(r.y[0, 0] - 0.5 * (h0 + h1)) < 1e-15 and abs(r.y[0, 1] - h0) < 1e-15
+    rng = _rng(83)
+    T, d, E, k = 10, 8, 3, 2
+    f = d
+    x = rng.normal(size=(T, d))
+    W1q = rng.integers(0x10, 0x38, size=(E, f, d)) | (rng.integers(0, 2, size=(E, f, d)) << 7)
+    W3q = rng.integers(0x10, 0x38, size=(E, f, d))
+    W1s = rng.uniform(1e-2, 2e-2, size=(E, f)).astype(np.float32)
+    W3s = rng.uniform(1e-2, 2e-2, size=(E, f)).astype(np.float32)
+    W2q = rng.integers(0x00, 0x7F, size=(E, d, f)) | (rng.integers(0, 2, size=(E, d, f)) << 7)
+    W2s = rng.uniform(0.5, 4.0, size=(E, d)).astype(np.float32)
+    W2 = np.empty((E, d, f))
+    for e in range(E):
+        for n in range(d):
+            for c in range(f):
+                W2[e, n, c] = float(W2s[e, n]) * _e4m3_value_by_definition(int(W2q[e, n, c]))
+    W_r = rng.normal(size=(E, d))
+    a = O.moe_forward_fp8(x, W_r, W1q, W1s, W3q, W3s, W2q, k, O.GATE_SOFTMAX_TOPK, W2s=W2s)
+    b = O.moe_forward_fp8(x, W_r, W1q, W1s, W3q, W3s, W2, k, O.GATE_SOFTMAX_TOPK)
+    np.testing.assert_allclose(a.y, b.y, rtol=1e-13, atol=1e-13)
+
+
 ALL_CHECKS = [
     check_router_onehot, check_topk_bruteforce, check_topk_ties, check_topk_gap, check_gates_closed_form,
     check_gates_invariants, check_router_probs, check_selection_bias,
@@ -585,5 +632,5 @@ ALL_CHECKS = [
     check_sparse_equals_dense, check_drop_is_identity_branch, check_dense_ffn_special_case,
     check_multiply_counts, check_balance_uniform, check_balance_hand_and_collapse,
     check_pipeline_stats_pre_drop, check_z_loss_closed_forms, check_bias_update_rule,
-    check_e4m3_format, check_row_scale_rule, check_fp8_layer,
+    check_e4m3_format, check_row_scale_rule, check_fp8_layer, check_fp8_down_weights,
 ]

@@ -261,7 +261,41 @@ def test_fp8_entry_point_checks_without_gpu():
     assert L.launch_count(L.config_for(W.get("gptoss16_fp8")), fp8=True) == 5
     assert L.launch_count(L.config_for(W.get("gptoss256")), fp8=False) == 4
     assert L.launch_count(L.config_for(W.get("gptoss256_fp8")), fp8=True) == 5
+    # the fp8 plan: the row quantisation replaces the gather and the fused
+    # projections (the bf16 decode layer's default form)
+    dec = L.config_for(W.get("gptoss1"))
+    assert "fused_projections" in L.plan_flags(dec)
+    assert not {"fused_projections", "gather_rows"} & L.plan_flags(dec, fp8=True)
+    assert "route_decode" in L.plan_flags(dec, fp8=True)
     # forcing the split router (tensor-core logits, top-k, permute)
     with L.tuning(router="tc"):
         assert L.launch_count(L.config_for(W.get("gptoss256")), fp8=False) == 6
         assert L.launch_count(L.config_for(W.get("gptoss256_fp8")), fp8=True) == 7
+
+
+def test_fp8_all_entry_point_checks_without_gpu():
+    """moe_forward_fp8_all (e4m3 down weights as well): missing or misaligned
+    down scales and the layers moe_forward_fp8 rejects are refused before any
+    device work."""
+    lib = N.lib()
+    fake = ctypes.c_void_p(1 << 20)
+    odd = ctypes.c_void_p((1 << 20) + 4)
+
+    def call(cfg, W2s=fake, W1s=fake):
+        args = [fake, fake, None, None, fake, W1s, fake, fake, fake, W2s,
+                fake, fake, fake, fake, fake, None, None, None, None, None]
+        return lib.moe_forward_fp8_all(ctypes.byref(cfg), *args, None, ctypes.c_size_t(0), None)
+
+    ok = L.make_config(T=16, d=256, E=8, k=2, f=64)
+    assert call(ok, W2s=None) == N.MOE_ERR_ARG
+    assert call(ok, W1s=None) == N.MOE_ERR_ARG
+    assert call(ok, W2s=odd) == N.MOE_ERR_ARG
+    assert call(ok) == N.MOE_ERR_WORKSPACE           # everything else valid, no workspace
+    for bad in (L.make_config(T=16, d=256, E=8, k=2, f=64, act=L.ACT_GELU),
+                L.make_config(T=16, d=264, E=8, k=2, f=64)):
+        assert call(bad) == N.MOE_ERR_UNSUPPORTED
+    fake_hosts = (ctypes.c_void_p * 2)(fake.value, fake.value)
+    n = L.workspace_size(ok, "host_io_fp8")
+    args = ([ctypes.byref(ok), ctypes.c_int32(2), fake_hosts, fake, None, None, fake, fake, fake,
+             fake, fake, None, fake_hosts, fake, fake, ctypes.c_size_t(n)] + [None] * 3)
+    assert lib.moe_forward_fp8_all_host_io_batches(*args) == N.MOE_ERR_ARG   # no W2s

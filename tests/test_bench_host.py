@@ -99,6 +99,27 @@ def test_accounting_fp8_gate_up_weights():
     assert lay_b["bytes"] - lay_f["bytes"] == act * 2 * f * d * 2 - act * 2 * f * (d + 4)
 
 
+def test_accounting_fp8_down_weights():
+    """e4m3 down weights count one byte each plus a float32 scale per output
+    channel; the up projection's figures are those of the fp8 gate/up layer;
+    the down projection's flops are unchanged."""
+    f8 = W.get("gptoss16_fp8")
+    fa = W.get("gptoss16_fp8all")
+    assert fa.w_fp8 and fa.w2_fp8 and not f8.w2_fp8
+    kept = [0] * f8.E
+    for e in range(0, 64, 4):
+        kept[e] = 4
+    acc_f, lay_f = bench.accounting(f8, kept)
+    acc_a, lay_a = bench.accounting(fa, kept)
+    act, d, f = 16, f8.d, f8.f
+    assert acc_a["up"] == acc_f["up"]
+    assert acc_a["down"]["bytes"] == act * d * (f + 4)
+    assert acc_f["down"]["bytes"] == act * d * f * 2
+    assert acc_a["down"]["flops"] == acc_f["down"]["flops"]
+    assert lay_f["bytes"] - lay_a["bytes"] == act * d * f * 2 - act * d * (f + 4)
+    assert bench.workload_config(fa)["expert_weights"].startswith("gate/up/down e4m3")
+
+
 def test_fp8_up_projection_uses_the_fp8_tensor_peak():
     peaks = dict(bench.FALLBACK_PEAKS)
     acc = {"up": {"bytes": 1e6, "flops": 1e12}}

@@ -3,7 +3,7 @@ range-tested on the device before the access it drives; a failure is recorded
 as MOE_ERR_BOUNDS and the access skipped, never a trap).  Over the parity
 shapes -- ragged tiles, capacity drops, many experts, every routing path
 (including the cluster router for 64 < E <= 256), the decode batches, the
-projections as one launch and a full-size layer -- it must report no
+projections as one launch, the e4m3 weight layers and a full-size layer -- it must report no
 out-of-range index and still match the oracle."""
 import pytest
 import torch
@@ -13,6 +13,7 @@ from sparse_mixture_experts_65_b300 import layer as L
 from sparse_mixture_experts_65_b300 import workloads as W
 
 from gpu_harness import check_layer, run_gpu
+import test_gpu_fp8 as TF
 import test_gpu_parity as TP
 
 pytestmark = pytest.mark.gpu
@@ -71,5 +72,17 @@ def test_checked_build_on_the_one_launch_projections(checked_library, case):
         cfg = L.config_for(shape)
         ws = L.alloc_workspace(cfg)
         _, out = run_gpu(inp, cfg, ws)
+    assert L.check_status(ws) == N.MOE_OK
+    check_layer(inp, out)
+
+
+@pytest.mark.parametrize("shape", TF.FP8 + TF.FP8_ALL, ids=lambda s: s.name)
+def test_checked_build_on_the_fp8_layers(checked_library, shape):
+    """e4m3 gate/up weights (and e4m3 down weights): the row quantisation,
+    the e4m3 projections and the on-chip expansion of the down codes."""
+    inp = W.make_inputs(shape, "cuda", seed=23)
+    cfg = L.config_for(shape)
+    ws = L.alloc_workspace(cfg, kind="fp8")
+    _, out = run_gpu(inp, cfg, ws)
     assert L.check_status(ws) == N.MOE_OK
     check_layer(inp, out)

@@ -4,6 +4,7 @@ counted near tie), integers exact given the GPU's choice, y within the bf16
 tolerance.  The row quantisation is exact on both sides (power-of-two scales),
 so only the float32 accumulation and the bf16 roundings of h, o and y differ.
 """
+import dataclasses
 import gc
 
 import pytest
@@ -114,3 +115,118 @@ def test_fp8_host_io_batches_match_device_entry_point():
     for y in y_h:
         assert torch.equal(y, dev.y.cpu())
     assert torch.all(aux_h == dev.aux_loss.cpu()[0])
+
+
+# e4m3 down weights as well (moe_forward_fp8_all): f a multiple of 16
+FP8_ALL = [
+    LayerShape("fp8all_decode_t1", 75, T=1, d=256, E=16, k=4, f=192, act=SW, gate=TOPK,
+               dtype="bf16", w_fp8=True, w2_fp8=True),
+    LayerShape("fp8all_decode_ragged", 76, T=13, d=272, E=40, k=3, f=208, act=SW, gate=SIG,
+               dtype="bf16", sel_bias_halfwidth=0.05, w_fp8=True, w2_fp8=True),
+    # d = 400: a ragged last down tile of output channels (their scales are
+    # not read); f = 336: a ragged last K block of codes
+    LayerShape("fp8all_one_launch", 77, T=700, d=400, E=24, k=2, f=336, act=SW, gate=TOPK,
+               dtype="bf16", w_fp8=True, w2_fp8=True),
+    LayerShape("fp8all_split_many", 78, T=300, d=256, E=100, k=4, f=128, act=SW, gate=SIG,
+               dtype="bf16", sel_bias_halfwidth=0.05, w_fp8=True, w2_fp8=True),
+    # top-1 with capacity drops: the combine in the down epilogue
+    LayerShape("fp8all_capacity_top1", 79, T=517, d=192, E=16, k=1, f=256, act=SW, gate=FULL,
+               dtype="bf16", capacity_factor=1.0, logit_offset_var=1.5, w_fp8=True,
+               w2_fp8=True),
+]
+
+
+@pytest.mark.parametrize("shape", FP8_ALL, ids=lambda s: s.name)
+def test_fp8_down_weight_layers(shape):
+    inp = W.make_inputs(shape, "cuda", seed=2)
+    assert inp.W2 is None and inp.W2q is not None
+    _, out = run_gpu(inp)
+    rep = check_layer(inp, out)
+    print(shape.name, rep)
+
+
+@pytest.mark.parametrize("T", [1, 16, 256])
+def test_fp8_down_weight_gptoss(T):
+    shape = W.get(f"gptoss{T}_fp8all")
+    inp = W.make_inputs(shape, "cuda")
+    _, out = run_gpu(inp)
+    sample = None if T <= 16 else list(range(0, T, max(1, T // 32)))
+    rep = check_layer(inp, out, sample=sample)
+    print("gptoss_fp8all", T, rep)
+    del inp, out
+    _free()
+
+
+def test_fp8_down_weight_repeat_calls_bitwise_identical():
+    inp = W.make_inputs(FP8_ALL[2], "cuda", seed=3)
+    cfg = L.config_for(inp.shape)
+    ws = L.alloc_workspace(cfg, kind="fp8")
+    _, a = run_gpu(inp, cfg, ws)
+    _, b = run_gpu(inp, cfg, ws)
+    for name in ("y", "topk_idx", "topk_w", "expert_counts", "aux_loss", "slot_pos"):
+        assert torch.equal(getattr(a, name), getattr(b, name)), name
+
+
+def test_fp8_down_weight_routing_matches_fp8_layer():
+    """The down weights' format changes only the down projection: routing,
+    gates and counts are those of moe_forward_fp8 on the same x."""
+    shape = FP8_ALL[3]
+    inp = W.make_inputs(shape, "cuda", seed=5)
+    ref = W.make_inputs(dataclasses.replace(shape, w2_fp8=False), "cuda", seed=5)
+    assert torch.equal(inp.x, ref.x) and torch.equal(inp.W1q, ref.W1q)
+    _, a = run_gpu(inp)
+    _, b = run_gpu(ref)
+    for name in ("topk_idx", "topk_w", "expert_counts", "aux_loss", "slot_pos"):
+        assert torch.equal(getattr(a, name), getattr(b, name)), name
+
+
+def test_fp8_down_weight_unsupported_width():
+    """f not a multiple of 16: a row of down codes is no TMA row."""
+    shape = LayerShape("fp8all_f200", 80, T=64, d=256, E=8, k=2, f=200, act=SW, gate=TOPK,
+                       dtype="bf16", w_fp8=True, w2_fp8=True)
+    inp = W.make_inputs(shape, "cuda")
+    with pytest.raises(L.N.MoeError) as e:
+        run_gpu(inp)
+    assert e.value.code == L.N.MOE_ERR_UNSUPPORTED
+
+
+def test_fp8_down_weight_host_io_batches_match_device_entry_point():
+    shape = FP8_ALL[1]
+    inp = W.make_inputs(shape, "cuda", seed=7)
+    cfg, dev = run_gpu(inp)
+    x_h = [inp.x.cpu().pin_memory() for _ in range(3)]
+    y_h = [torch.empty_like(x).pin_memory() for x in x_h]
+    aux_h = torch.empty(3, dtype=torch.float32).pin_memory()
+    b = L.BoundHostIOBatches(cfg, x_h, y_h, aux_h, inp)
+    assert b._fn.__name__ == "moe_forward_fp8_all_host_io_batches"
+    b()
+    torch.cuda.synchronize()
+    assert L.check_status(b.workspace) == 0
+    for y in y_h:
+        assert torch.equal(y, dev.y.cpu())
+    assert torch.all(aux_h == dev.aux_loss.cpu()[0])
+
+
+@pytest.mark.parametrize("codes", ["subnormal", "every"])
+def test_fp8_down_weight_code_ranges(codes):
+    """Down codes drawn only from the e4m3 subnormals (exponent field 0: a
+    kernel that flushed them would return y = 0), or uniformly from every
+    non-NaN code (exponents 2^-9 .. 2^8 in one matrix), against the oracle."""
+    shape = FP8_ALL[2]
+    inp = W.make_inputs(shape, "cuda", seed=8)
+    g = torch.Generator(device="cuda")
+    g.manual_seed(808)
+    n = inp.W2q.numel()
+    if codes == "subnormal":
+        mag = torch.randint(1, 8, (n,), generator=g, device="cuda")
+        unit = 2.0 ** -9                 # the smallest subnormal step
+    else:
+        mag = torch.randint(0, 0x7F, (n,), generator=g, device="cuda")
+        unit = 64.0                      # a typical magnitude of a uniform code
+    sign = torch.randint(0, 2, (n,), generator=g, device="cuda") << 7
+    inp.W2q.copy_((mag | sign).to(torch.uint8).view_as(inp.W2q))
+    inp.W2s.fill_(1.0 / (unit * 4.0 * shape.f ** 0.5))
+    _, out = run_gpu(inp)
+    assert torch.count_nonzero(out.y) > out.y.numel() // 2
+    rep = check_layer(inp, out)
+    print(codes, rep)

@@ -212,6 +212,13 @@ def _fp8_layer_unquantised_rows(x, W_r, W1q, W1s, W3q, W3s, W2, k, gate_mode, **
                          W3=M.dequantize_weights(W3q, W3s), **kw)
 
 
+def _fp8_down_scale_on_input_axis(x, W_r, W1q, W1s, W3q, W3s, W2, k, gate_mode, W2s=None,
+                                  **kw):
+    if W2s is not None:
+        W2 = M.e4m3_decode(W2) * np.asarray(W2s, dtype=float)[:, None, :]
+    return _orig["moe_forward_fp8"](x, W_r, W1q, W1s, W3q, W3s, W2, k, gate_mode, **kw)
+
+
 MUTATIONS = [
     ("router expert order reversed", "router_logits", _router_reversed, P.check_router_onehot),
     ("router offset sign flipped", "router_logits", _router_offset_sign, P.check_router_onehot),
@@ -249,6 +256,8 @@ MUTATIONS = [
      P.check_row_scale_rule),
     ("fp8 layer skips the row quantisation", "moe_forward_fp8", _fp8_layer_unquantised_rows,
      P.check_fp8_layer),
+    ("fp8 down scales along the input axis", "moe_forward_fp8", _fp8_down_scale_on_input_axis,
+     P.check_fp8_down_weights),
 ]
 
 
