@@ -1,8 +1,8 @@
 // combine.cu -- stage 6: y[t] = shared(x_t) + sum_j g_tj * o[row(t, j)],
 // over the kept slots, accumulated in float32 in the fixed order j = 0..k-1
-// (no atomics), then rounded once to the output dtype.  The expert outputs o
-// (and the shared expert's) arrive in the layer dtype: bf16 on the
-// tensor-core path, float32 on the float32 path.
+// (no atomics), then rounded once to the output dtype.  The routed expert
+// outputs o arrive in the layer dtype (bf16 on the tensor-core path, float32
+// on the float32 path), the shared expert's in float32 on both.
 //
 // "Mixture of Experts" (llm-tutorial ch. 11) § The mathematics and
 // "Mixture-of-Experts" (neural networks visually) § Show the math: the layer
@@ -61,7 +61,7 @@ __global__ void __launch_bounds__(kThreads) combine_kernel(const CombineArgs a) 
   }
   __syncthreads();
   const TOut* o = static_cast<const TOut*>(a.o);
-  const TOut* os = static_cast<const TOut*>(a.os);
+  const float* os = static_cast<const float*>(a.os);
   TOut* y = static_cast<TOut*>(a.y);
   for (int c = threadIdx.x * 4; c < a.d; c += kThreads * 4) {
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -98,19 +98,15 @@ __global__ void __launch_bounds__(kThreads) combine_bf16x8_kernel(const CombineA
   }
   __syncthreads();
   const __nv_bfloat16* o = static_cast<const __nv_bfloat16*>(a.o);
-  const __nv_bfloat16* os = static_cast<const __nv_bfloat16*>(a.os);
+  const float* os = static_cast<const float*>(a.os);
   __nv_bfloat16* y = static_cast<__nv_bfloat16*>(a.y);
   for (int c = threadIdx.x * 8; c < a.d; c += kThreads * 8) {
     float acc[8];
     if (os) {
-      const uint4 u = *reinterpret_cast<const uint4*>(os + (size_t)t * a.d + c);
-      const __nv_bfloat162* b = reinterpret_cast<const __nv_bfloat162*>(&u);
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const float2 f = __bfloat1622float2(b[i]);
-        acc[2 * i] = f.x;
-        acc[2 * i + 1] = f.y;
-      }
+      const float4* src = reinterpret_cast<const float4*>(os + (size_t)t * a.d + c);
+      const float4 u0 = src[0], u1 = src[1];
+      acc[0] = u0.x; acc[1] = u0.y; acc[2] = u0.z; acc[3] = u0.w;
+      acc[4] = u1.x; acc[5] = u1.y; acc[6] = u1.z; acc[7] = u1.w;
     } else {
 #pragma unroll
       for (int i = 0; i < 8; ++i) acc[i] = 0.f;

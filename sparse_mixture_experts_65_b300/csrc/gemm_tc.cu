@@ -281,6 +281,25 @@ __device__ __forceinline__ void epilogue_tile(const TcArgs& a, const TileInfo& t
     if (DUAL) tmem_ld32(t_row + BNH + c, r1);
     tmem_ld_wait();
     const int col = ti.n0 + c;
+    if ((EPI == EPI_OUT16 || EPI == EPI_COMBINEK) && ti.shared) {
+      // the shared expert's output stays float32 until the combine adds the
+      // routed slots to it: it enters y with weight 1, and a bf16 rounding
+      // here would add up to half a bf16 ulp of |y| to the layer's error
+      if (!row_ok) continue;
+      float* dstf = static_cast<float*>(a.out_sh) + orow * a.ld_out_sh + col;
+      if (col + 32 <= ti.N) {
+#pragma unroll
+        for (int v = 0; v < 8; ++v)
+          reinterpret_cast<float4*>(dstf)[v] =
+              make_float4(__uint_as_float(r0[4 * v]), __uint_as_float(r0[4 * v + 1]),
+                          __uint_as_float(r0[4 * v + 2]), __uint_as_float(r0[4 * v + 3]));
+      } else {
+#pragma unroll
+        for (int i = 0; i < 32; ++i)
+          if (col + i < ti.N) dstf[i] = __uint_as_float(r0[i]);
+      }
+      continue;
+    }
     __nv_bfloat16* out = static_cast<__nv_bfloat16*>(
         EPI == EPI_COMBINE1 ? a.y : (ti.shared ? a.out_sh : a.out));
     const int ld = EPI == EPI_COMBINE1 ? a.ld_y : (ti.shared ? a.ld_out_sh : a.ld_out);
@@ -415,22 +434,17 @@ __device__ __forceinline__ void combine_slice(const TcArgs& a, const TileInfo& t
   const int ncol = ti.N - ti.n0 < BNH ? ti.N - ti.n0 : BNH;
   const bool act = c < ncol;
   const __nv_bfloat16* o = static_cast<const __nv_bfloat16*>(a.out);
-  const __nv_bfloat16* os = static_cast<const __nv_bfloat16*>(a.out_sh);
+  const float* os = static_cast<const float*>(a.out_sh);   // float32 shared output
   const int* kr = a.key_row + (size_t)t * a.k_slots;
   const float* gt = a.gate + (size_t)t * a.k_slots;
   float acc[8];
 #pragma unroll
   for (int i = 0; i < 8; ++i) acc[i] = 0.f;
   if (a.has_shared && act) {
-    const uint4 u =
-        __ldcg(reinterpret_cast<const uint4*>(os + (size_t)t * a.ld_out_sh + ti.n0 + c));
-    const __nv_bfloat162* b = reinterpret_cast<const __nv_bfloat162*>(&u);
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const float2 f = __bfloat1622float2(b[i]);
-      acc[2 * i] = f.x;
-      acc[2 * i + 1] = f.y;
-    }
+    const float4* src = reinterpret_cast<const float4*>(os + (size_t)t * a.ld_out_sh + ti.n0 + c);
+    const float4 u0 = __ldcg(src), u1 = __ldcg(src + 1);
+    acc[0] = u0.x; acc[1] = u0.y; acc[2] = u0.z; acc[3] = u0.w;
+    acc[4] = u1.x; acc[5] = u1.y; acc[6] = u1.z; acc[7] = u1.w;
   }
   for (int j0 = 0; j0 < a.k_slots; j0 += 8) {
     int r[8];

@@ -325,7 +325,9 @@ int make_plan(const moe_config* cfg, WsKind kind, Plan* p, int num_sms) {
     L.o = take((size_t)P.R_cap * c.d * P.elem);
     if (c.n_shared) {
       L.hs = take((size_t)P.T_pad * c.f_shared * act_elem);
-      L.os = take((size_t)P.T_pad * c.d * P.elem);
+      // the shared expert's output in float32 on both paths: it enters y with
+      // weight 1, so it is rounded only once, in y
+      L.os = take((size_t)P.T_pad * c.d * sizeof(float));
     }
     // sized for the narrowest down tile (64 columns), so that the layout does
     // not depend on the tiling (which follows the GPU's SM count)
