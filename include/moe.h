@@ -506,7 +506,13 @@ int moe_plan_flags_fp8(const moe_config* cfg, uint32_t* flags);
  *                            launches; the default takes one launch for the
  *                            forms that measured faster (gathered ReLU up
  *                            projection with the combine in the down
- *                            projection, the 96-column decode tiling).
+ *                            projection, the 96-column decode tiling);
+ *   MOE_TUNE_F8_DOWN_FORM    moe_forward_fp8_all's down projection: 1 the
+ *                            weights as the MMA's M operand (128 output
+ *                            channels per tile, 32 token rows per pass), 0
+ *                            the weights as its N operand (token rows as M);
+ *                            the default takes the first where segments
+ *                            average at most one row (T*k <= E).
  * Errors: MOE_ERR_ARG for an unknown knob or a value out of range.  Not
  * synchronised with calls in flight on other threads.
  */
@@ -520,7 +526,8 @@ enum {
   MOE_TUNE_FUSED_COMBINE = 6,
   MOE_TUNE_CLUSTER = 7,
   MOE_TUNE_FUSED_PROJ = 8,
-  MOE_TUNE_COUNT = 9
+  MOE_TUNE_F8_DOWN_FORM = 9,
+  MOE_TUNE_COUNT = 10
 };
 enum { MOE_ROUTER_SIMT = 1, MOE_ROUTER_FUSED = 2, MOE_ROUTER_TC = 3 };
 int moe_set_tuning(int32_t knob, int32_t value);

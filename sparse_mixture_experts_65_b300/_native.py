@@ -28,7 +28,7 @@ MOE_GATE_SOFTMAX_TOPK, MOE_GATE_SIGMOID_RENORM, MOE_GATE_SOFTMAX_FULL = 0, 1, 2
 MOE_NUM_STAGES = 6
 MOE_TUNE_ROUTER, MOE_TUNE_GATHER, MOE_TUNE_TILE_N_UP, MOE_TUNE_TILE_N_DOWN = 0, 1, 2, 3
 MOE_TUNE_PARTIAL_A_ROWS, MOE_TUNE_MMA_M64, MOE_TUNE_FUSED_COMBINE = 4, 5, 6
-MOE_TUNE_CLUSTER, MOE_TUNE_FUSED_PROJ = 7, 8
+MOE_TUNE_CLUSTER, MOE_TUNE_FUSED_PROJ, MOE_TUNE_F8_DOWN_FORM = 7, 8, 9
 MOE_PLAN_ROUTE_ONE_LAUNCH, MOE_PLAN_ROUTE_CLUSTER, MOE_PLAN_ROUTE_DECODE = 1, 2, 4
 MOE_PLAN_GATHER_ROWS, MOE_PLAN_COMBINE_IN_DOWN, MOE_PLAN_FUSED_PROJECTIONS = 8, 16, 32
 MOE_ROUTER_SIMT, MOE_ROUTER_FUSED, MOE_ROUTER_TC = 1, 2, 3

@@ -108,6 +108,8 @@ struct TcArgs {
   unsigned* zero_ctr = nullptr;     // cleared by this launch (the next launch's counters)
   int zero_ctr_n = 0;
   int T_x = 0;                      // rows of x (tokens): range of row_token entries
+  int sched_bn = 0;                 // weights-as-M kernel: the column tile width that the
+                                    // device tile prefix counts (N tiles per segment)
   uint32_t* status;
   uint64_t timeout_ns;
 };
@@ -1952,15 +1954,15 @@ tc_down_f8w(const __grid_constant__ CUtensorMap mA, const __grid_constant__ CUte
           ok = false;
           break;
         }
-        const uint8_t* raw = smem + C::R_OFF + sr * C::R_BYTES;
-        uint8_t* bt = smem + C::B_OFF + sb * C::B_BYTES;
+        const uint32_t raw = stage_r(sr);
+        const uint32_t bt = stage_b(sb);
         constexpr int PER = (BNH * 8) / (C::CONVW * 32);
         static_assert(PER * C::CONVW * 32 == BNH * 8, "items per converter thread");
         uint2 codes[PER];
 #pragma unroll
         for (int j = 0; j < PER; ++j) {
           const int i = ct + j * 32 * C::CONVW;
-          codes[j] = *reinterpret_cast<const uint2*>(raw + (i >> 3) * 64 + (i & 7) * 8);
+          codes[j] = lds_u2(raw + (i >> 3) * 64 + (i & 7) * 8);
         }
         // the codes are in registers: the code stage can be refilled
         __syncwarp();
@@ -1970,8 +1972,7 @@ tc_down_f8w(const __grid_constant__ CUtensorMap mA, const __grid_constant__ CUte
           const int i = ct + j * 32 * C::CONVW;
           const int n = i >> 3, c = i & 7;
           const uint2 b01 = e4m3x4_to_bf16x4(codes[j].x), b23 = e4m3x4_to_bf16x4(codes[j].y);
-          *reinterpret_cast<uint4*>(bt + n * 128 + ((c ^ (n & 7)) << 4)) =
-              make_uint4(b01.x, b01.y, b23.x, b23.y);
+          sts_u4(bt + n * 128 + ((c ^ (n & 7)) << 4), make_uint4(b01.x, b01.y, b23.x, b23.y));
         }
         fence_proxy_async_smem();   // the tensor cores read what these threads wrote
         __syncwarp();
@@ -2018,6 +2019,372 @@ tc_down_f8w(const __grid_constant__ CUtensorMap mA, const __grid_constant__ CUte
       }
       tc_fence_before();
       mbar_arrive(tempty_bar(ab));
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, C::TMEM_COLS);
+  }
+}
+
+// ---------------------------------------------------------------- e4m3 down weights, weights as M
+// The same product for decode-sized segments, with the operands swapped:
+// o^T = W2 h^T, the 128 output channels of a tile as the MMA's M and the
+// segment's token rows as its N (32 per pass).  An expert segment of a decode
+// batch holds a few rows, so the weights-as-B form multiplies M = 64 rows, one
+// or two of them real, against every channel; here the tensor work per stage
+// shrinks by the row ratio, and the h rows of a stage (two 32-row boxes, 8 KB)
+// travel in the same stage as its codes (128 rows of 128 bytes: whole DRAM
+// lines, 16 KB), so they are requested as early as the codes are.  One ring
+// of code + h stages (the producer's), a ring of expanded bf16 weight tiles
+// (two 64-wide panels per stage, the converters'), two 32-column
+// accumulators.
+// A stage is free once the converters have read its codes and the MMAs that
+// read its h rows have completed.  Segments of more than 32 rows take one
+// pass per 32 rows, each re-streaming the tile's weights: the plan uses this
+// kernel where segments average at most one row.
+constexpr int kSwN = 32;   // token rows per pass (the MMA's N)
+template <int EPI>
+struct F8sCfg {
+  static constexpr int BNH = 128;                   // output channels per tile (the MMA's M)
+  static constexpr int KB = 128;                    // K per stage: whole 128-byte code rows
+  static constexpr int PANEL = 64;                  // K per 128-byte bf16 panel
+  static constexpr int R_BYTES = BNH * KB;          // codes of one K block
+  static constexpr int H_PANEL = kSwN * 128;        // h rows of one panel (a 32-row box)
+  static constexpr int H_BYTES = 2 * H_PANEL;
+  static constexpr int STAGE_BYTES = R_BYTES + H_BYTES;
+  static constexpr int W_PANEL = BNH * 128;         // expanded bf16 weights of one panel
+  static constexpr int W_BYTES = 2 * W_PANEL;
+  static constexpr int WST = 2;
+  static constexpr int RING_BUDGET = 208 * 1024;
+  static constexpr int ST_FIT = (RING_BUDGET - WST * W_BYTES) / STAGE_BYTES;
+  static constexpr int ST = ST_FIT > 16 ? 16 : ST_FIT;
+  static constexpr int W_OFF = ST * STAGE_BYTES;
+  static constexpr int RING_BYTES = W_OFF + WST * W_BYTES;
+  static constexpr int TMEM_COLS = 2 * kSwN;        // two accumulators of kSwN columns
+  static constexpr int EPIW = 4;
+  static constexpr int CONVW = 4;
+  static constexpr int EPI0 = 2;
+  static constexpr int CONV0 = EPI0 + EPIW;
+  static constexpr int THREADS = (CONV0 + CONVW) * 32;
+  static constexpr int NBARS = 2 * (ST + WST) + 5;
+  static constexpr int BAR_BYTES = 8 * NBARS + 16;
+  static constexpr int SCHED_INTS = 4 * (kMaxE + 2);
+  static constexpr int SMEM = 1024 + RING_BYTES + BAR_BYTES + 4 * SCHED_INTS;
+  static constexpr uint32_t IDESC = idesc_bf16_f32(BNH, kSwN);
+  static_assert(R_BYTES % 1024 == 0 && W_BYTES % 1024 == 0 && STAGE_BYTES % 1024 == 0,
+                "swizzled tiles start on 1024-byte boundaries");
+  static_assert(ST >= 5, "stage ring depth");
+  static_assert(SMEM <= 227 * 1024, "shared memory");
+};
+
+template <int EPI>
+__global__ void __launch_bounds__(F8sCfg<EPI>::THREADS, 1)
+tc_down_f8s(const __grid_constant__ CUtensorMap mA32, const __grid_constant__ CUtensorMap mW,
+            const TcArgs a) {
+  using C = F8sCfg<EPI>;
+  static_assert(EPI == EPI_OUT16 || EPI == EPI_COMBINE1, "down epilogues");
+  constexpr int BNH = C::BNH;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::RING_BYTES);
+  const uint32_t bar0 = smem_u32(bars);
+  // barriers: stages full / empty, bf16 weight tiles full / empty,
+  // accumulators full / empty, drain
+  auto sfull = [&](int s) { return bar0 + 8u * s; };
+  auto sempty = [&](int s) { return bar0 + 8u * (C::ST + s); };
+  auto wfull = [&](int s) { return bar0 + 8u * (2 * C::ST + s); };
+  auto wempty = [&](int s) { return bar0 + 8u * (2 * C::ST + C::WST + s); };
+  const uint32_t tb0 = bar0 + 8u * (2 * (C::ST + C::WST));
+  auto tfull_bar = [&](int b) { return tb0 + 8u * b; };
+  auto tempty_bar = [&](int b) { return tb0 + 8u * (2 + b); };
+  const uint32_t drain_bar = tb0 + 8u * 4;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + C::NBARS);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  const uint32_t smem_base = smem_u32(smem);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  auto stage_r = [&](int s) { return smem_base + s * C::STAGE_BYTES; };
+  auto stage_h = [&](int s) { return smem_base + s * C::STAGE_BYTES + C::R_BYTES; };
+  auto stage_w = [&](int s) { return smem_base + C::W_OFF + s * C::W_BYTES; };
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < C::ST; ++s) {
+      mbar_init(sfull(s), 1);
+      mbar_init(sempty(s), C::CONVW + 1);   // the converters' reads and the MMAs' commit
+    }
+    for (int s = 0; s < C::WST; ++s) {
+      mbar_init(wfull(s), C::CONVW);
+      mbar_init(wempty(s), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(tfull_bar(b), 1);
+      mbar_init(tempty_bar(b), 32 * C::EPIW);
+    }
+    mbar_init(drain_bar, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&mA32);
+    tma_prefetch_desc(&mW);
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_slot), C::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  // The tile schedule (written by the routing kernel, two launches back) is
+  // read before the wait.  Its prefix counts sched_bn-wide column tiles per
+  // M tile; every routed segment has the same count, so the prefix of this
+  // kernel's 128-wide tiles is (tp / nt_sched) * nt.
+  int* s_tp = reinterpret_cast<int*>(smem + C::RING_BYTES + C::BAR_BYTES);
+  int* s_seg = s_tp + (kMaxE + 2);
+  int* s_mt = s_seg + (kMaxE + 2);
+  int* s_kept = s_mt + (kMaxE + 2);
+  const int nt_sched = (a.N + a.sched_bn - 1) / a.sched_bn;
+  const int nt = (a.N + BNH - 1) / BNH;
+  for (int i = threadIdx.x; i <= a.E; i += blockDim.x) s_tp[i] = (__ldg(a.tp + i) / nt_sched) * nt;
+  for (int i = threadIdx.x; i < a.E; i += blockDim.x) {
+    s_mt[i] = __ldg(a.mtiles + i);
+    s_seg[i] = __ldg(a.seg_start + i);
+    s_kept[i] = __ldg(a.kept + i);
+  }
+  __syncthreads();
+  const Sched sc{s_tp, s_seg, s_mt, s_kept};
+  const int total = s_tp[a.E];
+  auto give_up = [&]() {
+    atomicOr(a.status, STATUS_TIMEOUT_GEMM);
+    *abort_flag = 1;
+  };
+  // passes (32-row groups) of a tile
+  auto passes_of = [&](const TileInfo& ti) {
+    const int rows = ti.row_end - ti.a_row < kTcBM ? ti.row_end - ti.a_row : kTcBM;
+    return rows > 0 ? (rows + kSwN - 1) / kSwN : 0;
+  };
+  uint32_t npre = 0;   // stages whose codes were issued before the wait
+  if (warp == 0 && lane == 0) {
+    for (int tile = blockIdx.x; tile < total && npre < (uint32_t)C::ST; tile += gridDim.x) {
+      const TileInfo ti = decode_tile(a, sc, tile, BNH);
+      const int nk = (ti.K + C::KB - 1) / C::KB;
+      const int np = passes_of(ti);
+      for (int ps = 0; ps < np && npre < (uint32_t)C::ST; ++ps)
+        for (int kb = 0; kb < nk && npre < (uint32_t)C::ST; ++kb, ++npre) {
+          mbar_arrive_expect_tx(sfull(npre), C::STAGE_BYTES);
+          tma_load_3d(stage_r(npre), &mW, sfull(npre), kb * (C::KB / 2), ti.n0, ti.seg);
+        }
+    }
+  }
+  pdl_wait();
+  pdl_trigger();
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ---------------- producer: codes and h rows of each stage ----------------
+      uint32_t g = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
+        const TileInfo ti = decode_tile(a, sc, tile, BNH);
+        const int nk = (ti.K + C::KB - 1) / C::KB;
+        const int np = passes_of(ti);
+        for (int ps = 0; ps < np && ok; ++ps) {
+          for (int kb = 0; kb < nk; ++kb, ++g) {
+            const int s = g % C::ST;
+            if (g >= npre) {
+              if (!mbar_wait_sleep_bounded(sempty(s), ((g / C::ST) & 1u) ^ 1u, a.timeout_ns,
+                                           abort_flag)) {
+                give_up();
+                ok = false;
+                break;
+              }
+              mbar_arrive_expect_tx(sfull(s), C::STAGE_BYTES);
+              tma_load_3d(stage_r(s), &mW, sfull(s), kb * (C::KB / 2), ti.n0, ti.seg);
+            }
+            const int row = ti.a_row + ps * kSwN;
+            tma_load_2d(stage_h(s), &mA32, sfull(s), kb * C::KB, row);
+            tma_load_2d(stage_h(s) + C::H_PANEL, &mA32, sfull(s), kb * C::KB + C::PANEL, row);
+          }
+        }
+      }
+      // every load issued has landed before the block exits
+      for (int s = 0; s < C::ST; ++s) {
+        if (g > static_cast<uint32_t>(s)) {
+          const uint32_t uses = (g - 1 - s) / C::ST + 1;
+          if (ok)
+            mbar_wait_sleep_bounded(sempty(s), (uses - 1) & 1u, a.timeout_ns, abort_flag);
+          else
+            mbar_wait_bounded(sfull(s), (uses - 1) & 1u, a.timeout_ns, nullptr);
+        }
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ---------------- MMA issuer ----------------
+      uint32_t g = 0;
+      int it = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
+        const TileInfo ti = decode_tile(a, sc, tile, BNH);
+        const int nk = (ti.K + C::KB - 1) / C::KB;
+        const int np = passes_of(ti);
+        for (int ps = 0; ps < np && ok; ++ps, ++it) {
+          const int ab = it & 1;
+          if (!mbar_wait_sleep_bounded(tempty_bar(ab), ((it >> 1) & 1) ^ 1u, a.timeout_ns,
+                                       abort_flag)) {
+            give_up();
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t d_tmem = tmem_base + ab * kSwN;
+          for (int kb = 0; kb < nk; ++kb, ++g) {
+            const int s = g % C::ST, w = g % C::WST;
+            // the stage's h rows have landed and its weights are expanded
+            if (!mbar_wait_sleep_bounded(sfull(s), (g / C::ST) & 1u, a.timeout_ns, abort_flag) ||
+                !mbar_wait_sleep_bounded(wfull(w), (g / C::WST) & 1u, a.timeout_ns,
+                                         abort_flag)) {
+              give_up();
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+#pragma unroll
+            for (int pn = 0; pn < 2; ++pn)
+#pragma unroll
+              for (int kk = 0; kk < 4; ++kk)
+                tc_mma_bf16(d_tmem, smem_desc_k128(stage_w(w) + pn * C::W_PANEL + kk * 32),
+                            smem_desc_k128(stage_h(s) + pn * C::H_PANEL + kk * 32), C::IDESC,
+                            (kb != 0 || pn != 0 || kk != 0) ? 1u : 0u);
+            tc_commit(sempty(s));
+            tc_commit(wempty(w));
+          }
+          if (!ok) break;
+          tc_commit(tfull_bar(ab));
+        }
+      }
+      if (!ok) {
+        tc_commit(drain_bar);
+        mbar_wait_bounded(drain_bar, 0, a.timeout_ns, nullptr);
+      }
+    }
+  } else if (warp >= C::CONV0) {
+    // ---------------- converter warps ----------------
+    // item i of a stage: weight row i / 16, eight codes i % 16 of its 128-byte
+    // code row: 16-byte chunk (i % 16) % 8 of the row's bf16 panel (i % 16) / 8,
+    // written in the 128-byte swizzle
+    const int ct = (warp - C::CONV0) * 32 + lane;
+    constexpr int PER = (BNH * 16) / (C::CONVW * 32);
+    static_assert(PER * C::CONVW * 32 == BNH * 16, "items per converter thread");
+    uint32_t g = 0;
+    bool ok = true;
+    for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
+      const TileInfo ti = decode_tile(a, sc, tile, BNH);
+      const int nk = (ti.K + C::KB - 1) / C::KB;
+      const int np = passes_of(ti);
+      for (int ps = 0; ps < np && ok; ++ps) {
+        for (int kb = 0; kb < nk; ++kb, ++g) {
+          const int s = g % C::ST, w = g % C::WST;
+          const bool okl =
+              mbar_wait_sleep_bounded(sfull(s), (g / C::ST) & 1u, a.timeout_ns, abort_flag) &&
+              mbar_wait_sleep_bounded(wempty(w), ((g / C::WST) & 1u) ^ 1u, a.timeout_ns,
+                                      abort_flag);
+          if (!__all_sync(0xffffffffu, okl)) {
+            if (lane == 0) give_up();
+            ok = false;
+            break;
+          }
+          const uint32_t raw = stage_r(s);
+          const uint32_t wt = stage_w(w);
+          uint2 codes[PER];
+#pragma unroll
+          for (int j = 0; j < PER; ++j) {
+            const int i = ct + j * 32 * C::CONVW;
+            codes[j] = lds_u2(raw + (i >> 4) * 128 + (i & 15) * 8);
+          }
+          __syncwarp();
+          if (lane == 0) mbar_arrive(sempty(s));   // the codes are in registers
+#pragma unroll
+          for (int j = 0; j < PER; ++j) {
+            const int i = ct + j * 32 * C::CONVW;
+            const int n = i >> 4, pn = (i >> 3) & 1, c = i & 7;
+            const uint2 b01 = e4m3x4_to_bf16x4(codes[j].x), b23 = e4m3x4_to_bf16x4(codes[j].y);
+            sts_u4(wt + pn * C::W_PANEL + n * 128 + ((c ^ (n & 7)) << 4),
+                   make_uint4(b01.x, b01.y, b23.x, b23.y));
+          }
+          fence_proxy_async_smem();   // the tensor cores read what these threads wrote
+          __syncwarp();
+          if (lane == 0) mbar_arrive(wfull(w));
+        }
+      }
+    }
+  } else {
+    // ---------------- epilogue (four warps, one per TMEM lane quarter) ----------------
+    // thread = output channel (TMEM lane), its 32 accumulator columns = the
+    // pass's 32 token rows
+    const int q = warp & 3;
+    if constexpr (EPI == EPI_COMBINE1) {
+      // a dropped token (key_row < 0, top-1) gets y = 0
+      uint4* y = static_cast<uint4*>(a.y);
+      const int nvec = a.ld_y * 2 / 16;
+      const int gw = blockIdx.x * C::EPIW + (warp - C::EPI0), nw = gridDim.x * C::EPIW;
+      for (int t = gw; t < a.T_tokens; t += nw) {
+        if (__ldg(a.key_row + t) < 0)
+          for (int c = lane; c < nvec; c += 32) y[(size_t)t * nvec + c] = make_uint4(0, 0, 0, 0);
+      }
+    }
+    int it = 0;
+    bool ok = true;
+    for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
+      const TileInfo ti = decode_tile(a, sc, tile, BNH);
+      const int np = passes_of(ti);
+      const int ch = ti.n0 + q * 32 + lane;
+      const bool ch_ok = ch < ti.N;
+      const float sc_ch = ch_ok ? __ldg(a.b0_scale + (size_t)ti.seg * a.N + ch) : 0.f;
+      for (int ps = 0; ps < np; ++ps, ++it) {
+        const int ab = it & 1;
+        if (!mbar_wait_sleep_bounded(tfull_bar(ab), (it >> 1) & 1, a.timeout_ns, abort_flag)) {
+          give_up();
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        uint32_t r[kSwN];
+        tmem_ld32(tmem_base + (static_cast<uint32_t>(q * 32) << 16) + ab * kSwN, r);
+        tmem_ld_wait();
+        tc_fence_before();
+        mbar_arrive(tempty_bar(ab));
+        const int row0 = ti.a_row + ps * kSwN;
+        int rend = ti.row_end - row0 < kSwN ? ti.row_end - row0 : kSwN;
+        if (rend > 0 && !in_bounds(row0 + rend <= a.R_cap, a.status))
+          rend = a.R_cap - row0 > 0 ? a.R_cap - row0 : 0;
+        if (!ch_ok) continue;
+        // unrolled over the pass's 32 columns (register-resident accumulator
+        // values), predicated on the real rows
+#pragma unroll
+        for (int j = 0; j < kSwN; ++j) {
+          if (j < rend) {
+            const int row = row0 + j;
+            const float v = __uint_as_float(r[j]) * sc_ch;
+            if constexpr (EPI == EPI_COMBINE1) {
+              const int tok = __ldg(a.row_token + row);
+              if (in_bounds(tok >= 0 && tok < a.T_tokens, a.status)) {
+                const float gt = __ldg(a.gate + tok);
+                static_cast<__nv_bfloat16*>(a.y)[(size_t)tok * a.ld_y + ch] =
+                    __float2bfloat16_rn(fmaf(gt, v, 0.f));
+              }
+            } else {
+              static_cast<__nv_bfloat16*>(a.out)[(size_t)row * a.ld_out + ch] =
+                  __float2bfloat16_rn(v);
+            }
+          }
+        }
+      }
     }
   }
 
@@ -2170,6 +2537,17 @@ static cudaError_t run_f8w(const TcMaps& m, const CUtensorMap& mW, const TcArgs&
   cudaError_t e = smem_attr_once(kern, C::SMEM, attr_done);
   if (e != cudaSuccess) return e;
   return launch_pdl(kern, dim3(grid), dim3(C::THREADS), C::SMEM, st, m.A, m.A32, mW, a);
+}
+
+template <int EPI>
+static cudaError_t run_f8s(const TcMaps& m, const CUtensorMap& mW, const TcArgs& a, int grid,
+                           cudaStream_t st) {
+  using C = F8sCfg<EPI>;
+  static std::atomic<uint64_t> attr_done{0};
+  auto kern = tc_down_f8s<EPI>;
+  cudaError_t e = smem_attr_once(kern, C::SMEM, attr_done);
+  if (e != cudaSuccess) return e;
+  return launch_pdl(kern, dim3(grid), dim3(C::THREADS), C::SMEM, st, m.A32, mW, a);
 }
 
 static cudaError_t dispatch_down_f8w(int bn, bool combine1, const TcMaps& m, const CUtensorMap& mW,
@@ -2413,10 +2791,23 @@ cudaError_t launch_experts_tc(const Plan& p, const void* x, const void* W1, cons
     if (!encode_3d_codes(&mW, W2, c.E, c.d, c.f, p.dn_bn)) return cudaErrorInvalidValue;
     TcArgs a8 = ad;
     a8.b0_scale = W2s;
+    a8.sched_bn = p.dn_bn;
+    CUtensorMap mWs;
+    if (p.dn_swap && !encode_3d_codes(&mWs, W2, c.E, c.d, c.f, F8sCfg<EPI_OUT16>::BNH,
+                                      F8sCfg<EPI_OUT16>::KB))
+      return cudaErrorInvalidValue;
     cudaError_t e = p.fp8 ? dispatch_up_f8(p.up_bn, mu, au, grid_up, st)
                           : dispatch_up(as, p.up_bn, c.act, mu, au, grid_up, st, p.cluster2_up);
     if (e != cudaSuccess) return e;
     if (mid_event && (e = cudaEventRecord(mid_event, st)) != cudaSuccess) return e;
+    if (p.dn_swap) {
+      // tiles of 128 output channels: the down tile count scaled to that width
+      const int nt_s = (c.d + F8sCfg<EPI_OUT16>::BNH - 1) / F8sCfg<EPI_OUT16>::BNH;
+      const long long tiles = (long long)(p.R_cap / kTcBM) * nt_s;
+      const int grid = tiles < p.num_sms ? (int)tiles : p.num_sms;
+      return p.combine_in_down ? run_f8s<EPI_COMBINE1>(md, mWs, a8, grid, st)
+                               : run_f8s<EPI_OUT16>(md, mWs, a8, grid, st);
+    }
     return dispatch_down_f8w(p.dn_bn, p.combine_in_down, md, mW, a8, grid_dn, st);
   }
   if (p.fused) {

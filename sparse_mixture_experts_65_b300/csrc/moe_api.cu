@@ -41,7 +41,7 @@ int make_plan(const moe_config* cfg, WsKind kind, Plan* p, int num_sms);
 
 // Process-wide overrides set through moe_set_tuning (tests and tile sweeps
 // only); -1 = no override.  Production calls never read the environment.
-static std::atomic<int> g_tune[MOE_TUNE_COUNT] = {-1, -1, -1, -1, -1, -1, -1, -1, -1};
+static std::atomic<int> g_tune[MOE_TUNE_COUNT] = {-1, -1, -1, -1, -1, -1, -1, -1, -1, -1};
 
 int tuning(int knob) {
   return knob >= 0 && knob < MOE_TUNE_COUNT ? g_tune[knob].load(std::memory_order_relaxed) : -1;
@@ -287,6 +287,14 @@ int make_plan(const moe_config* cfg, WsKind kind, Plan* p, int num_sms) {
   {
     const int fp = tuning(MOE_TUNE_FUSED_PROJ);
     P.fused = updown_eligible(P) && (fp == 1 || (fp < 0 && updown_default(P)));
+  }
+  // e4m3 down weights (moe_forward_fp8_all): the weights as the MMA's M
+  // operand where expert segments average at most one row (the smallest
+  // decode batches: measured faster there, slower from two rows on), else as
+  // its N operand
+  {
+    const int sw = tuning(MOE_TUNE_F8_DOWN_FORM);
+    P.dn_swap = P.fp8 && (sw == 1 || (sw < 0 && Tk <= (long long)c.E));
   }
 
   // ---- workspace layout ----
@@ -969,7 +977,8 @@ int moe_set_tuning(int32_t knob, int32_t value) {
   if (knob == MOE_TUNE_ROUTER && value > MOE_ROUTER_TC) return MOE_ERR_ARG;
   if (knob == MOE_TUNE_GATHER && value > 2) return MOE_ERR_ARG;
   if ((knob == MOE_TUNE_MMA_M64 || knob == MOE_TUNE_FUSED_COMBINE ||
-       knob == MOE_TUNE_CLUSTER || knob == MOE_TUNE_FUSED_PROJ) && value > 1)
+       knob == MOE_TUNE_CLUSTER || knob == MOE_TUNE_FUSED_PROJ ||
+       knob == MOE_TUNE_F8_DOWN_FORM) && value > 1)
     return MOE_ERR_ARG;
   g_tune[knob].store(value, std::memory_order_relaxed);
   return MOE_OK;

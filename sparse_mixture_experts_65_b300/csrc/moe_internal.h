@@ -125,6 +125,7 @@ struct Plan {
   bool cluster2_dn;           // the same for the down projection
   bool fp8;                   // gate/up weights in e4m3: quantised rows, fp8 up projection
   bool fused;                 // up and down projections in one persistent launch
+  bool dn_swap;               // e4m3 down weights: the weights as the MMA's M operand
   int num_sms;
   WsLayout ws;
 };

@@ -65,15 +65,16 @@ inline bool encode_3d(CUtensorMap* m, const void* ptr, uint64_t n_mat, uint64_t 
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// 3-D map over [n_mat][rows][cols] bytes (e4m3 codes) for tiles of 64 bytes
-// of a row x box_rows x 1, not swizzled (the tile is expanded on chip).
+// 3-D map over [n_mat][rows][cols] bytes (e4m3 codes) for tiles of box_bytes
+// (64 or 128) of a row x box_rows x 1, not swizzled (the tile is expanded on
+// chip); the bytes move as 16-bit units.
 inline bool encode_3d_codes(CUtensorMap* m, const void* ptr, uint64_t n_mat, uint64_t rows,
-                            uint64_t cols, uint32_t box_rows) {
+                            uint64_t cols, uint32_t box_rows, uint32_t box_bytes = 64) {
   EncodeTiledFn fn = get_encode_fn();
   if (!fn) return false;
   cuuint64_t dims[3] = {cols / 2, rows, n_mat};
   cuuint64_t strides[2] = {cols, rows * cols};
-  cuuint32_t box[3] = {32u, box_rows, 1};
+  cuuint32_t box[3] = {box_bytes / 2, box_rows, 1};
   cuuint32_t es[3] = {1, 1, 1};
   return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT16, 3, const_cast<void*>(ptr), dims, strides, box, es,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,

@@ -243,7 +243,8 @@ _TUNE_KNOBS = {"router": N.MOE_TUNE_ROUTER, "gather": N.MOE_TUNE_GATHER,
                "tile_n_up": N.MOE_TUNE_TILE_N_UP, "tile_n_down": N.MOE_TUNE_TILE_N_DOWN,
                "partial_a_rows": N.MOE_TUNE_PARTIAL_A_ROWS,
                "mma_m64": N.MOE_TUNE_MMA_M64, "fused_combine": N.MOE_TUNE_FUSED_COMBINE,
-               "cluster": N.MOE_TUNE_CLUSTER, "fused_proj": N.MOE_TUNE_FUSED_PROJ}
+               "cluster": N.MOE_TUNE_CLUSTER, "fused_proj": N.MOE_TUNE_FUSED_PROJ,
+               "f8_down_form": N.MOE_TUNE_F8_DOWN_FORM}
 _ROUTERS = {"simt": N.MOE_ROUTER_SIMT, "fused": N.MOE_ROUTER_FUSED, "tc": N.MOE_ROUTER_TC}
 
 

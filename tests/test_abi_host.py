@@ -267,6 +267,10 @@ def test_fp8_entry_point_checks_without_gpu():
     assert "fused_projections" in L.plan_flags(dec)
     assert not {"fused_projections", "gather_rows"} & L.plan_flags(dec, fp8=True)
     assert "route_decode" in L.plan_flags(dec, fp8=True)
+    # the knob of the e4m3 down projection's form takes 0 and 1 only
+    assert N.lib().moe_set_tuning(N.MOE_TUNE_F8_DOWN_FORM, 2) == N.MOE_ERR_ARG
+    with L.tuning(f8_down_form=1):
+        assert L.launch_count(L.config_for(W.get("gptoss16_fp8")), fp8=True) == 5
     # forcing the split router (tensor-core logits, top-k, permute)
     with L.tuning(router="tc"):
         assert L.launch_count(L.config_for(W.get("gptoss256")), fp8=False) == 6

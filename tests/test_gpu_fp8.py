@@ -230,3 +230,30 @@ def test_fp8_down_weight_code_ranges(codes):
     assert torch.count_nonzero(out.y) > out.y.numel() // 2
     rep = check_layer(inp, out)
     print(codes, rep)
+
+
+@pytest.mark.parametrize("form", [0, 1], ids=["weights_as_n", "weights_as_m"])
+@pytest.mark.parametrize("shape", FP8_ALL, ids=lambda s: s.name)
+def test_fp8_down_weight_both_kernel_forms(shape, form):
+    """Both down-projection forms (weights as the MMA's N operand, or as its M
+    operand with 32 token rows per pass: segments of more than 32 rows take
+    several passes) on every shape, whichever the plan would pick."""
+    inp = W.make_inputs(shape, "cuda", seed=9)
+    with L.tuning(f8_down_form=form):
+        cfg = L.config_for(shape)
+        _, out = run_gpu(inp, cfg)
+    rep = check_layer(inp, out)
+    print(shape.name, form, rep)
+
+
+def test_fp8_down_weight_many_rows_per_segment_weights_as_m():
+    """Weights as M with segments of up to ~200 rows (several 32-row passes
+    and several 128-row M tiles per expert), a ragged d and f."""
+    shape = LayerShape("fp8all_long_segments", 81, T=1500, d=336, E=8, k=1, f=272, act=SW,
+                       gate=TOPK, dtype="bf16", w_fp8=True, w2_fp8=True)
+    inp = W.make_inputs(shape, "cuda", seed=10)
+    with L.tuning(f8_down_form=1):
+        cfg = L.config_for(shape)
+        _, out = run_gpu(inp, cfg)
+    rep = check_layer(inp, out)
+    print(rep)
