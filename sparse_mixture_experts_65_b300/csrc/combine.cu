@@ -2,7 +2,8 @@
 // over the kept slots, accumulated in float32 in the fixed order j = 0..k-1
 // (no atomics), then rounded once to the output dtype.  The routed expert
 // outputs o arrive in the layer dtype (bf16 on the tensor-core path, float32
-// on the float32 path), the shared expert's in float32 on both.
+// on the float32 path), the shared expert's in float32 on the float32 path
+// and as scaled fp16 on the tensor-core path (shared_out.cuh).
 //
 // "Mixture of Experts" (llm-tutorial ch. 11) § The mathematics and
 // "Mixture-of-Experts" (neural networks visually) § Show the math: the layer
@@ -12,12 +13,15 @@
 #include "common.cuh"
 #include "launch.cuh"
 #include "moe_internal.h"
+#include "shared_out.cuh"
 
 namespace moe {
 
 struct CombineArgs {
   const void* o;         // [R_cap][d] TOut
-  const void* os;        // [T_pad][d] TOut, or null
+  const void* os;        // [T_pad][d]: float32 (float32 path) or scaled fp16; or null
+  const int8_t* os_exp;  // [T_pad][ld_exp] chunk exponents of the scaled fp16 form
+  int ld_exp;
   const int* key_row;    // [T*k]
   const float* topk_w;   // [T*k]
   void* y;               // [T][d]
@@ -61,11 +65,22 @@ __global__ void __launch_bounds__(kThreads) combine_kernel(const CombineArgs a) 
   }
   __syncthreads();
   const TOut* o = static_cast<const TOut*>(a.o);
-  const float* os = static_cast<const float*>(a.os);
   TOut* y = static_cast<TOut*>(a.y);
   for (int c = threadIdx.x * 4; c < a.d; c += kThreads * 4) {
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (os) acc = load4(os, (size_t)t * a.d + c);
+    if (a.os) {
+      if constexpr (sizeof(TOut) == 4) {
+        acc = load4(static_cast<const float*>(a.os), (size_t)t * a.d + c);
+      } else {
+        // four scaled fp16 values of one 32-column chunk
+        const uint2 u =
+            *reinterpret_cast<const uint2*>(static_cast<const __half*>(a.os) + (size_t)t * a.d + c);
+        const float s = sh_pow2(a.os_exp[(size_t)t * a.ld_exp + c / kShChunk]);
+        const float2 f0 = __half22float2(*reinterpret_cast<const __half2*>(&u.x));
+        const float2 f1 = __half22float2(*reinterpret_cast<const __half2*>(&u.y));
+        acc = make_float4(f0.x * s, f0.y * s, f1.x * s, f1.y * s);
+      }
+    }
     for (int j = 0; j < a.k; ++j) {
       const int r = rows[j];
       if (r < 0) continue;
@@ -98,15 +113,13 @@ __global__ void __launch_bounds__(kThreads) combine_bf16x8_kernel(const CombineA
   }
   __syncthreads();
   const __nv_bfloat16* o = static_cast<const __nv_bfloat16*>(a.o);
-  const float* os = static_cast<const float*>(a.os);
+  const __half* os = static_cast<const __half*>(a.os);
   __nv_bfloat16* y = static_cast<__nv_bfloat16*>(a.y);
   for (int c = threadIdx.x * 8; c < a.d; c += kThreads * 8) {
     float acc[8];
     if (os) {
-      const float4* src = reinterpret_cast<const float4*>(os + (size_t)t * a.d + c);
-      const float4 u0 = src[0], u1 = src[1];
-      acc[0] = u0.x; acc[1] = u0.y; acc[2] = u0.z; acc[3] = u0.w;
-      acc[4] = u1.x; acc[5] = u1.y; acc[6] = u1.z; acc[7] = u1.w;
+      const uint4 u = *reinterpret_cast<const uint4*>(os + (size_t)t * a.d + c);
+      sh_decode8(u, a.os_exp[(size_t)t * a.ld_exp + c / kShChunk], acc);
     } else {
 #pragma unroll
       for (int i = 0; i < 8; ++i) acc[i] = 0.f;
@@ -151,6 +164,8 @@ cudaError_t launch_combine(const Plan& p, const float* topk_w, void* y, void* ws
   char* w = static_cast<char*>(ws);
   a.o = w + p.ws.o;
   a.os = p.cfg.n_shared ? static_cast<const void*>(w + p.ws.os) : nullptr;
+  a.os_exp = p.cfg.n_shared && p.tc ? reinterpret_cast<const int8_t*>(w + p.ws.os_exp) : nullptr;
+  a.ld_exp = (p.cfg.d + kShChunk - 1) / kShChunk;
   a.key_row = reinterpret_cast<const int*>(w + p.ws.key_row);
   a.topk_w = topk_w;
   a.y = y;

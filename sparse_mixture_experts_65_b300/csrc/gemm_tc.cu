@@ -36,6 +36,7 @@
 #include "launch.cuh"
 #include "moe_internal.h"
 #include "ptx.cuh"
+#include "shared_out.cuh"
 #include "tma_host.cuh"
 
 namespace moe {
@@ -86,6 +87,8 @@ struct TcArgs {
   int ld_out;
   void* out_sh;           // shared output rows [T_pad][ld_out_sh]
   int ld_out_sh;
+  int8_t* out_sh_exp = nullptr;   // down projection: the shared output's chunk exponents
+  int ld_out_sh_exp = 0;          // [T_pad][ld_out_sh_exp]
   const float* col_bias;  // EPI_F32_CHUNKED: added per output column (may be null)
   int partial_rows;       // A tiles with at most this many real rows load 32-row boxes
   const int* row_token;   // token of each expert-ordered row (gather, EPI_COMBINE1)
@@ -284,21 +287,38 @@ __device__ __forceinline__ void epilogue_tile(const TcArgs& a, const TileInfo& t
     tmem_ld_wait();
     const int col = ti.n0 + c;
     if ((EPI == EPI_OUT16 || EPI == EPI_COMBINEK) && ti.shared) {
-      // the shared expert's output stays float32 until the combine adds the
-      // routed slots to it: it enters y with weight 1, and a bf16 rounding
-      // here would add up to half a bf16 ulp of |y| to the layer's error
-      if (!row_ok) continue;
-      float* dstf = static_cast<float*>(a.out_sh) + orow * a.ld_out_sh + col;
+      // the shared expert's output: fp16 scaled by 2^-e per 32-column chunk
+      // (shared_out.cuh); columns past N hold zeros (their weights load as
+      // zeros), so they do not move the chunk's maximum
+      if (!row_ok || col >= ti.N) continue;   // past the last column: nothing to store
+      float amax = 0.f;
+#pragma unroll
+      for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(__uint_as_float(r0[i])));
+      const int e = sh_chunk_exponent(amax);
+      const float s = sh_pow2(-e);
+      uint32_t ph[16];
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        __half2 h2 = __floats2half2_rn(__uint_as_float(r0[2 * i]) * s,
+                                       __uint_as_float(r0[2 * i + 1]) * s);
+        ph[i] = *reinterpret_cast<uint32_t*>(&h2);
+      }
+      __half* dsth = static_cast<__half*>(a.out_sh) + orow * a.ld_out_sh + col;
+      a.out_sh_exp[orow * a.ld_out_sh_exp + col / kShChunk] = static_cast<int8_t>(e);
       if (col + 32 <= ti.N) {
 #pragma unroll
-        for (int v = 0; v < 8; ++v)
-          reinterpret_cast<float4*>(dstf)[v] =
-              make_float4(__uint_as_float(r0[4 * v]), __uint_as_float(r0[4 * v + 1]),
-                          __uint_as_float(r0[4 * v + 2]), __uint_as_float(r0[4 * v + 3]));
+        for (int v = 0; v < 4; ++v)
+          reinterpret_cast<uint4*>(dsth)[v] =
+              make_uint4(ph[4 * v], ph[4 * v + 1], ph[4 * v + 2], ph[4 * v + 3]);
       } else {
 #pragma unroll
-        for (int i = 0; i < 32; ++i)
-          if (col + i < ti.N) dstf[i] = __uint_as_float(r0[i]);
+        for (int i = 0; i < 32; ++i) {
+          if (col + i < ti.N) {
+            const uint32_t w = ph[i >> 1];
+            reinterpret_cast<uint16_t*>(dsth)[i] =
+                (i & 1) ? static_cast<uint16_t>(w >> 16) : static_cast<uint16_t>(w);
+          }
+        }
       }
       continue;
     }
@@ -436,17 +456,17 @@ __device__ __forceinline__ void combine_slice(const TcArgs& a, const TileInfo& t
   const int ncol = ti.N - ti.n0 < BNH ? ti.N - ti.n0 : BNH;
   const bool act = c < ncol;
   const __nv_bfloat16* o = static_cast<const __nv_bfloat16*>(a.out);
-  const float* os = static_cast<const float*>(a.out_sh);   // float32 shared output
+  const __half* os = static_cast<const __half*>(a.out_sh);   // scaled fp16 shared output
   const int* kr = a.key_row + (size_t)t * a.k_slots;
   const float* gt = a.gate + (size_t)t * a.k_slots;
   float acc[8];
 #pragma unroll
   for (int i = 0; i < 8; ++i) acc[i] = 0.f;
   if (a.has_shared && act) {
-    const float4* src = reinterpret_cast<const float4*>(os + (size_t)t * a.ld_out_sh + ti.n0 + c);
-    const float4 u0 = __ldcg(src), u1 = __ldcg(src + 1);
-    acc[0] = u0.x; acc[1] = u0.y; acc[2] = u0.z; acc[3] = u0.w;
-    acc[4] = u1.x; acc[5] = u1.y; acc[6] = u1.z; acc[7] = u1.w;
+    const int col = ti.n0 + c;
+    const uint4 u = __ldcg(reinterpret_cast<const uint4*>(os + (size_t)t * a.ld_out_sh + col));
+    const int e = a.out_sh_exp[(size_t)t * a.ld_out_sh_exp + col / kShChunk];
+    sh_decode8(u, e, acc);
   }
   for (int j0 = 0; j0 < a.k_slots; j0 += 8) {
     int r[8];
@@ -2783,6 +2803,8 @@ cudaError_t launch_experts_tc(const Plan& p, const void* x, const void* W1, cons
   ad.ld_out = c.d;
   ad.out_sh = sh ? static_cast<void*>(w + p.ws.os) : nullptr;
   ad.ld_out_sh = sh ? c.d : 0;
+  ad.out_sh_exp = sh ? reinterpret_cast<int8_t*>(w + p.ws.os_exp) : nullptr;
+  ad.ld_out_sh_exp = sh ? (c.d + kShChunk - 1) / kShChunk : 0;
   const int grid_dn = p.max_tiles_dn < p.num_sms ? p.max_tiles_dn : p.num_sms;
   if (W2s != nullptr) {
     // e4m3 down weights: the codes by 64-byte tiles, expanded on chip

@@ -333,9 +333,11 @@ int make_plan(const moe_config* cfg, WsKind kind, Plan* p, int num_sms) {
     L.o = take((size_t)P.R_cap * c.d * P.elem);
     if (c.n_shared) {
       L.hs = take((size_t)P.T_pad * c.f_shared * act_elem);
-      // the shared expert's output in float32 on both paths: it enters y with
-      // weight 1, so it is rounded only once, in y
-      L.os = take((size_t)P.T_pad * c.d * sizeof(float));
+      // the shared expert's output: float32 on the float32 path; fp16 with a
+      // power-of-two exponent per 32-column chunk on the tensor-core path
+      // (shared_out.cuh)
+      L.os = take((size_t)P.T_pad * c.d * (P.tc ? 2 : 4));
+      L.os_exp = take(P.tc ? (size_t)P.T_pad * ((c.d + 31) / 32) : 0);
     }
     // sized for the narrowest down tile (64 columns), so that the layout does
     // not depend on the tiling (which follows the GPU's SM count)

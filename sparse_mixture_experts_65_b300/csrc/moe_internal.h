@@ -79,7 +79,9 @@ struct WsLayout {
   size_t h;           // dtype  [R_cap][f] expert hidden activations
   size_t o;           // dtype  [R_cap][d] expert outputs
   size_t hs;          // dtype  [T_pad][f_s] shared-expert hidden
-  size_t os;          // dtype  [T_pad][d]   shared-expert output
+  size_t os;          // [T_pad][d] shared-expert output: float32 (float32 path), or fp16
+                      //        scaled per 32-column chunk (tensor-core path)
+  size_t os_exp;      // int8   [T_pad][ceil(d/32)] the chunk exponents (tensor-core path)
   size_t cmb_ctr;     // uint32 [T][N tiles of the down projection]: combine arrival counters
   // host-io staging
   size_t x_dev, y_dev, topk_idx, topk_w, counts, aux;
