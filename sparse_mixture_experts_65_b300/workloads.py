@@ -81,6 +81,11 @@ def get(name: str) -> LayerShape:
         return replace(base, name=base.name + "_fp8", w_fp8=True)
     if name.startswith("gptoss") and name != "gptoss":
         return GPTOSS.with_T(int(name[len("gptoss"):].lstrip("_T")))
+    if name == "dsv3_e32":
+        # the DeepSeek-V3-shaped layer with 32 routed experts and T = 640 (the
+        # same ~160 rows per expert, 2 GB of weights): a case small enough for
+        # multi-pass counter captures of the same kernels
+        return replace(DSV3, name="dsv3_e32", T=640, E=32)
     return WORKLOADS[name]
 
 
