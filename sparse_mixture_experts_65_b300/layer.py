@@ -347,6 +347,18 @@ class BoundForwardFp8(BoundForward):
             self._timed = N.lib().moe_forward_fp8_all_timed
 
 
+def capture_graph(bound, stream) -> torch.cuda.CUDAGraph:
+    """A CUDA graph holding one call of a bound layer call (constructed with
+    `stream`, a non-default stream): a call only enqueues kernels (no host
+    synchronisation, no allocation), so replaying the graph re-runs the layer
+    on the same buffers.  Call `bound` once before capturing (first calls set
+    per-device kernel attributes)."""
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        bound()
+    return g
+
+
 def bound_forward(cfg: N.MoeConfig, inp, stream=None, workspace=None) -> BoundForward:
     """The bound call for a workload's inputs (fp8 gate/up weights or not;
     fp8 down weights when the inputs carry W2q)."""

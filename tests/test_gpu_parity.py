@@ -620,3 +620,32 @@ def test_fused_projections_match_two_launches_bitwise(case):
     assert torch.equal(one.y, two.y)
     assert torch.equal(again.y, one.y)
     check_layer(inp, one)
+
+
+@pytest.mark.parametrize("shape", [SMALL[2], ONE_LAUNCH[0], DECODE[1], ROUTE_WIDE[0]],
+                         ids=lambda s: s.name)
+def test_layer_call_replays_from_a_cuda_graph(shape):
+    """One layer call captured in a CUDA graph (kernels only: no host
+    synchronisation or allocation inside a call) replays to the direct call's
+    outputs bit for bit, with the device status clean."""
+    inp = W.make_inputs(shape, "cuda", seed=31)
+    cfg = L.config_for(shape)
+    stream = torch.cuda.Stream()
+    with torch.cuda.stream(stream):
+        direct = L.bound_forward(cfg, inp, stream=stream)
+        direct()
+        stream.synchronize()
+        ref = {n: getattr(direct.out, n).clone()
+               for n in ("y", "topk_idx", "topk_w", "expert_counts", "aux_loss", "slot_pos")}
+        bound = L.bound_forward(cfg, inp, stream=stream)
+        bound()
+        stream.synchronize()
+        g = L.capture_graph(bound, stream)
+        for n in ("y", "topk_w"):
+            getattr(bound.out, n).zero_()
+        for _ in range(3):
+            g.replay()
+        stream.synchronize()
+    assert L.check_status(bound.workspace) == 0
+    for n, t in ref.items():
+        assert torch.equal(getattr(bound.out, n), t), n
