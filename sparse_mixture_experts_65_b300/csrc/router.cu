@@ -522,14 +522,22 @@ __global__ void __launch_bounds__(kSmallThreads) route_small_kernel(const SmallA
       for (int j = 0; j < V; ++j) ws[(kk + j) * Ep + e] = v[j];
     }
     __syncthreads();
-    // thread (expert e, group of 4 tokens): a weight value is loaded once for
-    // the 4 tokens, the x values 4 k at a time (16-byte loads); every output
-    // still sums its 128 products in k order
+    // thread (expert e, group of 4 tokens, part kq of the slice): a weight
+    // value is loaded once for the 4 tokens, the x values 4 k at a time
+    // (16-byte loads).  Where expert x token-group items leave threads idle
+    // (small T), the slice's 128 k are split into KQ parts summed in k order
+    // by different threads, then added in part order; otherwise every output
+    // sums its 128 products in k order.
     const int ngrp = (T + 3) / 4;
-    for (int i = tid; i < E * ngrp; i += kSmallThreads) {
-      const int e = i % E, t0 = (i / E) * 4;
+    int KQ = 1;
+    while (KQ < 4 && E * ngrp * KQ * 2 <= kSmallThreads) KQ *= 2;
+    const int kw = kSmallKs / KQ;
+    float* red = ws + kSmallKs * Ep;                     // [KQ][T][E] part sums
+    for (int i = tid; i < E * ngrp * KQ; i += kSmallThreads) {
+      const int e = i % E, rest = i / E;
+      const int t0 = (rest % ngrp) * 4, kq = rest / ngrp;
       float acc[4] = {0.f, 0.f, 0.f, 0.f};
-      for (int kk = 0; kk < kSmallKs; kk += 4) {
+      for (int kk = kq * kw; kk < (kq + 1) * kw; kk += 4) {
         const float w0 = ws[kk * Ep + e], w1 = ws[(kk + 1) * Ep + e];
         const float w2 = ws[(kk + 2) * Ep + e], w3 = ws[(kk + 3) * Ep + e];
 #pragma unroll
@@ -544,8 +552,21 @@ __global__ void __launch_bounds__(kSmallThreads) route_small_kernel(const SmallA
         }
       }
 #pragma unroll
-      for (int j = 0; j < 4; ++j)
-        if (t0 + j < T) a.part[((size_t)s * T + t0 + j) * E + e] = acc[j];
+      for (int j = 0; j < 4; ++j) {
+        if (t0 + j >= T) continue;
+        if (KQ == 1)
+          a.part[((size_t)s * T + t0 + j) * E + e] = acc[j];
+        else
+          red[((size_t)kq * T + t0 + j) * E + e] = acc[j];
+      }
+    }
+    if (KQ > 1) {
+      __syncthreads();
+      for (int i = tid; i < T * E; i += kSmallThreads) {
+        float v = red[i];
+        for (int kq = 1; kq < KQ; ++kq) v += red[(size_t)kq * T * E + i];
+        a.part[(size_t)s * T * E + i] = v;
+      }
     }
   }
   __threadfence();
@@ -577,21 +598,54 @@ __global__ void __launch_bounds__(kSmallThreads) route_small_kernel(const SmallA
       bulk_load(smem_u32(stage) + t * row_bytes, static_cast<const char*>(a.x) + (size_t)t * row_bytes,
                 row_bytes, smem_u32(xbar));
   }
-  for (int i = tid; i < T * E; i += kSmallThreads) {
-    const int t = i / E, e = i - t * E;
-    const float* pp = a.part + (size_t)t * E + e;
-    const size_t ss = (size_t)T * E;   // slice stride
-    float l = 0.f;
-    // up to 32 loads in flight, added in slice order
-    for (int s0 = 0; s0 < a.S; s0 += 32) {
-      float v[32];
+  const int TE = T * E;
+  if (TE <= kSmallThreads || (TE & 3)) {
+    for (int i = tid; i < TE; i += kSmallThreads) {
+      const int t = i / E, e = i - t * E;
+      const float* pp = a.part + (size_t)t * E + e;
+      const size_t ss = (size_t)TE;   // slice stride
+      float l = 0.f;
+      // up to 32 loads in flight, added in slice order
+      for (int s0 = 0; s0 < a.S; s0 += 32) {
+        float v[32];
 #pragma unroll
-      for (int u = 0; u < 32; ++u) v[u] = s0 + u < a.S ? __ldcg(pp + (size_t)(s0 + u) * ss) : 0.f;
+        for (int u = 0; u < 32; ++u) v[u] = s0 + u < a.S ? __ldcg(pp + (size_t)(s0 + u) * ss) : 0.f;
 #pragma unroll
-      for (int u = 0; u < 32; ++u)
-        if (s0 + u < a.S) l += v[u];
+        for (int u = 0; u < 32; ++u)
+          if (s0 + u < a.S) l += v[u];
+      }
+      lg[t * E + e] = l + (a.logit_offset ? a.logit_offset[e] : 0.f);
     }
-    lg[t * E + e] = l + (a.logit_offset ? a.logit_offset[e] : 0.f);
+  } else {
+    // more outputs than threads: four consecutive outputs per thread
+    // (16-byte loads), 16 slices in flight, the same additions in slice order
+    const float4* p4 = reinterpret_cast<const float4*>(a.part);
+    const int n4 = TE / 4;
+    for (int i4 = tid; i4 < n4; i4 += kSmallThreads) {
+      float4 l = make_float4(0.f, 0.f, 0.f, 0.f);
+      for (int s0 = 0; s0 < a.S; s0 += 16) {
+        float4 v[16];
+#pragma unroll
+        for (int u = 0; u < 16; ++u)
+          v[u] = s0 + u < a.S ? __ldcg(p4 + (size_t)(s0 + u) * n4 + i4)
+                              : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int u = 0; u < 16; ++u) {
+          if (s0 + u < a.S) {
+            l.x += v[u].x;
+            l.y += v[u].y;
+            l.z += v[u].z;
+            l.w += v[u].w;
+          }
+        }
+      }
+      const int i = 4 * i4;
+      const float* off = a.logit_offset;
+      lg[i] = l.x + (off ? off[i % E] : 0.f);
+      lg[i + 1] = l.y + (off ? off[(i + 1) % E] : 0.f);
+      lg[i + 2] = l.z + (off ? off[(i + 2) % E] : 0.f);
+      lg[i + 3] = l.w + (off ? off[(i + 3) % E] : 0.f);
+    }
   }
   for (int e = tid; e < E; e += kSmallThreads) cnt[e] = 0;
   __syncthreads();
@@ -742,7 +796,10 @@ __global__ void __launch_bounds__(kSmallThreads) route_small_kernel(const SmallA
 }
 
 size_t route_small_smem(int E) {
-  const size_t p1 = sizeof(float) * ((size_t)kSmallT * kSmallKs + (size_t)kSmallKs * (E + 1));
+  // x and weight slices, then the part sums of the split dot products (at
+  // most 4 parts x 4 token groups' worth of outputs per thread: 4 x 512 x 4)
+  const size_t p1 = sizeof(float) * ((size_t)kSmallT * kSmallKs + (size_t)kSmallKs * (E + 1) +
+                                     (size_t)4 * kSmallThreads * 4);
   const size_t p2 = sizeof(float) * ((size_t)kSmallT * kMaxE + (kSmallThreads / 32) * kMaxE) +
                     sizeof(int) * ((size_t)kMaxE + kSmallT * kMaxK) +
                     sizeof(ScanSmem<kSmallThreads>) + 128 + kSmallStage + 8 * (kBulkIssuers + 1);
