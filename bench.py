@@ -667,7 +667,7 @@ def layer_roofline(layer, ms_step, peaks):
             "active_experts": layer["active_experts"], "kept_rows": layer["kept_rows"]}
 
 
-# The benchmark spec's two targets, measured in the default run beside the
+# Two performance targets of the layer, measured in the default run beside the
 # headline: the prefill-shaped layer's grouped GEMM against the bf16 tensor
 # peak, and the decode-shaped layer's active-expert weight streaming against
 # HBM, over the decode sweep.
