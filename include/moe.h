@@ -504,9 +504,9 @@ int moe_plan_flags_fp8(const moe_config* cfg, uint32_t* flags);
  *                            the layer's tiling (down tiles wait, bounded, for
  *                            the up tiles of their rows); 0: always two
  *                            launches; the default takes one launch for the
- *                            forms that measured faster (gathered ReLU up
+ *                            form that measured faster (gathered ReLU up
  *                            projection with the combine in the down
- *                            projection, the 96-column decode tiling);
+ *                            projection);
  *   MOE_TUNE_F8_DOWN_FORM    moe_forward_fp8_all's down projection: 1 the
  *                            weights as the MMA's M operand (128 output
  *                            channels per tile, 32 token rows per pass), 0

@@ -2659,15 +2659,17 @@ bool updown_eligible(const Plan& p) {
                          p.combine_in_down);
 }
 
-// The forms that measured faster as one launch (same box, A/B in one call):
+// The form that measures faster as one launch (same box, A/B in one call):
 // the gathered ReLU up projection with the combine in the down epilogue
-// (Switch-shaped layer 95.0 -> 89.5 us per step) and the 96-column decode
-// form (gpt-oss-shaped T = 1: 65.2 -> 64.6 us).  The 128-column SwiGLU forms
-// did not (DeepSeek-V3-shaped +0.5 %, Mixtral-shaped +1.3 %, gpt-oss-shaped
-// T = 16 +1.2 %): those layers run under the power cap, where closing the
-// idle gap between the projections saves no energy and so no time.
+// (Switch-shaped layer 95.0 -> 89.5 us per step).  The 128-column SwiGLU
+// forms do not (DeepSeek-V3-shaped +0.5 %, Mixtral-shaped +1.3 %, gpt-oss-
+// shaped T = 16 +1.2 %): those layers run under the power cap, where closing
+// the idle gap between the projections saves no energy and so no time.  The
+// 96-column decode form did at first (gpt-oss-shaped T = 1: 65.2 -> 64.6 us),
+// but with the current kernels two launches are ahead (63.4 against 62.5 us
+// per step, three calls).
 bool updown_default(const Plan& p) {
-  return (p.cfg.act == MOE_ACT_RELU && p.combine_in_down) || p.up_bn == 96;
+  return p.cfg.act == MOE_ACT_RELU && p.combine_in_down;
 }
 
 cudaError_t launch_experts_tc(const Plan& p, const void* x, const void* W1, const void* W3,

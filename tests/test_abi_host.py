@@ -262,10 +262,12 @@ def test_fp8_entry_point_checks_without_gpu():
     assert L.launch_count(L.config_for(W.get("gptoss256")), fp8=False) == 4
     assert L.launch_count(L.config_for(W.get("gptoss256_fp8")), fp8=True) == 5
     # the fp8 plan: the row quantisation replaces the gather and the fused
-    # projections (the bf16 decode layer's default form)
+    # projections (compiled for the bf16 decode layer's tiling, opt-in)
     dec = L.config_for(W.get("gptoss1"))
-    assert "fused_projections" in L.plan_flags(dec)
-    assert not {"fused_projections", "gather_rows"} & L.plan_flags(dec, fp8=True)
+    assert "fused_projections" not in L.plan_flags(dec)
+    with L.tuning(fused_proj=1):
+        assert "fused_projections" in L.plan_flags(dec)
+        assert not {"fused_projections", "gather_rows"} & L.plan_flags(dec, fp8=True)
     assert "route_decode" in L.plan_flags(dec, fp8=True)
     # the knob of the e4m3 down projection's form takes 0 and 1 only
     assert N.lib().moe_set_tuning(N.MOE_TUNE_F8_DOWN_FORM, 2) == N.MOE_ERR_ARG
