@@ -257,3 +257,20 @@ def test_fp8_down_weight_many_rows_per_segment_weights_as_m():
         _, out = run_gpu(inp, cfg)
     rep = check_layer(inp, out)
     print(rep)
+
+
+def test_fp8_down_weight_empty_batch_and_combine_override():
+    """T = 0 gives empty outputs and zero counts; the k-slot combine override
+    (no form with e4m3 down weights) is refused before any launch."""
+    shape = FP8_ALL[2]
+    empty = dataclasses.replace(shape, T=0)
+    inp = W.make_inputs(empty, "cuda", seed=12)
+    cfg, out = run_gpu(inp)
+    assert torch.count_nonzero(out.expert_counts) == 0
+    assert float(out.aux_loss.cpu()[0]) == 0.0
+    inp = W.make_inputs(shape, "cuda", seed=12)
+    with L.tuning(fused_combine=1):
+        cfg = L.config_for(shape)
+        with pytest.raises(L.N.MoeError) as e:
+            run_gpu(inp, cfg)
+    assert e.value.code == L.N.MOE_ERR_UNSUPPORTED
