@@ -115,7 +115,7 @@ __global__ void __launch_bounds__(kThreads) combine_bf16x8_kernel(const CombineA
   const __nv_bfloat16* o = static_cast<const __nv_bfloat16*>(a.o);
   const __half* os = static_cast<const __half*>(a.os);
   __nv_bfloat16* y = static_cast<__nv_bfloat16*>(a.y);
-  for (int c = threadIdx.x * 8; c < a.d; c += kThreads * 8) {
+  for (int c = threadIdx.x * 8; c < a.d; c += blockDim.x * 8) {
     float acc[8];
     if (os) {
       const uint4 u = *reinterpret_cast<const uint4*>(os + (size_t)t * a.d + c);
@@ -180,7 +180,10 @@ cudaError_t launch_combine(const Plan& p, const float* topk_w, void* y, void* ws
     // kernel measured faster (Mixtral-shaped 48 vs 52 us, gpt-oss-shaped
     // decode 8 vs 10 us)
     const dim3 g(p.cfg.T), b(kThreads);
-    if (p.cfg.k >= 8) return launch_pdl(combine_bf16x8_kernel<8>, g, b, 0, st, a);
+    // 128 threads per token row for the many-slot kernel: more blocks resident
+    // per SM to cover the slot rows' latency (DeepSeek-V3-shaped 118.0 ->
+    // 115.8 us; 64 threads: 117.5)
+    if (p.cfg.k >= 8) return launch_pdl(combine_bf16x8_kernel<8>, g, dim3(128), 0, st, a);
     return launch_pdl(combine_kernel<__nv_bfloat16>, g, b, 0, st, a);
   }
   return launch_pdl(combine_kernel<float>, dim3(p.cfg.T), dim3(kThreads), 0, st, a);
