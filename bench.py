@@ -176,6 +176,10 @@ def accounting(shape, kept, combine_in_down=False, fused=False):
 
 # dense fp8 over dense bf16 tensor-core rate, nominal (4.5 / 2.25 PFLOP/s)
 FP8_OVER_BF16 = 2.0
+# B300 datasheet figures, reported beside the measured denominators: HBM3e
+# bandwidth and the dense bf16 tensor-core rate
+NOMINAL_HBM_GBS = 7700.0
+NOMINAL_BF16_TFLOPS = 2250.0
 
 
 def roofline_for(stage, acc, ms, peaks, peak_kind, fp8=False):
@@ -193,13 +197,16 @@ def roofline_for(stage, acc, ms, peaks, peak_kind, fp8=False):
         what = ("e4m3 sustained (measured bf16 sustained x 2, the nominal fp8/bf16 ratio)"
                 if mult != 1.0 else "bf16 sustained")
         return {"bound": "tensor", "achieved": round(ach, 2), "peak": peak, "unit": "TFLOP/s",
-                "frac": round(ach / peak, 4), "kernel": stage,
+                "frac": round(ach / peak, 4),
+                "frac_of_nominal": round(ach / (mult * NOMINAL_BF16_TFLOPS), 4),
+                "kernel": stage,
                 "peak_source": f"{peak_kind} {what} (kernel runs inside a seconds-long loop)",
                 "flops_per_launch": a["flops"], "ms_per_launch": round(ms, 5)}
     ach = a["bytes"] / sec / 1e9
     peak = peaks["hbm_gbs"]
     return {"bound": "hbm", "achieved": round(ach, 1), "peak": peak, "unit": "GB/s",
-            "frac": round(ach / peak, 4), "kernel": stage, "peak_source": f"{peak_kind} HBM copy",
+            "frac": round(ach / peak, 4), "frac_of_nominal": round(ach / NOMINAL_HBM_GBS, 4),
+            "kernel": stage, "peak_source": f"{peak_kind} HBM copy",
             "bytes_per_launch": a["bytes"], "traffic_extra": a.get("extra", 0),
             "ms_per_launch": round(ms, 5)}
 
@@ -661,6 +668,7 @@ def measure_layer(shape, K, Wm, stream, dist=None, sample_clocks=True):
 def layer_roofline(layer, ms_step, peaks):
     sec = ms_step / 1e3
     return {"hbm_frac": round(layer["bytes"] / sec / 1e9 / peaks["hbm_gbs"], 4),
+            "hbm_frac_of_nominal": round(layer["bytes"] / sec / 1e9 / NOMINAL_HBM_GBS, 4),
             "tensor_frac_sustained": round(layer["flops"] / sec / 1e12 /
                                            peaks["bf16_tflops_sustained"], 4),
             "bytes_per_step": layer["bytes"], "flops_per_step": layer["flops"],

@@ -176,3 +176,16 @@ def test_fused_projections_count_as_one_kernel():
     assert one["up"]["bytes"] == two["up"]["bytes"] + two["down"]["bytes"]
     assert one["up"]["flops"] == two["up"]["flops"] + two["down"]["flops"]
     assert one["down"]["bytes"] == 0 and lay1 == lay2
+
+
+def test_roofline_reports_the_nominal_peaks_beside_the_measured_ones():
+    peaks = dict(bench.FALLBACK_PEAKS)
+    hbm = bench.roofline_for("down", {"down": {"bytes": 7.7e9, "flops": 1.0}}, 1000.0, peaks,
+                             "fallback")
+    assert hbm["bound"] == "hbm" and abs(hbm["frac_of_nominal"] - 1e-3) < 1e-9
+    ten = bench.roofline_for("up", {"up": {"bytes": 1.0, "flops": 2.25e15}}, 1000.0, peaks,
+                             "fallback")
+    assert ten["bound"] == "tensor" and abs(ten["frac_of_nominal"] - 1.0) < 1e-9
+    f8 = bench.roofline_for("up", {"up": {"bytes": 1.0, "flops": 2.25e15}}, 1000.0, peaks,
+                            "fallback", fp8=True)
+    assert abs(f8["frac_of_nominal"] - 0.5) < 1e-9
