@@ -270,9 +270,15 @@ int moe_launch_count_fp8(const moe_config* cfg, int32_t* launches);
  * count (moe_launch_count_fp8) is moe_forward_fp8's; W2q and W2s 16-byte
  * aligned, else MOE_ERR_ARG; f a multiple of 16 (a row of codes is read by
  * TMA) and no MOE_TUNE_FUSED_COMBINE override of 1, else
- * MOE_ERR_UNSUPPORTED.  moe_forward_fp8_all_timed takes the stage events
- * of moe_forward_fp8_timed; moe_forward_fp8_all_host_io_batches is
- * moe_forward_fp8_host_io_batches for this layer.
+ * MOE_ERR_UNSUPPORTED.  NaN codes (0x7F, 0xFF) are not weights: they are
+ * read as +-480.  The down projection multiplies the weights as the MMA's N
+ * operand (token rows as M), or, where expert segments average at most one
+ * row, as its M operand (MOE_TUNE_F8_DOWN_FORM overrides); the results agree
+ * within float32 accumulation.  moe_forward_fp8_all_timed takes the stage
+ * events of moe_forward_fp8_timed; moe_forward_fp8_all_host_io_batches is
+ * moe_forward_fp8_host_io_batches for this layer.  The e4m3 down weights pay
+ * on decode-sized batches; on prefill-sized ones the on-chip expansion costs
+ * more than the halved weight bytes save.
  */
 int moe_forward_fp8_all(const moe_config* cfg, const void* x, const void* W_r,
                         const float* logit_offset, const float* sel_bias,
