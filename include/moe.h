@@ -273,8 +273,8 @@ int moe_launch_count_fp8(const moe_config* cfg, int32_t* launches);
  * MOE_ERR_UNSUPPORTED.  NaN codes (0x7F, 0xFF) are not weights: they are
  * read as +-480.  The down projection multiplies the weights as the MMA's N
  * operand (token rows as M), or, where expert segments average at most one
- * row, as its M operand (MOE_TUNE_F8_DOWN_FORM overrides); the results agree
- * within float32 accumulation.  moe_forward_fp8_all_timed takes the stage
+ * row in eight, as its M operand (MOE_TUNE_F8_DOWN_FORM overrides); the
+ * results agree within float32 accumulation.  moe_forward_fp8_all_timed takes the stage
  * events of moe_forward_fp8_timed; moe_forward_fp8_all_host_io_batches is
  * moe_forward_fp8_host_io_batches for this layer.  The e4m3 down weights pay
  * on decode-sized batches; on prefill-sized ones the on-chip expansion costs
@@ -518,7 +518,7 @@ int moe_plan_flags_fp8(const moe_config* cfg, uint32_t* flags);
  *                            channels per tile, 32 token rows per pass), 0
  *                            the weights as its N operand (token rows as M);
  *                            the default takes the first where segments
- *                            average at most one row (T*k <= E).
+ *                            average at most one row in eight (8*T*k <= E).
  * Errors: MOE_ERR_ARG for an unknown knob or a value out of range.  Not
  * synchronised with calls in flight on other threads.
  */

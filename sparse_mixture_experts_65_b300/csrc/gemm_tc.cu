@@ -1815,8 +1815,13 @@ tc_down_f8w(const __grid_constant__ CUtensorMap mA, const __grid_constant__ CUte
   int* s_seg = s_tp + (kMaxE + 2);
   int* s_mt = s_seg + (kMaxE + 2);
   int* s_kept = s_mt + (kMaxE + 2);
-  const int nseg = a.E + a.has_shared;
-  for (int i = threadIdx.x; i <= nseg; i += blockDim.x) s_tp[i] = __ldg(a.tp + i);
+  // The prefix counts sched_bn-wide column tiles per M tile, the same number
+  // for every segment (no shared segment on this path), so the prefix of this
+  // kernel's BNH-wide tiles is (tp / nt_sched) * nt.
+  const int nseg = a.E;
+  const int nt_sched = (a.N + a.sched_bn - 1) / a.sched_bn;
+  const int nt = (a.N + BNH - 1) / BNH;
+  for (int i = threadIdx.x; i <= nseg; i += blockDim.x) s_tp[i] = (__ldg(a.tp + i) / nt_sched) * nt;
   for (int i = threadIdx.x; i < nseg; i += blockDim.x) s_mt[i] = __ldg(a.mtiles + i);
   for (int i = threadIdx.x; i < a.E; i += blockDim.x) {
     s_seg[i] = __ldg(a.seg_start + i);
@@ -2065,7 +2070,7 @@ tc_down_f8w(const __grid_constant__ CUtensorMap mA, const __grid_constant__ CUte
 // A stage is free once the converters have read its codes and the MMAs that
 // read its h rows have completed.  Segments of more than 32 rows take one
 // pass per 32 rows, each re-streaming the tile's weights: the plan uses this
-// kernel where segments average at most one row.
+// kernel where segments average at most one row in eight.
 constexpr int kSwN = 32;   // token rows per pass (the MMA's N)
 template <int EPI>
 struct F8sCfg {
@@ -2811,8 +2816,13 @@ cudaError_t launch_experts_tc(const Plan& p, const void* x, const void* W1, cons
   if (W2s != nullptr) {
     // e4m3 down weights: the codes by 64-byte tiles, expanded on chip
     if (sh || p.fused || p.combine_k) return cudaErrorInvalidValue;
+    // the weights-as-N form takes 256-column tiles whatever the bf16 tiling:
+    // it is bound by the MMA instructions it issues, and wider tiles carry
+    // more weight bytes per instruction (gpt-oss-shaped T = 16: 139 -> 130 us,
+    // T = 256: 283 -> 266 us against 192 columns)
+    constexpr int kF8wBn = 256;
     CUtensorMap mW;
-    if (!encode_3d_codes(&mW, W2, c.E, c.d, c.f, p.dn_bn)) return cudaErrorInvalidValue;
+    if (!encode_3d_codes(&mW, W2, c.E, c.d, c.f, kF8wBn)) return cudaErrorInvalidValue;
     TcArgs a8 = ad;
     a8.b0_scale = W2s;
     a8.sched_bn = p.dn_bn;
@@ -2832,7 +2842,9 @@ cudaError_t launch_experts_tc(const Plan& p, const void* x, const void* W1, cons
       return p.combine_in_down ? run_f8s<EPI_COMBINE1>(md, mWs, a8, grid, st)
                                : run_f8s<EPI_OUT16>(md, mWs, a8, grid, st);
     }
-    return dispatch_down_f8w(p.dn_bn, p.combine_in_down, md, mW, a8, grid_dn, st);
+    const long long tiles_w = (long long)(p.R_cap / kTcBM) * ((c.d + kF8wBn - 1) / kF8wBn);
+    const int grid_w = tiles_w < p.num_sms ? (int)tiles_w : p.num_sms;
+    return dispatch_down_f8w(kF8wBn, p.combine_in_down, md, mW, a8, grid_w, st);
   }
   if (p.fused) {
     // both projections in one launch; the up stage event then covers both

@@ -289,12 +289,11 @@ int make_plan(const moe_config* cfg, WsKind kind, Plan* p, int num_sms) {
     P.fused = updown_eligible(P) && (fp == 1 || (fp < 0 && updown_default(P)));
   }
   // e4m3 down weights (moe_forward_fp8_all): the weights as the MMA's M
-  // operand where expert segments average at most one row (the smallest
-  // decode batches: measured faster there, slower from two rows on), else as
-  // its N operand
+  // operand where expert segments average at most one row in eight (the
+  // smallest decode batches: measured faster there), else as its N operand
   {
     const int sw = tuning(MOE_TUNE_F8_DOWN_FORM);
-    P.dn_swap = P.fp8 && (sw == 1 || (sw < 0 && Tk <= (long long)c.E));
+    P.dn_swap = P.fp8 && (sw == 1 || (sw < 0 && 8 * Tk <= (long long)c.E));
   }
 
   // ---- workspace layout ----
