@@ -82,9 +82,10 @@ def get(name: str) -> LayerShape:
     if name.startswith("gptoss") and name != "gptoss":
         return GPTOSS.with_T(int(name[len("gptoss"):].lstrip("_T")))
     if name == "dsv3_e32":
-        # the DeepSeek-V3-shaped layer with 32 routed experts and T = 640 (the
-        # same ~160 rows per expert, 2 GB of weights): a case small enough for
-        # multi-pass counter captures of the same kernels
+        # the DeepSeek-V3-shaped layer with 32 routed experts and T = 640 (160
+        # rows per expert on average against the full layer's 128, 2 GB of
+        # weights): a case small enough for multi-pass counter captures of the
+        # same kernels
         return replace(DSV3, name="dsv3_e32", T=640, E=32)
     return WORKLOADS[name]
 

@@ -189,3 +189,22 @@ def test_roofline_reports_the_nominal_peaks_beside_the_measured_ones():
     f8 = bench.roofline_for("up", {"up": {"bytes": 1.0, "flops": 2.25e15}}, 1000.0, peaks,
                             "fallback", fp8=True)
     assert abs(f8["frac_of_nominal"] - 0.5) < 1e-9
+
+
+def test_workload_names():
+    """Every name the bench and the profiles use resolves to the shape it
+    names: the e4m3 suffixes, the decode sweep and the reduced DeepSeek-V3
+    capture case (160 rows per expert on average, the full layer 128)."""
+    full, small = W.get("dsv3"), W.get("dsv3_e32")
+    assert (small.E, small.T) == (32, 640) and small.d == full.d and small.f == full.f
+    assert small.T * small.k / small.E == 160 and full.T * full.k / full.E == 128
+    assert small.n_shared == full.n_shared and small.gate == full.gate
+    for T in (1, 16, 64, 256):
+        g = W.get(f"gptoss{T}")
+        assert g.T == T and not g.w_fp8
+        f8 = W.get(f"gptoss{T}_fp8")
+        assert f8.w_fp8 and not f8.w2_fp8 and f8.T == T
+        fa = W.get(f"gptoss{T}_fp8all")
+        assert fa.w_fp8 and fa.w2_fp8 and fa.T == T and fa.name == "gptoss_fp8all"
+    m = W.get("mixtral_fp8all")
+    assert m.w2_fp8 and m.f % 16 == 0
