@@ -369,6 +369,86 @@ def check_dense_ffn_special_case():
         np.testing.assert_allclose(r.y, ref, rtol=1e-12, atol=1e-13)
 
 
+def check_elementwise_primitives():
+    """The scalar maps of the stages against library routines in float64 and
+    the identities they satisfy.  sigmoid: scipy's expit, sigma(z) + sigma(-z)
+    = 1, sigma(0) = 1/2.  Row softmax: scipy's softmax, unchanged by a shift of
+    its row, finite at |z| = 1000.  GELU (erf form) and SiLU: torch's, and
+    both odd parts equal z, act(z) - act(-z) = z.  Affinity: the sigmoid of the
+    logit in the sigmoid gate mode, the logit itself in the softmax modes."""
+    from scipy import special
+    z = np.linspace(-40.0, 40.0, 801)
+    np.testing.assert_allclose(O.sigmoid(z), special.expit(z), rtol=1e-14, atol=0)
+    np.testing.assert_allclose(O.sigmoid(z) + O.sigmoid(-z), 1.0, rtol=0, atol=4e-16)
+    assert O.sigmoid(np.array([0.0]))[0] == 0.5
+    rng = _rng(91)
+    S = rng.normal(scale=4.0, size=(7, 13))
+    np.testing.assert_allclose(O.softmax_rows(S), special.softmax(S, axis=-1), rtol=1e-13)
+    shifted = S + 50.0 * rng.normal(size=(7, 1))
+    np.testing.assert_allclose(O.softmax_rows(shifted), O.softmax_rows(S), rtol=1e-11)
+    wide = np.array([[1000.0, 999.0, -1000.0]])
+    got = O.softmax_rows(wide)
+    assert np.all(np.isfinite(got))
+    np.testing.assert_allclose(got, special.softmax(wide, axis=-1), rtol=1e-14)
+    u = np.linspace(-10.0, 10.0, 401)
+    ut = torch.from_numpy(u)
+    np.testing.assert_allclose(O.gelu_erf(u), F.gelu(ut, approximate="none").numpy(),
+                               rtol=1e-13, atol=1e-15)
+    np.testing.assert_allclose(O.silu(u), F.silu(ut).numpy(), rtol=1e-13, atol=1e-15)
+    for act in (O.gelu_erf, O.silu):
+        np.testing.assert_allclose(act(u) - act(-u), u, rtol=0, atol=1e-14)
+        assert act(np.array([0.0]))[0] == 0.0
+    np.testing.assert_allclose(O.affinity(S, O.GATE_SIGMOID_RENORM), special.expit(S),
+                               rtol=1e-14)
+    for mode in (O.GATE_SOFTMAX_TOPK, O.GATE_SOFTMAX_FULL):
+        assert np.array_equal(O.affinity(S, mode), S)
+    try:
+        O.affinity(S, "no such mode")
+    except ValueError:
+        pass
+    else:
+        raise AssertionError("an unknown gate mode must be refused")
+
+
+def check_expert_ffn_rows_bruteforce():
+    """One expert on n rows by explicit sums over every index, with torch's
+    scalar activations (GELU erf form, ReLU, SiLU): f != d so a transposed
+    operand cannot pass; each row is independent of the others; the multiply
+    counter adds n*d*f per projection."""
+    rng = _rng(92)
+    n, d, f = 3, 4, 6
+    X = rng.normal(size=(n, d))
+    W1 = rng.normal(size=(f, d))
+    W3 = rng.normal(size=(f, d))
+    W2 = rng.normal(size=(d, f))
+    scalar_act = {
+        O.ACT_GELU: lambda a: float(F.gelu(torch.tensor(a, dtype=torch.float64),
+                                           approximate="none")),
+        O.ACT_RELU: lambda a: float(F.relu(torch.tensor(a, dtype=torch.float64))),
+    }
+    for act in O.ACTS:
+        ref = np.zeros((n, d))
+        for r in range(n):
+            h = np.zeros(f)
+            for i in range(f):
+                a = sum(W1[i, c] * X[r, c] for c in range(d))
+                if act == O.ACT_SWIGLU:
+                    b = sum(W3[i, c] * X[r, c] for c in range(d))
+                    h[i] = float(F.silu(torch.tensor(a, dtype=torch.float64))) * b
+                else:
+                    h[i] = scalar_act[act](a)
+            for m in range(d):
+                ref[r, m] = sum(W2[m, i] * h[i] for i in range(f))
+        cnt = O.MultiplyCounter()
+        got = O.expert_ffn_rows(X, W1, W2, act, W3=W3 if act == O.ACT_SWIGLU else None,
+                                counter=cnt)
+        np.testing.assert_allclose(got, ref, rtol=1e-12, atol=1e-13)
+        assert cnt.count == n * d * f * (3 if act == O.ACT_SWIGLU else 2)
+        for r in range(n):
+            one = O.expert_ffn(X[r], W1, W2, act, W3=W3 if act == O.ACT_SWIGLU else None)
+            np.testing.assert_allclose(one, ref[r], rtol=1e-12, atol=1e-13)
+
+
 def check_multiply_counts():
     """Toy layer multiplies per token (page figure): 65,536 at top-2 and
     262,144 when all 8 experts fire; SwiGLU experts cost 3*d*f; the active
@@ -630,6 +710,7 @@ ALL_CHECKS = [
     check_gates_invariants, check_router_probs, check_selection_bias,
     check_capacity_formula, check_capacity_drops, check_offsets_and_permutation,
     check_sparse_equals_dense, check_drop_is_identity_branch, check_dense_ffn_special_case,
+    check_elementwise_primitives, check_expert_ffn_rows_bruteforce,
     check_multiply_counts, check_balance_uniform, check_balance_hand_and_collapse,
     check_pipeline_stats_pre_drop, check_z_loss_closed_forms, check_bias_update_rule,
     check_e4m3_format, check_row_scale_rule, check_fp8_layer, check_fp8_down_weights,

@@ -17,7 +17,8 @@ _orig = {name: getattr(M, name) for name in (
     "router_logits", "topk_indices", "topk_gap", "gate_values", "affinity", "expert_capacity",
     "assign_slots", "gelu_erf", "silu", "expert_ffn_rows", "balance_stats", "router_probs",
     "softmax_rows", "router_z_loss", "bias_update", "e4m3_round", "row_scale_exponent",
-    "quantize_rows_e4m3", "moe_forward_fp8")}
+    "quantize_rows_e4m3", "moe_forward_fp8", "sigmoid", "near_tie_tokens", "selection_scores",
+    "permutation_rows", "e4m3_decode")}
 
 
 def _router_reversed(x, W_r, logit_offset=None):
@@ -219,6 +220,42 @@ def _fp8_down_scale_on_input_axis(x, W_r, W1q, W1s, W3q, W3s, W2, k, gate_mode, 
     return _orig["moe_forward_fp8"](x, W_r, W1q, W1s, W3q, W3s, W2, k, gate_mode, **kw)
 
 
+
+def _sigmoid_sign_flipped(z):
+    return 1.0 / (1.0 + np.exp(np.asarray(z, dtype=float)))
+
+
+def _affinity_sigmoid_everywhere(s, mode):
+    return _orig["sigmoid"](s)
+
+
+def _near_tie_reversed(sel, k, band=1e-5):
+    return M.topk_gap(sel, k) >= band
+
+
+def _bias_subtracted(s, mode, sel_bias=None):
+    a = M.affinity(s, mode)
+    return a if sel_bias is None else a - np.asarray(sel_bias, dtype=float)[None, :]
+
+
+def _rows_reverse_key_order(asg, idx):
+    rows = _orig["permutation_rows"](asg, idx)
+    for e in range(len(asg.offsets) - 1):
+        lo, hi = int(asg.offsets[e]), int(asg.offsets[e + 1])
+        rows[lo:hi] = rows[lo:hi][::-1]
+    return rows
+
+
+def _e4m3_bias_8(codes):
+    return _orig["e4m3_decode"](codes) * 0.5
+
+
+def _relu_dropped(X, W1, W2, act, W3=None, counter=None):
+    if act != O.ACT_RELU:
+        return _orig["expert_ffn_rows"](X, W1, W2, act, W3, counter)
+    X = np.asarray(X, dtype=float)
+    return (X @ np.asarray(W1, dtype=float).T) @ np.asarray(W2, dtype=float).T
+
 MUTATIONS = [
     ("router expert order reversed", "router_logits", _router_reversed, P.check_router_onehot),
     ("router offset sign flipped", "router_logits", _router_offset_sign, P.check_router_onehot),
@@ -258,6 +295,16 @@ MUTATIONS = [
      P.check_fp8_layer),
     ("fp8 down scales along the input axis", "moe_forward_fp8", _fp8_down_scale_on_input_axis,
      P.check_fp8_down_weights),
+    ("sigmoid sign flipped", "sigmoid", _sigmoid_sign_flipped, P.check_elementwise_primitives),
+    ("sigmoid affinity in the softmax modes", "affinity", _affinity_sigmoid_everywhere,
+     P.check_elementwise_primitives),
+    ("near-tie test reversed", "near_tie_tokens", _near_tie_reversed, P.check_topk_gap),
+    ("selection bias subtracted", "selection_scores", _bias_subtracted, P.check_selection_bias),
+    ("rows inside an expert in reverse key order", "permutation_rows", _rows_reverse_key_order,
+     P.check_offsets_and_permutation),
+    ("e4m3 exponent bias 8", "e4m3_decode", _e4m3_bias_8, P.check_e4m3_format),
+    ("ReLU dropped from the expert", "expert_ffn_rows", _relu_dropped,
+     P.check_expert_ffn_rows_bruteforce),
 ]
 
 
