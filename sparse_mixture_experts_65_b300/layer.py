@@ -51,6 +51,130 @@ def _stream_handle(stream: Optional[torch.cuda.Stream]):
     return ctypes.c_void_p(s.cuda_stream)
 
 
+# ------------------------------------------------------------ argument checks
+# The library receives bare pointers: a host tensor where device memory is
+# expected, or a buffer smaller than the layer's shape, would be read or
+# written out of bounds on the GPU.  So every tensor is checked here for its
+# memory (the call's CUDA device, or the host for the host-memory calls),
+# dtype and exact shape before its pointer is taken.  What the library checks
+# itself (NULL where a tensor is required, alignment, workspace size,
+# unsupported layers) is left to it and reported as MoeError.
+_LAYER_DT = {N.MOE_BF16: torch.bfloat16, N.MOE_F32: torch.float32}
+_CODES = (torch.uint8, torch.float8_e4m3fn)     # e4m3 codes: one byte each
+_F32 = (torch.float32,)
+_I32 = (torch.int32,)
+
+
+def _expect(name: str, t, shape, dtypes, device) -> None:
+    """`device`: the CUDA device of the call, or None for host memory; a
+    dtypes of None skips the dtype test (a layer dtype the library refuses)."""
+    if t is None:
+        return
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name}: expected a torch.Tensor, got {type(t).__name__}")
+    if device is None:
+        if t.device.type != "cpu":
+            raise ValueError(f"{name}: expected a host tensor, got one on {t.device}")
+    elif t.device != device:
+        raise ValueError(f"{name}: expected a tensor on {device}, got one on {t.device}")
+    if dtypes is not None and t.dtype not in dtypes:
+        raise ValueError(f"{name}: expected {' or '.join(str(d) for d in dtypes)}, "
+                         f"got {t.dtype}")
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name}: expected shape {tuple(shape)}, got {tuple(t.shape)}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name}: tensors passed to libmoe must be contiguous")
+
+
+def _cuda_device(t, name: str) -> torch.device:
+    if not isinstance(t, torch.Tensor) or t.device.type != "cuda":
+        where = t.device if isinstance(t, torch.Tensor) else type(t).__name__
+        raise ValueError(f"{name} must be a CUDA tensor (got {where}): the library reads "
+                         "device memory")
+    return t.device
+
+
+def _layer_dt(cfg: N.MoeConfig):
+    dt = _LAYER_DT.get(cfg.dtype)
+    return None if dt is None else (dt,)
+
+
+def _check_weights(cfg: N.MoeConfig, dev, W_r, logit_offset, sel_bias, W1, W3, W2,
+                   Ws1=None, Ws3=None, Ws2=None, W1s=None, W3s=None, W2s=None,
+                   fp8: bool = False) -> None:
+    """The router and expert weights of a layer call: bf16/float32 weights in
+    the layer dtype, or e4m3 codes (uint8 or float8_e4m3fn) with float32
+    channel scales for the fp8 calls (down weights as codes when W2s is given)."""
+    d, E, f, fs = cfg.d, cfg.E, cfg.f, cfg.f_shared
+    dt = _layer_dt(cfg)
+    _expect("W_r", W_r, (E, d), dt, dev)
+    _expect("logit_offset", logit_offset, (E,), _F32, dev)
+    _expect("sel_bias", sel_bias, (E,), _F32, dev)
+    _expect("W1", W1, (E, f, d), _CODES if fp8 else dt, dev)
+    _expect("W3", W3, (E, f, d), _CODES if fp8 else dt, dev)
+    _expect("W1s", W1s, (E, f), _F32, dev)
+    _expect("W3s", W3s, (E, f), _F32, dev)
+    _expect("W2", W2, (E, d, f), _CODES if W2s is not None else dt, dev)
+    _expect("W2s", W2s, (E, d), _F32, dev)
+    _expect("Ws1", Ws1, (fs, d), dt, dev)
+    _expect("Ws3", Ws3, (fs, d), dt, dev)
+    _expect("Ws2", Ws2, (d, fs), dt, dev)
+
+
+def _check_outputs(cfg: N.MoeConfig, dev, out: "MoeOutputs") -> None:
+    T, d, E, k = cfg.T, cfg.d, cfg.E, cfg.k
+    _expect("out.y", out.y, (T, d), _layer_dt(cfg), dev)
+    _expect("out.topk_idx", out.topk_idx, (T, k), _I32, dev)
+    _expect("out.topk_w", out.topk_w, (T, k), _F32, dev)
+    _expect("out.expert_counts", out.expert_counts, (E,), _I32, dev)
+    _expect("out.aux_loss", out.aux_loss, (1,), _F32, dev)
+    _expect("out.routed_counts", out.routed_counts, (E,), _I32, dev)
+    _expect("out.offsets", out.offsets, (E + 1,), _I32, dev)
+    _expect("out.slot_pos", out.slot_pos, (T, k), _I32, dev)
+    _expect("out.f", out.f, (E,), _F32, dev)
+    _expect("out.P", out.P, (E,), _F32, dev)
+
+
+def _check_workspace(ws, dev) -> None:
+    """Device bytes (uint8, so that numel is the size the library is told);
+    the library checks the size itself."""
+    if not isinstance(ws, torch.Tensor):
+        raise TypeError(f"workspace: expected a torch.Tensor, got {type(ws).__name__}")
+    _expect("workspace", ws, tuple(ws.shape), (torch.uint8,), dev)
+
+
+def _check_layer_call(cfg: N.MoeConfig, x, W_r, W1, W2, W3, logit_offset, sel_bias, Ws1=None,
+                      Ws3=None, Ws2=None, out=None, workspace=None, W1s=None, W3s=None,
+                      W2s=None, fp8: bool = False) -> torch.device:
+    """Every tensor of a device-memory layer call; returns x's CUDA device."""
+    dev = _cuda_device(x, "x")
+    _expect("x", x, (cfg.T, cfg.d), _layer_dt(cfg), dev)
+    _check_weights(cfg, dev, W_r, logit_offset, sel_bias, W1, W3, W2, Ws1, Ws3, Ws2, W1s, W3s,
+                   W2s, fp8)
+    if out is not None:
+        _check_outputs(cfg, dev, out)
+    if workspace is not None:
+        _check_workspace(workspace, dev)
+    return dev
+
+
+def _check_host_io_call(cfg: N.MoeConfig, x_host, y_host, aux_host, W_r, W1, W2, W3,
+                        logit_offset, sel_bias, Ws1=None, Ws3=None, Ws2=None, workspace=None,
+                        W1s=None, W3s=None, fp8: bool = False) -> torch.device:
+    """A host-memory layer call: x, y and the loss on the host, the weights
+    and the workspace on W_r's CUDA device; returns that device."""
+    dev = _cuda_device(W_r, "W_r")
+    dt = _layer_dt(cfg)
+    _expect("x_host", x_host, (cfg.T, cfg.d), dt, None)
+    _expect("y_host", y_host, (cfg.T, cfg.d), dt, None)
+    _expect("aux_host", aux_host, (1,), _F32, None)
+    _check_weights(cfg, dev, W_r, logit_offset, sel_bias, W1, W3, W2, Ws1, Ws3, Ws2, W1s, W3s,
+                   None, fp8)
+    if workspace is not None:
+        _check_workspace(workspace, dev)
+    return dev
+
+
 def workspace_size(cfg: N.MoeConfig, kind: str = "forward") -> int:
     n = ctypes.c_size_t(0)
     fn = {"forward": N.lib().moe_workspace_size, "route": N.lib().moe_route_workspace_size,
@@ -134,10 +258,12 @@ def forward(cfg: N.MoeConfig, x, W_r, W1, W2, W3=None, logit_offset=None, sel_bi
             workspace: Optional[torch.Tensor] = None, stream=None, events=None) -> MoeOutputs:
     """One call of moe_forward (or moe_forward_timed when `events` is a list of
     MOE_NUM_STAGES + 1 torch.cuda.Event objects)."""
+    dev = _check_layer_call(cfg, x, W_r, W1, W2, W3, logit_offset, sel_bias, Ws1, Ws3, Ws2,
+                            out=out, workspace=workspace)
     if out is None:
-        out = alloc_outputs(cfg, x.device, x.dtype)
+        out = alloc_outputs(cfg, dev, x.dtype)
     if workspace is None:
-        workspace = alloc_workspace(cfg, x.device)
+        workspace = alloc_workspace(cfg, dev)
     args = [ctypes.byref(cfg), _ptr(x), _ptr(W_r), _ptr(logit_offset), _ptr(sel_bias),
             _ptr(W1), _ptr(W3), _ptr(W2), _ptr(Ws1), _ptr(Ws3), _ptr(Ws2),
             _ptr(out.y), _ptr(out.topk_idx), _ptr(out.topk_w), _ptr(out.expert_counts),
@@ -169,6 +295,13 @@ def route(cfg: N.MoeConfig, x, W_r, logit_offset=None, sel_bias=None,
           out: Optional[MoeOutputs] = None, workspace: Optional[torch.Tensor] = None,
           stream=None) -> MoeOutputs:
     """Stages 1-3 and the balance statistics (moe_route)."""
+    dev = _cuda_device(x, "x")
+    _expect("x", x, (cfg.T, cfg.d), _layer_dt(cfg), dev)
+    _check_weights(cfg, dev, W_r, logit_offset, sel_bias, None, None, None)
+    if out is not None:
+        _check_outputs(cfg, dev, out)
+    if workspace is not None:
+        _check_workspace(workspace, dev)
     if out is None:
         out = alloc_outputs(cfg, x.device, x.dtype, with_y=False)
     if workspace is None:
@@ -185,6 +318,12 @@ def route(cfg: N.MoeConfig, x, W_r, logit_offset=None, sel_bias=None,
 def router_scores(cfg: N.MoeConfig, x, W_r, logit_offset=None, out=None, workspace=None,
                   stream=None) -> torch.Tensor:
     """Stage 1 alone (moe_router_scores): float32 logits [T, E]."""
+    dev = _cuda_device(x, "x")
+    _expect("x", x, (cfg.T, cfg.d), _layer_dt(cfg), dev)
+    _check_weights(cfg, dev, W_r, logit_offset, None, None, None, None)
+    _expect("out", out, (cfg.T, cfg.E), _F32, dev)
+    if workspace is not None:
+        _check_workspace(workspace, dev)
     if out is None:
         out = torch.empty((cfg.T, cfg.E), dtype=torch.float32, device=x.device)
     if workspace is None:
@@ -199,8 +338,10 @@ def router_scores(cfg: N.MoeConfig, x, W_r, logit_offset=None, out=None, workspa
 def router_z_loss(scores: torch.Tensor, out=None, stream=None) -> torch.Tensor:
     """Router z-loss of [T, E] float32 logits (moe_router_z_loss): a one-element
     float32 device tensor."""
+    dev = _cuda_device(scores, "scores")
     if scores.dtype != torch.float32 or scores.dim() != 2 or not scores.is_contiguous():
         raise ValueError("scores must be a contiguous [T, E] float32 tensor")
+    _expect("out", out, (1,), _F32, dev)
     if out is None:
         out = torch.empty(1, dtype=torch.float32, device=scores.device)
     T, E = scores.shape
@@ -217,6 +358,9 @@ def bias_update(sel_bias: torch.Tensor, routed_counts: torch.Tensor, T: int, k: 
         raise ValueError("sel_bias must be float32 and routed_counts int32")
     if sel_bias.numel() != routed_counts.numel():
         raise ValueError("sel_bias and routed_counts need one entry per expert")
+    dev = _cuda_device(sel_bias, "sel_bias")
+    _expect("sel_bias", sel_bias, (sel_bias.numel(),), _F32, dev)
+    _expect("routed_counts", routed_counts, (sel_bias.numel(),), _I32, dev)
     N.check(N.lib().moe_bias_update(_ptr(routed_counts), sel_bias.numel(), int(T), int(k),
                                     ctypes.c_float(gamma), _ptr(sel_bias),
                                     _stream_handle(stream)),
@@ -228,8 +372,10 @@ def forward_host_io(cfg: N.MoeConfig, x_host: torch.Tensor, y_host: torch.Tensor
                     aux_host: torch.Tensor, W_r, W1, W2, W3=None, logit_offset=None,
                     sel_bias=None, Ws1=None, Ws3=None, Ws2=None, workspace=None, stream=None):
     """moe_forward_host_io: x_host / y_host / aux_host are (pinned) host tensors."""
+    dev = _check_host_io_call(cfg, x_host, y_host, aux_host, W_r, W1, W2, W3, logit_offset,
+                              sel_bias, Ws1, Ws3, Ws2, workspace=workspace)
     if workspace is None:
-        workspace = alloc_workspace(cfg, W_r.device, "host_io")
+        workspace = alloc_workspace(cfg, dev, "host_io")
     rc = N.lib().moe_forward_host_io(
         ctypes.byref(cfg), _ptr(x_host), _ptr(W_r), _ptr(logit_offset), _ptr(sel_bias),
         _ptr(W1), _ptr(W3), _ptr(W2), _ptr(Ws1), _ptr(Ws3), _ptr(Ws2), _ptr(y_host),
@@ -270,10 +416,12 @@ def tuning(**knobs):
 
 def check_status(workspace: torch.Tensor, stream=None) -> int:
     """Synchronise and return (and clear) the device status of a workspace."""
+    _check_workspace(workspace, _cuda_device(workspace, "workspace"))
     return N.lib().moe_check_status(_ptr(workspace), _stream_handle(stream))
 
 
 def selftest_wait_timeout(workspace: torch.Tensor, wait_ns: int, stream=None) -> None:
+    _check_workspace(workspace, _cuda_device(workspace, "workspace"))
     N.check(N.lib().moe_selftest_wait_timeout(_ptr(workspace), ctypes.c_size_t(workspace.numel()),
                                               ctypes.c_uint64(wait_ns), _stream_handle(stream)),
             "moe_selftest_wait_timeout")
@@ -287,9 +435,11 @@ class BoundForward:
     def __init__(self, cfg: N.MoeConfig, x, W_r, W1, W2, W3=None, logit_offset=None,
                  sel_bias=None, Ws1=None, Ws3=None, Ws2=None, out: Optional[MoeOutputs] = None,
                  workspace: Optional[torch.Tensor] = None, stream=None):
+        dev = _check_layer_call(cfg, x, W_r, W1, W2, W3, logit_offset, sel_bias, Ws1, Ws3, Ws2,
+                                out=out, workspace=workspace)
         self.cfg = cfg
-        self.out = out if out is not None else alloc_outputs(cfg, x.device, x.dtype)
-        self.workspace = workspace if workspace is not None else alloc_workspace(cfg, x.device)
+        self.out = out if out is not None else alloc_outputs(cfg, dev, x.dtype)
+        self.workspace = workspace if workspace is not None else alloc_workspace(cfg, dev)
         self._keep = (x, W_r, W1, W2, W3, logit_offset, sel_bias, Ws1, Ws3, Ws2)
         o = self.out
         self.args = (ctypes.byref(cfg), _ptr(x), _ptr(W_r), _ptr(logit_offset), _ptr(sel_bias),
@@ -326,10 +476,12 @@ class BoundForwardFp8(BoundForward):
     def __init__(self, cfg: N.MoeConfig, x, W_r, W1q, W1s, W3q, W3s, W2, logit_offset=None,
                  sel_bias=None, out: Optional[MoeOutputs] = None,
                  workspace: Optional[torch.Tensor] = None, stream=None, W2s=None):
+        dev = _check_layer_call(cfg, x, W_r, W1q, W2, W3q, logit_offset, sel_bias, out=out,
+                                workspace=workspace, W1s=W1s, W3s=W3s, W2s=W2s, fp8=True)
         self.cfg = cfg
-        self.out = out if out is not None else alloc_outputs(cfg, x.device, x.dtype)
+        self.out = out if out is not None else alloc_outputs(cfg, dev, x.dtype)
         self.workspace = (workspace if workspace is not None
-                          else alloc_workspace(cfg, x.device, "fp8"))
+                          else alloc_workspace(cfg, dev, "fp8"))
         self._keep = (x, W_r, W1q, W1s, W3q, W3s, W2, W2s, logit_offset, sel_bias)
         o = self.out
         down = (_ptr(W2),) if W2s is None else (_ptr(W2), _ptr(W2s))
@@ -381,8 +533,11 @@ class BoundHostIOFp8:
     def __init__(self, cfg: N.MoeConfig, x_host, y_host, aux_host, W_r, W1q, W1s, W3q, W3s, W2,
                  logit_offset=None, sel_bias=None, workspace: Optional[torch.Tensor] = None,
                  stream=None):
+        dev = _check_host_io_call(cfg, x_host, y_host, aux_host, W_r, W1q, W2, W3q,
+                                  logit_offset, sel_bias, workspace=workspace, W1s=W1s, W3s=W3s,
+                                  fp8=True)
         self.workspace = (workspace if workspace is not None
-                          else alloc_workspace(cfg, W_r.device, "host_io_fp8"))
+                          else alloc_workspace(cfg, dev, "host_io_fp8"))
         self._keep = (x_host, y_host, aux_host, W_r, W1q, W1s, W3q, W3s, W2, logit_offset,
                       sel_bias)
         self.args = (ctypes.byref(cfg), _ptr(x_host), _ptr(W_r), _ptr(logit_offset),
@@ -412,7 +567,22 @@ class BoundHostIOBatches:
         if len(y_hosts) != n or aux_host.numel() < n:
             raise ValueError("one y buffer and one loss entry per batch")
         fp8 = getattr(inp, "W1q", None) is not None
-        dev = inp.W_r.device
+        dev = _cuda_device(inp.W_r, "W_r")
+        dt = _layer_dt(cfg)
+        for i in range(n):
+            _expect(f"x_hosts[{i}]", x_hosts[i], (cfg.T, cfg.d), dt, None)
+            _expect(f"y_hosts[{i}]", y_hosts[i], (cfg.T, cfg.d), dt, None)
+        _expect("aux_host", aux_host, (aux_host.numel(),), _F32, None)
+        if fp8:
+            w2q = getattr(inp, "W2q", None)
+            _check_weights(cfg, dev, inp.W_r, inp.logit_offset, inp.sel_bias, inp.W1q, inp.W3q,
+                           w2q if w2q is not None else inp.W2, W1s=inp.W1s, W3s=inp.W3s,
+                           W2s=inp.W2s if w2q is not None else None, fp8=True)
+        else:
+            _check_weights(cfg, dev, inp.W_r, inp.logit_offset, inp.sel_bias, inp.W1, inp.W3,
+                           inp.W2, inp.Ws1, inp.Ws3, inp.Ws2)
+        if workspace is not None:
+            _check_workspace(workspace, dev)
         self.workspace = (workspace if workspace is not None
                           else alloc_workspace(cfg, dev, "host_io_fp8" if fp8 else "host_io"))
         self.copy_in = copy_in_stream if copy_in_stream is not None else torch.cuda.Stream(dev)
@@ -450,8 +620,10 @@ class BoundHostIO:
     def __init__(self, cfg: N.MoeConfig, x_host, y_host, aux_host, W_r, W1, W2, W3=None,
                  logit_offset=None, sel_bias=None, Ws1=None, Ws3=None, Ws2=None,
                  workspace: Optional[torch.Tensor] = None, stream=None):
+        dev = _check_host_io_call(cfg, x_host, y_host, aux_host, W_r, W1, W2, W3, logit_offset,
+                                  sel_bias, Ws1, Ws3, Ws2, workspace=workspace)
         self.workspace = (workspace if workspace is not None
-                          else alloc_workspace(cfg, W_r.device, "host_io"))
+                          else alloc_workspace(cfg, dev, "host_io"))
         self._keep = (x_host, y_host, aux_host, W_r, W1, W2, W3, logit_offset, sel_bias, Ws1,
                       Ws3, Ws2)
         self.args = (ctypes.byref(cfg), _ptr(x_host), _ptr(W_r), _ptr(logit_offset),
