@@ -323,6 +323,38 @@ def check_sparse_equals_dense():
     np.testing.assert_allclose(r.y, ref, rtol=1e-12, atol=1e-12)
 
 
+
+def check_shared_expert_outside_routing():
+    """The shared expert is always on: it takes no part in routing (choices,
+    gates, slots, f, P and L are those of the layer without it), it is
+    outside capacity (a token whose every slot was dropped still gets its
+    output) and it is added at weight 1 to every token, whatever its gates.
+    Its output is written out with torch.nn.functional."""
+    T, d, E, f, k = 12, 6, 3, 8, 2
+    x, W_r, W1, W2, W3 = _rand_layer(42, T, d, E, f, True)
+    rng = _rng(43)
+    Ws = (rng.normal(size=(5, d)), rng.normal(size=(5, d)), rng.normal(size=(d, 5)))
+    kw = dict(W3=W3, capacity_factor=0.3)            # C = ceil(24 * 0.3 / 3) = 3
+    base = O.moe_forward(x, W_r, W1, W2, k, O.ACT_SWIGLU, O.GATE_SOFTMAX_TOPK, **kw)
+    sh = O.moe_forward(x, W_r, W1, W2, k, O.ACT_SWIGLU, O.GATE_SOFTMAX_TOPK, **kw,
+                       Ws1=Ws[0], Ws3=Ws[1], Ws2=Ws[2])
+    assert sh.asg.capacity == 3
+    np.testing.assert_array_equal(sh.topk_idx, base.topk_idx)
+    np.testing.assert_array_equal(sh.topk_w, base.topk_w)
+    np.testing.assert_array_equal(sh.asg.slot_pos, base.asg.slot_pos)
+    np.testing.assert_array_equal(sh.asg.kept, base.asg.kept)
+    np.testing.assert_array_equal(sh.f, base.f)
+    np.testing.assert_array_equal(sh.P, base.P)
+    assert sh.aux_loss == base.aux_loss
+    xt = torch.from_numpy(x)
+    Ws1, Ws3, Ws2 = (torch.from_numpy(w) for w in Ws)
+    shared = F.linear(F.silu(F.linear(xt, Ws1)) * F.linear(xt, Ws3), Ws2).numpy()
+    np.testing.assert_allclose(sh.y - base.y, shared, rtol=1e-12, atol=1e-12)
+    all_dropped = np.all(sh.asg.slot_pos < 0, axis=1)
+    partly = np.any(sh.asg.slot_pos < 0, axis=1) & ~all_dropped
+    assert all_dropped.any() and partly.any()        # the case the reading is about
+    np.testing.assert_allclose(sh.y[all_dropped], shared[all_dropped], rtol=1e-12, atol=1e-12)
+
 def check_drop_is_identity_branch():
     """A dropped slot contributes zero (the caller's residual carries the token);
     the surviving slot keeps its gate (no renormalisation)."""
@@ -709,7 +741,8 @@ ALL_CHECKS = [
     check_router_onehot, check_topk_bruteforce, check_topk_ties, check_topk_gap, check_gates_closed_form,
     check_gates_invariants, check_router_probs, check_selection_bias,
     check_capacity_formula, check_capacity_drops, check_offsets_and_permutation,
-    check_sparse_equals_dense, check_drop_is_identity_branch, check_dense_ffn_special_case,
+    check_sparse_equals_dense, check_shared_expert_outside_routing,
+    check_drop_is_identity_branch, check_dense_ffn_special_case,
     check_elementwise_primitives, check_expert_ffn_rows_bruteforce,
     check_multiply_counts, check_balance_uniform, check_balance_hand_and_collapse,
     check_pipeline_stats_pre_drop, check_z_loss_closed_forms, check_bias_update_rule,

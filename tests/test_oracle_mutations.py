@@ -18,7 +18,7 @@ _orig = {name: getattr(M, name) for name in (
     "assign_slots", "gelu_erf", "silu", "expert_ffn_rows", "balance_stats", "router_probs",
     "softmax_rows", "router_z_loss", "bias_update", "e4m3_round", "row_scale_exponent",
     "quantize_rows_e4m3", "moe_forward_fp8", "sigmoid", "near_tie_tokens", "selection_scores",
-    "permutation_rows", "e4m3_decode")}
+    "permutation_rows", "e4m3_decode", "moe_forward")}
 
 
 def _router_reversed(x, W_r, logit_offset=None):
@@ -256,6 +256,26 @@ def _relu_dropped(X, W1, W2, act, W3=None, counter=None):
     X = np.asarray(X, dtype=float)
     return (X @ np.asarray(W1, dtype=float).T) @ np.asarray(W2, dtype=float).T
 
+
+def _shared_only_where_kept(x, W_r, W1, W2, k, act, gate_mode, Ws1=None, Ws3=None, Ws2=None,
+                            **kw):
+    r = _orig["moe_forward"](x, W_r, W1, W2, k, act, gate_mode, **kw)
+    if Ws1 is not None:
+        kept = np.any(r.asg.slot_pos >= 0, axis=1)
+        sh = M.expert_ffn_rows(np.asarray(x, dtype=float), Ws1, Ws2, O.ACT_SWIGLU, Ws3)
+        r.y[kept] += sh[kept]
+    return r
+
+
+def _shared_scaled_by_kept_gates(x, W_r, W1, W2, k, act, gate_mode, Ws1=None, Ws3=None,
+                                 Ws2=None, **kw):
+    r = _orig["moe_forward"](x, W_r, W1, W2, k, act, gate_mode, **kw)
+    if Ws1 is not None:
+        w = np.where(r.asg.slot_pos >= 0, r.topk_w, 0.0).sum(axis=1)
+        sh = M.expert_ffn_rows(np.asarray(x, dtype=float), Ws1, Ws2, O.ACT_SWIGLU, Ws3)
+        r.y += w[:, None] * sh
+    return r
+
 MUTATIONS = [
     ("router expert order reversed", "router_logits", _router_reversed, P.check_router_onehot),
     ("router offset sign flipped", "router_logits", _router_offset_sign, P.check_router_onehot),
@@ -305,6 +325,10 @@ MUTATIONS = [
     ("e4m3 exponent bias 8", "e4m3_decode", _e4m3_bias_8, P.check_e4m3_format),
     ("ReLU dropped from the expert", "expert_ffn_rows", _relu_dropped,
      P.check_expert_ffn_rows_bruteforce),
+    ("shared expert only for tokens with a kept slot", "moe_forward", _shared_only_where_kept,
+     P.check_shared_expert_outside_routing),
+    ("shared expert scaled by the kept gates", "moe_forward", _shared_scaled_by_kept_gates,
+     P.check_shared_expert_outside_routing),
 ]
 
 
