@@ -355,6 +355,46 @@ def check_shared_expert_outside_routing():
     assert all_dropped.any() and partly.any()        # the case the reading is about
     np.testing.assert_allclose(sh.y[all_dropped], shared[all_dropped], rtol=1e-12, atol=1e-12)
 
+
+def check_conditioning_and_token_sample():
+    """Two evaluation modes the parity tests use.  (1) Conditioning on another
+    implementation's choice: forcing the oracle's own choice changes nothing;
+    forcing another choice gives that choice's gates, counts, slots and
+    statistics.  (2) A token sample: y is evaluated for the sampled tokens
+    only, but routing and capacity are those of the whole batch, so a sampled
+    token that the batch drops stays dropped."""
+    T, d, E, f, k = 16, 6, 3, 5, 2
+    x, W_r, W1, W2, W3 = _rand_layer(44, T, d, E, f, True)
+    kw = dict(W3=W3, capacity_factor=0.5)            # C = ceil(32 * 0.5 / 3) = 6
+    full = O.moe_forward(x, W_r, W1, W2, k, O.ACT_SWIGLU, O.GATE_SOFTMAX_TOPK, **kw)
+    same = O.moe_forward(x, W_r, W1, W2, k, O.ACT_SWIGLU, O.GATE_SOFTMAX_TOPK, **kw,
+                         forced_idx=full.topk_idx)
+    np.testing.assert_array_equal(same.y, full.y)
+    np.testing.assert_array_equal(same.asg.slot_pos, full.asg.slot_pos)
+    other = full.topk_idx.copy()
+    other[1::2] = other[1::2, ::-1]                  # odd tokens: the two choices swapped
+    other[0] = [(full.topk_idx[0, 0] + 1) % E, full.topk_idx[0, 0]]
+    if other[0, 0] == other[0, 1]:
+        raise AssertionError("test layer: need two distinct experts")
+    forced = O.moe_forward(x, W_r, W1, W2, k, O.ACT_SWIGLU, O.GATE_SOFTMAX_TOPK, **kw,
+                           forced_idx=other)
+    np.testing.assert_array_equal(forced.topk_idx, other)
+    np.testing.assert_array_equal(forced.asg.routed, np.bincount(other.ravel(), minlength=E))
+    s = x @ W_r.T
+    np.testing.assert_allclose(forced.topk_w, O.gate_values(s, other, O.GATE_SOFTMAX_TOPK),
+                               rtol=1e-15)
+    assert not np.array_equal(forced.asg.slot_pos, full.asg.slot_pos)
+    dropped = np.nonzero(np.all(full.asg.slot_pos < 0, axis=1))[0]
+    assert len(dropped) > 0
+    sample = np.array([dropped[-1], 0, T - 1, 5])
+    part = O.moe_forward(x, W_r, W1, W2, k, O.ACT_SWIGLU, O.GATE_SOFTMAX_TOPK, **kw,
+                         tokens=sample)
+    # the same sums over other groupings of the rows: equal to rounding
+    np.testing.assert_allclose(part.y, full.y[sample], rtol=1e-13, atol=1e-15)
+    np.testing.assert_array_equal(part.y[0], 0.0)   # dropped by the batch, not by the sample
+    np.testing.assert_array_equal(part.asg.slot_pos, full.asg.slot_pos)
+    assert part.aux_loss == full.aux_loss
+
 def check_drop_is_identity_branch():
     """A dropped slot contributes zero (the caller's residual carries the token);
     the surviving slot keeps its gate (no renormalisation)."""
@@ -742,6 +782,7 @@ ALL_CHECKS = [
     check_gates_invariants, check_router_probs, check_selection_bias,
     check_capacity_formula, check_capacity_drops, check_offsets_and_permutation,
     check_sparse_equals_dense, check_shared_expert_outside_routing,
+    check_conditioning_and_token_sample,
     check_drop_is_identity_branch, check_dense_ffn_special_case,
     check_elementwise_primitives, check_expert_ffn_rows_bruteforce,
     check_multiply_counts, check_balance_uniform, check_balance_hand_and_collapse,

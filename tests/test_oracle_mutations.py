@@ -18,7 +18,7 @@ _orig = {name: getattr(M, name) for name in (
     "assign_slots", "gelu_erf", "silu", "expert_ffn_rows", "balance_stats", "router_probs",
     "softmax_rows", "router_z_loss", "bias_update", "e4m3_round", "row_scale_exponent",
     "quantize_rows_e4m3", "moe_forward_fp8", "sigmoid", "near_tie_tokens", "selection_scores",
-    "permutation_rows", "e4m3_decode", "moe_forward")}
+    "permutation_rows", "e4m3_decode", "moe_forward", "route")}
 
 
 def _router_reversed(x, W_r, logit_offset=None):
@@ -276,6 +276,17 @@ def _shared_scaled_by_kept_gates(x, W_r, W1, W2, k, act, gate_mode, Ws1=None, Ws
         r.y += w[:, None] * sh
     return r
 
+
+def _route_ignores_forced_choice(*args, forced_idx=None, **kw):
+    return _orig["route"](*args[:8], **kw)   # the ninth positional argument is forced_idx
+
+
+def _sample_routed_alone(x, W_r, W1, W2, k, act, gate_mode, tokens=None, **kw):
+    if tokens is None:
+        return _orig["moe_forward"](x, W_r, W1, W2, k, act, gate_mode, **kw)
+    tok = np.asarray(tokens)
+    return _orig["moe_forward"](np.asarray(x)[tok], W_r, W1, W2, k, act, gate_mode, **kw)
+
 MUTATIONS = [
     ("router expert order reversed", "router_logits", _router_reversed, P.check_router_onehot),
     ("router offset sign flipped", "router_logits", _router_offset_sign, P.check_router_onehot),
@@ -329,6 +340,10 @@ MUTATIONS = [
      P.check_shared_expert_outside_routing),
     ("shared expert scaled by the kept gates", "moe_forward", _shared_scaled_by_kept_gates,
      P.check_shared_expert_outside_routing),
+    ("forced choice ignored", "route", _route_ignores_forced_choice,
+     P.check_conditioning_and_token_sample),
+    ("sampled tokens routed on their own", "moe_forward", _sample_routed_alone,
+     P.check_conditioning_and_token_sample),
 ]
 
 
