@@ -103,8 +103,10 @@ typedef struct {
   int32_t gate;     /* moe_gate */
   double capacity_factor; /* rho; <= 0 means no capacity limit.  Otherwise the
                              capacity is C = ceil((double)(k*T) * rho / E),
-                             the same C for every expert */
-  float alpha;      /* coefficient of the balance loss */
+                             the same C for every expert.  NaN or infinite:
+                             MOE_ERR_ARG */
+  float alpha;      /* coefficient of the balance loss; NaN or infinite:
+                       MOE_ERR_ARG */
   int32_t reserved; /* must be 0 */
 } moe_config;
 
