@@ -212,3 +212,51 @@ def test_host_memory_calls_check_their_host_buffers(stub):
     b = L.BoundHostIOBatches(cfg, xs, ys, torch.empty(3), inp, **kw)
     b()
     assert stub.called == ["moe_forward_host_io", "moe_forward_host_io_batches"]
+
+
+# ------------------------------------------------------------ the GPU tests' own inputs
+def _gpu_test_shapes():
+    """Every layer shape the GPU test modules and the named workloads define,
+    up to 60 MB of expert weights (the larger ones are the same kinds of layer)."""
+    import importlib
+    shapes = {}
+    for mod in ("test_gpu_parity", "test_gpu_fp8", "test_gpu_bounds", "test_gpu_balance"):
+        for v in vars(importlib.import_module(mod)).values():
+            for it in (v if isinstance(v, (list, tuple)) else [v]):
+                if isinstance(it, tuple):
+                    it = next((x for x in it if isinstance(x, W.LayerShape)), None)
+                if isinstance(it, W.LayerShape):
+                    shapes[it.name] = it
+    for s in W.WORKLOADS.values():
+        shapes[s.name] = s
+    return [s for _, s in sorted(shapes.items()) if s.E * s.f * s.d * 6 <= 6e7]
+
+
+def test_the_gpu_tests_inputs_pass_the_checks(stub):
+    """The checks refuse nothing the GPU tests, the bench or smoke() pass: the
+    calls those make, on every shape they use, reach the library."""
+    shapes = _gpu_test_shapes()
+    kinds = {(s.dtype, s.act, bool(s.n_shared), s.w_fp8, s.w2_fp8) for s in shapes}
+    assert len(shapes) >= 30 and len(kinds) >= 6
+    for s in shapes:
+        inp = W.make_inputs(s, "cpu")
+        cfg = L.config_for(s)
+        n = len(stub.called)
+        L.bound_forward(cfg, inp, workspace=_ws())()
+        xs = [inp.x.clone(), inp.x.clone()]
+        L.BoundHostIOBatches(cfg, xs, [torch.empty_like(x) for x in xs], torch.empty(4), inp,
+                             workspace=_ws(), copy_in_stream=object(),
+                             copy_out_stream=object())()
+        if inp.W1q is None:
+            L.forward(cfg, inp.x, inp.W_r, inp.W1, inp.W2, inp.W3, inp.logit_offset,
+                      inp.sel_bias, inp.Ws1, inp.Ws3, inp.Ws2, workspace=_ws())
+            L.route(cfg, inp.x, inp.W_r, inp.logit_offset, inp.sel_bias, workspace=_ws())
+            L.router_scores(cfg, inp.x, inp.W_r, inp.logit_offset, workspace=_ws())
+            L.forward_host_io(cfg, inp.x.clone(), torch.empty_like(inp.x), torch.empty(1),
+                              inp.W_r, inp.W1, inp.W2, inp.W3, inp.logit_offset, inp.sel_bias,
+                              inp.Ws1, inp.Ws3, inp.Ws2, workspace=_ws())
+        elif inp.W2q is None:
+            L.BoundHostIOFp8(cfg, inp.x.clone(), torch.empty_like(inp.x), torch.empty(1),
+                             inp.W_r, inp.W1q, inp.W1s, inp.W3q, inp.W3s, inp.W2,
+                             inp.logit_offset, inp.sel_bias, workspace=_ws())()
+        assert len(stub.called) > n + 1, s.name
